@@ -1,0 +1,157 @@
+"""numpy front end of the C oracle (test infrastructure only).
+
+Only the tests, the smoke check and the CPU-baseline leg of the benchmark may
+import this module.  It marshals numpy arrays into the plain loops of
+moe_oracle.c and shares nothing with the CUDA library.  bf16 tensors are
+passed as numpy uint16 arrays holding the raw bit patterns.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib(path: str = None):
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+def _bind(handle):
+    c_int, c_long, c_float = ctypes.c_int, ctypes.c_long, ctypes.c_float
+    p = ctypes.c_void_p
+    handle.oracle_f32_from_bf16.argtypes = [ctypes.c_uint16]
+    handle.oracle_f32_from_bf16.restype = c_float
+    handle.oracle_bf16_from_f32.argtypes = [c_float]
+    handle.oracle_bf16_from_f32.restype = ctypes.c_uint16
+    handle.oracle_route.argtypes = [c_int] * 5 + [p] * 8
+    handle.oracle_route.restype = c_long
+    handle.oracle_dispatch.argtypes = [c_int] * 6 + [p] * 8
+    handle.oracle_dispatch.restype = None
+    handle.oracle_combine.argtypes = ([c_int] * 5 + [p] * 6 + [c_float, p, c_long]
+                                      + [p] * 4)
+    handle.oracle_combine.restype = None
+    return handle
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _need(a, dtype, shape=None):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    if shape is not None and a.shape != tuple(shape):
+        raise ValueError("expected shape %s, got %s" % (tuple(shape), a.shape))
+    return a
+
+
+def bf16_bits(values, handle=None):
+    """Round binary32 values to bf16 bit patterns with the oracle's rule."""
+    h = handle or lib()
+    flat = np.asarray(values, dtype=np.float32).ravel()
+    out = np.empty(flat.shape, dtype=np.uint16)
+    for i, v in enumerate(flat):
+        out[i] = h.oracle_bf16_from_f32(float(v))
+    return out.reshape(np.shape(values))
+
+
+def bf16_to_f32(bits):
+    """Widen bf16 bit patterns (uint16) to float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def route(topk_ids, topk_w, num_experts: int, m: int, handle=None):
+    """Routing, dedup and slot assignment.  topk_ids/topk_w: [R, T, K]."""
+    h = handle or lib()
+    ids = _need(topk_ids, np.int32)
+    R, T, K = ids.shape
+    w = _need(topk_w, np.float32, ids.shape)
+    if num_experts % R:
+        raise ValueError("num_experts must be a multiple of ep_size")
+    if T > m:
+        raise ValueError("T > m")
+    out = dict(
+        dmask=np.empty((R, T), np.uint32),
+        wd=np.empty((R, T, R), np.float32),
+        send_slot=np.empty((R, T, R), np.int32),
+        recv_counts=np.empty((R, R), np.int32),
+        src_token=np.empty((R, R, m), np.int32),
+        local_expert_counts=np.empty((R, num_experts // R), np.int32),
+    )
+    out["invalid"] = h.oracle_route(
+        R, T, K, num_experts, m, _ptr(ids), _ptr(w), _ptr(out["dmask"]),
+        _ptr(out["wd"]), _ptr(out["send_slot"]), _ptr(out["recv_counts"]),
+        _ptr(out["src_token"]), _ptr(out["local_expert_counts"]))
+    return out
+
+
+def dispatch(topk_ids, topk_w, x, num_experts: int, m: int, routing,
+             recv_x=None, recv_ids=None, recv_w=None, handle=None):
+    """Copy rows and masked metadata into padded planes [R, R, m, ...].
+
+    Slots past each plane's count are left as they were in the given (or
+    freshly allocated, uninitialised) output arrays."""
+    h = handle or lib()
+    ids = _need(topk_ids, np.int32)
+    R, T, K = ids.shape
+    w = _need(topk_w, np.float32, ids.shape)
+    xb = _need(x, np.uint16)
+    H = xb.shape[-1]
+    if xb.shape != (R, T, H):
+        raise ValueError("x must be [R, T, H]")
+    if recv_x is None:
+        recv_x = np.empty((R, R, m, H), np.uint16)
+    if recv_ids is None:
+        recv_ids = np.empty((R, R, m, K), np.int32)
+    if recv_w is None:
+        recv_w = np.empty((R, R, m, K), np.float32)
+    h.oracle_dispatch(R, T, K, num_experts, H, m, _ptr(ids), _ptr(w), _ptr(xb),
+                      _ptr(_need(routing["recv_counts"], np.int32)),
+                      _ptr(_need(routing["src_token"], np.int32)),
+                      _ptr(recv_x), _ptr(recv_ids), _ptr(recv_w))
+    return dict(recv_x=recv_x, recv_ids=recv_ids, recv_w=recv_w)
+
+
+def combine(routing, expert_out, weighted: bool, residual=None, gamma=None,
+            eps: float = 1e-6, tokens=None, handle=None):
+    """Reduce each token's per-rank messages once; optional fused epilogue.
+
+    expert_out: uint16 [R, R, m, H] (only valid slots are read).
+    residual: uint16 [R, T, H] or None; gamma: uint16 [H] (fused only).
+    tokens: optional flat token indices s*T+t; outputs are [ntok, H].
+    Returns dict(acc=float32, out=uint16, residual_out=uint16|None, y=float64).
+    """
+    h = handle or lib()
+    dmask = _need(routing["dmask"], np.uint32)
+    R, T = dmask.shape
+    eo = expert_out if (isinstance(expert_out, np.ndarray)
+                        and expert_out.dtype == np.uint16
+                        and expert_out.flags.c_contiguous) else _need(expert_out, np.uint16)
+    if eo.ndim != 4 or eo.shape[:2] != (R, R):
+        raise ValueError("expert_out must be [R, R, m, H]")
+    m, H = eo.shape[2], eo.shape[3]
+    tok = None if tokens is None else _need(tokens, np.int64)
+    n = R * T if tok is None else tok.shape[0]
+    res = None
+    gam = None
+    if residual is not None:
+        res = _need(residual, np.uint16, (R, T, H))
+        gam = _need(gamma, np.uint16, (H,))
+    acc = np.empty((n, H), np.float32)
+    out = np.empty((n, H), np.uint16)
+    rout = np.empty((n, H), np.uint16) if res is not None else None
+    y = np.empty((n, H), np.float64)
+    h.oracle_combine(R, T, H, m, int(bool(weighted)), _ptr(dmask),
+                     _ptr(_need(routing["send_slot"], np.int32)),
+                     _ptr(_need(routing["wd"], np.float32)), _ptr(eo),
+                     _ptr(res), _ptr(gam), float(eps), _ptr(tok), n,
+                     _ptr(acc), _ptr(out), _ptr(rout), _ptr(y))
+    return dict(acc=acc, out=out, residual_out=rout, y=y)

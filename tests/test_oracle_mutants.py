@@ -1,0 +1,135 @@
+"""Plant plausible mistakes in copies of the oracle and check the pins fail.
+
+Each mutant is one textual edit of oracle/moe_oracle.c, compiled into a
+scratch directory.  The pins of tests/test_oracle_pins.py are then run
+against the mutant; at least one of them must fail.  The real oracle is
+never modified.
+"""
+import os
+import tempfile
+
+import numpy as np
+import pytest
+
+import test_oracle_pins as pins
+from oracle import build as obuild
+from oracle import oracle as real
+
+MUTANTS = {
+    "combine_descending_rank": (
+        "for (int d = 0; d < R; ++d) {\n                if (!(mask & (1u << d)))",
+        "for (int d = R - 1; d >= 0; --d) {\n                if (!(mask & (1u << d)))"),
+    "combine_drops_last_rank": (
+        "for (int d = 0; d < R; ++d) {\n                if (!(mask & (1u << d)))",
+        "for (int d = 0; d < R - 1; ++d) {\n                if (!(mask & (1u << d)))"),
+    "weighted_uses_fma": (
+        "float p = wd[(size_t)flat * R + d] * v;\n                    a = a + p;",
+        "a = fmaf(wd[(size_t)flat * R + d], v, a);"),
+    "weighted_ignores_weight": (
+        "float p = wd[(size_t)flat * R + d] * v;",
+        "float p = v;"),
+    "residual_added_after_narrowing": (
+        "hsum[h] = acc[h] + oracle_f32_from_bf16(",
+        "hsum[h] = oracle_f32_from_bf16(oracle_bf16_from_f32(acc[h])) + oracle_f32_from_bf16("),
+    "eps_outside_sqrt": (
+        "1.0 / sqrt(sumsq / (double)H + (double)eps)",
+        "1.0 / (sqrt(sumsq / (double)H) + (double)eps)"),
+    "mean_over_h_minus_1": (
+        "sumsq / (double)H + (double)eps",
+        "sumsq / (double)(H - 1) + (double)eps"),
+    "gamma_ignored": (
+        "double y = (double)hsum[h] * inv * (double)oracle_f32_from_bf16(gamma[h]);",
+        "double y = (double)hsum[h] * inv;"),
+    "wd_sums_all_k": (
+        "if (e / Epr == d)\n                        sum = sum + w[k];",
+        "sum = sum + w[k];"),
+    "no_nonlocal_id_masking": (
+        "recv_ids[slot * K + k] = local ? e : -1;",
+        "recv_ids[slot * K + k] = e;"),
+    "slots_in_descending_token_order": (
+        "for (int t = 0; t < T; ++t) {\n                size_t at",
+        "for (int t = T - 1; t >= 0; --t) {\n                size_t at"),
+    "narrowing_truncates": (
+        "kept += 1u;",
+        "kept += 0u;"),
+    "local_counts_collapsed": (
+        "local_expert_counts[d * Epr + (e - d * Epr)] += 1;",
+        "local_expert_counts[d * Epr] += 1;"),
+    "invalid_ids_not_counted": (
+        "invalid += 1;",
+        "invalid += 0;"),
+    "dispatch_copies_wrong_source_token": (
+        "const uint16_t *row = x + ((size_t)s * T + t) * H;",
+        "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
+}
+
+
+class MutantOracle:
+    """The numpy front end bound to a mutant library."""
+
+    def __init__(self, handle):
+        self.h = handle
+
+    def lib(self):
+        return self.h
+
+    def bf16_bits(self, v):
+        return real.bf16_bits(v, handle=self.h)
+
+    def route(self, *a, **k):
+        return real.route(*a, handle=self.h, **k)
+
+    def dispatch(self, *a, **k):
+        return real.dispatch(*a, handle=self.h, **k)
+
+    def combine(self, *a, **k):
+        return real.combine(*a, handle=self.h, **k)
+
+
+PIN_TESTS = [
+    (pins.test_bf16_rounding_matches_library_routine, {}),
+    (pins.test_probe_pow2_rank_sum_is_255, {}),
+    (pins.test_probe_reduction_discriminator, {}),
+    (pins.test_probe_slot_order_is_ascending_token, {}),
+    (pins.test_probe_partial_routing_and_duplicates, {}),
+    (pins.test_route_brute_force, {"seed": 3}),
+    (pins.test_route_brute_force, {"seed": 0}),
+    (pins.test_dispatch_payload_identity, {}),
+    (pins.test_identity_unweighted_is_n_times_x, {}),
+    (pins.test_identity_weighted_dyadic_returns_x_once, {}),
+    (pins.test_weighted_sum_within_fp32_error_bound, {}),
+    (pins.test_ascending_rank_order_closed_form, {}),
+    (pins.test_weighted_product_is_not_fused, {}),
+    (pins.test_residual_add_uses_fp32_sum, {}),
+    (pins.test_rmsnorm_constant_row_closed_form, {"cval": 1e-3}),
+    (pins.test_rmsnorm_matches_library_routine, {}),
+]
+
+
+def _compile_mutant(name, tmpdir):
+    old, new = MUTANTS[name]
+    src = open(obuild.SOURCE).read()
+    assert src.count(old) == 1, "mutation site for %s not found exactly once" % name
+    path = os.path.join(tmpdir, name + ".c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    return obuild.build(force=True, source=path, output=os.path.join(tmpdir, name + ".so"))
+
+
+def test_pins_pass_on_real_oracle():
+    o = MutantOracle(real.lib())
+    for fn, kw in PIN_TESTS:
+        fn(o, **kw)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    with tempfile.TemporaryDirectory() as tmp:
+        o = MutantOracle(real.lib(_compile_mutant(name, tmp)))
+        caught = []
+        for fn, kw in PIN_TESTS:
+            try:
+                fn(o, **kw)
+            except AssertionError:
+                caught.append(fn.__name__)
+        assert caught, "no pin caught mutant %s" % name

@@ -1,0 +1,507 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each test fixes the oracle against a value the pages print (tests/golden/),
+a closed form, a brute-force enumeration of the definition, an invariant, or
+a library routine in a special case where the method reduces to it.  None of
+them re-types the oracle's own loops.  tests/test_oracle_mutants.py plants
+mistakes in copies of the oracle and checks that these pins catch them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import read_golden, read_golden_table
+
+F32 = np.float32
+
+
+def bits(values):
+    import torch
+    t = torch.tensor(np.asarray(values, dtype=np.float32).ravel())
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(np.shape(values))
+
+
+def f32(b):
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def route_to_ranks(dest_lists, R, E, K):
+    """topk ids for tokens of source 0..: dest_lists[s][t] = list of ranks, one
+    expert per listed rank (the first expert of that rank), padded with -1."""
+    Epr = E // R
+    T = max(len(x) for x in dest_lists)
+    ids = np.full((R, T, K), -1, np.int32)
+    for s, toks in enumerate(dest_lists):
+        for t, ranks in enumerate(toks):
+            for k, d in enumerate(ranks):
+                ids[s, t, k] = d * Epr
+    return ids
+
+
+def planes_with(routing, R, m, H, value_fn):
+    """expert_out [R,R,m,H] whose valid slot (d,s,j) holds value_fn(d,s,j)."""
+    eo = np.full((R, R, m, H), 0x7FC0, np.uint16)    # NaN in padding
+    for d in range(R):
+        for s in range(R):
+            for j in range(routing["recv_counts"][d, s]):
+                eo[d, s, j, :] = bits(np.full(H, value_fn(d, s, j), np.float32))
+    return eo
+
+
+# --------------------------------------------------------------------------
+# bf16 narrowing: a library routine (torch's round-to-nearest-even) pins it
+# --------------------------------------------------------------------------
+
+def test_bf16_rounding_matches_library_routine(oracle):
+    rng = np.random.default_rng(1)
+    raw = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    vals = raw.view(np.float32)
+    vals = vals[~np.isnan(vals)]
+    # exact ties, subnormals, overflow edge, infinities, signed zeros
+    extra = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -130,
+                      3.3895314e38, 3.4e38, np.inf, -np.inf, 0.0, -0.0,
+                      1.013671875, 255.0], np.float32)
+    vals = np.concatenate([vals, extra])
+    got = oracle.bf16_bits(vals)
+    assert np.array_equal(got, bits(vals))
+    nan = oracle.bf16_bits(np.array([np.nan], np.float32))
+    assert np.isnan(f32(nan)).all()
+
+
+def test_bf16_widening_is_exact(oracle):
+    allb = np.arange(0, 2 ** 16, dtype=np.uint32).astype(np.uint16)
+    finite = ~np.isnan(f32(allb))
+    import torch
+    ref = torch.from_numpy(allb.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    h = oracle.lib()
+    got = np.array([h.oracle_f32_from_bf16(int(b)) for b in allb[finite][::7]], np.float32)
+    assert np.array_equal(got, ref[finite][::7])
+
+
+# --------------------------------------------------------------------------
+# The pages' probes (tests/golden)
+# --------------------------------------------------------------------------
+
+def test_probe_pow2_rank_sum_is_255(oracle):
+    g = read_golden("pow2_rank_sum.txt")
+    R = int(g["ep_size"])
+    E, K, H, T = R, R, 136, 1          # one expert per rank, TOPK = world
+    ids = route_to_ranks([[list(range(R))] * T for _ in range(R)], R, E, K)
+    w = np.full(ids.shape, 1.0 / K, np.float32)
+    r = oracle.route(ids, w, E, T)
+    eo = planes_with(r, R, T, H, lambda d, s, j: 2.0 ** d)
+    c = oracle.combine(r, eo, weighted=False)
+    assert np.all(f32(c["out"]) == float(g["combined"]))
+    assert np.all(c["acc"] == F32(float(g["combined"])))
+
+
+def _tree_bf16(vals, narrow):
+    """The pages' hand-unrolled pairwise tree over eight top-k slots with a
+    bf16 rounding after every add (((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)))."""
+    a = list(vals)
+    for stride in (1, 2, 4):
+        for i in range(0, 8, 2 * stride):
+            a[i] = narrow(a[i] + a[i + stride])
+    return a[0]
+
+
+def test_probe_reduction_discriminator(oracle):
+    g = read_golden("reduction_discriminator.txt")
+    contribs = [float(eval(v, {})) for v in g["contributions"].split(",")]
+    R = len(contribs)
+    E, K, H = R, R, 8
+    ids = route_to_ranks([[list(range(R))] for _ in range(R)], R, E, K)
+    r = oracle.route(ids, np.full(ids.shape, 0.125, np.float32), E, 1)
+    eo = planes_with(r, R, 1, H, lambda d, s, j: contribs[d])
+    c = oracle.combine(r, eo, weighted=False)
+    adopted = float(g[g["adopted"]])
+    assert np.all(f32(c["out"]) == adopted)                       # 1.015625
+    # The probe discriminates: the other two models give the other printed values.
+    narrow = lambda v: float(f32(oracle.bf16_bits(np.array([v], np.float32)))[0])
+    assert _tree_bf16(contribs, narrow) == float(g["bf16_tree"])
+    seq = 0.0
+    for v in contribs:
+        seq = narrow(seq + v)
+    assert seq == float(g["sequential_bf16"])
+    assert len({adopted, float(g["bf16_tree"]), float(g["sequential_bf16"])}) == 3
+
+
+def test_probe_slot_order_is_ascending_token(oracle):
+    g = read_golden("slot_order_probe.txt")
+    T, R = int(g["tokens"]), int(g["ep_size"])
+    E, K, H = R, R, 16
+    ids = route_to_ranks([[list(range(R))] * T for _ in range(R)], R, E, K)
+    r = oracle.route(ids, np.full(ids.shape, 0.125, np.float32), E, T)
+    eo = planes_with(r, R, T, H, lambda d, s, j: float(j))
+    c = oracle.combine(r, eo, weighted=False)
+    expect = [float(v) for v in g["expect"].split(",")]
+    got_fi = [float(v) for v in g["got_flashinfer"].split(",")]
+    for s in range(R):
+        per_token = f32(c["out"][s * T:(s + 1) * T, 0])
+        assert list(per_token) == expect
+        assert np.all(f32(c["out"][s * T:(s + 1) * T]) == per_token[:, None])
+    # the total is conserved under any per-rank permutation, so it cannot tell
+    assert sum(expect) == sum(got_fi) == float(g["total"])
+
+
+def test_probe_partial_routing_and_duplicates(oracle):
+    g = read_golden("routing_probes.txt")
+    R, E, K, H = 4, 16, 3, 24
+    Epr = E // R
+    # tokens alternate between destination pairs {0,2} and {1,3}; token 2 puts
+    # all three experts on rank 3 (duplicates on one rank).
+    ids = np.full((R, 6, K), -1, np.int32)
+    for s in range(R):
+        for t in range(6):
+            if t == 2:
+                ids[s, t] = [3 * Epr, 3 * Epr + 1, 3 * Epr + 1]
+            elif t % 2 == 0:
+                ids[s, t, :2] = [0 * Epr + t % Epr, 2 * Epr + 1]
+            else:
+                ids[s, t, :2] = [1 * Epr, 3 * Epr + 2]
+    r = oracle.route(ids, np.full(ids.shape, 0.5, np.float32), E, 6)
+    # compaction: each plane holds only the tokens routed there, in order
+    assert list(r["src_token"][0, 0, :3]) == [0, 4, -1]
+    assert list(r["src_token"][3, 0, :4]) == [1, 2, 3, 5]
+    x = np.full((R, 6, H), bits(np.float32(1.0)), np.uint16)
+    d = oracle.dispatch(ids, np.full(ids.shape, 0.5, np.float32), x, E, 6, r)
+    c = oracle.combine(r, d["recv_x"], weighted=False)
+    out = f32(c["out"]).reshape(R, 6, H)
+    two = float(g["partial_routing_two_destinations"])
+    one = float(g["duplicate_experts_one_rank"])
+    for t in range(6):
+        assert np.all(out[:, t] == (one if t == 2 else two))
+
+
+# --------------------------------------------------------------------------
+# Statistics of routing against a closed form and the pages' counts
+# --------------------------------------------------------------------------
+
+def expected_distinct(R, E, K):
+    """Expected number of distinct owner ranks of K distinct uniform experts:
+    a rank is missed iff all K experts avoid its E/R experts."""
+    return R * (1.0 - math.comb(E - E // R, K) / math.comb(E, K))
+
+
+@pytest.mark.parametrize("R,E,K,T,expected", [(8, 256, 8, 8192, 5.2947),
+                                              (16, 512, 8, 1024, 6.4876),
+                                              (2, 8, 2, 16, 1.5714)])
+def test_mean_distinct_ranks_closed_form(oracle, R, E, K, T, expected):
+    from combine_topk_ids_rank_gb300 import synth
+    assert abs(expected_distinct(R, E, K) - expected) < 1e-4
+    ids = synth.topk_ids(0, R, T, E, K, "uniform")
+    r = oracle.route(ids, synth.topk_weights(0, R, T, K), E, T)
+    n = R * T
+    per_token = np.array([bin(int(v)).count("1") for v in r["dmask"].ravel()])
+    assert r["recv_counts"].sum() == per_token.sum()
+    se = per_token.std() / math.sqrt(n)
+    assert abs(per_token.mean() - expected) < max(5 * se, 1e-9)
+
+
+def test_pages_recv_counts_match_closed_form():
+    rows = read_golden_table("recv_counts_ep8_top8.txt")
+    mu = expected_distinct(8, 256, 8)
+    # the standard deviation of the distinct-rank count of one token
+    sd = 0.75
+    for T, recv in rows:
+        n = 8 * T
+        assert abs(recv / n - mu) < 5 * sd / math.sqrt(n) + 1e-9, (T, recv)
+
+
+# --------------------------------------------------------------------------
+# Brute force on tiny inputs: the definition enumerated a different way
+# --------------------------------------------------------------------------
+
+def brute_force_route(ids, w, E):
+    R, T, K = ids.shape
+    Epr = E // R
+    valid = lambda e: 0 <= e < E
+    dests = [[{int(e) // Epr for e in ids[s, t] if valid(e)} for t in range(T)]
+             for s in range(R)]
+    slot = np.full((R, T, R), -1)
+    wd = np.zeros((R, T, R), np.float32)
+    for s in range(R):
+        for t in range(T):
+            for d in dests[s][t]:
+                # slot = number of earlier tokens of the same source sent to d
+                slot[s, t, d] = sum(1 for u in range(t) if d in dests[s][u])
+                acc = F32(0.0)
+                for k in range(K):
+                    if valid(ids[s, t, k]) and ids[s, t, k] // Epr == d:
+                        acc = F32(acc + w[s, t, k])
+                wd[s, t, d] = acc
+    counts = np.zeros((R, R), int)
+    for d in range(R):
+        for s in range(R):
+            counts[d, s] = sum(1 for t in range(T) if d in dests[s][t])
+    local = np.zeros((R, Epr), int)
+    for e in ids.ravel():
+        if valid(e):
+            local[e // Epr, e % Epr] += 1
+    bad = sum(1 for e in ids.ravel() if not valid(e) and e != -1)
+    return slot, wd, counts, local, bad
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_route_brute_force(oracle, seed):
+    rng = np.random.default_rng(seed)
+    R, T, K, E = [(4, 37, 3, 16), (2, 16, 2, 8), (8, 20, 8, 64), (3, 9, 5, 12)][seed]
+    ids = rng.integers(-1, E, (R, T, K)).astype(np.int32)   # repeats and -1 allowed
+    if seed == 3:
+        ids[0, 0, 0] = E          # invalid ids are counted and skipped
+        ids[1, 2, 1] = -7
+    w = rng.standard_normal((R, T, K)).astype(np.float32)
+    m = T + 3
+    r = oracle.route(ids, w, E, m)
+    slot, wd, counts, local, bad = brute_force_route(ids, w, E)
+    assert np.array_equal(r["send_slot"], slot)
+    assert np.array_equal(r["wd"].view(np.uint32), wd.view(np.uint32))
+    assert np.array_equal(r["recv_counts"], counts)
+    assert np.array_equal(r["local_expert_counts"], local)
+    assert r["invalid"] == bad
+    for d in range(R):
+        for s in range(R):
+            toks = [t for t in range(T) if slot[s, t, d] >= 0]
+            assert list(r["src_token"][d, s, :len(toks)]) == toks
+            assert np.all(r["src_token"][d, s, len(toks):] == -1)
+
+
+def test_route_invariants_decode_shape(oracle):
+    from combine_topk_ids_rank_gb300 import synth
+    R, T, E, K = 8, 64, 256, 8
+    ids = synth.topk_ids(3, R, T, E, K)
+    r = oracle.route(ids, synth.topk_weights(3, R, T, K), E, T)
+    pop = np.array([bin(int(v)).count("1") for v in r["dmask"].ravel()])
+    assert r["recv_counts"].sum() == pop.sum()
+    assert r["local_expert_counts"].sum() == (ids >= 0).sum()
+    seen = set()
+    for d in range(R):
+        for s in range(R):
+            c = r["recv_counts"][d, s]
+            for j in range(c):
+                t = r["src_token"][d, s, j]
+                assert r["send_slot"][s, t, d] == j
+                seen.add((s, t, d))
+    assert len(seen) == pop.sum()
+    assert np.all((r["send_slot"] >= 0) == (((r["dmask"][..., None] >> np.arange(R)) & 1) == 1))
+
+
+# --------------------------------------------------------------------------
+# Dispatch: identity encoded in the payload, metadata masking
+# --------------------------------------------------------------------------
+
+def test_dispatch_payload_identity(oracle):
+    R, T, K, E, H = 4, 50, 3, 16, 72     # H not a multiple of 64 nor of 8*32
+    rng = np.random.default_rng(7)
+    ids = rng.integers(-1, E, (R, T, K)).astype(np.int32)
+    w = rng.random((R, T, K)).astype(np.float32)
+    m = 64
+    # x[s,t,:] encodes (s, t, h) with small integers, exact in bf16
+    x = np.empty((R, T, H), np.float32)
+    for s in range(R):
+        for t in range(T):
+            x[s, t] = np.arange(H) % 200
+            x[s, t, 0], x[s, t, 1] = s, t
+    r = oracle.route(ids, w, E, m)
+    pad = np.uint16(0xFFFF)
+    d = oracle.dispatch(ids, w, bits(x), E, m, r,
+                        recv_x=np.full((R, R, m, H), pad, np.uint16),
+                        recv_ids=np.full((R, R, m, K), -99, np.int32),
+                        recv_w=np.full((R, R, m, K), -9.0, np.float32))
+    Epr = E // R
+    for dd in range(R):
+        for s in range(R):
+            c = r["recv_counts"][dd, s]
+            rows = f32(d["recv_x"][dd, s, :c])
+            assert np.all(rows[:, 0] == s)
+            assert np.array_equal(rows[:, 1].astype(int), r["src_token"][dd, s, :c])
+            assert np.all(rows[:, 2:] == (np.arange(2, H) % 200))
+            assert np.all(d["recv_x"][dd, s, c:] == pad)          # padding untouched
+            assert np.all(d["recv_ids"][dd, s, c:] == -99)
+            for j in range(c):
+                t = r["src_token"][dd, s, j]
+                for k in range(K):
+                    e = ids[s, t, k]
+                    local = 0 <= e < E and e // Epr == dd
+                    assert d["recv_ids"][dd, s, j, k] == (e if local else -1)
+                    assert d["recv_w"][dd, s, j, k] == (w[s, t, k] if local else 0.0)
+
+
+# --------------------------------------------------------------------------
+# Combine: closed forms with identity experts, exactly-once reduction
+# --------------------------------------------------------------------------
+
+def _identity_case(oracle, R=4, T=40, K=4, E=32, H=64, seed=5, weights=None):
+    from combine_topk_ids_rank_gb300 import synth
+    ids = synth.topk_ids(seed, R, T, E, K)
+    w = synth.topk_weights(seed, R, T, K) if weights is None else weights
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    r = oracle.route(ids, w, E, T)
+    d = oracle.dispatch(ids, w, x, E, T, r)
+    return ids, w, x, r, d
+
+
+def test_identity_unweighted_is_n_times_x(oracle):
+    ids, w, x, r, d = _identity_case(oracle)
+    c = oracle.combine(r, d["recv_x"], weighted=False)
+    R, T, H = x.shape
+    n = np.array([bin(int(v)).count("1") for v in r["dmask"].ravel()], np.float32)
+    # n*x is exact in binary32 (8-bit significand times n <= 8); the result is
+    # the round-to-nearest-even of that exact value
+    exact = n[:, None] * f32(x).reshape(R * T, H)
+    assert np.array_equal(c["acc"], exact)
+    assert np.array_equal(c["out"], bits(exact))
+
+
+def test_identity_weighted_dyadic_returns_x_once(oracle):
+    R, T, K = 4, 40, 8
+    w = np.full((R, T, K), 1.0 / K, np.float32)       # sums exactly to 1
+    ids, w, x, r, d = _identity_case(oracle, R=R, T=T, K=K, weights=w)
+    c = oracle.combine(r, d["recv_x"], weighted=True)
+    # reduced exactly once: x, not 2x (the double-reduce failure)
+    assert np.array_equal(c["out"], x.reshape(R * T, -1))
+
+
+def test_weighted_sum_within_fp32_error_bound(oracle):
+    from combine_topk_ids_rank_gb300 import synth
+    R, T, K, E, H = 8, 24, 8, 64, 40
+    ids = synth.topk_ids(11, R, T, E, K)
+    w = synth.topk_weights(11, R, T, K)
+    r = oracle.route(ids, w, E, T)
+    eo = synth.expert_out_planes(11, R, T, H, r["recv_counts"])
+    c = oracle.combine(r, eo, weighted=True)
+    Epr = E // R
+    for s in range(R):
+        for t in range(T):
+            terms, absum = np.zeros(H), np.zeros(H)
+            for dd in range(R):
+                j = r["send_slot"][s, t, dd]
+                if j < 0:
+                    continue
+                wsum = sum(float(w[s, t, k]) for k in range(K) if ids[s, t, k] // Epr == dd)
+                v = f32(eo[dd, s, j]).astype(np.float64)
+                terms += wsum * v
+                absum += abs(wsum * v)
+            got = c["acc"][s * T + t].astype(np.float64)
+            # <= 8 fp32 products and adds, plus the fp32 sum of the weights
+            assert np.all(np.abs(got - terms) <= 24 * 2.0 ** -24 * absum + 1e-30)
+
+
+def test_ascending_rank_order_closed_form(oracle):
+    # messages 2^24, 1, -2^24 on ranks 0, 1, 2: in fp32, (2^24 + 1) rounds to
+    # 2^24 (tie to even), so ascending order gives exactly 0; any other order
+    # that adds the 1 after a cancellation gives 1.
+    R, E, K, H = 3, 3, 3, 8
+    ids = route_to_ranks([[[0, 1, 2]] for _ in range(R)], R, E, K)
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 1)
+    vals = [2.0 ** 24, 1.0, -(2.0 ** 24)]
+    eo = planes_with(r, R, 1, H, lambda d, s, j: vals[d])
+    c = oracle.combine(r, eo, weighted=False)
+    assert np.all(c["acc"] == 0.0)
+
+
+def test_weighted_product_is_not_fused(oracle):
+    # rank 0: weight 1, message -(1 + 2^-7); rank 1: weight 1 + 2^-23,
+    # message 1 + 2^-7.  Rounded product then add gives 2^-23 exactly; a fused
+    # multiply-add keeps the 2^-30 term.  The pages: no FMA in the combine.
+    R, E, K, H = 2, 2, 2, 8
+    ids = route_to_ranks([[[0, 1]], [[0, 1]]], R, E, K)
+    w = np.zeros(ids.shape, np.float32)
+    w[:, :, 0] = 1.0
+    w[:, :, 1] = np.float32(1 + 2.0 ** -23)
+    r = oracle.route(ids, w, E, 1)
+    vals = [-(1 + 2.0 ** -7), 1 + 2.0 ** -7]
+    eo = planes_with(r, R, 1, H, lambda d, s, j: vals[d])
+    c = oracle.combine(r, eo, weighted=True)
+    assert np.all(c["acc"] == np.float32(2.0 ** -23))
+
+
+# --------------------------------------------------------------------------
+# Fused epilogue: special cases that reduce to closed forms / a library routine
+# --------------------------------------------------------------------------
+
+def test_residual_add_uses_fp32_sum(oracle):
+    # acc = 1 + 3*2^-9 (messages 1, 2^-9, 2^-8: exact in fp32), residual -2^-9:
+    # the fp32 sum 1 + 2^-8 is exact and a tie, so residual_out = bf16 1.0.
+    # Narrowing acc first would give 1.0078125.
+    R, E, K, H = 3, 3, 3, 8
+    ids = route_to_ranks([[[0, 1, 2]] for _ in range(R)], R, E, K)
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 1)
+    vals = [1.0, 2.0 ** -9, 2.0 ** -8]
+    eo = planes_with(r, R, 1, H, lambda d, s, j: vals[d])
+    res = bits(np.full((R, 1, H), -(2.0 ** -9), np.float32))
+    gam = bits(np.ones(H, np.float32))
+    c = oracle.combine(r, eo, weighted=False, residual=res, gamma=gam, eps=1e-6)
+    assert np.all(f32(c["residual_out"]) == 1.0)
+
+
+@pytest.mark.parametrize("cval", [1e-3, 0.75, -3.0])
+def test_rmsnorm_constant_row_closed_form(oracle, cval):
+    # one message per token equal to c everywhere, residual 0: hsum = c, so
+    # y = c / sqrt(c^2 + eps) * gamma.
+    R, E, K, H, eps = 2, 2, 1, 96, 1e-6
+    ids = route_to_ranks([[[0], [1]], [[1], [0]]], R, E, K)
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 2)
+    c_bf = float(f32(bits(np.float32(cval))))
+    eo = planes_with(r, R, 2, H, lambda d, s, j: c_bf)
+    res = np.zeros((R, 2, H), np.uint16)
+    g = bits((1.0 + 0.1 * np.sin(np.arange(H))).astype(np.float32))
+    out = oracle.combine(r, eo, weighted=False, residual=res, gamma=g, eps=eps)
+    eps32 = float(np.float32(eps))          # eps crosses the ABI as binary32
+    expect = c_bf / math.sqrt(c_bf * c_bf + eps32) * f32(g).astype(np.float64)
+    assert np.allclose(out["y"], expect[None, :], rtol=1e-12, atol=0)
+
+
+def test_rmsnorm_matches_library_routine(oracle):
+    import torch
+    from combine_topk_ids_rank_gb300 import synth
+    R, T, K, E, H = 4, 12, 4, 16, 200
+    ids = synth.topk_ids(2, R, T, E, K)
+    w = synth.topk_weights(2, R, T, K)
+    r = oracle.route(ids, w, E, T)
+    eo = synth.expert_out_planes(2, R, T, H, r["recv_counts"])
+    res = synth.per_rank_rows(2, synth.RESIDUAL, R, T, H)
+    g = synth.gamma(2, H)
+    c = oracle.combine(r, eo, weighted=True, residual=res, gamma=g, eps=1e-6)
+    # hsum is the binary32 sum of the reduced row and the residual
+    hsum32 = c["acc"] + f32(res).reshape(R * T, H)
+    hsum = torch.from_numpy(hsum32.astype(np.float64))
+    ref = torch.nn.functional.rms_norm(hsum, (H,), weight=torch.from_numpy(
+        f32(g).astype(np.float64)), eps=float(np.float32(1e-6))).numpy()
+    assert np.allclose(c["y"], ref, rtol=1e-12, atol=1e-12)
+    # out is y narrowed once (through binary32)
+    assert np.array_equal(c["out"], bits(c["y"].astype(np.float32)))
+
+
+def test_tokens_without_experts(oracle):
+    R, E, K, H = 2, 4, 2, 16
+    ids = np.full((R, 3, K), -1, np.int32)
+    ids[0, 1] = [0, 3]
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 3)
+    assert r["dmask"][0, 0] == 0 and r["dmask"][1, 2] == 0
+    eo = planes_with(r, R, 3, H, lambda d, s, j: 1.0)
+    res = bits(np.full((R, 3, H), 0.5, np.float32))
+    c0 = oracle.combine(r, eo, weighted=False)
+    assert np.all(f32(c0["out"]).reshape(R, 3, H)[1] == 0.0)
+    c1 = oracle.combine(r, eo, weighted=False, residual=res,
+                        gamma=bits(np.ones(H, np.float32)), eps=0.0)
+    # no expert: hsum = residual, y = RMSNorm(residual) = 1 for a constant row
+    assert np.all(f32(c1["residual_out"]).reshape(R, 3, H)[1] == 0.5)
+    assert np.allclose(c1["y"].reshape(R, 3, H)[1], 1.0)
+
+
+def test_token_subset_matches_full(oracle):
+    from combine_topk_ids_rank_gb300 import synth
+    R, T, K, E, H = 4, 20, 4, 16, 48
+    ids = synth.topk_ids(9, R, T, E, K)
+    w = synth.topk_weights(9, R, T, K)
+    r = oracle.route(ids, w, E, T)
+    eo = synth.expert_out_planes(9, R, T, H, r["recv_counts"])
+    res = synth.per_rank_rows(9, synth.RESIDUAL, R, T, H)
+    g = synth.gamma(9, H)
+    full = oracle.combine(r, eo, True, res, g, 1e-6)
+    pick = np.array([0, 7, 33, R * T - 1])
+    sub = oracle.combine(r, eo, True, res, g, 1e-6, tokens=pick)
+    for key in ("acc", "out", "residual_out", "y"):
+        assert np.array_equal(sub[key], full[key][pick])
