@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Benchmark of the dispatch + combine round trip on logical EP ranks.
+
+One step = the whole hot path on one batch: routing (two kernels), the
+dispatch row scatter, and the fused weighted combine with residual add and
+RMSNorm (one kernel) -- four launches through the C ABI.  The default
+workload is prefill: ep_size 8, 4096 tokens per rank, hidden 7168, 256
+experts, top-8 with Zipf(1.2) expert popularity (contiguous placement).
+
+Prints one JSON line.  `value` is tokens/s over all GPUs with inputs already
+in HBM; `e2e` is the same metric with the step's inputs copied from pinned
+host memory and its outputs copied back inside the timed region;
+`roofline` is the dominant kernel (the fused combine) against the measured
+HBM copy peak; `cpu_baseline` is the single-threaded C oracle on a bounded
+sample of the same workload.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun every rank runs its own replica (weak scaling: the ranks
+share no data); rank 0 prints.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default="prefill",
+                    choices=["tiny", "decode", "prefill", "wide", "ladder"])
+    ap.add_argument("--tokens", type=int, default=None, help="tokens per rank (ladder rung)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def workload(args):
+    from combine_topk_ids_rank_gb300 import synth
+    w = synth.WORKLOADS[args.config]
+    if args.tokens is not None:
+        w = w.rung(args.tokens)
+    return w
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def phase_bytes(w, recv_rows):
+    """Algorithmic payload bytes of one call of each phase (rows of 2H bytes)."""
+    N, row = w.tokens, 2 * w.hidden
+    dispatch = (N + recv_rows) * row
+    combine = recv_rows * row + N * row            # messages read, output written
+    if w.fused:
+        combine += 2 * N * row + row               # residual read, residual_out, gamma
+    return dispatch, combine
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The C oracle (single-threaded, as it stands) on the first T_s tokens
+    per rank of the workload: route + dispatch + combine, outputs
+    preallocated outside the timed call."""
+
+    def __init__(self, w, tokens_per_rank, seed):
+        import numpy as np
+        from combine_topk_ids_rank_gb300 import synth
+        from oracle import oracle
+        self.oracle = oracle
+        self.w = w.rung(tokens_per_rank)
+        ws = self.w
+        R, T, H, K = ws.ep_size, ws.tokens_per_rank, ws.hidden, ws.top_k
+        self.inp = synth.inputs(ws, seed)
+        r = oracle.route(self.inp["topk_ids"], self.inp["topk_w"], ws.num_experts, T)
+        self.eo = None
+        if not ws.identity_experts:
+            self.eo = synth.expert_out_planes(seed, R, T, H, r["recv_counts"])
+        self.recv = dict(recv_x=np.zeros((R, R, T, H), np.uint16),
+                         recv_ids=np.zeros((R, R, T, K), np.int32),
+                         recv_w=np.zeros((R, R, T, K), np.float32))
+        n = R * T
+        self.outs = dict(acc=np.zeros((n, H), np.float32), out=np.zeros((n, H), np.uint16),
+                         y=np.zeros((n, H), np.float64))
+        if ws.fused:
+            self.outs["residual_out"] = np.zeros((n, H), np.uint16)
+
+    @property
+    def tokens(self):
+        return self.w.tokens
+
+    def step(self) -> float:
+        o, ws, inp = self.oracle, self.w, self.inp
+        t0 = time.perf_counter()
+        r = o.route(inp["topk_ids"], inp["topk_w"], ws.num_experts, ws.tokens_per_rank)
+        d = o.dispatch(inp["topk_ids"], inp["topk_w"], inp["x"], ws.num_experts,
+                       ws.tokens_per_rank, r, **self.recv)
+        eo = d["recv_x"] if ws.identity_experts else self.eo
+        o.combine(r, eo, ws.weighted, inp.get("residual"), inp.get("gamma"), ws.eps,
+                  outputs=self.outs)
+        return time.perf_counter() - t0
+
+
+def oracle_seconds_per_token(w, seed):
+    s = OracleSample(w, min(w.tokens_per_rank, 16), seed)
+    s.step()
+    return min(s.step() for _ in range(2)) / s.tokens
+
+
+def cpu_baseline(w, seed, target_seconds):
+    per_tok = oracle_seconds_per_token(w, seed)
+    T_s = int(max(1, min(w.tokens_per_rank, target_seconds / per_tok / w.ep_size)))
+    sample = OracleSample(w, T_s, seed)
+    sec = sample.step()
+    return {"value": sample.tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "route+dispatch+combine of the first %d tokens per rank (%d tokens, "
+                      "%s), single-threaded C oracle, %.1f s" % (
+                          T_s, sample.tokens, w.name, sec)}
+
+
+def run_reference(args, w, rank):
+    """The oracle as the reference arm: each step a bounded sample."""
+    if rank != 0:
+        return
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_tok = oracle_seconds_per_token(w, args.seed)
+    T_s = int(max(1, min(w.tokens_per_rank, budget / per_tok / w.ep_size)))
+    sample = OracleSample(w, T_s, args.seed)
+    for _ in range(args.warmup):
+        sample.step()
+    secs = [sample.step() for _ in range(args.steps)]
+    total = sum(secs)
+    value = sample.tokens * args.steps / total
+    desc = ("route+dispatch+combine of the first %d tokens per rank (%d tokens of %s) "
+            "per step, single-threaded C oracle" % (T_s, sample.tokens, w.name))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, recv_rows=None):
+    d = {"workload": w.name, "ep_size": w.ep_size, "tokens_per_rank": w.tokens_per_rank,
+         "max_tokens_per_rank": w.max_tokens, "runtime_max_tokens_per_rank": w.runtime_max,
+         "hidden": w.hidden, "num_experts": w.num_experts, "top_k": w.top_k,
+         "routing": w.routing + ("(s=%.1f, contiguous placement)" % w.zipf_s
+                                 if w.routing == "zipf" else ""),
+         "combine": ("weighted" if w.weighted else "unweighted") +
+                    (" + residual + RMSNorm" if w.fused else ""),
+         "l2": "inputs larger than L2 (129 MB)" if w.tokens * w.hidden * 2 > 2 * 129e6
+               else "L2 flushed (256 MB write) before every timed phase"}
+    if recv_rows is not None:
+        d["recv_rows"] = int(recv_rows)
+        d["mean_dest_ranks"] = recv_rows / w.tokens
+    return d
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, w, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from combine_topk_ids_rank_gb300 import synth
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    R, T, H, E, K = w.ep_size, w.tokens_per_rank, w.hidden, w.num_experts, w.top_k
+    N = w.tokens
+
+    # ---- inputs: routing from the seeded generator, payloads N(0,1) bf16 ----
+    ids_h = torch.from_numpy(synth.topk_ids(args.seed, R, T, E, K, w.routing, w.zipf_s))
+    wts_h = torch.from_numpy(synth.topk_weights(args.seed, R, T, K))
+    g = torch.Generator().manual_seed(args.seed)
+    x_h = torch.randn((R, T, H), generator=g).to(torch.bfloat16)
+    res_h = torch.randn((R, T, H), generator=g).to(torch.bfloat16) if w.fused else None
+    gam_h = (1 + 0.1 * torch.randn((H,), generator=g)).to(torch.bfloat16)
+    ids, wts, x = ids_h.to(dev), wts_h.to(dev), x_h.to(dev)
+    res = res_h.to(dev) if w.fused else None
+    gam = gam_h.to(dev)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+    rout = torch.empty_like(out) if w.fused else None
+
+    a2a = MoeA2A(R, w.max_tokens, H, E, K, dev)
+    view = a2a.dispatch(ids, wts, x, w.runtime_max)
+    if not w.identity_experts:
+        gd = torch.Generator(device=dev).manual_seed(args.seed + 1)
+        pay = a2a.combine_payload()
+        pay.copy_(torch.randn(pay.shape, generator=gd, device=dev, dtype=torch.float32)
+                  .to(torch.bfloat16))
+    eo = view.recv_x if w.identity_experts else None
+    a2a.combine(eo, w.weighted, res, gam, w.eps, out, rout)
+    torch.cuda.synchronize()
+    recv_rows = int(view.recv_counts.sum().item())
+    st, flags = a2a.get_error()
+    if st != 0:
+        raise RuntimeError("device flag set: status %d flags %#x" % (st, flags))
+
+    def step(stream_events=None):
+        if stream_events is not None:
+            stream_events[0].record()
+        a2a.dispatch(ids, wts, x, w.runtime_max)
+        if stream_events is not None:
+            stream_events[1].record()
+        a2a.combine(eo, w.weighted, res, gam, w.eps, out, rout)
+        if stream_events is not None:
+            stream_events[2].record()
+
+    flush = None
+    cfg = config_dict(w, recv_rows)
+    if "flushed" in cfg["l2"]:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: inputs resident in HBM ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local_rank)
+    time.sleep(0.25)
+    start.record()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        step(ev[i])
+    stop.record()
+    torch.cuda.synchronize()
+    time.sleep(0.15)
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    disp_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if flush is not None:       # time only the two phases, not the flush
+        total_ms = sum(disp_ms) + sum(comb_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    st, flags = a2a.get_error()
+    if st != 0:
+        raise RuntimeError("device flag set during the timed region: %d %#x" % (st, flags))
+
+    d_bytes, c_bytes = phase_bytes(w, recv_rows)
+    peak, peak_kind = measured_peak()
+    d_avg, c_avg = statistics.fmean(disp_ms), statistics.fmean(comb_ms)
+
+    def pct(v, q):
+        s = sorted(v)
+        return s[min(len(s) - 1, int(q * len(s)))]
+
+    phases = {
+        "dispatch": {"ms_avg": d_avg, "ms_p50": pct(disp_ms, 0.5), "ms_p10": pct(disp_ms, 0.1),
+                     "ms_p90": pct(disp_ms, 0.9), "bytes": d_bytes,
+                     "gbs": d_bytes / d_avg / 1e6, "frac": d_bytes / d_avg / 1e6 / peak,
+                     "kernels": ["route_count", "route_scan", "dispatch_rows"]},
+        "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
+                    "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
+                    "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
+                    "kernels": ["combine"]},
+    }
+    eff_gbs = (d_bytes + c_bytes) / ms_per_step / 1e6
+    tokens_per_s = N * world / (ms_per_step / 1e3)
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()
+        hids, hw, hx = pin(ids_h), pin(wts_h), pin(x_h)
+        hres = pin(res_h) if w.fused else None
+        hout = torch.empty((R, T, H), dtype=torch.bfloat16).pin_memory()
+        hrout = torch.empty((R, T, H), dtype=torch.bfloat16).pin_memory() if w.fused else None
+        h2d = sum(t.numel() * t.element_size() for t in (hids, hw, hx, hres) if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in (hout, hrout) if t is not None)
+
+        def e2e_step():
+            ids.copy_(hids, non_blocking=True)
+            wts.copy_(hw, non_blocking=True)
+            x.copy_(hx, non_blocking=True)
+            if w.fused:
+                res.copy_(hres, non_blocking=True)
+            a2a.dispatch(ids, wts, x, w.runtime_max)
+            a2a.combine(eo, w.weighted, res, gam, w.eps, out, rout)
+            hout.copy_(out, non_blocking=True)
+            if w.fused:
+                hrout.copy_(rout, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": N * world / (e2e_ms / args.e2e_steps / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
+               "path": "pinned host -> device copies, moe_dispatch, moe_combine, "
+                       "device -> pinned host copies, one stream"}
+
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                tr = json.load(f)
+            ent = tr.get(w.name, {}).get("combine")
+            if ent and ent.get("source_sha1") == source_sha1("combine.cu"):
+                traffic = ent["dram_bytes_per_launch"]
+        except (OSError, ValueError, KeyError):
+            traffic = None
+
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded routing; N(0,1) bf16 payloads; random-init, no weights)",
+        "config": cfg,
+        "effective_gbs": eff_gbs, "hbm_frac": eff_gbs / peak,
+        "phases": phases,
+        "roofline": {"bound": "hbm", "kernel": "combine", "achieved": c_bytes / c_avg / 1e6,
+                     "peak": peak, "unit": "GB/s", "frac": c_bytes / c_avg / 1e6 / peak,
+                     "traffic": traffic, "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)"
+                     % peak_kind if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "gpu_launches": 4 * args.steps if T > 0 else 0,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    return line
+
+
+def source_sha1(name):
+    import hashlib
+    path = os.path.join(ROOT, "combine_topk_ids_rank_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workload(args)
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    line = run_gpu(args, w, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

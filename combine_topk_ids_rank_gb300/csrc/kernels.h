@@ -1,0 +1,97 @@
+// kernels.h -- parameter blocks and host launchers of the four kernels of
+// the dispatch / combine path.  Internal to libmoe_a2a.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Tokens per CTA of the two routing kernels (one token per thread).
+constexpr int kRouteTile = 256;
+
+// Routing, pass 1: destination mask of every token, per-tile destination
+// counts and per-tile expert histograms.
+struct RouteCountParams {
+    const int32_t *topk_ids;  // [R][T][K]
+    uint32_t *dmask;          // [R][T]
+    int32_t *tile_counts;     // [R][ntiles][RP]
+    int32_t *tile_hist;       // [R][ntiles][E]
+    uint32_t *flags;          // sticky device flag word
+    int R, T, K, E, Epr, RP, ntiles;
+};
+
+// Routing, pass 2: slots (ascending token order per plane), send table,
+// per-destination weights, source map, masked metadata rows, counts.
+struct RouteScanParams {
+    const int32_t *topk_ids;   // [R][T][K]
+    const float *topk_w;       // [R][T][K]
+    const uint32_t *dmask;     // [R][T]
+    const int32_t *tile_counts;
+    const int32_t *tile_hist;
+    int32_t *send_slot;        // [R][T][RP]
+    float *dest_weight;        // [R][T][RP]
+    int32_t *src_token;        // [R][R][m]
+    int32_t *recv_ids;         // [R][R][m][K]
+    float *recv_w;             // [R][R][m][K]
+    int32_t *recv_counts;      // [R][R]
+    int32_t *local_counts;     // [E]  (= [R][Epr])
+    int R, T, K, E, Epr, RP, m, ntiles;
+};
+
+// Dispatch rows: x[s][t] -> recv_x[d][s][slot] for every destination of
+// the token, staged through shared memory with bulk asynchronous copies.
+struct DispatchParams {
+    const uint8_t *x;          // bf16 [R][T][H] as bytes
+    const int32_t *send_slot;  // [R][T][RP]
+    uint8_t *recv_x;           // bf16 [R][R][m][H] as bytes
+    uint32_t *flags;
+    int R, T, RP, m;
+    int row_bytes;             // 2H
+    int chunk_bytes;           // <= row_bytes, multiple of 16
+    int chunks;                // ceil(row_bytes / chunk_bytes)
+    int stages;                // shared-memory ring depth
+    int stage_bytes;           // chunk_bytes + meta, 128-byte multiple
+    long long units;           // R * T * chunks
+};
+
+// Combine: ascending-rank fp32 gather-sum of each token's messages, with
+// the optional fused residual add + RMSNorm epilogue.
+struct CombineParams {
+    const uint16_t *expert_out;   // bf16 [R][R][m][H]
+    const int32_t *send_slot;     // [R][T][RP]
+    const float *dest_weight;     // [R][T][RP]
+    const uint16_t *residual;     // bf16 [R][T][H] or null
+    const uint16_t *gamma;        // bf16 [H] or null
+    uint16_t *out;                // bf16 [R][T][H]
+    uint16_t *residual_out;       // bf16 [R][T][H] or null
+    uint32_t *flags;
+    float eps;
+    int R, T, RP, m, H, H8;       // H8 = H / 8 (16-byte vectors per row)
+    long long tokens;             // R * T
+};
+
+struct LaunchShape {
+    int grid;
+    int block;
+    size_t smem;
+};
+
+cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st);
+cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pdl);
+
+// Dispatch: ring depth and per-SM residency for a row size.
+cudaError_t dispatch_prepare(int row_bytes, int RP, int num_sms, DispatchParams *p,
+                             LaunchShape *shape);
+cudaError_t launch_dispatch_rows(const DispatchParams &p, const LaunchShape &shape,
+                                 cudaStream_t st, bool pdl);
+
+// Combine: vectors per thread, block size and grid for a hidden size.
+cudaError_t combine_prepare(int H, bool weighted, bool fused, int num_sms,
+                            LaunchShape *shape, int *vpt);
+cudaError_t launch_combine(const CombineParams &p, bool weighted, bool fused, int vpt,
+                           const LaunchShape &shape, cudaStream_t st);
+
+}  // namespace moe

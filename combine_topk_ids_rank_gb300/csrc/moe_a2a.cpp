@@ -1,0 +1,332 @@
+// moe_a2a.cpp -- the C ABI declared in include/moe_a2a.h: configuration
+// checks, workspace layout, the dispatch/combine phase contract and the
+// launches of the four kernels.
+//
+// Phase contract (InferenceX PR #2450, "CollectiveX: add FlashInfer
+// one-sided NVLink EP for the GB SKUs", "The adapter" table): dispatch
+// refuses to run twice without a combine, combine requires a pending
+// dispatch, and the state returns to idle after combine;
+// runtime_max_tokens_per_rank <= max_num_tokens, with the workspace sized
+// once for the maximum.
+#include "moe_a2a.h"
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    size_t recv_x, expert_out, recv_ids, recv_w, src_token, recv_counts, local_counts;
+    size_t send_slot, dest_weight, dmask, tile_counts, tile_hist, flags, total;
+    int RP, ntiles_max;
+};
+
+bool config_ok(const moe_a2a_config_t *c) {
+    if (c == nullptr) return false;
+    if (c->ep_size < 1 || c->ep_size > MOE_MAX_EP_SIZE) return false;
+    if (c->max_tokens_per_rank < 1 || c->max_tokens_per_rank > (1 << 24)) return false;
+    if (c->hidden < 8 || c->hidden > MOE_MAX_HIDDEN || c->hidden % 8 != 0) return false;
+    if (c->num_experts < c->ep_size || c->num_experts > MOE_MAX_EXPERTS) return false;
+    if (c->num_experts % c->ep_size != 0) return false;
+    if (c->top_k < 1 || c->top_k > MOE_MAX_TOP_K) return false;
+    return true;
+}
+
+// Regions of the workspace, each 256-byte aligned, sized for M tokens.
+bool compute_layout(const moe_a2a_config_t *c, Layout *L) {
+    if (!config_ok(c)) return false;
+    const size_t R = c->ep_size, M = c->max_tokens_per_rank, H = c->hidden;
+    const size_t E = c->num_experts, K = c->top_k;
+    L->RP = (int)((R + 3) / 4 * 4);
+    L->ntiles_max = (int)((M + moe::kRouteTile - 1) / moe::kRouteTile);
+    const size_t RP = L->RP, NT = L->ntiles_max;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, kAlign);
+        return o;
+    };
+    L->recv_x = take(R * R * M * H * 2);
+    L->expert_out = take(R * R * M * H * 2);
+    L->recv_ids = take(R * R * M * K * 4);
+    L->recv_w = take(R * R * M * K * 4);
+    L->src_token = take(R * R * M * 4);
+    L->recv_counts = take(R * R * 4);
+    L->local_counts = take(E * 4);
+    L->send_slot = take(R * M * RP * 4);
+    L->dest_weight = take(R * M * RP * 4);
+    L->dmask = take(R * M * 4);
+    L->tile_counts = take(R * NT * RP * 4);
+    L->tile_hist = take(R * NT * E * 4);
+    L->flags = take(kAlign);
+    L->total = off;
+    return true;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct moe_a2a {
+    moe_a2a_config_t cfg;
+    uint8_t *ws;
+    size_t ws_bytes;
+    Layout L;
+    int phase;  // 0 idle, 1 dispatched
+    int T, m;   // of the pending dispatch
+    // lazily initialised on the first call that queues work
+    bool ready;
+    int device;
+    int num_sms;
+    moe::DispatchParams dispatch_tmpl;
+    moe::LaunchShape dispatch_shape;
+    bool combine_ready[4];
+    int combine_vpt[4];
+    moe::LaunchShape combine_shape[4];
+};
+
+namespace {
+
+template <typename T>
+T *at(moe_a2a_t *h, size_t off) {
+    return reinterpret_cast<T *>(h->ws + off);
+}
+
+int init_device(moe_a2a_t *h, cudaStream_t st) {
+    if (h->ready) return MOE_OK;
+    if (cudaGetDevice(&h->device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    std::memset(&h->dispatch_tmpl, 0, sizeof h->dispatch_tmpl);
+    if (moe::dispatch_prepare(2 * h->cfg.hidden, h->L.RP, h->num_sms, &h->dispatch_tmpl,
+                              &h->dispatch_shape) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    h->ready = true;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_a2a_workspace_bytes(const moe_a2a_config_t *cfg) {
+    Layout L;
+    return compute_layout(cfg, &L) ? L.total : 0;
+}
+
+int moe_a2a_create(const moe_a2a_config_t *cfg, void *d_workspace, size_t workspace_bytes,
+                   moe_a2a_t **out) {
+    if (out == nullptr) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    Layout L;
+    if (!compute_layout(cfg, &L)) return MOE_ERR_INVALID_ARG;
+    if (d_workspace == nullptr || !aligned(d_workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total) return MOE_ERR_CAPACITY;
+    moe_a2a_t *h = new (std::nothrow) moe_a2a_t;
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    std::memset(h, 0, sizeof *h);
+    h->cfg = *cfg;
+    h->ws = static_cast<uint8_t *>(d_workspace);
+    h->ws_bytes = workspace_bytes;
+    h->L = L;
+    h->phase = 0;
+    *out = h;
+    return MOE_OK;
+}
+
+int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
+                 const void *d_x, int32_t tokens_per_rank, int32_t runtime_max_tokens_per_rank,
+                 void *stream, moe_dispatch_view_t *out_view) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 0) return MOE_ERR_PHASE;
+    const int T = tokens_per_rank, m = runtime_max_tokens_per_rank;
+    if (T < 0 || m < 1) return MOE_ERR_INVALID_ARG;
+    if (m > h->cfg.max_tokens_per_rank || T > m) return MOE_ERR_CAPACITY;
+    if (T > 0) {
+        if (d_topk_ids == nullptr || d_topk_w == nullptr || d_x == nullptr)
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned(d_topk_ids, 4) || !aligned(d_topk_w, 4) || !aligned(d_x, 16))
+            return MOE_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = init_device(h, st);
+    if (rc != MOE_OK) return rc;
+
+    const int R = h->cfg.ep_size, E = h->cfg.num_experts, K = h->cfg.top_k;
+    const int RP = h->L.RP;
+    uint32_t *flags = at<uint32_t>(h, h->L.flags);
+
+    if (T == 0) {
+        if (cudaMemsetAsync(h->ws + h->L.recv_counts, 0, sizeof(int32_t) * R * R, st) !=
+                cudaSuccess ||
+            cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else {
+        const int ntiles = (T + moe::kRouteTile - 1) / moe::kRouteTile;
+
+        moe::RouteCountParams rc_p;
+        rc_p.topk_ids = d_topk_ids;
+        rc_p.dmask = at<uint32_t>(h, h->L.dmask);
+        rc_p.tile_counts = at<int32_t>(h, h->L.tile_counts);
+        rc_p.tile_hist = at<int32_t>(h, h->L.tile_hist);
+        rc_p.flags = flags;
+        rc_p.R = R, rc_p.T = T, rc_p.K = K, rc_p.E = E, rc_p.Epr = E / R, rc_p.RP = RP;
+        rc_p.ntiles = ntiles;
+        if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+        moe::RouteScanParams rs;
+        rs.topk_ids = d_topk_ids;
+        rs.topk_w = d_topk_w;
+        rs.dmask = rc_p.dmask;
+        rs.tile_counts = rc_p.tile_counts;
+        rs.tile_hist = rc_p.tile_hist;
+        rs.send_slot = at<int32_t>(h, h->L.send_slot);
+        rs.dest_weight = at<float>(h, h->L.dest_weight);
+        rs.src_token = at<int32_t>(h, h->L.src_token);
+        rs.recv_ids = at<int32_t>(h, h->L.recv_ids);
+        rs.recv_w = at<float>(h, h->L.recv_w);
+        rs.recv_counts = at<int32_t>(h, h->L.recv_counts);
+        rs.local_counts = at<int32_t>(h, h->L.local_counts);
+        rs.R = R, rs.T = T, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
+        rs.ntiles = ntiles;
+        if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+
+        moe::DispatchParams dp = h->dispatch_tmpl;
+        dp.x = static_cast<const uint8_t *>(d_x);
+        dp.send_slot = rs.send_slot;
+        dp.recv_x = at<uint8_t>(h, h->L.recv_x);
+        dp.flags = flags;
+        dp.R = R, dp.T = T, dp.RP = RP, dp.m = m;
+        dp.units = (long long)R * T * dp.chunks;
+        if (moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+
+    h->T = T;
+    h->m = m;
+    h->phase = 1;
+    if (out_view != nullptr) {
+        out_view->recv_x = h->ws + h->L.recv_x;
+        out_view->recv_topk_ids = at<int32_t>(h, h->L.recv_ids);
+        out_view->recv_topk_w = at<float>(h, h->L.recv_w);
+        out_view->src_token = at<int32_t>(h, h->L.src_token);
+        out_view->recv_counts = at<int32_t>(h, h->L.recv_counts);
+        out_view->local_expert_counts = at<int32_t>(h, h->L.local_counts);
+        out_view->send_slot = at<int32_t>(h, h->L.send_slot);
+        out_view->dest_weight = at<float>(h, h->L.dest_weight);
+        out_view->plane_stride = m;
+        out_view->tokens_per_rank = T;
+        out_view->send_stride = RP;
+        out_view->reserved = 0;
+    }
+    return MOE_OK;
+}
+
+void *moe_combine_payload(moe_a2a_t *h) {
+    return h == nullptr ? nullptr : h->ws + h->L.expert_out;
+}
+
+int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const void *d_residual,
+                const void *d_gamma, float eps, void *d_out, void *d_residual_out, void *stream) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 1) return MOE_ERR_PHASE;
+    const bool fused = d_residual != nullptr;
+    const void *eo = d_expert_out != nullptr ? d_expert_out : h->ws + h->L.expert_out;
+    if (h->T > 0) {
+        if (d_out == nullptr || !aligned(d_out, 16) || !aligned(eo, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (fused && (d_gamma == nullptr || !aligned(d_residual, 16) || !aligned(d_gamma, 16)))
+            return MOE_ERR_INVALID_ARG;
+        if (fused && d_residual_out != nullptr && !aligned(d_residual_out, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (!fused && d_residual_out != nullptr) return MOE_ERR_INVALID_ARG;
+        if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (h->T > 0) {
+        const int variant = (weighted ? 2 : 0) + (fused ? 1 : 0);
+        if (!h->combine_ready[variant]) {
+            if (moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
+                                     &h->combine_shape[variant],
+                                     &h->combine_vpt[variant]) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            h->combine_ready[variant] = true;
+        }
+        moe::CombineParams cp;
+        cp.expert_out = static_cast<const uint16_t *>(eo);
+        cp.send_slot = at<int32_t>(h, h->L.send_slot);
+        cp.dest_weight = at<float>(h, h->L.dest_weight);
+        cp.residual = static_cast<const uint16_t *>(d_residual);
+        cp.gamma = static_cast<const uint16_t *>(d_gamma);
+        cp.out = static_cast<uint16_t *>(d_out);
+        cp.residual_out = static_cast<uint16_t *>(d_residual_out);
+        cp.eps = eps;
+        cp.flags = at<uint32_t>(h, h->L.flags);
+        cp.R = h->cfg.ep_size, cp.T = h->T, cp.RP = h->L.RP, cp.m = h->m;
+        cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
+        cp.tokens = (long long)h->cfg.ep_size * h->T;
+        if (moe::launch_combine(cp, weighted != 0, fused, h->combine_vpt[variant],
+                                h->combine_shape[variant], st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    h->phase = 0;
+    return MOE_OK;
+}
+
+int moe_a2a_get_error(moe_a2a_t *h, void *stream, uint32_t *flags) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (flags != nullptr) *flags = 0;
+    if (!h->ready) return MOE_OK;  // nothing was ever queued
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    if (cudaMemcpyAsync(&bits, h->ws + h->L.flags, sizeof bits, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (bits != 0 &&
+        (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof bits, st) != cudaSuccess ||
+         cudaStreamSynchronize(st) != cudaSuccess))
+        return MOE_ERR_CUDA;
+    if (flags != nullptr) *flags = bits;
+    if (bits & MOE_DEVICE_FLAG_WAIT_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+    if (bits & MOE_DEVICE_FLAG_BAD_SLOT) return MOE_ERR_INTERNAL;
+    if (bits & MOE_DEVICE_FLAG_BAD_EXPERT_ID) return MOE_ERR_ROUTING;
+    return MOE_OK;
+}
+
+int moe_a2a_destroy(moe_a2a_t *h) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    delete h;
+    return MOE_OK;
+}
+
+int moe_a2a_phase(const moe_a2a_t *h) { return h == nullptr ? -1 : h->phase; }
+
+const char *moe_a2a_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_PHASE: return "phase error (dispatch twice, or combine without dispatch)";
+        case MOE_ERR_CAPACITY: return "capacity exceeded (runtime max or tokens per rank)";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_ROUTING: return "expert id outside [-1, num_experts) seen on device";
+        case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+        case MOE_ERR_INTERNAL: return "internal consistency guard fired on device";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

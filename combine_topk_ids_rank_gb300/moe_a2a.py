@@ -1,0 +1,280 @@
+"""Thin ctypes binding of the C ABI in include/moe_a2a.h (libmoe_a2a.so).
+
+The module-level functions carry the C names and take raw device pointers
+(ints) and sizes; they return the C status codes.  `MoeA2A` wraps them for
+torch tensors: it allocates the workspace with torch, checks dtypes, shapes
+and devices, passes data pointers and the current CUDA stream, and raises
+`MoeA2AError` on any status other than MOE_OK.  Every step of the path runs
+in the library's CUDA kernels; there is no fallback: if the library is
+missing, importing this module fails.
+"""
+import ctypes
+import os
+
+LIBRARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_a2a.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_PHASE = 2
+MOE_ERR_CAPACITY = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_ROUTING = 5
+MOE_ERR_DEVICE_TIMEOUT = 6
+MOE_ERR_INTERNAL = 7
+MOE_DEVICE_FLAG_BAD_EXPERT_ID = 0x1
+MOE_DEVICE_FLAG_WAIT_TIMEOUT = 0x2
+MOE_DEVICE_FLAG_BAD_SLOT = 0x4
+
+EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
+           "moe_combine_payload", "moe_combine", "moe_a2a_get_error",
+           "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string")
+
+
+class MoeA2AConfig(ctypes.Structure):
+    _fields_ = [("ep_size", ctypes.c_int32), ("max_tokens_per_rank", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32)]
+
+
+class MoeDispatchView(ctypes.Structure):
+    _fields_ = [("recv_x", ctypes.c_void_p), ("recv_topk_ids", ctypes.c_void_p),
+                ("recv_topk_w", ctypes.c_void_p), ("src_token", ctypes.c_void_p),
+                ("recv_counts", ctypes.c_void_p), ("local_expert_counts", ctypes.c_void_p),
+                ("send_slot", ctypes.c_void_p), ("dest_weight", ctypes.c_void_p),
+                ("plane_stride", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
+                ("send_stride", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class MoeA2AError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (where, status_string(status), status))
+
+
+def _load(path: str = LIBRARY):
+    if not os.path.exists(path):
+        raise ImportError("libmoe_a2a.so is not built (%s); run __graft_entry__.build()" % path)
+    # torch first, so that the CUDA runtime it loaded is the one the library binds to
+    try:
+        import torch  # noqa: F401
+    except ImportError:
+        pass
+    lib = ctypes.CDLL(path)
+    p, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    cfgp = ctypes.POINTER(MoeA2AConfig)
+    lib.moe_a2a_workspace_bytes.argtypes = [cfgp]
+    lib.moe_a2a_workspace_bytes.restype = sz
+    lib.moe_a2a_create.argtypes = [cfgp, p, sz, ctypes.POINTER(p)]
+    lib.moe_a2a_create.restype = ctypes.c_int
+    lib.moe_dispatch.argtypes = [p, p, p, p, i32, i32, p, ctypes.POINTER(MoeDispatchView)]
+    lib.moe_dispatch.restype = ctypes.c_int
+    lib.moe_combine_payload.argtypes = [p]
+    lib.moe_combine_payload.restype = p
+    lib.moe_combine.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p, p]
+    lib.moe_combine.restype = ctypes.c_int
+    lib.moe_a2a_get_error.argtypes = [p, p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.moe_a2a_get_error.restype = ctypes.c_int
+    lib.moe_a2a_destroy.argtypes = [p]
+    lib.moe_a2a_destroy.restype = ctypes.c_int
+    lib.moe_a2a_phase.argtypes = [p]
+    lib.moe_a2a_phase.restype = ctypes.c_int
+    lib.moe_a2a_status_string.argtypes = [ctypes.c_int]
+    lib.moe_a2a_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+# ---- the C ABI, one function per entry point ---------------------------------
+
+def config(ep_size, max_tokens_per_rank, hidden, num_experts, top_k) -> MoeA2AConfig:
+    return MoeA2AConfig(ep_size, max_tokens_per_rank, hidden, num_experts, top_k)
+
+
+def moe_a2a_workspace_bytes(cfg: MoeA2AConfig) -> int:
+    return int(_lib.moe_a2a_workspace_bytes(ctypes.byref(cfg)))
+
+
+def moe_a2a_create(cfg: MoeA2AConfig, d_workspace: int, workspace_bytes: int):
+    """Returns (status, handle)."""
+    h = ctypes.c_void_p()
+    st = _lib.moe_a2a_create(ctypes.byref(cfg), ctypes.c_void_p(d_workspace),
+                             workspace_bytes, ctypes.byref(h))
+    return st, h
+
+
+def moe_dispatch(h, d_topk_ids: int, d_topk_w: int, d_x: int, tokens_per_rank: int,
+                 runtime_max_tokens_per_rank: int, stream: int = 0):
+    """Returns (status, MoeDispatchView)."""
+    view = MoeDispatchView()
+    st = _lib.moe_dispatch(h, ctypes.c_void_p(d_topk_ids), ctypes.c_void_p(d_topk_w),
+                           ctypes.c_void_p(d_x), tokens_per_rank, runtime_max_tokens_per_rank,
+                           ctypes.c_void_p(stream), ctypes.byref(view))
+    return st, view
+
+
+def moe_combine_payload(h) -> int:
+    return _lib.moe_combine_payload(h) or 0
+
+
+def moe_combine(h, d_expert_out: int, weighted: bool, d_residual: int, d_gamma: int, eps: float,
+                d_out: int, d_residual_out: int, stream: int = 0) -> int:
+    return _lib.moe_combine(h, ctypes.c_void_p(d_expert_out), int(bool(weighted)),
+                            ctypes.c_void_p(d_residual), ctypes.c_void_p(d_gamma),
+                            float(eps), ctypes.c_void_p(d_out), ctypes.c_void_p(d_residual_out),
+                            ctypes.c_void_p(stream))
+
+
+def moe_a2a_get_error(h, stream: int = 0):
+    """Returns (status, device flag bits)."""
+    flags = ctypes.c_uint32(0)
+    st = _lib.moe_a2a_get_error(h, ctypes.c_void_p(stream), ctypes.byref(flags))
+    return st, int(flags.value)
+
+
+def moe_a2a_destroy(h) -> int:
+    return _lib.moe_a2a_destroy(h)
+
+
+def moe_a2a_phase(h) -> int:
+    return _lib.moe_a2a_phase(h)
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_a2a_status_string(status).decode()
+
+
+# ---- torch convenience wrapper ------------------------------------------------
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+class DispatchView:
+    """torch views into the workspace produced by one dispatch."""
+
+    def __init__(self, owner, raw: MoeDispatchView):
+        import torch
+        R, K, E = owner.ep_size, owner.top_k, owner.num_experts
+        H, m, T, RP = owner.hidden, raw.plane_stride, raw.tokens_per_rank, raw.send_stride
+
+        def region(ptr, dtype, shape):
+            n = 1
+            for s in shape:
+                n *= s
+            off = ptr - owner.workspace.data_ptr()
+            nbytes = n * torch.empty((), dtype=dtype).element_size()
+            return owner.workspace[off:off + nbytes].view(dtype).view(shape)
+
+        self.plane_stride, self.tokens_per_rank, self.send_stride = m, T, RP
+        self.recv_x = region(raw.recv_x, torch.bfloat16, (R, R, m, H))
+        self.recv_topk_ids = region(raw.recv_topk_ids, torch.int32, (R, R, m, K))
+        self.recv_topk_w = region(raw.recv_topk_w, torch.float32, (R, R, m, K))
+        self.src_token = region(raw.src_token, torch.int32, (R, R, m))
+        self.recv_counts = region(raw.recv_counts, torch.int32, (R, R))
+        self.local_expert_counts = region(raw.local_expert_counts, torch.int32, (R, E // R))
+        self.send_slot = region(raw.send_slot, torch.int32, (R, T, RP))
+        self.dest_weight = region(raw.dest_weight, torch.float32, (R, T, RP))
+
+
+class MoeA2A:
+    """One dispatch/combine handle over a torch-allocated device workspace."""
+
+    def __init__(self, ep_size: int, max_tokens_per_rank: int, hidden: int, num_experts: int,
+                 top_k: int, device=None):
+        import torch
+        self.ep_size, self.max_tokens_per_rank, self.hidden = ep_size, max_tokens_per_rank, hidden
+        self.num_experts, self.top_k = num_experts, top_k
+        self.cfg = config(ep_size, max_tokens_per_rank, hidden, num_experts, top_k)
+        nbytes = moe_a2a_workspace_bytes(self.cfg)
+        if nbytes == 0:
+            raise MoeA2AError(MOE_ERR_INVALID_ARG, "moe_a2a_workspace_bytes")
+        self.device = torch.device(device if device is not None else "cuda")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        st, self.handle = moe_a2a_create(self.cfg, self.workspace.data_ptr(), nbytes)
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_a2a_create")
+        self.last_view = None
+
+    def _stream(self, stream) -> int:
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+    def _check(self, t, dtype, shape, name):
+        if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+            raise ValueError("%s: expected %s %s, got %s %s" % (name, dtype, tuple(shape),
+                                                               t.dtype, tuple(t.shape)))
+        if not t.is_contiguous() or t.device != self.workspace.device:
+            raise ValueError("%s must be contiguous on %s" % (name, self.workspace.device))
+
+    @property
+    def phase(self) -> int:
+        return moe_a2a_phase(self.handle)
+
+    def dispatch(self, topk_ids, topk_w, x, runtime_max_tokens_per_rank: int = None,
+                 stream=None) -> DispatchView:
+        import torch
+        R, H, K = self.ep_size, self.hidden, self.top_k
+        T = topk_ids.shape[1]
+        m = T if runtime_max_tokens_per_rank is None else runtime_max_tokens_per_rank
+        self._check(topk_ids, torch.int32, (R, T, K), "topk_ids")
+        self._check(topk_w, torch.float32, (R, T, K), "topk_w")
+        self._check(x, torch.bfloat16, (R, T, H), "x")
+        st, raw = moe_dispatch(self.handle, _ptr(topk_ids), _ptr(topk_w), _ptr(x), T, m,
+                               self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_dispatch")
+        self.last_view = DispatchView(self, raw)
+        return self.last_view
+
+    def combine_payload(self):
+        """bf16 [R, R, m, H] view of the in-workspace combine payload region."""
+        import torch
+        if self.last_view is None:
+            raise RuntimeError("no dispatch yet")
+        R, H, m = self.ep_size, self.hidden, self.last_view.plane_stride
+        off = moe_combine_payload(self.handle) - self.workspace.data_ptr()
+        n = R * R * m * H * 2
+        return self.workspace[off:off + n].view(torch.bfloat16).view(R, R, m, H)
+
+    def combine(self, expert_out=None, weighted: bool = False, residual=None, gamma=None,
+                eps: float = 1e-6, out=None, residual_out=None, stream=None):
+        import torch
+        if self.last_view is None:
+            st = moe_combine(self.handle, 0, weighted, 0, 0, eps, 0, 0, self._stream(stream))
+            raise MoeA2AError(st if st != MOE_OK else MOE_ERR_PHASE, "moe_combine")
+        R, H = self.ep_size, self.hidden
+        T, m = self.last_view.tokens_per_rank, self.last_view.plane_stride
+        if expert_out is not None:
+            self._check(expert_out, torch.bfloat16, (R, R, m, H), "expert_out")
+        if residual is not None:
+            self._check(residual, torch.bfloat16, (R, T, H), "residual")
+            self._check(gamma, torch.bfloat16, (H,), "gamma")
+            if residual_out is not None:
+                self._check(residual_out, torch.bfloat16, (R, T, H), "residual_out")
+        if out is None:
+            out = torch.empty((R, T, H), dtype=torch.bfloat16, device=self.workspace.device)
+        self._check(out, torch.bfloat16, (R, T, H), "out")
+        st = moe_combine(self.handle, _ptr(expert_out), weighted, _ptr(residual), _ptr(gamma),
+                         eps, _ptr(out), _ptr(residual_out), self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_combine")
+        return out
+
+    def get_error(self, stream=None):
+        """Synchronise, read and clear the device flag word: (status, bits)."""
+        return moe_a2a_get_error(self.handle, self._stream(stream))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            moe_a2a_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

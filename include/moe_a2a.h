@@ -1,0 +1,208 @@
+/*
+ * moe_a2a.h -- C ABI of the GB300-native top-k expert-parallel dispatch /
+ * combine library (libmoe_a2a.so).
+ *
+ * The ep_size "ranks" are logical partitions of ONE GPU's memory: dispatch
+ * scatters token rows into a padded receive workspace laid out per
+ * destination rank, combine gathers each token's per-rank messages back and
+ * reduces them once.  There is no peer memory, no NVLink traffic and no
+ * collective.
+ *
+ * Sources of the operations (web pages, cited by title and section):
+ *   [IX] SemiAnalysisAI/InferenceX PR #2450, "CollectiveX: add FlashInfer
+ *        one-sided NVLink EP for the GB SKUs": "The adapter" table (phase
+ *        contract; receive padded [ep_size, runtime_max_tokens_per_rank,
+ *        hidden]; runtime_max_tokens_per_rank <= max_num_tokens, workspace
+ *        sized once), the on-metal probe comment (the MoeAlltoAll
+ *        __init__/dispatch/combine signatures), the bring-up run table
+ *        (routing metadata as payloads, non-local expert ids masked,
+ *        local_expert_counts), "Kernel arithmetic read from source"
+ *        (fp32 accumulation, round-to-nearest-even bf16 store), "Best
+ *        remaining lead" (recv counters are the authoritative per-source
+ *        counts), "Update -- the correctness failures are resolved"
+ *        (fp32 accumulator with a single narrowing; the combine payload can
+ *        be written straight into the workspace).
+ *   [VL] vllm-project/vllm PR #41382, "[Bugfix] Fix double reduce in
+ *        flashinfer_nvlink_two_sided and flashinfer_nvlink_one_sided
+ *        backends": the combine output is already reduced and is final.
+ *   [MG] magik.net, "Fusing the Allreduce: A Precision Investigation into
+ *        FlashInfer's Verify-Path Optimization", "The Message Itself": the
+ *        reduction is fused with residual add + RMSNorm in one kernel.
+ *
+ * Notation: R = ep_size, M = max_tokens_per_rank, m = runtime max of one
+ * call (T <= m <= M), T = tokens per source rank of one call, H = hidden,
+ * E = num_experts, K = top_k, Epr = E / R.  Expert e lives on rank e / Epr.
+ * bf16 tensors are IEEE bfloat16 bit patterns, row-major, dense.
+ *
+ * Ownership: the caller owns every device buffer, including the workspace.
+ * The handle owns host state only.  Views returned by moe_dispatch alias the
+ * workspace and stay valid until the next moe_dispatch on the handle.
+ *
+ * Errors: every entry point returns a moe_status code and never aborts.  A
+ * call that returns an error leaves the phase unchanged.  Host-side checks
+ * (sizes, pointers, alignment, phase) run before anything is queued.
+ * Expert ids outside [-1, E) are detected on the device: the entry is
+ * skipped and a sticky device flag is raised, which moe_a2a_get_error
+ * reads.  Expert id -1 (the invalid_token_expert_id sentinel) means "no
+ * expert" and is skipped silently.
+ *
+ * Streams: `stream` arguments are cudaStream_t values passed as void*
+ * (NULL = the legacy default stream).  All work of a call is queued on that
+ * stream; calls return without synchronising, except moe_a2a_get_error.
+ * A handle is bound to the CUDA device that is current at its first
+ * dispatch.
+ */
+#ifndef MOE_A2A_H
+#define MOE_A2A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad config, NULL/misaligned pointer, bad size */
+    MOE_ERR_PHASE = 2,         /* dispatch twice without combine, or combine
+                                  without a dispatch ([IX] "The adapter") */
+    MOE_ERR_CAPACITY = 3,      /* runtime_max > max_tokens_per_rank, or
+                                  tokens_per_rank > runtime_max */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_ROUTING = 5,       /* device flag: an expert id outside [-1, E) */
+    MOE_ERR_DEVICE_TIMEOUT = 6,/* device flag: a bounded on-chip wait ran out */
+    MOE_ERR_INTERNAL = 7       /* device flag: a consistency guard fired (a
+                                  routing slot outside its plane was skipped);
+                                  never expected, reported rather than faulting */
+};
+
+/* Bits of the sticky device flag word (see moe_a2a_get_error). */
+#define MOE_DEVICE_FLAG_BAD_EXPERT_ID 0x1u
+#define MOE_DEVICE_FLAG_WAIT_TIMEOUT 0x2u
+#define MOE_DEVICE_FLAG_BAD_SLOT 0x4u
+
+/* Limits checked by moe_a2a_create. */
+#define MOE_MAX_EP_SIZE 32
+#define MOE_MAX_TOP_K 32
+#define MOE_MAX_EXPERTS 8192
+#define MOE_MAX_HIDDEN 16384
+
+/* Sizes fixed for the life of a handle ([IX] MoeAlltoAll __init__:
+ * max_num_tokens, top_k, num_experts, hidden_size; the workspace is sized
+ * once from max_tokens_per_rank). */
+typedef struct moe_a2a_config {
+    int32_t ep_size;             /* R, 1..32 logical ranks */
+    int32_t max_tokens_per_rank; /* M >= 1 */
+    int32_t hidden;              /* H, multiple of 8, 8..16384 */
+    int32_t num_experts;         /* E, multiple of R, <= 8192 */
+    int32_t top_k;               /* K, 1..32 */
+} moe_a2a_config_t;
+
+typedef struct moe_a2a moe_a2a_t;
+
+/* Device pointers into the workspace, produced by moe_dispatch.  All arrays
+ * are dense with plane stride m = runtime max of the call ([IX] "The
+ * adapter": padded, not compact).  Slots j >= recv_counts[d][s] of a plane
+ * are padding: never written by dispatch and never read by combine. */
+typedef struct moe_dispatch_view {
+    void *recv_x;                 /* bf16  [R dst][R src][m][H] */
+    int32_t *recv_topk_ids;       /* int32 [R][R][m][K]: expert id if it lives
+                                     on dst, else -1 (non-local masking) */
+    float *recv_topk_w;           /* fp32  [R][R][m][K]: weight if local, else 0 */
+    int32_t *src_token;           /* int32 [R][R][m]: source token of slot j */
+    int32_t *recv_counts;         /* int32 [R dst][R src] */
+    int32_t *local_expert_counts; /* int32 [R][Epr]: valid (token, k) entries
+                                     per local expert, over all sources */
+    int32_t *send_slot;           /* int32 [R src][T][send_stride]: slot of
+                                     token (s,t) in plane (d,s), -1 if not sent */
+    float *dest_weight;           /* fp32 [R src][T][send_stride]: sum, in
+                                     ascending k, of the token's top-k weights
+                                     whose expert lives on d (0 if not sent) */
+    int32_t plane_stride;         /* m */
+    int32_t tokens_per_rank;      /* T */
+    int32_t send_stride;          /* R rounded up to a multiple of 4 */
+    int32_t reserved;
+} moe_dispatch_view_t;
+
+/* Bytes of device workspace a handle with this config needs (0 if the
+ * config is invalid).  Sized once for max_tokens_per_rank ([IX] "The
+ * adapter": workspace sized once from the ladder maximum). */
+size_t moe_a2a_workspace_bytes(const moe_a2a_config_t *cfg);
+
+/* Create a handle over a caller-owned device workspace of at least
+ * moe_a2a_workspace_bytes(cfg) bytes, 256-byte aligned.  Host-only: queues
+ * nothing and needs no GPU.  On success *out receives the handle in the
+ * IDLE phase. */
+int moe_a2a_create(const moe_a2a_config_t *cfg, void *d_workspace,
+                   size_t workspace_bytes, moe_a2a_t **out);
+
+/* Dispatch ([IX] dispatch(token_selected_experts, input_payloads,
+ * runtime_max_tokens_per_rank, invalid_token_expert_id)).
+ *   d_topk_ids  int32 [R][T][K], 4-byte aligned; -1 = no expert
+ *   d_topk_w    fp32  [R][T][K], 4-byte aligned
+ *   d_x         bf16  [R][T][H], 16-byte aligned
+ *   tokens_per_rank T (0 <= T <= runtime_max), runtime_max m (1 <= m <= M).
+ * Routes every token to each distinct rank owning one of its experts (one
+ * message per (token, rank)), assigns slots in ascending source-token order
+ * within each (destination, source) plane, copies x rows and the masked
+ * top-k metadata into the planes, and counts rows per plane and per local
+ * expert.  Queues three kernels on `stream`.  IDLE -> DISPATCHED; returns
+ * MOE_ERR_PHASE if already DISPATCHED.  If out_view is not NULL it receives
+ * the views of this call. */
+int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
+                 const void *d_x, int32_t tokens_per_rank,
+                 int32_t runtime_max_tokens_per_rank, void *stream,
+                 moe_dispatch_view_t *out_view);
+
+/* Device pointer to the combine payload region of the workspace ([IX]
+ * get_combine_payload_tensor_in_workspace): bf16 [R][R][m][H] with the m of
+ * the current dispatch.  Experts may write their outputs here and pass
+ * NULL (or this pointer) as d_expert_out, so combine needs no staging copy.
+ * NULL if h is NULL. */
+void *moe_combine_payload(moe_a2a_t *h);
+
+/* Combine ([IX] combine(payload, runtime_max_tokens_per_rank,
+ * payload_in_workspace); [VL]; [MG]).  For each source token (s,t):
+ *   acc = sum over its destination ranks d, ascending d, of
+ *         v = expert_out[d][s][send_slot(s,t,d)][:]  (weighted = 0), or
+ *         dest_weight(s,t,d) * v                      (weighted != 0),
+ *   in fp32 starting from +0.0, one IEEE multiply and one add per term
+ *   (no FMA); each message is read exactly once and the result is final
+ *   (it must not be reduced again).
+ * Unfused (d_residual == NULL): d_out[s][t][:] = bf16_rn(acc).
+ * Fused: hsum = acc + residual (fp32); d_residual_out = bf16_rn(hsum) if
+ *   not NULL (it may be the same buffer as d_residual);
+ *   d_out = bf16_rn(hsum * rsqrt(mean(hsum^2) + eps) * gamma).
+ *   d_expert_out bf16 [R][R][m][H] (NULL = the in-workspace payload region;
+ *       the recv_x view is also accepted, i.e. identity experts)
+ *   d_residual, d_residual_out, d_out bf16 [R][T][H]; d_gamma bf16 [H]
+ *   All bf16 pointers 16-byte aligned.  d_out must not overlap any input.
+ * Queues one kernel on `stream`.  DISPATCHED -> IDLE; returns MOE_ERR_PHASE
+ * if no dispatch is pending. */
+int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted,
+                const void *d_residual, const void *d_gamma, float eps,
+                void *d_out, void *d_residual_out, void *stream);
+
+/* Synchronise `stream`, read and clear the sticky device flag word.
+ * Returns MOE_OK if no flag was set, MOE_ERR_ROUTING if an expert id outside
+ * [-1, E) was seen, MOE_ERR_DEVICE_TIMEOUT if a bounded wait ran out (the
+ * kernel then stopped early and its outputs are incomplete), or
+ * MOE_ERR_CUDA.  If flags is not NULL it receives the raw bits. */
+int moe_a2a_get_error(moe_a2a_t *h, void *stream, uint32_t *flags);
+
+/* Free the handle (host memory only; the workspace stays the caller's). */
+int moe_a2a_destroy(moe_a2a_t *h);
+
+/* Phase of the handle: 0 = IDLE, 1 = DISPATCHED, -1 if h is NULL. */
+int moe_a2a_phase(const moe_a2a_t *h);
+
+/* Static text for a status code. */
+const char *moe_a2a_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_A2A_H */

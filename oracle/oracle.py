@@ -121,13 +121,14 @@ def dispatch(topk_ids, topk_w, x, num_experts: int, m: int, routing,
 
 
 def combine(routing, expert_out, weighted: bool, residual=None, gamma=None,
-            eps: float = 1e-6, tokens=None, handle=None):
+            eps: float = 1e-6, tokens=None, handle=None, outputs=None):
     """Reduce each token's per-rank messages once; optional fused epilogue.
 
     expert_out: uint16 [R, R, m, H] (only valid slots are read).
     residual: uint16 [R, T, H] or None; gamma: uint16 [H] (fused only).
     tokens: optional flat token indices s*T+t; outputs are [ntok, H].
     Returns dict(acc=float32, out=uint16, residual_out=uint16|None, y=float64).
+    `outputs` may hold preallocated arrays of those names and shapes.
     """
     h = handle or lib()
     dmask = _need(routing["dmask"], np.uint32)
@@ -145,10 +146,21 @@ def combine(routing, expert_out, weighted: bool, residual=None, gamma=None,
     if residual is not None:
         res = _need(residual, np.uint16, (R, T, H))
         gam = _need(gamma, np.uint16, (H,))
-    acc = np.empty((n, H), np.float32)
-    out = np.empty((n, H), np.uint16)
-    rout = np.empty((n, H), np.uint16) if res is not None else None
-    y = np.empty((n, H), np.float64)
+    o = outputs or {}
+    acc = o.get("acc")
+    acc = np.empty((n, H), np.float32) if acc is None else acc
+    out = o.get("out")
+    out = np.empty((n, H), np.uint16) if out is None else out
+    rout = None
+    if res is not None:
+        rout = o.get("residual_out")
+        rout = np.empty((n, H), np.uint16) if rout is None else rout
+    y = o.get("y")
+    y = np.empty((n, H), np.float64) if y is None else y
+    for name, a, dt in (("acc", acc, np.float32), ("out", out, np.uint16),
+                        ("y", y, np.float64), ("residual_out", rout, np.uint16)):
+        if a is not None and (a.shape != (n, H) or a.dtype != dt or not a.flags.c_contiguous):
+            raise ValueError("output %s must be a contiguous %s [%d, %d]" % (name, dt, n, H))
     h.oracle_combine(R, T, H, m, int(bool(weighted)), _ptr(dmask),
                      _ptr(_need(routing["send_slot"], np.int32)),
                      _ptr(_need(routing["wd"], np.float32)), _ptr(eo),

@@ -1,0 +1,171 @@
+"""Run one workload through the CUDA library and through the oracle, and
+compare: routing, counts, slot maps, dispatched rows and metadata bit for
+bit; the combine sum / residual_out bit for bit; the fused RMSNorm output
+within |err| <= 2e-2 and |err| <= 1e-2 |ref| (and the pages' own gate,
+max_rel <= 8 * 2^-8 with a 0.02 denominator floor, as a looser check).
+
+Inputs come from combine_topk_ids_rank_gb300.synth on the host; the oracle
+never sees a value produced by the GPU.
+"""
+import numpy as np
+
+from combine_topk_ids_rank_gb300 import synth
+from oracle import oracle
+
+ABS_TOL = 2e-2
+REL_TOL = 1e-2
+PAGES_GATE = 8 * 2.0 ** -8      # max_rel gate of the pages, 0.02 denominator floor
+POISON = 0xFF                   # bf16 0xFFFF is NaN: unwritten padding shows up
+
+
+def f32(b):
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def to_dev(a, torch_dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if torch_dtype == torch.bfloat16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.to("cuda")
+
+
+def to_host_u16(t):
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def sample_tokens(routing, n_max, seed=0):
+    """All tokens when few; else a seeded sample plus the edge tokens: the
+    first and last token of every source, tokens with the most and the
+    fewest destinations."""
+    R, T = routing["dmask"].shape
+    N = R * T
+    if N <= n_max:
+        return np.arange(N, dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    pop = np.array([bin(int(v)).count("1") for v in routing["dmask"].ravel()])
+    pick = set(rng.choice(N, n_max, replace=False).tolist())
+    for s in range(R):
+        pick.update([s * T, s * T + T - 1])
+    pick.update(np.flatnonzero(pop == pop.max())[:16].tolist())
+    pick.update(np.flatnonzero(pop == pop.min())[:16].tolist())
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+class Case:
+    """One handle, reused across calls (the workspace is sized once)."""
+
+    def __init__(self, w: synth.Workload, poison: bool = True):
+        import torch
+        from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+        self.w = w
+        self.a2a = MoeA2A(w.ep_size, w.max_tokens, w.hidden, w.num_experts, w.top_k, "cuda")
+        if poison:
+            self.a2a.workspace.fill_(POISON)
+        torch.cuda.synchronize()
+
+    def run(self, T=None, seed=0, sample=4096, inputs=None, big_eo=None, check_rows=True):
+        """Dispatch + combine T tokens per rank; returns a report dict.
+
+        `inputs` / `big_eo` let ladder rungs reuse the host inputs of the
+        largest rung (rungs are prefixes of each other)."""
+        import torch
+        w = self.w if T is None else self.w.rung(T)
+        R, T, m, H, E, K = (w.ep_size, w.tokens_per_rank, w.runtime_max, w.hidden,
+                            w.num_experts, w.top_k)
+        inp = inputs if inputs is not None else synth.inputs(w, seed)
+        ids = np.ascontiguousarray(inp["topk_ids"][:, :T])
+        wts = np.ascontiguousarray(inp["topk_w"][:, :T])
+        x = np.ascontiguousarray(inp["x"][:, :T])
+
+        # ---- oracle routing (host) ----
+        r = oracle.route(ids, wts, E, m)
+        rep = dict(workload=w.name, T=T, recv_rows=int(r["recv_counts"].sum()))
+
+        # ---- GPU dispatch ----
+        a = self.a2a
+        view = a.dispatch(to_dev(ids, torch.int32), to_dev(wts, torch.float32),
+                          to_dev(x, torch.bfloat16), m)
+        torch.cuda.synchronize()
+        st, flags = a.get_error()
+        assert st == 0 and flags == 0, (st, flags)
+
+        counts = view.recv_counts.cpu().numpy()
+        assert np.array_equal(counts, r["recv_counts"]), "recv_counts"
+        assert np.array_equal(view.local_expert_counts.cpu().numpy(),
+                              r["local_expert_counts"]), "local_expert_counts"
+        ss = view.send_slot.cpu().numpy()[:, :, :R]
+        assert np.array_equal(ss, r["send_slot"]), "send_slot"
+        dw = view.dest_weight.cpu().numpy()[:, :, :R]
+        assert np.array_equal(dw.view(np.uint32), r["wd"].view(np.uint32)), "dest_weight"
+        src = view.src_token.cpu().numpy()
+        rid = view.recv_topk_ids.cpu().numpy()
+        rw = view.recv_topk_w.cpu().numpy()
+
+        od = oracle.dispatch(ids, wts, x, E, m, r)
+        gx = to_host_u16(view.recv_x) if check_rows else None
+        for d in range(R):
+            for s in range(R):
+                c = counts[d, s]
+                assert np.array_equal(src[d, s, :c], r["src_token"][d, s, :c]), "src_token"
+                assert np.array_equal(rid[d, s, :c], od["recv_ids"][d, s, :c]), "recv_topk_ids"
+                assert np.array_equal(rw[d, s, :c].view(np.uint32),
+                                      od["recv_w"][d, s, :c].view(np.uint32)), "recv_topk_w"
+                if check_rows:
+                    assert np.array_equal(gx[d, s, :c], od["recv_x"][d, s, :c]), \
+                        "recv_x plane (%d,%d)" % (d, s)
+        del gx
+
+        # ---- expert outputs ----
+        if w.identity_experts:
+            eo_dev = view.recv_x
+            eo_host = od["recv_x"]
+        else:
+            if big_eo is None:
+                eo_host = synth.expert_out_planes(seed, R, m, H, counts)
+            else:
+                eo_host = big_eo          # [R, R, M, H] with at least these rows drawn
+            payload = a.combine_payload()
+            for d in range(R):
+                for s in range(R):
+                    c = int(counts[d, s])
+                    if c:
+                        payload[d, s, :c].copy_(to_dev(eo_host[d, s, :c], torch.bfloat16))
+            eo_dev = None                 # in-workspace payload (zero-copy form)
+
+        # ---- GPU combine ----
+        out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+        if w.fused:
+            res = to_dev(np.ascontiguousarray(inp["residual"][:, :T]), torch.bfloat16)
+            gam = to_dev(inp["gamma"], torch.bfloat16)
+            rout = torch.empty_like(res)
+            a.combine(eo_dev, w.weighted, res, gam, w.eps, out, rout)
+        else:
+            rout = None
+            a.combine(eo_dev, w.weighted, out=out)
+        torch.cuda.synchronize()
+        assert a.phase == 0
+
+        # ---- oracle combine on (a sample of) tokens ----
+        tok = sample_tokens(r, sample, seed)
+        rep["tokens_checked"] = int(tok.size)
+        oc = oracle.combine(r, eo_host, w.weighted,
+                            inp["residual"][:, :T] if w.fused else None,
+                            inp["gamma"] if w.fused else None, w.eps, tokens=tok)
+        g_out = to_host_u16(out).reshape(R * T, H)[tok]
+        if not w.fused:
+            assert np.array_equal(g_out, oc["out"]), "combine sum (bit-exact)"
+            rep["max_abs_err"] = 0.0
+        else:
+            g_rout = to_host_u16(rout).reshape(R * T, H)[tok]
+            assert np.array_equal(g_rout, oc["residual_out"]), "residual_out (bit-exact)"
+            y = f32(g_out).astype(np.float64)
+            err = np.abs(y - oc["y"])
+            rep["max_abs_err"] = float(err.max())
+            rep["max_rel_floor"] = float((err / np.maximum(np.abs(oc["y"]), 0.02)).max())
+            bad = (err > ABS_TOL) | (err > REL_TOL * np.abs(oc["y"]))
+            assert not bad.any(), "RMSNorm tolerance: %d elements, max abs %g" % (
+                bad.sum(), err.max())
+            assert rep["max_rel_floor"] <= PAGES_GATE
+        return rep

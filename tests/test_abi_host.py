@@ -1,0 +1,131 @@
+"""C-ABI contract checks that need no GPU.
+
+The library must load, export every entry point include/moe_a2a.h declares,
+and enforce the phase contract and the size/pointer checks on the host
+before anything is queued (InferenceX PR #2450, "CollectiveX: add FlashInfer
+one-sided NVLink EP for the GB SKUs", "The adapter" table).
+"""
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_a2a.h")
+
+
+@pytest.fixture(scope="module")
+def abi():
+    from combine_topk_ids_rank_gb300 import build_lib
+    build_lib.build()
+    from combine_topk_ids_rank_gb300 import moe_a2a
+    return moe_a2a
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def declared_enum():
+    text = open(HEADER).read()
+    return {k: int(v) for k, v in re.findall(r"\b(MOE_\w+)\s*=\s*(\d+)", text)}
+
+
+def test_exports_every_declared_symbol(abi):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(abi._lib, n), n
+    assert set(names) == set(abi.EXPORTS)
+
+
+def test_status_codes_match_header(abi):
+    enum = declared_enum()
+    for k, v in enum.items():
+        assert getattr(abi, k) == v
+    for v in enum.values():
+        assert abi.status_string(v) not in ("", "unknown status")
+
+
+CFG = (8, 4096, 7168, 256, 8)
+
+
+def test_workspace_bytes_rejects_bad_configs(abi):
+    good = abi.moe_a2a_workspace_bytes(abi.config(*CFG))
+    # two bf16 payload regions dominate: 2 * R*R*M*H*2 bytes
+    assert good >= 2 * 8 * 8 * 4096 * 7168 * 2
+    assert good < 2 * 8 * 8 * 4096 * 7168 * 2 * 1.05
+    bad = [(0, 4096, 7168, 256, 8), (33, 64, 128, 33 * 2, 2), (8, 0, 7168, 256, 8),
+           (8, 64, 7170, 256, 8), (8, 64, 32768, 256, 8), (8, 64, 128, 250, 8),
+           (8, 64, 128, 256, 0), (8, 64, 128, 256, 33), (8, 64, 128, 16384, 2)]
+    for c in bad:
+        assert abi.moe_a2a_workspace_bytes(abi.config(*c)) == 0, c
+
+
+def test_workspace_sized_once_grows_with_max_tokens(abi):
+    a = abi.moe_a2a_workspace_bytes(abi.config(8, 64, 7168, 256, 8))
+    b = abi.moe_a2a_workspace_bytes(abi.config(8, 8192, 7168, 256, 8))
+    assert b > 100 * a
+
+
+def _handle(abi, cfg=CFG, nbytes=None):
+    c = abi.config(*cfg)
+    need = abi.moe_a2a_workspace_bytes(c)
+    st, h = abi.moe_a2a_create(c, 1 << 30, need if nbytes is None else nbytes)
+    return st, h
+
+
+def test_create_checks(abi):
+    c = abi.config(*CFG)
+    need = abi.moe_a2a_workspace_bytes(c)
+    assert abi.moe_a2a_create(c, 0, need)[0] == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_create(c, (1 << 30) + 16, need)[0] == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_create(c, 1 << 30, need - 1)[0] == abi.MOE_ERR_CAPACITY
+    assert abi.moe_a2a_create(abi.config(0, 1, 8, 1, 1), 1 << 30, need)[0] == \
+        abi.MOE_ERR_INVALID_ARG
+    st, h = _handle(abi)
+    assert st == abi.MOE_OK and abi.moe_a2a_phase(h) == 0
+    assert abi.moe_combine_payload(h) >= (1 << 30)
+    assert abi.moe_a2a_destroy(h) == abi.MOE_OK
+
+
+def test_combine_without_dispatch_is_a_phase_error(abi):
+    st, h = _handle(abi)
+    assert abi.moe_combine(h, 0, 1, 0, 0, 1e-6, 1 << 20, 0, 0) == abi.MOE_ERR_PHASE
+    assert abi.moe_a2a_phase(h) == 0
+    abi.moe_a2a_destroy(h)
+
+
+def test_dispatch_capacity_and_argument_checks(abi):
+    st, h = _handle(abi)
+    A = 1 << 20                       # an aligned stand-in pointer (never touched)
+    d = lambda ids, w, x, T, m: abi.moe_dispatch(h, ids, w, x, T, m, 0)[0]
+    assert d(A, A, A, 10, 4097) == abi.MOE_ERR_CAPACITY          # runtime max > max
+    assert d(A, A, A, 17, 16) == abi.MOE_ERR_CAPACITY            # T > runtime max
+    assert d(A, A, A, -1, 16) == abi.MOE_ERR_INVALID_ARG
+    assert d(A, A, A, 1, 0) == abi.MOE_ERR_INVALID_ARG
+    assert d(0, A, A, 4, 16) == abi.MOE_ERR_INVALID_ARG
+    assert d(A, 0, A, 4, 16) == abi.MOE_ERR_INVALID_ARG
+    assert d(A, A, 0, 4, 16) == abi.MOE_ERR_INVALID_ARG
+    assert d(A, A, A + 8, 4, 16) == abi.MOE_ERR_INVALID_ARG       # x not 16-byte aligned
+    assert d(A + 2, A, A, 4, 16) == abi.MOE_ERR_INVALID_ARG       # ids not 4-byte aligned
+    assert abi.moe_a2a_phase(h) == 0                              # errors leave the phase
+    abi.moe_a2a_destroy(h)
+
+
+def test_null_handle(abi):
+    assert abi.moe_a2a_destroy(None) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_phase(None) == -1
+    assert abi.moe_combine_payload(None) == 0
+    assert abi.moe_dispatch(None, 0, 0, 0, 0, 1, 0)[0] == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_combine(None, 0, 0, 0, 0, 0.0, 0, 0, 0) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_get_error(None)[0] == abi.MOE_ERR_INVALID_ARG
+
+
+def test_get_error_before_any_work(abi):
+    st, h = _handle(abi)
+    assert abi.moe_a2a_get_error(h) == (abi.MOE_OK, 0)
+    abi.moe_a2a_destroy(h)

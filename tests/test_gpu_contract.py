@@ -1,0 +1,180 @@
+"""Contract of the C ABI on the GPU: phase errors, the device flag for bad
+expert ids, empty input, tokens without experts, in-place residual, the
+zero-copy payload region, exactly-once reduction, no leakage between calls.
+"""
+import numpy as np
+import pytest
+
+from combine_topk_ids_rank_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import parity  # noqa: E402
+from oracle import oracle  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def mod():
+    from combine_topk_ids_rank_gb300 import build_lib
+    build_lib.build()
+    from combine_topk_ids_rank_gb300 import moe_a2a
+    return moe_a2a
+
+
+def dev(a, dt):
+    return parity.to_dev(a, dt)
+
+
+def make(mod, R=4, M=64, H=128, E=16, K=4):
+    return mod.MoeA2A(R, M, H, E, K, "cuda")
+
+
+def inputs(R=4, T=32, H=128, E=16, K=4, seed=0):
+    return dict(topk_ids=synth.topk_ids(seed, R, T, E, K),
+                topk_w=synth.topk_weights(seed, R, T, K),
+                x=synth.per_rank_rows(seed, synth.X, R, T, H),
+                residual=synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H),
+                gamma=synth.gamma(seed, H))
+
+
+def test_dispatch_twice_is_a_phase_error(mod):
+    a = make(mod)
+    i = inputs()
+    args = (dev(i["topk_ids"], torch.int32), dev(i["topk_w"], torch.float32),
+            dev(i["x"], torch.bfloat16))
+    a.dispatch(*args)
+    with pytest.raises(mod.MoeA2AError) as e:
+        a.dispatch(*args)
+    assert e.value.status == mod.MOE_ERR_PHASE and a.phase == 1
+    a.combine(a.last_view.recv_x)
+    assert a.phase == 0
+    with pytest.raises(mod.MoeA2AError) as e:
+        a.combine(a.last_view.recv_x)       # state reset after combine
+    assert e.value.status == mod.MOE_ERR_PHASE
+
+
+def test_capacity_errors_on_device_handle(mod):
+    a = make(mod, M=64)
+    i = inputs(T=32)
+    args = (dev(i["topk_ids"], torch.int32), dev(i["topk_w"], torch.float32),
+            dev(i["x"], torch.bfloat16))
+    for m in (16, 65):
+        with pytest.raises(mod.MoeA2AError) as e:
+            a.dispatch(*args, runtime_max_tokens_per_rank=m)
+        assert e.value.status == mod.MOE_ERR_CAPACITY
+    assert a.phase == 0
+
+
+def test_bad_expert_ids_raise_the_device_flag(mod):
+    a = make(mod)
+    i = inputs()
+    ids = i["topk_ids"].copy()
+    ids[0, 3, 1] = 16          # == E
+    ids[2, 7, 0] = -5
+    ids[1, 1, :] = -1          # the sentinel is fine
+    view = a.dispatch(dev(ids, torch.int32), dev(i["topk_w"], torch.float32),
+                      dev(i["x"], torch.bfloat16))
+    st, flags = a.get_error()
+    assert st == mod.MOE_ERR_ROUTING and flags == mod.MOE_DEVICE_FLAG_BAD_EXPERT_ID
+    assert a.get_error() == (mod.MOE_OK, 0)          # read clears it
+    r = oracle.route(ids, i["topk_w"], 16, 32)
+    assert r["invalid"] == 2
+    assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"])
+    assert np.array_equal(view.send_slot.cpu().numpy()[:, :, :4], r["send_slot"])
+    a.combine(view.recv_x)
+
+
+def test_empty_input(mod):
+    a = make(mod)
+    e = torch.empty((4, 0, 4), dtype=torch.int32, device="cuda")
+    view = a.dispatch(e, e.float(), torch.empty((4, 0, 128), dtype=torch.bfloat16,
+                                                device="cuda"), runtime_max_tokens_per_rank=8)
+    assert view.recv_counts.sum().item() == 0
+    assert view.local_expert_counts.sum().item() == 0
+    out = a.combine(None, True)
+    assert out.shape == (4, 0, 128) and a.phase == 0
+    assert a.get_error() == (mod.MOE_OK, 0)
+
+
+def test_tokens_without_experts(mod):
+    a = make(mod)
+    i = inputs()
+    ids = i["topk_ids"].copy()
+    ids[:, ::3, :] = -1
+    view = a.dispatch(dev(ids, torch.int32), dev(i["topk_w"], torch.float32),
+                      dev(i["x"], torch.bfloat16))
+    res = dev(i["residual"], torch.bfloat16)
+    gam = dev(i["gamma"], torch.bfloat16)
+    out = a.combine(view.recv_x, True, res, gam, 1e-6)
+    r = oracle.route(ids, i["topk_w"], 16, 32)
+    od = oracle.dispatch(ids, i["topk_w"], i["x"], 16, 32, r)
+    oc = oracle.combine(r, od["recv_x"], True, i["residual"], i["gamma"], 1e-6)
+    y = parity.f32(parity.to_host_u16(out)).reshape(-1, 128).astype(np.float64)
+    assert np.all(np.abs(y - oc["y"]) <= 2e-2)
+    # unfused: a token with no expert combines to exactly zero
+    view = a.dispatch(dev(ids, torch.int32), dev(i["topk_w"], torch.float32),
+                      dev(i["x"], torch.bfloat16))
+    out = a.combine(view.recv_x, False)
+    assert torch.count_nonzero(out[:, ::3].float()).item() == 0
+
+
+def test_in_place_residual_and_external_expert_out(mod):
+    R, T, H = 4, 32, 128
+    i = inputs()
+    outs = []
+    for mode in ("payload", "external", "inplace"):
+        a = make(mod)
+        view = a.dispatch(dev(i["topk_ids"], torch.int32), dev(i["topk_w"], torch.float32),
+                          dev(i["x"], torch.bfloat16))
+        counts = view.recv_counts.cpu().numpy()
+        eo = synth.expert_out_planes(9, R, T, H, counts)
+        eo_dev = torch.zeros((R, R, T, H), dtype=torch.bfloat16, device="cuda")
+        for d in range(R):
+            for s in range(R):
+                eo_dev[d, s, :counts[d, s]] = dev(eo[d, s, :counts[d, s]], torch.bfloat16)
+        res = dev(i["residual"], torch.bfloat16)
+        gam = dev(i["gamma"], torch.bfloat16)
+        if mode == "payload":
+            a.combine_payload().copy_(eo_dev)
+            rout = torch.empty_like(res)
+            y = a.combine(None, True, res, gam, 1e-6, residual_out=rout)
+        elif mode == "external":
+            rout = torch.empty_like(res)
+            y = a.combine(eo_dev, True, res, gam, 1e-6, residual_out=rout)
+        else:
+            y = a.combine(eo_dev, True, res, gam, 1e-6, residual_out=res)
+            rout = res
+        outs.append((parity.to_host_u16(y), parity.to_host_u16(rout)))
+    for y, rout in outs[1:]:
+        assert np.array_equal(y, outs[0][0]) and np.array_equal(rout, outs[0][1])
+
+
+def test_weighted_identity_reduces_exactly_once(mod):
+    # top-k weights 1/8 sum to exactly 1: the combine of identity experts is x
+    # itself, bit for bit (a second reduction would give 2x)
+    R, T, H, E, K = 8, 48, 7168, 256, 8
+    a = mod.MoeA2A(R, T, H, E, K, "cuda")
+    ids = synth.topk_ids(1, R, T, E, K)
+    w = np.full((R, T, K), 1.0 / K, np.float32)
+    x = synth.per_rank_rows(1, synth.X, R, T, H)
+    view = a.dispatch(dev(ids, torch.int32), dev(w, torch.float32), dev(x, torch.bfloat16))
+    out = a.combine(view.recv_x, True)
+    assert np.array_equal(parity.to_host_u16(out), x)
+
+
+def test_no_leakage_between_calls(mod):
+    # a large call followed by a small one on the same handle gives the same
+    # result as the small call on a fresh, poisoned handle
+    from dataclasses import replace
+    w = replace(synth.WORKLOADS["decode"], tokens_per_rank=64, max_tokens=64,
+                runtime_max=64, hidden=512)
+    shared = parity.Case(w)
+    shared.run(T=64, seed=1)
+    small = replace(w, tokens_per_rank=10, runtime_max=12)
+    shared.w = small
+    rep = shared.run(seed=2)
+    assert rep["T"] == 10
