@@ -44,6 +44,9 @@ def parse_args():
     ap.add_argument("--config", default="prefill",
                     choices=["tiny", "decode", "prefill", "wide", "ladder"])
     ap.add_argument("--tokens", type=int, default=None, help="tokens per rank (ladder rung)")
+    ap.add_argument("--workspace-tokens", type=int, default=None,
+                    help="size the workspace for this many tokens per rank (small profiling "
+                         "cases); default: the workload's max_tokens_per_rank")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -62,6 +65,9 @@ def workload(args):
     w = synth.WORKLOADS[args.config]
     if args.tokens is not None:
         w = w.rung(args.tokens)
+    if args.workspace_tokens is not None:
+        from dataclasses import replace
+        w = replace(w, max_tokens=max(args.workspace_tokens, w.runtime_max))
     return w
 
 
@@ -159,14 +165,18 @@ class OracleSample:
         self.eo = None
         if not ws.identity_experts:
             self.eo = synth.expert_out_planes(seed, R, T, H, r["recv_counts"])
-        self.recv = dict(recv_x=np.zeros((R, R, T, H), np.uint16),
-                         recv_ids=np.zeros((R, R, T, K), np.int32),
-                         recv_w=np.zeros((R, R, T, K), np.float32))
+        def touched(shape, dtype):
+            a = np.empty(shape, dtype)
+            a.fill(0)              # commit the pages outside the timed call
+            return a
+        self.recv = dict(recv_x=touched((R, R, T, H), np.uint16),
+                         recv_ids=touched((R, R, T, K), np.int32),
+                         recv_w=touched((R, R, T, K), np.float32))
         n = R * T
-        self.outs = dict(acc=np.zeros((n, H), np.float32), out=np.zeros((n, H), np.uint16),
-                         y=np.zeros((n, H), np.float64))
+        self.outs = dict(acc=touched((n, H), np.float32), out=touched((n, H), np.uint16),
+                         y=touched((n, H), np.float64))
         if ws.fused:
-            self.outs["residual_out"] = np.zeros((n, H), np.uint16)
+            self.outs["residual_out"] = touched((n, H), np.uint16)
 
     @property
     def tokens(self):
@@ -332,11 +342,8 @@ def run_gpu(args, w, rank, world, local_rank):
     comb_ms = [e[1].elapsed_time(e[2]) for e in ev]
     if flush is not None:       # time only the two phases, not the flush
         total_ms = sum(disp_ms) + sum(comb_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
+    total_ms, ms_per_step, tokens_per_s = aggregate_over_ranks(total_ms, N, args.steps, world,
+                                                               dev)
     st, flags = a2a.get_error()
     if st != 0:
         raise RuntimeError("device flag set during the timed region: %d %#x" % (st, flags))
@@ -360,7 +367,6 @@ def run_gpu(args, w, rank, world, local_rank):
                     "kernels": ["combine"]},
     }
     eff_gbs = (d_bytes + c_bytes) / ms_per_step / 1e6
-    tokens_per_s = N * world / (ms_per_step / 1e3)
 
     # ---- end to end through the public API, host buffers ----
     e2e = None
@@ -396,12 +402,9 @@ def run_gpu(args, w, rank, world, local_rank):
             e2e_step()
         e1.record()
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": N * world / (e2e_ms / args.e2e_steps / 1e3), "unit": "tokens/s",
+        e2e_ms, _, e2e_tps = aggregate_over_ranks(e0.elapsed_time(e1), N, args.e2e_steps,
+                                                  world, dev)
+        e2e = {"value": e2e_tps, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
                "path": "pinned host -> device copies, moe_dispatch, moe_combine, "
@@ -436,6 +439,22 @@ def run_gpu(args, w, rank, world, local_rank):
         "e2e": e2e,
     }
     return line
+
+
+def aggregate_over_ranks(local_ms: float, tokens_per_rank_batch: int, steps: int, world: int,
+                         device=None):
+    """Whole-job timing of weak-scaled replicas: the slowest rank's elapsed
+    time (all-reduce MAX) and the tokens all ranks processed per second.
+    Returns (max_ms, ms_per_step, tokens_per_s)."""
+    max_ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([max_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+    ms_per_step = max_ms / steps
+    return max_ms, ms_per_step, tokens_per_rank_batch * world / (ms_per_step / 1e3)
 
 
 def source_sha1(name):
