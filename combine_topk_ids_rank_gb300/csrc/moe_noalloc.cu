@@ -1,0 +1,151 @@
+// moe_noalloc.cu -- the routing pass with its scratch in a fixed device
+// array, for callers that cannot allocate device memory.
+//
+// Who needs this: code that runs inside a host framework which owns every
+// byte of device memory and hands out no allocator (a plugin or custom op
+// in an inference engine), and serving loops that forbid device allocation
+// after start-up because cudaMalloc can synchronise the whole device and
+// fragments a fixed memory budget.  Such callers can still pass their own
+// input and output buffers; what they cannot do is provide the routing
+// pass's temporary working memory.  Here that memory is a file-scope
+// __device__ array that the CUDA runtime creates when the library is loaded
+// on a device and keeps until the process exits.
+//
+// The entry point runs the same two routing kernels as moe_dispatch
+// (route_count, route_scan); only the source of their scratch differs.
+#include "moe_a2a.h"
+
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = MOE_STATIC_SCRATCH_BYTES;
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+// The scratch: per-token destination masks, per-tile destination counts,
+// per-tile expert histograms, and one word that absorbs device flags when
+// the caller passes no flag output.  Shared by every call on a device.
+static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
+
+std::mutex g_mutex;
+void *g_scratch_addr[kMaxDevices];
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Device address of g_route_scratch on the current device, looked up once
+// per device (host code cannot use the symbol itself as a device pointer).
+int scratch_address(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+            return MOE_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return MOE_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" size_t moe_route_static_scratch_bytes(int32_t ep_size, int32_t num_experts,
+                                                 int32_t tokens_per_rank) {
+    if (ep_size < 1 || num_experts < 1 || tokens_per_rank < 0) return 0;
+    const size_t R = ep_size, E = num_experts, T = tokens_per_rank;
+    const size_t RP = (R + 3) / 4 * 4;
+    const size_t tiles = (T + moe::kRouteTile - 1) / moe::kRouteTile;
+    return align_up(R * T * 4, kAlign) + align_up(R * tiles * RP * 4, kAlign) +
+           align_up(R * tiles * E * 4, kAlign) + kAlign;
+}
+
+extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, int32_t top_k,
+                                        int32_t tokens_per_rank,
+                                        int32_t runtime_max_tokens_per_rank,
+                                        const int32_t *d_topk_ids, const float *d_topk_w,
+                                        int32_t *d_send_slot, float *d_dest_weight,
+                                        int32_t *d_src_token, int32_t *d_recv_counts,
+                                        int32_t *d_local_expert_counts,
+                                        int32_t *d_recv_topk_ids, float *d_recv_topk_w,
+                                        uint32_t *d_flags, void *stream) {
+    const int R = ep_size, E = num_experts, K = top_k, T = tokens_per_rank;
+    const int m = runtime_max_tokens_per_rank;
+    if (R < 1 || R > MOE_MAX_EP_SIZE || E < R || E > MOE_MAX_EXPERTS || E % R != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (K < 1 || K > MOE_MAX_TOP_K || T < 0 || m < 1) return MOE_ERR_INVALID_ARG;
+    if (T > m) return MOE_ERR_CAPACITY;
+    if (moe_route_static_scratch_bytes(R, E, T) > kScratchBytes) return MOE_ERR_CAPACITY;
+    if (d_recv_counts == nullptr || d_local_expert_counts == nullptr) return MOE_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (d_topk_ids == nullptr || d_topk_w == nullptr || d_send_slot == nullptr ||
+            d_dest_weight == nullptr || d_src_token == nullptr || d_recv_topk_ids == nullptr ||
+            d_recv_topk_w == nullptr)
+            return MOE_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(d_topk_ids) & 3u) ||
+            (reinterpret_cast<uintptr_t>(d_topk_w) & 3u) || !aligned16(d_send_slot) ||
+            !aligned16(d_dest_weight) || !aligned16(d_src_token) ||
+            !aligned16(d_recv_topk_ids) || !aligned16(d_recv_topk_w))
+            return MOE_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (T == 0) {
+        if (cudaMemsetAsync(d_recv_counts, 0, sizeof(int32_t) * R * R, st) != cudaSuccess ||
+            cudaMemsetAsync(d_local_expert_counts, 0, sizeof(int32_t) * E, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+
+    void *base = nullptr;
+    const int rc = scratch_address(&base);
+    if (rc != MOE_OK) return rc;
+
+    // Carve the scratch.  Every word the kernels read from it is written
+    // earlier in the same call, so nothing has to start at zero.
+    const int RP = (R + 3) / 4 * 4;
+    const int ntiles = (T + moe::kRouteTile - 1) / moe::kRouteTile;
+    unsigned char *p = static_cast<unsigned char *>(base);
+    uint32_t *dmask = reinterpret_cast<uint32_t *>(p);
+    p += align_up((size_t)R * T * 4, kAlign);
+    int32_t *tile_counts = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)R * ntiles * RP * 4, kAlign);
+    int32_t *tile_hist = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)R * ntiles * E * 4, kAlign);
+    uint32_t *sink_flags = reinterpret_cast<uint32_t *>(p);
+
+    moe::RouteCountParams c;
+    c.topk_ids = d_topk_ids;
+    c.dmask = dmask;
+    c.tile_counts = tile_counts;
+    c.tile_hist = tile_hist;
+    c.flags = d_flags != nullptr ? d_flags : sink_flags;
+    c.R = R, c.T = T, c.K = K, c.E = E, c.Epr = E / R, c.RP = RP, c.ntiles = ntiles;
+    if (moe::launch_route_count(c, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    moe::RouteScanParams s;
+    s.topk_ids = d_topk_ids;
+    s.topk_w = d_topk_w;
+    s.dmask = dmask;
+    s.tile_counts = tile_counts;
+    s.tile_hist = tile_hist;
+    s.send_slot = d_send_slot;
+    s.dest_weight = d_dest_weight;
+    s.src_token = d_src_token;
+    s.recv_ids = d_recv_topk_ids;
+    s.recv_w = d_recv_topk_w;
+    s.recv_counts = d_recv_counts;
+    s.local_counts = d_local_expert_counts;
+    s.R = R, s.T = T, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
+    if (moe::launch_route_scan(s, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}

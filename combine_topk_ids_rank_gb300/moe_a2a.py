@@ -27,7 +27,9 @@ MOE_DEVICE_FLAG_BAD_SLOT = 0x4
 
 EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_combine_payload", "moe_combine", "moe_a2a_get_error",
-           "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string")
+           "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string",
+           "moe_route_static_scratch_bytes", "moe_route_static_scratch")
+MOE_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 class MoeA2AConfig(ctypes.Structure):
@@ -143,6 +145,32 @@ def moe_a2a_phase(h) -> int:
 
 def status_string(status: int) -> str:
     return _lib.moe_a2a_status_string(status).decode()
+
+
+def moe_route_static_scratch_bytes(ep_size: int, num_experts: int, tokens_per_rank: int) -> int:
+    f = _lib.moe_route_static_scratch_bytes
+    f.argtypes = [ctypes.c_int32] * 3
+    f.restype = ctypes.c_size_t
+    return int(f(ep_size, num_experts, tokens_per_rank))
+
+
+def moe_route_static_scratch(ep_size: int, num_experts: int, top_k: int, tokens_per_rank: int,
+                             runtime_max_tokens_per_rank: int, d_topk_ids: int, d_topk_w: int,
+                             d_send_slot: int, d_dest_weight: int, d_src_token: int,
+                             d_recv_counts: int, d_local_expert_counts: int,
+                             d_recv_topk_ids: int, d_recv_topk_w: int, d_flags: int = 0,
+                             stream: int = 0) -> int:
+    """The routing pass with no device allocation (see include/moe_a2a.h):
+    every buffer is the caller's, the temporary memory is the library's
+    fixed device array.  Returns the C status code."""
+    f = _lib.moe_route_static_scratch
+    f.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_void_p] * 11
+    f.restype = ctypes.c_int
+    v = ctypes.c_void_p
+    return f(ep_size, num_experts, top_k, tokens_per_rank, runtime_max_tokens_per_rank,
+             v(d_topk_ids), v(d_topk_w), v(d_send_slot), v(d_dest_weight), v(d_src_token),
+             v(d_recv_counts), v(d_local_expert_counts), v(d_recv_topk_ids), v(d_recv_topk_w),
+             v(d_flags), v(stream))
 
 
 # ---- torch convenience wrapper ------------------------------------------------

@@ -201,6 +201,57 @@ int moe_a2a_phase(const moe_a2a_t *h);
 /* Static text for a status code. */
 const char *moe_a2a_status_string(int status);
 
+/* ---- Routing without any device allocation --------------------------------
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory: a plugin or custom op running
+ * inside a framework that owns the whole device memory pool and exposes no
+ * allocator, or a serving loop that forbids cudaMalloc after start-up
+ * (cudaMalloc can synchronise the device and fragments a fixed budget).
+ *
+ * It runs the same routing pass as moe_dispatch (destination dedup,
+ * ascending-token slots, send table, per-destination weights, source map,
+ * masked metadata rows, recv counts, local-expert counts) into buffers the
+ * caller passes, and keeps the pass's temporary memory in a file-scope
+ * device array of MOE_STATIC_SCRATCH_BYTES.  The library allocates nothing
+ * (no cudaMalloc/cudaFree, no allocating library call); the array is created
+ * by the CUDA runtime on every device that loads the library and is held
+ * until the process exits.
+ *
+ * Set-up: the first call on a device (with that device current) looks up
+ * the array's device address once; make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents: calls whose work overlaps on the GPU (other streams, or
+ * other threads without ordering) race on it and must be serialised by the
+ * caller.  Every scratch word read is written earlier in the same call, so
+ * no clearing is needed.
+ *
+ * Limit: moe_route_static_scratch_bytes(R, E, T) must not exceed
+ * MOE_STATIC_SCRATCH_BYTES (R*T*4 + R*ceil(T/256)*(RP + E)*4 plus
+ * alignment; e.g. R=8, E=256: up to T = 64512) else MOE_ERR_CAPACITY.
+ * Outputs (layouts as in moe_dispatch_view_t, RP = R rounded up to 4, all
+ * 16-byte aligned): d_send_slot int32 [R][T][RP], d_dest_weight fp32
+ * [R][T][RP], d_src_token int32 [R][R][m], d_recv_counts int32 [R][R],
+ * d_local_expert_counts int32 [E], d_recv_topk_ids int32 [R][R][m][K],
+ * d_recv_topk_w fp32 [R][R][m][K]; only valid slots of the [R][R][m]
+ * arrays are written.  d_flags (optional, caller-zeroed uint32) receives
+ * MOE_DEVICE_FLAG_BAD_EXPERT_ID if an id outside [-1, E) is seen.
+ * Inputs: d_topk_ids int32 / d_topk_w fp32 [R][T][K], 4-byte aligned.
+ * Queues two kernels on `stream`; no handle, no phase. */
+#define MOE_STATIC_SCRATCH_BYTES (4u << 20)
+
+size_t moe_route_static_scratch_bytes(int32_t ep_size, int32_t num_experts,
+                                      int32_t tokens_per_rank);
+
+int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, int32_t top_k,
+                             int32_t tokens_per_rank,
+                             int32_t runtime_max_tokens_per_rank,
+                             const int32_t *d_topk_ids, const float *d_topk_w,
+                             int32_t *d_send_slot, float *d_dest_weight,
+                             int32_t *d_src_token, int32_t *d_recv_counts,
+                             int32_t *d_local_expert_counts,
+                             int32_t *d_recv_topk_ids, float *d_recv_topk_w,
+                             uint32_t *d_flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
