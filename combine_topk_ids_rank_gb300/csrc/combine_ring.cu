@@ -1,0 +1,476 @@
+// combine_ring.cu -- the combine with its row loads on the copy engine.
+//
+// Same operation as combine.cu (InferenceX PR #2450 "CollectiveX: add
+// FlashInfer one-sided NVLink EP for the GB SKUs", "Kernel arithmetic read
+// from source" and "Update -- the correctness failures are resolved":
+// fp32 accumulation, one round-to-nearest-even narrowing; vLLM PR #41382:
+// reduced exactly once; magik.net "Fusing the Allreduce ...", "The Message
+// Itself": residual add + RMSNorm fused):
+//   acc[h] = sum over d in dmask(s,t), ascending d, of v or w(s,t,d) * v
+//   unfused: out = bf16_rn(acc)
+//   fused:   hsum = acc + residual; residual_out = bf16_rn(hsum);
+//            out = bf16_rn(hsum * rsqrt(mean(hsum^2) + eps) * gamma)
+//
+// GB300 design: persistent CTAs (two or more per SM), warp-specialised.
+//   * The producer warp walks the CTA's tokens, reads each token's send
+//     row (slot per destination, prefetched one token ahead), publishes a
+//     token descriptor (row count and per-row weights, ascending rank) and
+//     streams the token's residual row and message rows into a ring of
+//     shared-memory row buffers with 1-D bulk asynchronous copies, each
+//     completing on the buffer's "full" mbarrier.
+//   * Consumer warps own 16-byte vectors of the row.  For every token they
+//     take the rows in ring order (residual first, then messages in
+//     ascending rank), accumulate in fp32 registers, release each buffer on
+//     its "empty" mbarrier, and finish the epilogue: the mean of squares
+//     is a warp shuffle reduction and a cross-warp pass through shared
+//     memory synchronised by an mbarrier; outputs are stored directly.
+// The ring is shallow (~48 KB, three rows at H=7168) so that several CTAs
+// share an SM: each has a token in its epilogue while the others' rows are
+// in flight, and the copy engine keeps the loads going independently of
+// registers.  Every wait
+// is bounded: on time-out the warp raises the timeout flag and stops, and
+// the producer waits (bounded) for its copies still landing before exit.
+#include "kernels.h"
+#include "ptx.cuh"
+
+#include "moe_a2a.h"
+
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kDesc = 8;                  // token descriptors in flight
+constexpr int kMaxRingSlots = 32;
+constexpr int kMaxConsumerWarps = 8;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr size_t kRingBytesTarget = 48 * 1024;
+
+struct TokenDesc {
+    int32_t n;       // message rows of the token
+    int32_t pad;
+    float w[32];     // per-row weight, ascending destination rank
+};
+
+struct Ring {
+    uint8_t *rows;
+    uint64_t *full, *empty, *dfull, *dempty, *rbar;
+    TokenDesc *desc;
+    float *red;      // [2][kMaxConsumerWarps]
+};
+
+__host__ __device__ inline size_t ring_stride(int row_bytes) {
+    return ((size_t)row_bytes + 127) / 128 * 128;
+}
+
+__host__ __device__ inline size_t ring_smem_bytes(int row_bytes, int slots) {
+    return ring_stride(row_bytes) * slots + sizeof(uint64_t) * (2 * slots + 2 * kDesc + 2) +
+           sizeof(TokenDesc) * kDesc + sizeof(float) * 2 * kMaxConsumerWarps;
+}
+
+__device__ inline Ring carve(uint8_t *smem, int row_bytes, int slots) {
+    Ring r;
+    r.rows = smem;
+    r.full = reinterpret_cast<uint64_t *>(smem + ring_stride(row_bytes) * slots);
+    r.empty = r.full + slots;
+    r.dfull = r.empty + slots;
+    r.dempty = r.dfull + kDesc;
+    r.rbar = r.dempty + kDesc;
+    r.desc = reinterpret_cast<TokenDesc *>(r.rbar + 2);
+    r.red = reinterpret_cast<float *>(r.desc + kDesc);
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                     ptx::smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
+    return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                      pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+}
+
+template <bool WEIGHTED>
+__device__ __forceinline__ void accumulate8(float (&a)[8], const uint4 v, const float w) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = lo_f(u[i]), hi = hi_f(u[i]);
+        if (WEIGHTED) {
+            a[2 * i] = __fadd_rn(a[2 * i], __fmul_rn(w, lo));
+            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __fmul_rn(w, hi));
+        } else {
+            a[2 * i] = __fadd_rn(a[2 * i], lo);
+            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], hi);
+        }
+    }
+}
+
+// ---- producer warp ----------------------------------------------------------
+
+template <bool WEIGHTED, bool FUSED>
+__device__ void produce(const CombineParams &p, const Ring &r, int slots) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *eo = reinterpret_cast<const uint8_t *>(p.expert_out);
+    const uint8_t *res = reinterpret_cast<const uint8_t *>(p.residual);
+    const uint32_t row_bytes = 2u * (uint32_t)p.H;
+    const size_t stride = ring_stride((int)row_bytes);
+    const uint32_t lt = lanemask_lt();
+
+    auto load_route = [&](long long tok, int &slot, float &w) {
+        slot = -1;
+        w = 0.0f;
+        if (tok < p.tokens && lane < p.R) {
+            slot = __ldg(p.send_slot + tok * p.RP + lane);
+            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.RP + lane);
+        }
+    };
+
+    uint32_t q = 0;  // rows issued
+    bool ok = true;
+    auto issue_row = [&](const uint8_t *src) -> bool {
+        const uint32_t b = q % slots;
+        if (!ptx::mbar_wait_bounded(&r.empty[b], ((q / slots) & 1u) ^ 1u, kWaitLimit))
+            return false;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&r.full[b], row_bytes);
+            ptx::bulk_g2s(r.rows + b * stride, src, row_bytes, &r.full[b]);
+        }
+        ++q;
+        return true;
+    };
+
+    int slot, slot_next;
+    float w, w_next;
+    long long tok = blockIdx.x;
+    load_route(tok, slot, w);
+    for (uint32_t j = 0; tok < p.tokens; tok += gridDim.x, ++j) {
+        load_route(tok + gridDim.x, slot_next, w_next);
+        const int s = (int)(tok / p.T);
+        bool valid = slot >= 0;
+        if (valid && slot >= p.m) {  // guard: never expected from the routing pass
+            atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+            valid = false;
+        }
+        const uint32_t bal = __ballot_sync(kFull, valid);
+
+        const int ds = j % kDesc;
+        if (!ptx::mbar_wait_bounded(&r.dempty[ds], ((j / kDesc) & 1u) ^ 1u, kWaitLimit)) {
+            ok = false;
+            break;
+        }
+        if (valid) r.desc[ds].w[__popc(bal & lt)] = w;
+        if (lane == 0) r.desc[ds].n = __popc(bal);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.dfull[ds]);
+
+        if (FUSED && !issue_row(res + tok * row_bytes)) {
+            ok = false;
+            break;
+        }
+        uint32_t b = bal;
+        while (b != 0) {
+            const int d = __ffs(b) - 1;
+            b &= b - 1;
+            const int sl = __shfl_sync(kFull, slot, d);
+            const long long row = ((long long)d * p.R + s) * p.m + sl;
+            if (!issue_row(eo + row * row_bytes)) {
+                ok = false;
+                break;
+            }
+        }
+        if (!ok) break;
+        slot = slot_next;
+        w = w_next;
+    }
+    if (!ok) {
+        if (lane == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+        // Let the copies already issued land before the CTA's shared memory goes away.
+        const uint32_t first = q > (uint32_t)slots ? q - slots : 0u;
+        for (uint32_t k = first; k < q; ++k)
+            ptx::mbar_wait_bounded(&r.full[k % slots], (k / slots) & 1u, kWaitLimit);
+    }
+}
+
+// ---- consumer warps ---------------------------------------------------------
+
+template <int VPT, bool WEIGHTED, bool FUSED>
+__device__ void consume(const CombineParams &p, const Ring &r, int slots, int ncw) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nct = ncw * 32;
+    const size_t stride = ring_stride(2 * p.H);
+    const uint4 *gam = reinterpret_cast<const uint4 *>(p.gamma);
+    uint4 *out = reinterpret_cast<uint4 *>(p.out);
+    uint4 *rout = reinterpret_cast<uint4 *>(p.residual_out);
+
+    uint32_t q = 0, nfused = 0;
+    bool ok = true;
+    for (long long tok = blockIdx.x, j = 0; tok < p.tokens; tok += gridDim.x, ++j) {
+        const int ds = (int)(j % kDesc);
+        if (!ptx::mbar_wait_bounded(&r.dfull[ds], (uint32_t)((j / kDesc) & 1), kWaitLimit)) {
+            ok = false;
+            break;
+        }
+        const int n = r.desc[ds].n;
+
+        uint4 rv[FUSED ? VPT : 1];
+        if (FUSED) {
+            const uint32_t b = q % slots;
+            if (!ptx::mbar_wait_bounded(&r.full[b], (q / slots) & 1u, kWaitLimit)) {
+                ok = false;
+                break;
+            }
+            const uint4 *row = reinterpret_cast<const uint4 *>(r.rows + b * stride);
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = tid + v * nct;
+                rv[v] = c < p.H8 ? row[c] : make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.empty[b]);
+            ++q;
+        }
+
+        float acc[VPT][8];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[v][e] = 0.0f;
+
+        for (int i = 0; i < n; ++i) {
+            const float wi = WEIGHTED ? r.desc[ds].w[i] : 1.0f;
+            const uint32_t b = q % slots;
+            if (!ptx::mbar_wait_bounded(&r.full[b], (q / slots) & 1u, kWaitLimit)) {
+                ok = false;
+                break;
+            }
+            const uint4 *row = reinterpret_cast<const uint4 *>(r.rows + b * stride);
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = tid + v * nct;
+                if (c < p.H8) accumulate8<WEIGHTED>(acc[v], row[c], wi);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.empty[b]);
+            ++q;
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.dempty[ds]);
+
+        const long long row0 = tok * p.H8;
+        if (!FUSED) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = tid + v * nct;
+                if (c < p.H8) __stcs(out + row0 + c, pack8(acc[v]));
+            }
+            continue;
+        }
+
+        float ss = 0.0f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const uint32_t u[4] = {rv[v].x, rv[v].y, rv[v].z, rv[v].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[v][2 * i] = __fadd_rn(acc[v][2 * i], lo_f(u[i]));
+                acc[v][2 * i + 1] = __fadd_rn(acc[v][2 * i + 1], hi_f(u[i]));
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss += acc[v][e] * acc[v][e];
+            const int c = tid + v * nct;
+            if (rout != nullptr && c < p.H8) __stcs(rout + row0 + c, pack8(acc[v]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+        const int par = nfused & 1;
+        if (lane == 0) {
+            r.red[par * kMaxConsumerWarps + warp] = ss;
+            mbar_arrive(&r.rbar[par]);
+        }
+        if (!ptx::mbar_wait_bounded(&r.rbar[par], (nfused >> 1) & 1u, kWaitLimit)) {
+            ok = false;
+            break;
+        }
+        ++nfused;
+        float total = 0.0f;
+        for (int i = 0; i < ncw; ++i) total += r.red[par * kMaxConsumerWarps + i];
+        const float inv = rsqrtf(total / (float)p.H + p.eps);
+
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = tid + v * nct;
+            if (c >= p.H8) continue;
+            const uint4 g = __ldg(gam + c);
+            const uint32_t u[4] = {g.x, g.y, g.z, g.w};
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                y[2 * i] = acc[v][2 * i] * inv * lo_f(u[i]);
+                y[2 * i + 1] = acc[v][2 * i + 1] * inv * hi_f(u[i]);
+            }
+            __stcs(out + row0 + c, pack8(y));
+        }
+    }
+    if (!ok && lane == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+}
+
+template <int VPT, bool WEIGHTED, bool FUSED>
+__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
+    combine_ring_kernel(const CombineParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int slots = p.ring_slots;
+    const int ncw = (int)(blockDim.x >> 5) - 1;
+    const Ring r = carve(smem, 2 * p.H, slots);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < slots; ++i) {
+            ptx::mbar_init(&r.full[i], 1);
+            ptx::mbar_init(&r.empty[i], ncw);
+        }
+        for (int i = 0; i < kDesc; ++i) {
+            ptx::mbar_init(&r.dfull[i], 1);
+            ptx::mbar_init(&r.dempty[i], ncw);
+        }
+        ptx::mbar_init(&r.rbar[0], ncw);
+        ptx::mbar_init(&r.rbar[1], ncw);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    ptx::grid_dependency_wait();
+    if ((int)(threadIdx.x >> 5) == ncw)
+        produce<WEIGHTED, FUSED>(p, r, slots);
+    else
+        consume<VPT, WEIGHTED, FUSED>(p, r, slots, ncw);
+}
+
+template <int VPT, bool W, bool F>
+cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStream_t st) {
+    long long grid = shape.grid;
+    if (grid > p.tokens) grid = p.tokens;
+    if (grid < 1) return cudaSuccess;
+    combine_ring_kernel<VPT, W, F><<<(unsigned)grid, shape.block, shape.smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int VPT, bool W, bool F>
+cudaError_t set_smem(size_t smem) {
+    return cudaFuncSetAttribute(combine_ring_kernel<VPT, W, F>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <int VPT>
+cudaError_t by_flags(bool w, bool f, const CombineParams *p, const LaunchShape &shape,
+                     cudaStream_t st) {
+    if (p == nullptr) {  // preparation: allow the dynamic shared memory
+        if (w && f) return set_smem<VPT, true, true>(shape.smem);
+        if (w) return set_smem<VPT, true, false>(shape.smem);
+        if (f) return set_smem<VPT, false, true>(shape.smem);
+        return set_smem<VPT, false, false>(shape.smem);
+    }
+    if (w && f) return launch_t<VPT, true, true>(*p, shape, st);
+    if (w) return launch_t<VPT, true, false>(*p, shape, st);
+    if (f) return launch_t<VPT, false, true>(*p, shape, st);
+    return launch_t<VPT, false, false>(*p, shape, st);
+}
+
+template <int VPT>
+cudaError_t occ_flags(bool w, bool f, int block, size_t smem, int *per_sm) {
+    if (w && f)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            per_sm, combine_ring_kernel<VPT, true, true>, block, smem);
+    if (w)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            per_sm, combine_ring_kernel<VPT, true, false>, block, smem);
+    if (f)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            per_sm, combine_ring_kernel<VPT, false, true>, block, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        per_sm, combine_ring_kernel<VPT, false, false>, block, smem);
+}
+
+cudaError_t occupancy(int vpt, bool w, bool f, int block, size_t smem, int *per_sm) {
+    switch (vpt) {
+        case 1: return occ_flags<1>(w, f, block, smem, per_sm);
+        case 2: return occ_flags<2>(w, f, block, smem, per_sm);
+        case 4: return occ_flags<4>(w, f, block, smem, per_sm);
+        case 8: return occ_flags<8>(w, f, block, smem, per_sm);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t by_vpt(int vpt, bool w, bool f, const CombineParams *p, const LaunchShape &shape,
+                   cudaStream_t st) {
+    switch (vpt) {
+        case 1: return by_flags<1>(w, f, p, shape, st);
+        case 2: return by_flags<2>(w, f, p, shape, st);
+        case 4: return by_flags<4>(w, f, p, shape, st);
+        case 8: return by_flags<8>(w, f, p, shape, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, int num_sms,
+                                 LaunchShape *shape, int *vpt, int *slots) {
+    const int H8 = H / 8;
+    int v = 1;
+    while (v < 8 && (H8 + v - 1) / v > kMaxConsumerWarps * 32) v *= 2;
+    const int ncw = ((H8 + v - 1) / v + 31) / 32;
+    if (ncw > kMaxConsumerWarps) return cudaErrorInvalidValue;
+    int dev = 0, optin = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (err != cudaSuccess) return err;
+    // About 48 KB of ring per CTA (3 rows at H=7168): the residency of
+    // several CTAs per SM (several tokens in the reduce/epilogue stage at
+    // once) matters more than a deep ring; measured best on the prefill
+    // shape (2-6 slots swept).
+    int s = (int)(kRingBytesTarget / ring_stride(2 * H));
+    s = s < 2 ? 2 : (s > kMaxRingSlots ? kMaxRingSlots : s);
+    if (const char *e = std::getenv("MOE_COMBINE_RING_SLOTS")) {
+        const int x = std::atoi(e);
+        if (x >= 2 && x <= kMaxRingSlots) s = x;
+    }
+    while (s > 2 && ring_smem_bytes(2 * H, s) > (size_t)optin) --s;
+    if (ring_smem_bytes(2 * H, s) > (size_t)optin) return cudaErrorInvalidValue;
+    *vpt = v;
+    *slots = s;
+    shape->block = (ncw + 1) * 32;
+    shape->smem = ring_smem_bytes(2 * H, s);
+    err = by_vpt(v, weighted, fused, nullptr, *shape, nullptr);
+    if (err != cudaSuccess) return err;
+    int per_sm = 1;
+    err = occupancy(v, weighted, fused, shape->block, shape->smem, &per_sm);
+    if (err != cudaSuccess) return err;
+    shape->grid = num_sms * (per_sm < 1 ? 1 : per_sm);
+    return cudaSuccess;
+}
+
+cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, int vpt,
+                                const LaunchShape &shape, cudaStream_t st) {
+    return by_vpt(vpt, weighted, fused, &p, shape, st);
+}
+
+}  // namespace moe

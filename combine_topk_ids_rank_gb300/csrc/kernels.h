@@ -70,6 +70,7 @@ struct CombineParams {
     uint32_t *flags;
     float eps;
     int R, T, RP, m, H, H8;       // H8 = H / 8 (16-byte vectors per row)
+    int ring_slots;               // shared-memory row buffers (ring kernel)
     long long tokens;             // R * T
 };
 
@@ -93,5 +94,12 @@ cudaError_t combine_prepare(int H, bool weighted, bool fused, int num_sms,
                             LaunchShape *shape, int *vpt);
 cudaError_t launch_combine(const CombineParams &p, bool weighted, bool fused, int vpt,
                            const LaunchShape &shape, cudaStream_t st);
+
+// Combine with bulk-copy row streaming (one CTA per SM, producer warp +
+// consumer warps): vectors per consumer thread, ring depth and shape.
+cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, int num_sms,
+                                 LaunchShape *shape, int *vpt, int *slots);
+cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, int vpt,
+                                const LaunchShape &shape, cudaStream_t st);
 
 }  // namespace moe

@@ -11,6 +11,7 @@
 #include "moe_a2a.h"
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -90,7 +91,9 @@ struct moe_a2a {
     moe::DispatchParams dispatch_tmpl;
     moe::LaunchShape dispatch_shape;
     bool combine_ready[4];
+    bool combine_ring[4];
     int combine_vpt[4];
+    int combine_slots[4];
     moe::LaunchShape combine_shape[4];
 };
 
@@ -259,10 +262,23 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
     if (h->T > 0) {
         const int variant = (weighted ? 2 : 0) + (fused ? 1 : 0);
         if (!h->combine_ready[variant]) {
-            if (moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
-                                     &h->combine_shape[variant],
-                                     &h->combine_vpt[variant]) != cudaSuccess)
-                return MOE_ERR_CUDA;
+            // The fused combine streams its rows through a shared-memory
+            // ring (its epilogue then overlaps other tokens' loads); the
+            // plain gather-sum keeps rows in registers, which measured
+            // faster there.  MOE_COMBINE_KERNEL=ring|regs overrides.
+            const char *sel = std::getenv("MOE_COMBINE_KERNEL");
+            bool ring = fused;
+            if (sel != nullptr && std::strcmp(sel, "regs") == 0) ring = false;
+            if (sel != nullptr && std::strcmp(sel, "ring") == 0) ring = true;
+            cudaError_t e =
+                ring ? moe::combine_ring_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
+                                                 &h->combine_shape[variant],
+                                                 &h->combine_vpt[variant],
+                                                 &h->combine_slots[variant])
+                     : moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
+                                            &h->combine_shape[variant], &h->combine_vpt[variant]);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            h->combine_ring[variant] = ring;
             h->combine_ready[variant] = true;
         }
         moe::CombineParams cp;
@@ -278,9 +294,14 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
         cp.R = h->cfg.ep_size, cp.T = h->T, cp.RP = h->L.RP, cp.m = h->m;
         cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
         cp.tokens = (long long)h->cfg.ep_size * h->T;
-        if (moe::launch_combine(cp, weighted != 0, fused, h->combine_vpt[variant],
-                                h->combine_shape[variant], st) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        cp.ring_slots = h->combine_slots[variant];
+        const cudaError_t e =
+            h->combine_ring[variant]
+                ? moe::launch_combine_ring(cp, weighted != 0, fused, h->combine_vpt[variant],
+                                           h->combine_shape[variant], st)
+                : moe::launch_combine(cp, weighted != 0, fused, h->combine_vpt[variant],
+                                      h->combine_shape[variant], st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     h->phase = 0;
     return MOE_OK;
