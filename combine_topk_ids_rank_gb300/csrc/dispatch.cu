@@ -40,8 +40,10 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         ptx::fence_mbar_init();
     }
     __syncwarp();
-    ptx::grid_dependency_wait();  // send-slot table of the routing pass
-    if (threadIdx.x != 0) return;
+    if (threadIdx.x != 0) {
+        ptx::grid_dependency_wait();
+        return;
+    }
 
     const long long first = blockIdx.x, step = gridDim.x;
     const long long n = first < p.units ? (p.units - 1 - first) / step + 1 : 0;
@@ -51,7 +53,9 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         const int left = p.row_bytes - chunk * p.chunk_bytes;
         return (uint32_t)(left < p.chunk_bytes ? left : p.chunk_bytes);
     };
-    auto issue = [&](long long i) {
+    // A unit's stage receives its row chunk (an input of the call) and its
+    // send row (written by the routing pass); both complete on one barrier.
+    auto issue_row = [&](long long i) {
         const long long u = first + i * step;
         const long long token = u / p.chunks;
         const int chunk = (int)(u - token * p.chunks);
@@ -62,11 +66,23 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         ptx::mbar_arrive_expect_tx(&bars[stage], bytes + meta_bytes);
         ptx::bulk_g2s(buf, p.x + token * p.row_bytes + (long long)chunk * p.chunk_bytes, bytes,
                       &bars[stage]);
+    };
+    auto issue_meta = [&](long long i) {
+        const long long token = (first + i * step) / p.chunks;
+        const int stage = (int)(i % p.stages);
+        uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         ptx::bulk_g2s(buf + p.chunk_bytes, p.send_slot + token * p.RP, meta_bytes, &bars[stage]);
     };
+    auto issue = [&](long long i) {
+        issue_row(i);
+        issue_meta(i);
+    };
 
+    // The first stages' rows are in flight while the routing pass finishes.
     const long long prologue = n < p.stages ? n : p.stages;
-    for (long long i = 0; i < prologue; ++i) issue(i);
+    for (long long i = 0; i < prologue; ++i) issue_row(i);
+    ptx::grid_dependency_wait();  // send-slot table of the routing pass
+    for (long long i = 0; i < prologue; ++i) issue_meta(i);
     long long issued = prologue;
 
     for (long long i = 0; i < n; ++i) {

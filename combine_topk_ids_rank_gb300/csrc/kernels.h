@@ -9,18 +9,31 @@
 
 namespace moe {
 
-// Tokens per CTA of the two routing kernels (one token per thread).
+// Largest number of tokens per CTA of the two routing kernels (one token
+// per thread); the tile of a call is 32, 64, 128 or 256.
 constexpr int kRouteTile = 256;
+constexpr int kRouteMinTile = 32;
 
-// Routing, pass 1: destination mask of every token, per-tile destination
-// counts and per-tile expert histograms.
+// Tile of one call: the largest power of two in [32, 256] that still gives
+// about two CTAs per SM.
+inline int route_tile(long long R, long long T, int num_sms) {
+    int tile = kRouteTile;
+    while (tile > kRouteMinTile && R * ((T + tile - 1) / tile) < 2ll * num_sms) tile /= 2;
+    return tile;
+}
+
+// Routing, pass 1: per-tile destination counts, their exclusive per-tile
+// prefixes (by the last tile of each source), recv counts, the expert
+// histogram accumulated with atomics.
 struct RouteCountParams {
     const int32_t *topk_ids;  // [R][T][K]
-    uint32_t *dmask;          // [R][T]
     int32_t *tile_counts;     // [R][ntiles][RP]
-    int32_t *tile_hist;       // [R][ntiles][E]
+    int32_t *tile_prefix;     // [R][ntiles][RP]
+    int32_t *tile_ticket;     // [R], zero between calls
+    int32_t *hist_accum;      // [R][E], zero between calls
+    int32_t *recv_counts;     // [R][R]
     uint32_t *flags;          // sticky device flag word
-    int R, T, K, E, Epr, RP, ntiles;
+    int R, T, K, E, Epr, RP, ntiles, tile;
 };
 
 // Routing, pass 2: slots (ascending token order per plane), send table,
@@ -28,17 +41,15 @@ struct RouteCountParams {
 struct RouteScanParams {
     const int32_t *topk_ids;   // [R][T][K]
     const float *topk_w;       // [R][T][K]
-    const uint32_t *dmask;     // [R][T]
-    const int32_t *tile_counts;
-    const int32_t *tile_hist;
+    const int32_t *tile_prefix;
+    int32_t *hist_accum;       // read, then set back to zero
     int32_t *send_slot;        // [R][T][RP]
     float *dest_weight;        // [R][T][RP]
     int32_t *src_token;        // [R][R][m]
     int32_t *recv_ids;         // [R][R][m][K]
     float *recv_w;             // [R][R][m][K]
-    int32_t *recv_counts;      // [R][R]
     int32_t *local_counts;     // [E]  (= [R][Epr])
-    int R, T, K, E, Epr, RP, m, ntiles;
+    int R, T, K, E, Epr, RP, m, ntiles, tile;
 };
 
 // Dispatch rows: x[s][t] -> recv_x[d][s][slot] for every destination of

@@ -27,7 +27,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
     size_t recv_x, expert_out, recv_ids, recv_w, src_token, recv_counts, local_counts;
-    size_t send_slot, dest_weight, dmask, tile_counts, tile_hist, flags, total;
+    size_t send_slot, dest_weight, tile_counts, tile_prefix, tile_ticket, hist_accum, flags;
+    size_t total;
     int RP, ntiles_max;
 };
 
@@ -48,7 +49,7 @@ bool compute_layout(const moe_a2a_config_t *c, Layout *L) {
     const size_t R = c->ep_size, M = c->max_tokens_per_rank, H = c->hidden;
     const size_t E = c->num_experts, K = c->top_k;
     L->RP = (int)((R + 3) / 4 * 4);
-    L->ntiles_max = (int)((M + moe::kRouteTile - 1) / moe::kRouteTile);
+    L->ntiles_max = (int)((M + moe::kRouteMinTile - 1) / moe::kRouteMinTile);
     const size_t RP = L->RP, NT = L->ntiles_max;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -65,9 +66,10 @@ bool compute_layout(const moe_a2a_config_t *c, Layout *L) {
     L->local_counts = take(E * 4);
     L->send_slot = take(R * M * RP * 4);
     L->dest_weight = take(R * M * RP * 4);
-    L->dmask = take(R * M * 4);
     L->tile_counts = take(R * NT * RP * 4);
-    L->tile_hist = take(R * NT * E * 4);
+    L->tile_prefix = take(R * NT * RP * 4);
+    L->tile_ticket = take(R * 4);  // ticket and histogram accumulator are
+    L->hist_accum = take(R * E * 4);  // zero between calls
     L->flags = take(kAlign);
     L->total = off;
     return true;
@@ -84,6 +86,7 @@ struct moe_a2a {
     Layout L;
     int phase;  // 0 idle, 1 dispatched
     int T, m;   // of the pending dispatch
+    bool accum_dirty;  // routing pass interrupted: re-zero its accumulators
     // lazily initialised on the first call that queues work
     bool ready;
     int device;
@@ -116,6 +119,7 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
         return MOE_ERR_CUDA;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
+    h->accum_dirty = true;
     h->ready = true;
     return MOE_OK;
 }
@@ -178,34 +182,47 @@ int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
                 cudaSuccess)
             return MOE_ERR_CUDA;
     } else {
-        const int ntiles = (T + moe::kRouteTile - 1) / moe::kRouteTile;
+        if (h->accum_dirty) {
+            if (cudaMemsetAsync(h->ws + h->L.tile_ticket, 0, sizeof(int32_t) * R, st) !=
+                    cudaSuccess ||
+                cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * R * E, st) !=
+                    cudaSuccess)
+                return MOE_ERR_CUDA;
+            h->accum_dirty = false;
+        }
+        const int tile = moe::route_tile(R, T, h->num_sms);
+        const int ntiles = (T + tile - 1) / tile;
 
         moe::RouteCountParams rc_p;
         rc_p.topk_ids = d_topk_ids;
-        rc_p.dmask = at<uint32_t>(h, h->L.dmask);
         rc_p.tile_counts = at<int32_t>(h, h->L.tile_counts);
-        rc_p.tile_hist = at<int32_t>(h, h->L.tile_hist);
+        rc_p.tile_prefix = at<int32_t>(h, h->L.tile_prefix);
+        rc_p.tile_ticket = at<int32_t>(h, h->L.tile_ticket);
+        rc_p.hist_accum = at<int32_t>(h, h->L.hist_accum);
+        rc_p.recv_counts = at<int32_t>(h, h->L.recv_counts);
         rc_p.flags = flags;
         rc_p.R = R, rc_p.T = T, rc_p.K = K, rc_p.E = E, rc_p.Epr = E / R, rc_p.RP = RP;
         rc_p.ntiles = ntiles;
+        rc_p.tile = tile;
         if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
+        h->accum_dirty = true;  // until the scan pass that clears it is queued
 
         moe::RouteScanParams rs;
         rs.topk_ids = d_topk_ids;
         rs.topk_w = d_topk_w;
-        rs.dmask = rc_p.dmask;
-        rs.tile_counts = rc_p.tile_counts;
-        rs.tile_hist = rc_p.tile_hist;
+        rs.tile_prefix = rc_p.tile_prefix;
+        rs.hist_accum = rc_p.hist_accum;
         rs.send_slot = at<int32_t>(h, h->L.send_slot);
         rs.dest_weight = at<float>(h, h->L.dest_weight);
         rs.src_token = at<int32_t>(h, h->L.src_token);
         rs.recv_ids = at<int32_t>(h, h->L.recv_ids);
         rs.recv_w = at<float>(h, h->L.recv_w);
-        rs.recv_counts = at<int32_t>(h, h->L.recv_counts);
         rs.local_counts = at<int32_t>(h, h->L.local_counts);
         rs.R = R, rs.T = T, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
         rs.ntiles = ntiles;
+        rs.tile = tile;
         if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+        h->accum_dirty = false;
 
         moe::DispatchParams dp = h->dispatch_tmpl;
         dp.x = static_cast<const uint8_t *>(d_x);

@@ -28,9 +28,10 @@ constexpr size_t kScratchBytes = MOE_STATIC_SCRATCH_BYTES;
 constexpr size_t kAlign = 256;
 constexpr int kMaxDevices = 64;
 
-// The scratch: per-token destination masks, per-tile destination counts,
-// per-tile expert histograms, and one word that absorbs device flags when
-// the caller passes no flag output.  Shared by every call on a device.
+// The scratch: per-tile destination counts and prefixes (tiles of 256
+// tokens), per-source tickets, per-source expert histograms, and one
+// word that absorbs device flags when the caller passes no flag output.
+// Shared by every call on a device.
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
 std::mutex g_mutex;
@@ -65,8 +66,8 @@ extern "C" size_t moe_route_static_scratch_bytes(int32_t ep_size, int32_t num_ex
     const size_t R = ep_size, E = num_experts, T = tokens_per_rank;
     const size_t RP = (R + 3) / 4 * 4;
     const size_t tiles = (T + moe::kRouteTile - 1) / moe::kRouteTile;
-    return align_up(R * T * 4, kAlign) + align_up(R * tiles * RP * 4, kAlign) +
-           align_up(R * tiles * E * 4, kAlign) + kAlign;
+    return 2 * align_up(R * tiles * RP * 4, kAlign) + align_up(R * 4 + R * E * 4, kAlign) +
+           kAlign;
 }
 
 extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, int32_t top_k,
@@ -110,42 +111,49 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     const int rc = scratch_address(&base);
     if (rc != MOE_OK) return rc;
 
-    // Carve the scratch.  Every word the kernels read from it is written
-    // earlier in the same call, so nothing has to start at zero.
+    // Carve the scratch: per-tile counts and prefixes (written before they
+    // are read in this call), then the per-source tickets and the expert
+    // histogram accumulator, which must start at zero and are cleared here.
     const int RP = (R + 3) / 4 * 4;
     const int ntiles = (T + moe::kRouteTile - 1) / moe::kRouteTile;
     unsigned char *p = static_cast<unsigned char *>(base);
-    uint32_t *dmask = reinterpret_cast<uint32_t *>(p);
-    p += align_up((size_t)R * T * 4, kAlign);
     int32_t *tile_counts = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)R * ntiles * RP * 4, kAlign);
-    int32_t *tile_hist = reinterpret_cast<int32_t *>(p);
-    p += align_up((size_t)R * ntiles * E * 4, kAlign);
+    int32_t *tile_prefix = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)R * ntiles * RP * 4, kAlign);
+    int32_t *tile_ticket = reinterpret_cast<int32_t *>(p);
+    int32_t *hist_accum = tile_ticket + R;
+    if (cudaMemsetAsync(tile_ticket, 0, sizeof(int32_t) * ((size_t)R + (size_t)R * E), st) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    p += align_up((size_t)R * 4 + (size_t)R * E * 4, kAlign);
     uint32_t *sink_flags = reinterpret_cast<uint32_t *>(p);
 
     moe::RouteCountParams c;
     c.topk_ids = d_topk_ids;
-    c.dmask = dmask;
     c.tile_counts = tile_counts;
-    c.tile_hist = tile_hist;
+    c.tile_prefix = tile_prefix;
+    c.tile_ticket = tile_ticket;
+    c.hist_accum = hist_accum;
+    c.recv_counts = d_recv_counts;
     c.flags = d_flags != nullptr ? d_flags : sink_flags;
     c.R = R, c.T = T, c.K = K, c.E = E, c.Epr = E / R, c.RP = RP, c.ntiles = ntiles;
+    c.tile = moe::kRouteTile;
     if (moe::launch_route_count(c, st) != cudaSuccess) return MOE_ERR_CUDA;
 
     moe::RouteScanParams s;
     s.topk_ids = d_topk_ids;
     s.topk_w = d_topk_w;
-    s.dmask = dmask;
-    s.tile_counts = tile_counts;
-    s.tile_hist = tile_hist;
+    s.tile_prefix = tile_prefix;
+    s.hist_accum = hist_accum;
     s.send_slot = d_send_slot;
     s.dest_weight = d_dest_weight;
     s.src_token = d_src_token;
     s.recv_ids = d_recv_topk_ids;
     s.recv_w = d_recv_topk_w;
-    s.recv_counts = d_recv_counts;
     s.local_counts = d_local_expert_counts;
     s.R = R, s.T = T, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
+    s.tile = moe::kRouteTile;
     if (moe::launch_route_scan(s, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -12,15 +12,23 @@
 //   recv_counts[d][s], src_token[d][s][slot], masked metadata rows,
 //   local_expert_counts[e] = #valid (s,t,k) entries with e_k = e.
 //
-// Two passes over tiles of 256 tokens of one source rank (grid: tiles x R):
-//   pass 1 (route_count): destination mask per token, destination counts
-//          and an expert histogram per tile;
-//   pass 2 (route_scan):  exclusive prefix of the earlier tiles' counts plus
-//          a warp-ballot / cross-warp scan inside the tile gives each
-//          token's slot on every destination; then all routing outputs are
-//          written, and the per-tile histograms are reduced.
-// Both passes are O(T) in work; pass 2 starts early through programmatic
-// dependent launch and waits for pass 1 on the device.
+// Two passes over tiles of `tile` tokens (32..256, one token per thread) of
+// one source rank, grid = tiles x R; the tile is chosen so the grid covers
+// about two CTAs per SM:
+//   pass 1 (route_count): per-tile destination counts (warp ballots), the
+//          expert histogram added into the source rank's accumulator (so
+//          that only that source's tiles contend for an address), the
+//          bad-id flag.  The last tile of a source to finish (atomic ticket after
+//          a fence; nothing waits) scans that source's tile counts into
+//          exclusive per-tile prefixes and writes its recv counts.
+//   pass 2 (route_scan):  loads its tokens' ids and weights and rebuilds
+//          their destination masks while pass 1 still runs (programmatic
+//          dependent launch), then adds its tile prefix to a warp-ballot /
+//          cross-warp scan inside the tile to get each token's slot on
+//          every destination; writes all routing outputs (send rows as
+//          16-byte vectors); copies its share of the histogram accumulator
+//          to local_expert_counts and sets it back to zero for the next call.
+// Both passes are O(T) in work and O(1) in cross-tile reads per CTA.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -30,13 +38,8 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarps = kRouteTile / 32;
-
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
+constexpr int kMaxWarps = kRouteTile / 32;
+constexpr int kScanChunk = 2048;  // ints staged per step of the tile scan
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -44,22 +47,25 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+__device__ __forceinline__ bool is_local(int e, int E, int Epr, int d) {
+    return e >= 0 && e < E && e / Epr == d;
+}
+
 // KT > 0: top_k known at compile time (ids/weights held in registers);
 // KT == 0: any top_k, read from global memory (L1) when needed.
 template <int KT>
-__global__ void __launch_bounds__(kRouteTile)
-    route_count_kernel(const RouteCountParams p) {
+__global__ void __launch_bounds__(kRouteTile) route_count_kernel(const RouteCountParams p) {
     extern __shared__ int32_t hist[];  // [E]
-    __shared__ int32_t warp_cnt[kWarps][32];
+    __shared__ int32_t warp_cnt[kMaxWarps][32];
     const int tile = blockIdx.x, s = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t = tile * kRouteTile + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = p.tile >> 5;
+    const int t = tile * p.tile + threadIdx.x;
     const int K = KT > 0 ? KT : p.K;
 
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
 
-    for (int e = threadIdx.x; e < p.E; e += kRouteTile) hist[e] = 0;
+    for (int e = threadIdx.x; e < p.E; e += p.tile) hist[e] = 0;
     __syncthreads();
 
     uint32_t mask = 0;
@@ -77,7 +83,6 @@ __global__ void __launch_bounds__(kRouteTile)
             mask |= 1u << (e / p.Epr);
             atomicAdd(&hist[e], 1);
         }
-        p.dmask[(size_t)s * p.T + t] = mask;
     }
     if (bad) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_EXPERT_ID);
 
@@ -91,154 +96,193 @@ __global__ void __launch_bounds__(kRouteTile)
         const int d = threadIdx.x;
         int sum = 0;
         if (d < p.R)
-            for (int w = 0; w < kWarps; ++w) sum += warp_cnt[w][d];
+            for (int w = 0; w < nwarps; ++w) sum += warp_cnt[w][d];
         p.tile_counts[((size_t)s * p.ntiles + tile) * p.RP + d] = sum;
     }
-    int32_t *th = p.tile_hist + ((size_t)s * p.ntiles + tile) * p.E;
-    for (int e = threadIdx.x; e < p.E; e += kRouteTile) th[e] = hist[e];
+    int32_t *acc = p.hist_accum + (size_t)s * p.E;  // one accumulator per source rank
+    for (int e = threadIdx.x; e < p.E; e += p.tile)
+        if (hist[e] != 0) atomicAdd(&acc[e], hist[e]);
+
+    // The last tile of this source to get here turns the tile counts into
+    // exclusive prefixes.  Classic fence-then-ticket: no thread waits.
+    __shared__ int last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&p.tile_ticket[s], 1) == p.ntiles - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // Stage the source's tile counts through shared memory (the histogram
+    // buffer, at least kScanChunk ints) in coalesced chunks; one thread per
+    // destination turns each column into an exclusive running sum.
+    int *buf = hist;
+    const int chunk_tiles = kScanChunk / p.RP;
+    const int32_t *src = p.tile_counts + (size_t)s * p.ntiles * p.RP;
+    int32_t *dst = p.tile_prefix + (size_t)s * p.ntiles * p.RP;
+    int carry = 0;
+    for (int c0 = 0; c0 < p.ntiles; c0 += chunk_tiles) {
+        const int nt = min(chunk_tiles, p.ntiles - c0);
+        __syncthreads();
+        for (int x = threadIdx.x; x < nt * p.RP; x += p.tile)
+            buf[x] = __ldcg(src + (size_t)c0 * p.RP + x);
+        __syncthreads();
+        if (threadIdx.x < p.R) {
+            for (int i = 0; i < nt; ++i) {
+                const int v = buf[i * p.RP + threadIdx.x];
+                buf[i * p.RP + threadIdx.x] = carry;
+                carry += v;
+            }
+        }
+        __syncthreads();
+        for (int x = threadIdx.x; x < nt * p.RP; x += p.tile)
+            dst[(size_t)c0 * p.RP + x] = buf[x];
+    }
+    if (threadIdx.x < p.R) p.recv_counts[threadIdx.x * p.R + s] = carry;
+    if (threadIdx.x == 0) p.tile_ticket[s] = 0;  // ready for the next call
 }
 
 template <int KT>
-__global__ void __launch_bounds__(kRouteTile)
-    route_scan_kernel(const RouteScanParams p) {
+__global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanParams p) {
     __shared__ int32_t prefix[32];
-    __shared__ int32_t warp_cnt[kWarps][32];
-    __shared__ int32_t warp_off[kWarps][32];
-    __shared__ int32_t tile_total[32];
+    __shared__ int32_t warp_cnt[kMaxWarps][32];
+    __shared__ int32_t warp_off[kMaxWarps][32];
     const int tile = blockIdx.x, s = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t = tile * kRouteTile + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = p.tile >> 5;
+    const int t = tile * p.tile + threadIdx.x;
     const int K = KT > 0 ? KT : p.K;
+    const bool active = t < p.T;
 
     ptx::launch_dependents();
-    ptx::grid_dependency_wait();  // pass 1 complete
 
-    // Exclusive prefix of destination counts over the earlier tiles.
-    for (int d = warp; d < p.R; d += kWarps) {
-        int sum = 0;
-        for (int i = lane; i < tile; i += 32)
-            sum += p.tile_counts[((size_t)s * p.ntiles + i) * p.RP + d];
-        sum = warp_sum(sum);
-        if (lane == 0) prefix[d] = sum;
-    }
-
-    // This CTA also finishes the experts e == cta (mod ncta) of the
-    // local-expert histogram (sum of all tiles' partial counts).
-    {
-        const int ncta = p.R * p.ntiles, cta = s * p.ntiles + tile;
-        for (int e = cta + warp * ncta; e < p.E; e += kWarps * ncta) {
-            int sum = 0;
-            for (int c = lane; c < ncta; c += 32) sum += p.tile_hist[(size_t)c * p.E + e];
-            sum = warp_sum(sum);
-            if (lane == 0) p.local_counts[e] = sum;
-        }
-    }
-
-    const bool active = t < p.T;
-    const uint32_t mask = active ? p.dmask[(size_t)s * p.T + t] : 0u;
-    for (int d = 0; d < p.R; ++d) {
-        const uint32_t b = __ballot_sync(kFull, (mask >> d) & 1u);
-        if (lane == 0) warp_cnt[warp][d] = __popc(b);
-    }
-    __syncthreads();
-    if (threadIdx.x < p.R) {
-        const int d = threadIdx.x;
-        int run = prefix[d];
-        for (int w = 0; w < kWarps; ++w) {
-            warp_off[w][d] = run;
-            run += warp_cnt[w][d];
-        }
-        tile_total[d] = run;
-    }
-    __syncthreads();
-
+    // Inputs first (they do not depend on pass 1): ids, weights, mask.
     const size_t tok = (size_t)s * p.T + (active ? t : 0);
     const int32_t *ids = p.topk_ids + tok * K;
     const float *wts = p.topk_w + tok * K;
     constexpr int KR = KT > 0 ? KT : 1;
     int32_t id_r[KR];
     float w_r[KR];
-    if (KT > 0 && active) {
+    uint32_t mask = 0;
+    if (active) {
+        if constexpr (KT > 0) {
 #pragma unroll
-        for (int k = 0; k < KR; ++k) {
-            id_r[k] = ids[k];
-            w_r[k] = wts[k];
+            for (int k = 0; k < KR; ++k) {
+                id_r[k] = ids[k];
+                w_r[k] = wts[k];
+                if (id_r[k] >= 0 && id_r[k] < p.E) mask |= 1u << (id_r[k] / p.Epr);
+            }
+        } else {
+            for (int k = 0; k < K; ++k) {
+                const int e = ids[k];
+                if (e >= 0 && e < p.E) mask |= 1u << (e / p.Epr);
+            }
         }
     }
+    for (int d = 0; d < p.R; ++d) {
+        const uint32_t b = __ballot_sync(kFull, (mask >> d) & 1u);
+        if (lane == 0) warp_cnt[warp][d] = __popc(b);
+    }
+
+    ptx::grid_dependency_wait();  // pass 1 complete: prefixes and histogram
+
+    if (threadIdx.x < p.R)
+        prefix[threadIdx.x] = p.tile_prefix[((size_t)s * p.ntiles + tile) * p.RP + threadIdx.x];
+
+    // This CTA owns the experts e == cta (mod ncta) of the histogram: sum
+    // the per-source accumulators and leave them at zero for the next call.
+    {
+        const int ncta = p.R * p.ntiles, cta = s * p.ntiles + tile;
+        for (int e = cta + (int)threadIdx.x * ncta; e < p.E; e += p.tile * ncta) {
+            int sum = 0;
+            for (int r = 0; r < p.R; ++r) sum += p.hist_accum[(size_t)r * p.E + e];
+            for (int r = 0; r < p.R; ++r) p.hist_accum[(size_t)r * p.E + e] = 0;
+            p.local_counts[e] = sum;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < p.R) {
+        const int d = threadIdx.x;
+        int run = prefix[d];
+        for (int w = 0; w < nwarps; ++w) {
+            warp_off[w][d] = run;
+            run += warp_cnt[w][d];
+        }
+    }
+    __syncthreads();
+
     const uint32_t lt = lanemask_lt();
     int32_t *srow = p.send_slot + tok * p.RP;
     float *wrow = p.dest_weight + tok * p.RP;
 
-    for (int d = 0; d < p.R; ++d) {
-        const bool has = (mask >> d) & 1u;
-        const uint32_t b = __ballot_sync(kFull, has);
-        if (!active) continue;
-        int32_t slot = -1;
-        float wsum = 0.0f;
-        if (has) {
-            slot = warp_off[warp][d] + __popc(b & lt);
-            const size_t row = ((size_t)d * p.R + s) * p.m + slot;
-            p.src_token[row] = t;
-            int32_t *rid = p.recv_ids + row * K;
-            float *rw = p.recv_w + row * K;
-            if constexpr (KT > 0 && KT % 4 == 0) {
+    for (int d0 = 0; d0 < p.RP; d0 += 4) {
+        int4 sv;
+        float4 wv;
+        int32_t *se = &sv.x;
+        float *we = &wv.x;
 #pragma unroll
-                for (int k0 = 0; k0 < KT; k0 += 4) {
-                    int4 iv;
-                    float4 fv;
-                    int32_t *ie = &iv.x;
-                    float *fe = &fv.x;
+        for (int q = 0; q < 4; ++q) {
+            const int d = d0 + q;
+            const bool has = d < p.R && ((mask >> d) & 1u);
+            const uint32_t b = __ballot_sync(kFull, has);
+            int32_t slot = -1;
+            float wsum = 0.0f;
+            if (has) {
+                slot = warp_off[warp][d] + __popc(b & lt);
+                const size_t row = ((size_t)d * p.R + s) * p.m + slot;
+                p.src_token[row] = t;
+                int32_t *rid = p.recv_ids + row * K;
+                float *rw = p.recv_w + row * K;
+                if constexpr (KT > 0 && KT % 4 == 0) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int e = id_r[k0 + q];
-                        const bool local = e >= 0 && e < p.E && e / p.Epr == d;
-                        ie[q] = local ? e : -1;
-                        fe[q] = local ? w_r[k0 + q] : 0.0f;
-                        if (local) wsum = __fadd_rn(wsum, w_r[k0 + q]);
+                    for (int k0 = 0; k0 < KT; k0 += 4) {
+                        int4 iv;
+                        float4 fv;
+                        int32_t *ie = &iv.x;
+                        float *fe = &fv.x;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const bool local = is_local(id_r[k0 + u], p.E, p.Epr, d);
+                            ie[u] = local ? id_r[k0 + u] : -1;
+                            fe[u] = local ? w_r[k0 + u] : 0.0f;
+                            if (local) wsum = __fadd_rn(wsum, w_r[k0 + u]);
+                        }
+                        reinterpret_cast<int4 *>(rid)[k0 / 4] = iv;
+                        reinterpret_cast<float4 *>(rw)[k0 / 4] = fv;
                     }
-                    reinterpret_cast<int4 *>(rid)[k0 / 4] = iv;
-                    reinterpret_cast<float4 *>(rw)[k0 / 4] = fv;
-                }
-            } else if constexpr (KT > 0) {
+                } else if constexpr (KT > 0) {
 #pragma unroll
-                for (int k = 0; k < KT; ++k) {
-                    const int e = id_r[k];
-                    const bool local = e >= 0 && e < p.E && e / p.Epr == d;
-                    rid[k] = local ? e : -1;
-                    rw[k] = local ? w_r[k] : 0.0f;
-                    if (local) wsum = __fadd_rn(wsum, w_r[k]);
-                }
-            } else {
-                for (int k = 0; k < K; ++k) {
-                    const int e = ids[k];
-                    const float wk = wts[k];
-                    const bool local = e >= 0 && e < p.E && e / p.Epr == d;
-                    rid[k] = local ? e : -1;
-                    rw[k] = local ? wk : 0.0f;
-                    if (local) wsum = __fadd_rn(wsum, wk);
+                    for (int k = 0; k < KT; ++k) {
+                        const bool local = is_local(id_r[k], p.E, p.Epr, d);
+                        rid[k] = local ? id_r[k] : -1;
+                        rw[k] = local ? w_r[k] : 0.0f;
+                        if (local) wsum = __fadd_rn(wsum, w_r[k]);
+                    }
+                } else {
+                    for (int k = 0; k < K; ++k) {
+                        const int e = ids[k];
+                        const float wk = wts[k];
+                        const bool local = is_local(e, p.E, p.Epr, d);
+                        rid[k] = local ? e : -1;
+                        rw[k] = local ? wk : 0.0f;
+                        if (local) wsum = __fadd_rn(wsum, wk);
+                    }
                 }
             }
+            se[q] = slot;
+            we[q] = wsum;
         }
-        srow[d] = slot;
-        wrow[d] = wsum;
-    }
-    if (active) {
-        for (int d = p.R; d < p.RP; ++d) {
-            srow[d] = -1;
-            wrow[d] = 0.0f;
+        if (active) {
+            *reinterpret_cast<int4 *>(srow + d0) = sv;
+            *reinterpret_cast<float4 *>(wrow + d0) = wv;
         }
     }
-
-    if (tile == p.ntiles - 1 && threadIdx.x < p.R)
-        p.recv_counts[threadIdx.x * p.R + s] = tile_total[threadIdx.x];
 }
 
 template <typename Kern, typename P>
-cudaError_t launch2d(Kern kern, const P &p, int ntiles, int R, size_t smem, cudaStream_t st,
-                     bool pdl) {
+cudaError_t launch2d(Kern kern, const P &p, size_t smem, cudaStream_t st, bool pdl) {
+    if (p.tile < 32 || p.tile > kRouteTile || p.tile % 32 != 0) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ntiles, R, 1);
-    cfg.blockDim = dim3(kRouteTile, 1, 1);
+    cfg.gridDim = dim3(p.ntiles, p.R, 1);
+    cfg.blockDim = dim3(p.tile, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -252,21 +296,21 @@ cudaError_t launch2d(Kern kern, const P &p, int ntiles, int R, size_t smem, cuda
 }  // namespace
 
 cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st) {
-    const size_t smem = (size_t)p.E * sizeof(int32_t);
+    const size_t smem = (size_t)(p.E > kScanChunk ? p.E : kScanChunk) * sizeof(int32_t);
     switch (p.K) {
-        case 2: return launch2d(route_count_kernel<2>, p, p.ntiles, p.R, smem, st, false);
-        case 4: return launch2d(route_count_kernel<4>, p, p.ntiles, p.R, smem, st, false);
-        case 8: return launch2d(route_count_kernel<8>, p, p.ntiles, p.R, smem, st, false);
-        default: return launch2d(route_count_kernel<0>, p, p.ntiles, p.R, smem, st, false);
+        case 2: return launch2d(route_count_kernel<2>, p, smem, st, false);
+        case 4: return launch2d(route_count_kernel<4>, p, smem, st, false);
+        case 8: return launch2d(route_count_kernel<8>, p, smem, st, false);
+        default: return launch2d(route_count_kernel<0>, p, smem, st, false);
     }
 }
 
 cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pdl) {
     switch (p.K) {
-        case 2: return launch2d(route_scan_kernel<2>, p, p.ntiles, p.R, 0, st, pdl);
-        case 4: return launch2d(route_scan_kernel<4>, p, p.ntiles, p.R, 0, st, pdl);
-        case 8: return launch2d(route_scan_kernel<8>, p, p.ntiles, p.R, 0, st, pdl);
-        default: return launch2d(route_scan_kernel<0>, p, p.ntiles, p.R, 0, st, pdl);
+        case 2: return launch2d(route_scan_kernel<2>, p, 0, st, pdl);
+        case 4: return launch2d(route_scan_kernel<4>, p, 0, st, pdl);
+        case 8: return launch2d(route_scan_kernel<8>, p, 0, st, pdl);
+        default: return launch2d(route_scan_kernel<0>, p, 0, st, pdl);
     }
 }
 

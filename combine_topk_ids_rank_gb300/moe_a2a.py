@@ -224,6 +224,8 @@ class MoeA2A:
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_a2a_create")
         self.last_view = None
+        self._view_key = None
+        self._payload = None
 
     def _stream(self, stream) -> int:
         import torch
@@ -255,7 +257,11 @@ class MoeA2A:
                                self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_dispatch")
-        self.last_view = DispatchView(self, raw)
+        # The views depend only on (m, T): reuse them across calls.
+        key = (raw.plane_stride, raw.tokens_per_rank)
+        if self.last_view is None or self._view_key != key:
+            self.last_view = DispatchView(self, raw)
+            self._view_key = key
         return self.last_view
 
     def combine_payload(self):
@@ -264,9 +270,11 @@ class MoeA2A:
         if self.last_view is None:
             raise RuntimeError("no dispatch yet")
         R, H, m = self.ep_size, self.hidden, self.last_view.plane_stride
-        off = moe_combine_payload(self.handle) - self.workspace.data_ptr()
-        n = R * R * m * H * 2
-        return self.workspace[off:off + n].view(torch.bfloat16).view(R, R, m, H)
+        if self._payload is None or self._payload.shape[2] != m:
+            off = moe_combine_payload(self.handle) - self.workspace.data_ptr()
+            n = R * R * m * H * 2
+            self._payload = self.workspace[off:off + n].view(torch.bfloat16).view(R, R, m, H)
+        return self._payload
 
     def combine(self, expert_out=None, weighted: bool = False, residual=None, gamma=None,
                 eps: float = 1e-6, out=None, residual_out=None, stream=None):

@@ -222,12 +222,13 @@ const char *moe_a2a_status_string(int status);
  * capture.  All calls on a device share the one array and it keeps the last
  * call's contents: calls whose work overlaps on the GPU (other streams, or
  * other threads without ordering) race on it and must be serialised by the
- * caller.  Every scratch word read is written earlier in the same call, so
- * no clearing is needed.
+ * caller.  The parts that must start at zero (a ticket and an expert
+ * histogram accumulator per source rank) are cleared at the start of every call
+ * with cudaMemsetAsync on `stream`; the rest is written before it is read.
  *
  * Limit: moe_route_static_scratch_bytes(R, E, T) must not exceed
- * MOE_STATIC_SCRATCH_BYTES (R*T*4 + R*ceil(T/256)*(RP + E)*4 plus
- * alignment; e.g. R=8, E=256: up to T = 64512) else MOE_ERR_CAPACITY.
+ * MOE_STATIC_SCRATCH_BYTES (2*R*ceil(T/256)*RP*4 + (R + R*E)*4 plus
+ * alignment; e.g. R=8, E=256: up to T = 2092800) else MOE_ERR_CAPACITY.
  * Outputs (layouts as in moe_dispatch_view_t, RP = R rounded up to 4, all
  * 16-byte aligned): d_send_slot int32 [R][T][RP], d_dest_weight fp32
  * [R][T][RP], d_src_token int32 [R][R][m], d_recv_counts int32 [R][R],

@@ -95,7 +95,7 @@ def test_static_scratch_matches_dispatch_on_consecutive_calls(mod):
 
 
 def test_static_scratch_rejects_sizes_beyond_its_array(mod):
-    R, E, T = 32, 8192, 8192
+    R, E, T = 32, 8192, 1 << 20
     assert mod.moe_route_static_scratch_bytes(R, E, T) > mod.MOE_STATIC_SCRATCH_BYTES
     dummy = 1 << 20                 # never touched: the size check comes first
     st = mod.moe_route_static_scratch(R, E, 8, T, T, *([dummy] * 9))
