@@ -455,7 +455,7 @@ def run_gpu(args, w, rank, world, local_rank):
             with open(prof) as f:
                 tr = json.load(f)
             ent = tr.get(w.name, {}).get("combine")
-            if ent and ent.get("source_sha1") == source_sha1("combine.cu"):
+            if ent and ent.get("source_sha1") == source_sha1(ent.get("source", "combine_ring.cu")):
                 traffic = ent["dram_bytes_per_launch"]
         except (OSError, ValueError, KeyError):
             traffic = None
