@@ -407,46 +407,76 @@ def run_gpu(args, w, rank, world, local_rank):
     eff_gbs = (d_bytes + c_bytes) / ms_per_step / 1e6
 
     # ---- end to end through the public API, host buffers ----
+    # Every step copies its inputs (ids, weights, x, residual) from pinned
+    # host memory and its outputs (y, residual_out) back.  Double-buffered on
+    # three streams: step i+1's inputs go up and step i-1's outputs come down
+    # while step i runs dispatch + combine on the compute stream.
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.pin_memory()
         hids, hw, hx = pin(ids_h), pin(wts_h), pin(x_h)
         hres = pin(res_h) if w.fused else None
-        hout = torch.empty((R, T, H), dtype=torch.bfloat16).pin_memory()
-        hrout = torch.empty((R, T, H), dtype=torch.bfloat16).pin_memory() if w.fused else None
-        h2d = sum(t.numel() * t.element_size() for t in (hids, hw, hx, hres) if t is not None)
-        d2h = sum(t.numel() * t.element_size() for t in (hout, hrout) if t is not None)
+        hin = [t for t in (hids, hw, hx, hres) if t is not None]
+        hout = [[torch.empty((R, T, H), dtype=torch.bfloat16).pin_memory()
+                 for _ in range(2 if w.fused else 1)] for _ in range(2)]
+        din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(2)]
+        dout = [[torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+                 for _ in range(2 if w.fused else 1)] for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in hin)
+        d2h = sum(t.numel() * t.element_size() for t in hout[0])
+        compute = torch.cuda.current_stream(dev)
+        up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev = lambda: torch.cuda.Event()
+        in_ready, in_free = [ev(), ev()], [ev(), ev()]
+        out_ready, out_free = [ev(), ev()], [ev(), ev()]
+        for b in range(2):
+            in_free[b].record(compute)
+            out_free[b].record(compute)
 
-        def e2e_step():
-            ids.copy_(hids, non_blocking=True)
-            wts.copy_(hw, non_blocking=True)
-            x.copy_(hx, non_blocking=True)
-            if w.fused:
-                res.copy_(hres, non_blocking=True)
-            a2a.dispatch(ids, wts, x, w.runtime_max)
-            a2a.combine(eo, w.weighted, res, gam, w.eps, out, rout)
-            hout.copy_(out, non_blocking=True)
-            if w.fused:
-                hrout.copy_(rout, non_blocking=True)
+        def e2e_step(i):
+            b = i & 1
+            with torch.cuda.stream(up):
+                up.wait_event(in_free[b])
+                for dst, src in zip(din[b], hin):
+                    dst.copy_(src, non_blocking=True)
+                in_ready[b].record(up)
+            compute.wait_event(in_ready[b])
+            compute.wait_event(out_free[b])
+            d_ids, d_w, d_x = din[b][0], din[b][1], din[b][2]
+            d_res = din[b][3] if w.fused else None
+            a2a.dispatch(d_ids, d_w, d_x, w.runtime_max)
+            a2a.combine(eo, w.weighted, d_res, gam, w.eps, dout[b][0],
+                        dout[b][1] if w.fused else None)
+            in_free[b].record(compute)
+            out_ready[b].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(out_ready[b])
+                for dst, src in zip(hout[b], dout[b]):
+                    dst.copy_(src, non_blocking=True)
+                out_free[b].record(down)
 
-        for _ in range(3):
-            e2e_step()
+        for i in range(4):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record()
+        e0.record(compute)
+        up.wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        compute.wait_stream(down)
+        e1.record(compute)
         torch.cuda.synchronize()
         e2e_ms, _, e2e_tps = aggregate_over_ranks(e0.elapsed_time(e1), N, args.e2e_steps,
                                                   world, dev)
         e2e = {"value": e2e_tps, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
-               "path": "pinned host -> device copies, moe_dispatch, moe_combine, "
-                       "device -> pinned host copies, one stream"}
+               "path": "pinned host -> device copies on a copy stream, moe_dispatch + "
+                       "moe_combine on the compute stream, device -> pinned host copies on a "
+                       "third stream; double-buffered so one step's inputs and another's "
+                       "outputs move while a step computes"}
 
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")

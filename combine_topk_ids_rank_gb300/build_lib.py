@@ -16,8 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libmoe_a2a.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["route.cu", "dispatch.cu", "combine.cu", "combine_ring.cu", "moe_a2a.cpp",
-           "moe_noalloc.cu"]
+SOURCES = ["route.cu", "dispatch.cu", "combine.cu", "combine_ring.cu", "combine_tree.cu",
+           "moe_a2a.cpp", "moe_noalloc.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -48,6 +48,7 @@ struct RouteScanParams {
     int32_t *src_token;        // [R][R][m]
     int32_t *recv_ids;         // [R][R][m][K]
     float *recv_w;             // [R][R][m][K]
+    int8_t *topk_dest;         // [R][T][K] or null: rank whose message slot k carries
     int32_t *local_counts;     // [E]  (= [R][Epr])
     int R, T, K, E, Epr, RP, m, ntiles, tile;
 };
@@ -85,6 +86,21 @@ struct CombineParams {
     long long tokens;             // R * T
 };
 
+// Compatibility combine: bf16 pairwise tree over the top-k slots.
+struct CombineTreeParams {
+    const uint16_t *expert_out;  // bf16 [R][R][m][H]
+    const int32_t *send_slot;    // [R][T][RP]
+    const int8_t *topk_dest;     // [R][T][K]
+    const uint16_t *residual;    // bf16 [R][T][H] or null
+    const uint16_t *gamma;       // bf16 [H] or null
+    uint16_t *out;
+    uint16_t *residual_out;
+    uint32_t *flags;
+    float eps;
+    int R, T, RP, m, H, H8, K, P;  // P = K rounded up to a power of two (<= 8)
+    long long tokens;
+};
+
 struct LaunchShape {
     int grid;
     int block;
@@ -112,5 +128,7 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, int num_sms,
                                  LaunchShape *shape, int *vpt, int *slots);
 cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, int vpt,
                                 const LaunchShape &shape, cudaStream_t st);
+
+cudaError_t launch_combine_tree(const CombineTreeParams &p, int num_sms, cudaStream_t st);
 
 }  // namespace moe

@@ -27,7 +27,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
     size_t recv_x, expert_out, recv_ids, recv_w, src_token, recv_counts, local_counts;
-    size_t send_slot, dest_weight, tile_counts, tile_prefix, tile_ticket, hist_accum, flags;
+    size_t send_slot, dest_weight, topk_dest, tile_counts, tile_prefix, tile_ticket, hist_accum,
+        flags;
     size_t total;
     int RP, ntiles_max;
 };
@@ -66,6 +67,7 @@ bool compute_layout(const moe_a2a_config_t *c, Layout *L) {
     L->local_counts = take(E * 4);
     L->send_slot = take(R * M * RP * 4);
     L->dest_weight = take(R * M * RP * 4);
+    L->topk_dest = take(R * M * K);
     L->tile_counts = take(R * NT * RP * 4);
     L->tile_prefix = take(R * NT * RP * 4);
     L->tile_ticket = take(R * 4);  // ticket and histogram accumulator are
@@ -87,6 +89,7 @@ struct moe_a2a {
     int phase;  // 0 idle, 1 dispatched
     int T, m;   // of the pending dispatch
     bool accum_dirty;  // routing pass interrupted: re-zero its accumulators
+    int reduction;     // MOE_REDUCE_*
     // lazily initialised on the first call that queues work
     bool ready;
     int device;
@@ -217,6 +220,7 @@ int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
         rs.src_token = at<int32_t>(h, h->L.src_token);
         rs.recv_ids = at<int32_t>(h, h->L.recv_ids);
         rs.recv_w = at<float>(h, h->L.recv_w);
+        rs.topk_dest = at<int8_t>(h, h->L.topk_dest);
         rs.local_counts = at<int32_t>(h, h->L.local_counts);
         rs.R = R, rs.T = T, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
         rs.ntiles = ntiles;
@@ -275,8 +279,26 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
         if (!fused && d_residual_out != nullptr) return MOE_ERR_INVALID_ARG;
         if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
     }
+    if (h->reduction == MOE_REDUCE_BF16_TOPK_TREE && weighted) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (h->T > 0) {
+    if (h->T > 0 && h->reduction == MOE_REDUCE_BF16_TOPK_TREE) {
+        moe::CombineTreeParams tp;
+        tp.expert_out = static_cast<const uint16_t *>(eo);
+        tp.send_slot = at<int32_t>(h, h->L.send_slot);
+        tp.topk_dest = at<int8_t>(h, h->L.topk_dest);
+        tp.residual = static_cast<const uint16_t *>(d_residual);
+        tp.gamma = static_cast<const uint16_t *>(d_gamma);
+        tp.out = static_cast<uint16_t *>(d_out);
+        tp.residual_out = static_cast<uint16_t *>(d_residual_out);
+        tp.flags = at<uint32_t>(h, h->L.flags);
+        tp.eps = eps;
+        tp.R = h->cfg.ep_size, tp.T = h->T, tp.RP = h->L.RP, tp.m = h->m;
+        tp.H = h->cfg.hidden, tp.H8 = h->cfg.hidden / 8, tp.K = h->cfg.top_k;
+        tp.P = 1;
+        while (tp.P < tp.K) tp.P *= 2;
+        tp.tokens = (long long)h->cfg.ep_size * h->T;
+        if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    } else if (h->T > 0) {
         const int variant = (weighted ? 2 : 0) + (fused ? 1 : 0);
         if (!h->combine_ready[variant]) {
             // The fused combine streams its rows through a shared-memory
@@ -352,6 +374,19 @@ int moe_a2a_destroy(moe_a2a_t *h) {
 }
 
 int moe_a2a_phase(const moe_a2a_t *h) { return h == nullptr ? -1 : h->phase; }
+
+int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (reduction == MOE_REDUCE_FP32_RANK_ORDER) {
+        h->reduction = reduction;
+        return MOE_OK;
+    }
+    if (reduction == MOE_REDUCE_BF16_TOPK_TREE && h->cfg.top_k <= 8) {
+        h->reduction = reduction;
+        return MOE_OK;
+    }
+    return MOE_ERR_INVALID_ARG;
+}
 
 const char *moe_a2a_status_string(int status) {
     switch (status) {

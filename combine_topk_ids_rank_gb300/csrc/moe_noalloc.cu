@@ -151,6 +151,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     s.src_token = d_src_token;
     s.recv_ids = d_recv_topk_ids;
     s.recv_w = d_recv_topk_w;
+    s.topk_dest = nullptr;
     s.local_counts = d_local_expert_counts;
     s.R = R, s.T = T, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
     s.tile = moe::kRouteTile;

@@ -209,6 +209,25 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
     }
     __syncthreads();
 
+    // the rank whose message each top-k slot carries (first slot of a rank;
+    // later slots of the same rank and invalid ids carry none)
+    if (p.topk_dest != nullptr && active) {
+        int8_t *dst = p.topk_dest + tok * K;
+        uint32_t seen = 0;
+        for (int k = 0; k < K; ++k) {
+            const int e = KT > 0 ? id_r[k < KR ? k : 0] : ids[k];
+            int8_t v = -1;
+            if (e >= 0 && e < p.E) {
+                const int d = e / p.Epr;
+                if (!((seen >> d) & 1u)) {
+                    v = (int8_t)d;
+                    seen |= 1u << d;
+                }
+            }
+            dst[k] = v;
+        }
+    }
+
     const uint32_t lt = lanemask_lt();
     int32_t *srow = p.send_slot + tok * p.RP;
     float *wrow = p.dest_weight + tok * p.RP;

@@ -28,7 +28,10 @@ MOE_DEVICE_FLAG_BAD_SLOT = 0x4
 EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_combine_payload", "moe_combine", "moe_a2a_get_error",
            "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string",
-           "moe_route_static_scratch_bytes", "moe_route_static_scratch")
+           "moe_route_static_scratch_bytes", "moe_route_static_scratch",
+           "moe_a2a_set_reduction")
+MOE_REDUCE_FP32_RANK_ORDER = 0
+MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -80,6 +83,8 @@ def _load(path: str = LIBRARY):
     lib.moe_a2a_destroy.restype = ctypes.c_int
     lib.moe_a2a_phase.argtypes = [p]
     lib.moe_a2a_phase.restype = ctypes.c_int
+    lib.moe_a2a_set_reduction.argtypes = [p, i32]
+    lib.moe_a2a_set_reduction.restype = ctypes.c_int
     lib.moe_a2a_status_string.argtypes = [ctypes.c_int]
     lib.moe_a2a_status_string.restype = ctypes.c_char_p
     return lib
@@ -141,6 +146,10 @@ def moe_a2a_destroy(h) -> int:
 
 def moe_a2a_phase(h) -> int:
     return _lib.moe_a2a_phase(h)
+
+
+def moe_a2a_set_reduction(h, reduction: int) -> int:
+    return _lib.moe_a2a_set_reduction(h, reduction)
 
 
 def status_string(status: int) -> str:
@@ -299,6 +308,12 @@ class MoeA2A:
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_combine")
         return out
+
+    def set_reduction(self, reduction: int):
+        """MOE_REDUCE_FP32_RANK_ORDER (default) or MOE_REDUCE_BF16_TOPK_TREE."""
+        st = moe_a2a_set_reduction(self.handle, reduction)
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_a2a_set_reduction")
 
     def get_error(self, stream=None):
         """Synchronise, read and clear the device flag word: (status, bits)."""

@@ -201,6 +201,25 @@ int moe_a2a_phase(const moe_a2a_t *h);
 /* Static text for a status code. */
 const char *moe_a2a_status_string(int status);
 
+/* Reduction used by moe_combine.
+ * MOE_REDUCE_FP32_RANK_ORDER (default): fp32 sum over destination ranks in
+ *   ascending order, one narrowing ([IX] "Update": the fp32 accumulator of
+ *   version 0.6.16 on, "domain-fp32").
+ * MOE_REDUCE_BF16_TOPK_TREE: the reduction of FlashInfer's one-sided combine
+ *   through version 0.6.15 ([IX] "Update", "topk-slot-tree"): one bf16
+ *   accumulator per top-k slot, each rank's message in the first slot whose
+ *   expert lives on that rank (later slots of the same rank and invalid ids
+ *   hold zero), reduced by the pairwise tree (a0+a1)(a2+a3)...; (a0+a2)...;
+ *   (a0+a4) with a bf16 rounding after every add (slots padded with zeros to
+ *   a power of two).  Unweighted only (moe_combine with weighted != 0
+ *   returns MOE_ERR_INVALID_ARG); requires top_k <= 8.  The fused epilogue,
+ *   when requested, applies to the tree's result. */
+enum moe_reduction { MOE_REDUCE_FP32_RANK_ORDER = 0, MOE_REDUCE_BF16_TOPK_TREE = 1 };
+
+/* Select the reduction of subsequent moe_combine calls (host-only).
+ * Returns MOE_ERR_INVALID_ARG for an unknown mode or top_k > 8 with the tree. */
+int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction);
+
 /* ---- Routing without any device allocation --------------------------------
  * The source pages have no counterpart to this entry point; it exists for
  * callers that cannot allocate device memory: a plugin or custom op running

@@ -318,3 +318,109 @@ void oracle_combine(int R, int T, int H, int m, int weighted,
     free(acc);
     free(hsum);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Compatibility reduction: bf16 pairwise tree over the top-k slots          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [IX] "Update -- the correctness failures are resolved": through version
+ * 0.6.15 FlashInfer's one-sided combine keeps one accumulator per top-k
+ * slot in the payload type (bf16), with each operand at its original top-k
+ * slot (duplicate-rank slots are blanked in place, not compacted), and
+ * reduces the slots with a pairwise tree -- (a0+a1)(a2+a3)(a4+a5)(a6+a7),
+ * then (a0+a2)(a4+a6), then (a0+a4) -- rounding to bf16 after every add.
+ *
+ * For each requested token (flat s*T + t; tokens == NULL means all):
+ *   slot k holds f32(expert_out[d][s][send_slot(s,t,d)][h]) when e_k is a
+ *   valid expert, d = owner(e_k), and no earlier slot k' < k has a valid
+ *   expert on the same rank d; otherwise slot k holds 0.
+ *   The K slots are padded with zeros to the next power of two P; for
+ *   stride = 1, 2, 4, ... < P: a[i] = bf16(a[i] + a[i + stride]) for every i
+ *   that is a multiple of 2*stride.  The result is a[0] (already bf16).
+ * Unfused (residual == NULL): out = a[0].  Fused: the same epilogue as
+ * oracle_combine with acc = a[0]: hsum = acc + residual (fp32),
+ * residual_out = bf16(hsum), y = hsum / sqrt(mean(hsum^2) + eps) * gamma.
+ * The reduction is unweighted, as FlashInfer's combine is.
+ */
+void oracle_combine_topk_tree(int R, int T, int K, int E, int H, int m,
+                              const int32_t *topk_ids, const int32_t *send_slot,
+                              const uint16_t *expert_out, const uint16_t *residual,
+                              const uint16_t *gamma, float eps,
+                              const int64_t *tokens, long ntokens,
+                              uint16_t *out, uint16_t *residual_out, double *y_ref)
+{
+    const int Epr = E / R;
+    int P = 1;
+    while (P < K)
+        P *= 2;
+    long n = tokens ? ntokens : (long)R * T;
+    int *slot_dest = (int *)malloc((size_t)P * sizeof(int));
+    float *a = (float *)malloc((size_t)P * sizeof(float));
+    float *hsum = (float *)malloc((size_t)H * sizeof(float));
+    if (!slot_dest || !a || !hsum) {
+        free(slot_dest);
+        free(a);
+        free(hsum);
+        return;
+    }
+    for (long i = 0; i < n; ++i) {
+        long flat = tokens ? (long)tokens[i] : i;
+        int s = (int)(flat / T);
+        const int32_t *ids = topk_ids + (size_t)flat * K;
+        size_t o = (size_t)i * H;
+
+        /* which rank's message sits in which slot (first occurrence wins) */
+        for (int k = 0; k < P; ++k) {
+            slot_dest[k] = -1;
+            if (k >= K || ids[k] < 0 || ids[k] >= E)
+                continue;
+            int d = ids[k] / Epr;
+            int earlier = 0;
+            for (int k2 = 0; k2 < k; ++k2)
+                if (ids[k2] >= 0 && ids[k2] < E && ids[k2] / Epr == d)
+                    earlier = 1;
+            if (!earlier)
+                slot_dest[k] = d;
+        }
+
+        double sumsq = 0.0;
+        for (int h = 0; h < H; ++h) {
+            for (int k = 0; k < P; ++k) {
+                a[k] = 0.0f;
+                if (slot_dest[k] >= 0) {
+                    int d = slot_dest[k];
+                    int32_t j = send_slot[(size_t)flat * R + d];
+                    size_t row = ((size_t)d * R + s) * m + (size_t)j;
+                    a[k] = oracle_f32_from_bf16(expert_out[row * H + h]);
+                }
+            }
+            for (int stride = 1; stride < P; stride *= 2)
+                for (int k = 0; k + stride < P; k += 2 * stride)
+                    a[k] = oracle_f32_from_bf16(oracle_bf16_from_f32(a[k] + a[k + stride]));
+            if (residual == 0) {
+                out[o + h] = oracle_bf16_from_f32(a[0]);
+                if (y_ref)
+                    y_ref[o + h] = (double)a[0];
+                continue;
+            }
+            hsum[h] = a[0] + oracle_f32_from_bf16(residual[((size_t)flat) * H + h]);
+            if (residual_out)
+                residual_out[o + h] = oracle_bf16_from_f32(hsum[h]);
+            sumsq += (double)hsum[h] * (double)hsum[h];
+        }
+        if (residual == 0)
+            continue;
+        double inv = 1.0 / sqrt(sumsq / (double)H + (double)eps);
+        for (int h = 0; h < H; ++h) {
+            double y = (double)hsum[h] * inv * (double)oracle_f32_from_bf16(gamma[h]);
+            if (y_ref)
+                y_ref[o + h] = y;
+            out[o + h] = oracle_bf16_from_f32((float)y);
+        }
+    }
+    free(slot_dest);
+    free(a);
+    free(hsum);
+}
+

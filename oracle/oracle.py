@@ -39,6 +39,9 @@ def _bind(handle):
     handle.oracle_combine.argtypes = ([c_int] * 5 + [p] * 6 + [c_float, p, c_long]
                                       + [p] * 4)
     handle.oracle_combine.restype = None
+    handle.oracle_combine_topk_tree.argtypes = ([c_int] * 6 + [p] * 5 + [c_float, p, c_long]
+                                                + [p] * 3)
+    handle.oracle_combine_topk_tree.restype = None
     return handle
 
 
@@ -167,3 +170,31 @@ def combine(routing, expert_out, weighted: bool, residual=None, gamma=None,
                      _ptr(res), _ptr(gam), float(eps), _ptr(tok), n,
                      _ptr(acc), _ptr(out), _ptr(rout), _ptr(y))
     return dict(acc=acc, out=out, residual_out=rout, y=y)
+
+
+def combine_topk_tree(routing, topk_ids, num_experts: int, expert_out, residual=None,
+                      gamma=None, eps: float = 1e-6, tokens=None, handle=None):
+    """The bf16 top-k-slot tree reduction (compatibility mode), unweighted.
+
+    Returns dict(out=uint16, residual_out=uint16|None, y=float64), rows per
+    requested token."""
+    h = handle or lib()
+    ids = _need(topk_ids, np.int32)
+    R, T, K = ids.shape
+    eo = _need(expert_out, np.uint16)
+    m, H = eo.shape[2], eo.shape[3]
+    tok = None if tokens is None else _need(tokens, np.int64)
+    n = R * T if tok is None else tok.shape[0]
+    res = gam = rout = None
+    if residual is not None:
+        res = _need(residual, np.uint16, (R, T, H))
+        gam = _need(gamma, np.uint16, (H,))
+        rout = np.empty((n, H), np.uint16)
+    out = np.empty((n, H), np.uint16)
+    y = np.empty((n, H), np.float64)
+    h.oracle_combine_topk_tree(R, T, K, num_experts, H, m, _ptr(ids),
+                               _ptr(_need(routing["send_slot"], np.int32)), _ptr(eo),
+                               _ptr(res), _ptr(gam), float(eps), _ptr(tok), n,
+                               _ptr(out), _ptr(rout), _ptr(y))
+    return dict(out=out, residual_out=rout, y=y)
+

@@ -22,6 +22,11 @@ def f32(b):
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def f32_to_bits(values):
+    """float32 values (exact in bf16) -> bf16 bit patterns."""
+    return (np.asarray(values, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
 def to_dev(a, torch_dtype):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(a))

@@ -129,3 +129,15 @@ def test_get_error_before_any_work(abi):
     st, h = _handle(abi)
     assert abi.moe_a2a_get_error(h) == (abi.MOE_OK, 0)
     abi.moe_a2a_destroy(h)
+
+
+def test_set_reduction_checks(abi):
+    st, h = _handle(abi)                      # top_k = 8
+    assert abi.moe_a2a_set_reduction(h, abi.MOE_REDUCE_BF16_TOPK_TREE) == abi.MOE_OK
+    assert abi.moe_a2a_set_reduction(h, abi.MOE_REDUCE_FP32_RANK_ORDER) == abi.MOE_OK
+    assert abi.moe_a2a_set_reduction(h, 7) == abi.MOE_ERR_INVALID_ARG
+    abi.moe_a2a_destroy(h)
+    st, h = _handle(abi, cfg=(8, 64, 128, 256, 9))
+    assert abi.moe_a2a_set_reduction(h, abi.MOE_REDUCE_BF16_TOPK_TREE) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_set_reduction(None, 0) == abi.MOE_ERR_INVALID_ARG
+    abi.moe_a2a_destroy(h)

@@ -96,3 +96,89 @@ def test_repeat_calls_bit_identical():
                                parity.to_dev(inp["gamma"], torch.bfloat16), 1e-6)
         outs.append(parity.to_host_u16(out))
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+# --------------------------------------------------------------------------
+# Compatibility reduction (bf16 tree over top-k slots) against its oracle
+# --------------------------------------------------------------------------
+
+def _tree_case(R, T, H, E, K, seed, fused, ids=None, eo_fn=None):
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_REDUCE_BF16_TOPK_TREE
+    from oracle import oracle
+    ids = synth.topk_ids(seed, R, T, E, K) if ids is None else ids
+    w = synth.topk_weights(seed, R, T, K)
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    a.workspace.fill_(parity.POISON)
+    a.set_reduction(MOE_REDUCE_BF16_TOPK_TREE)
+    view = a.dispatch(parity.to_dev(ids, torch.int32), parity.to_dev(w, torch.float32),
+                      parity.to_dev(x, torch.bfloat16))
+    counts = view.recv_counts.cpu().numpy()
+    r = oracle.route(ids, w, E, T)
+    if eo_fn is None:
+        eo = synth.expert_out_planes(seed, R, T, H, counts)
+    else:
+        eo = np.full((R, R, T, H), 0x7FC0, np.uint16)
+        for d in range(R):
+            for s in range(R):
+                eo[d, s, :counts[d, s]] = parity.f32_to_bits(eo_fn(d))
+    pay = a.combine_payload()
+    for d in range(R):
+        for s in range(R):
+            c = int(counts[d, s])
+            if c:
+                pay[d, s, :c].copy_(parity.to_dev(eo[d, s, :c], torch.bfloat16))
+    res = synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H) if fused else None
+    gam = synth.gamma(seed, H) if fused else None
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(out) if fused else None
+    a.combine(None, False, parity.to_dev(res, torch.bfloat16) if fused else None,
+              parity.to_dev(gam, torch.bfloat16) if fused else None, 1e-6, out, rout)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    oc = oracle.combine_topk_tree(r, ids, E, eo, res, gam, 1e-6)
+    g = parity.to_host_u16(out).reshape(R * T, H)
+    if not fused:
+        assert np.array_equal(g, oc["out"])
+    else:
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H), oc["residual_out"])
+        err = np.abs(parity.f32(g).astype(np.float64) - oc["y"])
+        assert (err <= parity.ABS_TOL).all() and (err <= parity.REL_TOL * np.abs(oc["y"])).all()
+    return parity.f32(g)
+
+
+def test_topk_tree_pages_probe_on_gpu():
+    # {1.0, 7 x 2^-9} over eight slots -> 1.0078125 (the bf16 tree's value)
+    R = 8
+    ids = np.tile(np.arange(R, dtype=np.int32), (R, 1, 1)).reshape(R, 1, R)
+    vals = [1.0] + [2.0 ** -9] * 7
+    out = _tree_case(R, 1, 64, R, R, 0, False, ids=ids,
+                     eo_fn=lambda d: np.full(64, vals[d], np.float32))
+    assert np.all(out == 1.0078125)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_topk_tree_decode_shape(fused):
+    _tree_case(8, 64, 7168, 256, 8, 3, fused)
+
+
+def test_topk_tree_duplicates_and_missing_ids():
+    R, T, E, K = 4, 70, 16, 6
+    rng = np.random.default_rng(4)
+    ids = rng.integers(-1, E, (R, T, K)).astype(np.int32)   # repeats and -1
+    _tree_case(R, T, 200, E, K, 4, True, ids=ids)
+
+
+def test_topk_tree_rejects_weighted():
+    from combine_topk_ids_rank_gb300.moe_a2a import (MoeA2A, MoeA2AError,
+                                                     MOE_REDUCE_BF16_TOPK_TREE,
+                                                     MOE_ERR_INVALID_ARG)
+    a = MoeA2A(2, 8, 64, 4, 2, "cuda")
+    a.set_reduction(MOE_REDUCE_BF16_TOPK_TREE)
+    ids = parity.to_dev(synth.topk_ids(0, 2, 8, 4, 2), torch.int32)
+    w = parity.to_dev(synth.topk_weights(0, 2, 8, 2), torch.float32)
+    v = a.dispatch(ids, w, torch.zeros((2, 8, 64), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(MoeA2AError) as e:
+        a.combine(v.recv_x, True)
+    assert e.value.status == MOE_ERR_INVALID_ARG and a.phase == 1
+    a.combine(v.recv_x, False)

@@ -58,6 +58,15 @@ MUTANTS = {
     "invalid_ids_not_counted": (
         "invalid += 1;",
         "invalid += 0;"),
+    "tree_without_bf16_rounding": (
+        "a[k] = oracle_f32_from_bf16(oracle_bf16_from_f32(a[k] + a[k + stride]));",
+        "a[k] = a[k] + a[k + stride];"),
+    "tree_keeps_duplicate_ranks": (
+        "            if (!earlier)\n                slot_dest[k] = d;",
+        "            (void)earlier;\n            slot_dest[k] = d;"),
+    "tree_slots_in_rank_order": (
+        "            int d = ids[k] / Epr;\n            int earlier = 0;",
+        "            int d = (K - 1 - k) % R;\n            int earlier = 0;"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -85,6 +94,9 @@ class MutantOracle:
     def combine(self, *a, **k):
         return real.combine(*a, handle=self.h, **k)
 
+    def combine_topk_tree(self, *a, **k):
+        return real.combine_topk_tree(*a, handle=self.h, **k)
+
 
 PIN_TESTS = [
     (pins.test_bf16_rounding_matches_library_routine, {}),
@@ -103,16 +115,21 @@ PIN_TESTS = [
     (pins.test_residual_add_uses_fp32_sum, {}),
     (pins.test_rmsnorm_constant_row_closed_form, {"cval": 1e-3}),
     (pins.test_rmsnorm_matches_library_routine, {}),
+    (pins.test_probe_topk_tree_gives_the_pages_bf16_tree_value, {}),
+    (pins.test_topk_tree_blanks_duplicate_ranks, {}),
+    (pins.test_topk_tree_keeps_top_k_slot_order, {}),
 ]
 
 
 def _compile_mutant(name, tmpdir):
+    """Apply the edit at its first occurrence (for the epilogue lines, which
+    oracle_combine and oracle_combine_topk_tree share, that is oracle_combine)."""
     old, new = MUTANTS[name]
     src = open(obuild.SOURCE).read()
-    assert src.count(old) == 1, "mutation site for %s not found exactly once" % name
+    assert src.count(old) >= 1, "mutation site for %s not found" % name
     path = os.path.join(tmpdir, name + ".c")
     with open(path, "w") as f:
-        f.write(src.replace(old, new))
+        f.write(src.replace(old, new, 1))
     return obuild.build(force=True, source=path, output=os.path.join(tmpdir, name + ".so"))
 
 

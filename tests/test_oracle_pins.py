@@ -505,3 +505,61 @@ def test_token_subset_matches_full(oracle):
     sub = oracle.combine(r, eo, True, res, g, 1e-6, tokens=pick)
     for key in ("acc", "out", "residual_out", "y"):
         assert np.array_equal(sub[key], full[key][pick])
+
+
+# --------------------------------------------------------------------------
+# Compatibility reduction: bf16 tree over top-k slots
+# --------------------------------------------------------------------------
+
+def test_probe_topk_tree_gives_the_pages_bf16_tree_value(oracle):
+    g = read_golden("reduction_discriminator.txt")
+    contribs = [float(eval(v, {})) for v in g["contributions"].split(",")]
+    R = len(contribs)
+    E, K, H = R, R, 8
+    ids = route_to_ranks([[list(range(R))] for _ in range(R)], R, E, K)
+    r = oracle.route(ids, np.full(ids.shape, 0.125, np.float32), E, 1)
+    eo = planes_with(r, R, 1, H, lambda d, s, j: contribs[d])
+    c = oracle.combine_topk_tree(r, ids, E, eo)
+    assert np.all(f32(c["out"]) == float(g["bf16_tree"]))            # 1.0078125
+
+
+def test_topk_tree_blanks_duplicate_ranks(oracle):
+    g = read_golden("routing_probes.txt")
+    R, E, K, H = 2, 4, 2, 8
+    ids = np.array([[[0, 1]], [[2, 3]]], np.int32)      # both experts on one rank
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 1)
+    eo = planes_with(r, R, 1, H, lambda d, s, j: 1.0)
+    c = oracle.combine_topk_tree(r, ids, E, eo)
+    assert np.all(f32(c["out"]) == float(g["duplicate_experts_one_rank"]))
+
+
+def test_topk_tree_keeps_top_k_slot_order(oracle):
+    # slots [rank 2: 2^-8, rank 1: 2^-8, rank 0: 1.0, empty]: the tree gives
+    # (2^-8 + 2^-8) + (1 + 0) = 1 + 2^-7 exactly; compacting in rank order
+    # would give (1 + 2^-8) + 2^-8 -> 1.0 (ties to even twice).
+    R, E, K, H = 3, 3, 4, 8
+    ids = np.array([[[2, 1, 0, -1]]] * R, np.int32)
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 1)
+    vals = [1.0, 2.0 ** -8, 2.0 ** -8]
+    eo = planes_with(r, R, 1, H, lambda d, s, j: vals[d])
+    c = oracle.combine_topk_tree(r, ids, E, eo)
+    assert np.all(f32(c["out"]) == 1.0078125)
+    # the fp32 rank-order reduction of the same messages narrows to 1.0078125
+    # too (1 + 2^-7 exact); the tree differs from it on the pages' probe above
+    full = oracle.combine(r, eo, weighted=False)
+    assert np.all(f32(full["out"]) == 1.0078125)
+
+
+def test_topk_tree_fused_epilogue_matches_rank_sum_when_exact(oracle):
+    # with messages whose sums are exact in bf16 the two reductions agree, and
+    # so do their fused epilogues
+    R, E, K, H = 4, 16, 4, 32
+    ids = np.array([[[0, 5, 9, 13]] * 3] * R, np.int32)
+    r = oracle.route(ids, np.ones(ids.shape, np.float32), E, 3)
+    eo = planes_with(r, R, 3, H, lambda d, s, j: float(d + 1))
+    res = bits(np.full((R, 3, H), 0.5, np.float32))
+    gam = bits(np.ones(H, np.float32))
+    a = oracle.combine_topk_tree(r, ids, E, eo, res, gam, 1e-6)
+    b = oracle.combine(r, eo, False, res, gam, 1e-6)
+    assert np.array_equal(a["residual_out"], b["residual_out"])
+    assert np.array_equal(a["out"], b["out"])
