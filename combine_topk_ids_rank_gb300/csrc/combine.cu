@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
     ptx::grid_dependency_wait();
 
     int parity = 0;
-    for (long long tok = blockIdx.x; tok < p.tokens; tok += gridDim.x, parity ^= 1) {
-        const int s = (int)(tok / p.T);
+    for (long long i = blockIdx.x; i < p.tokens; i += gridDim.x, parity ^= 1) {
+        int s, t;
+        token_of(p.map, p.R, i, s, t);
+        const long long tok = (long long)s * p.map.stride + t;  // row of the token arrays
         const long long row0 = tok * p.H8;
 
         uint4 r[FUSED ? VPT : 1];
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
                     if (tid == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
                     slot[q] = -1;
                 }
+                if (!((p.active >> ((d0 + q) & 31)) & 1u)) slot[q] = -1;  // rank gone
             }
             uint4 v[G][VPT];
 #pragma unroll

@@ -136,10 +136,18 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
     const size_t stride = ring_stride((int)row_bytes);
     const uint32_t lt = lanemask_lt();
 
-    auto load_route = [&](long long tok, int &slot, float &w) {
+    // the CTA's i-th token: its row in the token arrays and its source rank
+    auto row_of = [&](long long i, int &s) -> long long {
+        int t;
+        token_of(p.map, p.R, i, s, t);
+        return (long long)s * p.map.stride + t;
+    };
+    auto load_route = [&](long long i, int &slot, float &w) {
         slot = -1;
         w = 0.0f;
-        if (tok < p.tokens && lane < p.R) {
+        if (i < p.tokens && lane < p.R && ((p.active >> lane) & 1u)) {
+            int s;
+            const long long tok = row_of(i, s);
             slot = __ldg(p.send_slot + tok * p.RP + lane);
             if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.RP + lane);
         }
@@ -161,11 +169,12 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
 
     int slot, slot_next;
     float w, w_next;
-    long long tok = blockIdx.x;
-    load_route(tok, slot, w);
-    for (uint32_t j = 0; tok < p.tokens; tok += gridDim.x, ++j) {
-        load_route(tok + gridDim.x, slot_next, w_next);
-        const int s = (int)(tok / p.T);
+    long long i = blockIdx.x;
+    load_route(i, slot, w);
+    for (uint32_t j = 0; i < p.tokens; i += gridDim.x, ++j) {
+        load_route(i + gridDim.x, slot_next, w_next);
+        int s;
+        const long long tok = row_of(i, s);
         bool valid = slot >= 0;
         if (valid && slot >= p.m) {  // guard: never expected from the routing pass
             atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
@@ -224,7 +233,10 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
 
     uint32_t q = 0, nfused = 0;
     bool ok = true;
-    for (long long tok = blockIdx.x, j = 0; tok < p.tokens; tok += gridDim.x, ++j) {
+    for (long long i = blockIdx.x, j = 0; i < p.tokens; i += gridDim.x, ++j) {
+        int s, t;
+        token_of(p.map, p.R, i, s, t);
+        const long long tok = (long long)s * p.map.stride + t;
         const int ds = (int)(j % kDesc);
         if (!ptx::mbar_wait_bounded(&r.dfull[ds], (uint32_t)((j / kDesc) & 1), kWaitLimit)) {
             ok = false;

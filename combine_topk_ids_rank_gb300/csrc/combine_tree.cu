@@ -57,10 +57,13 @@ __global__ void __launch_bounds__(kThreads) combine_tree_kernel(const CombineTre
     uint4 *rout = reinterpret_cast<uint4 *>(p.residual_out);
 
     ptx::grid_dependency_wait();
-    for (long long tok = blockIdx.x; tok < p.tokens; tok += gridDim.x) {
-        const int s = (int)(tok / p.T);
+    for (long long i = blockIdx.x; i < p.tokens; i += gridDim.x) {
+        int s, t;
+        token_of(p.map, p.R, i, s, t);
+        const long long tok = (long long)s * p.map.stride + t;
         if (tid < 8) {
             int d = tid < p.K ? p.topk_dest[tok * p.K + tid] : -1;
+            if (d >= 0 && !((p.active >> d) & 1u)) d = -1;  // rank gone since dispatch
             int sl = d >= 0 ? p.send_slot[tok * p.RP + d] : -1;
             if (sl >= p.m) {  // guard: never expected from the routing pass
                 atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);

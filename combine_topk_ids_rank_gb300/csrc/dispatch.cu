@@ -53,12 +53,22 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         const int left = p.row_bytes - chunk * p.chunk_bytes;
         return (uint32_t)(left < p.chunk_bytes ? left : p.chunk_bytes);
     };
+    // Unit i of this CTA: a chunk of the row of token (s, t), stored at row
+    // s * stride + t of the token arrays.
+    auto unit_of = [&](long long i, int &s, long long &row, int &chunk) {
+        const long long u = first + i * step;
+        const long long k = u / p.chunks;
+        chunk = (int)(u - k * p.chunks);
+        int t;
+        token_of(p.map, p.R, k, s, t);
+        row = (long long)s * p.map.stride + t;
+    };
     // A unit's stage receives its row chunk (an input of the call) and its
     // send row (written by the routing pass); both complete on one barrier.
     auto issue_row = [&](long long i) {
-        const long long u = first + i * step;
-        const long long token = u / p.chunks;
-        const int chunk = (int)(u - token * p.chunks);
+        int s, chunk;
+        long long token;
+        unit_of(i, s, token, chunk);
         const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         const uint32_t bytes = unit_bytes(chunk);
@@ -68,7 +78,9 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
                       &bars[stage]);
     };
     auto issue_meta = [&](long long i) {
-        const long long token = (first + i * step) / p.chunks;
+        int s, chunk;
+        long long token;
+        unit_of(i, s, token, chunk);
         const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         ptx::bulk_g2s(buf + p.chunk_bytes, p.send_slot + token * p.RP, meta_bytes, &bars[stage]);
@@ -96,10 +108,9 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
                                        kWaitLimit);
             return;
         }
-        const long long u = first + i * step;
-        const long long token = u / p.chunks;
-        const int chunk = (int)(u - token * p.chunks);
-        const int s = (int)(token / p.T);
+        int s, chunk;
+        long long token;
+        unit_of(i, s, token, chunk);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         const int32_t *slots = reinterpret_cast<const int32_t *>(buf + p.chunk_bytes);
         const uint32_t bytes = unit_bytes(chunk);

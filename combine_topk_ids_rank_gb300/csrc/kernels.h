@@ -9,6 +9,31 @@
 
 namespace moe {
 
+constexpr int kMaxRanks = 32;
+
+// The tokens of one call: source rank s holds count[s] tokens, stored at rows
+// s * stride + t (t < count[s]) of the [R][stride] token arrays; first[s] is
+// the exclusive prefix of the counts (first[R] = all tokens).  The uniform
+// case is count[s] = stride = T.
+struct TokenMap {
+    int stride;
+    int uniform;  // every count equals stride
+    int count[kMaxRanks];
+    int first[kMaxRanks + 1];
+};
+
+// (source, token) of the i-th token of the call, i < first[R].
+__host__ __device__ inline void token_of(const TokenMap &m, int R, long long i, int &s,
+                                         int &t) {
+    if (m.uniform) {
+        s = (int)(i / m.stride);
+    } else {
+        s = 0;
+        while (s + 1 < R && i >= m.first[s + 1]) ++s;
+    }
+    t = (int)(i - m.first[s]);
+}
+
 // Largest number of tokens per CTA of the two routing kernels (one token
 // per thread); the tile of a call is 32, 64, 128 or 256.
 constexpr int kRouteTile = 256;
@@ -33,7 +58,9 @@ struct RouteCountParams {
     int32_t *hist_accum;      // [R][E], zero between calls
     int32_t *recv_counts;     // [R][R]
     uint32_t *flags;          // sticky device flag word
-    int R, T, K, E, Epr, RP, ntiles, tile;
+    TokenMap map;
+    uint32_t active;          // ranks that receive messages
+    int R, K, E, Epr, RP, ntiles, tile;
 };
 
 // Routing, pass 2: slots (ascending token order per plane), send table,
@@ -50,7 +77,9 @@ struct RouteScanParams {
     float *recv_w;             // [R][R][m][K]
     int8_t *topk_dest;         // [R][T][K] or null: rank whose message slot k carries
     int32_t *local_counts;     // [E]  (= [R][Epr])
-    int R, T, K, E, Epr, RP, m, ntiles, tile;
+    TokenMap map;
+    uint32_t active;
+    int R, K, E, Epr, RP, m, ntiles, tile;
 };
 
 // Dispatch rows: x[s][t] -> recv_x[d][s][slot] for every destination of
@@ -60,13 +89,14 @@ struct DispatchParams {
     const int32_t *send_slot;  // [R][T][RP]
     uint8_t *recv_x;           // bf16 [R][R][m][H] as bytes
     uint32_t *flags;
-    int R, T, RP, m;
+    TokenMap map;
+    int R, RP, m;
     int row_bytes;             // 2H
     int chunk_bytes;           // <= row_bytes, multiple of 16
     int chunks;                // ceil(row_bytes / chunk_bytes)
     int stages;                // shared-memory ring depth
     int stage_bytes;           // chunk_bytes + meta, 128-byte multiple
-    long long units;           // R * T * chunks
+    long long units;           // tokens * chunks
 };
 
 // Combine: ascending-rank fp32 gather-sum of each token's messages, with
@@ -81,9 +111,11 @@ struct CombineParams {
     uint16_t *residual_out;       // bf16 [R][T][H] or null
     uint32_t *flags;
     float eps;
-    int R, T, RP, m, H, H8;       // H8 = H / 8 (16-byte vectors per row)
+    TokenMap map;
+    uint32_t active;              // ranks whose messages are summed
+    int R, RP, m, H, H8;          // H8 = H / 8 (16-byte vectors per row)
     int ring_slots;               // shared-memory row buffers (ring kernel)
-    long long tokens;             // R * T
+    long long tokens;             // map.first[R]
 };
 
 // Compatibility combine: bf16 pairwise tree over the top-k slots.
@@ -97,7 +129,9 @@ struct CombineTreeParams {
     uint16_t *residual_out;
     uint32_t *flags;
     float eps;
-    int R, T, RP, m, H, H8, K, P;  // P = K rounded up to a power of two (<= 8)
+    TokenMap map;
+    uint32_t active;
+    int R, RP, m, H, H8, K, P;  // P = K rounded up to a power of two (<= 8)
     long long tokens;
 };
 

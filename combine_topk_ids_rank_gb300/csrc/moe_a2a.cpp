@@ -87,7 +87,10 @@ struct moe_a2a {
     size_t ws_bytes;
     Layout L;
     int phase;  // 0 idle, 1 dispatched
-    int T, m;   // of the pending dispatch
+    moe::TokenMap map;  // tokens of the pending dispatch
+    long long ntok;     // map.first[R]
+    int m;              // plane stride of the pending dispatch
+    uint32_t active;    // ranks that take part (all by default)
     bool accum_dirty;  // routing pass interrupted: re-zero its accumulators
     int reduction;     // MOE_REDUCE_*
     // lazily initialised on the first call that queues work
@@ -127,6 +130,125 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
     return MOE_OK;
 }
 
+void uniform_map(int R, int T, moe::TokenMap *map) {
+    map->stride = T;
+    map->uniform = 1;
+    for (int s = 0; s < moe::kMaxRanks; ++s) {
+        map->count[s] = s < R ? T : 0;
+        map->first[s] = (s < R ? s : R) * T;
+    }
+    map->first[moe::kMaxRanks] = R * T;
+}
+
+// The dispatch phase for the tokens described by `map` (rows of stride
+// map.stride in the [R][stride] input arrays).
+int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
+                  const void *d_x, const moe::TokenMap &map, int m, void *stream,
+                  moe_dispatch_view_t *out_view) {
+    const int R = h->cfg.ep_size, E = h->cfg.num_experts, K = h->cfg.top_k;
+    const long long ntok = map.first[R];
+    if (ntok > 0) {
+        if (d_topk_ids == nullptr || d_topk_w == nullptr || d_x == nullptr)
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned(d_topk_ids, 4) || !aligned(d_topk_w, 4) || !aligned(d_x, 16))
+            return MOE_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = init_device(h, st);
+    if (rc != MOE_OK) return rc;
+
+    const int RP = h->L.RP;
+    uint32_t *flags = at<uint32_t>(h, h->L.flags);
+    int tmax = 0;
+    for (int s = 0; s < R; ++s) tmax = map.count[s] > tmax ? map.count[s] : tmax;
+
+    if (ntok == 0) {
+        if (cudaMemsetAsync(h->ws + h->L.recv_counts, 0, sizeof(int32_t) * R * R, st) !=
+                cudaSuccess ||
+            cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else {
+        if (h->accum_dirty) {
+            if (cudaMemsetAsync(h->ws + h->L.tile_ticket, 0, sizeof(int32_t) * R, st) !=
+                    cudaSuccess ||
+                cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * R * E, st) !=
+                    cudaSuccess)
+                return MOE_ERR_CUDA;
+            h->accum_dirty = false;
+        }
+        const int tile = moe::route_tile(R, tmax, h->num_sms);
+        const int ntiles = (tmax + tile - 1) / tile;
+
+        moe::RouteCountParams rc_p;
+        rc_p.topk_ids = d_topk_ids;
+        rc_p.tile_counts = at<int32_t>(h, h->L.tile_counts);
+        rc_p.tile_prefix = at<int32_t>(h, h->L.tile_prefix);
+        rc_p.tile_ticket = at<int32_t>(h, h->L.tile_ticket);
+        rc_p.hist_accum = at<int32_t>(h, h->L.hist_accum);
+        rc_p.recv_counts = at<int32_t>(h, h->L.recv_counts);
+        rc_p.flags = flags;
+        rc_p.map = map;
+        rc_p.active = h->active;
+        rc_p.R = R, rc_p.K = K, rc_p.E = E, rc_p.Epr = E / R, rc_p.RP = RP;
+        rc_p.ntiles = ntiles;
+        rc_p.tile = tile;
+        if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
+        h->accum_dirty = true;  // until the scan pass that clears it is queued
+
+        moe::RouteScanParams rs;
+        rs.topk_ids = d_topk_ids;
+        rs.topk_w = d_topk_w;
+        rs.tile_prefix = rc_p.tile_prefix;
+        rs.hist_accum = rc_p.hist_accum;
+        rs.send_slot = at<int32_t>(h, h->L.send_slot);
+        rs.dest_weight = at<float>(h, h->L.dest_weight);
+        rs.src_token = at<int32_t>(h, h->L.src_token);
+        rs.recv_ids = at<int32_t>(h, h->L.recv_ids);
+        rs.recv_w = at<float>(h, h->L.recv_w);
+        rs.topk_dest = at<int8_t>(h, h->L.topk_dest);
+        rs.local_counts = at<int32_t>(h, h->L.local_counts);
+        rs.map = map;
+        rs.active = h->active;
+        rs.R = R, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
+        rs.ntiles = ntiles;
+        rs.tile = tile;
+        if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+        h->accum_dirty = false;
+
+        moe::DispatchParams dp = h->dispatch_tmpl;
+        dp.x = static_cast<const uint8_t *>(d_x);
+        dp.send_slot = rs.send_slot;
+        dp.recv_x = at<uint8_t>(h, h->L.recv_x);
+        dp.flags = flags;
+        dp.map = map;
+        dp.R = R, dp.RP = RP, dp.m = m;
+        dp.units = ntok * dp.chunks;
+        if (moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+
+    h->map = map;
+    h->ntok = ntok;
+    h->m = m;
+    h->phase = 1;
+    if (out_view != nullptr) {
+        out_view->recv_x = h->ws + h->L.recv_x;
+        out_view->recv_topk_ids = at<int32_t>(h, h->L.recv_ids);
+        out_view->recv_topk_w = at<float>(h, h->L.recv_w);
+        out_view->src_token = at<int32_t>(h, h->L.src_token);
+        out_view->recv_counts = at<int32_t>(h, h->L.recv_counts);
+        out_view->local_expert_counts = at<int32_t>(h, h->L.local_counts);
+        out_view->send_slot = at<int32_t>(h, h->L.send_slot);
+        out_view->dest_weight = at<float>(h, h->L.dest_weight);
+        out_view->plane_stride = m;
+        out_view->tokens_per_rank = map.uniform ? map.stride : -1;
+        out_view->send_stride = RP;
+        out_view->token_stride = map.stride;
+    }
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -152,6 +274,7 @@ int moe_a2a_create(const moe_a2a_config_t *cfg, void *d_workspace, size_t worksp
     h->ws_bytes = workspace_bytes;
     h->L = L;
     h->phase = 0;
+    h->active = cfg->ep_size >= 32 ? 0xffffffffu : ((1u << cfg->ep_size) - 1u);
     *out = h;
     return MOE_OK;
 }
@@ -164,98 +287,43 @@ int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
     const int T = tokens_per_rank, m = runtime_max_tokens_per_rank;
     if (T < 0 || m < 1) return MOE_ERR_INVALID_ARG;
     if (m > h->cfg.max_tokens_per_rank || T > m) return MOE_ERR_CAPACITY;
-    if (T > 0) {
-        if (d_topk_ids == nullptr || d_topk_w == nullptr || d_x == nullptr)
-            return MOE_ERR_INVALID_ARG;
-        if (!aligned(d_topk_ids, 4) || !aligned(d_topk_w, 4) || !aligned(d_x, 16))
-            return MOE_ERR_INVALID_ARG;
+    moe::TokenMap map;
+    uniform_map(h->cfg.ep_size, T, &map);
+    return dispatch_impl(h, d_topk_ids, d_topk_w, d_x, map, m, stream, out_view);
+}
+
+int moe_dispatch_varlen(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
+                        const void *d_x, const int32_t *tokens_per_rank,
+                        int32_t runtime_max_tokens_per_rank, void *stream,
+                        moe_dispatch_view_t *out_view) {
+    if (h == nullptr || tokens_per_rank == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 0) return MOE_ERR_PHASE;
+    const int R = h->cfg.ep_size, m = runtime_max_tokens_per_rank;
+    if (m < 1) return MOE_ERR_INVALID_ARG;
+    if (m > h->cfg.max_tokens_per_rank) return MOE_ERR_CAPACITY;
+    moe::TokenMap map;
+    map.stride = m;
+    map.first[0] = 0;
+    bool same = true;
+    for (int s = 0; s < R; ++s) {
+        const int c = tokens_per_rank[s];
+        if (c < 0) return MOE_ERR_INVALID_ARG;
+        if (c > m) return MOE_ERR_CAPACITY;
+        map.count[s] = c;
+        map.first[s + 1] = map.first[s] + c;
+        same = same && c == m;
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int rc = init_device(h, st);
-    if (rc != MOE_OK) return rc;
+    for (int s = R; s < moe::kMaxRanks; ++s) map.count[s] = 0, map.first[s + 1] = map.first[R];
+    map.uniform = same ? 1 : 0;
+    return dispatch_impl(h, d_topk_ids, d_topk_w, d_x, map, m, stream, out_view);
+}
 
-    const int R = h->cfg.ep_size, E = h->cfg.num_experts, K = h->cfg.top_k;
-    const int RP = h->L.RP;
-    uint32_t *flags = at<uint32_t>(h, h->L.flags);
-
-    if (T == 0) {
-        if (cudaMemsetAsync(h->ws + h->L.recv_counts, 0, sizeof(int32_t) * R * R, st) !=
-                cudaSuccess ||
-            cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
-                cudaSuccess)
-            return MOE_ERR_CUDA;
-    } else {
-        if (h->accum_dirty) {
-            if (cudaMemsetAsync(h->ws + h->L.tile_ticket, 0, sizeof(int32_t) * R, st) !=
-                    cudaSuccess ||
-                cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * R * E, st) !=
-                    cudaSuccess)
-                return MOE_ERR_CUDA;
-            h->accum_dirty = false;
-        }
-        const int tile = moe::route_tile(R, T, h->num_sms);
-        const int ntiles = (T + tile - 1) / tile;
-
-        moe::RouteCountParams rc_p;
-        rc_p.topk_ids = d_topk_ids;
-        rc_p.tile_counts = at<int32_t>(h, h->L.tile_counts);
-        rc_p.tile_prefix = at<int32_t>(h, h->L.tile_prefix);
-        rc_p.tile_ticket = at<int32_t>(h, h->L.tile_ticket);
-        rc_p.hist_accum = at<int32_t>(h, h->L.hist_accum);
-        rc_p.recv_counts = at<int32_t>(h, h->L.recv_counts);
-        rc_p.flags = flags;
-        rc_p.R = R, rc_p.T = T, rc_p.K = K, rc_p.E = E, rc_p.Epr = E / R, rc_p.RP = RP;
-        rc_p.ntiles = ntiles;
-        rc_p.tile = tile;
-        if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
-        h->accum_dirty = true;  // until the scan pass that clears it is queued
-
-        moe::RouteScanParams rs;
-        rs.topk_ids = d_topk_ids;
-        rs.topk_w = d_topk_w;
-        rs.tile_prefix = rc_p.tile_prefix;
-        rs.hist_accum = rc_p.hist_accum;
-        rs.send_slot = at<int32_t>(h, h->L.send_slot);
-        rs.dest_weight = at<float>(h, h->L.dest_weight);
-        rs.src_token = at<int32_t>(h, h->L.src_token);
-        rs.recv_ids = at<int32_t>(h, h->L.recv_ids);
-        rs.recv_w = at<float>(h, h->L.recv_w);
-        rs.topk_dest = at<int8_t>(h, h->L.topk_dest);
-        rs.local_counts = at<int32_t>(h, h->L.local_counts);
-        rs.R = R, rs.T = T, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
-        rs.ntiles = ntiles;
-        rs.tile = tile;
-        if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
-        h->accum_dirty = false;
-
-        moe::DispatchParams dp = h->dispatch_tmpl;
-        dp.x = static_cast<const uint8_t *>(d_x);
-        dp.send_slot = rs.send_slot;
-        dp.recv_x = at<uint8_t>(h, h->L.recv_x);
-        dp.flags = flags;
-        dp.R = R, dp.T = T, dp.RP = RP, dp.m = m;
-        dp.units = (long long)R * T * dp.chunks;
-        if (moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
-
-    h->T = T;
-    h->m = m;
-    h->phase = 1;
-    if (out_view != nullptr) {
-        out_view->recv_x = h->ws + h->L.recv_x;
-        out_view->recv_topk_ids = at<int32_t>(h, h->L.recv_ids);
-        out_view->recv_topk_w = at<float>(h, h->L.recv_w);
-        out_view->src_token = at<int32_t>(h, h->L.src_token);
-        out_view->recv_counts = at<int32_t>(h, h->L.recv_counts);
-        out_view->local_expert_counts = at<int32_t>(h, h->L.local_counts);
-        out_view->send_slot = at<int32_t>(h, h->L.send_slot);
-        out_view->dest_weight = at<float>(h, h->L.dest_weight);
-        out_view->plane_stride = m;
-        out_view->tokens_per_rank = T;
-        out_view->send_stride = RP;
-        out_view->reserved = 0;
-    }
+int moe_a2a_set_active_ranks(moe_a2a_t *h, uint32_t active) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    const uint32_t all =
+        h->cfg.ep_size >= 32 ? 0xffffffffu : ((1u << h->cfg.ep_size) - 1u);
+    if (active & ~all) return MOE_ERR_INVALID_ARG;
+    h->active = active;
     return MOE_OK;
 }
 
@@ -269,7 +337,7 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
     if (h->phase != 1) return MOE_ERR_PHASE;
     const bool fused = d_residual != nullptr;
     const void *eo = d_expert_out != nullptr ? d_expert_out : h->ws + h->L.expert_out;
-    if (h->T > 0) {
+    if (h->ntok > 0) {
         if (d_out == nullptr || !aligned(d_out, 16) || !aligned(eo, 16))
             return MOE_ERR_INVALID_ARG;
         if (fused && (d_gamma == nullptr || !aligned(d_residual, 16) || !aligned(d_gamma, 16)))
@@ -281,7 +349,7 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
     }
     if (h->reduction == MOE_REDUCE_BF16_TOPK_TREE && weighted) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (h->T > 0 && h->reduction == MOE_REDUCE_BF16_TOPK_TREE) {
+    if (h->ntok > 0 && h->reduction == MOE_REDUCE_BF16_TOPK_TREE) {
         moe::CombineTreeParams tp;
         tp.expert_out = static_cast<const uint16_t *>(eo);
         tp.send_slot = at<int32_t>(h, h->L.send_slot);
@@ -292,13 +360,15 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
         tp.residual_out = static_cast<uint16_t *>(d_residual_out);
         tp.flags = at<uint32_t>(h, h->L.flags);
         tp.eps = eps;
-        tp.R = h->cfg.ep_size, tp.T = h->T, tp.RP = h->L.RP, tp.m = h->m;
+        tp.map = h->map;
+        tp.active = h->active;
+        tp.R = h->cfg.ep_size, tp.RP = h->L.RP, tp.m = h->m;
         tp.H = h->cfg.hidden, tp.H8 = h->cfg.hidden / 8, tp.K = h->cfg.top_k;
         tp.P = 1;
         while (tp.P < tp.K) tp.P *= 2;
-        tp.tokens = (long long)h->cfg.ep_size * h->T;
+        tp.tokens = h->ntok;
         if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-    } else if (h->T > 0) {
+    } else if (h->ntok > 0) {
         const int variant = (weighted ? 2 : 0) + (fused ? 1 : 0);
         if (!h->combine_ready[variant]) {
             // The fused combine streams its rows through a shared-memory
@@ -330,9 +400,11 @@ int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const 
         cp.residual_out = static_cast<uint16_t *>(d_residual_out);
         cp.eps = eps;
         cp.flags = at<uint32_t>(h, h->L.flags);
-        cp.R = h->cfg.ep_size, cp.T = h->T, cp.RP = h->L.RP, cp.m = h->m;
+        cp.map = h->map;
+        cp.active = h->active;
+        cp.R = h->cfg.ep_size, cp.RP = h->L.RP, cp.m = h->m;
         cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
-        cp.tokens = (long long)h->cfg.ep_size * h->T;
+        cp.tokens = h->ntok;
         cp.ring_slots = h->combine_slots[variant];
         const cudaError_t e =
             h->combine_ring[variant]

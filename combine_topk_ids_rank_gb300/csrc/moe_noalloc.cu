@@ -129,6 +129,16 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     p += align_up((size_t)R * 4 + (size_t)R * E * 4, kAlign);
     uint32_t *sink_flags = reinterpret_cast<uint32_t *>(p);
 
+    moe::TokenMap map;
+    map.stride = T;
+    map.uniform = 1;
+    for (int r = 0; r < moe::kMaxRanks; ++r) {
+        map.count[r] = r < R ? T : 0;
+        map.first[r] = (r < R ? r : R) * T;
+    }
+    map.first[moe::kMaxRanks] = R * T;
+    const uint32_t all = R >= 32 ? 0xffffffffu : ((1u << R) - 1u);
+
     moe::RouteCountParams c;
     c.topk_ids = d_topk_ids;
     c.tile_counts = tile_counts;
@@ -137,7 +147,9 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     c.hist_accum = hist_accum;
     c.recv_counts = d_recv_counts;
     c.flags = d_flags != nullptr ? d_flags : sink_flags;
-    c.R = R, c.T = T, c.K = K, c.E = E, c.Epr = E / R, c.RP = RP, c.ntiles = ntiles;
+    c.map = map;
+    c.active = all;
+    c.R = R, c.K = K, c.E = E, c.Epr = E / R, c.RP = RP, c.ntiles = ntiles;
     c.tile = moe::kRouteTile;
     if (moe::launch_route_count(c, st) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -153,7 +165,9 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     s.recv_w = d_recv_topk_w;
     s.topk_dest = nullptr;
     s.local_counts = d_local_expert_counts;
-    s.R = R, s.T = T, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
+    s.map = map;
+    s.active = all;
+    s.R = R, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
     s.tile = moe::kRouteTile;
     if (moe::launch_route_scan(s, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;

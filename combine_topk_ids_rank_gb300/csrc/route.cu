@@ -51,6 +51,13 @@ __device__ __forceinline__ bool is_local(int e, int E, int Epr, int d) {
     return e >= 0 && e < E && e / Epr == d;
 }
 
+// Destination rank of a valid expert on an active rank, else -1.
+__device__ __forceinline__ int live_rank(int e, int E, int Epr, uint32_t active) {
+    if (e < 0 || e >= E) return -1;
+    const int d = e / Epr;
+    return ((active >> d) & 1u) ? d : -1;
+}
+
 // KT > 0: top_k known at compile time (ids/weights held in registers);
 // KT == 0: any top_k, read from global memory (L1) when needed.
 template <int KT>
@@ -70,8 +77,8 @@ __global__ void __launch_bounds__(kRouteTile) route_count_kernel(const RouteCoun
 
     uint32_t mask = 0;
     bool bad = false;
-    if (t < p.T) {
-        const int32_t *ids = p.topk_ids + ((size_t)s * p.T + t) * K;
+    if (t < p.map.count[s]) {
+        const int32_t *ids = p.topk_ids + ((size_t)s * p.map.stride + t) * K;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int e = ids[k];
@@ -80,7 +87,9 @@ __global__ void __launch_bounds__(kRouteTile) route_count_kernel(const RouteCoun
                 bad = true;
                 continue;
             }
-            mask |= 1u << (e / p.Epr);
+            const int d = e / p.Epr;
+            if (!((p.active >> d) & 1u)) continue;  // expert on an inactive rank
+            mask |= 1u << d;
             atomicAdd(&hist[e], 1);
         }
     }
@@ -150,12 +159,12 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = p.tile >> 5;
     const int t = tile * p.tile + threadIdx.x;
     const int K = KT > 0 ? KT : p.K;
-    const bool active = t < p.T;
+    const bool active = t < p.map.count[s];
 
     ptx::launch_dependents();
 
     // Inputs first (they do not depend on pass 1): ids, weights, mask.
-    const size_t tok = (size_t)s * p.T + (active ? t : 0);
+    const size_t tok = (size_t)s * p.map.stride + (active ? t : 0);
     const int32_t *ids = p.topk_ids + tok * K;
     const float *wts = p.topk_w + tok * K;
     constexpr int KR = KT > 0 ? KT : 1;
@@ -168,12 +177,13 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
             for (int k = 0; k < KR; ++k) {
                 id_r[k] = ids[k];
                 w_r[k] = wts[k];
-                if (id_r[k] >= 0 && id_r[k] < p.E) mask |= 1u << (id_r[k] / p.Epr);
+                const int d = live_rank(id_r[k], p.E, p.Epr, p.active);
+                if (d >= 0) mask |= 1u << d;
             }
         } else {
             for (int k = 0; k < K; ++k) {
-                const int e = ids[k];
-                if (e >= 0 && e < p.E) mask |= 1u << (e / p.Epr);
+                const int d = live_rank(ids[k], p.E, p.Epr, p.active);
+                if (d >= 0) mask |= 1u << d;
             }
         }
     }
@@ -216,13 +226,11 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
         uint32_t seen = 0;
         for (int k = 0; k < K; ++k) {
             const int e = KT > 0 ? id_r[k < KR ? k : 0] : ids[k];
+            const int d = live_rank(e, p.E, p.Epr, p.active);
             int8_t v = -1;
-            if (e >= 0 && e < p.E) {
-                const int d = e / p.Epr;
-                if (!((seen >> d) & 1u)) {
-                    v = (int8_t)d;
-                    seen |= 1u << d;
-                }
+            if (d >= 0 && !((seen >> d) & 1u)) {
+                v = (int8_t)d;
+                seen |= 1u << d;
             }
             dst[k] = v;
         }

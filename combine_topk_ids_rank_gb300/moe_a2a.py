@@ -29,7 +29,7 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_combine_payload", "moe_combine", "moe_a2a_get_error",
            "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string",
            "moe_route_static_scratch_bytes", "moe_route_static_scratch",
-           "moe_a2a_set_reduction")
+           "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
@@ -47,7 +47,7 @@ class MoeDispatchView(ctypes.Structure):
                 ("recv_counts", ctypes.c_void_p), ("local_expert_counts", ctypes.c_void_p),
                 ("send_slot", ctypes.c_void_p), ("dest_weight", ctypes.c_void_p),
                 ("plane_stride", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
-                ("send_stride", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("send_stride", ctypes.c_int32), ("token_stride", ctypes.c_int32)]
 
 
 class MoeA2AError(RuntimeError):
@@ -83,6 +83,11 @@ def _load(path: str = LIBRARY):
     lib.moe_a2a_destroy.restype = ctypes.c_int
     lib.moe_a2a_phase.argtypes = [p]
     lib.moe_a2a_phase.restype = ctypes.c_int
+    lib.moe_dispatch_varlen.argtypes = [p, p, p, p, ctypes.POINTER(ctypes.c_int32), i32, p,
+                                        ctypes.POINTER(MoeDispatchView)]
+    lib.moe_dispatch_varlen.restype = ctypes.c_int
+    lib.moe_a2a_set_active_ranks.argtypes = [p, ctypes.c_uint32]
+    lib.moe_a2a_set_active_ranks.restype = ctypes.c_int
     lib.moe_a2a_set_reduction.argtypes = [p, i32]
     lib.moe_a2a_set_reduction.restype = ctypes.c_int
     lib.moe_a2a_status_string.argtypes = [ctypes.c_int]
@@ -119,6 +124,21 @@ def moe_dispatch(h, d_topk_ids: int, d_topk_w: int, d_x: int, tokens_per_rank: i
                            ctypes.c_void_p(d_x), tokens_per_rank, runtime_max_tokens_per_rank,
                            ctypes.c_void_p(stream), ctypes.byref(view))
     return st, view
+
+
+def moe_dispatch_varlen(h, d_topk_ids: int, d_topk_w: int, d_x: int, tokens_per_rank,
+                        runtime_max_tokens_per_rank: int, stream: int = 0):
+    """Returns (status, MoeDispatchView); tokens_per_rank is a host sequence."""
+    view = MoeDispatchView()
+    counts = (ctypes.c_int32 * len(tokens_per_rank))(*[int(c) for c in tokens_per_rank])
+    st = _lib.moe_dispatch_varlen(h, ctypes.c_void_p(d_topk_ids), ctypes.c_void_p(d_topk_w),
+                                  ctypes.c_void_p(d_x), counts, runtime_max_tokens_per_rank,
+                                  ctypes.c_void_p(stream), ctypes.byref(view))
+    return st, view
+
+
+def moe_a2a_set_active_ranks(h, active: int) -> int:
+    return _lib.moe_a2a_set_active_ranks(h, active)
 
 
 def moe_combine_payload(h) -> int:
@@ -194,7 +214,8 @@ class DispatchView:
     def __init__(self, owner, raw: MoeDispatchView):
         import torch
         R, K, E = owner.ep_size, owner.top_k, owner.num_experts
-        H, m, T, RP = owner.hidden, raw.plane_stride, raw.tokens_per_rank, raw.send_stride
+        H, m, RP = owner.hidden, raw.plane_stride, raw.send_stride
+        T = raw.token_stride
 
         def region(ptr, dtype, shape):
             n = 1
@@ -204,7 +225,8 @@ class DispatchView:
             nbytes = n * torch.empty((), dtype=dtype).element_size()
             return owner.workspace[off:off + nbytes].view(dtype).view(shape)
 
-        self.plane_stride, self.tokens_per_rank, self.send_stride = m, T, RP
+        self.plane_stride, self.send_stride = m, RP
+        self.tokens_per_rank, self.token_stride = raw.tokens_per_rank, T
         self.recv_x = region(raw.recv_x, torch.bfloat16, (R, R, m, H))
         self.recv_topk_ids = region(raw.recv_topk_ids, torch.int32, (R, R, m, K))
         self.recv_topk_w = region(raw.recv_topk_w, torch.float32, (R, R, m, K))
@@ -266,12 +288,36 @@ class MoeA2A:
                                self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_dispatch")
-        # The views depend only on (m, T): reuse them across calls.
-        key = (raw.plane_stride, raw.tokens_per_rank)
+        # The views depend only on (m, token stride): reuse them across calls.
+        key = (raw.plane_stride, raw.token_stride)
         if self.last_view is None or self._view_key != key:
             self.last_view = DispatchView(self, raw)
             self._view_key = key
         return self.last_view
+
+    def dispatch_varlen(self, topk_ids, topk_w, x, tokens_per_rank, stream=None) -> DispatchView:
+        """Per-rank token counts: inputs [R, m, ...], rows t < tokens_per_rank[s]."""
+        import torch
+        R, H, K = self.ep_size, self.hidden, self.top_k
+        m = topk_ids.shape[1]
+        self._check(topk_ids, torch.int32, (R, m, K), "topk_ids")
+        self._check(topk_w, torch.float32, (R, m, K), "topk_w")
+        self._check(x, torch.bfloat16, (R, m, H), "x")
+        st, raw = moe_dispatch_varlen(self.handle, _ptr(topk_ids), _ptr(topk_w), _ptr(x),
+                                      list(tokens_per_rank), m, self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_dispatch_varlen")
+        key = (raw.plane_stride, raw.token_stride)
+        if self.last_view is None or self._view_key != key:
+            self.last_view = DispatchView(self, raw)
+            self._view_key = key
+        return self.last_view
+
+    def set_active_ranks(self, active: int):
+        """Bit d set = logical rank d alive (default: all)."""
+        st = moe_a2a_set_active_ranks(self.handle, active)
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_a2a_set_active_ranks")
 
     def combine_payload(self):
         """bf16 [R, R, m, H] view of the in-workspace combine payload region."""
@@ -292,7 +338,7 @@ class MoeA2A:
             st = moe_combine(self.handle, 0, weighted, 0, 0, eps, 0, 0, self._stream(stream))
             raise MoeA2AError(st if st != MOE_OK else MOE_ERR_PHASE, "moe_combine")
         R, H = self.ep_size, self.hidden
-        T, m = self.last_view.tokens_per_rank, self.last_view.plane_stride
+        T, m = self.last_view.token_stride, self.last_view.plane_stride
         if expert_out is not None:
             self._check(expert_out, torch.bfloat16, (R, R, m, H), "expert_out")
         if residual is not None:

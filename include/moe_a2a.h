@@ -121,9 +121,11 @@ typedef struct moe_dispatch_view {
                                      ascending k, of the token's top-k weights
                                      whose expert lives on d (0 if not sent) */
     int32_t plane_stride;         /* m */
-    int32_t tokens_per_rank;      /* T */
+    int32_t tokens_per_rank;      /* T (moe_dispatch), -1 (moe_dispatch_varlen) */
     int32_t send_stride;          /* R rounded up to a multiple of 4 */
-    int32_t reserved;
+    int32_t token_stride;         /* rows per source rank of the token arrays
+                                     (x, send_slot, dest_weight, residual, out):
+                                     T, or m for moe_dispatch_varlen */
 } moe_dispatch_view_t;
 
 /* Bytes of device workspace a handle with this config needs (0 if the
@@ -155,6 +157,31 @@ int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
                  const void *d_x, int32_t tokens_per_rank,
                  int32_t runtime_max_tokens_per_rank, void *stream,
                  moe_dispatch_view_t *out_view);
+
+/* Dispatch with a token count per source rank (the pages' upstream API
+ * sizes each rank's batch separately; the readings: tokens past a rank's
+ * count are absent, exactly as if their expert ids were all -1, and nothing
+ * of theirs is read or written).
+ *   tokens_per_rank: HOST array of R counts, each 0..runtime_max.
+ *   d_topk_ids int32 [R][m][K], d_topk_w fp32 [R][m][K], d_x bf16 [R][m][H]:
+ *   the rows of source s are s*m + t for t < tokens_per_rank[s]; the rows
+ *   past a count are never read.
+ * Everything else as moe_dispatch; the following moe_combine reads residual
+ * and writes out / residual_out with the same [R][m][H] row layout and
+ * leaves the rows past each count untouched. */
+int moe_dispatch_varlen(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
+                        const void *d_x, const int32_t *tokens_per_rank,
+                        int32_t runtime_max_tokens_per_rank, void *stream,
+                        moe_dispatch_view_t *out_view);
+
+/* Mark which logical ranks take part ([IX] upstream combine's
+ * active_rank_mask; "dead-rank" marking).  Bit d set = rank d is alive.
+ * Dispatch treats an expert that lives on a dead rank exactly as an absent
+ * expert (id -1): no message, not counted, masked in the metadata rows;
+ * combine skips the messages of ranks that are dead at combine time (also
+ * those sent before the rank was marked dead).  Default: all ranks alive.
+ * Host-only; returns MOE_ERR_INVALID_ARG for bits at or above ep_size. */
+int moe_a2a_set_active_ranks(moe_a2a_t *h, uint32_t active);
 
 /* Device pointer to the combine payload region of the workspace ([IX]
  * get_combine_payload_tensor_in_workspace): bf16 [R][R][m][H] with the m of

@@ -141,3 +141,21 @@ def test_set_reduction_checks(abi):
     assert abi.moe_a2a_set_reduction(h, abi.MOE_REDUCE_BF16_TOPK_TREE) == abi.MOE_ERR_INVALID_ARG
     assert abi.moe_a2a_set_reduction(None, 0) == abi.MOE_ERR_INVALID_ARG
     abi.moe_a2a_destroy(h)
+
+
+def test_varlen_and_active_rank_checks(abi):
+    import ctypes
+    st, h = _handle(abi, cfg=(4, 64, 128, 16, 2))
+    A = 1 << 20
+    d = lambda counts, m: abi.moe_dispatch_varlen(h, A, A, A, counts, m, 0)[0]
+    assert d([1, 2, 3, 65], 64) == abi.MOE_ERR_CAPACITY        # a count above runtime max
+    assert d([1, -2, 3, 4], 64) == abi.MOE_ERR_INVALID_ARG
+    assert d([1, 2, 3, 4], 65) == abi.MOE_ERR_CAPACITY        # runtime max above max
+    assert d([1, 2, 3, 4], 0) == abi.MOE_ERR_INVALID_ARG
+    assert abi._lib.moe_dispatch_varlen(h, None, None, None, None, 8, None, None) == \
+        abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_phase(h) == 0
+    assert abi.moe_a2a_set_active_ranks(h, 0b1011) == abi.MOE_OK
+    assert abi.moe_a2a_set_active_ranks(h, 0b10000) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_set_active_ranks(None, 1) == abi.MOE_ERR_INVALID_ARG
+    abi.moe_a2a_destroy(h)
