@@ -424,3 +424,108 @@ void oracle_combine_topk_tree(int R, int T, int K, int E, int H, int m,
     free(hsum);
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 (OCP e4m3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no  */
+/* infinity, NaN = S.1111.111, largest finite 448) and per-token scaling     */
+/* ------------------------------------------------------------------------ */
+
+/* Widening is exact: exponent field 0 holds subnormals m * 2^-9. */
+float oracle_f32_from_fp8e4m3(uint8_t q)
+{
+    int sign = (q >> 7) & 1;
+    int e = (q >> 3) & 0xf;
+    int m = q & 7;
+    float v;
+    if (e == 0xf && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexpf((float)m, -9);
+    else
+        v = ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return sign ? -v : v;
+}
+
+/* Narrowing with round-to-nearest, ties-to-even, saturating to +-448
+ * (magnitudes above the largest finite value become 448); NaN stays NaN.
+ * Works on the binary32 bit pattern: the kept bits are the leading
+ * significand bits that fit the target exponent (3 below the leading 1 for
+ * normals, fewer for subnormals); the dropped bits are compared with one
+ * half of the kept unit. */
+uint8_t oracle_fp8e4m3_from_f32(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    uint8_t sign = (uint8_t)((bits >> 31) << 7);
+    uint32_t exp32 = (bits >> 23) & 0xffu;
+    uint32_t man32 = bits & 0x7fffffu;
+    if (exp32 == 0xffu && man32 != 0u)
+        return (uint8_t)(sign | 0x7f);
+    if (exp32 == 0xffu || fabsf(f) > 448.0f)
+        return (uint8_t)(sign | 0x7e);
+    if (exp32 == 0u)            /* binary32 zero or subnormal: below 2^-126 */
+        return sign;
+    /* value = 1.man32 * 2^(exp32 - 127); count in units of the target ulp */
+    int e = (int)exp32 - 127;
+    int ulp_exp = e >= -6 ? e - 3 : -9;          /* exponent of the kept unit */
+    uint64_t sig = (uint64_t)(0x800000u | man32); /* times 2^(e - 23) */
+    int shift = ulp_exp - (e - 23);              /* bits dropped */
+    if (shift >= 64)           /* far below half of the smallest subnormal */
+        return sign;
+    uint64_t kept = sig >> shift;
+    uint64_t dropped = sig & (((uint64_t)1 << shift) - 1);
+    uint64_t half = (uint64_t)1 << (shift - 1);
+    if (dropped > half || (dropped == half && (kept & 1u)))
+        kept += 1;
+    /* kept counts units of 2^ulp_exp: rebuild the code */
+    if (e < -6) {
+        /* subnormal units of 2^-9; 8 units is the smallest normal, code 0x08 */
+        return (uint8_t)(sign | (uint8_t)kept);
+    }
+    /* normal: kept in [8, 16]; 16 means the next binade */
+    int ee = e;
+    if (kept == 16) {
+        kept = 8;
+        ee += 1;
+    }
+    if (ee > 8 || (ee == 8 && kept > 14))
+        return (uint8_t)(sign | 0x7e);               /* saturate */
+    return (uint8_t)(sign | (uint8_t)(((ee + 7) << 3) | (uint8_t)(kept - 8)));
+}
+
+/* Per-token FP8 quantisation of bf16 rows [n][H]: amax = max_h |x_h|
+ * (binary32, exact), scale = amax / 448 (one binary32 division; 1 when the
+ * row is all zero), q_h = fp8(x_h / scale) (one binary32 division, then the
+ * narrowing above).  Dequantised value: f32(q_h) * scale. */
+void oracle_quantize_rows_fp8(long n, int H, const uint16_t *x, uint8_t *q, float *scale)
+{
+    for (long i = 0; i < n; ++i) {
+        const uint16_t *row = x + (size_t)i * H;
+        float amax = 0.0f;
+        for (int h = 0; h < H; ++h) {
+            float a = fabsf(oracle_f32_from_bf16(row[h]));
+            if (a > amax)
+                amax = a;
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[i] = sc;
+        for (int h = 0; h < H; ++h)
+            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(oracle_f32_from_bf16(row[h]) / sc);
+    }
+}
+
+/* The same for binary32 rows (the combine's output before narrowing). */
+void oracle_quantize_f32_rows_fp8(long n, int H, const float *x, uint8_t *q, float *scale)
+{
+    for (long i = 0; i < n; ++i) {
+        const float *row = x + (size_t)i * H;
+        float amax = 0.0f;
+        for (int h = 0; h < H; ++h)
+            if (fabsf(row[h]) > amax)
+                amax = fabsf(row[h]);
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[i] = sc;
+        for (int h = 0; h < H; ++h)
+            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(row[h] / sc);
+    }
+}
+

@@ -42,6 +42,14 @@ def _bind(handle):
     handle.oracle_combine_topk_tree.argtypes = ([c_int] * 6 + [p] * 5 + [c_float, p, c_long]
                                                 + [p] * 3)
     handle.oracle_combine_topk_tree.restype = None
+    handle.oracle_f32_from_fp8e4m3.argtypes = [ctypes.c_uint8]
+    handle.oracle_f32_from_fp8e4m3.restype = c_float
+    handle.oracle_fp8e4m3_from_f32.argtypes = [c_float]
+    handle.oracle_fp8e4m3_from_f32.restype = ctypes.c_uint8
+    handle.oracle_quantize_rows_fp8.argtypes = [c_long, c_int, p, p, p]
+    handle.oracle_quantize_rows_fp8.restype = None
+    handle.oracle_quantize_f32_rows_fp8.argtypes = [c_long, c_int, p, p, p]
+    handle.oracle_quantize_f32_rows_fp8.restype = None
     return handle
 
 
@@ -197,4 +205,43 @@ def combine_topk_tree(routing, topk_ids, num_experts: int, expert_out, residual=
                                _ptr(res), _ptr(gam), float(eps), _ptr(tok), n,
                                _ptr(out), _ptr(rout), _ptr(y))
     return dict(out=out, residual_out=rout, y=y)
+
+
+def fp8_bits(values, handle=None):
+    """binary32 values -> e4m3 codes (uint8), the oracle's narrowing."""
+    h = handle or lib()
+    flat = np.asarray(values, dtype=np.float32).ravel()
+    out = np.array([h.oracle_fp8e4m3_from_f32(float(v)) for v in flat], np.uint8)
+    return out.reshape(np.shape(values))
+
+
+def fp8_to_f32(codes, handle=None):
+    h = handle or lib()
+    flat = np.asarray(codes, dtype=np.uint8).ravel()
+    out = np.array([h.oracle_f32_from_fp8e4m3(int(c)) for c in flat], np.float32)
+    return out.reshape(np.shape(codes))
+
+
+def quantize_rows_fp8(x_bf16, handle=None):
+    """bf16 rows [..., H] -> (e4m3 codes [..., H], fp32 scales [...])."""
+    h = handle or lib()
+    xb = _need(x_bf16, np.uint16)
+    H = xb.shape[-1]
+    n = xb.size // H
+    q = np.empty(xb.shape, np.uint8)
+    sc = np.empty(xb.shape[:-1], np.float32)
+    h.oracle_quantize_rows_fp8(n, H, _ptr(xb), _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def quantize_f32_rows_fp8(x_f32, handle=None):
+    """binary32 rows [..., H] -> (e4m3 codes, fp32 scales)."""
+    h = handle or lib()
+    xf = _need(x_f32, np.float32)
+    H = xf.shape[-1]
+    n = xf.size // H
+    q = np.empty(xf.shape, np.uint8)
+    sc = np.empty(xf.shape[:-1], np.float32)
+    h.oracle_quantize_f32_rows_fp8(n, H, _ptr(xf), _ptr(q), _ptr(sc))
+    return q, sc
 

@@ -67,6 +67,15 @@ MUTANTS = {
     "tree_slots_in_rank_order": (
         "            int d = ids[k] / Epr;\n            int earlier = 0;",
         "            int d = (K - 1 - k) % R;\n            int earlier = 0;"),
+    "fp8_truncates": (
+        "    if (dropped > half || (dropped == half && (kept & 1u)))\n        kept += 1;",
+        "    if (0)\n        kept += 1;"),
+    "fp8_scale_for_wrong_format_max": (
+        "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;\n        scale[i] = sc;\n        for (int h = 0; h < H; ++h)\n            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(oracle_f32_from_bf16(",
+        "float sc = amax > 0.0f ? amax / 240.0f : 1.0f;\n        scale[i] = sc;\n        for (int h = 0; h < H; ++h)\n            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(oracle_f32_from_bf16("),
+    "fp8_overflow_to_nan": (
+        "    if (exp32 == 0xffu || fabsf(f) > 448.0f)\n        return (uint8_t)(sign | 0x7e);",
+        "    if (exp32 == 0xffu || fabsf(f) > 448.0f)\n        return (uint8_t)(sign | 0x7f);"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -97,6 +106,15 @@ class MutantOracle:
     def combine_topk_tree(self, *a, **k):
         return real.combine_topk_tree(*a, handle=self.h, **k)
 
+    def fp8_bits(self, v):
+        return real.fp8_bits(v, handle=self.h)
+
+    def fp8_to_f32(self, v):
+        return real.fp8_to_f32(v, handle=self.h)
+
+    def quantize_rows_fp8(self, x):
+        return real.quantize_rows_fp8(x, handle=self.h)
+
 
 PIN_TESTS = [
     (pins.test_bf16_rounding_matches_library_routine, {}),
@@ -118,6 +136,10 @@ PIN_TESTS = [
     (pins.test_probe_topk_tree_gives_the_pages_bf16_tree_value, {}),
     (pins.test_topk_tree_blanks_duplicate_ranks, {}),
     (pins.test_topk_tree_keeps_top_k_slot_order, {}),
+    (pins.test_fp8_narrowing_matches_library_routine, {}),
+    (pins.test_fp8_saturates_and_keeps_nan, {}),
+    (pins.test_fp8_row_scaling_closed_forms, {}),
+    (pins.test_fp8_round_trip_within_format_bound, {}),
 ]
 
 

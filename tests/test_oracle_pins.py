@@ -563,3 +563,58 @@ def test_topk_tree_fused_epilogue_matches_rank_sum_when_exact(oracle):
     b = oracle.combine(r, eo, False, res, gam, 1e-6)
     assert np.array_equal(a["residual_out"], b["residual_out"])
     assert np.array_equal(a["out"], b["out"])
+
+
+# --------------------------------------------------------------------------
+# FP8 (e4m3) payloads: conversion pinned to a library routine, scaling to
+# closed forms and the format's error bound
+# --------------------------------------------------------------------------
+
+def test_fp8_narrowing_matches_library_routine(oracle):
+    import torch
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([rng.standard_normal(20000).astype(np.float32) * 60,
+                           rng.standard_normal(4000).astype(np.float32) * 1e-2,
+                           (rng.random(4000).astype(np.float32) - 0.5) * 2 ** -5,
+                           np.array([448, -448, 0, -0.0, 2 ** -9, 2 ** -10, 3 * 2 ** -11,
+                                     2 ** -6, 15 * 2 ** -10, 0.5, 0.5625, 0.53125],
+                                    np.float32)])
+    vals = vals[np.abs(vals) <= 448]
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.fp8_bits(vals), ref)
+    codes = np.arange(256, dtype=np.uint8)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    got = oracle.fp8_to_f32(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(dec))
+    assert np.array_equal(got[~np.isnan(got)], dec[~np.isnan(dec)])
+
+
+def test_fp8_saturates_and_keeps_nan(oracle):
+    codes = oracle.fp8_bits(np.array([449.0, 1e30, -600.0, np.inf, np.nan], np.float32))
+    assert list(codes[:4]) == [0x7E, 0x7E, 0xFE, 0x7E]
+    assert codes[4] & 0x7F == 0x7F
+
+
+def test_fp8_row_scaling_closed_forms(oracle):
+    # amax 448: scale 1, codes are the plain narrowing; an all-zero row has
+    # scale 1 and zero codes; any row's scale is amax / 448 in binary32
+    r = np.array([448.0, -3.0, 0.5, 2 ** -9, 0.0, 100.0, -448.0, 7.0], np.float32)
+    q, sc = oracle.quantize_rows_fp8(bits(np.stack([r, np.zeros(8, np.float32)])))
+    assert sc[0] == 1.0 and np.array_equal(q[0], oracle.fp8_bits(r))
+    assert sc[1] == 1.0 and not q[1].any()
+    x = bits(np.random.default_rng(6).standard_normal((5, 64)).astype(np.float32))
+    q, sc = oracle.quantize_rows_fp8(x)
+    amax = np.abs(f32(x)).max(axis=1)
+    assert np.array_equal(sc, (amax / np.float32(448)).astype(np.float32))
+    assert (np.abs(oracle.fp8_to_f32(q)).max(axis=1) == 448.0).all()
+
+
+def test_fp8_round_trip_within_format_bound(oracle):
+    # e4m3 keeps 3 mantissa bits: a relative half-unit of 2^-4 for normals,
+    # an absolute half-unit of 2^-10 (times the scale) for subnormals
+    x = bits(np.random.default_rng(7).standard_normal((64, 256)).astype(np.float32) *
+             np.logspace(-3, 2, 64, dtype=np.float32)[:, None])
+    q, sc = oracle.quantize_rows_fp8(x)
+    back = oracle.fp8_to_f32(q) * sc[:, None]
+    xv = f32(x)
+    assert (np.abs(back - xv) <= 2.0 ** -4 * np.abs(xv) + 2.0 ** -10 * sc[:, None] * 1.0001).all()
