@@ -53,6 +53,9 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 payloads: e4m3 dispatch rows with a per-token scale and an "
+                         "e4m3 combine output with a per-token scale (needs hidden %% 16 == 0)")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of each phase's C-ABI call instead of "
                          "direct calls (measured no faster on GB300)")
@@ -84,11 +87,14 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def phase_bytes(w, recv_rows):
-    """Algorithmic payload bytes of one call of each phase (rows of 2H bytes)."""
+def phase_bytes(w, recv_rows, fp8=False):
+    """Algorithmic payload bytes of one call of each phase: rows of 2H bytes
+    (bf16), or H bytes plus a 4-byte scale (e4m3) for the received rows and
+    the combine output in the FP8 variant."""
     N, row = w.tokens, 2 * w.hidden
-    dispatch = (N + recv_rows) * row
-    combine = recv_rows * row + N * row            # messages read, output written
+    row8 = w.hidden + 4
+    dispatch = N * row + recv_rows * (row8 if fp8 else row)
+    combine = recv_rows * row + N * (row8 if fp8 else row)  # messages read, output written
     if w.fused:
         combine += 2 * N * row + row               # residual read, residual_out, gamma
     return dispatch, combine
@@ -267,7 +273,7 @@ def run_gpu(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
     from combine_topk_ids_rank_gb300 import synth
-    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -284,18 +290,32 @@ def run_gpu(args, w, rank, world, local_rank):
     ids, wts, x = ids_h.to(dev), wts_h.to(dev), x_h.to(dev)
     res = res_h.to(dev) if w.fused else None
     gam = gam_h.to(dev)
+    fp8 = args.fp8
     out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
     rout = torch.empty_like(out) if w.fused else None
+    out8 = torch.empty((R, T, H), dtype=torch.float8_e4m3fn, device=dev) if fp8 else None
+    osc = torch.empty((R, T), dtype=torch.float32, device=dev) if fp8 else None
+    identity = w.identity_experts and not fp8      # e4m3 rows are not a bf16 payload
 
     a2a = MoeA2A(R, w.max_tokens, H, E, K, dev)
+    if fp8:
+        a2a.set_recv_format(MOE_FORMAT_FP8_E4M3)
     view = a2a.dispatch(ids, wts, x, w.runtime_max)
-    if not w.identity_experts:
+    if not identity:
         gd = torch.Generator(device=dev).manual_seed(args.seed + 1)
         pay = a2a.combine_payload()
         pay.copy_(torch.randn(pay.shape, generator=gd, device=dev, dtype=torch.float32)
                   .to(torch.bfloat16))
-    eo = view.recv_x if w.identity_experts else None
-    a2a.combine(eo, w.weighted, res, gam, w.eps, out, rout)
+    eo = view.recv_x if identity else None
+
+    def combine_into(res_, outs):
+        if fp8:
+            a2a.combine_fp8(eo, w.weighted, res_, gam, w.eps, outs[0], outs[1], outs[2])
+        else:
+            a2a.combine(eo, w.weighted, res_, gam, w.eps, outs[0], outs[1])
+
+    outs_main = [out8, osc, rout] if fp8 else [out, rout]
+    combine_into(res, outs_main)
     torch.cuda.synchronize()
     recv_rows = int(view.recv_counts.sum().item())
     st, flags = a2a.get_error()
@@ -306,7 +326,7 @@ def run_gpu(args, w, rank, world, local_rank):
         a2a.dispatch(ids, wts, x, w.runtime_max)
 
     def run_combine():
-        a2a.combine(eo, w.weighted, res, gam, w.eps, out, rout)
+        combine_into(res, outs_main)
 
     if args.graph:
         # Capture each phase once (the same C-ABI calls, kernels only) and
@@ -341,6 +361,9 @@ def run_gpu(args, w, rank, world, local_rank):
 
     flush = None
     cfg = config_dict(w, recv_rows)
+    if fp8:
+        cfg["payload"] = ("e4m3 dispatch rows + fp32 per-token scale; combine output e4m3 + "
+                          "fp32 per-token scale (residual_out bf16)")
     if "flushed" in cfg["l2"]:
         # write a buffer twice the size of L2, then read another one, so the
         # timed kernels find L2 holding clean, unrelated lines
@@ -386,7 +409,7 @@ def run_gpu(args, w, rank, world, local_rank):
     if st != 0:
         raise RuntimeError("device flag set during the timed region: %d %#x" % (st, flags))
 
-    d_bytes, c_bytes = phase_bytes(w, recv_rows)
+    d_bytes, c_bytes = phase_bytes(w, recv_rows, fp8)
     peak, peak_kind = measured_peak()
     d_avg, c_avg = statistics.fmean(disp_ms), statistics.fmean(comb_ms)
 
@@ -398,7 +421,8 @@ def run_gpu(args, w, rank, world, local_rank):
         "dispatch": {"ms_avg": d_avg, "ms_p50": pct(disp_ms, 0.5), "ms_p10": pct(disp_ms, 0.1),
                      "ms_p90": pct(disp_ms, 0.9), "bytes": d_bytes,
                      "gbs": d_bytes / d_avg / 1e6, "frac": d_bytes / d_avg / 1e6 / peak,
-                     "kernels": ["route_count", "route_scan", "dispatch_rows"]},
+                     "kernels": ["route_count", "route_scan",
+                                 "dispatch_fp8" if fp8 else "dispatch_rows"]},
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
                     "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
                     "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
@@ -417,11 +441,13 @@ def run_gpu(args, w, rank, world, local_rank):
         hids, hw, hx = pin(ids_h), pin(wts_h), pin(x_h)
         hres = pin(res_h) if w.fused else None
         hin = [t for t in (hids, hw, hx, hres) if t is not None]
-        hout = [[torch.empty((R, T, H), dtype=torch.bfloat16).pin_memory()
-                 for _ in range(2 if w.fused else 1)] for _ in range(2)]
+        specs = [((R, T, H), torch.float8_e4m3fn), ((R, T), torch.float32)] if fp8 else \
+            [((R, T, H), torch.bfloat16)]
+        if w.fused:
+            specs.append(((R, T, H), torch.bfloat16))
+        hout = [[torch.empty(sh, dtype=dt).pin_memory() for sh, dt in specs] for _ in range(2)]
         din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(2)]
-        dout = [[torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
-                 for _ in range(2 if w.fused else 1)] for _ in range(2)]
+        dout = [[torch.empty(sh, dtype=dt, device=dev) for sh, dt in specs] for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in hin)
         d2h = sum(t.numel() * t.element_size() for t in hout[0])
         compute = torch.cuda.current_stream(dev)
@@ -445,8 +471,9 @@ def run_gpu(args, w, rank, world, local_rank):
             d_ids, d_w, d_x = din[b][0], din[b][1], din[b][2]
             d_res = din[b][3] if w.fused else None
             a2a.dispatch(d_ids, d_w, d_x, w.runtime_max)
-            a2a.combine(eo, w.weighted, d_res, gam, w.eps, dout[b][0],
-                        dout[b][1] if w.fused else None)
+            o = dout[b]
+            combine_into(d_res, [o[0], o[1], o[2] if w.fused else None] if fp8
+                         else [o[0], o[1] if w.fused else None])
             in_free[b].record(compute)
             out_ready[b].record(compute)
             with torch.cuda.stream(down):
@@ -484,7 +511,7 @@ def run_gpu(args, w, rank, world, local_rank):
         try:
             with open(prof) as f:
                 tr = json.load(f)
-            ent = tr.get(w.name, {}).get("combine")
+            ent = tr.get(w.name + ("-fp8" if fp8 else ""), {}).get("combine")
             if ent and ent.get("source_sha1") == source_sha1(ent.get("source", "combine_ring.cu")):
                 traffic = ent["dram_bytes_per_launch"]
         except (OSError, ValueError, KeyError):

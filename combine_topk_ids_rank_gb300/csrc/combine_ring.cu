@@ -32,12 +32,14 @@
 // the producer waits (bounded) for its copies still landing before exit.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "fp8.cuh"
 
 #include "moe_a2a.h"
 
 #include <cuda_bf16.h>
 
 #include <cstdlib>
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -59,7 +61,7 @@ struct Ring {
     uint8_t *rows;
     uint64_t *full, *empty, *dfull, *dempty, *rbar;
     TokenDesc *desc;
-    float *red;      // [2][kMaxConsumerWarps]
+    float *red;      // [2 parities][2 values][kMaxConsumerWarps]
 };
 
 __host__ __device__ inline size_t ring_stride(int row_bytes) {
@@ -68,7 +70,7 @@ __host__ __device__ inline size_t ring_stride(int row_bytes) {
 
 __host__ __device__ inline size_t ring_smem_bytes(int row_bytes, int slots) {
     return ring_stride(row_bytes) * slots + sizeof(uint64_t) * (2 * slots + 2 * kDesc + 2) +
-           sizeof(TokenDesc) * kDesc + sizeof(float) * 2 * kMaxConsumerWarps;
+           sizeof(TokenDesc) * kDesc + sizeof(float) * 4 * kMaxConsumerWarps;
 }
 
 __device__ inline Ring carve(uint8_t *smem, int row_bytes, int slots) {
@@ -222,7 +224,7 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
 
 // ---- consumer warps ---------------------------------------------------------
 
-template <int VPT, bool WEIGHTED, bool FUSED>
+template <int VPT, bool WEIGHTED, bool FUSED, bool OUT8>
 __device__ void consume(const CombineParams &p, const Ring &r, int slots, int ncw) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nct = ncw * 32;
@@ -231,8 +233,38 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
     uint4 *out = reinterpret_cast<uint4 *>(p.out);
     uint4 *rout = reinterpret_cast<uint4 *>(p.residual_out);
 
-    uint32_t q = 0, nfused = 0;
+    uint32_t q = 0, nred = 0;
     bool ok = true;
+    // Over the CTA's consumer threads: the sum of `a` and, if TWO, the max of
+    // `b` -- warp shuffles, then one slot per warp and value in shared
+    // memory, synchronised by an mbarrier (two slot sets / barriers used
+    // alternately).
+    auto block_reduce = [&](auto two, float a, float b, float &ra, float &rb) -> bool {
+        constexpr bool TWO = decltype(two)::value;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(kFull, a, o);
+            if (TWO) b = fmaxf(b, __shfl_xor_sync(kFull, b, o));
+        }
+        float *red = r.red + (nred & 1) * 2 * kMaxConsumerWarps;
+        uint64_t *bar = &r.rbar[nred & 1];
+        if (lane == 0) {
+            red[warp] = a;
+            if (TWO) red[kMaxConsumerWarps + warp] = b;
+            mbar_arrive(bar);
+        }
+        if (!ptx::mbar_wait_bounded(bar, (nred >> 1) & 1u, kWaitLimit)) return false;
+        ++nred;
+        ra = 0.0f;
+        rb = 0.0f;
+        for (int i = 0; i < ncw; ++i) {
+            ra += red[i];
+            if (TWO) rb = fmaxf(rb, red[kMaxConsumerWarps + i]);
+        }
+        return true;
+    };
+    using One = std::false_type;
+    using Two = std::true_type;
     for (long long i = blockIdx.x, j = 0; i < p.tokens; i += gridDim.x, ++j) {
         int s, t;
         token_of(p.map, p.R, i, s, t);
@@ -290,7 +322,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
         if (lane == 0) mbar_arrive(&r.dempty[ds]);
 
         const long long row0 = tok * p.H8;
-        if (!FUSED) {
+        if (!FUSED && !OUT8) {
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 const int c = tid + v * nct;
@@ -299,55 +331,99 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
             continue;
         }
 
-        float ss = 0.0f;
+        float amax = 0.0f;  // OUT8: max |value quantised| of the row
+        if (FUSED) {
+            // hsum = acc + residual (fp32); residual_out = bf16(hsum);
+            // y = hsum * rsqrt(mean(hsum^2) + eps) * gamma.  With FP8 output
+            // the kernel forms y = inv * (hsum * gamma): inv > 0 and
+            // rounding is monotone, so max|y| = inv * max|hsum * gamma|
+            // exactly and one reduction serves both the mean and the amax.
+            float ss = 0.0f, gmax = 0.0f;
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const uint32_t u[4] = {rv[v].x, rv[v].y, rv[v].z, rv[v].w};
+            for (int v = 0; v < VPT; ++v) {
+                const uint32_t u[4] = {rv[v].x, rv[v].y, rv[v].z, rv[v].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[v][2 * i] = __fadd_rn(acc[v][2 * i], lo_f(u[i]));
-                acc[v][2 * i + 1] = __fadd_rn(acc[v][2 * i + 1], hi_f(u[i]));
+                for (int i = 0; i < 4; ++i) {
+                    acc[v][2 * i] = __fadd_rn(acc[v][2 * i], lo_f(u[i]));
+                    acc[v][2 * i + 1] = __fadd_rn(acc[v][2 * i + 1], hi_f(u[i]));
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss += acc[v][e] * acc[v][e];
+                const int c = tid + v * nct;
+                if (rout != nullptr && c < p.H8) __stcs(rout + row0 + c, pack8(acc[v]));
+                if (OUT8 && c < p.H8) {
+                    const uint4 g = __ldg(gam + c);
+                    const uint32_t gu[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[v][2 * i] = __fmul_rn(acc[v][2 * i], lo_f(gu[i]));
+                        acc[v][2 * i + 1] = __fmul_rn(acc[v][2 * i + 1], hi_f(gu[i]));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gmax = fmaxf(gmax, fabsf(acc[v][e]));
+                }
             }
+            float total, gtot;
+            if (!block_reduce(std::integral_constant<bool, OUT8>(), ss, gmax, total, gtot)) {
+                ok = false;
+                break;
+            }
+            const float inv = rsqrtf(total / (float)p.H + p.eps);
+            if (OUT8) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss += acc[v][e] * acc[v][e];
-            const int c = tid + v * nct;
-            if (rout != nullptr && c < p.H8) __stcs(rout + row0 + c, pack8(acc[v]));
-        }
+                for (int v = 0; v < VPT; ++v)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-        const int par = nfused & 1;
-        if (lane == 0) {
-            r.red[par * kMaxConsumerWarps + warp] = ss;
-            mbar_arrive(&r.rbar[par]);
+                    for (int e = 0; e < 8; ++e) acc[v][e] = __fmul_rn(inv, acc[v][e]);
+                amax = __fmul_rn(inv, gtot);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    const int c = tid + v * nct;
+                    if (c >= p.H8) continue;
+                    const uint4 g = __ldg(gam + c);
+                    const uint32_t u[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[v][2 * i] = acc[v][2 * i] * inv * lo_f(u[i]);
+                        acc[v][2 * i + 1] = acc[v][2 * i + 1] * inv * hi_f(u[i]);
+                    }
+                    __stcs(out + row0 + c, pack8(acc[v]));
+                }
+                continue;
+            }
+        } else {
+            // FP8 output of the plain sum: amax of the fp32 accumulator
+            float m = 0.0f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = tid + v * nct;
+                if (c < p.H8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(acc[v][e]));
+            }
+            float unused;
+            if (!block_reduce(Two(), 0.0f, m, unused, amax)) {
+                ok = false;
+                break;
+            }
         }
-        if (!ptx::mbar_wait_bounded(&r.rbar[par], (nfused >> 1) & 1u, kWaitLimit)) {
-            ok = false;
-            break;
-        }
-        ++nfused;
-        float total = 0.0f;
-        for (int i = 0; i < ncw; ++i) total += r.red[par * kMaxConsumerWarps + i];
-        const float inv = rsqrtf(total / (float)p.H + p.eps);
 
+        // FP8 output: per-token scale amax / 448, e4m3 codes of value / scale
+        const fp8::RowScale rs = fp8::row_scale(amax);
+        uint2 *out8 = reinterpret_cast<uint2 *>(p.out8 + tok * (long long)p.H);
+        uint2 codes[VPT];
+        fp8::quantize_row<VPT>(acc, rs, codes);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = tid + v * nct;
-            if (c >= p.H8) continue;
-            const uint4 g = __ldg(gam + c);
-            const uint32_t u[4] = {g.x, g.y, g.z, g.w};
-            float y[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                y[2 * i] = acc[v][2 * i] * inv * lo_f(u[i]);
-                y[2 * i + 1] = acc[v][2 * i + 1] * inv * hi_f(u[i]);
-            }
-            __stcs(out + row0 + c, pack8(y));
+            if (c < p.H8) __stcs(out8 + c, codes[v]);
         }
+        if (tid == 0) p.out_scale[tok] = rs.s;
     }
     if (!ok && lane == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
 }
 
-template <int VPT, bool WEIGHTED, bool FUSED>
+template <int VPT, bool WEIGHTED, bool FUSED, bool OUT8>
 __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
     combine_ring_kernel(const CombineParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -372,78 +448,68 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
     if ((int)(threadIdx.x >> 5) == ncw)
         produce<WEIGHTED, FUSED>(p, r, slots);
     else
-        consume<VPT, WEIGHTED, FUSED>(p, r, slots, ncw);
+        consume<VPT, WEIGHTED, FUSED, OUT8>(p, r, slots, ncw);
 }
 
-template <int VPT, bool W, bool F>
+template <int VPT, bool W, bool F, bool O>
 cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStream_t st) {
     long long grid = shape.grid;
     if (grid > p.tokens) grid = p.tokens;
     if (grid < 1) return cudaSuccess;
-    combine_ring_kernel<VPT, W, F><<<(unsigned)grid, shape.block, shape.smem, st>>>(p);
+    combine_ring_kernel<VPT, W, F, O><<<(unsigned)grid, shape.block, shape.smem, st>>>(p);
     return cudaGetLastError();
 }
 
-template <int VPT, bool W, bool F>
-cudaError_t set_smem(size_t smem) {
-    return cudaFuncSetAttribute(combine_ring_kernel<VPT, W, F>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-}
+// One of three actions on the instantiation selected by (vpt, w, f, o):
+// allow its dynamic shared memory, query its occupancy, or launch it.
+enum class Act { Prepare, Occupancy, Launch };
 
-template <int VPT>
-cudaError_t by_flags(bool w, bool f, const CombineParams *p, const LaunchShape &shape,
-                     cudaStream_t st) {
-    if (p == nullptr) {  // preparation: allow the dynamic shared memory
-        if (w && f) return set_smem<VPT, true, true>(shape.smem);
-        if (w) return set_smem<VPT, true, false>(shape.smem);
-        if (f) return set_smem<VPT, false, true>(shape.smem);
-        return set_smem<VPT, false, false>(shape.smem);
-    }
-    if (w && f) return launch_t<VPT, true, true>(*p, shape, st);
-    if (w) return launch_t<VPT, true, false>(*p, shape, st);
-    if (f) return launch_t<VPT, false, true>(*p, shape, st);
-    return launch_t<VPT, false, false>(*p, shape, st);
-}
-
-template <int VPT>
-cudaError_t occ_flags(bool w, bool f, int block, size_t smem, int *per_sm) {
-    if (w && f)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            per_sm, combine_ring_kernel<VPT, true, true>, block, smem);
-    if (w)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            per_sm, combine_ring_kernel<VPT, true, false>, block, smem);
-    if (f)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            per_sm, combine_ring_kernel<VPT, false, true>, block, smem);
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        per_sm, combine_ring_kernel<VPT, false, false>, block, smem);
-}
-
-cudaError_t occupancy(int vpt, bool w, bool f, int block, size_t smem, int *per_sm) {
-    switch (vpt) {
-        case 1: return occ_flags<1>(w, f, block, smem, per_sm);
-        case 2: return occ_flags<2>(w, f, block, smem, per_sm);
-        case 4: return occ_flags<4>(w, f, block, smem, per_sm);
-        case 8: return occ_flags<8>(w, f, block, smem, per_sm);
-        default: return cudaErrorInvalidValue;
+template <int VPT, bool W, bool F, bool O>
+cudaError_t act_t(Act a, const CombineParams *p, const LaunchShape &shape, cudaStream_t st,
+                  int *per_sm) {
+    switch (a) {
+        case Act::Prepare:
+            return cudaFuncSetAttribute(combine_ring_kernel<VPT, W, F, O>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)shape.smem);
+        case Act::Occupancy:
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                per_sm, combine_ring_kernel<VPT, W, F, O>, shape.block, shape.smem);
+        default:
+            return launch_t<VPT, W, F, O>(*p, shape, st);
     }
 }
 
-cudaError_t by_vpt(int vpt, bool w, bool f, const CombineParams *p, const LaunchShape &shape,
-                   cudaStream_t st) {
+template <int VPT>
+cudaError_t by_flags(Act a, bool w, bool f, bool o, const CombineParams *p,
+                     const LaunchShape &shape, cudaStream_t st, int *per_sm) {
+    const int k = (w ? 4 : 0) + (f ? 2 : 0) + (o ? 1 : 0);
+    switch (k) {
+        case 0: return act_t<VPT, false, false, false>(a, p, shape, st, per_sm);
+        case 1: return act_t<VPT, false, false, true>(a, p, shape, st, per_sm);
+        case 2: return act_t<VPT, false, true, false>(a, p, shape, st, per_sm);
+        case 3: return act_t<VPT, false, true, true>(a, p, shape, st, per_sm);
+        case 4: return act_t<VPT, true, false, false>(a, p, shape, st, per_sm);
+        case 5: return act_t<VPT, true, false, true>(a, p, shape, st, per_sm);
+        case 6: return act_t<VPT, true, true, false>(a, p, shape, st, per_sm);
+        default: return act_t<VPT, true, true, true>(a, p, shape, st, per_sm);
+    }
+}
+
+cudaError_t by_vpt(Act a, int vpt, bool w, bool f, bool o, const CombineParams *p,
+                   const LaunchShape &shape, cudaStream_t st, int *per_sm) {
     switch (vpt) {
-        case 1: return by_flags<1>(w, f, p, shape, st);
-        case 2: return by_flags<2>(w, f, p, shape, st);
-        case 4: return by_flags<4>(w, f, p, shape, st);
-        case 8: return by_flags<8>(w, f, p, shape, st);
+        case 1: return by_flags<1>(a, w, f, o, p, shape, st, per_sm);
+        case 2: return by_flags<2>(a, w, f, o, p, shape, st, per_sm);
+        case 4: return by_flags<4>(a, w, f, o, p, shape, st, per_sm);
+        case 8: return by_flags<8>(a, w, f, o, p, shape, st, per_sm);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, int num_sms,
+cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, int num_sms,
                                  LaunchShape *shape, int *vpt, int *slots) {
     const int H8 = H / 8;
     int v = 1;
@@ -471,18 +537,18 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, int num_sms,
     *slots = s;
     shape->block = (ncw + 1) * 32;
     shape->smem = ring_smem_bytes(2 * H, s);
-    err = by_vpt(v, weighted, fused, nullptr, *shape, nullptr);
+    err = by_vpt(Act::Prepare, v, weighted, fused, out8, nullptr, *shape, nullptr, nullptr);
     if (err != cudaSuccess) return err;
     int per_sm = 1;
-    err = occupancy(v, weighted, fused, shape->block, shape->smem, &per_sm);
+    err = by_vpt(Act::Occupancy, v, weighted, fused, out8, nullptr, *shape, nullptr, &per_sm);
     if (err != cudaSuccess) return err;
     shape->grid = num_sms * (per_sm < 1 ? 1 : per_sm);
     return cudaSuccess;
 }
 
-cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, int vpt,
-                                const LaunchShape &shape, cudaStream_t st) {
-    return by_vpt(vpt, weighted, fused, &p, shape, st);
+cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, bool out8,
+                                int vpt, const LaunchShape &shape, cudaStream_t st) {
+    return by_vpt(Act::Launch, vpt, weighted, fused, out8, &p, shape, st, nullptr);
 }
 
 }  // namespace moe

@@ -1,0 +1,280 @@
+// dispatch_fp8.cu -- dispatch with an FP8 row payload and a per-token scale,
+// and the standalone FP8 row quantiser.
+//
+// Operation (InferenceX PR #2450, "CollectiveX: add FlashInfer one-sided
+// NVLink EP for the GB SKUs", "The adapter": an FP8 dispatch carries a
+// scale payload next to the row and is validated against the cast round
+// trip).  Readings: OCP e4m3, per-token scale = amax_h |x_h| / 448 (binary32
+// division; 1 for an all-zero row), q_h = e4m3_rn_satfinite(x_h / scale)
+// (binary32 quotient):
+//   recv_x8[d][s][slot(s,t,d)][:] = q(x[s][t]),  recv_scale[d][s][slot] = scale
+// for every destination of the token; padding never written.
+//
+// GB300 design: persistent CTAs of 256 threads, one token row at a time.
+// One thread keeps the next few bf16 rows of the CTA in flight with 1-D bulk
+// copies into a shared-memory ring (mbarrier completion, bounded waits);
+// each thread takes VPT 16-byte vectors of the row into registers, the
+// row's amax is a warp shuffle + one cross-warp step (the only CTA barrier
+// per token, which also frees the stage for the next copy), and every
+// thread quantises its own vectors (fp8.cuh: one reciprocal per row,
+// FMA-refined quotients) and writes 8 code bytes per vector straight to each
+// destination row -- consecutive threads write consecutive 8-byte pieces,
+// so each warp store covers 256 contiguous bytes.  The row is read once and
+// written once per destination at half the bf16 bytes.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "fp8.cuh"
+
+#include "moe_a2a.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kThreads = 256;          // at most; the launch fits the row
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        f[2 * k] = lo_f(u[k]);
+        f[2 * k + 1] = hi_f(u[k]);
+    }
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const DispatchFp8Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];  // p.stages bf16 rows
+    __shared__ uint64_t full[kMaxStages];
+    __shared__ int32_t slots[2][kMaxRanks];
+    __shared__ float red[2][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nt = blockDim.x, nw = nt >> 5;
+    const int S = p.stages;
+    const uint32_t row_bytes = (uint32_t)p.H * 2;
+    const size_t stride = ((size_t)row_bytes + 127) / 128 * 128;
+
+    // Token k of this CTA is i = blockIdx.x + k * gridDim.x; its row goes
+    // to stage k % S.  Thread 0 keeps S rows in flight.
+    auto issue = [&](long long k) {
+        const long long i = blockIdx.x + k * (long long)gridDim.x;
+        if (i >= p.tokens) return;
+        int s, t;
+        token_of(p.map, p.R, i, s, t);
+        const int b = (int)(k % S);
+        ptx::mbar_arrive_expect_tx(&full[b], row_bytes);
+        ptx::bulk_g2s(smem + b * stride, p.x + ((long long)s * p.map.stride + t) * p.H,
+                      row_bytes, &full[b]);
+    };
+    if (tid == 0) {
+        for (int b = 0; b < S; ++b) ptx::mbar_init(&full[b], 1);
+        ptx::fence_mbar_init();
+        for (int k = 0; k < S; ++k) issue(k);  // inputs: before the routing pass ends
+    }
+    __syncthreads();
+    ptx::grid_dependency_wait();
+
+    bool ok = true;
+    long long k = 0;
+    for (long long i = blockIdx.x; i < p.tokens; i += gridDim.x, ++k) {
+        const int par = (int)(k & 1);
+        int s, t;
+        token_of(p.map, p.R, i, s, t);
+        const long long tok = (long long)s * p.map.stride + t;
+        if (tid < p.R) {
+            int sl = p.send_slot[tok * p.RP + tid];
+            if (sl >= p.m) {  // guard: never expected from the routing pass
+                atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                sl = -1;
+            }
+            slots[par][tid] = sl;
+        }
+        const int b = (int)(k % S);
+        ok = ptx::mbar_wait_bounded(&full[b], (uint32_t)((k / S) & 1), kWaitLimit);
+        uint4 cur[VPT];
+        const uint4 *row = reinterpret_cast<const uint4 *>(smem + b * stride);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = tid + j * nt;
+            cur[j] = (ok && c < p.H8) ? row[c] : make_uint4(0, 0, 0, 0);
+            const uint32_t u[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                amax = fmaxf(amax, fmaxf(fabsf(lo_f(u[e])), fabsf(hi_f(u[e]))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        if (lane == 0) red[par][warp] = amax;
+        // One barrier per token.  It also releases stage b (every thread has
+        // its vectors in registers) and makes the wait outcome collective.
+        // red[] and slots[] alternate by token parity: no thread reaches the
+        // barrier of token k+2 before all have passed that of k+1, i.e.
+        // finished token k.
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
+        if (tid == 0) {
+            ptx::fence_proxy_async_smem();
+            issue(k + S);
+        }
+        amax = red[par][0];
+        for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[par][w]);
+        const fp8::RowScale rs = fp8::row_scale(amax);
+
+        float f[VPT][8];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) unpack8(cur[j], f[j]);
+        uint2 q[VPT];
+        fp8::quantize_row<VPT>(f, rs, q);
+        for (int d = 0; d < p.R; ++d) {
+            const int sl = slots[par][d];
+            if (sl < 0) continue;
+            const long long dst_row = ((long long)d * p.R + s) * p.m + sl;
+            uint2 *dst = reinterpret_cast<uint2 *>(p.recv_x8 + dst_row * p.H);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int c = tid + j * nt;
+                if (c < p.H8) __stcs(dst + c, q[j]);
+            }
+            if (tid == 0) p.recv_scale[dst_row] = rs.s;
+        }
+    }
+    if (!ok && tid == 0) {
+        atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+        // let the copies in flight land before the shared memory goes away
+        for (long long j = k; j < k + S; ++j)
+            if (blockIdx.x + j * (long long)gridDim.x < p.tokens)
+                ptx::mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), kWaitLimit);
+    }
+}
+
+// fp32 rows -> e4m3 codes + per-row scale; one CTA per row at a time.
+template <int VPT>
+__global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *x, long long rows,
+                                                                 int H, uint8_t *q, float *scale) {
+    __shared__ float red[2][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H8 = H / 8, nt = blockDim.x, nw = nt >> 5;
+    int par = 0;
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x, par ^= 1) {
+        const float4 *src = reinterpret_cast<const float4 *>(x + r * (long long)H);
+        float v[VPT][8];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = tid + j * nt;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (c < H8) {
+                a = __ldcs(src + 2 * c);
+                b = __ldcs(src + 2 * c + 1);
+            }
+            v[j][0] = a.x, v[j][1] = a.y, v[j][2] = a.z, v[j][3] = a.w;
+            v[j][4] = b.x, v[j][5] = b.y, v[j][6] = b.z, v[j][7] = b.w;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[j][e]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        if (lane == 0) red[par][warp] = amax;
+        __syncthreads();
+        amax = red[par][0];
+        for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[par][w]);
+        const fp8::RowScale rs = fp8::row_scale(amax);
+        uint2 *dst = reinterpret_cast<uint2 *>(q + r * (long long)H);
+        uint2 codes[VPT];
+        fp8::quantize_row<VPT>(v, rs, codes);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = tid + j * nt;
+            if (c < H8) __stcs(dst + c, codes[j]);
+        }
+        if (tid == 0) scale[r] = rs.s;
+    }
+}
+
+// Threads per CTA: the fewest whole warps that cover the row with VPT
+// vectors each (224 at H = 7168, VPT = 4), so no thread idles at the tail.
+int fit_threads(int H8, int VPT) { return ((H8 + VPT - 1) / VPT + 31) / 32 * 32; }
+
+template <int VPT>
+cudaError_t launch_t(DispatchFp8Params p, int num_sms, cudaStream_t st) {
+    const int threads = fit_threads(p.H8, VPT);
+    // Stages: about 56 KB of bf16 rows per CTA (4 rows at H = 7168), at
+    // least 2; three CTAs per SM.
+    const size_t stride = ((size_t)p.H * 2 + 127) / 128 * 128;
+    int S = (int)((56u << 10) / stride);
+    S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+    p.stages = S;
+    const size_t smem = stride * S;
+    cudaError_t err = cudaFuncSetAttribute(dispatch_fp8_kernel<VPT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel<VPT>,
+                                                        threads, smem);
+    if (err != cudaSuccess) return err;
+    long long grid = (long long)num_sms * (per_sm < 1 ? 1 : per_sm);
+    if (grid > p.tokens) grid = p.tokens;
+    if (grid < 1) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dispatch_fp8_kernel<VPT>, p);
+}
+
+template <int VPT>
+cudaError_t launch_q(const float *x, long long rows, int H, uint8_t *q, float *scale,
+                     int num_sms, cudaStream_t st) {
+    const int threads = fit_threads(H / 8, VPT);
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, quantize_rows_kernel<VPT>, threads, 0);
+    if (err != cudaSuccess) return err;
+    long long grid = (long long)num_sms * (per_sm < 1 ? 1 : per_sm);
+    if (grid > rows) grid = rows;
+    if (grid < 1) return cudaSuccess;
+    quantize_rows_kernel<VPT><<<(unsigned)grid, threads, 0, st>>>(x, rows, H, q, scale);
+    return cudaGetLastError();
+}
+
+int vectors_per_thread(int H8) { return (H8 + kThreads - 1) / kThreads; }
+
+}  // namespace
+
+cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, int num_sms, cudaStream_t st) {
+    if (p.H % 16 != 0) return cudaErrorInvalidValue;
+    const int need = vectors_per_thread(p.H8);
+    if (need <= 1) return launch_t<1>(p, num_sms, st);
+    if (need <= 2) return launch_t<2>(p, num_sms, st);
+    if (need <= 4) return launch_t<4>(p, num_sms, st);
+    if (need <= 8) return launch_t<8>(p, num_sms, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_rows_fp8(const float *x, long long rows, int H, uint8_t *q,
+                                     float *scale, int num_sms, cudaStream_t st) {
+    if (H % 8 != 0) return cudaErrorInvalidValue;
+    const int need = vectors_per_thread(H / 8);
+    if (need <= 1) return launch_q<1>(x, rows, H, q, scale, num_sms, st);
+    if (need <= 2) return launch_q<2>(x, rows, H, q, scale, num_sms, st);
+    if (need <= 4) return launch_q<4>(x, rows, H, q, scale, num_sms, st);
+    if (need <= 8) return launch_q<8>(x, rows, H, q, scale, num_sms, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -109,6 +109,8 @@ struct CombineParams {
     const uint16_t *gamma;        // bf16 [H] or null
     uint16_t *out;                // bf16 [R][T][H]
     uint16_t *residual_out;       // bf16 [R][T][H] or null
+    uint8_t *out8;                // e4m3 [R][T][H] (FP8 output variant) or null
+    float *out_scale;             // [R][T] (FP8 output variant) or null
     uint32_t *flags;
     float eps;
     TokenMap map;
@@ -158,10 +160,28 @@ cudaError_t launch_combine(const CombineParams &p, bool weighted, bool fused, in
 
 // Combine with bulk-copy row streaming (one CTA per SM, producer warp +
 // consumer warps): vectors per consumer thread, ring depth and shape.
-cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, int num_sms,
+cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, int num_sms,
                                  LaunchShape *shape, int *vpt, int *slots);
-cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, int vpt,
-                                const LaunchShape &shape, cudaStream_t st);
+cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, bool out8,
+                                int vpt, const LaunchShape &shape, cudaStream_t st);
+
+// Dispatch with FP8 rows: per-token e4m3 quantisation into the receive
+// planes plus a per-row scale (see dispatch_fp8.cu).
+struct DispatchFp8Params {
+    const uint16_t *x;        // bf16 [R][T][H]
+    const int32_t *send_slot; // [R][T][RP]
+    uint8_t *recv_x8;         // e4m3 [R][R][m][H]
+    float *recv_scale;        // [R][R][m]
+    uint32_t *flags;
+    TokenMap map;
+    int R, RP, m, H, H8;
+    int stages;               // set by the launcher
+    long long tokens;
+};
+cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, int num_sms, cudaStream_t st);
+// fp32 rows [rows][H] -> e4m3 codes [rows][H] + scale [rows] (H % 8 == 0).
+cudaError_t launch_quantize_rows_fp8(const float *x, long long rows, int H, uint8_t *q,
+                                     float *scale, int num_sms, cudaStream_t st);
 
 cudaError_t launch_combine_tree(const CombineTreeParams &p, int num_sms, cudaStream_t st);
 

@@ -1,6 +1,6 @@
 // moe_a2a.cpp -- the C ABI declared in include/moe_a2a.h: configuration
 // checks, workspace layout, the dispatch/combine phase contract and the
-// launches of the four kernels.
+// kernel launches.
 //
 // Phase contract (InferenceX PR #2450, "CollectiveX: add FlashInfer
 // one-sided NVLink EP for the GB SKUs", "The adapter" table): dispatch
@@ -26,7 +26,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t recv_x, expert_out, recv_ids, recv_w, src_token, recv_counts, local_counts;
+    size_t recv_x, expert_out, recv_ids, recv_w, recv_scale, src_token, recv_counts,
+        local_counts;
     size_t send_slot, dest_weight, topk_dest, tile_counts, tile_prefix, tile_ticket, hist_accum,
         flags;
     size_t total;
@@ -62,6 +63,7 @@ bool compute_layout(const moe_a2a_config_t *c, Layout *L) {
     L->expert_out = take(R * R * M * H * 2);
     L->recv_ids = take(R * R * M * K * 4);
     L->recv_w = take(R * R * M * K * 4);
+    L->recv_scale = take(R * R * M * 4);
     L->src_token = take(R * R * M * 4);
     L->recv_counts = take(R * R * 4);
     L->local_counts = take(E * 4);
@@ -93,17 +95,19 @@ struct moe_a2a {
     uint32_t active;    // ranks that take part (all by default)
     bool accum_dirty;  // routing pass interrupted: re-zero its accumulators
     int reduction;     // MOE_REDUCE_*
+    int recv_format;   // MOE_FORMAT_*
     // lazily initialised on the first call that queues work
     bool ready;
     int device;
     int num_sms;
     moe::DispatchParams dispatch_tmpl;
     moe::LaunchShape dispatch_shape;
-    bool combine_ready[4];
-    bool combine_ring[4];
-    int combine_vpt[4];
-    int combine_slots[4];
-    moe::LaunchShape combine_shape[4];
+    // combine launch shapes by variant: 4 * out8 + 2 * weighted + fused
+    bool combine_ready[8];
+    bool combine_ring[8];
+    int combine_vpt[8];
+    int combine_slots[8];
+    moe::LaunchShape combine_shape[8];
 };
 
 namespace {
@@ -216,16 +220,31 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
         h->accum_dirty = false;
 
-        moe::DispatchParams dp = h->dispatch_tmpl;
-        dp.x = static_cast<const uint8_t *>(d_x);
-        dp.send_slot = rs.send_slot;
-        dp.recv_x = at<uint8_t>(h, h->L.recv_x);
-        dp.flags = flags;
-        dp.map = map;
-        dp.R = R, dp.RP = RP, dp.m = m;
-        dp.units = ntok * dp.chunks;
-        if (moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (h->recv_format == MOE_FORMAT_FP8_E4M3) {
+            moe::DispatchFp8Params fp;
+            fp.x = static_cast<const uint16_t *>(d_x);
+            fp.send_slot = rs.send_slot;
+            fp.recv_x8 = at<uint8_t>(h, h->L.recv_x);
+            fp.recv_scale = at<float>(h, h->L.recv_scale);
+            fp.flags = flags;
+            fp.map = map;
+            fp.R = R, fp.RP = RP, fp.m = m;
+            fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
+            fp.tokens = ntok;
+            if (moe::launch_dispatch_fp8(fp, h->num_sms, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        } else {
+            moe::DispatchParams dp = h->dispatch_tmpl;
+            dp.x = static_cast<const uint8_t *>(d_x);
+            dp.send_slot = rs.send_slot;
+            dp.recv_x = at<uint8_t>(h, h->L.recv_x);
+            dp.flags = flags;
+            dp.map = map;
+            dp.R = R, dp.RP = RP, dp.m = m;
+            dp.units = ntok * dp.chunks;
+            if (moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
     }
 
     h->map = map;
@@ -245,7 +264,106 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         out_view->tokens_per_rank = map.uniform ? map.stride : -1;
         out_view->send_stride = RP;
         out_view->token_stride = map.stride;
+        const bool fp8 = h->recv_format == MOE_FORMAT_FP8_E4M3;
+        out_view->recv_scale = fp8 ? at<float>(h, h->L.recv_scale) : nullptr;
+        out_view->recv_format = h->recv_format;
     }
+    return MOE_OK;
+}
+
+// The combine phase; out8 selects the FP8 output (d_out = e4m3 rows plus
+// d_out_scale) instead of bf16 rows.
+int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const void *d_residual,
+                 const void *d_gamma, float eps, void *d_out, float *d_out_scale,
+                 void *d_residual_out, bool out8, void *stream) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 1) return MOE_ERR_PHASE;
+    const bool fused = d_residual != nullptr;
+    const void *eo = d_expert_out != nullptr ? d_expert_out : h->ws + h->L.expert_out;
+    if (h->ntok > 0) {
+        if (d_out == nullptr || !aligned(d_out, 16) || !aligned(eo, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (out8 && (d_out_scale == nullptr || !aligned(d_out_scale, 4)))
+            return MOE_ERR_INVALID_ARG;
+        if (fused && (d_gamma == nullptr || !aligned(d_residual, 16) || !aligned(d_gamma, 16)))
+            return MOE_ERR_INVALID_ARG;
+        if (fused && d_residual_out != nullptr && !aligned(d_residual_out, 16))
+            return MOE_ERR_INVALID_ARG;
+        if (!fused && d_residual_out != nullptr) return MOE_ERR_INVALID_ARG;
+        if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    }
+    if (h->reduction == MOE_REDUCE_BF16_TOPK_TREE && (weighted || out8))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (h->ntok > 0 && h->reduction == MOE_REDUCE_BF16_TOPK_TREE) {
+        moe::CombineTreeParams tp;
+        tp.expert_out = static_cast<const uint16_t *>(eo);
+        tp.send_slot = at<int32_t>(h, h->L.send_slot);
+        tp.topk_dest = at<int8_t>(h, h->L.topk_dest);
+        tp.residual = static_cast<const uint16_t *>(d_residual);
+        tp.gamma = static_cast<const uint16_t *>(d_gamma);
+        tp.out = static_cast<uint16_t *>(d_out);
+        tp.residual_out = static_cast<uint16_t *>(d_residual_out);
+        tp.flags = at<uint32_t>(h, h->L.flags);
+        tp.eps = eps;
+        tp.map = h->map;
+        tp.active = h->active;
+        tp.R = h->cfg.ep_size, tp.RP = h->L.RP, tp.m = h->m;
+        tp.H = h->cfg.hidden, tp.H8 = h->cfg.hidden / 8, tp.K = h->cfg.top_k;
+        tp.P = 1;
+        while (tp.P < tp.K) tp.P *= 2;
+        tp.tokens = h->ntok;
+        if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    } else if (h->ntok > 0) {
+        const int variant = (out8 ? 4 : 0) + (weighted ? 2 : 0) + (fused ? 1 : 0);
+        if (!h->combine_ready[variant]) {
+            // The fused combine streams its rows through a shared-memory
+            // ring (its epilogue then overlaps other tokens' loads); the
+            // plain gather-sum keeps rows in registers, which measured
+            // faster there.  MOE_COMBINE_KERNEL=ring|regs overrides.  The
+            // FP8 output exists on the ring kernel only.
+            const char *sel = std::getenv("MOE_COMBINE_KERNEL");
+            bool ring = fused || out8;
+            if (sel != nullptr && std::strcmp(sel, "regs") == 0) ring = out8;
+            if (sel != nullptr && std::strcmp(sel, "ring") == 0) ring = true;
+            cudaError_t e =
+                ring ? moe::combine_ring_prepare(h->cfg.hidden, weighted != 0, fused, out8,
+                                                 h->num_sms, &h->combine_shape[variant],
+                                                 &h->combine_vpt[variant],
+                                                 &h->combine_slots[variant])
+                     : moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
+                                            &h->combine_shape[variant], &h->combine_vpt[variant]);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            h->combine_ring[variant] = ring;
+            h->combine_ready[variant] = true;
+        }
+        moe::CombineParams cp;
+        cp.expert_out = static_cast<const uint16_t *>(eo);
+        cp.send_slot = at<int32_t>(h, h->L.send_slot);
+        cp.dest_weight = at<float>(h, h->L.dest_weight);
+        cp.residual = static_cast<const uint16_t *>(d_residual);
+        cp.gamma = static_cast<const uint16_t *>(d_gamma);
+        cp.out = out8 ? nullptr : static_cast<uint16_t *>(d_out);
+        cp.residual_out = static_cast<uint16_t *>(d_residual_out);
+        cp.out8 = out8 ? static_cast<uint8_t *>(d_out) : nullptr;
+        cp.out_scale = out8 ? d_out_scale : nullptr;
+        cp.eps = eps;
+        cp.flags = at<uint32_t>(h, h->L.flags);
+        cp.map = h->map;
+        cp.active = h->active;
+        cp.R = h->cfg.ep_size, cp.RP = h->L.RP, cp.m = h->m;
+        cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
+        cp.tokens = h->ntok;
+        cp.ring_slots = h->combine_slots[variant];
+        const cudaError_t e =
+            h->combine_ring[variant]
+                ? moe::launch_combine_ring(cp, weighted != 0, fused, out8,
+                                           h->combine_vpt[variant], h->combine_shape[variant], st)
+                : moe::launch_combine(cp, weighted != 0, fused, h->combine_vpt[variant],
+                                      h->combine_shape[variant], st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    h->phase = 0;
     return MOE_OK;
 }
 
@@ -333,89 +451,15 @@ void *moe_combine_payload(moe_a2a_t *h) {
 
 int moe_combine(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const void *d_residual,
                 const void *d_gamma, float eps, void *d_out, void *d_residual_out, void *stream) {
-    if (h == nullptr) return MOE_ERR_INVALID_ARG;
-    if (h->phase != 1) return MOE_ERR_PHASE;
-    const bool fused = d_residual != nullptr;
-    const void *eo = d_expert_out != nullptr ? d_expert_out : h->ws + h->L.expert_out;
-    if (h->ntok > 0) {
-        if (d_out == nullptr || !aligned(d_out, 16) || !aligned(eo, 16))
-            return MOE_ERR_INVALID_ARG;
-        if (fused && (d_gamma == nullptr || !aligned(d_residual, 16) || !aligned(d_gamma, 16)))
-            return MOE_ERR_INVALID_ARG;
-        if (fused && d_residual_out != nullptr && !aligned(d_residual_out, 16))
-            return MOE_ERR_INVALID_ARG;
-        if (!fused && d_residual_out != nullptr) return MOE_ERR_INVALID_ARG;
-        if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
-    }
-    if (h->reduction == MOE_REDUCE_BF16_TOPK_TREE && weighted) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (h->ntok > 0 && h->reduction == MOE_REDUCE_BF16_TOPK_TREE) {
-        moe::CombineTreeParams tp;
-        tp.expert_out = static_cast<const uint16_t *>(eo);
-        tp.send_slot = at<int32_t>(h, h->L.send_slot);
-        tp.topk_dest = at<int8_t>(h, h->L.topk_dest);
-        tp.residual = static_cast<const uint16_t *>(d_residual);
-        tp.gamma = static_cast<const uint16_t *>(d_gamma);
-        tp.out = static_cast<uint16_t *>(d_out);
-        tp.residual_out = static_cast<uint16_t *>(d_residual_out);
-        tp.flags = at<uint32_t>(h, h->L.flags);
-        tp.eps = eps;
-        tp.map = h->map;
-        tp.active = h->active;
-        tp.R = h->cfg.ep_size, tp.RP = h->L.RP, tp.m = h->m;
-        tp.H = h->cfg.hidden, tp.H8 = h->cfg.hidden / 8, tp.K = h->cfg.top_k;
-        tp.P = 1;
-        while (tp.P < tp.K) tp.P *= 2;
-        tp.tokens = h->ntok;
-        if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-    } else if (h->ntok > 0) {
-        const int variant = (weighted ? 2 : 0) + (fused ? 1 : 0);
-        if (!h->combine_ready[variant]) {
-            // The fused combine streams its rows through a shared-memory
-            // ring (its epilogue then overlaps other tokens' loads); the
-            // plain gather-sum keeps rows in registers, which measured
-            // faster there.  MOE_COMBINE_KERNEL=ring|regs overrides.
-            const char *sel = std::getenv("MOE_COMBINE_KERNEL");
-            bool ring = fused;
-            if (sel != nullptr && std::strcmp(sel, "regs") == 0) ring = false;
-            if (sel != nullptr && std::strcmp(sel, "ring") == 0) ring = true;
-            cudaError_t e =
-                ring ? moe::combine_ring_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
-                                                 &h->combine_shape[variant],
-                                                 &h->combine_vpt[variant],
-                                                 &h->combine_slots[variant])
-                     : moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
-                                            &h->combine_shape[variant], &h->combine_vpt[variant]);
-            if (e != cudaSuccess) return MOE_ERR_CUDA;
-            h->combine_ring[variant] = ring;
-            h->combine_ready[variant] = true;
-        }
-        moe::CombineParams cp;
-        cp.expert_out = static_cast<const uint16_t *>(eo);
-        cp.send_slot = at<int32_t>(h, h->L.send_slot);
-        cp.dest_weight = at<float>(h, h->L.dest_weight);
-        cp.residual = static_cast<const uint16_t *>(d_residual);
-        cp.gamma = static_cast<const uint16_t *>(d_gamma);
-        cp.out = static_cast<uint16_t *>(d_out);
-        cp.residual_out = static_cast<uint16_t *>(d_residual_out);
-        cp.eps = eps;
-        cp.flags = at<uint32_t>(h, h->L.flags);
-        cp.map = h->map;
-        cp.active = h->active;
-        cp.R = h->cfg.ep_size, cp.RP = h->L.RP, cp.m = h->m;
-        cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
-        cp.tokens = h->ntok;
-        cp.ring_slots = h->combine_slots[variant];
-        const cudaError_t e =
-            h->combine_ring[variant]
-                ? moe::launch_combine_ring(cp, weighted != 0, fused, h->combine_vpt[variant],
-                                           h->combine_shape[variant], st)
-                : moe::launch_combine(cp, weighted != 0, fused, h->combine_vpt[variant],
-                                      h->combine_shape[variant], st);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-    }
-    h->phase = 0;
-    return MOE_OK;
+    return combine_impl(h, d_expert_out, weighted, d_residual, d_gamma, eps, d_out, nullptr,
+                        d_residual_out, false, stream);
+}
+
+int moe_combine_fp8(moe_a2a_t *h, const void *d_expert_out, int32_t weighted,
+                    const void *d_residual, const void *d_gamma, float eps, void *d_out_fp8,
+                    float *d_out_scale, void *d_residual_out, void *stream) {
+    return combine_impl(h, d_expert_out, weighted, d_residual, d_gamma, eps, d_out_fp8,
+                        d_out_scale, d_residual_out, true, stream);
 }
 
 int moe_a2a_get_error(moe_a2a_t *h, void *stream, uint32_t *flags) {
@@ -446,6 +490,34 @@ int moe_a2a_destroy(moe_a2a_t *h) {
 }
 
 int moe_a2a_phase(const moe_a2a_t *h) { return h == nullptr ? -1 : h->phase; }
+
+int moe_a2a_set_recv_format(moe_a2a_t *h, int32_t format) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 0) return MOE_ERR_PHASE;
+    if (format == MOE_FORMAT_BF16 || (format == MOE_FORMAT_FP8_E4M3 && h->cfg.hidden % 16 == 0)) {
+        h->recv_format = format;
+        return MOE_OK;
+    }
+    return MOE_ERR_INVALID_ARG;
+}
+
+int moe_quantize_rows_fp8(const float *d_x, int64_t rows, int32_t hidden, void *d_q,
+                          float *d_scale, void *stream) {
+    if (rows < 0 || hidden < 8 || hidden > MOE_MAX_HIDDEN || hidden % 8 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (d_x == nullptr || d_q == nullptr || d_scale == nullptr || !aligned(d_x, 16) ||
+        !aligned(d_q, 16) || !aligned(d_scale, 4))
+        return MOE_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return moe::launch_quantize_rows_fp8(d_x, rows, hidden, static_cast<uint8_t *>(d_q), d_scale,
+                                         sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
 
 int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;

@@ -29,10 +29,13 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_combine_payload", "moe_combine", "moe_a2a_get_error",
            "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string",
            "moe_route_static_scratch_bytes", "moe_route_static_scratch",
-           "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks")
+           "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks",
+           "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
+MOE_FORMAT_BF16 = 0
+MOE_FORMAT_FP8_E4M3 = 1
 
 
 class MoeA2AConfig(ctypes.Structure):
@@ -47,7 +50,8 @@ class MoeDispatchView(ctypes.Structure):
                 ("recv_counts", ctypes.c_void_p), ("local_expert_counts", ctypes.c_void_p),
                 ("send_slot", ctypes.c_void_p), ("dest_weight", ctypes.c_void_p),
                 ("plane_stride", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
-                ("send_stride", ctypes.c_int32), ("token_stride", ctypes.c_int32)]
+                ("send_stride", ctypes.c_int32), ("token_stride", ctypes.c_int32),
+                ("recv_scale", ctypes.c_void_p), ("recv_format", ctypes.c_int32)]
 
 
 class MoeA2AError(RuntimeError):
@@ -88,6 +92,12 @@ def _load(path: str = LIBRARY):
     lib.moe_dispatch_varlen.restype = ctypes.c_int
     lib.moe_a2a_set_active_ranks.argtypes = [p, ctypes.c_uint32]
     lib.moe_a2a_set_active_ranks.restype = ctypes.c_int
+    lib.moe_combine_fp8.argtypes = [p, p, i32, p, p, ctypes.c_float, p, p, p, p]
+    lib.moe_combine_fp8.restype = ctypes.c_int
+    lib.moe_quantize_rows_fp8.argtypes = [p, ctypes.c_int64, i32, p, p, p]
+    lib.moe_quantize_rows_fp8.restype = ctypes.c_int
+    lib.moe_a2a_set_recv_format.argtypes = [p, i32]
+    lib.moe_a2a_set_recv_format.restype = ctypes.c_int
     lib.moe_a2a_set_reduction.argtypes = [p, i32]
     lib.moe_a2a_set_reduction.restype = ctypes.c_int
     lib.moe_a2a_status_string.argtypes = [ctypes.c_int]
@@ -151,6 +161,46 @@ def moe_combine(h, d_expert_out: int, weighted: bool, d_residual: int, d_gamma: 
                             ctypes.c_void_p(d_residual), ctypes.c_void_p(d_gamma),
                             float(eps), ctypes.c_void_p(d_out), ctypes.c_void_p(d_residual_out),
                             ctypes.c_void_p(stream))
+
+
+def moe_combine_fp8(h, d_expert_out: int, weighted: bool, d_residual: int, d_gamma: int,
+                    eps: float, d_out_fp8: int, d_out_scale: int, d_residual_out: int,
+                    stream: int = 0) -> int:
+    v = ctypes.c_void_p
+    return _lib.moe_combine_fp8(h, v(d_expert_out), int(bool(weighted)), v(d_residual),
+                                v(d_gamma), float(eps), v(d_out_fp8), v(d_out_scale),
+                                v(d_residual_out), v(stream))
+
+
+def moe_quantize_rows_fp8(d_x: int, rows: int, hidden: int, d_q: int, d_scale: int,
+                          stream: int = 0) -> int:
+    v = ctypes.c_void_p
+    return _lib.moe_quantize_rows_fp8(v(d_x), rows, hidden, v(d_q), v(d_scale), v(stream))
+
+
+def quantize_rows_fp8(x, out=None, scale=None, stream=None):
+    """fp32 [..., H] CUDA tensor -> (float8_e4m3fn [..., H], float32 [...])."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    H = x.shape[-1]
+    rows = x.numel() // H if H else 0
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    st = moe_quantize_rows_fp8(x.data_ptr(), rows, H, out.data_ptr(), scale.data_ptr(),
+                               stream.cuda_stream if hasattr(stream, "cuda_stream")
+                               else int(stream))
+    if st != MOE_OK:
+        raise MoeA2AError(st, "moe_quantize_rows_fp8")
+    return out, scale
+
+
+def moe_a2a_set_recv_format(h, fmt: int) -> int:
+    return _lib.moe_a2a_set_recv_format(h, fmt)
 
 
 def moe_a2a_get_error(h, stream: int = 0):
@@ -227,7 +277,13 @@ class DispatchView:
 
         self.plane_stride, self.send_stride = m, RP
         self.tokens_per_rank, self.token_stride = raw.tokens_per_rank, T
-        self.recv_x = region(raw.recv_x, torch.bfloat16, (R, R, m, H))
+        self.recv_format = raw.recv_format
+        if raw.recv_format == MOE_FORMAT_FP8_E4M3:
+            self.recv_x = region(raw.recv_x, torch.float8_e4m3fn, (R, R, m, H))
+            self.recv_scale = region(raw.recv_scale, torch.float32, (R, R, m))
+        else:
+            self.recv_x = region(raw.recv_x, torch.bfloat16, (R, R, m, H))
+            self.recv_scale = None
         self.recv_topk_ids = region(raw.recv_topk_ids, torch.int32, (R, R, m, K))
         self.recv_topk_w = region(raw.recv_topk_w, torch.float32, (R, R, m, K))
         self.src_token = region(raw.src_token, torch.int32, (R, R, m))
@@ -288,8 +344,8 @@ class MoeA2A:
                                self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_dispatch")
-        # The views depend only on (m, token stride): reuse them across calls.
-        key = (raw.plane_stride, raw.token_stride)
+        # The views depend only on (m, token stride, format): reuse them across calls.
+        key = (raw.plane_stride, raw.token_stride, raw.recv_format)
         if self.last_view is None or self._view_key != key:
             self.last_view = DispatchView(self, raw)
             self._view_key = key
@@ -307,7 +363,7 @@ class MoeA2A:
                                       list(tokens_per_rank), m, self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_dispatch_varlen")
-        key = (raw.plane_stride, raw.token_stride)
+        key = (raw.plane_stride, raw.token_stride, raw.recv_format)
         if self.last_view is None or self._view_key != key:
             self.last_view = DispatchView(self, raw)
             self._view_key = key
@@ -354,6 +410,45 @@ class MoeA2A:
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_combine")
         return out
+
+    def combine_fp8(self, expert_out=None, weighted: bool = False, residual=None, gamma=None,
+                    eps: float = 1e-6, out=None, out_scale=None, residual_out=None,
+                    stream=None):
+        """As combine, with an e4m3 output and one fp32 scale per token row:
+        returns (out float8_e4m3fn [R, T, H], out_scale float32 [R, T])."""
+        import torch
+        if self.last_view is None:
+            st = moe_combine_fp8(self.handle, 0, weighted, 0, 0, eps, 0, 0, 0,
+                                 self._stream(stream))
+            raise MoeA2AError(st if st != MOE_OK else MOE_ERR_PHASE, "moe_combine_fp8")
+        R, H = self.ep_size, self.hidden
+        T, m = self.last_view.token_stride, self.last_view.plane_stride
+        if expert_out is not None:
+            self._check(expert_out, torch.bfloat16, (R, R, m, H), "expert_out")
+        if residual is not None:
+            self._check(residual, torch.bfloat16, (R, T, H), "residual")
+            self._check(gamma, torch.bfloat16, (H,), "gamma")
+            if residual_out is not None:
+                self._check(residual_out, torch.bfloat16, (R, T, H), "residual_out")
+        dev = self.workspace.device
+        if out is None:
+            out = torch.empty((R, T, H), dtype=torch.float8_e4m3fn, device=dev)
+        if out_scale is None:
+            out_scale = torch.empty((R, T), dtype=torch.float32, device=dev)
+        self._check(out, torch.float8_e4m3fn, (R, T, H), "out")
+        self._check(out_scale, torch.float32, (R, T), "out_scale")
+        st = moe_combine_fp8(self.handle, _ptr(expert_out), weighted, _ptr(residual),
+                             _ptr(gamma), eps, _ptr(out), _ptr(out_scale), _ptr(residual_out),
+                             self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_combine_fp8")
+        return out, out_scale
+
+    def set_recv_format(self, fmt: int):
+        """MOE_FORMAT_BF16 (default) or MOE_FORMAT_FP8_E4M3 rows in recv_x."""
+        st = moe_a2a_set_recv_format(self.handle, fmt)
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_a2a_set_recv_format")
 
     def set_reduction(self, reduction: int):
         """MOE_REDUCE_FP32_RANK_ORDER (default) or MOE_REDUCE_BF16_TOPK_TREE."""

@@ -126,6 +126,9 @@ typedef struct moe_dispatch_view {
     int32_t token_stride;         /* rows per source rank of the token arrays
                                      (x, send_slot, dest_weight, residual, out):
                                      T, or m for moe_dispatch_varlen */
+    float *recv_scale;            /* fp32 [R][R][m]: per-row scale of recv_x
+                                     in the FP8 receive format, else NULL */
+    int32_t recv_format;          /* MOE_FORMAT_* of recv_x */
 } moe_dispatch_view_t;
 
 /* Bytes of device workspace a handle with this config needs (0 if the
@@ -246,6 +249,55 @@ enum moe_reduction { MOE_REDUCE_FP32_RANK_ORDER = 0, MOE_REDUCE_BF16_TOPK_TREE =
 /* Select the reduction of subsequent moe_combine calls (host-only).
  * Returns MOE_ERR_INVALID_ARG for an unknown mode or top_k > 8 with the tree. */
 int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction);
+
+/* ---- FP8 payloads ----------------------------------------------------------
+ * [IX] "The adapter" (the paragraph on why the adapter is BF16-only): an FP8
+ * dispatch carries a scale payload beside the rows and is validated against
+ * the cast round trip; the combine side accepts FP8 output dtypes ([IX] the
+ * comment on the shipped combine signature: upstream output_dtype /
+ * use_low_precision).  Readings: OCP FP8 E4M3 (bias 7, largest finite 448,
+ * no infinities), one scale per token row:
+ *   scale = amax_h |v_h| / 448 in binary32 (1 for an all-zero row),
+ *   q_h   = e4m3(v_h / scale), binary32 division, round-to-nearest-even,
+ *           magnitudes past 448 saturate to 448, NaN stays NaN;
+ * dequantised value q_h * scale.
+ *
+ * Receive format (host-only, IDLE phase only; MOE_ERR_PHASE otherwise):
+ *   MOE_FORMAT_BF16 (default): recv_x bf16 [R][R][m][H], recv_scale NULL.
+ *   MOE_FORMAT_FP8_E4M3: dispatch writes recv_x as e4m3 bytes [R][R][m][H]
+ *     (the first half of the bf16 region) with v = the bf16 row x[s][t], and
+ *     recv_scale fp32 [R][R][m]; the metadata rows, counts and send tables
+ *     are unchanged.  Needs H a multiple of 16 (MOE_ERR_INVALID_ARG).
+ *   The expert outputs that combine reads stay bf16 in either format. */
+enum moe_format { MOE_FORMAT_BF16 = 0, MOE_FORMAT_FP8_E4M3 = 1 };
+
+int moe_a2a_set_recv_format(moe_a2a_t *h, int32_t format);
+
+/* Combine with an FP8 output: the reduction and the fused epilogue exactly as
+ * moe_combine (fp32 rank-order reduction only: MOE_ERR_INVALID_ARG with the
+ * bf16 top-k tree), then, per token row, v = the fp32 result that moe_combine
+ * would narrow to bf16 (acc unfused; the RMSNorm output fused) is quantised
+ * as above into
+ *   d_out_fp8   e4m3 [R][T][H] (16-byte aligned) and
+ *   d_out_scale fp32 [R][T]    (4-byte aligned).
+ * d_residual_out stays bf16.  Queues one kernel; DISPATCHED -> IDLE. */
+int moe_combine_fp8(moe_a2a_t *h, const void *d_expert_out, int32_t weighted,
+                    const void *d_residual, const void *d_gamma, float eps,
+                    void *d_out_fp8, float *d_out_scale, void *d_residual_out,
+                    void *stream);
+
+/* The same per-row quantisation as a standalone call, for fp32 rows (e.g.
+ * activations headed for an FP8 expert GEMM, or a check of the cast):
+ *   d_x     fp32 [rows][H], 16-byte aligned, H a multiple of 8 (8..16384)
+ *   d_q     e4m3 [rows][H], 16-byte aligned
+ *   d_scale fp32 [rows], 4-byte aligned
+ * rows >= 0 (0 queues nothing).  Queues one kernel on `stream`; no handle.
+ * The quotients are the correctly rounded binary32 x / scale (one
+ * reciprocal per row refined by FMA remainder steps, exact by Markstein's
+ * theorem; rows with a scale outside [2^-100, 2^100] refine the pair
+ * scaled by 2^100 or 2^-100, which leaves the quotient unchanged). */
+int moe_quantize_rows_fp8(const float *d_x, int64_t rows, int32_t hidden, void *d_q,
+                          float *d_scale, void *stream);
 
 /* ---- Routing without any device allocation --------------------------------
  * The source pages have no counterpart to this entry point; it exists for

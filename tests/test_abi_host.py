@@ -159,3 +159,41 @@ def test_varlen_and_active_rank_checks(abi):
     assert abi.moe_a2a_set_active_ranks(h, 0b10000) == abi.MOE_ERR_INVALID_ARG
     assert abi.moe_a2a_set_active_ranks(None, 1) == abi.MOE_ERR_INVALID_ARG
     abi.moe_a2a_destroy(h)
+
+
+def test_recv_format_and_fp8_combine_checks(abi):
+    st, h = _handle(abi, cfg=(4, 64, 136, 16, 2))     # H = 136: not a multiple of 16
+    assert abi.moe_a2a_set_recv_format(h, abi.MOE_FORMAT_FP8_E4M3) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_set_recv_format(h, abi.MOE_FORMAT_BF16) == abi.MOE_OK
+    abi.moe_a2a_destroy(h)
+    st, h = _handle(abi, cfg=(4, 64, 128, 16, 2))
+    assert abi.moe_a2a_set_recv_format(h, abi.MOE_FORMAT_FP8_E4M3) == abi.MOE_OK
+    assert abi.moe_a2a_set_recv_format(h, 2) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_set_recv_format(None, 0) == abi.MOE_ERR_INVALID_ARG
+    A = 1 << 20
+    assert abi.moe_combine_fp8(h, 0, 0, 0, 0, 1e-6, A, A, 0) == abi.MOE_ERR_PHASE
+    assert abi.moe_combine_fp8(None, 0, 0, 0, 0, 1e-6, A, A, 0) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_phase(h) == 0
+    abi.moe_a2a_destroy(h)
+
+
+def test_view_struct_matches_header(abi):
+    import ctypes
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct moe_dispatch_view {"):text.index("} moe_dispatch_view_t;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"\*?\s*(\w+);", body)
+    assert names == [f[0] for f in abi.MoeDispatchView._fields_]
+
+
+def test_quantize_rows_fp8_checks(abi):
+    A = 1 << 20
+    q = abi.moe_quantize_rows_fp8
+    assert q(A, 0, 64, A, A) == abi.MOE_OK                  # nothing to do, nothing queued
+    assert q(A, -1, 64, A, A) == abi.MOE_ERR_INVALID_ARG
+    assert q(A, 4, 60, A, A) == abi.MOE_ERR_INVALID_ARG      # H not a multiple of 8
+    assert q(A, 4, 32768, A, A) == abi.MOE_ERR_INVALID_ARG
+    assert q(0, 4, 64, A, A) == abi.MOE_ERR_INVALID_ARG
+    assert q(A + 4, 4, 64, A, A) == abi.MOE_ERR_INVALID_ARG  # x not 16-byte aligned
+    assert q(A, 4, 64, A + 8, A) == abi.MOE_ERR_INVALID_ARG
+    assert q(A, 4, 64, A, A + 2) == abi.MOE_ERR_INVALID_ARG

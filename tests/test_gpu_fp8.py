@@ -1,0 +1,347 @@
+"""FP8 payloads against the oracle.
+
+InferenceX PR #2450, "CollectiveX: add FlashInfer one-sided NVLink EP for the
+GB SKUs", "The adapter": an FP8 dispatch carries a per-token scale payload
+next to the rows and is checked against the cast round trip; the combine
+side accepts FP8 output dtypes.  Readings: OCP e4m3, scale = amax / 448 in
+binary32 (1 for a zero row), codes = e4m3_rn_satfinite(v / scale).
+
+Dispatch in the FP8 receive format and the unfused FP8 combine are compared
+bit for bit (codes and scales) with the oracle's quantisation of the same
+bf16 rows / of the oracle's own fp32 sum.  The fused FP8 combine quantises
+the RMSNorm output, which the oracle computes in fp64: its scales must agree
+to binary32 rounding, its codes to one e4m3 step, and the dequantised values
+lie within the format's half step of the oracle's y.
+"""
+import numpy as np
+import pytest
+
+from combine_topk_ids_rank_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import parity  # noqa: E402
+from oracle import oracle  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from combine_topk_ids_rank_gb300 import build_lib
+    build_lib.build()
+
+
+def u8(t):
+    return t.view(torch.uint8).cpu().numpy()
+
+
+def edge_rows(x, H):
+    """Overwrite the first rows of every source with the format's edge cases:
+    zeros, one spike, a huge row, a row mixing huge and tiny values (fp8
+    subnormals and underflow), and a row of equal magnitudes."""
+    R, T = x.shape[:2]
+    rows = []
+    rows.append(np.zeros(H, np.float32))
+    spike = np.zeros(H, np.float32)
+    spike[H // 3] = -3.0
+    rows.append(spike)
+    rows.append(np.linspace(-2.0 ** 120, 2.0 ** 120, H, dtype=np.float32))
+    mix = np.full(H, 2.0 ** -20, np.float32)
+    mix[::7] = 1000.0
+    mix[1::5] = -3.0 * 2.0 ** -8
+    rows.append(mix)
+    rows.append(np.where(np.arange(H) % 2 == 0, 0.75, -0.75).astype(np.float32))
+    for s in range(R):
+        for j, r in enumerate(rows[:T]):
+            x[s, j] = parity.f32_to_bits(r)
+    return x
+
+
+def code_step(c):
+    """e4m3 code -> its signed position on the ordered code line."""
+    c = np.asarray(c, np.int32)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def run_dispatch_fp8(R, T, H, E, K, seed, m=None, counts=None, routing="uniform"):
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    m = T if m is None else m
+    ids = synth.topk_ids(seed, R, T, E, K, routing)
+    w = synth.topk_weights(seed, R, T, K)
+    x = edge_rows(synth.per_rank_rows(seed, synth.X, R, T, H), H)
+    if counts is not None:
+        ids_o = ids.copy()
+        for s, c in enumerate(counts):
+            ids_o[s, c:] = -1
+    else:
+        ids_o = ids
+    a = MoeA2A(R, m, H, E, K, "cuda")
+    a.workspace.fill_(parity.POISON)
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    dev = parity.to_dev
+    if counts is not None:
+        view = a.dispatch_varlen(dev(ids, torch.int32), dev(w, torch.float32),
+                                 dev(x, torch.bfloat16), counts)
+    else:
+        view = a.dispatch(dev(ids, torch.int32), dev(w, torch.float32),
+                          dev(x, torch.bfloat16), m)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    assert view.recv_x.dtype == torch.float8_e4m3fn and view.recv_scale is not None
+
+    r = oracle.route(ids_o, w, E, m)
+    cnt = view.recv_counts.cpu().numpy()
+    assert np.array_equal(cnt, r["recv_counts"])
+    assert np.array_equal(view.send_slot.cpu().numpy()[:, :, :R], r["send_slot"])
+    q_ref, sc_ref = oracle.quantize_rows_fp8(x)            # [R, T, H], [R, T]
+    gq, gs = u8(view.recv_x), view.recv_scale.cpu().numpy()
+    src = view.src_token.cpu().numpy()
+    for d in range(R):
+        for s in range(R):
+            c = int(cnt[d, s])
+            t = src[d, s, :c]
+            assert np.array_equal(gq[d, s, :c], q_ref[s, t]), "codes (%d,%d)" % (d, s)
+            assert np.array_equal(gs[d, s, :c].view(np.uint32),
+                                  sc_ref[s, t].view(np.uint32)), "scales (%d,%d)" % (d, s)
+            # padding is never written
+            assert (gq[d, s, c:m] == parity.POISON).all()
+            assert (gs[d, s, c:m].view(np.uint32) == 0xFFFFFFFF).all()
+    return a, view, dict(ids=ids, ids_o=ids_o, w=w, x=x, r=r, cnt=cnt, m=m)
+
+
+@pytest.mark.parametrize("R,T,H,E,K", [(6, 300, 144, 48, 5), (4, 40, 16, 8, 2),
+                                       (8, 64, 7168, 256, 8)])
+def test_fp8_dispatch_codes_and_scales_bit_exact(R, T, H, E, K):
+    run_dispatch_fp8(R, T, H, E, K, seed=R + K)
+
+
+def test_fp8_dispatch_prefill_shape():
+    run_dispatch_fp8(8, 4096, 7168, 256, 8, seed=0, routing="zipf")
+
+
+def test_fp8_dispatch_cast_round_trip():
+    """The pages' check: dequantised rows equal the cast round trip of x
+    (codes * scale, the oracle's decode), within the e4m3 half step."""
+    a, view, d = run_dispatch_fp8(4, 50, 256, 16, 4, seed=9)
+    cnt, src = d["cnt"], view.src_token.cpu().numpy()
+    x = parity.f32(d["x"]).astype(np.float64)
+    gq, gs = u8(view.recv_x), view.recv_scale.cpu().numpy().astype(np.float64)
+    for dd in range(4):
+        for s in range(4):
+            c = int(cnt[dd, s])
+            deq = oracle.fp8_to_f32(gq[dd, s, :c]).astype(np.float64) * gs[dd, s, :c, None]
+            ref = x[s, src[dd, s, :c]]
+            bound = 2.0 ** -4 * np.abs(ref) + 2.0 ** -10 * gs[dd, s, :c, None]
+            assert (np.abs(deq - ref) <= bound * (1 + 1e-6)).all()
+
+
+def test_fp8_dispatch_varlen():
+    run_dispatch_fp8(8, 96, 384, 64, 8, seed=2, counts=[96, 0, 5, 95, 1, 64, 33, 96])
+
+
+def _payload(a, cnt, m, H, seed):
+    eo = synth.expert_out_planes(seed, a.ep_size, m, H, cnt)
+    pay = a.combine_payload()
+    for d in range(a.ep_size):
+        for s in range(a.ep_size):
+            c = int(cnt[d, s])
+            if c:
+                pay[d, s, :c].copy_(parity.to_dev(eo[d, s, :c], torch.bfloat16))
+    return eo
+
+
+def _dispatch_bf16(R, T, H, E, K, seed):
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+    ids = synth.topk_ids(seed, R, T, E, K)
+    ids[0, :3] = -1                                 # tokens with no destination
+    w = synth.topk_weights(seed, R, T, K)
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    view = a.dispatch(parity.to_dev(ids, torch.int32), parity.to_dev(w, torch.float32),
+                      parity.to_dev(x, torch.bfloat16))
+    r = oracle.route(ids, w, E, T)
+    return a, view, r
+
+
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("R,T,H,E,K", [(6, 300, 136, 48, 5), (8, 512, 7168, 256, 8)])
+def test_fp8_combine_unfused_bit_exact(weighted, R, T, H, E, K):
+    a, view, r = _dispatch_bf16(R, T, H, E, K, seed=11)
+    cnt = view.recv_counts.cpu().numpy()
+    eo = _payload(a, cnt, T, H, 11)
+    out, sc = a.combine_fp8(None, weighted)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0) and a.phase == 0
+    oc = oracle.combine(r, eo, weighted)
+    q_ref, s_ref = oracle.quantize_f32_rows_fp8(oc["acc"])
+    assert np.array_equal(u8(out).reshape(R * T, H), q_ref)
+    assert np.array_equal(sc.cpu().numpy().ravel().view(np.uint32), s_ref.view(np.uint32))
+    assert (s_ref[:3] == 1.0).all() and (q_ref[:3] == 0).all()      # empty tokens
+
+
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("R,T,H,E,K", [(6, 300, 136, 48, 5), (8, 512, 7168, 256, 8)])
+def test_fp8_combine_fused(weighted, R, T, H, E, K):
+    a, view, r = _dispatch_bf16(R, T, H, E, K, seed=12)
+    cnt = view.recv_counts.cpu().numpy()
+    eo = _payload(a, cnt, T, H, 12)
+    res = synth.per_rank_rows(12, synth.RESIDUAL, R, T, H)
+    gam = synth.gamma(12, H)
+    rout = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    out, sc = a.combine_fp8(None, weighted, parity.to_dev(res, torch.bfloat16),
+                            parity.to_dev(gam, torch.bfloat16), 1e-6, residual_out=rout)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    oc = oracle.combine(r, eo, weighted, res, gam, 1e-6)
+    assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H), oc["residual_out"])
+    y = oc["y"]
+    q_ref, s_ref = oracle.quantize_f32_rows_fp8(y.astype(np.float32))
+    g_q = u8(out).reshape(R * T, H)
+    g_s = sc.cpu().numpy().ravel().astype(np.float64)
+    assert (np.abs(g_s - s_ref) <= 1e-5 * s_ref).all()
+    assert (np.abs(code_step(g_q) - code_step(q_ref)) <= 1).all()
+    deq = oracle.fp8_to_f32(g_q).astype(np.float64) * g_s[:, None]
+    bound = (2.0 ** -4 + 1e-4) * np.abs(y) + 2.0 ** -10 * g_s[:, None] + 1e-6
+    assert (np.abs(deq - y) <= bound).all()
+
+
+def test_fp8_mode_contract():
+    from combine_topk_ids_rank_gb300.moe_a2a import (MoeA2A, MoeA2AError, MOE_ERR_PHASE,
+                                                     MOE_ERR_INVALID_ARG, MOE_FORMAT_BF16,
+                                                     MOE_FORMAT_FP8_E4M3,
+                                                     MOE_REDUCE_BF16_TOPK_TREE)
+    a, view, r = _dispatch_bf16(2, 8, 64, 4, 2, seed=1)
+    with pytest.raises(MoeA2AError) as e:               # not while DISPATCHED
+        a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    assert e.value.status == MOE_ERR_PHASE
+    a.combine(None, False)
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    a.set_reduction(MOE_REDUCE_BF16_TOPK_TREE)
+    ids = parity.to_dev(synth.topk_ids(1, 2, 8, 4, 2), torch.int32)
+    w = parity.to_dev(synth.topk_weights(1, 2, 8, 2), torch.float32)
+    v = a.dispatch(ids, w, torch.zeros((2, 8, 64), dtype=torch.bfloat16, device="cuda"))
+    assert v.recv_x.dtype == torch.float8_e4m3fn
+    with pytest.raises(MoeA2AError) as e:               # the bf16 tree has no FP8 output
+        a.combine_fp8(None, False)
+    assert e.value.status == MOE_ERR_INVALID_ARG and a.phase == 1
+    a.combine(None, False)                              # the tree itself still runs
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    a.set_recv_format(MOE_FORMAT_BF16)
+    v = a.dispatch(ids, w, torch.zeros((2, 8, 64), dtype=torch.bfloat16, device="cuda"))
+    assert v.recv_x.dtype == torch.bfloat16 and v.recv_scale is None
+    a.combine(None, False)
+
+
+# --------------------------------------------------------------------------
+# The quotient at the e4m3 rounding boundaries: the kernels replace the
+# per-element division by FMA-refined products with the row's reciprocal,
+# which must give the correctly rounded binary32 quotient everywhere (the
+# oracle divides).  Inputs sit on and one to three binary32 steps around
+# every e4m3 midpoint times the row's scale, for row maxima across the whole
+# binary32 range (including the rows that take the per-element division).
+# --------------------------------------------------------------------------
+
+E4M3_VALUES = None
+
+
+def e4m3_positive_values():
+    global E4M3_VALUES
+    if E4M3_VALUES is None:
+        E4M3_VALUES = oracle.fp8_to_f32(np.arange(0, 0x7F, dtype=np.uint8)).astype(np.float64)
+    return E4M3_VALUES
+
+
+def boundary_row(A, H, rng):
+    A = np.float32(A)
+    s = np.float32(A / np.float32(448.0))
+    v = e4m3_positive_values()
+    mids = (v[:-1] + v[1:]) / 2
+    pts = np.concatenate([mids, v[1:]])
+    base = (pts * np.float64(s)).astype(np.float32)
+    cand = [base]
+    up, dn = base.copy(), base.copy()
+    for _ in range(3):
+        up = np.nextafter(up, np.float32(np.inf))
+        dn = np.nextafter(dn, np.float32(0))
+        cand += [up, dn]
+    c = np.concatenate(cand)
+    c = c[np.abs(c) <= A]
+    c = np.concatenate([c, -c])
+    row = rng.uniform(-1, 1, H).astype(np.float32) * A
+    row[1:1 + c.size] = c[:H - 1]
+    row[0] = A
+    rng.shuffle(row[1:])
+    return row
+
+
+def test_quantize_rows_fp8_rounding_boundaries():
+    from combine_topk_ids_rank_gb300.moe_a2a import quantize_rows_fp8
+    rng = np.random.default_rng(17)
+    H = 4096
+    maxima = [448.0, 1.0, 0.5, 3.0, 1000.0, 2.0 ** -20, 2.0 ** 40,
+              448.0 * 2.0 ** -100, 448.0 * 2.0 ** 100,       # at the edges of the fast path
+              2.0 ** -95, 2.0 ** -120, 2.0 ** 127, 3.0e38]    # per-element division rows
+    maxima += list(np.exp2(rng.uniform(-90, 100, 40)))
+    x = np.stack([boundary_row(A, H, rng) for A in maxima])
+    # a row whose quotients underflow binary32 (fp8 code: signed zero)
+    tiny = np.full(H, 2.0 ** -40, np.float32)
+    tiny[1::2] = -2.0 ** -40
+    tiny[0] = 2.0 ** 100
+    x = np.concatenate([x, tiny[None], np.zeros((1, H), np.float32)])
+    q_ref, s_ref = oracle.quantize_f32_rows_fp8(x)
+    q, s = quantize_rows_fp8(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    g = u8(q)
+    bad = np.argwhere(g != q_ref)
+    assert bad.size == 0, [(int(r), float(x[r, c]), int(g[r, c]), int(q_ref[r, c]))
+                           for r, c in bad[:8]]
+
+
+def test_quantize_rows_fp8_ragged_and_empty():
+    from combine_topk_ids_rank_gb300.moe_a2a import quantize_rows_fp8
+    rng = np.random.default_rng(3)
+    for rows, H in [(1, 8), (7, 136), (300, 7168), (3, 16384), (0, 64)]:
+        x = (rng.standard_normal((rows, H)) * rng.uniform(0.01, 100, (rows, 1))).astype(np.float32)
+        q, s = quantize_rows_fp8(torch.from_numpy(x).cuda())
+        torch.cuda.synchronize()
+        q_ref, s_ref = oracle.quantize_f32_rows_fp8(x) if rows else (np.zeros((0, H)), np.zeros(0))
+        assert np.array_equal(u8(q), q_ref) and np.array_equal(s.cpu().numpy(), s_ref)
+
+
+def test_fp8_dispatch_every_bf16_value_near_the_row_max():
+    """Every bf16 value within 11 binades below the row maximum, both signs,
+    for 64 row maxima; both destinations get the row."""
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    R, T, H, E, K = 2, 64, 4096, 2, 2
+    rng = np.random.default_rng(5)
+    x = np.zeros((R, T, H), np.uint16)
+    for s in range(R):
+        for t in range(T):
+            e = int(rng.integers(-120, 120))                # binade of the row max
+            top = (e + 127) << 7 | int(rng.integers(0, 128))
+            lo = max(top - 11 * 128, 1)
+            vals = np.arange(lo, top + 1, dtype=np.uint16)
+            row = np.concatenate([vals, vals | 0x8000])
+            rng.shuffle(row)
+            x[s, t, :row.size] = row
+            x[s, t, row.size:] = top                        # pad with the max
+    ids = np.tile(np.array([0, 1], np.int32), (R, T, 1))
+    w = np.full((R, T, K), 0.5, np.float32)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    view = a.dispatch(parity.to_dev(ids, torch.int32), parity.to_dev(w, torch.float32),
+                      parity.to_dev(x, torch.bfloat16))
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    q_ref, s_ref = oracle.quantize_rows_fp8(x)
+    gq, gs = u8(view.recv_x), view.recv_scale.cpu().numpy()
+    for d in range(R):
+        for s in range(R):
+            assert np.array_equal(gq[d, s, :T], q_ref[s])
+            assert np.array_equal(gs[d, s, :T], s_ref[s])
