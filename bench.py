@@ -512,7 +512,7 @@ def run_gpu(args, w, rank, world, local_rank):
             with open(prof) as f:
                 tr = json.load(f)
             ent = tr.get(w.name + ("-fp8" if fp8 else ""), {}).get("combine")
-            if ent and ent.get("source_sha1") == source_sha1(ent.get("source", "combine_ring.cu")):
+            if ent and ent.get("sources_sha1") == sources_sha1(ent.get("sources", [])):
                 traffic = ent["dram_bytes_per_launch"]
         except (OSError, ValueError, KeyError):
             traffic = None
@@ -554,11 +554,18 @@ def aggregate_over_ranks(local_ms: float, tokens_per_rank_batch: int, steps: int
     return max_ms, ms_per_step, tokens_per_rank_batch * world / (ms_per_step / 1e3)
 
 
-def source_sha1(name):
+def sources_sha1(names):
+    """One sha1 over the listed kernel sources (csrc/), in order: the
+    counters in profiles/traffic.json hold while it matches."""
     import hashlib
-    path = os.path.join(ROOT, "combine_topk_ids_rank_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+    h = hashlib.sha1()
+    if not names:
+        return None
+    for name in names:
+        path = os.path.join(ROOT, "combine_topk_ids_rank_gb300", "csrc", name)
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def main():

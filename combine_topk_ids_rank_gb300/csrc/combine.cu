@@ -17,10 +17,12 @@
 //
 // GB300 design: one CTA per token row at a time, persistent over tokens.
 // Each thread owns VPT 16-byte vectors (8 bf16) of the row, strided by the
-// block so every warp load is 512 contiguous bytes.  Destinations are
-// visited in groups of G with all G rows' loads issued before the group is
-// accumulated in ascending order, so G rows (plus the residual row) are in
-// flight per CTA.  Loads and stores of the streamed rows bypass L1 and are
+// block so every warp load is 512 contiguous bytes.  Lane d of each warp
+// holds the token's slot and weight for destination d (the next token's are
+// loaded while the current one is summed); a ballot gives the live
+// destinations, which are gathered in groups of G with all G rows' loads
+// issued before the group is accumulated in ascending order, so G rows (plus
+// the residual row) are in flight per CTA.  Loads and stores of the streamed rows bypass L1 and are
 // marked evict-first; gamma stays in L1.  The mean of squares is a warp
 // shuffle reduction followed by a cross-warp pass through shared memory.
 #include "kernels.h"
@@ -82,8 +84,30 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
 
     ptx::grid_dependency_wait();
 
+    // Lane d of every warp holds destination d's slot and weight of a token;
+    // the next token's are loaded while the current one is summed.
+    auto load_route = [&](long long i, int &slot, float &w) {
+        slot = -1;
+        w = 0.0f;
+        if (i < p.tokens && lane < p.R && ((p.active >> lane) & 1u)) {
+            int s, t;
+            token_of(p.map, p.R, i, s, t);
+            const long long tok = (long long)s * p.map.stride + t;
+            slot = __ldg(p.send_slot + tok * p.RP + lane);
+            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.RP + lane);
+            if (slot >= p.m) {  // guard: never expected from the routing pass
+                if (warp == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                slot = -1;
+            }
+        }
+    };
+    int slot_l, slot_n;
+    float w_l, w_n;
+    load_route(blockIdx.x, slot_l, w_l);
+
     int parity = 0;
     for (long long i = blockIdx.x; i < p.tokens; i += gridDim.x, parity ^= 1) {
+        load_route(i + gridDim.x, slot_n, w_n);
         int s, t;
         token_of(p.map, p.R, i, s, t);
         const long long tok = (long long)s * p.map.stride + t;  // row of the token arrays
@@ -104,36 +128,21 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
 
-        const int32_t *srow = p.send_slot + tok * p.RP;
-        const float *wrow = p.dest_weight + tok * p.RP;
-        for (int d0 = 0; d0 < p.R; d0 += G) {
-            int slot[G];
-            float w[G];
-#pragma unroll
-            for (int q = 0; q < G; q += 4) {
-                const int4 sv = __ldg(reinterpret_cast<const int4 *>(srow + d0 + q));
-                slot[q] = sv.x, slot[q + 1] = sv.y, slot[q + 2] = sv.z, slot[q + 3] = sv.w;
-                if (WEIGHTED) {
-                    const float4 wv = __ldg(reinterpret_cast<const float4 *>(wrow + d0 + q));
-                    w[q] = wv.x, w[q + 1] = wv.y, w[q + 2] = wv.z, w[q + 3] = wv.w;
-                } else {
-                    w[q] = w[q + 1] = w[q + 2] = w[q + 3] = 1.0f;
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < G; ++q) {
-                if (slot[q] >= p.m) {  // guard: never expected from the routing pass
-                    if (tid == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
-                    slot[q] = -1;
-                }
-                if (!((p.active >> ((d0 + q) & 31)) & 1u)) slot[q] = -1;  // rank gone
-            }
+        // The token's destinations, ascending; up to G rows in flight at once.
+        uint32_t live = __ballot_sync(kFull, slot_l >= 0);
+        while (live != 0) {
+            int dq[G], sq[G];
+            float wq[G];
             uint4 v[G][VPT];
 #pragma unroll
             for (int q = 0; q < G; ++q) {
-                if (slot[q] >= 0) {
-                    const long long base =
-                        (((long long)(d0 + q) * p.R + s) * p.m + slot[q]) * p.H8;
+                dq[q] = live != 0 ? __ffs(live) - 1 : -1;
+                if (live != 0) live &= live - 1;
+                const int src = dq[q] < 0 ? 0 : dq[q];
+                sq[q] = __shfl_sync(kFull, slot_l, src);
+                wq[q] = WEIGHTED ? __shfl_sync(kFull, w_l, src) : 1.0f;
+                if (dq[q] >= 0) {
+                    const long long base = (((long long)dq[q] * p.R + s) * p.m + sq[q]) * p.H8;
 #pragma unroll
                     for (int j = 0; j < VPT; ++j) {
                         const int c = tid + j * nthreads;
@@ -143,12 +152,14 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
             }
 #pragma unroll
             for (int q = 0; q < G; ++q) {
-                if (slot[q] >= 0) {
+                if (dq[q] >= 0) {
 #pragma unroll
-                    for (int j = 0; j < VPT; ++j) accumulate8<WEIGHTED>(acc[j], v[q][j], w[q]);
+                    for (int j = 0; j < VPT; ++j) accumulate8<WEIGHTED>(acc[j], v[q][j], wq[q]);
                 }
             }
         }
+        slot_l = slot_n;
+        w_l = w_n;
 
         if (!FUSED) {
 #pragma unroll
@@ -221,12 +232,16 @@ cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStrea
     return cudaGetLastError();
 }
 
-constexpr int kGroup = 4;
+// Rows in flight per group: 8 while a thread holds at most 2 vectors of a
+// row, else 4 (register budget).
+template <int VPT>
+constexpr int group_of() { return VPT <= 2 ? 8 : 4; }
 
 template <int VPT>
 cudaError_t dispatch_flags(bool weighted, bool fused, const CombineParams *p, int nthreads,
                            int num_sms, LaunchShape *shape, const LaunchShape *use,
                            cudaStream_t st) {
+    constexpr int kGroup = group_of<VPT>();
     if (p == nullptr) {
         if (weighted && fused) return shape_of<VPT, kGroup, true, true>(nthreads, num_sms, shape);
         if (weighted) return shape_of<VPT, kGroup, true, false>(nthreads, num_sms, shape);

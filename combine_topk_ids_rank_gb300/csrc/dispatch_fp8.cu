@@ -27,11 +27,13 @@
 
 #include "moe_a2a.h"
 
+#include <cstdlib>
+
 namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kThreads = 256;          // at most; the launch fits the row
+constexpr int kThreads = 256;          // at most; the launch fits the row (fit_threads)
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -200,17 +202,25 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *x,
     }
 }
 
-// Threads per CTA: the fewest whole warps that cover the row with VPT
-// vectors each (224 at H = 7168, VPT = 4), so no thread idles at the tail.
-int fit_threads(int H8, int VPT) { return ((H8 + VPT - 1) / VPT + 31) / 32 * 32; }
+// Threads per CTA: 128 while a row fits in 8 vectors per thread, else the
+// fewest whole warps that cover it with 8; every thread then takes VPT =
+// ceil(H8 / threads) vectors (H = 7168: 128 threads x 7 vectors, no idle
+// tail), so the per-token work (reduction, scale, routing reads, address
+// arithmetic) is spread over as many elements per thread as the registers
+// allow.
+int fit_threads(int H8) {
+    if (H8 <= 8 * 128) return 128;
+    return ((H8 + 7) / 8 + 31) / 32 * 32;
+}
 
 template <int VPT>
 cudaError_t launch_t(DispatchFp8Params p, int num_sms, cudaStream_t st) {
-    const int threads = fit_threads(p.H8, VPT);
-    // Stages: about 56 KB of bf16 rows per CTA (4 rows at H = 7168), at
-    // least 2; three CTAs per SM.
+    const int threads = fit_threads(p.H8);
+    // Stages: about 42 KB of bf16 rows per CTA (3 rows at H = 7168), at
+    // least 2.  MOE_FP8_DISPATCH_STAGES overrides (2..8).
     const size_t stride = ((size_t)p.H * 2 + 127) / 128 * 128;
-    int S = (int)((56u << 10) / stride);
+    int S = (int)((42u << 10) / stride);
+    if (const char *e = std::getenv("MOE_FP8_DISPATCH_STAGES")) S = std::atoi(e);
     S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
     p.stages = S;
     const size_t smem = stride * S;
@@ -240,7 +250,7 @@ cudaError_t launch_t(DispatchFp8Params p, int num_sms, cudaStream_t st) {
 template <int VPT>
 cudaError_t launch_q(const float *x, long long rows, int H, uint8_t *q, float *scale,
                      int num_sms, cudaStream_t st) {
-    const int threads = fit_threads(H / 8, VPT);
+    const int threads = fit_threads(H / 8);
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, quantize_rows_kernel<VPT>, threads, 0);
@@ -252,29 +262,53 @@ cudaError_t launch_q(const float *x, long long rows, int H, uint8_t *q, float *s
     return cudaGetLastError();
 }
 
-int vectors_per_thread(int H8) { return (H8 + kThreads - 1) / kThreads; }
+int vectors_per_thread(int H8) {
+    const int nt = fit_threads(H8);
+    return (H8 + nt - 1) / nt;
+}
+
+// Instantiations for VPT = 1..8.
+template <template <int> class F, typename... A>
+cudaError_t by_vpt(int vpt, A... a) {
+    switch (vpt) {
+        case 1: return F<1>::run(a...);
+        case 2: return F<2>::run(a...);
+        case 3: return F<3>::run(a...);
+        case 4: return F<4>::run(a...);
+        case 5: return F<5>::run(a...);
+        case 6: return F<6>::run(a...);
+        case 7: return F<7>::run(a...);
+        case 8: return F<8>::run(a...);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int VPT>
+struct DispatchLaunch {
+    static cudaError_t run(const DispatchFp8Params *p, int num_sms, cudaStream_t st) {
+        return launch_t<VPT>(*p, num_sms, st);
+    }
+};
+
+template <int VPT>
+struct QuantLaunch {
+    static cudaError_t run(const float *x, long long rows, int H, uint8_t *q, float *scale,
+                           int num_sms, cudaStream_t st) {
+        return launch_q<VPT>(x, rows, H, q, scale, num_sms, st);
+    }
+};
 
 }  // namespace
 
 cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, int num_sms, cudaStream_t st) {
-    if (p.H % 16 != 0) return cudaErrorInvalidValue;
-    const int need = vectors_per_thread(p.H8);
-    if (need <= 1) return launch_t<1>(p, num_sms, st);
-    if (need <= 2) return launch_t<2>(p, num_sms, st);
-    if (need <= 4) return launch_t<4>(p, num_sms, st);
-    if (need <= 8) return launch_t<8>(p, num_sms, st);
-    return cudaErrorInvalidValue;
+    if (p.H % 16 != 0 || p.H8 > 2048) return cudaErrorInvalidValue;
+    return by_vpt<DispatchLaunch>(vectors_per_thread(p.H8), &p, num_sms, st);
 }
 
 cudaError_t launch_quantize_rows_fp8(const float *x, long long rows, int H, uint8_t *q,
                                      float *scale, int num_sms, cudaStream_t st) {
-    if (H % 8 != 0) return cudaErrorInvalidValue;
-    const int need = vectors_per_thread(H / 8);
-    if (need <= 1) return launch_q<1>(x, rows, H, q, scale, num_sms, st);
-    if (need <= 2) return launch_q<2>(x, rows, H, q, scale, num_sms, st);
-    if (need <= 4) return launch_q<4>(x, rows, H, q, scale, num_sms, st);
-    if (need <= 8) return launch_q<8>(x, rows, H, q, scale, num_sms, st);
-    return cudaErrorInvalidValue;
+    if (H % 8 != 0 || H / 8 > 2048) return cudaErrorInvalidValue;
+    return by_vpt<QuantLaunch>(vectors_per_thread(H / 8), x, rows, H, q, scale, num_sms, st);
 }
 
 }  // namespace moe

@@ -26,7 +26,8 @@ struct TokenMap {
 __host__ __device__ inline void token_of(const TokenMap &m, int R, long long i, int &s,
                                          int &t) {
     if (m.uniform) {
-        s = (int)(i / m.stride);
+        // i < R * stride <= 2^29: a 32-bit division suffices
+        s = (int)((uint32_t)i / (uint32_t)m.stride);
     } else {
         s = 0;
         while (s + 1 < R && i >= m.first[s + 1]) ++s;
