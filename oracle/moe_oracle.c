@@ -220,6 +220,48 @@ void oracle_dispatch(int R, int T, int K, int E, int H, int m,
 }
 
 /* ------------------------------------------------------------------------ */
+/* a4: the fused epilogue of one reduced row (shared by every combine)       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * acc[0..H): the token's reduced fp32 row.  res_row == NULL: unfused,
+ * out_row = bf16(acc), y_row = acc.  Otherwise hsum = acc + f32(res_row)
+ * (fp32 add), rout_row = bf16(hsum) (if not NULL), ms = sum hsum^2 / H
+ * (double), y = hsum * (1 / sqrt(ms + eps)) * f32(gamma) (double), y_row = y,
+ * out_row = bf16((float)y).  hsum is scratch of H floats.
+ * [MG] "The Message Itself": residual add + RMSNorm after the reduction.
+ */
+static void finish_row(int H, const float *acc, const uint16_t *res_row,
+                       const uint16_t *gamma, float eps, float *hsum,
+                       uint16_t *out_row, uint16_t *rout_row, double *y_row)
+{
+    if (res_row == 0) {
+        /* unfused: the reduced sum is the output, narrowed once */
+        for (int h = 0; h < H; ++h) {
+            out_row[h] = oracle_bf16_from_f32(acc[h]);
+            if (y_row)
+                y_row[h] = (double)acc[h];
+        }
+        return;
+    }
+    /* residual add, then RMSNorm of the fp32 sum */
+    double sumsq = 0.0;
+    for (int h = 0; h < H; ++h) {
+        hsum[h] = acc[h] + oracle_f32_from_bf16(res_row[h]);
+        if (rout_row)
+            rout_row[h] = oracle_bf16_from_f32(hsum[h]);
+        sumsq += (double)hsum[h] * (double)hsum[h];
+    }
+    double inv = 1.0 / sqrt(sumsq / (double)H + (double)eps);
+    for (int h = 0; h < H; ++h) {
+        double y = (double)hsum[h] * inv * (double)oracle_f32_from_bf16(gamma[h]);
+        if (y_row)
+            y_row[h] = y;
+        out_row[h] = oracle_bf16_from_f32((float)y);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* a3 + a4: combine (reduce once, ascending rank, fp32) and fused epilogue   */
 /* ------------------------------------------------------------------------ */
 
@@ -289,31 +331,8 @@ void oracle_combine(int R, int T, int H, int m, int weighted,
                 acc_out[o + h] = a;
         }
 
-        if (residual == 0) {
-            /* unfused: the reduced sum is the output, narrowed once */
-            for (int h = 0; h < H; ++h) {
-                out[o + h] = oracle_bf16_from_f32(acc[h]);
-                if (y_ref)
-                    y_ref[o + h] = (double)acc[h];
-            }
-            continue;
-        }
-
-        /* a4: residual add, then RMSNorm of the fp32 sum */
-        double sumsq = 0.0;
-        for (int h = 0; h < H; ++h) {
-            hsum[h] = acc[h] + oracle_f32_from_bf16(residual[((size_t)s * T + t) * H + h]);
-            if (residual_out)
-                residual_out[o + h] = oracle_bf16_from_f32(hsum[h]);
-            sumsq += (double)hsum[h] * (double)hsum[h];
-        }
-        double inv = 1.0 / sqrt(sumsq / (double)H + (double)eps);
-        for (int h = 0; h < H; ++h) {
-            double y = (double)hsum[h] * inv * (double)oracle_f32_from_bf16(gamma[h]);
-            if (y_ref)
-                y_ref[o + h] = y;
-            out[o + h] = oracle_bf16_from_f32((float)y);
-        }
+        finish_row(H, acc, residual ? residual + ((size_t)s * T + t) * H : 0, gamma, eps,
+                   hsum, out + o, residual_out ? residual_out + o : 0, y_ref ? y_ref + o : 0);
     }
     free(acc);
     free(hsum);
@@ -357,10 +376,12 @@ void oracle_combine_topk_tree(int R, int T, int K, int E, int H, int m,
     long n = tokens ? ntokens : (long)R * T;
     int *slot_dest = (int *)malloc((size_t)P * sizeof(int));
     float *a = (float *)malloc((size_t)P * sizeof(float));
+    float *acc = (float *)malloc((size_t)H * sizeof(float));
     float *hsum = (float *)malloc((size_t)H * sizeof(float));
-    if (!slot_dest || !a || !hsum) {
+    if (!slot_dest || !a || !acc || !hsum) {
         free(slot_dest);
         free(a);
+        free(acc);
         free(hsum);
         return;
     }
@@ -384,7 +405,6 @@ void oracle_combine_topk_tree(int R, int T, int K, int E, int H, int m,
                 slot_dest[k] = d;
         }
 
-        double sumsq = 0.0;
         for (int h = 0; h < H; ++h) {
             for (int k = 0; k < P; ++k) {
                 a[k] = 0.0f;
@@ -398,29 +418,164 @@ void oracle_combine_topk_tree(int R, int T, int K, int E, int H, int m,
             for (int stride = 1; stride < P; stride *= 2)
                 for (int k = 0; k + stride < P; k += 2 * stride)
                     a[k] = oracle_f32_from_bf16(oracle_bf16_from_f32(a[k] + a[k + stride]));
-            if (residual == 0) {
-                out[o + h] = oracle_bf16_from_f32(a[0]);
-                if (y_ref)
-                    y_ref[o + h] = (double)a[0];
-                continue;
-            }
-            hsum[h] = a[0] + oracle_f32_from_bf16(residual[((size_t)flat) * H + h]);
-            if (residual_out)
-                residual_out[o + h] = oracle_bf16_from_f32(hsum[h]);
-            sumsq += (double)hsum[h] * (double)hsum[h];
+            acc[h] = a[0];
         }
-        if (residual == 0)
-            continue;
-        double inv = 1.0 / sqrt(sumsq / (double)H + (double)eps);
-        for (int h = 0; h < H; ++h) {
-            double y = (double)hsum[h] * inv * (double)oracle_f32_from_bf16(gamma[h]);
-            if (y_ref)
-                y_ref[o + h] = y;
-            out[o + h] = oracle_bf16_from_f32((float)y);
-        }
+        finish_row(H, acc, residual ? residual + (size_t)flat * H : 0, gamma, eps, hsum,
+                   out + o, residual_out ? residual_out + o : 0, y_ref ? y_ref + o : 0);
     }
     free(slot_dest);
     free(a);
+    free(acc);
+    free(hsum);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Expert-major layout: every received row carries one expert                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [IX] "Best remaining lead" (the association-order analysis): backends
+ * whose received rows each carry a single expert -- the low-latency padded
+ * layouts -- never meet the per-rank aggregation question; [IX] review of
+ * the harness: those backends declare "weighted-kernel-sum", the gates
+ * being applied by the combine kernel, and the oracle's message sums the
+ * top-k axis in problem order.  Readings (the pages name the layout, not its
+ * arithmetic):
+ *   - expert e has a plane of cap = R * m rows; one row per distinct
+ *     (token, expert) with 0 <= e < E, in ascending (source rank, token);
+ *   - send_row[s][t][k] = e_k * cap + slot for the first k with that expert,
+ *     -1 for a later duplicate or an id outside [0, E);
+ *   - wsum[s][t][k] = sum over the token's k' with the same expert, in
+ *     ascending k', of w[k'] from +0.0f (first occurrence; 0.0f elsewhere);
+ *   - recv_counts[e] = rows of expert e; src_row[e][j] = s * T + t of row j
+ *     (-1 past the count); recv_w[e][j] = the row's wsum;
+ *   - local_expert_counts[e] counts valid (token, k) entries, duplicates
+ *     included, as in the rank layout.
+ * Returns the number of ids outside [-1, E).
+ */
+long oracle_route_experts(int R, int T, int K, int E, int m,
+                          const int32_t *topk_ids, const float *topk_w,
+                          int32_t *send_row, float *wsum, int32_t *recv_counts,
+                          int32_t *src_row, float *recv_w, int32_t *local_expert_counts)
+{
+    const long cap = (long)R * m;
+    long invalid = 0;
+    for (int e = 0; e < E; ++e) {
+        recv_counts[e] = 0;
+        local_expert_counts[e] = 0;
+    }
+    for (long i = 0; i < (long)E * cap; ++i) {
+        src_row[i] = -1;
+        recv_w[i] = 0.0f;
+    }
+    /* sources in ascending order, tokens in ascending order: each distinct
+       expert of a token takes the next row of that expert's plane */
+    for (int s = 0; s < R; ++s) {
+        for (int t = 0; t < T; ++t) {
+            long flat = (long)s * T + t;
+            const int32_t *ids = topk_ids + (size_t)flat * K;
+            const float *w = topk_w + (size_t)flat * K;
+            for (int k = 0; k < K; ++k) {
+                int32_t e = ids[k];
+                send_row[(size_t)flat * K + k] = -1;
+                wsum[(size_t)flat * K + k] = 0.0f;
+                if (e == -1)
+                    continue;
+                if (e < -1 || e >= E) {
+                    invalid += 1;
+                    continue;
+                }
+                local_expert_counts[e] += 1;
+                int first = 1;
+                for (int k2 = 0; k2 < k; ++k2)
+                    if (ids[k2] == e)
+                        first = 0;
+                if (!first)
+                    continue;
+                float sum = 0.0f;
+                for (int k2 = k; k2 < K; ++k2)
+                    if (ids[k2] == e)
+                        sum = sum + w[k2];
+                long j = recv_counts[e];
+                recv_counts[e] += 1;
+                send_row[(size_t)flat * K + k] = (int32_t)(e * cap + j);
+                wsum[(size_t)flat * K + k] = sum;
+                src_row[e * cap + j] = (int32_t)flat;
+                recv_w[e * cap + j] = sum;
+            }
+        }
+    }
+    return invalid;
+}
+
+/*
+ * recv_x [E][cap][H] bf16: row j of expert e = x[src_row[e][j]]; only rows
+ * j < recv_counts[e] are written.
+ */
+void oracle_dispatch_experts(int R, int E, int H, int m, const uint16_t *x,
+                             const int32_t *recv_counts, const int32_t *src_row,
+                             uint16_t *recv_x)
+{
+    const long cap = (long)R * m;
+    for (int e = 0; e < E; ++e) {
+        for (int j = 0; j < recv_counts[e]; ++j) {
+            long flat = src_row[e * cap + j];
+            for (int h = 0; h < H; ++h)
+                recv_x[((size_t)e * cap + j) * H + h] = x[(size_t)flat * H + h];
+        }
+    }
+}
+
+/*
+ * For each requested token (flat s*T + t; tokens == NULL means all):
+ *   acc[h] = sum over k ascending with send_row[s][t][k] >= 0 of
+ *            v = f32(expert_out[send_row][h])                   (weighted=0)
+ *            wsum[s][t][k] * v                                   (weighted=1)
+ *            from +0.0f, one fp32 multiply and one fp32 add each
+ * ("weighted-kernel-sum" in problem order), then the epilogue of
+ * finish_row.  expert_out is [E][cap][H] bf16.
+ */
+void oracle_combine_experts(int R, int T, int K, int H, int weighted,
+                            const int32_t *send_row, const float *wsum,
+                            const uint16_t *expert_out, const uint16_t *residual,
+                            const uint16_t *gamma, float eps,
+                            const int64_t *tokens, long ntokens,
+                            float *acc_out, uint16_t *out, uint16_t *residual_out,
+                            double *y_ref)
+{
+    long n = tokens ? ntokens : (long)R * T;
+    float *acc = (float *)malloc((size_t)H * sizeof(float));
+    float *hsum = (float *)malloc((size_t)H * sizeof(float));
+    if (!acc || !hsum) {
+        free(acc);
+        free(hsum);
+        return;
+    }
+    for (long i = 0; i < n; ++i) {
+        long flat = tokens ? (long)tokens[i] : i;
+        size_t o = (size_t)i * H;
+        for (int h = 0; h < H; ++h) {
+            float a = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int32_t row = send_row[(size_t)flat * K + k];
+                if (row < 0)
+                    continue;
+                float v = oracle_f32_from_bf16(expert_out[(size_t)row * H + h]);
+                if (weighted) {
+                    float p = wsum[(size_t)flat * K + k] * v;
+                    a = a + p;
+                } else {
+                    a = a + v;
+                }
+            }
+            acc[h] = a;
+            if (acc_out)
+                acc_out[o + h] = a;
+        }
+        finish_row(H, acc, residual ? residual + (size_t)flat * H : 0, gamma, eps, hsum,
+                   out + o, residual_out ? residual_out + o : 0, y_ref ? y_ref + o : 0);
+    }
+    free(acc);
     free(hsum);
 }
 

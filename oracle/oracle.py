@@ -42,6 +42,13 @@ def _bind(handle):
     handle.oracle_combine_topk_tree.argtypes = ([c_int] * 6 + [p] * 5 + [c_float, p, c_long]
                                                 + [p] * 3)
     handle.oracle_combine_topk_tree.restype = None
+    handle.oracle_route_experts.argtypes = [c_int] * 5 + [p] * 8
+    handle.oracle_route_experts.restype = c_long
+    handle.oracle_dispatch_experts.argtypes = [c_int] * 4 + [p] * 4
+    handle.oracle_dispatch_experts.restype = None
+    handle.oracle_combine_experts.argtypes = ([c_int] * 5 + [p] * 5 + [c_float, p, c_long]
+                                              + [p] * 4)
+    handle.oracle_combine_experts.restype = None
     handle.oracle_f32_from_fp8e4m3.argtypes = [ctypes.c_uint8]
     handle.oracle_f32_from_fp8e4m3.restype = c_float
     handle.oracle_fp8e4m3_from_f32.argtypes = [c_float]
@@ -205,6 +212,75 @@ def combine_topk_tree(routing, topk_ids, num_experts: int, expert_out, residual=
                                _ptr(res), _ptr(gam), float(eps), _ptr(tok), n,
                                _ptr(out), _ptr(rout), _ptr(y))
     return dict(out=out, residual_out=rout, y=y)
+
+
+def route_experts(topk_ids, topk_w, num_experts: int, m: int, handle=None):
+    """Routing of the expert-major layout (one row per distinct (token,
+    expert), planes of cap = R * m rows, ascending (source, token)).
+    topk_ids/topk_w: [R, T, K]."""
+    h = handle or lib()
+    ids = _need(topk_ids, np.int32)
+    R, T, K = ids.shape
+    w = _need(topk_w, np.float32, ids.shape)
+    if T > m:
+        raise ValueError("T > m")
+    E, cap = num_experts, R * m
+    out = dict(
+        send_row=np.empty((R, T, K), np.int32),
+        wsum=np.empty((R, T, K), np.float32),
+        recv_counts=np.empty(E, np.int32),
+        src_row=np.empty((E, cap), np.int32),
+        recv_w=np.empty((E, cap), np.float32),
+        local_expert_counts=np.empty(E, np.int32),
+        cap=cap,
+    )
+    out["invalid"] = h.oracle_route_experts(
+        R, T, K, E, m, _ptr(ids), _ptr(w), _ptr(out["send_row"]), _ptr(out["wsum"]),
+        _ptr(out["recv_counts"]), _ptr(out["src_row"]), _ptr(out["recv_w"]),
+        _ptr(out["local_expert_counts"]))
+    return out
+
+
+def dispatch_experts(x, num_experts: int, m: int, routing, recv_x=None, handle=None):
+    """recv_x [E, cap, H] (uint16 bf16 bits) of the expert-major layout; rows
+    past each count are left as given (zeros if recv_x is None)."""
+    h = handle or lib()
+    xb = _need(x, np.uint16)
+    R, T, H = xb.shape
+    cap = R * m
+    if recv_x is None:
+        recv_x = np.zeros((num_experts, cap, H), np.uint16)
+    h.oracle_dispatch_experts(R, num_experts, H, m, _ptr(xb),
+                              _ptr(_need(routing["recv_counts"], np.int32)),
+                              _ptr(_need(routing["src_row"], np.int32)), _ptr(recv_x))
+    return recv_x
+
+
+def combine_experts(routing, expert_out, weighted: bool, residual=None, gamma=None,
+                    eps: float = 1e-6, tokens=None, handle=None):
+    """Weighted-kernel-sum combine of the expert-major layout (ascending k).
+    expert_out: [E, cap, H] uint16.  Returns dict(acc, out, residual_out, y)
+    with one row per requested token."""
+    h = handle or lib()
+    send_row = _need(routing["send_row"], np.int32)
+    R, T, K = send_row.shape
+    eo = _need(expert_out, np.uint16)
+    H = eo.shape[-1]
+    tok = None if tokens is None else _need(tokens, np.int64)
+    n = R * T if tok is None else tok.shape[0]
+    res = gam = rout = None
+    if residual is not None:
+        res = _need(residual, np.uint16, (R, T, H))
+        gam = _need(gamma, np.uint16, (H,))
+        rout = np.empty((n, H), np.uint16)
+    acc = np.empty((n, H), np.float32)
+    out = np.empty((n, H), np.uint16)
+    y = np.empty((n, H), np.float64)
+    h.oracle_combine_experts(R, T, K, H, int(bool(weighted)), _ptr(send_row),
+                             _ptr(_need(routing["wsum"], np.float32)), _ptr(eo), _ptr(res),
+                             _ptr(gam), float(eps), _ptr(tok), n, _ptr(acc), _ptr(out),
+                             _ptr(rout), _ptr(y))
+    return dict(acc=acc, out=out, residual_out=rout, y=y)
 
 
 def fp8_bits(values, handle=None):

@@ -76,6 +76,18 @@ MUTANTS = {
     "fp8_overflow_to_nan": (
         "    if (exp32 == 0xffu || fabsf(f) > 448.0f)\n        return (uint8_t)(sign | 0x7e);",
         "    if (exp32 == 0xffu || fabsf(f) > 448.0f)\n        return (uint8_t)(sign | 0x7f);"),
+    "experts_sources_descending": (
+        "for (int s = 0; s < R; ++s) {\n        for (int t = 0; t < T; ++t) {\n            long flat",
+        "for (int s = R - 1; s >= 0; --s) {\n        for (int t = 0; t < T; ++t) {\n            long flat"),
+    "experts_duplicate_weights_not_summed": (
+        "if (ids[k2] == e)\n                        sum = sum + w[k2];",
+        "if (k2 == k)\n                        sum = sum + w[k2];"),
+    "experts_duplicates_sent_twice": (
+        "if (!first)\n                    continue;",
+        "(void)first;"),
+    "experts_combine_reverse_k": (
+        "for (int k = 0; k < K; ++k) {\n                int32_t row = send_row",
+        "for (int k = K - 1; k >= 0; --k) {\n                int32_t row = send_row"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -105,6 +117,15 @@ class MutantOracle:
 
     def combine_topk_tree(self, *a, **k):
         return real.combine_topk_tree(*a, handle=self.h, **k)
+
+    def route_experts(self, *a, **k):
+        return real.route_experts(*a, handle=self.h, **k)
+
+    def dispatch_experts(self, *a, **k):
+        return real.dispatch_experts(*a, handle=self.h, **k)
+
+    def combine_experts(self, *a, **k):
+        return real.combine_experts(*a, handle=self.h, **k)
 
     def fp8_bits(self, v):
         return real.fp8_bits(v, handle=self.h)
@@ -140,6 +161,11 @@ PIN_TESTS = [
     (pins.test_fp8_saturates_and_keeps_nan, {}),
     (pins.test_fp8_row_scaling_closed_forms, {}),
     (pins.test_fp8_round_trip_within_format_bound, {}),
+    (pins.test_route_experts_brute_force, {"seed": 1}),
+    (pins.test_expert_dispatch_payload_identity, {}),
+    (pins.test_expert_identity_unweighted_counts_distinct_experts, {}),
+    (pins.test_expert_identity_weighted_sums_duplicate_weights, {}),
+    (pins.test_expert_combine_sums_in_problem_order, {}),
 ]
 
 

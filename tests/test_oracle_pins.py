@@ -618,3 +618,151 @@ def test_fp8_round_trip_within_format_bound(oracle):
     back = oracle.fp8_to_f32(q) * sc[:, None]
     xv = f32(x)
     assert (np.abs(back - xv) <= 2.0 ** -4 * np.abs(xv) + 2.0 ** -10 * sc[:, None] * 1.0001).all()
+
+
+# --------------------------------------------------------------------------
+# Expert-major layout (one expert per received row, "weighted-kernel-sum")
+# --------------------------------------------------------------------------
+
+def brute_force_route_experts(ids, w, E, m):
+    """The definition enumerated expert by expert: expert e's rows are the
+    tokens, in ascending (s, t), whose valid ids contain e."""
+    R, T, K = ids.shape
+    cap = R * m
+    counts = np.zeros(E, np.int32)
+    src_row = np.full((E, cap), -1, np.int32)
+    send_row = np.full((R, T, K), -1, np.int32)
+    wsum = np.zeros((R, T, K), np.float32)
+    for e in range(E):
+        j = 0
+        for s in range(R):
+            for t in range(T):
+                ks = [k for k in range(K) if ids[s, t, k] == e]
+                if not ks:
+                    continue
+                acc = F32(0.0)
+                for k in ks:
+                    acc = F32(acc + w[s, t, k])
+                send_row[s, t, ks[0]] = e * cap + j
+                wsum[s, t, ks[0]] = acc
+                src_row[e, j] = s * T + t
+                j += 1
+        counts[e] = j
+    valid = ids[(ids >= 0) & (ids < E)]
+    local = np.bincount(valid, minlength=E).astype(np.int32)
+    return dict(recv_counts=counts, src_row=src_row, send_row=send_row, wsum=wsum,
+                local_expert_counts=local)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_route_experts_brute_force(oracle, seed):
+    rng = np.random.default_rng(40 + seed)
+    R, T, K, E = [(2, 5, 3, 4), (3, 9, 4, 12), (4, 16, 6, 8)][seed]
+    m = T + seed
+    ids = rng.integers(-1, E, (R, T, K)).astype(np.int32)   # -1 and repeats
+    ids[0, 0, :] = -1
+    w = rng.random((R, T, K)).astype(np.float32)
+    got = oracle.route_experts(ids, w, E, m)
+    ref = brute_force_route_experts(ids, w, E, m)
+    for key in ("recv_counts", "src_row", "send_row", "local_expert_counts"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert np.array_equal(got["wsum"].view(np.uint32), ref["wsum"].view(np.uint32))
+    # every (token, distinct valid expert) has exactly one row
+    n_pairs = sum(len(set(x for x in ids[s, t] if 0 <= x < E))
+                  for s in range(R) for t in range(T))
+    assert got["recv_counts"].sum() == n_pairs
+    bad = ids.copy()
+    bad[1, 2, 0] = E
+    assert oracle.route_experts(bad, w, E, m)["invalid"] == 1
+
+
+def _expert_identity(oracle, ids, w, E, H=32, seed=9):
+    """Expert outputs equal to the received rows (identity experts)."""
+    R, T, K = ids.shape
+    x = bits(np.random.default_rng(seed).standard_normal((R, T, H)).astype(np.float32))
+    r = oracle.route_experts(ids, w, E, T)
+    eo = oracle.dispatch_experts(x, E, T, r)
+    return x, r, eo
+
+
+def test_expert_dispatch_payload_identity(oracle):
+    R, T, K, E = 3, 11, 4, 9
+    ids = np.random.default_rng(2).integers(-1, E, (R, T, K)).astype(np.int32)
+    w = np.ones((R, T, K), np.float32)
+    H = 8
+    x = np.zeros((R, T, H), np.uint16)
+    for s in range(R):
+        for t in range(T):
+            x[s, t, :] = bits(np.float32(s * 64 + t))     # the row names its token
+    r = oracle.route_experts(ids, w, E, T)
+    rx = oracle.dispatch_experts(x, E, T, r)
+    for e in range(E):
+        for j in range(r["recv_counts"][e]):
+            s, t = divmod(int(r["src_row"][e, j]), T)
+            assert f32(rx[e, j, 0]) == s * 64 + t and e in ids[s, t]
+
+
+def test_expert_identity_unweighted_counts_distinct_experts(oracle):
+    R, T, K, E = 4, 20, 6, 16
+    ids = np.random.default_rng(3).integers(-1, E, (R, T, K)).astype(np.int32)
+    w = np.ones((R, T, K), np.float32)
+    x, r, eo = _expert_identity(oracle, ids, w, E)
+    out = oracle.combine_experts(r, eo, False)["out"].reshape(R, T, -1)
+    for s in range(R):
+        for t in range(T):
+            n = len(set(v for v in ids[s, t] if 0 <= v < E))
+            assert np.array_equal(out[s, t], bits(F32(n) * f32(x[s, t])))
+
+
+def test_expert_identity_weighted_sums_duplicate_weights(oracle):
+    # weights 1/8 on every slot, duplicates included: sum_k w_k x = x exactly
+    R, T, K, E = 3, 16, 8, 12
+    ids = np.random.default_rng(4).integers(0, E, (R, T, K)).astype(np.int32)
+    ids[0, 0, :] = 5                                    # all eight slots one expert
+    w = np.full((R, T, K), 0.125, np.float32)
+    x, r, eo = _expert_identity(oracle, ids, w, E)
+    out = oracle.combine_experts(r, eo, True)["out"].reshape(R, T, -1)
+    assert np.array_equal(out, x)
+    assert r["wsum"][0, 0, 0] == 1.0 and (r["send_row"][0, 0, 1:] == -1).all()
+
+
+def test_expert_combine_sums_in_problem_order(oracle):
+    # top-k order [5, 1, 3] with messages 2^24, 1, -2^24: in problem order
+    # (2^24 + 1) rounds to 2^24 and the sum is 0; in expert-id order it is 1
+    E, H = 8, 4
+    ids = np.array([[[5, 1, 3]]], np.int32)
+    w = np.ones((1, 1, 3), np.float32)
+    r = oracle.route_experts(ids, w, E, 1)
+    eo = np.zeros((E, 1, H), np.uint16)
+    for e, v in ((5, 2.0 ** 24), (1, 1.0), (3, -2.0 ** 24)):
+        eo[e, 0, :] = bits(np.full(H, v, np.float32))
+    out = oracle.combine_experts(r, eo, False)
+    assert (out["acc"] == 0.0).all()
+
+
+def test_expert_combine_fused_matches_rank_layout_when_one_expert_per_rank(oracle):
+    # with one expert per rank and the expert outputs equal per rank, the two
+    # layouts describe the same sums in the same (ascending) order
+    R, T, K, E, H = 4, 12, 4, 4, 16
+    ids = np.stack([np.stack([np.random.default_rng(s * 100 + t).permutation(E)[:K]
+                              for t in range(T)]) for s in range(R)]).astype(np.int32)
+    ids.sort(axis=2)
+    w = np.random.default_rng(6).random((R, T, K)).astype(np.float32)
+    rng = np.random.default_rng(7)
+    res = bits(rng.standard_normal((R, T, H)).astype(np.float32))
+    gam = bits(1 + 0.1 * rng.standard_normal(H).astype(np.float32))
+    re = oracle.route_experts(ids, w, E, T)
+    rr = oracle.route(ids, w, E, T)
+    eo_e = np.zeros((E, R * T, H), np.uint16)
+    eo_r = np.zeros((R, R, T, H), np.uint16)
+    vals = bits(rng.standard_normal((R, T, E, H)).astype(np.float32))
+    for s in range(R):
+        for t in range(T):
+            for k in range(K):
+                e = ids[s, t, k]
+                eo_e[e, re["send_row"][s, t, k] - e * R * T] = vals[s, t, e]
+                eo_r[e, s, rr["send_slot"][s, t, e]] = vals[s, t, e]
+    a = oracle.combine_experts(re, eo_e, True, res, gam, 1e-6)
+    b = oracle.combine(rr, eo_r, True, res, gam, 1e-6)
+    assert np.array_equal(a["out"], b["out"])
+    assert np.array_equal(a["residual_out"], b["residual_out"])
