@@ -89,15 +89,20 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
     auto load_route = [&](long long i, int &slot, float &w) {
         slot = -1;
         w = 0.0f;
-        if (i < p.tokens && lane < p.R && ((p.active >> lane) & 1u)) {
+        if (i < p.tokens && lane < p.dest.P) {
             int s, t;
             token_of(p.map, p.R, i, s, t);
             const long long tok = (long long)s * p.map.stride + t;
-            slot = __ldg(p.send_slot + tok * p.RP + lane);
-            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.RP + lane);
-            if (slot >= p.m) {  // guard: never expected from the routing pass
-                if (warp == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
-                slot = -1;
+            slot = __ldg(p.send_slot + tok * p.dest.P + lane);
+            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.dest.P + lane);
+            if (slot >= 0) {
+                if (dest_row(p.dest, p.R, p.m, lane, s, slot) < 0) {
+                    // guard: never expected from the routing pass
+                    if (warp == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                    slot = -1;
+                } else if (!((p.active >> dest_rank(p.dest, lane, slot)) & 1u)) {
+                    slot = -1;  // the rank is gone
+                }
             }
         }
     };
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
                 sq[q] = __shfl_sync(kFull, slot_l, src);
                 wq[q] = WEIGHTED ? __shfl_sync(kFull, w_l, src) : 1.0f;
                 if (dq[q] >= 0) {
-                    const long long base = (((long long)dq[q] * p.R + s) * p.m + sq[q]) * p.H8;
+                    const long long base = dest_row(p.dest, p.R, p.m, dq[q], s, sq[q]) * p.H8;
 #pragma unroll
                     for (int j = 0; j < VPT; ++j) {
                         const int c = tid + j * nthreads;

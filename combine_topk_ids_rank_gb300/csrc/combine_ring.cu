@@ -147,11 +147,20 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
     auto load_route = [&](long long i, int &slot, float &w) {
         slot = -1;
         w = 0.0f;
-        if (i < p.tokens && lane < p.R && ((p.active >> lane) & 1u)) {
+        if (i < p.tokens && lane < p.dest.P) {
             int s;
             const long long tok = row_of(i, s);
-            slot = __ldg(p.send_slot + tok * p.RP + lane);
-            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.RP + lane);
+            slot = __ldg(p.send_slot + tok * p.dest.P + lane);
+            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.dest.P + lane);
+            if (slot >= 0) {
+                if (dest_row(p.dest, p.R, p.m, lane, s, slot) < 0) {
+                    // guard: never expected from the routing pass
+                    atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                    slot = -1;
+                } else if (!((p.active >> dest_rank(p.dest, lane, slot)) & 1u)) {
+                    slot = -1;  // the rank is gone
+                }
+            }
         }
     };
 
@@ -177,11 +186,7 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
         load_route(i + gridDim.x, slot_next, w_next);
         int s;
         const long long tok = row_of(i, s);
-        bool valid = slot >= 0;
-        if (valid && slot >= p.m) {  // guard: never expected from the routing pass
-            atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
-            valid = false;
-        }
+        const bool valid = slot >= 0;
         const uint32_t bal = __ballot_sync(kFull, valid);
 
         const int ds = j % kDesc;
@@ -203,7 +208,7 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
             const int d = __ffs(b) - 1;
             b &= b - 1;
             const int sl = __shfl_sync(kFull, slot, d);
-            const long long row = ((long long)d * p.R + s) * p.m + sl;
+            const long long row = dest_row(p.dest, p.R, p.m, d, s, sl);
             if (!issue_row(eo + row * row_bytes)) {
                 ok = false;
                 break;

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
 
     const long long first = blockIdx.x, step = gridDim.x;
     const long long n = first < p.units ? (p.units - 1 - first) / step + 1 : 0;
-    const uint32_t meta_bytes = (uint32_t)p.RP * 4u;
+    const uint32_t meta_bytes = (uint32_t)p.dest.P * 4u;
 
     auto unit_bytes = [&](int chunk) -> uint32_t {
         const int left = p.row_bytes - chunk * p.chunk_bytes;
@@ -83,7 +83,8 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         unit_of(i, s, token, chunk);
         const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
-        ptx::bulk_g2s(buf + p.chunk_bytes, p.send_slot + token * p.RP, meta_bytes, &bars[stage]);
+        ptx::bulk_g2s(buf + p.chunk_bytes, p.send_slot + token * p.dest.P, meta_bytes,
+                      &bars[stage]);
     };
     auto issue = [&](long long i) {
         issue_row(i);
@@ -115,14 +116,14 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         const int32_t *slots = reinterpret_cast<const int32_t *>(buf + p.chunk_bytes);
         const uint32_t bytes = unit_bytes(chunk);
         const long long col = (long long)chunk * p.chunk_bytes;
-        for (int d = 0; d < p.R; ++d) {
+        for (int d = 0; d < p.dest.P; ++d) {
             const int32_t slot = slots[d];
             if (slot < 0) continue;
-            if (slot >= p.m) {  // guard: never expected from the routing pass
+            const long long row = dest_row(p.dest, p.R, p.m, d, s, slot);
+            if (row < 0) {  // guard: never expected from the routing pass
                 atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
                 continue;
             }
-            const long long row = ((long long)d * p.R + s) * p.m + slot;
             ptx::bulk_s2g(p.recv_x + row * p.row_bytes + col, buf, bytes);
         }
         ptx::bulk_commit();
@@ -145,12 +146,12 @@ int env_int(const char *name, int fallback) {
 
 }  // namespace
 
-cudaError_t dispatch_prepare(int row_bytes, int RP, int num_sms, DispatchParams *p,
+cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, DispatchParams *p,
                              LaunchShape *shape) {
     const int chunks = (row_bytes + kMaxChunk - 1) / kMaxChunk;
     int chunk = (row_bytes + chunks - 1) / chunks;
     chunk = (chunk + 15) / 16 * 16;
-    const int stage_bytes = (chunk + RP * 4 + 127) / 128 * 128;
+    const int stage_bytes = (chunk + P * 4 + 127) / 128 * 128;
     int stages = 65536 / stage_bytes;
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     stages = env_int("MOE_DISPATCH_STAGES", stages);

@@ -54,7 +54,7 @@ template <int VPT>
 __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const DispatchFp8Params p) {
     extern __shared__ __align__(128) uint8_t smem[];  // p.stages bf16 rows
     __shared__ uint64_t full[kMaxStages];
-    __shared__ int32_t slots[2][kMaxRanks];
+    __shared__ long long rows[2][kMaxTopK];  // destination rows (-1: none)
     __shared__ float red[2][kWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nt = blockDim.x, nw = nt >> 5;
@@ -89,13 +89,15 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
         int s, t;
         token_of(p.map, p.R, i, s, t);
         const long long tok = (long long)s * p.map.stride + t;
-        if (tid < p.R) {
-            int sl = p.send_slot[tok * p.RP + tid];
-            if (sl >= p.m) {  // guard: never expected from the routing pass
-                atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
-                sl = -1;
+        if (tid < p.dest.P) {
+            const int sl = p.send_slot[tok * p.dest.P + tid];
+            long long row = -1;
+            if (sl >= 0) {
+                row = dest_row(p.dest, p.R, p.m, tid, s, sl);
+                if (row < 0)  // guard: never expected from the routing pass
+                    atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
             }
-            slots[par][tid] = sl;
+            rows[par][tid] = row;
         }
         const int b = (int)(k % S);
         ok = ptx::mbar_wait_bounded(&full[b], (uint32_t)((k / S) & 1), kWaitLimit);
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
         if (lane == 0) red[par][warp] = amax;
         // One barrier per token.  It also releases stage b (every thread has
         // its vectors in registers) and makes the wait outcome collective.
-        // red[] and slots[] alternate by token parity: no thread reaches the
+        // red[] and rows[] alternate by token parity: no thread reaches the
         // barrier of token k+2 before all have passed that of k+1, i.e.
         // finished token k.
         if (!__syncthreads_and(ok)) {
@@ -136,10 +138,9 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
         for (int j = 0; j < VPT; ++j) unpack8(cur[j], f[j]);
         uint2 q[VPT];
         fp8::quantize_row<VPT>(f, rs, q);
-        for (int d = 0; d < p.R; ++d) {
-            const int sl = slots[par][d];
-            if (sl < 0) continue;
-            const long long dst_row = ((long long)d * p.R + s) * p.m + sl;
+        for (int d = 0; d < p.dest.P; ++d) {
+            const long long dst_row = rows[par][d];
+            if (dst_row < 0) continue;
             uint2 *dst = reinterpret_cast<uint2 *>(p.recv_x8 + dst_row * p.H);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {

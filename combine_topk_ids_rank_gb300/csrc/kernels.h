@@ -83,14 +83,61 @@ struct RouteScanParams {
     int R, K, E, Epr, RP, m, ntiles, tile;
 };
 
+// Expert-major layout routing (route_expert.cu).
+constexpr int kMaxTopK = 32;
+constexpr int kMaxExpertsExpertLayout = 1024;
+struct RouteExpertParams {
+    const int32_t *topk_ids;  // [R][stride][K]
+    const float *topk_w;      // [R][stride][K]
+    int32_t *tile_counts;     // [R][ntiles][E]
+    int32_t *send_row;        // [R][stride][KP]: absolute row of the expert planes or -1
+    float *wsum;              // [R][stride][KP]
+    int32_t *src_token;       // [E][cap]: s * stride + t
+    float *recv_w;            // [E][cap]
+    int32_t *recv_counts;     // [E]
+    int32_t *local_counts;    // [E], zeroed before the call
+    uint32_t *flags;
+    TokenMap map;
+    uint32_t active;
+    int R, K, E, Epr, KP, cap, ntiles;
+};
+int route_expert_tile();
+cudaError_t launch_route_expert(const RouteExpertParams &p, cudaStream_t st);
+
+// Where the entries of a token's send row point.  Rank layout: entry d is
+// the token's slot in plane (d, s), i.e. row (d * R + s) * m + slot of the
+// receive region.  Expert layout: entry k already is the absolute row
+// (e * cap + slot) of the expert planes.
+struct DestRows {
+    int P;           // entries per send row: RP (rank) or KP (expert)
+    int expert;      // 0: rank planes, 1: absolute rows
+    long long rows;  // rows of the receive region (expert layout guard)
+    int cap;         // rows per expert plane (expert layout)
+    int Epr;         // experts per rank (expert layout: owner of a row)
+};
+
+// Row of the receive region for send-row entry d holding v >= 0, or -1 if
+// v lies outside its plane (a guard; never produced by the routing pass).
+__device__ __forceinline__ long long dest_row(const DestRows &D, int R, int m, int d, int s,
+                                              int v) {
+    if (D.expert) return v < D.rows ? (long long)v : -1;
+    return v < m ? ((long long)d * R + s) * m + v : -1;
+}
+
+// Rank that owns send-row entry d holding v >= 0 (for the active-rank test).
+__device__ __forceinline__ int dest_rank(const DestRows &D, int d, int v) {
+    return D.expert ? (v / D.cap) / D.Epr : d;
+}
+
 // Dispatch rows: x[s][t] -> recv_x[d][s][slot] for every destination of
 // the token, staged through shared memory with bulk asynchronous copies.
 struct DispatchParams {
     const uint8_t *x;          // bf16 [R][T][H] as bytes
     const int32_t *send_slot;  // [R][T][RP]
-    uint8_t *recv_x;           // bf16 [R][R][m][H] as bytes
+    uint8_t *recv_x;           // bf16 receive rows as bytes
     uint32_t *flags;
     TokenMap map;
+    DestRows dest;
     int R, RP, m;
     int row_bytes;             // 2H
     int chunk_bytes;           // <= row_bytes, multiple of 16
@@ -115,6 +162,7 @@ struct CombineParams {
     uint32_t *flags;
     float eps;
     TokenMap map;
+    DestRows dest;
     uint32_t active;              // ranks whose messages are summed
     int R, RP, m, H, H8;          // H8 = H / 8 (16-byte vectors per row)
     int ring_slots;               // shared-memory row buffers (ring kernel)
@@ -147,8 +195,9 @@ struct LaunchShape {
 cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st);
 cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pdl);
 
-// Dispatch: ring depth and per-SM residency for a row size.
-cudaError_t dispatch_prepare(int row_bytes, int RP, int num_sms, DispatchParams *p,
+// Dispatch: ring depth and per-SM residency for a row size and P send-row
+// entries per token.
+cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, DispatchParams *p,
                              LaunchShape *shape);
 cudaError_t launch_dispatch_rows(const DispatchParams &p, const LaunchShape &shape,
                                  cudaStream_t st, bool pdl);
@@ -171,10 +220,11 @@ cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fuse
 struct DispatchFp8Params {
     const uint16_t *x;        // bf16 [R][T][H]
     const int32_t *send_slot; // [R][T][RP]
-    uint8_t *recv_x8;         // e4m3 [R][R][m][H]
-    float *recv_scale;        // [R][R][m]
+    uint8_t *recv_x8;         // e4m3 receive rows [rows][H]
+    float *recv_scale;        // [rows]
     uint32_t *flags;
     TokenMap map;
+    DestRows dest;
     int R, RP, m, H, H8;
     int stages;               // set by the launcher
     long long tokens;

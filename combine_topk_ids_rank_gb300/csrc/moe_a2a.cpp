@@ -31,7 +31,9 @@ struct Layout {
     size_t send_slot, dest_weight, topk_dest, tile_counts, tile_prefix, tile_ticket, hist_accum,
         flags;
     size_t total;
+    int layout;      // MOE_LAYOUT_*
     int RP, ntiles_max;
+    int P;           // send-row entries per token: RP (rank) or KP (expert)
 };
 
 bool config_ok(const moe_a2a_config_t *c) {
@@ -46,19 +48,49 @@ bool config_ok(const moe_a2a_config_t *c) {
 }
 
 // Regions of the workspace, each 256-byte aligned, sized for M tokens.
-bool compute_layout(const moe_a2a_config_t *c, Layout *L) {
+bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
     if (!config_ok(c)) return false;
+    if (layout != MOE_LAYOUT_RANK && layout != MOE_LAYOUT_EXPERT) return false;
     const size_t R = c->ep_size, M = c->max_tokens_per_rank, H = c->hidden;
     const size_t E = c->num_experts, K = c->top_k;
+    L->layout = layout;
     L->RP = (int)((R + 3) / 4 * 4);
-    L->ntiles_max = (int)((M + moe::kRouteMinTile - 1) / moe::kRouteMinTile);
-    const size_t RP = L->RP, NT = L->ntiles_max;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off = align_up(off + bytes, kAlign);
         return o;
     };
+    if (layout == MOE_LAYOUT_EXPERT) {
+        // Expert planes of cap = R * M rows; one row per (token, expert).
+        if (E > (size_t)moe::kMaxExpertsExpertLayout) return false;
+        const size_t KP = (K + 3) / 4 * 4, cap = R * M;
+        if (E * cap >= ((size_t)1 << 31)) return false;  // rows are int32 in the send table
+        const size_t NT = (M + moe::route_expert_tile() - 1) / moe::route_expert_tile();
+        L->P = (int)KP;
+        L->ntiles_max = (int)NT;
+        L->recv_x = take(E * cap * H * 2);
+        L->expert_out = take(E * cap * H * 2);
+        L->recv_ids = take(0);
+        L->recv_w = take(E * cap * 4);
+        L->recv_scale = take(E * cap * 4);
+        L->src_token = take(E * cap * 4);
+        L->recv_counts = take(E * 4);
+        L->local_counts = take(E * 4);
+        L->send_slot = take(R * M * KP * 4);
+        L->dest_weight = take(R * M * KP * 4);
+        L->topk_dest = take(0);
+        L->tile_counts = take(R * NT * E * 4);
+        L->tile_prefix = take(0);
+        L->tile_ticket = take(0);
+        L->hist_accum = take(0);
+        L->flags = take(kAlign);
+        L->total = off;
+        return true;
+    }
+    L->P = L->RP;
+    L->ntiles_max = (int)((M + moe::kRouteMinTile - 1) / moe::kRouteMinTile);
+    const size_t RP = L->RP, NT = L->ntiles_max;
     L->recv_x = take(R * R * M * H * 2);
     L->expert_out = take(R * R * M * H * 2);
     L->recv_ids = take(R * R * M * K * 4);
@@ -124,14 +156,25 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
         cudaSuccess)
         return MOE_ERR_CUDA;
     std::memset(&h->dispatch_tmpl, 0, sizeof h->dispatch_tmpl);
-    if (moe::dispatch_prepare(2 * h->cfg.hidden, h->L.RP, h->num_sms, &h->dispatch_tmpl,
+    if (moe::dispatch_prepare(2 * h->cfg.hidden, h->L.P, h->num_sms, &h->dispatch_tmpl,
                               &h->dispatch_shape) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    h->accum_dirty = true;
+    h->accum_dirty = h->L.layout == MOE_LAYOUT_RANK;
     h->ready = true;
     return MOE_OK;
+}
+
+// Where the send-table entries of the current call point (kernels.h).
+moe::DestRows dest_rows(const moe_a2a_t *h, int m) {
+    moe::DestRows D;
+    D.P = h->L.P;
+    D.expert = h->L.layout == MOE_LAYOUT_EXPERT;
+    D.cap = h->cfg.ep_size * m;
+    D.rows = (long long)h->cfg.num_experts * D.cap;
+    D.Epr = h->cfg.num_experts / h->cfg.ep_size;
+    return D;
 }
 
 void uniform_map(int R, int T, moe::TokenMap *map) {
@@ -142,6 +185,41 @@ void uniform_map(int R, int T, moe::TokenMap *map) {
         map->first[s] = (s < R ? s : R) * T;
     }
     map->first[moe::kMaxRanks] = R * T;
+}
+
+// The row copy of the dispatch phase (after the routing pass queued its
+// send table): bf16 rows, or e4m3 rows + scales in the FP8 receive format.
+int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
+                const moe::DestRows &dest, long long ntok, cudaStream_t st) {
+    const int R = h->cfg.ep_size;
+    uint32_t *flags = at<uint32_t>(h, h->L.flags);
+    if (h->recv_format == MOE_FORMAT_FP8_E4M3) {
+        moe::DispatchFp8Params fp;
+        fp.x = static_cast<const uint16_t *>(d_x);
+        fp.send_slot = at<int32_t>(h, h->L.send_slot);
+        fp.recv_x8 = at<uint8_t>(h, h->L.recv_x);
+        fp.recv_scale = at<float>(h, h->L.recv_scale);
+        fp.flags = flags;
+        fp.map = map;
+        fp.dest = dest;
+        fp.R = R, fp.RP = h->L.RP, fp.m = m;
+        fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
+        fp.tokens = ntok;
+        return moe::launch_dispatch_fp8(fp, h->num_sms, st) == cudaSuccess ? MOE_OK
+                                                                            : MOE_ERR_CUDA;
+    }
+    moe::DispatchParams dp = h->dispatch_tmpl;
+    dp.x = static_cast<const uint8_t *>(d_x);
+    dp.send_slot = at<int32_t>(h, h->L.send_slot);
+    dp.recv_x = at<uint8_t>(h, h->L.recv_x);
+    dp.flags = flags;
+    dp.map = map;
+    dp.dest = dest;
+    dp.R = R, dp.RP = h->L.RP, dp.m = m;
+    dp.units = ntok * dp.chunks;
+    return moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 // The dispatch phase for the tokens described by `map` (rows of stride
@@ -166,12 +244,37 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
     int tmax = 0;
     for (int s = 0; s < R; ++s) tmax = map.count[s] > tmax ? map.count[s] : tmax;
 
+    const bool expert = h->L.layout == MOE_LAYOUT_EXPERT;
+    const moe::DestRows dest = dest_rows(h, m);
     if (ntok == 0) {
-        if (cudaMemsetAsync(h->ws + h->L.recv_counts, 0, sizeof(int32_t) * R * R, st) !=
+        const size_t nrc = expert ? (size_t)E : (size_t)R * R;
+        if (cudaMemsetAsync(h->ws + h->L.recv_counts, 0, sizeof(int32_t) * nrc, st) !=
                 cudaSuccess ||
             cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
                 cudaSuccess)
             return MOE_ERR_CUDA;
+    } else if (expert) {
+        if (cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        moe::RouteExpertParams rp;
+        rp.topk_ids = d_topk_ids;
+        rp.topk_w = d_topk_w;
+        rp.tile_counts = at<int32_t>(h, h->L.tile_counts);
+        rp.send_row = at<int32_t>(h, h->L.send_slot);
+        rp.wsum = at<float>(h, h->L.dest_weight);
+        rp.src_token = at<int32_t>(h, h->L.src_token);
+        rp.recv_w = at<float>(h, h->L.recv_w);
+        rp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+        rp.local_counts = at<int32_t>(h, h->L.local_counts);
+        rp.flags = flags;
+        rp.map = map;
+        rp.active = h->active;
+        rp.R = R, rp.K = K, rp.E = E, rp.Epr = E / R, rp.KP = h->L.P, rp.cap = dest.cap;
+        rp.ntiles = (tmax + moe::route_expert_tile() - 1) / moe::route_expert_tile();
+        if (moe::launch_route_expert(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+        rc = launch_rows(h, d_x, map, m, dest, ntok, st);
+        if (rc != MOE_OK) return rc;
     } else {
         if (h->accum_dirty) {
             if (cudaMemsetAsync(h->ws + h->L.tile_ticket, 0, sizeof(int32_t) * R, st) !=
@@ -220,31 +323,8 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
         h->accum_dirty = false;
 
-        if (h->recv_format == MOE_FORMAT_FP8_E4M3) {
-            moe::DispatchFp8Params fp;
-            fp.x = static_cast<const uint16_t *>(d_x);
-            fp.send_slot = rs.send_slot;
-            fp.recv_x8 = at<uint8_t>(h, h->L.recv_x);
-            fp.recv_scale = at<float>(h, h->L.recv_scale);
-            fp.flags = flags;
-            fp.map = map;
-            fp.R = R, fp.RP = RP, fp.m = m;
-            fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
-            fp.tokens = ntok;
-            if (moe::launch_dispatch_fp8(fp, h->num_sms, st) != cudaSuccess)
-                return MOE_ERR_CUDA;
-        } else {
-            moe::DispatchParams dp = h->dispatch_tmpl;
-            dp.x = static_cast<const uint8_t *>(d_x);
-            dp.send_slot = rs.send_slot;
-            dp.recv_x = at<uint8_t>(h, h->L.recv_x);
-            dp.flags = flags;
-            dp.map = map;
-            dp.R = R, dp.RP = RP, dp.m = m;
-            dp.units = ntok * dp.chunks;
-            if (moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) != cudaSuccess)
-                return MOE_ERR_CUDA;
-        }
+        rc = launch_rows(h, d_x, map, m, dest, ntok, st);
+        if (rc != MOE_OK) return rc;
     }
 
     h->map = map;
@@ -253,20 +333,21 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
     h->phase = 1;
     if (out_view != nullptr) {
         out_view->recv_x = h->ws + h->L.recv_x;
-        out_view->recv_topk_ids = at<int32_t>(h, h->L.recv_ids);
+        out_view->recv_topk_ids = expert ? nullptr : at<int32_t>(h, h->L.recv_ids);
         out_view->recv_topk_w = at<float>(h, h->L.recv_w);
         out_view->src_token = at<int32_t>(h, h->L.src_token);
         out_view->recv_counts = at<int32_t>(h, h->L.recv_counts);
         out_view->local_expert_counts = at<int32_t>(h, h->L.local_counts);
         out_view->send_slot = at<int32_t>(h, h->L.send_slot);
         out_view->dest_weight = at<float>(h, h->L.dest_weight);
-        out_view->plane_stride = m;
+        out_view->plane_stride = expert ? dest.cap : m;
         out_view->tokens_per_rank = map.uniform ? map.stride : -1;
-        out_view->send_stride = RP;
+        out_view->send_stride = h->L.P;
         out_view->token_stride = map.stride;
         const bool fp8 = h->recv_format == MOE_FORMAT_FP8_E4M3;
         out_view->recv_scale = fp8 ? at<float>(h, h->L.recv_scale) : nullptr;
         out_view->recv_format = h->recv_format;
+        out_view->layout = h->L.layout;
     }
     return MOE_OK;
 }
@@ -293,7 +374,7 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
         if (!(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
     }
     if (h->reduction == MOE_REDUCE_BF16_TOPK_TREE && (weighted || out8))
-        return MOE_ERR_INVALID_ARG;
+        return MOE_ERR_INVALID_ARG;  // (the tree exists for the rank layout only)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (h->ntok > 0 && h->reduction == MOE_REDUCE_BF16_TOPK_TREE) {
         moe::CombineTreeParams tp;
@@ -351,6 +432,7 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
         cp.flags = at<uint32_t>(h, h->L.flags);
         cp.map = h->map;
         cp.active = h->active;
+        cp.dest = dest_rows(h, h->m);
         cp.R = h->cfg.ep_size, cp.RP = h->L.RP, cp.m = h->m;
         cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
         cp.tokens = h->ntok;
@@ -372,16 +454,25 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
 extern "C" {
 
 size_t moe_a2a_workspace_bytes(const moe_a2a_config_t *cfg) {
+    return moe_a2a_workspace_bytes_layout(cfg, MOE_LAYOUT_RANK);
+}
+
+size_t moe_a2a_workspace_bytes_layout(const moe_a2a_config_t *cfg, int32_t layout) {
     Layout L;
-    return compute_layout(cfg, &L) ? L.total : 0;
+    return compute_layout(cfg, layout, &L) ? L.total : 0;
 }
 
 int moe_a2a_create(const moe_a2a_config_t *cfg, void *d_workspace, size_t workspace_bytes,
                    moe_a2a_t **out) {
+    return moe_a2a_create_layout(cfg, MOE_LAYOUT_RANK, d_workspace, workspace_bytes, out);
+}
+
+int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_workspace,
+                          size_t workspace_bytes, moe_a2a_t **out) {
     if (out == nullptr) return MOE_ERR_INVALID_ARG;
     *out = nullptr;
     Layout L;
-    if (!compute_layout(cfg, &L)) return MOE_ERR_INVALID_ARG;
+    if (!compute_layout(cfg, layout, &L)) return MOE_ERR_INVALID_ARG;
     if (d_workspace == nullptr || !aligned(d_workspace, kAlign)) return MOE_ERR_INVALID_ARG;
     if (workspace_bytes < L.total) return MOE_ERR_CAPACITY;
     moe_a2a_t *h = new (std::nothrow) moe_a2a_t;
@@ -525,7 +616,8 @@ int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction) {
         h->reduction = reduction;
         return MOE_OK;
     }
-    if (reduction == MOE_REDUCE_BF16_TOPK_TREE && h->cfg.top_k <= 8) {
+    if (reduction == MOE_REDUCE_BF16_TOPK_TREE && h->cfg.top_k <= 8 &&
+        h->L.layout == MOE_LAYOUT_RANK) {
         h->reduction = reduction;
         return MOE_OK;
     }

@@ -30,12 +30,15 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_a2a_destroy", "moe_a2a_phase", "moe_a2a_status_string",
            "moe_route_static_scratch_bytes", "moe_route_static_scratch",
            "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks",
-           "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8")
+           "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8",
+           "moe_a2a_workspace_bytes_layout", "moe_a2a_create_layout")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
 MOE_FORMAT_BF16 = 0
 MOE_FORMAT_FP8_E4M3 = 1
+MOE_LAYOUT_RANK = 0
+MOE_LAYOUT_EXPERT = 1
 
 
 class MoeA2AConfig(ctypes.Structure):
@@ -51,7 +54,8 @@ class MoeDispatchView(ctypes.Structure):
                 ("send_slot", ctypes.c_void_p), ("dest_weight", ctypes.c_void_p),
                 ("plane_stride", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
                 ("send_stride", ctypes.c_int32), ("token_stride", ctypes.c_int32),
-                ("recv_scale", ctypes.c_void_p), ("recv_format", ctypes.c_int32)]
+                ("recv_scale", ctypes.c_void_p), ("recv_format", ctypes.c_int32),
+                ("layout", ctypes.c_int32)]
 
 
 class MoeA2AError(RuntimeError):
@@ -75,6 +79,10 @@ def _load(path: str = LIBRARY):
     lib.moe_a2a_workspace_bytes.restype = sz
     lib.moe_a2a_create.argtypes = [cfgp, p, sz, ctypes.POINTER(p)]
     lib.moe_a2a_create.restype = ctypes.c_int
+    lib.moe_a2a_workspace_bytes_layout.argtypes = [cfgp, i32]
+    lib.moe_a2a_workspace_bytes_layout.restype = sz
+    lib.moe_a2a_create_layout.argtypes = [cfgp, i32, p, sz, ctypes.POINTER(p)]
+    lib.moe_a2a_create_layout.restype = ctypes.c_int
     lib.moe_dispatch.argtypes = [p, p, p, p, i32, i32, p, ctypes.POINTER(MoeDispatchView)]
     lib.moe_dispatch.restype = ctypes.c_int
     lib.moe_combine_payload.argtypes = [p]
@@ -123,6 +131,19 @@ def moe_a2a_create(cfg: MoeA2AConfig, d_workspace: int, workspace_bytes: int):
     h = ctypes.c_void_p()
     st = _lib.moe_a2a_create(ctypes.byref(cfg), ctypes.c_void_p(d_workspace),
                              workspace_bytes, ctypes.byref(h))
+    return st, h
+
+
+def moe_a2a_workspace_bytes_layout(cfg: MoeA2AConfig, layout: int) -> int:
+    return int(_lib.moe_a2a_workspace_bytes_layout(ctypes.byref(cfg), layout))
+
+
+def moe_a2a_create_layout(cfg: MoeA2AConfig, layout: int, d_workspace: int,
+                          workspace_bytes: int):
+    """Returns (status, handle)."""
+    h = ctypes.c_void_p()
+    st = _lib.moe_a2a_create_layout(ctypes.byref(cfg), layout, ctypes.c_void_p(d_workspace),
+                                    workspace_bytes, ctypes.byref(h))
     return st, h
 
 
@@ -277,18 +298,28 @@ class DispatchView:
 
         self.plane_stride, self.send_stride = m, RP
         self.tokens_per_rank, self.token_stride = raw.tokens_per_rank, T
-        self.recv_format = raw.recv_format
+        self.recv_format, self.layout = raw.recv_format, raw.layout
+        # planes: (dst rank, src rank) of m rows, or (expert) of cap = m rows
+        planes = (E,) if raw.layout == MOE_LAYOUT_EXPERT else (R, R)
         if raw.recv_format == MOE_FORMAT_FP8_E4M3:
-            self.recv_x = region(raw.recv_x, torch.float8_e4m3fn, (R, R, m, H))
-            self.recv_scale = region(raw.recv_scale, torch.float32, (R, R, m))
+            self.recv_x = region(raw.recv_x, torch.float8_e4m3fn, planes + (m, H))
+            self.recv_scale = region(raw.recv_scale, torch.float32, planes + (m,))
         else:
-            self.recv_x = region(raw.recv_x, torch.bfloat16, (R, R, m, H))
+            self.recv_x = region(raw.recv_x, torch.bfloat16, planes + (m, H))
             self.recv_scale = None
-        self.recv_topk_ids = region(raw.recv_topk_ids, torch.int32, (R, R, m, K))
-        self.recv_topk_w = region(raw.recv_topk_w, torch.float32, (R, R, m, K))
-        self.src_token = region(raw.src_token, torch.int32, (R, R, m))
-        self.recv_counts = region(raw.recv_counts, torch.int32, (R, R))
-        self.local_expert_counts = region(raw.local_expert_counts, torch.int32, (R, E // R))
+        if raw.layout == MOE_LAYOUT_EXPERT:
+            self.recv_topk_ids = None
+            self.recv_topk_w = region(raw.recv_topk_w, torch.float32, (E, m))
+            self.src_token = region(raw.src_token, torch.int32, (E, m))
+            self.recv_counts = region(raw.recv_counts, torch.int32, (E,))
+            self.local_expert_counts = region(raw.local_expert_counts, torch.int32, (E,))
+        else:
+            self.recv_topk_ids = region(raw.recv_topk_ids, torch.int32, (R, R, m, K))
+            self.recv_topk_w = region(raw.recv_topk_w, torch.float32, (R, R, m, K))
+            self.src_token = region(raw.src_token, torch.int32, (R, R, m))
+            self.recv_counts = region(raw.recv_counts, torch.int32, (R, R))
+            self.local_expert_counts = region(raw.local_expert_counts, torch.int32,
+                                              (R, E // R))
         self.send_slot = region(raw.send_slot, torch.int32, (R, T, RP))
         self.dest_weight = region(raw.dest_weight, torch.float32, (R, T, RP))
 
@@ -297,17 +328,18 @@ class MoeA2A:
     """One dispatch/combine handle over a torch-allocated device workspace."""
 
     def __init__(self, ep_size: int, max_tokens_per_rank: int, hidden: int, num_experts: int,
-                 top_k: int, device=None):
+                 top_k: int, device=None, layout: int = MOE_LAYOUT_RANK):
         import torch
         self.ep_size, self.max_tokens_per_rank, self.hidden = ep_size, max_tokens_per_rank, hidden
-        self.num_experts, self.top_k = num_experts, top_k
+        self.num_experts, self.top_k, self.layout = num_experts, top_k, layout
         self.cfg = config(ep_size, max_tokens_per_rank, hidden, num_experts, top_k)
-        nbytes = moe_a2a_workspace_bytes(self.cfg)
+        nbytes = moe_a2a_workspace_bytes_layout(self.cfg, layout)
         if nbytes == 0:
-            raise MoeA2AError(MOE_ERR_INVALID_ARG, "moe_a2a_workspace_bytes")
+            raise MoeA2AError(MOE_ERR_INVALID_ARG, "moe_a2a_workspace_bytes_layout")
         self.device = torch.device(device if device is not None else "cuda")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
-        st, self.handle = moe_a2a_create(self.cfg, self.workspace.data_ptr(), nbytes)
+        st, self.handle = moe_a2a_create_layout(self.cfg, layout, self.workspace.data_ptr(),
+                                                nbytes)
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_a2a_create")
         self.last_view = None
@@ -326,6 +358,10 @@ class MoeA2A:
                                                                t.dtype, tuple(t.shape)))
         if not t.is_contiguous() or t.device != self.workspace.device:
             raise ValueError("%s must be contiguous on %s" % (name, self.workspace.device))
+
+    def _planes(self):
+        return (self.num_experts,) if self.layout == MOE_LAYOUT_EXPERT else (
+            self.ep_size, self.ep_size)
 
     @property
     def phase(self) -> int:
@@ -381,10 +417,12 @@ class MoeA2A:
         if self.last_view is None:
             raise RuntimeError("no dispatch yet")
         R, H, m = self.ep_size, self.hidden, self.last_view.plane_stride
-        if self._payload is None or self._payload.shape[2] != m:
+        planes = (self.num_experts,) if self.layout == MOE_LAYOUT_EXPERT else (R, R)
+        if self._payload is None or self._payload.shape[-2] != m:
             off = moe_combine_payload(self.handle) - self.workspace.data_ptr()
-            n = R * R * m * H * 2
-            self._payload = self.workspace[off:off + n].view(torch.bfloat16).view(R, R, m, H)
+            n = planes[0] * (planes[1] if len(planes) > 1 else 1) * m * H * 2
+            self._payload = self.workspace[off:off + n].view(torch.bfloat16).view(
+                *planes, m, H)
         return self._payload
 
     def combine(self, expert_out=None, weighted: bool = False, residual=None, gamma=None,
@@ -396,7 +434,7 @@ class MoeA2A:
         R, H = self.ep_size, self.hidden
         T, m = self.last_view.token_stride, self.last_view.plane_stride
         if expert_out is not None:
-            self._check(expert_out, torch.bfloat16, (R, R, m, H), "expert_out")
+            self._check(expert_out, torch.bfloat16, self._planes() + (m, H), "expert_out")
         if residual is not None:
             self._check(residual, torch.bfloat16, (R, T, H), "residual")
             self._check(gamma, torch.bfloat16, (H,), "gamma")
@@ -424,7 +462,7 @@ class MoeA2A:
         R, H = self.ep_size, self.hidden
         T, m = self.last_view.token_stride, self.last_view.plane_stride
         if expert_out is not None:
-            self._check(expert_out, torch.bfloat16, (R, R, m, H), "expert_out")
+            self._check(expert_out, torch.bfloat16, self._planes() + (m, H), "expert_out")
         if residual is not None:
             self._check(residual, torch.bfloat16, (R, T, H), "residual")
             self._check(gamma, torch.bfloat16, (H,), "gamma")

@@ -126,9 +126,11 @@ typedef struct moe_dispatch_view {
     int32_t token_stride;         /* rows per source rank of the token arrays
                                      (x, send_slot, dest_weight, residual, out):
                                      T, or m for moe_dispatch_varlen */
-    float *recv_scale;            /* fp32 [R][R][m]: per-row scale of recv_x
-                                     in the FP8 receive format, else NULL */
+    float *recv_scale;            /* fp32 per-row scale of recv_x in the FP8
+                                     receive format ([R][R][m], or [E][cap]
+                                     in the expert layout), else NULL */
     int32_t recv_format;          /* MOE_FORMAT_* of recv_x */
+    int32_t layout;               /* MOE_LAYOUT_* of the handle */
 } moe_dispatch_view_t;
 
 /* Bytes of device workspace a handle with this config needs (0 if the
@@ -136,12 +138,56 @@ typedef struct moe_dispatch_view {
  * adapter": workspace sized once from the ladder maximum). */
 size_t moe_a2a_workspace_bytes(const moe_a2a_config_t *cfg);
 
+/* ---- Receive layouts --------------------------------------------------------
+ * MOE_LAYOUT_RANK (moe_a2a_create): one plane per (destination rank, source
+ *   rank), one row per (token, destination rank), as described above.
+ * MOE_LAYOUT_EXPERT (moe_a2a_create_layout): every received row carries a
+ *   single expert -- [IX] the association-order analysis ("the low-latency
+ *   padded layouts", whose rows carry one expert each) and the harness
+ *   review ("weighted-kernel-sum": the combine kernel applies the gates).
+ *   Readings: expert e has a plane of cap = R * m rows (R * M in the
+ *   workspace); one row per distinct (token, expert) whose id is valid and
+ *   whose rank is active, rows in ascending (source rank, token).  The view
+ *   of a dispatch then holds
+ *     recv_x       bf16 [E][cap][H] (e4m3 [E][cap][H] in the FP8 format)
+ *     recv_topk_w  fp32 [E][cap]: the row's weight wsum (below)
+ *     recv_topk_ids NULL (a row's expert is its plane)
+ *     src_token    int32 [E][cap]: s * token_stride + t of the row's token
+ *     recv_counts  int32 [E]: rows per expert
+ *     local_expert_counts int32 [E]: valid (token, k) entries, duplicates
+ *                  included
+ *     send_slot    int32 [R][token_stride][send_stride]: entry k = the
+ *                  absolute row e_k * cap + slot of recv_x for the first k
+ *                  carrying that expert; -1 for later duplicates, absent or
+ *                  dead experts and entries k >= K
+ *     dest_weight  fp32, same shape: wsum = sum over the token's slots with
+ *                  that expert, ascending k, of its weights from +0.0 (0
+ *                  where send_slot is -1)
+ *     plane_stride cap; send_stride = top_k rounded up to a multiple of 4.
+ *   Combine sums, per token, over k ascending with send_slot >= 0, of
+ *   v = expert_out[row] (weighted = 0) or wsum * v (weighted = 1) in fp32
+ *   from +0.0, no FMA, then the epilogue of moe_combine; expert_out is
+ *   [E][cap][H].  Requires num_experts <= 1024; the bf16 top-k tree
+ *   reduction is not available in this layout.  The workspace grows as
+ *   E * R * M * H (two bf16 regions): this layout is meant for decode-sized
+ *   batches. */
+enum moe_layout { MOE_LAYOUT_RANK = 0, MOE_LAYOUT_EXPERT = 1 };
+
+/* moe_a2a_workspace_bytes for a layout (0 if the pair is invalid). */
+size_t moe_a2a_workspace_bytes_layout(const moe_a2a_config_t *cfg, int32_t layout);
+
 /* Create a handle over a caller-owned device workspace of at least
  * moe_a2a_workspace_bytes(cfg) bytes, 256-byte aligned.  Host-only: queues
  * nothing and needs no GPU.  On success *out receives the handle in the
  * IDLE phase. */
 int moe_a2a_create(const moe_a2a_config_t *cfg, void *d_workspace,
                    size_t workspace_bytes, moe_a2a_t **out);
+
+/* moe_a2a_create for a layout (MOE_LAYOUT_*); the layout is fixed for the
+ * life of the handle.  MOE_ERR_INVALID_ARG for an unknown layout or a config
+ * the layout cannot take. */
+int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_workspace,
+                          size_t workspace_bytes, moe_a2a_t **out);
 
 /* Dispatch ([IX] dispatch(token_selected_experts, input_payloads,
  * runtime_max_tokens_per_rank, invalid_token_expert_id)).
@@ -235,7 +281,7 @@ const char *moe_a2a_status_string(int status);
  * MOE_REDUCE_FP32_RANK_ORDER (default): fp32 sum over destination ranks in
  *   ascending order, one narrowing ([IX] "Update": the fp32 accumulator of
  *   version 0.6.16 on, "domain-fp32").
- * MOE_REDUCE_BF16_TOPK_TREE: the reduction of FlashInfer's one-sided combine
+ * MOE_REDUCE_BF16_TOPK_TREE (rank layout only): the reduction of FlashInfer's one-sided combine
  *   through version 0.6.15 ([IX] "Update", "topk-slot-tree"): one bf16
  *   accumulator per top-k slot, each rank's message in the first slot whose
  *   expert lives on that rank (later slots of the same rank and invalid ids

@@ -197,3 +197,23 @@ def test_quantize_rows_fp8_checks(abi):
     assert q(A + 4, 4, 64, A, A) == abi.MOE_ERR_INVALID_ARG  # x not 16-byte aligned
     assert q(A, 4, 64, A + 8, A) == abi.MOE_ERR_INVALID_ARG
     assert q(A, 4, 64, A, A + 2) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_expert_layout_host_checks(abi):
+    c = abi.config(8, 64, 7168, 256, 8)
+    rank = abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_RANK)
+    assert rank == abi.moe_a2a_workspace_bytes(c)
+    ex = abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_EXPERT)
+    # two bf16 regions of E * R * M rows dominate
+    assert 2 * 256 * 8 * 64 * 7168 * 2 <= ex < 2 * 256 * 8 * 64 * 7168 * 2 * 1.05
+    assert abi.moe_a2a_workspace_bytes_layout(c, 2) == 0
+    assert abi.moe_a2a_workspace_bytes_layout(abi.config(8, 64, 128, 2048, 8),
+                                              abi.MOE_LAYOUT_EXPERT) == 0   # E > 1024
+    st, h = abi.moe_a2a_create_layout(c, abi.MOE_LAYOUT_EXPERT, 1 << 30, ex)
+    assert st == abi.MOE_OK
+    assert abi.moe_a2a_set_reduction(h, abi.MOE_REDUCE_BF16_TOPK_TREE) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_set_reduction(h, abi.MOE_REDUCE_FP32_RANK_ORDER) == abi.MOE_OK
+    abi.moe_a2a_destroy(h)
+    assert abi.moe_a2a_create_layout(c, 5, 1 << 30, ex)[0] == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_a2a_create_layout(c, abi.MOE_LAYOUT_EXPERT, 1 << 30, ex - 1)[0] == \
+        abi.MOE_ERR_CAPACITY
