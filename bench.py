@@ -53,6 +53,9 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
+                    help="receive layout: planes per (destination, source) rank, or one "
+                         "row per (token, expert) in per-expert planes")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 payloads: e4m3 dispatch rows with a per-token scale and an "
                          "e4m3 combine output with a per-token scale (needs hidden %% 16 == 0)")
@@ -273,7 +276,8 @@ def run_gpu(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
     from combine_topk_ids_rank_gb300 import synth
-    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    from combine_topk_ids_rank_gb300.moe_a2a import (MoeA2A, MOE_FORMAT_FP8_E4M3,
+                                                     MOE_LAYOUT_EXPERT, MOE_LAYOUT_RANK)
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -297,7 +301,8 @@ def run_gpu(args, w, rank, world, local_rank):
     osc = torch.empty((R, T), dtype=torch.float32, device=dev) if fp8 else None
     identity = w.identity_experts and not fp8      # e4m3 rows are not a bf16 payload
 
-    a2a = MoeA2A(R, w.max_tokens, H, E, K, dev)
+    layout = MOE_LAYOUT_EXPERT if args.layout == "expert" else MOE_LAYOUT_RANK
+    a2a = MoeA2A(R, w.max_tokens, H, E, K, dev, layout=layout)
     if fp8:
         a2a.set_recv_format(MOE_FORMAT_FP8_E4M3)
     view = a2a.dispatch(ids, wts, x, w.runtime_max)
@@ -361,6 +366,10 @@ def run_gpu(args, w, rank, world, local_rank):
 
     flush = None
     cfg = config_dict(w, recv_rows)
+    if args.layout == "expert":
+        cfg["layout"] = ("expert-major: one row per (token, expert) in per-expert planes of "
+                         "R*m rows; combine sums the top-k axis in problem order")
+        cfg["mean_rows_per_token"] = cfg.pop("mean_dest_ranks")
     if fp8:
         cfg["payload"] = ("e4m3 dispatch rows + fp32 per-token scale; combine output e4m3 + "
                           "fp32 per-token scale (residual_out bf16)")
@@ -511,7 +520,8 @@ def run_gpu(args, w, rank, world, local_rank):
         try:
             with open(prof) as f:
                 tr = json.load(f)
-            ent = tr.get(w.name + ("-fp8" if fp8 else ""), {}).get("combine")
+            key = w.name + ("-expert" if args.layout == "expert" else "") + ("-fp8" if fp8 else "")
+            ent = tr.get(key, {}).get("combine")
             if ent and ent.get("sources_sha1") == sources_sha1(ent.get("sources", [])):
                 traffic = ent["dram_bytes_per_launch"]
         except (OSError, ValueError, KeyError):
