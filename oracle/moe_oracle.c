@@ -580,6 +580,38 @@ void oracle_combine_experts(int R, int T, int K, int H, int weighted,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Expert-side consumer of the expert planes: a grouped matrix product       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [IX] "Why" / the harness review: between dispatch and combine each
+ * expert applies its own weights to the rows it received (vLLM applies the
+ * gates in the MoE layer, around this product).  Reading: one linear map per
+ * expert, W_e of N x H (row n holds the weights of output n, as a linear
+ * layer stores them), applied to every received row of that expert:
+ *   y[e][j][n] = sum over h of f32(x[e][j][h]) * f32(w[e][n][h])
+ * for j < recv_counts[e], taken here in double (the exact value of the sum of
+ * the bf16 products, up to double rounding); rows j >= recv_counts[e] of y
+ * are not written.  x is [E][cap][H] bf16, w [E][N][H] bf16, y [E][cap][N].
+ */
+void oracle_expert_gemm(int E, long cap, int H, int N, const int32_t *recv_counts,
+                        const uint16_t *x, const uint16_t *w, double *y)
+{
+    for (int e = 0; e < E; ++e) {
+        for (long j = 0; j < recv_counts[e]; ++j) {
+            const uint16_t *xr = x + ((size_t)e * cap + j) * H;
+            for (int n = 0; n < N; ++n) {
+                const uint16_t *wr = w + ((size_t)e * N + n) * H;
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h)
+                    acc += (double)oracle_f32_from_bf16(xr[h]) * (double)oracle_f32_from_bf16(wr[h]);
+                y[((size_t)e * cap + j) * N + n] = acc;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* FP8 (OCP e4m3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no  */
 /* infinity, NaN = S.1111.111, largest finite 448) and per-token scaling     */
 /* ------------------------------------------------------------------------ */

@@ -49,6 +49,8 @@ def _bind(handle):
     handle.oracle_combine_experts.argtypes = ([c_int] * 5 + [p] * 5 + [c_float, p, c_long]
                                               + [p] * 4)
     handle.oracle_combine_experts.restype = None
+    handle.oracle_expert_gemm.argtypes = [c_int, c_long, c_int, c_int, p, p, p, p]
+    handle.oracle_expert_gemm.restype = None
     handle.oracle_f32_from_fp8e4m3.argtypes = [ctypes.c_uint8]
     handle.oracle_f32_from_fp8e4m3.restype = c_float
     handle.oracle_fp8e4m3_from_f32.argtypes = [c_float]
@@ -281,6 +283,23 @@ def combine_experts(routing, expert_out, weighted: bool, residual=None, gamma=No
                              _ptr(gam), float(eps), _ptr(tok), n, _ptr(acc), _ptr(out),
                              _ptr(rout), _ptr(y))
     return dict(acc=acc, out=out, residual_out=rout, y=y)
+
+
+def expert_gemm(x, w, recv_counts, handle=None):
+    """Per-expert product y[e][j] = x[e][j] . w[e]^T in double for the rows
+    j < recv_counts[e].  x: [E, cap, H] uint16 (bf16 bits), w: [E, N, H]
+    uint16.  Returns float64 [E, cap, N] with NaN in the rows past a count."""
+    h = handle or lib()
+    xb = _need(x, np.uint16)
+    wb = _need(w, np.uint16)
+    E, cap, H = xb.shape
+    N = wb.shape[1]
+    if wb.shape != (E, N, H):
+        raise ValueError("w must be [E, N, H]")
+    y = np.full((E, cap, N), np.nan, np.float64)
+    h.oracle_expert_gemm(E, cap, H, N, _ptr(_need(recv_counts, np.int32, (E,))), _ptr(xb),
+                         _ptr(wb), _ptr(y))
+    return y
 
 
 def fp8_bits(values, handle=None):

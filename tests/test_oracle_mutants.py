@@ -88,6 +88,12 @@ MUTANTS = {
     "experts_combine_reverse_k": (
         "for (int k = 0; k < K; ++k) {\n                int32_t row = send_row",
         "for (int k = K - 1; k >= 0; --k) {\n                int32_t row = send_row"),
+    "gemm_weights_transposed": (
+        "const uint16_t *wr = w + ((size_t)e * N + n) * H;\n                double acc = 0.0;\n                for (int h = 0; h < H; ++h)\n                    acc += (double)oracle_f32_from_bf16(xr[h]) * (double)oracle_f32_from_bf16(wr[h]);",
+        "const uint16_t *wr = w + (size_t)e * N * H;\n                double acc = 0.0;\n                for (int h = 0; h < H; ++h)\n                    acc += (double)oracle_f32_from_bf16(xr[h]) * (double)oracle_f32_from_bf16(wr[(size_t)h * N + n]);"),
+    "gemm_wrong_expert_weights": (
+        "const uint16_t *wr = w + ((size_t)e * N + n) * H;",
+        "const uint16_t *wr = w + ((size_t)((e + 1) % E) * N + n) * H;"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -126,6 +132,9 @@ class MutantOracle:
 
     def combine_experts(self, *a, **k):
         return real.combine_experts(*a, handle=self.h, **k)
+
+    def expert_gemm(self, *a, **k):
+        return real.expert_gemm(*a, handle=self.h, **k)
 
     def fp8_bits(self, v):
         return real.fp8_bits(v, handle=self.h)
@@ -166,6 +175,8 @@ PIN_TESTS = [
     (pins.test_expert_identity_unweighted_counts_distinct_experts, {}),
     (pins.test_expert_identity_weighted_sums_duplicate_weights, {}),
     (pins.test_expert_combine_sums_in_problem_order, {}),
+    (pins.test_expert_gemm_identity_and_power_of_two_weights, {}),
+    (pins.test_expert_gemm_matches_library_matmul, {}),
 ]
 
 

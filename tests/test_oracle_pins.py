@@ -766,3 +766,33 @@ def test_expert_combine_fused_matches_rank_layout_when_one_expert_per_rank(oracl
     b = oracle.combine(rr, eo_r, True, res, gam, 1e-6)
     assert np.array_equal(a["out"], b["out"])
     assert np.array_equal(a["residual_out"], b["residual_out"])
+
+
+# --------------------------------------------------------------------------
+# Expert-side grouped product (the consumer between dispatch and combine)
+# --------------------------------------------------------------------------
+
+def test_expert_gemm_identity_and_power_of_two_weights(oracle):
+    E, cap, H = 3, 10, 32
+    rng = np.random.default_rng(11)
+    x = bits(rng.standard_normal((E, cap, H)).astype(np.float32))
+    counts = np.array([10, 0, 7], np.int32)
+    eye = np.stack([np.eye(H, dtype=np.float32) * (2.0 ** e) for e in range(E)])
+    y = oracle.expert_gemm(x, bits(eye), counts)
+    for e in range(E):
+        assert np.array_equal(y[e, :counts[e]], f32(x[e, :counts[e]]) * 2.0 ** e)
+        assert np.isnan(y[e, counts[e]:]).all()          # rows past a count untouched
+
+
+def test_expert_gemm_matches_library_matmul(oracle):
+    # a library routine (numpy's float64 matmul) on a non-square, non-symmetric case
+    E, cap, H, N = 4, 9, 24, 40
+    rng = np.random.default_rng(12)
+    x = bits(rng.standard_normal((E, cap, H)).astype(np.float32))
+    w = bits(rng.standard_normal((E, N, H)).astype(np.float32))
+    counts = np.array([9, 3, 0, 5], np.int32)
+    y = oracle.expert_gemm(x, w, counts)
+    for e in range(E):
+        c = counts[e]
+        ref = f32(x[e, :c]).astype(np.float64) @ f32(w[e]).astype(np.float64).T
+        assert np.allclose(y[e, :c], ref, rtol=0, atol=1e-12)
