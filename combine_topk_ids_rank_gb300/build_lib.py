@@ -17,8 +17,9 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libmoe_a2a.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["route.cu", "dispatch.cu", "combine.cu", "combine_ring.cu", "combine_tree.cu",
-           "dispatch_fp8.cu", "route_expert.cu", "moe_a2a.cpp", "moe_noalloc.cu"]
-HEADERS = ["kernels.h", "ptx.cuh"]
+           "dispatch_fp8.cu", "route_expert.cu", "expert_gemm.cu",
+           "moe_a2a.cpp", "moe_noalloc.cu"]
+HEADERS = ["kernels.h", "ptx.cuh", "fp8.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -236,4 +236,15 @@ cudaError_t launch_quantize_rows_fp8(const float *x, long long rows, int H, uint
 
 cudaError_t launch_combine_tree(const CombineTreeParams &p, int num_sms, cudaStream_t st);
 
+// Expert-side grouped product over the expert planes (expert_gemm.cu).
+struct ExpertGemmParams {
+    const void *x;               // bf16 [E][cap][H]
+    const void *w;               // bf16 [E][N][H]
+    void *out;                   // bf16 [E][cap][N]
+    const int32_t *recv_counts;  // [E]
+    uint32_t *flags;
+    int E, cap, H, N, mtiles;    // mtiles = ceil(cap / 128)
+};
+cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st);
+
 }  // namespace moe

@@ -610,6 +610,33 @@ int moe_quantize_rows_fp8(const float *d_x, int64_t rows, int32_t hidden, void *
                : MOE_ERR_CUDA;
 }
 
+int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 1) return MOE_ERR_PHASE;
+    const int H = h->cfg.hidden;
+    if (h->L.layout != MOE_LAYOUT_EXPERT || h->recv_format != MOE_FORMAT_BF16)
+        return MOE_ERR_INVALID_ARG;
+    if (H % 64 != 0 || N < 128 || N % 128 != 0 || d_w == nullptr || !aligned(d_w, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (d_out == nullptr && N != H) return MOE_ERR_INVALID_ARG;
+    if (d_out != nullptr && !aligned(d_out, 16)) return MOE_ERR_INVALID_ARG;
+    if (h->ntok == 0) return MOE_OK;
+    moe::ExpertGemmParams gp;
+    gp.x = h->ws + h->L.recv_x;
+    gp.w = d_w;
+    gp.out = d_out != nullptr ? d_out : h->ws + h->L.expert_out;
+    gp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+    gp.flags = at<uint32_t>(h, h->L.flags);
+    gp.E = h->cfg.num_experts;
+    gp.cap = h->cfg.ep_size * h->m;
+    gp.H = H;
+    gp.N = N;
+    gp.mtiles = (gp.cap + 127) / 128;
+    return moe::launch_expert_gemm(gp, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
 int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;
     if (reduction == MOE_REDUCE_FP32_RANK_ORDER) {

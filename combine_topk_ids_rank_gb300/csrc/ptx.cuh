@@ -55,6 +55,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for a phase for at most `limit_ns` nanoseconds of wall time (the
+// global timer), whatever a single probe costs.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity,
+                                                uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ---- 1-D bulk copies --------------------------------------------------------
 
 // global -> shared, completion counted in bytes on `bar`.  Addresses and size

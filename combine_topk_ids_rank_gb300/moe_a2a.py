@@ -31,7 +31,8 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_route_static_scratch_bytes", "moe_route_static_scratch",
            "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks",
            "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8",
-           "moe_a2a_workspace_bytes_layout", "moe_a2a_create_layout")
+           "moe_a2a_workspace_bytes_layout", "moe_a2a_create_layout",
+           "moe_expert_gemm")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
@@ -104,6 +105,8 @@ def _load(path: str = LIBRARY):
     lib.moe_combine_fp8.restype = ctypes.c_int
     lib.moe_quantize_rows_fp8.argtypes = [p, ctypes.c_int64, i32, p, p, p]
     lib.moe_quantize_rows_fp8.restype = ctypes.c_int
+    lib.moe_expert_gemm.argtypes = [p, p, i32, p, p]
+    lib.moe_expert_gemm.restype = ctypes.c_int
     lib.moe_a2a_set_recv_format.argtypes = [p, i32]
     lib.moe_a2a_set_recv_format.restype = ctypes.c_int
     lib.moe_a2a_set_reduction.argtypes = [p, i32]
@@ -218,6 +221,11 @@ def quantize_rows_fp8(x, out=None, scale=None, stream=None):
     if st != MOE_OK:
         raise MoeA2AError(st, "moe_quantize_rows_fp8")
     return out, scale
+
+
+def moe_expert_gemm(h, d_w: int, N: int, d_out: int, stream: int = 0) -> int:
+    v = ctypes.c_void_p
+    return _lib.moe_expert_gemm(h, v(d_w), N, v(d_out), v(stream))
 
 
 def moe_a2a_set_recv_format(h, fmt: int) -> int:
@@ -481,6 +489,21 @@ class MoeA2A:
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_combine_fp8")
         return out, out_scale
+
+    def expert_gemm(self, w, out=None, stream=None):
+        """Expert layout: out[e][j] = x[e][j] . w[e]^T for the received rows.
+        w: bf16 [E, N, H]; out: bf16 [E, cap, N], or None to write the
+        combine payload (N == H).  Returns the output tensor."""
+        import torch
+        E, H = self.num_experts, self.hidden
+        N = w.shape[1]
+        self._check(w, torch.bfloat16, (E, N, H), "w")
+        if out is not None:
+            self._check(out, torch.bfloat16, (E, self.last_view.plane_stride, N), "out")
+        st = moe_expert_gemm(self.handle, _ptr(w), N, _ptr(out), self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_expert_gemm")
+        return out if out is not None else self.combine_payload()
 
     def set_recv_format(self, fmt: int):
         """MOE_FORMAT_BF16 (default) or MOE_FORMAT_FP8_E4M3 rows in recv_x."""

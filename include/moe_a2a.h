@@ -173,6 +173,25 @@ size_t moe_a2a_workspace_bytes(const moe_a2a_config_t *cfg);
  *   batches. */
 enum moe_layout { MOE_LAYOUT_RANK = 0, MOE_LAYOUT_EXPERT = 1 };
 
+/* Expert-side consumer of the expert planes ([IX] "Why": between dispatch
+ * and combine each expert applies its own weights to the rows it received;
+ * vLLM applies the gates in the MoE layer around it).  Reading: one linear
+ * map per expert, W_e of N x H stored as a linear layer stores it (row n =
+ * the weights of output n).  For every expert e and received row
+ * j < recv_counts[e] of the current dispatch:
+ *   out[e][j][n] = bf16_rn( sum_h x[e][j][h] * w[e][n][h] ),
+ * bf16 products accumulated in fp32 on the tensor cores (tcgen05; the order
+ * of the additions is the hardware's).  Rows past a count are not written.
+ *   d_w   bf16 [E][N][H], 16-byte aligned;
+ *   N     a multiple of 128; the hidden size H must be a multiple of 64;
+ *   d_out bf16 [E][cap][N] (cap = plane_stride of the dispatch), or NULL to
+ *         write the combine payload region (then N must equal H), so that
+ *         moe_combine(h, NULL, ...) reduces the experts' outputs.
+ * Requires the expert layout and the bf16 receive format, and a pending
+ * dispatch (MOE_ERR_PHASE otherwise); the phase does not change.  Queues one
+ * kernel on `stream`. */
+int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream);
+
 /* moe_a2a_workspace_bytes for a layout (0 if the pair is invalid). */
 size_t moe_a2a_workspace_bytes_layout(const moe_a2a_config_t *cfg, int32_t layout);
 
