@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default="prefill",
-                    choices=["tiny", "decode", "prefill", "wide", "ladder"])
+                    choices=["tiny", "decode", "prefill", "wide", "ladder", "moe_layer"])
     ap.add_argument("--tokens", type=int, default=None, help="tokens per rank (ladder rung)")
     ap.add_argument("--workspace-tokens", type=int, default=None,
                     help="size the workspace for this many tokens per rank (small profiling "
@@ -56,13 +56,22 @@ def parse_args():
     ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
                     help="receive layout: planes per (destination, source) rank, or one "
                          "row per (token, expert) in per-expert planes")
+    ap.add_argument("--expert-gemm", action="store_true",
+                    help="expert layout with the expert-side product between dispatch and "
+                         "combine (random bf16 weights W_e of H x H, output into the combine "
+                         "payload): one step is a whole single-matrix MoE layer")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 payloads: e4m3 dispatch rows with a per-token scale and an "
                          "e4m3 combine output with a per-token scale (needs hidden %% 16 == 0)")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of each phase's C-ABI call instead of "
                          "direct calls (measured no faster on GB300)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.expert_gemm:
+        if args.fp8 or args.graph:
+            ap.error("--expert-gemm takes bf16 rows and direct calls")
+        args.layout = "expert"
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -78,6 +87,16 @@ def workload(args):
         from dataclasses import replace
         w = replace(w, max_tokens=max(args.workspace_tokens, w.runtime_max))
     return w
+
+
+def measured_tensor_peak():
+    """Sustained bf16 tensor throughput (the product runs inside a long step)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback"
 
 
 def measured_peak():
@@ -312,6 +331,14 @@ def run_gpu(args, w, rank, world, local_rank):
         pay.copy_(torch.randn(pay.shape, generator=gd, device=dev, dtype=torch.float32)
                   .to(torch.bfloat16))
     eo = view.recv_x if identity else None
+    gemm = args.expert_gemm
+    if gemm:
+        gw = torch.Generator(device=dev).manual_seed(args.seed + 2)
+        w_exp = torch.randn((E, H, H), generator=gw, device=dev, dtype=torch.bfloat16)
+        w_exp.mul_(1.0 / H ** 0.5)      # in place: E x H x H can be tens of GB
+
+        def run_gemm():
+            a2a.expert_gemm(w_exp)      # into the combine payload
 
     def combine_into(res_, outs):
         if fp8:
@@ -354,15 +381,15 @@ def run_gpu(args, w, rank, world, local_rank):
     else:
         phase_dispatch, phase_combine = run_dispatch, run_combine
 
+    phase_fns = [phase_dispatch] + ([run_gemm] if gemm else []) + [phase_combine]
+
     def step(stream_events=None):
+        for j, fn in enumerate(phase_fns):
+            if stream_events is not None:
+                stream_events[j].record()
+            fn()
         if stream_events is not None:
-            stream_events[0].record()
-        phase_dispatch()
-        if stream_events is not None:
-            stream_events[1].record()
-        phase_combine()
-        if stream_events is not None:
-            stream_events[2].record()
+            stream_events[len(phase_fns)].record()
 
     flush = None
     cfg = config_dict(w, recv_rows)
@@ -388,7 +415,8 @@ def run_gpu(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
 
     # ---- timed region: inputs resident in HBM ----
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    nev = len(phase_fns) + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -409,9 +437,10 @@ def run_gpu(args, w, rank, world, local_rank):
         dist.barrier()
     total_ms = start.elapsed_time(stop)
     disp_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    comb_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    if flush is not None:       # time only the two phases, not the flush
-        total_ms = sum(disp_ms) + sum(comb_ms)
+    comb_ms = [e[-2].elapsed_time(e[-1]) for e in ev]
+    gemm_ms = [e[1].elapsed_time(e[2]) for e in ev] if gemm else []
+    if flush is not None:       # time only the phases, not the flush
+        total_ms = sum(disp_ms) + sum(comb_ms) + sum(gemm_ms)
     total_ms, ms_per_step, tokens_per_s = aggregate_over_ranks(total_ms, N, args.steps, world,
                                                                dev)
     st, flags = a2a.get_error()
@@ -432,6 +461,12 @@ def run_gpu(args, w, rank, world, local_rank):
                      "gbs": d_bytes / d_avg / 1e6, "frac": d_bytes / d_avg / 1e6 / peak,
                      "kernels": ["route_count", "route_scan",
                                  "dispatch_fp8" if fp8 else "dispatch_rows"]},
+        **({"expert_gemm": {
+            "ms_avg": statistics.fmean(gemm_ms), "ms_p50": pct(gemm_ms, 0.5),
+            "ms_p10": pct(gemm_ms, 0.1), "ms_p90": pct(gemm_ms, 0.9),
+            "flops": 2.0 * recv_rows * H * H, "weight_bytes": E * H * H * 2,
+            "tflops": 2.0 * recv_rows * H * H / statistics.fmean(gemm_ms) / 1e9,
+            "kernels": ["expert_gemm"]}} if gemm else {}),
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
                     "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
                     "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
@@ -480,6 +515,8 @@ def run_gpu(args, w, rank, world, local_rank):
             d_ids, d_w, d_x = din[b][0], din[b][1], din[b][2]
             d_res = din[b][3] if w.fused else None
             a2a.dispatch(d_ids, d_w, d_x, w.runtime_max)
+            if gemm:
+                run_gemm()
             o = dout[b]
             combine_into(d_res, [o[0], o[1], o[2] if w.fused else None] if fp8
                          else [o[0], o[1] if w.fused else None])
@@ -539,12 +576,25 @@ def run_gpu(args, w, rank, world, local_rank):
                      "peak": peak, "unit": "GB/s", "frac": c_bytes / c_avg / 1e6 / peak,
                      "traffic": traffic, "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)"
                      % peak_kind if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "gpu_launches": 4 * args.steps if T > 0 else 0,
+        "gpu_launches": (5 if gemm else 4) * args.steps if T > 0 else 0,
         "launch": "CUDA-graph replay of each phase's C-ABI call" if args.graph
                   else "direct C-ABI calls",
         "clocks": clk,
         "e2e": e2e,
     }
+    if gemm:
+        # the product dominates the step: report it against the tensor peak
+        tpk, tkind = measured_tensor_peak()
+        tf = phases["expert_gemm"]["tflops"]
+        line["roofline"] = {"bound": "tensor", "kernel": "expert_gemm", "achieved": tf,
+                            "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk, "traffic": None,
+                            "peak_source": "%s (MEASURED_PEAKS.json bf16_tflops_sustained)"
+                            % tkind}
+        line["roofline_combine"] = {"bound": "hbm", "achieved": c_bytes / c_avg / 1e6,
+                                    "peak": peak, "unit": "GB/s",
+                                    "frac": c_bytes / c_avg / 1e6 / peak}
+        cfg["expert_gemm"] = "W_e bf16 [%d][%d][%d], N(0,1/H), output into the combine payload" % (
+            E, H, H)
     return line
 
 

@@ -10,24 +10,22 @@
 //   y[e][j][n] = bf16_rn( sum_h x[e][j][h] * w[e][n][h] ),  j < recv_counts[e],
 // products of bf16 values accumulated in fp32 (order of the tensor cores).
 //
-// GB300 design: one CTA per 128 x BN output tile of one expert; tiles that
-// start past the expert's row count leave at once (the counts are read on
-// the device, no host round trip).  Four warps:
-//   warp 0, one thread: TMA producer -- 2-D tiled loads (128-byte swizzle)
+// GB300 design: a persistent kernel, one CTA per SM, over the useful
+// 128 x BN output tiles only (tile list built in shared memory from the
+// device-side row counts; raster: expert by expert, groups of 8 row tiles,
+// column tile outer inside a group, so that concurrent CTAs share weight and
+// row tiles in L2).  Six warps:
+//   warp 4, one thread: TMA producer -- 2-D tiled loads (128-byte swizzle)
 //     of the A tile (128 rows x 64 of x) and the B tile (BN rows x 64 of W)
-//     into a ring of shared-memory stages, completing on the stage's full
-//     mbarrier;
-//   warp 1, one thread: MMA issuer -- per stage four tcgen05.mma of
-//     128 x BN x 16 (bf16 in, f32 accumulated in tensor memory), then a
-//     tcgen05.commit that frees the stage; a final commit signals the
-//     epilogue;
-//   warp 2 owns the tensor-memory allocation (BN columns);
-//   epilogue, all four warps: warp w reads tensor-memory lanes 32w..32w+31
-//     (rows of the tile) 32 columns at a time, narrows to bf16 and stores the
-//     rows below the expert's count.
-// Every mbarrier wait is bounded in wall time; on a timeout the kernel
-// raises the flag, lets its issued copies and products finish, frees
-// tensor memory and returns.
+//     into a ring of shared-memory stages that runs on across tiles;
+//   warp 5: tensor-memory owner (2 x BN columns: two accumulators) and, one
+//     thread, the MMA issuer -- per stage four tcgen05.mma of 128 x BN x 16
+//     (bf16 in, f32 accumulated in tensor memory), a tcgen05.commit that
+//     frees the stage, and one per tile that hands the accumulator over;
+//   warps 0-3: epilogue -- warp w reads tensor-memory lanes 32w..32w+31 (rows
+//     of the tile) 32 columns at a time, narrows to bf16, stores the rows
+//     below the expert's count and frees the accumulator, while the MMA
+//     thread already fills the other one.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -43,8 +41,12 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;  // bf16 elements per 128-byte swizzled row
-constexpr int kThreads = 128;
+constexpr int kBK = 64;           // bf16 elements per 128-byte swizzled row
+constexpr int kEpiWarps = 4;      // warps 0-3: epilogue (tensor-memory lane quadrants)
+constexpr int kProducerWarp = 4;  // TMA
+constexpr int kMmaWarp = 5;       // MMA issue + tensor-memory allocation
+constexpr int kThreads = 6 * 32;
+constexpr int kGroupM = 8;        // row tiles per raster group
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000;  // 0.5 s of wall time per wait
 
 template <int BN, int STAGES>
@@ -52,9 +54,9 @@ struct GemmSmem {
     static constexpr int kA = kBM * kBK * 2;  // bytes of an A stage
     static constexpr int kB = BN * kBK * 2;   // bytes of a B stage
     static constexpr int kTiles = STAGES * (kA + kB);
-    // tiles (1024-aligned) + barriers + the tensor-memory slot, + 1024 for
-    // aligning the dynamic shared memory base
-    static constexpr int kBytes = kTiles + (2 * STAGES + 1) * 8 + 16 + 1024;
+    // tiles (1024-aligned) + ring and accumulator barriers + the tensor-memory
+    // slot, + 1024 for aligning the dynamic shared memory base
+    static constexpr int kBytes = kTiles + (2 * STAGES + 5) * 8 + 16 + 1024;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -62,23 +64,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&b);
 }
 
+__device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                     ptx::smem_u32(bar))
+                 : "memory");
+}
+
+// Useful tiles of the call, in raster order: experts in turn; inside an
+// expert, groups of kGroupM row tiles, column tile outer and row tile inner
+// within a group, so that the CTAs at work at one time share a few weight
+// tiles and a group of row tiles in L2.
+struct TileMap {
+    const int *first;  // [E + 1] exclusive prefix of tiles per expert (shared memory)
+    int E, NT;
+    const int *mtiles;  // [E] row tiles per expert (shared memory)
+    __device__ void of(int t, int &e, int &mt, int &nt) const {
+        int lo = 0, hi = E - 1;  // last expert whose first tile is <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (first[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        e = lo;
+        const int u = t - first[e], MT = mtiles[e];
+        const int g = u / (kGroupM * NT);
+        const int gm = min(kGroupM, MT - g * kGroupM);
+        const int v = u - g * kGroupM * NT;
+        nt = v / gm;
+        mt = g * kGroupM + v % gm;
+    }
+};
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                        const __grid_constant__ CUtensorMap tmap_w, const ExpertGemmParams p) {
     using L = GemmSmem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int issued_s, failed_s;
+    __shared__ int s_first[kMaxExpertsExpertLayout + 1];
+    __shared__ int s_mtiles[kMaxExpertsExpertLayout];
+    __shared__ int s_count[kMaxExpertsExpertLayout];
+    __shared__ volatile int s_failed;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // tile -> (expert, row tile, column tile)
-    const int nt_per = p.N / BN;
-    const long long tile = blockIdx.x;
-    const int e = (int)(tile / ((long long)p.mtiles * nt_per));
-    const int rest = (int)(tile % ((long long)p.mtiles * nt_per));
-    const int mt = rest / nt_per, nt = rest % nt_per;
-    const int count = p.recv_counts[e];
-    if (mt * kBM >= count) return;  // uniform: nothing allocated yet
 
     const uint32_t base = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
@@ -86,98 +112,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *b_tiles = smem + STAGES * L::kA;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kTiles);
     uint64_t *empty = full + STAGES;
-    uint64_t *done = empty + STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *acc_full = empty + STAGES;   // [2] products of a tile done
+    uint64_t *acc_empty = acc_full + 2;    // [2] epilogue done with a buffer
+    uint64_t *drain = acc_empty + 2;       // all products issued have finished
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
+    // tile list from the device-side counts
+    for (int e = tid; e < p.E; e += kThreads) {
+        const int c = p.recv_counts[e];
+        s_count[e] = c;
+        s_mtiles[e] = (c + kBM - 1) / kBM;
+    }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        ptx::mbar_init(done, 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], kEpiWarps);
+        }
+        ptx::mbar_init(drain, 1);
         ptx::fence_mbar_init();
-        issued_s = 0;
-        failed_s = 0;
+        s_failed = 0;
     }
-    if (warp == 2) tc::tmem_alloc(tmem_slot, BN);
+    if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, 2 * BN);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (tid == 0) {
+        const int NT = p.N / BN;
+        s_first[0] = 0;
+        for (int e = 0; e < p.E; ++e) s_first[e + 1] = s_first[e] + s_mtiles[e] * NT;
+    }
+    __syncthreads();
     const uint32_t taddr = *tmem_slot;
-
+    const TileMap tm{s_first, p.E, p.N / BN, s_mtiles};
+    const int ntiles = s_first[p.E];
     const int KB = p.H / kBK;
-    const int row0 = e * p.cap + mt * kBM;  // first row of the A tile
-    const int wrow0 = e * p.N + nt * BN;    // first row of the B tile
 
-    if (warp == 0 && lane == 0) {
-        // producer
-        int kb = 0;
-        for (; kb < KB; ++kb) {
-            const int s = kb % STAGES;
-            if (kb >= STAGES &&
-                !ptx::mbar_wait_timed(&empty[s], (uint32_t)((kb / STAGES - 1) & 1), kWaitNs)) {
-                failed_s = 1;
-                break;
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            uint32_t kc = 0;  // k-blocks issued by this CTA, across tiles
+            for (int t = blockIdx.x; t < ntiles && !s_failed; t += gridDim.x) {
+                int e, mt, nt;
+                tm.of(t, e, mt, nt);
+                const int row0 = e * p.cap + mt * kBM, wrow0 = e * p.N + nt * BN;
+                for (int kb = 0; kb < KB; ++kb, ++kc) {
+                    const int s = (int)(kc % STAGES);
+                    if (!ptx::mbar_wait_timed(&empty[s], ((kc / STAGES) & 1u) ^ 1u, kWaitNs)) {
+                        s_failed = 1;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)(L::kA + L::kB));
+                    tc::tma_load_2d(a_tiles + s * L::kA, &tmap_x, kb * kBK, row0, &full[s]);
+                    tc::tma_load_2d(b_tiles + s * L::kB, &tmap_w, kb * kBK, wrow0, &full[s]);
+                }
             }
-            ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)(L::kA + L::kB));
-            tc::tma_load_2d(a_tiles + s * L::kA, &tmap_x, kb * kBK, row0, &full[s]);
-            tc::tma_load_2d(b_tiles + s * L::kB, &tmap_w, kb * kBK, wrow0, &full[s]);
+            // copies still in flight land before shared memory goes away
+            const uint32_t first = kc > (uint32_t)STAGES ? kc - STAGES : 0u;
+            for (uint32_t k = first; k < kc; ++k)
+                ptx::mbar_wait_timed(&full[k % STAGES], (k / STAGES) & 1u, kWaitNs);
         }
-        issued_s = kb;
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer
-        constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % STAGES;
-            if (!ptx::mbar_wait_timed(&full[s], (uint32_t)((kb / STAGES) & 1), kWaitNs)) {
-                failed_s = 1;
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
+            uint32_t kc = 0, it = 0;
+            for (int t = blockIdx.x; t < ntiles && !s_failed; t += gridDim.x, ++it) {
+                const uint32_t b = it & 1u;
+                if (!ptx::mbar_wait_timed(&acc_empty[b], ((it >> 1) & 1u) ^ 1u, kWaitNs)) {
+                    s_failed = 1;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t d = taddr + b * BN;
+                for (int kb = 0; kb < KB; ++kb, ++kc) {
+                    const int s = (int)(kc % STAGES);
+                    if (!ptx::mbar_wait_timed(&full[s], (kc / STAGES) & 1u, kWaitNs)) {
+                        s_failed = 1;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint64_t ad = tc::smem_desc_sw128(ptx::smem_u32(a_tiles + s * L::kA));
+                    const uint64_t bd = tc::smem_desc_sw128(ptx::smem_u32(b_tiles + s * L::kB));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 units
+                        tc::mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    tc::commit(&empty[s]);  // frees the stage once these products finish
+                }
+                tc::commit(&acc_full[b]);  // the tile's accumulator is complete
+                if (s_failed) break;
+            }
+            // every product issued above has finished before tensor memory is freed
+            tc::commit(drain);
+            ptx::mbar_wait_timed(drain, 0, kWaitNs);
+        }
+    } else {
+        // epilogue: warp w owns tensor-memory lanes 32w..32w+31 = tile rows
+        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out);
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            const uint32_t b = it & 1u;
+            const bool ok = ptx::mbar_wait_timed(&acc_full[b], (it >> 1) & 1u, kWaitNs);
+            __syncwarp();
+            if (!ok || s_failed) {
+                if (lane == 0) s_failed = 1;
                 break;
             }
             tc::fence_after_sync();
-            const uint64_t ad = tc::smem_desc_sw128(ptx::smem_u32(a_tiles + s * L::kA));
-            const uint64_t bd = tc::smem_desc_sw128(ptx::smem_u32(b_tiles + s * L::kB));
+            int e, mt, nt;
+            tm.of(t, e, mt, nt);
+            const int r = mt * kBM + 32 * warp + lane;  // row within the expert
+            const bool live = r < s_count[e];
+            __nv_bfloat16 *dst_row = out + ((long long)e * p.cap + r) * p.N + (long long)nt * BN;
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tc::ld_32x32(taddr + b * BN + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+                tc::wait_ld();
+                if (live) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c0);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 descriptor units
-                tc::mma_bf16(taddr, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-            tc::commit(&empty[s]);
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]),
+                                          __uint_as_float(v[8 * q + 1]));
+                        o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]),
+                                          __uint_as_float(v[8 * q + 3]));
+                        o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]),
+                                          __uint_as_float(v[8 * q + 5]));
+                        o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]),
+                                          __uint_as_float(v[8 * q + 7]));
+                        dst[q] = o;
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(&acc_empty[b]);
         }
-        tc::commit(done);  // arrives once every product issued above has completed
     }
 
-    // epilogue
-    const bool ok = ptx::mbar_wait_timed(done, 0, kWaitNs);
-    __syncwarp();  // lane 0 of warps 0 and 1 rejoin before the warp-wide loads
-    tc::fence_after_sync();
-    const int r = mt * kBM + 32 * warp + lane;  // row of this thread within the expert
-    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out);
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tc::ld_32x32(taddr + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
-        tc::wait_ld();
-        if (ok && r < count) {
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                out + ((long long)e * p.cap + r) * p.N + (long long)nt * BN + c0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                dst[q] = o;
-            }
-        }
-    }
     tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0 && (failed_s || !ok)) {
-        atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
-        // copies issued but never consumed must land before shared memory goes
-        for (int kb = issued_s - STAGES < 0 ? 0 : issued_s - STAGES; kb < issued_s; ++kb)
-            ptx::mbar_wait_timed(&full[kb % STAGES], (uint32_t)((kb / STAGES) & 1), kWaitNs);
-    }
-    __syncthreads();
-    if (warp == 2) tc::tmem_dealloc(taddr, BN);
+    if (tid == 0 && s_failed) atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+    if (warp == kMmaWarp) tc::tmem_dealloc(taddr, 2 * BN);
 }
 
 // ---- host: tensor maps -------------------------------------------------------
@@ -227,16 +305,24 @@ cudaError_t launch_t(const ExpertGemmParams &p, cudaStream_t st) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            L::kBytes);
     if (err != cudaSuccess) return err;
-    const long long tiles = (long long)p.E * p.mtiles * (p.N / BN);
-    if (tiles < 1) return cudaSuccess;
-    expert_gemm_kernel<BN, STAGES><<<(unsigned)tiles, kThreads, L::kBytes, st>>>(mx, mw, p);
+    // persistent: one CTA per SM (the ring fills most of shared memory), or
+    // fewer when the call cannot have that many tiles
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
+    const long long most = (long long)p.E * p.mtiles * (p.N / BN);
+    const int grid = (int)(most < sms ? most : sms);
+    if (grid < 1) return cudaSuccess;
+    expert_gemm_kernel<BN, STAGES><<<grid, kThreads, L::kBytes, st>>>(mx, mw, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st) {
-    if (p.H % kBK != 0 || p.H < kBK || p.N % 128 != 0 || p.N < 128 || p.cap < 1)
+    if (p.H % kBK != 0 || p.H < kBK || p.N % 128 != 0 || p.N < 128 || p.cap < 1 ||
+        p.E > kMaxExpertsExpertLayout)
         return cudaErrorInvalidValue;
     if (p.N % 256 == 0) return launch_t<256, 4>(p, st);
     return launch_t<128, 6>(p, st);

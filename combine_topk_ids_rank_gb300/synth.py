@@ -72,6 +72,9 @@ WORKLOADS = {
     "wide": Workload("wide", 16, 1024, 2048, 1024, 4096, 512, 8, "uniform",
                      weighted=False, fused=False),
     "ladder": Workload("ladder", 8, 8192, 8192, 8192, 7168, 256, 8, "uniform"),
+    # one expert per rank with many rows each: the shape at which the expert-side
+    # product (expert layout) is bound by the tensor cores rather than by weights
+    "moe_layer": Workload("moe_layer", 8, 4096, 4096, 4096, 7168, 8, 2, "uniform"),
 }
 LADDER_RUNGS = tuple(2 ** i for i in range(14))   # 1 .. 8192
 
