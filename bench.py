@@ -553,11 +553,11 @@ def run_gpu(args, w, rank, world, local_rank):
 
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
+    key = w.name + ("-expert" if args.layout == "expert" else "") + ("-fp8" if fp8 else "")
     if os.path.exists(prof):
         try:
             with open(prof) as f:
                 tr = json.load(f)
-            key = w.name + ("-expert" if args.layout == "expert" else "") + ("-fp8" if fp8 else "")
             ent = tr.get(key, {}).get("combine")
             if ent and ent.get("sources_sha1") == sources_sha1(ent.get("sources", [])):
                 traffic = ent["dram_bytes_per_launch"]
@@ -586,8 +586,17 @@ def run_gpu(args, w, rank, world, local_rank):
         # the product dominates the step: report it against the tensor peak
         tpk, tkind = measured_tensor_peak()
         tf = phases["expert_gemm"]["tflops"]
+        gtraffic = None
+        try:
+            with open(prof) as f:
+                ent = json.load(f).get(key, {}).get("expert_gemm")
+            if ent and ent.get("sources_sha1") == sources_sha1(ent.get("sources", [])):
+                gtraffic = ent["dram_bytes_per_launch"]
+        except (OSError, ValueError, KeyError):
+            gtraffic = None
         line["roofline"] = {"bound": "tensor", "kernel": "expert_gemm", "achieved": tf,
-                            "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk, "traffic": None,
+                            "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
+                            "traffic": gtraffic,
                             "peak_source": "%s (MEASURED_PEAKS.json bf16_tflops_sustained)"
                             % tkind}
         line["roofline_combine"] = {"bound": "hbm", "achieved": c_bytes / c_avg / 1e6,
