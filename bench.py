@@ -543,9 +543,33 @@ def run_gpu(args, w, rank, world, local_rank):
         torch.cuda.synchronize()
         e2e_ms, _, e2e_tps = aggregate_over_ranks(e0.elapsed_time(e1), N, args.e2e_steps,
                                                   world, dev)
+        # The same copies with no kernels, up and down at once: the host
+        # link's bound on this machine for the end-to-end step.
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(4, args.e2e_steps // 4)
+        torch.cuda.synchronize()
+        c0.record(compute)
+        up.wait_event(c0)
+        down.wait_event(c0)
+        for i in range(reps):
+            b = i & 1
+            with torch.cuda.stream(up):
+                for dst, src in zip(din[b], hin):
+                    dst.copy_(src, non_blocking=True)
+            with torch.cuda.stream(down):
+                for dst, src in zip(hout[b], dout[b]):
+                    dst.copy_(src, non_blocking=True)
+        compute.wait_stream(up)
+        compute.wait_stream(down)
+        c1.record(compute)
+        torch.cuda.synchronize()
+        copy_ms = c0.elapsed_time(c1) / reps
         e2e = {"value": e2e_tps, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
+               "copy_only_ms_per_step": copy_ms,
+               "link_gbs": (h2d + d2h) / copy_ms / 1e6,
+               "frac_of_copy_bound": copy_ms / (e2e_ms / args.e2e_steps),
                "path": "pinned host -> device copies on a copy stream, moe_dispatch + "
                        "moe_combine on the compute stream, device -> pinned host copies on a "
                        "third stream; double-buffered so one step's inputs and another's "
