@@ -611,6 +611,37 @@ void oracle_expert_gemm(int E, long cap, int H, int N, const int32_t *recv_count
     }
 }
 
+/* forward declaration: the e4m3 decoding defined with the FP8 helpers below */
+float oracle_f32_from_fp8e4m3(uint8_t q);
+
+/*
+ * The same product on FP8 operands: the rows as the FP8 receive format holds
+ * them (e4m3 codes qx with one scale sx per row) and weights as e4m3 codes qw
+ * with one scale sw per output channel.  Reading (the pages name FP8
+ * payloads with a scale payload, not this arithmetic): dequantised operands,
+ *   y[e][j][n] = sx[e][j] * sw[e][n] * sum_h f(qx[e][j][h]) * f(qw[e][n][h]),
+ * f the e4m3 value; the sum and the scaling in double here.  Rows past a
+ * count are not written.  qx [E][cap][H], sx [E][cap], qw [E][N][H], sw [E][N].
+ */
+void oracle_expert_gemm_fp8(int E, long cap, int H, int N, const int32_t *recv_counts,
+                            const uint8_t *qx, const float *sx, const uint8_t *qw,
+                            const float *sw, double *y)
+{
+    for (int e = 0; e < E; ++e) {
+        for (long j = 0; j < recv_counts[e]; ++j) {
+            const uint8_t *xr = qx + ((size_t)e * cap + j) * H;
+            for (int n = 0; n < N; ++n) {
+                const uint8_t *wr = qw + ((size_t)e * N + n) * H;
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h)
+                    acc += (double)oracle_f32_from_fp8e4m3(xr[h]) * (double)oracle_f32_from_fp8e4m3(wr[h]);
+                y[((size_t)e * cap + j) * N + n] =
+                    (double)sx[(size_t)e * cap + j] * (double)sw[(size_t)e * N + n] * acc;
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* FP8 (OCP e4m3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no  */
 /* infinity, NaN = S.1111.111, largest finite 448) and per-token scaling     */

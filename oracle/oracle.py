@@ -51,6 +51,8 @@ def _bind(handle):
     handle.oracle_combine_experts.restype = None
     handle.oracle_expert_gemm.argtypes = [c_int, c_long, c_int, c_int, p, p, p, p]
     handle.oracle_expert_gemm.restype = None
+    handle.oracle_expert_gemm_fp8.argtypes = [c_int, c_long, c_int, c_int] + [p] * 6
+    handle.oracle_expert_gemm_fp8.restype = None
     handle.oracle_f32_from_fp8e4m3.argtypes = [ctypes.c_uint8]
     handle.oracle_f32_from_fp8e4m3.restype = c_float
     handle.oracle_fp8e4m3_from_f32.argtypes = [c_float]
@@ -299,6 +301,24 @@ def expert_gemm(x, w, recv_counts, handle=None):
     y = np.full((E, cap, N), np.nan, np.float64)
     h.oracle_expert_gemm(E, cap, H, N, _ptr(_need(recv_counts, np.int32, (E,))), _ptr(xb),
                          _ptr(wb), _ptr(y))
+    return y
+
+
+def expert_gemm_fp8(qx, sx, qw, sw, recv_counts, handle=None):
+    """FP8 operands: y[e][j][n] = sx[e][j] sw[e][n] sum_h f(qx) f(qw) in
+    double.  qx [E, cap, H] / qw [E, N, H] uint8 e4m3 codes, sx [E, cap] /
+    sw [E, N] float32.  Returns float64 [E, cap, N], NaN past a count."""
+    h = handle or lib()
+    qxb = _need(qx, np.uint8)
+    qwb = _need(qw, np.uint8)
+    E, cap, H = qxb.shape
+    N = qwb.shape[1]
+    if qwb.shape != (E, N, H):
+        raise ValueError("qw must be [E, N, H]")
+    y = np.full((E, cap, N), np.nan, np.float64)
+    h.oracle_expert_gemm_fp8(E, cap, H, N, _ptr(_need(recv_counts, np.int32, (E,))), _ptr(qxb),
+                             _ptr(_need(sx, np.float32, (E, cap))), _ptr(qwb),
+                             _ptr(_need(sw, np.float32, (E, N))), _ptr(y))
     return y
 
 

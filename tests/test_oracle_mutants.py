@@ -94,6 +94,9 @@ MUTANTS = {
     "gemm_wrong_expert_weights": (
         "const uint16_t *wr = w + ((size_t)e * N + n) * H;",
         "const uint16_t *wr = w + ((size_t)((e + 1) % E) * N + n) * H;"),
+    "gemm_fp8_ignores_channel_scale": (
+        "(double)sx[(size_t)e * cap + j] * (double)sw[(size_t)e * N + n] * acc;",
+        "(double)sx[(size_t)e * cap + j] * acc;"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -136,6 +139,9 @@ class MutantOracle:
     def expert_gemm(self, *a, **k):
         return real.expert_gemm(*a, handle=self.h, **k)
 
+    def expert_gemm_fp8(self, *a, **k):
+        return real.expert_gemm_fp8(*a, handle=self.h, **k)
+
     def fp8_bits(self, v):
         return real.fp8_bits(v, handle=self.h)
 
@@ -177,6 +183,7 @@ PIN_TESTS = [
     (pins.test_expert_combine_sums_in_problem_order, {}),
     (pins.test_expert_gemm_identity_and_power_of_two_weights, {}),
     (pins.test_expert_gemm_matches_library_matmul, {}),
+    (pins.test_expert_gemm_fp8_identity_and_library_matmul, {}),
 ]
 
 

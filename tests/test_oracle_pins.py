@@ -796,3 +796,33 @@ def test_expert_gemm_matches_library_matmul(oracle):
         c = counts[e]
         ref = f32(x[e, :c]).astype(np.float64) @ f32(w[e]).astype(np.float64).T
         assert np.allclose(y[e, :c], ref, rtol=0, atol=1e-12)
+
+
+def test_expert_gemm_fp8_identity_and_library_matmul(oracle):
+    # identity weights (code 0x38 = 1.0) with unit channel scales give back
+    # sx * f(qx); random codes agree with numpy's float64 matmul of the
+    # decoded values times the two scales (a library routine)
+    E, cap, H = 2, 6, 32
+    rng = np.random.default_rng(21)
+    qx = rng.integers(0, 256, (E, cap, H)).astype(np.uint8)
+    qx[(qx & 0x7F) == 0x7F] = 0x10                      # no NaN codes
+    sx = rng.uniform(0.5, 4.0, (E, cap)).astype(np.float32)
+    counts = np.array([6, 4], np.int32)
+    eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+    qw = np.stack([eye, eye])
+    y = oracle.expert_gemm_fp8(qx, sx, qw, np.ones((E, H), np.float32), counts)
+    fx = oracle.fp8_to_f32(qx).astype(np.float64)
+    for e in range(E):
+        c = counts[e]
+        assert np.array_equal(y[e, :c], fx[e, :c] * sx[e, :c, None].astype(np.float64))
+        assert np.isnan(y[e, c:]).all()
+    N = 24
+    qw = rng.integers(0, 256, (E, N, H)).astype(np.uint8)
+    qw[(qw & 0x7F) == 0x7F] = 0x21
+    sw = rng.uniform(0.01, 2.0, (E, N)).astype(np.float32)
+    y = oracle.expert_gemm_fp8(qx, sx, qw, sw, counts)
+    fw = oracle.fp8_to_f32(qw).astype(np.float64)
+    for e in range(E):
+        c = counts[e]
+        ref = (fx[e, :c] @ fw[e].T) * sx[e, :c, None] * sw[e][None, :]
+        assert np.allclose(y[e, :c], ref, rtol=1e-14, atol=0)
