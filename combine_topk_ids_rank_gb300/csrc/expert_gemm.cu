@@ -41,7 +41,8 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;           // bf16 elements per 128-byte swizzled row
+constexpr int kRowBytes = 128;    // bytes of a stage row (one 128-byte swizzle span):
+                                  // 64 bf16 or 128 e4m3 values
 constexpr int kEpiWarps = 4;      // warps 0-3: epilogue (tensor-memory lane quadrants)
 constexpr int kProducerWarp = 4;  // TMA
 constexpr int kMmaWarp = 5;       // MMA issue + tensor-memory allocation
@@ -51,8 +52,8 @@ constexpr uint64_t kWaitNs = 500ull * 1000 * 1000;  // 0.5 s of wall time per wa
 
 template <int BN, int STAGES>
 struct GemmSmem {
-    static constexpr int kA = kBM * kBK * 2;  // bytes of an A stage
-    static constexpr int kB = BN * kBK * 2;   // bytes of a B stage
+    static constexpr int kA = kBM * kRowBytes;  // bytes of an A stage
+    static constexpr int kB = BN * kRowBytes;   // bytes of a B stage
     static constexpr int kTiles = STAGES * (kA + kB);
     // tiles (1024-aligned) + ring and accumulator barriers + the tensor-memory
     // slot, + 1024 for aligning the dynamic shared memory base
@@ -94,7 +95,7 @@ struct TileMap {
     }
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                        const __grid_constant__ CUtensorMap tmap_w, const ExpertGemmParams p) {
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t taddr = *tmem_slot;
     const TileMap tm{s_first, p.E, p.N / BN, s_mtiles};
     const int ntiles = s_first[p.E];
+    constexpr int kBK = FP8 ? kRowBytes : kRowBytes / 2;  // values of a stage row
     const int KB = p.H / kBK;
 
     if (warp == kProducerWarp) {
@@ -176,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
+            constexpr uint32_t idesc =
+                FP8 ? tc::idesc_e4m3_f32(kBM, BN) : tc::idesc_bf16_f32(kBM, BN);
             uint32_t kc = 0, it = 0;
             for (int t = blockIdx.x; t < ntiles && !s_failed; t += gridDim.x, ++it) {
                 const uint32_t b = it & 1u;
@@ -195,9 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after_sync();
                     const uint64_t ad = tc::smem_desc_sw128(ptx::smem_u32(a_tiles + s * L::kA));
                     const uint64_t bd = tc::smem_desc_sw128(ptx::smem_u32(b_tiles + s * L::kB));
+                    // four K steps of 32 bytes (16 bf16 or 32 e4m3) = 2 descriptor units
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 units
-                        tc::mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (FP8)
+                            tc::mma_f8(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                        else
+                            tc::mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    }
                     tc::commit(&empty[s]);  // frees the stage once these products finish
                 }
                 tc::commit(&acc_full[b]);  // the tile's accumulator is complete
@@ -224,11 +232,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tm.of(t, e, mt, nt);
             const int r = mt * kBM + 32 * warp + lane;  // row within the expert
             const bool live = r < s_count[e];
+            // FP8 operands: y = acc * sx[row] * sw[column], two fp32 products
+            const float sx = (FP8 && live) ? p.x_scale[(long long)e * p.cap + r] : 1.0f;
+            const float *swr = FP8 ? p.w_scale + (long long)e * p.N + (long long)nt * BN : nullptr;
             __nv_bfloat16 *dst_row = out + ((long long)e * p.cap + r) * p.N + (long long)nt * BN;
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tc::ld_32x32(taddr + b * BN + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
                 tc::wait_ld();
+                if (FP8) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __float_as_uint(
+                            __fmul_rn(__fmul_rn(__uint_as_float(v[i]), sx), __ldg(swr + c0 + i)));
+                }
                 if (live) {
                     uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c0);
 #pragma unroll
@@ -281,27 +298,30 @@ EncodeTiled encoder() {
 
 // bf16 matrix of `rows` x `cols` (row-major, cols contiguous), boxes of
 // box_rows x 64 with the 128-byte swizzle; rows past the end read as zero.
-bool make_map(CUtensorMap *m, const void *base, long long rows, int cols, int box_rows) {
+bool make_map(CUtensorMap *m, const void *base, long long rows, int cols, int box_rows,
+              bool fp8) {
     EncodeTiled enc = encoder();
     if (enc == nullptr) return false;
+    const int esize = fp8 ? 1 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esize), (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool FP8>
 cudaError_t launch_t(const ExpertGemmParams &p, cudaStream_t st) {
     using L = GemmSmem<BN, STAGES>;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, p.x, (long long)p.E * p.cap, p.H, kBM) ||
-        !make_map(&mw, p.w, (long long)p.E * p.N, p.H, BN))
+    if (!make_map(&mx, p.x, (long long)p.E * p.cap, p.H, kBM, FP8) ||
+        !make_map(&mw, p.w, (long long)p.E * p.N, p.H, BN, FP8))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<BN, STAGES>,
+    cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<BN, STAGES, FP8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            L::kBytes);
     if (err != cudaSuccess) return err;
@@ -314,18 +334,22 @@ cudaError_t launch_t(const ExpertGemmParams &p, cudaStream_t st) {
     const long long most = (long long)p.E * p.mtiles * (p.N / BN);
     const int grid = (int)(most < sms ? most : sms);
     if (grid < 1) return cudaSuccess;
-    expert_gemm_kernel<BN, STAGES><<<grid, kThreads, L::kBytes, st>>>(mx, mw, p);
+    expert_gemm_kernel<BN, STAGES, FP8><<<grid, kThreads, L::kBytes, st>>>(mx, mw, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st) {
-    if (p.H % kBK != 0 || p.H < kBK || p.N % 128 != 0 || p.N < 128 || p.cap < 1 ||
+    const int bk = p.fp8 ? kRowBytes : kRowBytes / 2;
+    if (p.H % bk != 0 || p.H < bk || p.N % 128 != 0 || p.N < 128 || p.cap < 1 ||
         p.E > kMaxExpertsExpertLayout)
         return cudaErrorInvalidValue;
-    if (p.N % 256 == 0) return launch_t<256, 4>(p, st);
-    return launch_t<128, 6>(p, st);
+    if (p.fp8) {
+        if (p.x_scale == nullptr || p.w_scale == nullptr) return cudaErrorInvalidValue;
+        return p.N % 256 == 0 ? launch_t<256, 4, true>(p, st) : launch_t<128, 6, true>(p, st);
+    }
+    return p.N % 256 == 0 ? launch_t<256, 4, false>(p, st) : launch_t<128, 6, false>(p, st);
 }
 
 }  // namespace moe

@@ -242,8 +242,11 @@ struct ExpertGemmParams {
     const void *w;               // bf16 [E][N][H]
     void *out;                   // bf16 [E][cap][N]
     const int32_t *recv_counts;  // [E]
+    const float *x_scale;        // FP8 operands: [E][cap] row scales, else null
+    const float *w_scale;        // FP8 operands: [E][N] channel scales, else null
     uint32_t *flags;
     int E, cap, H, N, mtiles;    // mtiles = ceil(cap / 128)
+    int fp8;                     // 1: x and w are e4m3 codes (x_scale, w_scale used)
 };
 cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st);
 

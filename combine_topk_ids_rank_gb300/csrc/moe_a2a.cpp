@@ -610,14 +610,19 @@ int moe_quantize_rows_fp8(const float *d_x, int64_t rows, int32_t hidden, void *
                : MOE_ERR_CUDA;
 }
 
-int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream) {
+namespace {
+
+int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int32_t N,
+                     void *d_out, bool fp8, void *stream) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;
     if (h->phase != 1) return MOE_ERR_PHASE;
     const int H = h->cfg.hidden;
-    if (h->L.layout != MOE_LAYOUT_EXPERT || h->recv_format != MOE_FORMAT_BF16)
+    const int want = fp8 ? MOE_FORMAT_FP8_E4M3 : MOE_FORMAT_BF16;
+    if (h->L.layout != MOE_LAYOUT_EXPERT || h->recv_format != want) return MOE_ERR_INVALID_ARG;
+    if (H % (fp8 ? 128 : 64) != 0 || N < 128 || N % 128 != 0 || d_w == nullptr ||
+        !aligned(d_w, 16))
         return MOE_ERR_INVALID_ARG;
-    if (H % 64 != 0 || N < 128 || N % 128 != 0 || d_w == nullptr || !aligned(d_w, 16))
-        return MOE_ERR_INVALID_ARG;
+    if (fp8 && (d_w_scale == nullptr || !aligned(d_w_scale, 4))) return MOE_ERR_INVALID_ARG;
     if (d_out == nullptr && N != H) return MOE_ERR_INVALID_ARG;
     if (d_out != nullptr && !aligned(d_out, 16)) return MOE_ERR_INVALID_ARG;
     if (h->ntok == 0) return MOE_OK;
@@ -626,15 +631,29 @@ int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void 
     gp.w = d_w;
     gp.out = d_out != nullptr ? d_out : h->ws + h->L.expert_out;
     gp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+    gp.x_scale = fp8 ? at<float>(h, h->L.recv_scale) : nullptr;
+    gp.w_scale = fp8 ? d_w_scale : nullptr;
     gp.flags = at<uint32_t>(h, h->L.flags);
     gp.E = h->cfg.num_experts;
     gp.cap = h->cfg.ep_size * h->m;
     gp.H = H;
     gp.N = N;
     gp.mtiles = (gp.cap + 127) / 128;
+    gp.fp8 = fp8 ? 1 : 0;
     return moe::launch_expert_gemm(gp, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream) {
+    return expert_gemm_impl(h, d_w, nullptr, N, d_out, false, stream);
+}
+
+int moe_expert_gemm_fp8(moe_a2a_t *h, const void *d_w8, const float *d_w_scale, int32_t N,
+                        void *d_out, void *stream) {
+    return expert_gemm_impl(h, d_w8, d_w_scale, N, d_out, true, stream);
 }
 
 int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction) {

@@ -7,8 +7,9 @@
 //    [0,14), leading-dimension byte offset >> 4 in [16,30), stride-dimension
 //    byte offset >> 4 in [32,46), the constant 0b001 in [46,49), base offset
 //    in [49,52), swizzle mode in [61,64) (2 = 128-byte swizzle);
-//  * instruction descriptor of .kind::f16 (32 bits): D format in [4,6)
-//    (1 = f32), A format in [7,10) and B format in [10,13) (1 = bf16),
+//  * instruction descriptor of .kind::f16 / .kind::f8f6f4 (32 bits): D
+//    format in [4,6) (1 = f32), A format in [7,10) and B format in [10,13)
+//    (f16 kind: 1 = bf16; f8f6f4 kind: 0 = E4M3),
 //    A / B major in bits 15 / 16 (0 = K-major), N >> 3 in [17,23),
 //    M >> 4 in [24,29);
 //  * tensor-memory address: lane in bits [16,32), column in [0,16).
@@ -38,6 +39,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// e4m3 x e4m3 -> f32 (.kind::f8f6f4, format code 0 = E4M3), both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Allocation of `ncols` tensor-memory columns (a power of two >= 32) by one
@@ -71,6 +77,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T on 8-bit operands (32 per K step).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
         : "memory");
 }

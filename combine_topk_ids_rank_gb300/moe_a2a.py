@@ -32,7 +32,7 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks",
            "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8",
            "moe_a2a_workspace_bytes_layout", "moe_a2a_create_layout",
-           "moe_expert_gemm")
+           "moe_expert_gemm", "moe_expert_gemm_fp8")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
@@ -107,6 +107,8 @@ def _load(path: str = LIBRARY):
     lib.moe_quantize_rows_fp8.restype = ctypes.c_int
     lib.moe_expert_gemm.argtypes = [p, p, i32, p, p]
     lib.moe_expert_gemm.restype = ctypes.c_int
+    lib.moe_expert_gemm_fp8.argtypes = [p, p, p, i32, p, p]
+    lib.moe_expert_gemm_fp8.restype = ctypes.c_int
     lib.moe_a2a_set_recv_format.argtypes = [p, i32]
     lib.moe_a2a_set_recv_format.restype = ctypes.c_int
     lib.moe_a2a_set_reduction.argtypes = [p, i32]
@@ -226,6 +228,12 @@ def quantize_rows_fp8(x, out=None, scale=None, stream=None):
 def moe_expert_gemm(h, d_w: int, N: int, d_out: int, stream: int = 0) -> int:
     v = ctypes.c_void_p
     return _lib.moe_expert_gemm(h, v(d_w), N, v(d_out), v(stream))
+
+
+def moe_expert_gemm_fp8(h, d_w8: int, d_w_scale: int, N: int, d_out: int,
+                        stream: int = 0) -> int:
+    v = ctypes.c_void_p
+    return _lib.moe_expert_gemm_fp8(h, v(d_w8), v(d_w_scale), N, v(d_out), v(stream))
 
 
 def moe_a2a_set_recv_format(h, fmt: int) -> int:
@@ -503,6 +511,25 @@ class MoeA2A:
         st = moe_expert_gemm(self.handle, _ptr(w), N, _ptr(out), self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_expert_gemm")
+        return out if out is not None else self.combine_payload()
+
+    def expert_gemm_fp8(self, w8, w_scale, out=None, stream=None):
+        """FP8 receive format: out[e][j] = (qx[e][j] . qw[e]^T) sx[e][j] sw[e].
+        w8: e4m3 [E, N, H] (float8_e4m3fn or uint8); w_scale: float32 [E, N];
+        out: bf16 [E, cap, N], or None to write the combine payload (N == H)."""
+        import torch
+        E, H = self.num_experts, self.hidden
+        N = w8.shape[1]
+        if w8.dtype not in (torch.float8_e4m3fn, torch.uint8) or tuple(w8.shape) != (E, N, H) \
+                or not w8.is_contiguous():
+            raise ValueError("w8: expected contiguous e4m3 [%d, N, %d]" % (E, H))
+        self._check(w_scale, torch.float32, (E, N), "w_scale")
+        if out is not None:
+            self._check(out, torch.bfloat16, (E, self.last_view.plane_stride, N), "out")
+        st = moe_expert_gemm_fp8(self.handle, _ptr(w8), _ptr(w_scale), N, _ptr(out),
+                                 self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_expert_gemm_fp8")
         return out if out is not None else self.combine_payload()
 
     def set_recv_format(self, fmt: int):

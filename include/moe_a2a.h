@@ -192,6 +192,20 @@ enum moe_layout { MOE_LAYOUT_RANK = 0, MOE_LAYOUT_EXPERT = 1 };
  * kernel on `stream`. */
 int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream);
 
+/* The same product on FP8 operands (tcgen05 .kind::f8f6f4, e4m3 x e4m3 into
+ * fp32), for a dispatch made in the FP8 receive format: the rows are the
+ * e4m3 codes qx with their per-row scales sx (recv_scale), the weights e4m3
+ * codes qw [E][N][H] with one fp32 scale per output channel sw [E][N]
+ * (reading: dequantised operands, the FP8 payload of [IX] "The adapter"):
+ *   out[e][j][n] = bf16_rn( (sum_h f(qx) * f(qw)) * sx[e][j] * sw[e][n] ),
+ * the products of e4m3 values exact, the sum in fp32 on the tensor cores,
+ * then two fp32 multiplies.  H must be a multiple of 128, N of 128; d_w8
+ * 16-byte and d_w_scale 4-byte aligned; d_out as for moe_expert_gemm (bf16,
+ * NULL = the combine payload when N == H).  Requires the expert layout and
+ * the FP8 receive format. */
+int moe_expert_gemm_fp8(moe_a2a_t *h, const void *d_w8, const float *d_w_scale, int32_t N,
+                        void *d_out, void *stream);
+
 /* moe_a2a_workspace_bytes for a layout (0 if the pair is invalid). */
 size_t moe_a2a_workspace_bytes_layout(const moe_a2a_config_t *cfg, int32_t layout);
 

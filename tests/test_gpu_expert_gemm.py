@@ -175,3 +175,117 @@ def test_expert_gemm_contract():
         b.expert_gemm(wt)
     assert ex.value.status == MOE_ERR_INVALID_ARG
     b.combine(None, False)
+
+
+# --------------------------------------------------------------------------
+# FP8 operands: the FP8 receive format (e4m3 rows + per-row scale) against
+# e4m3 weights with per-channel scales (tcgen05 .kind::f8f6f4)
+# --------------------------------------------------------------------------
+
+def dispatched_fp8(R, T, H, E, K, seed):
+    from combine_topk_ids_rank_gb300.moe_a2a import (MoeA2A, MOE_LAYOUT_EXPERT,
+                                                     MOE_FORMAT_FP8_E4M3)
+    ids = synth.topk_ids(seed, R, T, E, K)
+    w = synth.topk_weights(seed, R, T, K)
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    a = MoeA2A(R, T, H, E, K, "cuda", layout=MOE_LAYOUT_EXPERT)
+    a.workspace.fill_(parity.POISON)
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    view = a.dispatch(parity.to_dev(ids, torch.int32), parity.to_dev(w, torch.float32),
+                      parity.to_dev(x, torch.bfloat16))
+    r = oracle.route_experts(ids, w, E, T)
+    q, sc = oracle.quantize_rows_fp8(x)                  # the oracle's own quantisation
+    cap = R * T
+    qx = np.zeros((E, cap, H), np.uint8)
+    sx = np.ones((E, cap), np.float32)
+    for e in range(E):
+        for j in range(r["recv_counts"][e]):
+            s, t = divmod(int(r["src_row"][e, j]), T)
+            qx[e, j], sx[e, j] = q[s, t], sc[s, t]
+    return a, view, dict(r=r, qx=qx, sx=sx)
+
+
+def fp8_weights(seed, E, N, H):
+    rng = np.random.default_rng(seed)
+    qw = rng.integers(0, 256, (E, N, H)).astype(np.uint8)
+    qw[(qw & 0x7F) >= 0x70] &= 0x8F                       # keep |w| small, no NaN codes
+    sw = rng.uniform(0.5 / np.sqrt(H), 2.0 / np.sqrt(H), (E, N)).astype(np.float32)
+    return qw, sw
+
+
+def check_rows_fp8(got, d, qw, sw, rows):
+    E, _, H = qw.shape
+    counts = d["r"]["recv_counts"]
+    fw_all = oracle.fp8_to_f32(qw).astype(np.float64)
+    for e in range(E):
+        js = [j for j in rows if j < counts[e]]
+        if not js:
+            continue
+        y = oracle.expert_gemm_fp8(d["qx"][e, js][None], d["sx"][e, js][None], qw[e][None],
+                                   sw[e][None], np.array([len(js)], np.int32))[0]
+        fx = np.abs(oracle.fp8_to_f32(d["qx"][e, js]).astype(np.float64))
+        absum = (fx @ np.abs(fw_all[e]).T) * d["sx"][e, js, None] * sw[e][None, :]
+        bound = (2.0 ** -8 + 2.0 ** -22) * np.abs(y) + H * 2.0 ** -23 * absum + 1e-30
+        err = np.abs(parity.f32(got[e, js]).astype(np.float64) - y)
+        assert (err <= bound).all(), (e, float(err.max()), float((err / bound).max()))
+
+
+@pytest.mark.parametrize("R,T,H,E,K,N", [(2, 64, 128, 4, 2, 128), (4, 100, 256, 8, 4, 512),
+                                         (3, 50, 384, 6, 3, 384)])
+def test_expert_gemm_fp8_small(R, T, H, E, K, N):
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=R + N)
+    cap = view.plane_stride
+    qw, sw = fp8_weights(11, E, N, H)
+    out = torch.full((E, cap, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    a.expert_gemm_fp8(parity.to_dev(qw, torch.uint8), parity.to_dev(sw, torch.float32), out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(out)
+    check_rows_fp8(got, d, qw, sw, range(cap))
+    counts = d["r"]["recv_counts"]
+    for e in range(E):
+        assert (got[e, counts[e]:] == 0x7FC0).all()
+    a.combine(None, False)
+
+
+def test_expert_gemm_fp8_identity_is_exact():
+    # identity codes (0x38 = 1.0), unit channel scales: out = bf16(f(qx) * sx)
+    R, T, H, E, K = 4, 70, 256, 8, 3
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=8)
+    eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+    qw = np.ascontiguousarray(np.broadcast_to(eye, (E, H, H)))
+    out = a.expert_gemm_fp8(parity.to_dev(qw, torch.uint8),
+                            torch.ones((E, H), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(out)
+    counts = d["r"]["recv_counts"]
+    for e in range(E):
+        c = counts[e]
+        want = oracle.fp8_to_f32(d["qx"][e, :c]) * d["sx"][e, :c, None]   # fp32 product
+        assert np.array_equal(got[e, :c], oracle.bf16_bits(want.astype(np.float32)))
+    a.combine(None, False)
+
+
+def test_expert_gemm_fp8_hidden_7168():
+    R, T, H, E, K, N = 8, 32, 7168, 8, 8, 7168
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=12)
+    cap = view.plane_stride
+    qw, sw = fp8_weights(13, E, N, H)
+    out = torch.empty((E, cap, N), dtype=torch.bfloat16, device="cuda")
+    a.expert_gemm_fp8(parity.to_dev(qw, torch.uint8), parity.to_dev(sw, torch.float32), out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    check_rows_fp8(parity.to_host_u16(out), d, qw, sw, [0, 100, 127, 128, 255])
+    a.combine(None, False)
+
+
+def test_expert_gemm_fp8_contract():
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2AError, MOE_ERR_INVALID_ARG
+    a, view, d = dispatched_fp8(2, 16, 128, 4, 2, seed=1)
+    w8 = torch.zeros((4, 128, 128), dtype=torch.uint8, device="cuda")
+    with pytest.raises(MoeA2AError) as ex:          # bf16 product on e4m3 rows
+        a.expert_gemm(torch.zeros((4, 128, 128), dtype=torch.bfloat16, device="cuda"))
+    assert ex.value.status == MOE_ERR_INVALID_ARG
+    a.expert_gemm_fp8(w8, torch.ones((4, 128), dtype=torch.float32, device="cuda"))
+    a.combine(None, False)
