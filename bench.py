@@ -68,8 +68,8 @@ def parse_args():
                          "direct calls (measured no faster on GB300)")
     args = ap.parse_args()
     if args.expert_gemm:
-        if args.fp8 or args.graph:
-            ap.error("--expert-gemm takes bf16 rows and direct calls")
+        if args.graph:
+            ap.error("--expert-gemm takes direct calls")
         args.layout = "expert"
     return args
 
@@ -335,10 +335,19 @@ def run_gpu(args, w, rank, world, local_rank):
     if gemm:
         gw = torch.Generator(device=dev).manual_seed(args.seed + 2)
         w_exp = torch.randn((E, H, H), generator=gw, device=dev, dtype=torch.bfloat16)
-        w_exp.mul_(1.0 / H ** 0.5)      # in place: E x H x H can be tens of GB
+        if fp8:
+            # e4m3 weights of N(0,1) with a per-channel scale 1/sqrt(H)
+            w8 = w_exp.to(torch.float8_e4m3fn)
+            del w_exp
+            w8_scale = torch.full((E, H), 1.0 / H ** 0.5, dtype=torch.float32, device=dev)
 
-        def run_gemm():
-            a2a.expert_gemm(w_exp)      # into the combine payload
+            def run_gemm():
+                a2a.expert_gemm_fp8(w8, w8_scale)   # into the combine payload
+        else:
+            w_exp.mul_(1.0 / H ** 0.5)      # in place: E x H x H can be tens of GB
+
+            def run_gemm():
+                a2a.expert_gemm(w_exp)      # into the combine payload
 
     def combine_into(res_, outs):
         if fp8:
@@ -464,7 +473,7 @@ def run_gpu(args, w, rank, world, local_rank):
         **({"expert_gemm": {
             "ms_avg": statistics.fmean(gemm_ms), "ms_p50": pct(gemm_ms, 0.5),
             "ms_p10": pct(gemm_ms, 0.1), "ms_p90": pct(gemm_ms, 0.9),
-            "flops": 2.0 * recv_rows * H * H, "weight_bytes": E * H * H * 2,
+            "flops": 2.0 * recv_rows * H * H, "weight_bytes": E * H * H * (1 if fp8 else 2),
             "tflops": 2.0 * recv_rows * H * H / statistics.fmean(gemm_ms) / 1e9,
             "kernels": ["expert_gemm"]}} if gemm else {}),
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
@@ -608,7 +617,10 @@ def run_gpu(args, w, rank, world, local_rank):
     }
     if gemm:
         # the product dominates the step: report it against the tensor peak
+        # (e4m3: the measured bf16 peak times the nominal fp8 / bf16 ratio, 2)
         tpk, tkind = measured_tensor_peak()
+        if fp8:
+            tpk, tkind = 2.0 * tpk, tkind + ", x2 for e4m3"
         tf = phases["expert_gemm"]["tflops"]
         gtraffic = None
         try:
@@ -626,8 +638,8 @@ def run_gpu(args, w, rank, world, local_rank):
         line["roofline_combine"] = {"bound": "hbm", "achieved": c_bytes / c_avg / 1e6,
                                     "peak": peak, "unit": "GB/s",
                                     "frac": c_bytes / c_avg / 1e6 / peak}
-        cfg["expert_gemm"] = "W_e bf16 [%d][%d][%d], N(0,1/H), output into the combine payload" % (
-            E, H, H)
+        cfg["expert_gemm"] = ("W_e %s [%d][%d][%d], output into the combine payload" % (
+            "e4m3 (per-channel scale 1/sqrt(H))" if fp8 else "bf16 N(0,1/H)", E, H, H))
     return line
 
 
