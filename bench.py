@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
                     help="receive layout: planes per (destination, source) rank, or one "
                          "row per (token, expert) in per-expert planes")
+    ap.add_argument("--l2-hot", action="store_true",
+                    help="no L2 flush between steps even for small inputs (reports the "
+                         "L2-hot figure beside the default flushed one; not a bench line)")
     ap.add_argument("--expert-gemm", action="store_true",
                     help="expert layout with the expert-side product between dispatch and "
                          "combine (random bf16 weights W_e of H x H, output into the combine "
@@ -409,6 +412,8 @@ def run_gpu(args, w, rank, world, local_rank):
     if fp8:
         cfg["payload"] = ("e4m3 dispatch rows + fp32 per-token scale; combine output e4m3 + "
                           "fp32 per-token scale (residual_out bf16)")
+    if args.l2_hot:
+        cfg["l2"] = "L2 hot: no flush between steps (small inputs may stay in L2)"
     if "flushed" in cfg["l2"]:
         # write a buffer twice the size of L2, then read another one, so the
         # timed kernels find L2 holding clean, unrelated lines
