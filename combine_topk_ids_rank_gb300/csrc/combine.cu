@@ -70,7 +70,9 @@ __device__ __forceinline__ void accumulate8(float (&a)[8], const uint4 v, const 
     }
 }
 
-template <int VPT, int G, bool WEIGHTED, bool FUSED>
+// EXP: send-table entries are absolute rows of the expert layout (lane =
+// top-k slot); otherwise slots of the (rank, source) planes (lane = rank).
+template <int VPT, int G, bool WEIGHTED, bool FUSED, bool EXP>
 __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParams p) {
     __shared__ float red[2][kMaxThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -89,7 +91,17 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
     auto load_route = [&](long long i, int &slot, float &w) {
         slot = -1;
         w = 0.0f;
-        if (i < p.tokens && lane < p.dest.P) {
+        if (!EXP && i < p.tokens && lane < p.R && ((p.active >> lane) & 1u)) {
+            int s, t;
+            token_of(p.map, p.R, i, s, t);
+            const long long tok = (long long)s * p.map.stride + t;
+            slot = __ldg(p.send_slot + tok * p.RP + lane);
+            if (WEIGHTED) w = __ldg(p.dest_weight + tok * p.RP + lane);
+            if (slot >= p.m) {  // guard: never expected from the routing pass
+                if (warp == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                slot = -1;
+            }
+        } else if (EXP && i < p.tokens && lane < p.dest.P) {
             int s, t;
             token_of(p.map, p.R, i, s, t);
             const long long tok = (long long)s * p.map.stride + t;
@@ -101,7 +113,7 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
                     if (warp == 0) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
                     slot = -1;
                 } else if (!((p.active >> dest_rank(p.dest, lane, slot)) & 1u)) {
-                    slot = -1;  // the rank is gone
+                    slot = -1;  // the expert's rank is gone
                 }
             }
         }
@@ -147,7 +159,9 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
                 sq[q] = __shfl_sync(kFull, slot_l, src);
                 wq[q] = WEIGHTED ? __shfl_sync(kFull, w_l, src) : 1.0f;
                 if (dq[q] >= 0) {
-                    const long long base = dest_row(p.dest, p.R, p.m, dq[q], s, sq[q]) * p.H8;
+                    const long long base =
+                        (EXP ? (long long)sq[q]
+                             : ((long long)dq[q] * p.R + s) * p.m + sq[q]) * p.H8;
 #pragma unroll
                     for (int j = 0; j < VPT; ++j) {
                         const int c = tid + j * nthreads;
@@ -217,9 +231,13 @@ __global__ void __launch_bounds__(kMaxThreads) combine_kernel(const CombineParam
 
 template <int VPT, int G, bool W, bool F>
 cudaError_t shape_of(int nthreads, int num_sms, LaunchShape *shape) {
-    int per_sm = 0;
+    int per_sm = 0, per_sm_e = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, combine_kernel<VPT, G, W, F>, nthreads, 0);
+        &per_sm, combine_kernel<VPT, G, W, F, false>, nthreads, 0);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm_e, combine_kernel<VPT, G, W, F, true>, nthreads, 0);
+    per_sm = per_sm_e < per_sm ? per_sm_e : per_sm;  // one shape serves both layouts
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     shape->grid = num_sms * per_sm;
@@ -233,7 +251,10 @@ cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStrea
     long long grid = shape.grid;
     if (grid > p.tokens) grid = p.tokens;
     if (grid < 1) return cudaSuccess;
-    combine_kernel<VPT, G, W, F><<<(unsigned)grid, shape.block, 0, st>>>(p);
+    if (p.dest.expert)
+        combine_kernel<VPT, G, W, F, true><<<(unsigned)grid, shape.block, 0, st>>>(p);
+    else
+        combine_kernel<VPT, G, W, F, false><<<(unsigned)grid, shape.block, 0, st>>>(p);
     return cudaGetLastError();
 }
 

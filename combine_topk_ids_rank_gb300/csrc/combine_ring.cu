@@ -208,7 +208,7 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
             const int d = __ffs(b) - 1;
             b &= b - 1;
             const int sl = __shfl_sync(kFull, slot, d);
-            const long long row = dest_row(p.dest, p.R, p.m, d, s, sl);
+            const long long row = dest_row_checked(p.dest, p.R, p.m, d, s, sl);
             if (!issue_row(eo + row * row_bytes)) {
                 ok = false;
                 break;

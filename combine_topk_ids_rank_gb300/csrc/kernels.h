@@ -124,6 +124,13 @@ __device__ __forceinline__ long long dest_row(const DestRows &D, int R, int m, i
     return v < m ? ((long long)d * R + s) * m + v : -1;
 }
 
+// The same row for an entry already checked with dest_row (no guard, no
+// branch: for the load-issue paths of the combines).
+__device__ __forceinline__ long long dest_row_checked(const DestRows &D, int R, int m, int d,
+                                                      int s, int v) {
+    return D.expert ? (long long)v : ((long long)d * R + s) * m + v;
+}
+
 // Rank that owns send-row entry d holding v >= 0 (for the active-rank test).
 __device__ __forceinline__ int dest_rank(const DestRows &D, int d, int v) {
     return D.expert ? (v / D.cap) / D.Epr : d;
