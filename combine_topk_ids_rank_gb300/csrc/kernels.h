@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 
 #include <cuda_runtime.h>
 
@@ -40,12 +41,18 @@ __host__ __device__ inline void token_of(const TokenMap &m, int R, long long i, 
 constexpr int kRouteTile = 256;
 constexpr int kRouteMinTile = 32;
 
-// Tile of one call: the largest power of two in [32, 256] that still gives
-// about two CTAs per SM.
+// Tile of one call: 256 tokens.  Smaller tiles (more CTAs per SM) measured
+// slower on every shape tried -- wide EP 206.6 us at 32 vs 199-200 us at
+// 128-256, prefill 321.5 vs 318.8, decode 32.0 vs 31.4 (dispatch phase) --
+// since the work per token is a few dependent memory accesses and more CTAs
+// only add scan steps.  MOE_ROUTE_TILE=32|64|128|256 overrides (tuning).
 inline int route_tile(long long R, long long T, int num_sms) {
-    int tile = kRouteTile;
-    while (tile > kRouteMinTile && R * ((T + tile - 1) / tile) < 2ll * num_sms) tile /= 2;
-    return tile;
+    (void)R, (void)T, (void)num_sms;
+    if (const char *e = std::getenv("MOE_ROUTE_TILE")) {
+        const int t = std::atoi(e);
+        if (t == 32 || t == 64 || t == 128 || t == 256) return t;
+    }
+    return kRouteTile;
 }
 
 // Routing, pass 1: per-tile destination counts, their exclusive per-tile
