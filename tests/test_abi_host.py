@@ -217,3 +217,18 @@ def test_expert_layout_host_checks(abi):
     assert abi.moe_a2a_create_layout(c, 5, 1 << 30, ex)[0] == abi.MOE_ERR_INVALID_ARG
     assert abi.moe_a2a_create_layout(c, abi.MOE_LAYOUT_EXPERT, 1 << 30, ex - 1)[0] == \
         abi.MOE_ERR_CAPACITY
+
+
+def test_expert_gemm_host_checks(abi):
+    A = 1 << 20
+    assert abi.moe_expert_gemm(None, A, 128, 0) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_expert_gemm_fp8(None, A, A, 128, 0) == abi.MOE_ERR_INVALID_ARG
+    c = abi.config(4, 64, 256, 16, 2)
+    need = abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_EXPERT)
+    st, h = abi.moe_a2a_create_layout(c, abi.MOE_LAYOUT_EXPERT, 1 << 30, need)
+    assert st == abi.MOE_OK
+    # no dispatch pending: the phase error comes first, nothing is queued
+    assert abi.moe_expert_gemm(h, A, 256, 0) == abi.MOE_ERR_PHASE
+    assert abi.moe_expert_gemm_fp8(h, A, A, 256, 0) == abi.MOE_ERR_PHASE
+    assert abi.moe_a2a_phase(h) == 0
+    abi.moe_a2a_destroy(h)
