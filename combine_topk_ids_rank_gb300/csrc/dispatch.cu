@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
     const long long first = blockIdx.x, step = gridDim.x;
     const long long n = first < p.units ? (p.units - 1 - first) / step + 1 : 0;
     const uint32_t meta_bytes = (uint32_t)p.dest.P * 4u;
+    const bool split = p.tile_prefix != nullptr;  // local slots + tile prefixes
 
     auto unit_bytes = [&](int chunk) -> uint32_t {
         const int left = p.row_bytes - chunk * p.chunk_bytes;
@@ -55,36 +56,39 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
     };
     // Unit i of this CTA: a chunk of the row of token (s, t), stored at row
     // s * stride + t of the token arrays.
-    auto unit_of = [&](long long i, int &s, long long &row, int &chunk) {
+    auto unit_of = [&](long long i, int &s, long long &row, int &chunk, int &t) {
         const long long u = first + i * step;
         const long long k = u / p.chunks;
         chunk = (int)(u - k * p.chunks);
-        int t;
         token_of(p.map, p.R, k, s, t);
         row = (long long)s * p.map.stride + t;
     };
     // A unit's stage receives its row chunk (an input of the call) and its
     // send row (written by the routing pass); both complete on one barrier.
     auto issue_row = [&](long long i) {
-        int s, chunk;
+        int s, chunk, t;
         long long token;
-        unit_of(i, s, token, chunk);
+        unit_of(i, s, token, chunk, t);
         const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         const uint32_t bytes = unit_bytes(chunk);
         ptx::fence_proxy_async_smem();  // earlier ordinary reads of this stage
-        ptx::mbar_arrive_expect_tx(&bars[stage], bytes + meta_bytes);
+        ptx::mbar_arrive_expect_tx(&bars[stage], bytes + (split ? 2 : 1) * meta_bytes);
         ptx::bulk_g2s(buf, p.x + token * p.row_bytes + (long long)chunk * p.chunk_bytes, bytes,
                       &bars[stage]);
     };
     auto issue_meta = [&](long long i) {
-        int s, chunk;
+        int s, chunk, t;
         long long token;
-        unit_of(i, s, token, chunk);
+        unit_of(i, s, token, chunk, t);
         const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         ptx::bulk_g2s(buf + p.chunk_bytes, p.send_slot + token * p.dest.P, meta_bytes,
                       &bars[stage]);
+        if (split)  // the exclusive prefix of the token's tile, per destination
+            ptx::bulk_g2s(buf + p.chunk_bytes + meta_bytes,
+                          p.tile_prefix + ((long long)s * p.ntiles + t / p.tile) * p.dest.P,
+                          meta_bytes, &bars[stage]);
     };
     auto issue = [&](long long i) {
         issue_row(i);
@@ -109,15 +113,16 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
                                        kWaitLimit);
             return;
         }
-        int s, chunk;
+        int s, chunk, t;
         long long token;
-        unit_of(i, s, token, chunk);
+        unit_of(i, s, token, chunk, t);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         const int32_t *slots = reinterpret_cast<const int32_t *>(buf + p.chunk_bytes);
+        const int32_t *prefix = slots + p.dest.P;
         const uint32_t bytes = unit_bytes(chunk);
         const long long col = (long long)chunk * p.chunk_bytes;
         for (int d = 0; d < p.dest.P; ++d) {
-            const int32_t slot = slots[d];
+            const int32_t slot = slots[d] < 0 ? -1 : slots[d] + (split ? prefix[d] : 0);
             if (slot < 0) continue;
             const long long row = dest_row(p.dest, p.R, p.m, d, s, slot);
             if (row < 0) {  // guard: never expected from the routing pass
@@ -151,7 +156,7 @@ cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, DispatchParams *
     const int chunks = (row_bytes + kMaxChunk - 1) / kMaxChunk;
     int chunk = (row_bytes + chunks - 1) / chunks;
     chunk = (chunk + 15) / 16 * 16;
-    const int stage_bytes = (chunk + P * 4 + 127) / 128 * 128;
+    const int stage_bytes = (chunk + 2 * P * 4 + 127) / 128 * 128;  // row, slots, prefixes
     int stages = 65536 / stage_bytes;
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     stages = env_int("MOE_DISPATCH_STAGES", stages);

@@ -65,6 +65,7 @@ struct RouteCountParams {
     int32_t *tile_ticket;     // [R], zero between calls
     int32_t *hist_accum;      // [R][E], zero between calls
     int32_t *recv_counts;     // [R][R]
+    int32_t *local_slot;      // [R][T][RP] slots inside the token's tile, or null
     uint32_t *flags;          // sticky device flag word
     TokenMap map;
     uint32_t active;          // ranks that receive messages
@@ -152,6 +153,11 @@ struct DispatchParams {
     uint32_t *flags;
     TokenMap map;
     DestRows dest;
+    // Rank layout straight after route_count: send_slot holds slots inside
+    // the token's tile and tile_prefix the tiles' exclusive prefixes; else
+    // (tile_prefix null) send_slot holds the final entries.
+    const int32_t *tile_prefix;  // [R][ntiles][RP] or null
+    int tile, ntiles;
     int R, RP, m;
     int row_bytes;             // 2H
     int chunk_bytes;           // <= row_bytes, multiple of 16

@@ -29,7 +29,7 @@ struct Layout {
     size_t recv_x, expert_out, recv_ids, recv_w, recv_scale, src_token, recv_counts,
         local_counts;
     size_t send_slot, dest_weight, topk_dest, tile_counts, tile_prefix, tile_ticket, hist_accum,
-        flags;
+        local_slot, flags;
     size_t total;
     int layout;      // MOE_LAYOUT_*
     int RP, ntiles_max;
@@ -84,6 +84,7 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
         L->tile_prefix = take(0);
         L->tile_ticket = take(0);
         L->hist_accum = take(0);
+        L->local_slot = take(0);
         L->flags = take(kAlign);
         L->total = off;
         return true;
@@ -106,6 +107,7 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
     L->tile_prefix = take(R * NT * RP * 4);
     L->tile_ticket = take(R * 4);  // ticket and histogram accumulator are
     L->hist_accum = take(R * E * 4);  // zero between calls
+    L->local_slot = take(R * M * RP * 4);
     L->flags = take(kAlign);
     L->total = off;
     return true;
@@ -134,6 +136,12 @@ struct moe_a2a {
     int num_sms;
     moe::DispatchParams dispatch_tmpl;
     moe::LaunchShape dispatch_shape;
+    // The rank layout's second routing pass runs on `side`, beside the row
+    // copy: forked after the first pass (ev_count), joined before the call
+    // returns (ev_scan).
+    bool overlap;
+    cudaStream_t side;
+    cudaEvent_t ev_count, ev_scan;
     // combine launch shapes by variant: 4 * out8 + 2 * weighted + fused
     bool combine_ready[8];
     bool combine_ring[8];
@@ -161,6 +169,14 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
         return MOE_ERR_CUDA;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
+    const char *ov = std::getenv("MOE_ROUTE_OVERLAP");
+    h->overlap = h->L.layout == MOE_LAYOUT_RANK && !(ov != nullptr && ov[0] == '0');
+    if (h->overlap && h->side == nullptr) {
+        if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_count, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_scan, cudaEventDisableTiming) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     h->accum_dirty = h->L.layout == MOE_LAYOUT_RANK;
     h->ready = true;
     return MOE_OK;
@@ -189,8 +205,12 @@ void uniform_map(int R, int T, moe::TokenMap *map) {
 
 // The row copy of the dispatch phase (after the routing pass queued its
 // send table): bf16 rows, or e4m3 rows + scales in the FP8 receive format.
+//
+// With `tile` > 0 (bf16 rank layout, second routing pass still running) the
+// copy reads the first pass's tile-local slots and adds the tile prefixes.
 int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
-                const moe::DestRows &dest, long long ntok, cudaStream_t st) {
+                const moe::DestRows &dest, long long ntok, cudaStream_t st, int tile = 0,
+                int ntiles = 0) {
     const int R = h->cfg.ep_size;
     uint32_t *flags = at<uint32_t>(h, h->L.flags);
     if (h->recv_format == MOE_FORMAT_FP8_E4M3) {
@@ -217,6 +237,11 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
     dp.dest = dest;
     dp.R = R, dp.RP = h->L.RP, dp.m = m;
     dp.units = ntok * dp.chunks;
+    if (tile > 0) {
+        dp.send_slot = at<int32_t>(h, h->L.local_slot);
+        dp.tile_prefix = at<int32_t>(h, h->L.tile_prefix);
+        dp.tile = tile, dp.ntiles = ntiles;
+    }
     return moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
@@ -300,6 +325,8 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rc_p.R = R, rc_p.K = K, rc_p.E = E, rc_p.Epr = E / R, rc_p.RP = RP;
         rc_p.ntiles = ntiles;
         rc_p.tile = tile;
+        const bool overlap = h->overlap && h->recv_format == MOE_FORMAT_BF16;
+        rc_p.local_slot = overlap ? at<int32_t>(h, h->L.local_slot) : nullptr;
         if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
         h->accum_dirty = true;  // until the scan pass that clears it is queued
 
@@ -320,11 +347,26 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rs.R = R, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
         rs.ntiles = ntiles;
         rs.tile = tile;
-        if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
-        h->accum_dirty = false;
-
-        rc = launch_rows(h, d_x, map, m, dest, ntok, st);
-        if (rc != MOE_OK) return rc;
+        if (overlap) {
+            // The row copy needs only the first pass; the second (send
+            // table, weights, metadata rows) runs beside it on `side`.
+            if (cudaEventRecord(h->ev_count, st) != cudaSuccess ||
+                cudaStreamWaitEvent(h->side, h->ev_count, 0) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            if (moe::launch_route_scan(rs, h->side, false) != cudaSuccess) return MOE_ERR_CUDA;
+            const int rows_rc = launch_rows(h, d_x, map, m, dest, ntok, st, tile, ntiles);
+            // Join whatever happened to the copy, so `side` never outlives the call.
+            if (cudaEventRecord(h->ev_scan, h->side) != cudaSuccess ||
+                cudaStreamWaitEvent(st, h->ev_scan, 0) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            h->accum_dirty = false;
+            if (rows_rc != MOE_OK) return rows_rc;
+        } else {
+            if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+            h->accum_dirty = false;
+            rc = launch_rows(h, d_x, map, m, dest, ntok, st);
+            if (rc != MOE_OK) return rc;
+        }
     }
 
     h->map = map;
@@ -576,6 +618,10 @@ int moe_a2a_get_error(moe_a2a_t *h, void *stream, uint32_t *flags) {
 
 int moe_a2a_destroy(moe_a2a_t *h) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    // Pending work on `side` completes before its resources are released.
+    if (h->ev_scan != nullptr) cudaEventDestroy(h->ev_scan);
+    if (h->ev_count != nullptr) cudaEventDestroy(h->ev_count);
+    if (h->side != nullptr) cudaStreamDestroy(h->side);
     delete h;
     return MOE_OK;
 }

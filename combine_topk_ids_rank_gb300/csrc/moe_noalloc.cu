@@ -143,6 +143,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     c.topk_ids = d_topk_ids;
     c.tile_counts = tile_counts;
     c.tile_prefix = tile_prefix;
+    c.local_slot = nullptr;
     c.tile_ticket = tile_ticket;
     c.hist_accum = hist_accum;
     c.recv_counts = d_recv_counts;

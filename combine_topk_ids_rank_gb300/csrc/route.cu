@@ -108,6 +108,31 @@ __global__ void __launch_bounds__(kRouteTile) route_count_kernel(const RouteCoun
             for (int w = 0; w < nwarps; ++w) sum += warp_cnt[w][d];
         p.tile_counts[((size_t)s * p.ntiles + tile) * p.RP + d] = sum;
     }
+    // Slots inside the tile (the tile's exclusive prefix, once known, turns
+    // them into plane slots): the row copy needs nothing else, so it can
+    // start as soon as this pass ends.
+    if (p.local_slot != nullptr) {
+        const uint32_t lt = lanemask_lt();
+        const bool token = t < p.map.count[s];
+        int32_t *lrow = p.local_slot + ((size_t)s * p.map.stride + (token ? t : 0)) * p.RP;
+        for (int d0 = 0; d0 < p.RP; d0 += 4) {
+            int4 v;
+            int32_t *ve = &v.x;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int d = d0 + q;
+                const bool has = d < p.R && ((mask >> d) & 1u);
+                const uint32_t b = __ballot_sync(kFull, has);  // whole warp: converged
+                int slot = -1;
+                if (has) {
+                    slot = __popc(b & lt);
+                    for (int w = 0; w < warp; ++w) slot += warp_cnt[w][d];
+                }
+                ve[q] = slot;
+            }
+            if (token) *reinterpret_cast<int4 *>(lrow + d0) = v;
+        }
+    }
     int32_t *acc = p.hist_accum + (size_t)s * p.E;  // one accumulator per source rank
     for (int e = threadIdx.x; e < p.E; e += p.tile)
         if (hist[e] != 0) atomicAdd(&acc[e], hist[e]);

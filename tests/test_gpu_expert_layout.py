@@ -176,3 +176,43 @@ def test_expert_layout_rejects_tree_and_large_E():
         a.set_reduction(MOE_REDUCE_BF16_TOPK_TREE)
     with pytest.raises(MoeA2AError):
         MoeA2A(2, 8, 64, 2048, 2, "cuda", layout=MOE_LAYOUT_EXPERT)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_expert_layout_fp8_combine_output(fused):
+    # the FP8 combine output in the expert layout: plain sum bit for bit,
+    # fused RMSNorm output within one e4m3 step of the oracle's quantisation
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_LAYOUT_EXPERT
+    R, T, H, E, K = 4, 90, 256, 32, 6
+    inp = make(R, T, H, E, K, 21, dup=True)
+    a = MoeA2A(R, T, H, E, K, "cuda", layout=MOE_LAYOUT_EXPERT)
+    dev = parity.to_dev
+    view = a.dispatch(dev(inp["ids"], torch.int32), dev(inp["w"], torch.float32),
+                      dev(inp["x"], torch.bfloat16))
+    r = oracle.route_experts(inp["ids"], inp["w"], E, T)
+    cnt = view.recv_counts.cpu().numpy()
+    cap = view.plane_stride
+    eo = np.full((E, cap, H), 0x7FC0, np.uint16)
+    rng = np.random.default_rng(22)
+    for e in range(E):
+        if cnt[e]:
+            eo[e, :cnt[e]] = parity.f32_to_bits(rng.standard_normal((cnt[e], H)).astype(np.float32))
+    a.combine_payload().copy_(dev(eo, torch.bfloat16))
+    res = dev(inp["res"], torch.bfloat16) if fused else None
+    gam = dev(inp["g"], torch.bfloat16) if fused else None
+    out, sc = a.combine_fp8(None, True, res, gam, 1e-6)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    oc = oracle.combine_experts(r, eo, True, inp["res"] if fused else None,
+                                inp["g"] if fused else None, 1e-6)
+    g_q = out.view(torch.uint8).cpu().numpy().reshape(R * T, H)
+    g_s = sc.cpu().numpy().ravel()
+    if not fused:
+        q_ref, s_ref = oracle.quantize_f32_rows_fp8(oc["acc"])
+        assert np.array_equal(g_q, q_ref)
+        assert np.array_equal(g_s.view(np.uint32), s_ref.view(np.uint32))
+    else:
+        q_ref, s_ref = oracle.quantize_f32_rows_fp8(oc["y"].astype(np.float32))
+        assert (np.abs(g_s.astype(np.float64) - s_ref) <= 1e-5 * s_ref).all()
+        step = lambda c: np.where(c & 0x80, -(c.astype(np.int32) & 0x7F), c.astype(np.int32) & 0x7F)
+        assert (np.abs(step(g_q) - step(q_ref)) <= 1).all()
