@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
         token_of(p.map, p.R, i, s, t);
         const long long tok = (long long)s * p.map.stride + t;
         if (tid < p.dest.P) {
-            const int sl = p.send_slot[tok * p.dest.P + tid];
+            int sl = p.send_slot[tok * p.dest.P + tid];
+            if (sl >= 0 && p.tile_prefix != nullptr)  // tile-local slot + the tile's prefix
+                sl += p.tile_prefix[((long long)s * p.ntiles + t / p.tile) * p.dest.P + tid];
             long long row = -1;
             if (sl >= 0) {
                 row = dest_row(p.dest, p.R, p.m, tid, s, sl);

@@ -239,7 +239,9 @@ cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fuse
 // planes plus a per-row scale (see dispatch_fp8.cu).
 struct DispatchFp8Params {
     const uint16_t *x;        // bf16 [R][T][H]
-    const int32_t *send_slot; // [R][T][RP]
+    const int32_t *send_slot; // [R][T][RP]; tile-local slots when tile_prefix is set
+    const int32_t *tile_prefix;  // [R][ntiles][RP] or null
+    int tile, ntiles;
     uint8_t *recv_x8;         // e4m3 receive rows [rows][H]
     float *recv_scale;        // [rows]
     uint32_t *flags;

@@ -206,8 +206,8 @@ void uniform_map(int R, int T, moe::TokenMap *map) {
 // The row copy of the dispatch phase (after the routing pass queued its
 // send table): bf16 rows, or e4m3 rows + scales in the FP8 receive format.
 //
-// With `tile` > 0 (bf16 rank layout, second routing pass still running) the
-// copy reads the first pass's tile-local slots and adds the tile prefixes.
+// With `tile` > 0 (rank layout, second routing pass still running) the copy
+// reads the first pass's tile-local slots and adds the tile prefixes.
 int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
                 const moe::DestRows &dest, long long ntok, cudaStream_t st, int tile = 0,
                 int ntiles = 0) {
@@ -225,6 +225,13 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
         fp.R = R, fp.RP = h->L.RP, fp.m = m;
         fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
         fp.tokens = ntok;
+        fp.tile_prefix = nullptr;
+        fp.tile = fp.ntiles = 0;
+        if (tile > 0) {
+            fp.send_slot = at<int32_t>(h, h->L.local_slot);
+            fp.tile_prefix = at<int32_t>(h, h->L.tile_prefix);
+            fp.tile = tile, fp.ntiles = ntiles;
+        }
         return moe::launch_dispatch_fp8(fp, h->num_sms, st) == cudaSuccess ? MOE_OK
                                                                             : MOE_ERR_CUDA;
     }
@@ -325,7 +332,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rc_p.R = R, rc_p.K = K, rc_p.E = E, rc_p.Epr = E / R, rc_p.RP = RP;
         rc_p.ntiles = ntiles;
         rc_p.tile = tile;
-        const bool overlap = h->overlap && h->recv_format == MOE_FORMAT_BF16;
+        const bool overlap = h->overlap;
         rc_p.local_slot = overlap ? at<int32_t>(h, h->L.local_slot) : nullptr;
         if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
         h->accum_dirty = true;  // until the scan pass that clears it is queued
