@@ -51,6 +51,10 @@ constexpr int kMaxConsumerWarps = 8;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr size_t kRingBytesTarget = 48 * 1024;
 
+__host__ __device__ constexpr int consumer_warps_max(int vpt) {
+    return vpt == 4 ? 7 : kMaxConsumerWarps;
+}
+
 struct TokenDesc {
     int32_t n;       // message rows of the token
     int32_t pad;
@@ -238,6 +242,18 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
     uint4 *out = reinterpret_cast<uint4 *>(p.out);
     uint4 *rout = reinterpret_cast<uint4 *>(p.residual_out);
 
+    // gamma stays in registers for the whole kernel where the row is short
+    // enough (it is read once per token, on the epilogue's critical path)
+    constexpr bool kGammaRegs = FUSED && VPT == 4;
+    uint4 gv[kGammaRegs ? VPT : 1];
+    if constexpr (kGammaRegs) {
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = tid + v * nct;
+            gv[v] = c < p.H8 ? __ldg(gam + c) : make_uint4(0, 0, 0, 0);
+        }
+    }
+
     uint32_t q = 0, nred = 0;
     bool ok = true;
     // Over the CTA's consumer threads: the sum of `a` and, if TWO, the max of
@@ -357,7 +373,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
                 const int c = tid + v * nct;
                 if (rout != nullptr && c < p.H8) __stcs(rout + row0 + c, pack8(acc[v]));
                 if (OUT8 && c < p.H8) {
-                    const uint4 g = __ldg(gam + c);
+                    const uint4 g = kGammaRegs ? gv[kGammaRegs ? v : 0] : __ldg(gam + c);
                     const uint32_t gu[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -385,7 +401,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
                 for (int v = 0; v < VPT; ++v) {
                     const int c = tid + v * nct;
                     if (c >= p.H8) continue;
-                    const uint4 g = __ldg(gam + c);
+                    const uint4 g = kGammaRegs ? gv[kGammaRegs ? v : 0] : __ldg(gam + c);
                     const uint32_t u[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -429,8 +445,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
 }
 
 template <int VPT, bool WEIGHTED, bool FUSED, bool OUT8>
-__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
-    combine_ring_kernel(const CombineParams p) {
+__device__ __forceinline__ void ring_main(const CombineParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int slots = p.ring_slots;
     const int ncw = (int)(blockDim.x >> 5) - 1;
@@ -456,12 +471,33 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
         consume<VPT, WEIGHTED, FUSED, OUT8>(p, r, slots, ncw);
 }
 
+template <int VPT, bool WEIGHTED, bool FUSED, bool OUT8>
+__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
+    combine_ring_kernel(const CombineParams p) {
+    ring_main<VPT, WEIGHTED, FUSED, OUT8>(p);
+}
+
+// Four vectors per thread (4096 < H <= 7168): at most 7 consumer warps, so
+// that two CTAs of 8 warps per SM leave 128 registers per thread (4 warps
+// per SM sub-partition) and gamma fits in registers beside the accumulators.
+template <bool WEIGHTED, bool FUSED, bool OUT8>
+__global__ void __launch_bounds__((consumer_warps_max(4) + 1) * 32, 2)
+    combine_ring_kernel_v4(const CombineParams p) {
+    ring_main<4, WEIGHTED, FUSED, OUT8>(p);
+}
+
+template <int VPT, bool W, bool F, bool O>
+constexpr void (*ring_kernel())(CombineParams) {
+    if constexpr (VPT == 4) return combine_ring_kernel_v4<W, F, O>;
+    else return combine_ring_kernel<VPT, W, F, O>;
+}
+
 template <int VPT, bool W, bool F, bool O>
 cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStream_t st) {
     long long grid = shape.grid;
     if (grid > p.tokens) grid = p.tokens;
     if (grid < 1) return cudaSuccess;
-    combine_ring_kernel<VPT, W, F, O><<<(unsigned)grid, shape.block, shape.smem, st>>>(p);
+    ring_kernel<VPT, W, F, O>()<<<(unsigned)grid, shape.block, shape.smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -474,12 +510,12 @@ cudaError_t act_t(Act a, const CombineParams *p, const LaunchShape &shape, cudaS
                   int *per_sm) {
     switch (a) {
         case Act::Prepare:
-            return cudaFuncSetAttribute(combine_ring_kernel<VPT, W, F, O>,
+            return cudaFuncSetAttribute(ring_kernel<VPT, W, F, O>(),
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)shape.smem);
         case Act::Occupancy:
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                per_sm, combine_ring_kernel<VPT, W, F, O>, shape.block, shape.smem);
+                per_sm, ring_kernel<VPT, W, F, O>(), shape.block, shape.smem);
         default:
             return launch_t<VPT, W, F, O>(*p, shape, st);
     }
@@ -518,9 +554,9 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, in
                                  LaunchShape *shape, int *vpt, int *slots) {
     const int H8 = H / 8;
     int v = 1;
-    while (v < 8 && (H8 + v - 1) / v > kMaxConsumerWarps * 32) v *= 2;
+    while (v < 8 && (H8 + v - 1) / v > consumer_warps_max(v) * 32) v *= 2;
     const int ncw = ((H8 + v - 1) / v + 31) / 32;
-    if (ncw > kMaxConsumerWarps) return cudaErrorInvalidValue;
+    if (ncw > consumer_warps_max(v)) return cudaErrorInvalidValue;
     int dev = 0, optin = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;

@@ -50,9 +50,11 @@ __device__ __forceinline__ RowScale row_scale(float amax) {
     return r;
 }
 
-// RN32(x / s).
+// RN32(x / s).  SCALED: the pair is prescaled by r.m (rows whose scale is
+// outside [2^-100, 2^100]); otherwise r.m = 1 and r.sd = r.s.
+template <bool SCALED>
 __device__ __forceinline__ float quotient(float x, const RowScale &r) {
-    const float xs = __fmul_rn(x, r.m);
+    const float xs = SCALED ? __fmul_rn(x, r.m) : x;
     float q = __fmul_rn(xs, r.y);
     float e = __fmaf_rn(-q, r.sd, xs);
     q = __fmaf_rn(e, r.y, q);
@@ -67,19 +69,25 @@ __device__ __forceinline__ uint32_t cvt2(float a, float b) {
 }
 
 // Eight values of a row -> eight codes packed in 8 bytes.
+template <bool SCALED>
 __device__ __forceinline__ uint2 quantize8(const float (&v)[8], const RowScale &r) {
     uint32_t c[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        c[i] = cvt2(quotient(v[2 * i], r), quotient(v[2 * i + 1], r));
+        c[i] = cvt2(quotient<SCALED>(v[2 * i], r), quotient<SCALED>(v[2 * i + 1], r));
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 template <int VPT>
 __device__ __forceinline__ void quantize_row(const float (&v)[VPT][8], const RowScale &r,
                                              uint2 (&q)[VPT]) {
+    if (r.m == 1.0f) {  // the row is uniform: one branch for all lanes
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) q[j] = quantize8(v[j], r);
+        for (int j = 0; j < VPT; ++j) q[j] = quantize8<false>(v[j], r);
+    } else {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) q[j] = quantize8<true>(v[j], r);
+    }
 }
 
 }  // namespace fp8
