@@ -12,18 +12,21 @@
 //   recv_counts[d][s], src_token[d][s][slot], masked metadata rows,
 //   local_expert_counts[e] = #valid (s,t,k) entries with e_k = e.
 //
-// Two passes over tiles of `tile` tokens (32..256, one token per thread) of
-// one source rank, grid = tiles x R; the tile is chosen so the grid covers
-// about two CTAs per SM:
+// Two passes over tiles of `tile` tokens (256 by default, 32..256, one token
+// per thread) of one source rank, grid = tiles x R:
 //   pass 1 (route_count): per-tile destination counts (warp ballots), the
 //          expert histogram added into the source rank's accumulator (so
 //          that only that source's tiles contend for an address), the
-//          bad-id flag.  The last tile of a source to finish (atomic ticket after
+//          bad-id flag, and (when asked) each token's slots inside its
+//          tile, which with the tile prefixes is all the row copy needs.
+//          The last tile of a source to finish (atomic ticket after
 //          a fence; nothing waits) scans that source's tile counts into
-//          exclusive per-tile prefixes and writes its recv counts.
+//          exclusive per-tile prefixes and writes its recv counts (a source
+//          of one tile writes its zero prefix and counts without the ticket).
 //   pass 2 (route_scan):  loads its tokens' ids and weights and rebuilds
-//          their destination masks while pass 1 still runs (programmatic
-//          dependent launch), then adds its tile prefix to a warp-ballot /
+//          their destination masks (while pass 1 still runs when chained
+//          to it by programmatic dependent launch; beside the row copy, on
+//          a second stream, otherwise), then adds its tile prefix to a warp-ballot /
 //          cross-warp scan inside the tile to get each token's slot on
 //          every destination; writes all routing outputs (send rows as
 //          16-byte vectors); copies its share of the histogram accumulator
@@ -137,6 +140,16 @@ __global__ void __launch_bounds__(kRouteTile) route_count_kernel(const RouteCoun
     for (int e = threadIdx.x; e < p.E; e += p.tile)
         if (hist[e] != 0) atomicAdd(&acc[e], hist[e]);
 
+    if (p.ntiles == 1) {  // the source's only tile: its prefix is zero
+        if (threadIdx.x < p.RP) p.tile_prefix[(size_t)s * p.RP + threadIdx.x] = 0;
+        if (threadIdx.x < p.R) {
+            int sum = 0;
+            for (int w = 0; w < nwarps; ++w) sum += warp_cnt[w][threadIdx.x];
+            p.recv_counts[threadIdx.x * p.R + s] = sum;
+        }
+        return;
+    }
+
     // The last tile of this source to get here turns the tile counts into
     // exclusive prefixes.  Classic fence-then-ticket: no thread waits.
     __shared__ int last;
@@ -228,7 +241,14 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
         const int ncta = p.R * p.ntiles, cta = s * p.ntiles + tile;
         for (int e = cta + (int)threadIdx.x * ncta; e < p.E; e += p.tile * ncta) {
             int sum = 0;
-            for (int r = 0; r < p.R; ++r) sum += p.hist_accum[(size_t)r * p.E + e];
+            for (int r0 = 0; r0 < p.R; r0 += 8) {  // 8 loads in flight at a time
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    v[u] = r0 + u < p.R ? __ldcg(p.hist_accum + (size_t)(r0 + u) * p.E + e) : 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) sum += v[u];
+            }
             for (int r = 0; r < p.R; ++r) p.hist_accum[(size_t)r * p.E + e] = 0;
             p.local_counts[e] = sum;
         }
