@@ -13,7 +13,11 @@
 // memory stages with 1-D bulk asynchronous copies: a bulk load brings the
 // row chunk and the token's send-slot row into a stage (completion counted
 // on the stage's mbarrier), then one bulk store per destination writes the
-// chunk out of shared memory.  Stages are refilled one iteration after
+// chunk out of shared memory.  Launched straight after the first routing
+// pass (rank layout), the send-slot row holds the token's slots inside its
+// routing tile and a third bulk load brings the tile's exclusive prefix
+// row; their sum is the slot, so the copy does not wait for the second
+// pass, which runs beside it.  Stages are refilled one iteration after
 // their stores were issued, so S-1 loads stay in flight per CTA while the
 // stores drain.  The copy engine moves every byte; the thread only issues.
 // Waits are bounded: if one runs out the kernel raises the timeout flag,

@@ -47,10 +47,15 @@
  * expert" and is skipped silently.
  *
  * Streams: `stream` arguments are cudaStream_t values passed as void*
- * (NULL = the legacy default stream).  All work of a call is queued on that
- * stream; calls return without synchronising, except moe_a2a_get_error.
- * A handle is bound to the CUDA device that is current at its first
- * dispatch.
+ * (NULL = the legacy default stream).  All work of a call is ordered on
+ * that stream: moe_dispatch in the rank layout runs the second half of its
+ * routing pass on a stream the handle creates at its first dispatch,
+ * forked from `stream` by an event after the first half and joined back
+ * into `stream` by another event before the call returns, so later work on
+ * `stream` sees every output, and capturing `stream` into a CUDA graph
+ * captures both branches.  Calls return without synchronising, except
+ * moe_a2a_get_error.  A handle is bound to the CUDA device that is current
+ * at its first dispatch; moe_a2a_destroy releases its stream and events.
  */
 #ifndef MOE_A2A_H
 #define MOE_A2A_H

@@ -119,6 +119,15 @@ def test_fp8_dispatch_codes_and_scales_bit_exact(R, T, H, E, K):
     run_dispatch_fp8(R, T, H, E, K, seed=R + K)
 
 
+@pytest.mark.parametrize("overlap", ["0", "1"])
+def test_fp8_dispatch_route_overlap_modes(monkeypatch, overlap):
+    # 700 tokens per source: three 256-token routing tiles and a ragged tail;
+    # the row copy either adds tile prefixes to tile-local slots beside the
+    # second routing pass ("1", the default) or reads the finished send table
+    monkeypatch.setenv("MOE_ROUTE_OVERLAP", overlap)
+    run_dispatch_fp8(5, 700, 144, 40, 6, seed=21, m=720)
+
+
 def test_fp8_dispatch_prefill_shape():
     run_dispatch_fp8(8, 4096, 7168, 256, 8, seed=0, routing="zipf")
 

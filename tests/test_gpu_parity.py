@@ -46,6 +46,19 @@ def test_variants_small(weighted, fused):
     parity.Case(w).run(seed=3)
 
 
+@pytest.mark.parametrize("overlap", ["0", "1"])
+def test_route_overlap_modes(monkeypatch, overlap):
+    # Three 256-token routing tiles per source plus a ragged tail.  "1" (the
+    # default): the row copy starts after the first routing pass and adds
+    # each tile's prefix to the token's tile-local slots while the second
+    # pass runs on the handle's own stream; "0": the passes run in stream
+    # order in front of the copy.  Both must equal the oracle.
+    monkeypatch.setenv("MOE_ROUTE_OVERLAP", overlap)
+    w = small("decode", ep_size=6, tokens_per_rank=700, max_tokens=720, runtime_max=710,
+              hidden=136, num_experts=48, top_k=5, weighted=True, fused=True)
+    parity.Case(w).run(seed=11)
+
+
 @pytest.mark.parametrize("K", [1, 2, 4, 8, 3])
 def test_top_k_variants(K):
     w = small("decode", ep_size=4, tokens_per_rank=77, max_tokens=80, runtime_max=80,
