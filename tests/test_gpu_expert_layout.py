@@ -160,6 +160,14 @@ def test_expert_layout_runtime_max_above_tokens():
     run(4, 40, 128, 32, 4, 6, True, True, m=56)
 
 
+def test_expert_layout_limits():
+    # the layout's largest expert count (1024, lane masks in shared memory),
+    # 32 ranks and top-32 (32 send-table entries per token), long rows
+    run(8, 70, 64, 1024, 8, 41, True, True)
+    run(32, 12, 64, 64, 32, 42, True, True)
+    run(2, 10, 16384, 4, 2, 43, True, True)
+
+
 def test_expert_layout_varlen_and_dead_rank():
     run(8, 96, 256, 64, 8, 7, True, True, counts=[96, 0, 5, 95, 1, 64, 33, 96], dead=0b100100)
 

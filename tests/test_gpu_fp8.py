@@ -128,6 +128,12 @@ def test_fp8_dispatch_route_overlap_modes(monkeypatch, overlap):
     run_dispatch_fp8(5, 700, 144, 40, 6, seed=21, m=720)
 
 
+def test_fp8_dispatch_limits():
+    # 16384-wide rows (the longest) and 32 ranks with top-32
+    run_dispatch_fp8(2, 20, 16384, 4, 2, seed=31)
+    run_dispatch_fp8(32, 12, 64, 64, 32, seed=32)
+
+
 def test_fp8_dispatch_prefill_shape():
     run_dispatch_fp8(8, 4096, 7168, 256, 8, seed=0, routing="zipf")
 

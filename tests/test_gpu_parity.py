@@ -66,6 +66,36 @@ def test_top_k_variants(K):
     parity.Case(w).run(seed=K)
 
 
+# The handle's limits (MOE_MAX_EP_SIZE 32, MOE_MAX_TOP_K 32, MOE_MAX_HIDDEN
+# 16384, MOE_MAX_EXPERTS 8192) and the row lengths where the combine's
+# vectors per thread change (4096 -> 4104, 7168 -> 7176).
+@pytest.mark.parametrize("fused", [False, True])
+def test_limit_32_ranks_top_32(fused):
+    w = small("decode", ep_size=32, tokens_per_rank=40, max_tokens=48, runtime_max=44,
+              hidden=64, num_experts=256, top_k=32, weighted=True, fused=fused)
+    parity.Case(w).run(seed=5)
+
+
+@pytest.mark.parametrize("weighted,fused", [(False, False), (True, True)])
+def test_limit_hidden_16384(weighted, fused):
+    w = small("decode", ep_size=2, tokens_per_rank=20, max_tokens=24, runtime_max=20,
+              hidden=16384, num_experts=4, top_k=2, weighted=weighted, fused=fused)
+    parity.Case(w).run(seed=6)
+
+
+def test_limit_8192_experts():
+    w = small("decode", ep_size=8, tokens_per_rank=300, max_tokens=300, runtime_max=300,
+              hidden=64, num_experts=8192, top_k=8)
+    parity.Case(w).run(seed=7)
+
+
+@pytest.mark.parametrize("H", [4096, 4104, 7168, 7176, 8192])
+def test_hidden_at_vector_boundaries(H):
+    w = small("decode", ep_size=4, tokens_per_rank=33, max_tokens=40, runtime_max=36,
+              hidden=H, num_experts=16, top_k=4)
+    parity.Case(w).run(seed=H % 97)
+
+
 def test_decode():
     rep = parity.Case(synth.WORKLOADS["decode"]).run()
     assert rep["tokens_checked"] == 512
