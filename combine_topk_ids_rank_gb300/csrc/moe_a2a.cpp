@@ -171,9 +171,14 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
         return MOE_ERR_CUDA;
     const char *ov = std::getenv("MOE_ROUTE_OVERLAP");
     h->overlap = h->L.layout == MOE_LAYOUT_RANK && !(ov != nullptr && ov[0] == '0');
-    if (h->overlap && h->side == nullptr) {
-        if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h->ev_count, cudaEventDisableTiming) != cudaSuccess ||
+    if (h->overlap) {  // each object once, also after a partial failure
+        if (h->side == nullptr &&
+            cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (h->ev_count == nullptr &&
+            cudaEventCreateWithFlags(&h->ev_count, cudaEventDisableTiming) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (h->ev_scan == nullptr &&
             cudaEventCreateWithFlags(&h->ev_scan, cudaEventDisableTiming) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
