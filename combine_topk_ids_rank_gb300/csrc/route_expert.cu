@@ -25,7 +25,8 @@
 //   pass 2 (route_e_scan): rebuilds the masks while pass 1 still runs
 //          (programmatic dependent launch), sums the counts of every
 //          earlier (source, tile) per expert -- O(tiles * E) reads per CTA,
-//          meant for the decode-sized batches of this layout -- and gives
+//          split over the CTA's threads in interleaved partial sums when
+//          there are fewer experts than threads -- and gives
 //          each (token, expert) its row: that base + the popcounts of the
 //          earlier warps' masks + the popcount of its own warp's mask
 //          below its lane.  The last CTA writes recv_counts.
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
     constexpr int KA = KT > 0 ? KT : kMaxTopK;
     __shared__ uint32_t masks[kWarps][kMaxExpertsExpertLayout];
     __shared__ int32_t base[kMaxExpertsExpertLayout];
+    __shared__ int32_t part_sum[kTile > kMaxExpertsExpertLayout ? kTile : kMaxExpertsExpertLayout];
     const int tile = blockIdx.x, s = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = tile * kTile + threadIdx.x;
@@ -137,11 +139,22 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
     ptx::grid_dependency_wait();  // tile counts of the count pass
 
     // Rows of this expert that come before this tile: all tiles of earlier
-    // sources and the earlier tiles of this source.
-    const long long before = (long long)s * p.ntiles + tile;
+    // sources and the earlier tiles of this source.  With few experts the
+    // threads split each expert's (source, tile) range into `parts`
+    // interleaved partial sums, so no thread walks a long chain of loads.
+    const int before = s * p.ntiles + tile;
+    const int parts = p.E >= kTile ? 1 : kTile / p.E;
+    for (int x = threadIdx.x; x < p.E * parts; x += kTile) {
+        const int e = x % p.E, part = x / p.E;
+        int b = 0;
+#pragma unroll 4
+        for (int i = part; i < before; i += parts) b += p.tile_counts[(size_t)i * p.E + e];
+        part_sum[x] = b;
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += kTile) {
         int b = 0;
-        for (long long i = 0; i < before; ++i) b += p.tile_counts[i * p.E + e];
+        for (int part = 0; part < parts; ++part) b += part_sum[part * p.E + e];
         base[e] = b;
     }
     __syncthreads();
