@@ -226,13 +226,22 @@ int route_expert_tile() { return kTile; }
 cudaError_t launch_route_expert(const RouteExpertParams &p, cudaStream_t st) {
     if (p.E > kMaxExpertsExpertLayout || p.K > kMaxTopK || p.KP < p.K || p.ntiles < 1)
         return cudaErrorInvalidValue;
+    // Common top-k values get their own instantiation: the per-slot loops
+    // (duplicate checks, weight sums) are unrolled over KT slots, where the
+    // generic one runs them over kMaxTopK.
     cudaError_t e;
     switch (p.K) {
+        case 1: e = launch2d(route_e_count_kernel<1>, p, st, false); break;
+        case 2: e = launch2d(route_e_count_kernel<2>, p, st, false); break;
+        case 4: e = launch2d(route_e_count_kernel<4>, p, st, false); break;
         case 8: e = launch2d(route_e_count_kernel<8>, p, st, false); break;
         default: e = launch2d(route_e_count_kernel<0>, p, st, false); break;
     }
     if (e != cudaSuccess) return e;
     switch (p.K) {
+        case 1: return launch2d(route_e_scan_kernel<1>, p, st, true);
+        case 2: return launch2d(route_e_scan_kernel<2>, p, st, true);
+        case 4: return launch2d(route_e_scan_kernel<4>, p, st, true);
         case 8: return launch2d(route_e_scan_kernel<8>, p, st, true);
         default: return launch2d(route_e_scan_kernel<0>, p, st, true);
     }

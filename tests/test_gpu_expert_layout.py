@@ -145,6 +145,13 @@ def test_expert_layout_variants_ragged(weighted, fused):
     run(6, 100, 136, 48, 5, 3, weighted, fused, dup=True)
 
 
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 8])
+def test_expert_layout_top_k_instantiations(K):
+    # top-k values with their own routing instantiation (1, 2, 4, 8) and a
+    # generic one (3); repeats and -1 ids; three tiles on one source
+    run(3, 530, 64, 24, K, 50 + K, True, True, dup=True)
+
+
 def test_expert_layout_decode_shape():
     a, view, r = run(8, 64, 7168, 256, 8, 0, True, True)
     # every token has 8 distinct experts: 8 rows per token
