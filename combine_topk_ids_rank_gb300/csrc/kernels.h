@@ -89,6 +89,7 @@ struct RouteScanParams {
     TokenMap map;
     uint32_t active;
     int R, K, E, Epr, RP, m, ntiles, tile;
+    int dg;                    // destinations per CTA (1 or 4): grid z = RP / dg
 };
 
 // Expert-major layout routing (route_expert.cu).

@@ -359,6 +359,10 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rs.R = R, rs.K = K, rs.E = E, rs.Epr = E / R, rs.RP = RP, rs.m = m;
         rs.ntiles = ntiles;
         rs.tile = tile;
+        // Destinations per CTA of the second pass: 4 (16-byte send-row
+        // stores) once the grid has a CTA per SM, else 1 so that a small
+        // batch's per-destination work spreads over RP times the CTAs.
+        rs.dg = R * ntiles * (RP / 4) >= h->num_sms ? 4 : 1;
         if (overlap) {
             // The row copy needs only the first pass; the second (send
             // table, weights, metadata rows) runs beside it on `side`.

@@ -170,6 +170,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     s.active = all;
     s.R = R, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
     s.tile = moe::kRouteTile;
+    s.dg = 4;
     if (moe::launch_route_scan(s, st, true) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

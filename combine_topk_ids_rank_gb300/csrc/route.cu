@@ -29,7 +29,9 @@
 //          a second stream, otherwise), then adds its tile prefix to a warp-ballot /
 //          cross-warp scan inside the tile to get each token's slot on
 //          every destination; writes all routing outputs (send rows as
-//          16-byte vectors); copies its share of the histogram accumulator
+//          16-byte vectors); grid z splits the destinations into groups of
+//          dg (4, or 1 so that small batches still spread over many CTAs);
+//          copies its share of the histogram accumulator
 //          to local_expert_counts and sets it back to zero for the next call.
 // Both passes are O(T) in work and O(1) in cross-tile reads per CTA.
 #include "kernels.h"
@@ -193,11 +195,13 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
     __shared__ int32_t prefix[32];
     __shared__ int32_t warp_cnt[kMaxWarps][32];
     __shared__ int32_t warp_off[kMaxWarps][32];
-    const int tile = blockIdx.x, s = blockIdx.y;
+    const int tile = blockIdx.x, s = blockIdx.y, group = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = p.tile >> 5;
     const int t = tile * p.tile + threadIdx.x;
     const int K = KT > 0 ? KT : p.K;
     const bool active = t < p.map.count[s];
+    // This CTA's destinations: [d_lo, d_lo + dg)
+    const int d_lo = group * p.dg;
 
     ptx::launch_dependents();
 
@@ -238,7 +242,8 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
     // This CTA owns the experts e == cta (mod ncta) of the histogram: sum
     // the per-source accumulators and leave them at zero for the next call.
     {
-        const int ncta = p.R * p.ntiles, cta = s * p.ntiles + tile;
+        const int ncta = p.R * p.ntiles * (int)gridDim.z;
+        const int cta = (s * p.ntiles + tile) * (int)gridDim.z + group;
         for (int e = cta + (int)threadIdx.x * ncta; e < p.E; e += p.tile * ncta) {
             int sum = 0;
             for (int r0 = 0; r0 < p.R; r0 += 8) {  // 8 loads in flight at a time
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
 
     // the rank whose message each top-k slot carries (first slot of a rank;
     // later slots of the same rank and invalid ids carry none)
-    if (p.topk_dest != nullptr && active) {
+    if (p.topk_dest != nullptr && active && group == 0) {
         int8_t *dst = p.topk_dest + tok * K;
         uint32_t seen = 0;
         for (int k = 0; k < K; ++k) {
@@ -285,7 +290,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
     int32_t *srow = p.send_slot + tok * p.RP;
     float *wrow = p.dest_weight + tok * p.RP;
 
-    for (int d0 = 0; d0 < p.RP; d0 += 4) {
+    for (int d0 = d_lo; d0 < d_lo + p.dg; d0 += 4) {
         int4 sv;
         float4 wv;
         int32_t *se = &sv.x;
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int d = d0 + q;
+            if (q >= p.dg) break;  // fewer than 4 destinations per CTA
             const bool has = d < p.R && ((mask >> d) & 1u);
             const uint32_t b = __ballot_sync(kFull, has);
             int32_t slot = -1;
@@ -343,17 +349,23 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
             we[q] = wsum;
         }
         if (active) {
-            *reinterpret_cast<int4 *>(srow + d0) = sv;
-            *reinterpret_cast<float4 *>(wrow + d0) = wv;
+            if (p.dg == 4) {
+                *reinterpret_cast<int4 *>(srow + d0) = sv;
+                *reinterpret_cast<float4 *>(wrow + d0) = wv;
+            } else {
+                srow[d0] = sv.x;
+                wrow[d0] = wv.x;
+            }
         }
     }
 }
 
 template <typename Kern, typename P>
-cudaError_t launch2d(Kern kern, const P &p, size_t smem, cudaStream_t st, bool pdl) {
+cudaError_t launch2d(Kern kern, const P &p, size_t smem, cudaStream_t st, bool pdl,
+                     unsigned gz = 1) {
     if (p.tile < 32 || p.tile > kRouteTile || p.tile % 32 != 0) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.ntiles, p.R, 1);
+    cfg.gridDim = dim3(p.ntiles, p.R, gz);
     cfg.blockDim = dim3(p.tile, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -378,11 +390,13 @@ cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pdl) {
+    if ((p.dg != 1 && p.dg != 4) || p.RP % p.dg != 0) return cudaErrorInvalidValue;
+    const unsigned gz = (unsigned)(p.RP / p.dg);
     switch (p.K) {
-        case 2: return launch2d(route_scan_kernel<2>, p, 0, st, pdl);
-        case 4: return launch2d(route_scan_kernel<4>, p, 0, st, pdl);
-        case 8: return launch2d(route_scan_kernel<8>, p, 0, st, pdl);
-        default: return launch2d(route_scan_kernel<0>, p, 0, st, pdl);
+        case 2: return launch2d(route_scan_kernel<2>, p, 0, st, pdl, gz);
+        case 4: return launch2d(route_scan_kernel<4>, p, 0, st, pdl, gz);
+        case 8: return launch2d(route_scan_kernel<8>, p, 0, st, pdl, gz);
+        default: return launch2d(route_scan_kernel<0>, p, 0, st, pdl, gz);
     }
 }
 
