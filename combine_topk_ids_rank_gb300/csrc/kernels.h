@@ -109,6 +109,7 @@ struct RouteExpertParams {
     TokenMap map;
     uint32_t active;
     int R, K, E, Epr, KP, cap, ntiles;
+    int kg;                   // top-k slots per CTA of the second pass: grid z = KP / kg
 };
 int route_expert_tile();
 cudaError_t launch_route_expert(const RouteExpertParams &p, cudaStream_t st);

@@ -309,6 +309,9 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rp.active = h->active;
         rp.R = R, rp.K = K, rp.E = E, rp.Epr = E / R, rp.KP = h->L.P, rp.cap = dest.cap;
         rp.ntiles = (tmax + moe::route_expert_tile() - 1) / moe::route_expert_tile();
+        // Top-k slots per CTA of the second pass: all, or one each while the
+        // (tile, source) grid would cover fewer than half the SMs.
+        rp.kg = R * rp.ntiles * 2 >= h->num_sms ? rp.KP : 1;
         if (moe::launch_route_expert(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
         rc = launch_rows(h, d_x, map, m, dest, ntok, st);
         if (rc != MOE_OK) return rc;

@@ -29,7 +29,10 @@
 //          there are fewer experts than threads -- and gives
 //          each (token, expert) its row: that base + the popcounts of the
 //          earlier warps' masks + the popcount of its own warp's mask
-//          below its lane.  The last CTA writes recv_counts.
+//          below its lane.  Grid z splits the top-k slots into groups of
+//          kg (all KP, or one slot per CTA when the batch is small); every
+//          CTA rebuilds the masks and bases it needs.  The last CTA writes
+//          recv_counts.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
     const int t = tile * kTile + threadIdx.x;
     const int K = KT > 0 ? KT : p.K;
     const bool has_token = t < p.map.count[s];
+    const int k_lo = (int)blockIdx.z * p.kg, k_hi = k_lo + p.kg;  // this CTA's slots
     ptx::launch_dependents();  // the row copy may start loading its inputs
 
     // Inputs of the call: loaded and marked before the count pass finishes.
@@ -166,6 +170,7 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
         const uint32_t lt = lanemask_lt();
 #pragma unroll
         for (int k = 0; k < KA; ++k) {
+            if (k < k_lo || k >= k_hi) continue;
             const int e = ids[k];
             bool first = e >= 0;
 #pragma unroll
@@ -188,13 +193,13 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
                 wrow[k] = sum;
             }
         }
-        for (int k = K; k < p.KP; ++k) {
+        for (int k = max(K, k_lo); k < min(p.KP, k_hi); ++k) {
             srow[k] = -1;
             wrow[k] = 0.0f;
         }
     }
 
-    if (s == p.R - 1 && tile == p.ntiles - 1) {
+    if (s == p.R - 1 && tile == p.ntiles - 1 && blockIdx.z == 0) {
         for (int e = threadIdx.x; e < p.E; e += kTile) {
             int c = base[e];
 #pragma unroll
@@ -205,9 +210,10 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
 }
 
 template <typename Kern>
-cudaError_t launch2d(Kern kern, const RouteExpertParams &p, cudaStream_t st, bool pdl) {
+cudaError_t launch2d(Kern kern, const RouteExpertParams &p, cudaStream_t st, bool pdl,
+                     unsigned gz = 1) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.ntiles, p.R, 1);
+    cfg.gridDim = dim3(p.ntiles, p.R, gz);
     cfg.blockDim = dim3(kTile, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -238,12 +244,14 @@ cudaError_t launch_route_expert(const RouteExpertParams &p, cudaStream_t st) {
         default: e = launch2d(route_e_count_kernel<0>, p, st, false); break;
     }
     if (e != cudaSuccess) return e;
+    if (p.kg < 1 || p.KP % p.kg != 0) return cudaErrorInvalidValue;
+    const unsigned gz = (unsigned)(p.KP / p.kg);
     switch (p.K) {
-        case 1: return launch2d(route_e_scan_kernel<1>, p, st, true);
-        case 2: return launch2d(route_e_scan_kernel<2>, p, st, true);
-        case 4: return launch2d(route_e_scan_kernel<4>, p, st, true);
-        case 8: return launch2d(route_e_scan_kernel<8>, p, st, true);
-        default: return launch2d(route_e_scan_kernel<0>, p, st, true);
+        case 1: return launch2d(route_e_scan_kernel<1>, p, st, true, gz);
+        case 2: return launch2d(route_e_scan_kernel<2>, p, st, true, gz);
+        case 4: return launch2d(route_e_scan_kernel<4>, p, st, true, gz);
+        case 8: return launch2d(route_e_scan_kernel<8>, p, st, true, gz);
+        default: return launch2d(route_e_scan_kernel<0>, p, st, true, gz);
     }
 }
 
