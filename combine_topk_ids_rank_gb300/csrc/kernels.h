@@ -104,7 +104,8 @@ struct RouteExpertParams {
     int32_t *src_token;       // [E][cap]: s * stride + t
     float *recv_w;            // [E][cap]
     int32_t *recv_counts;     // [E]
-    int32_t *local_counts;    // [E], zeroed before the call
+    int32_t *hist_accum;      // [E], zero between calls: pass 1 adds, pass 2 moves it out
+    int32_t *local_counts;    // [E], written by pass 2
     uint32_t *flags;
     TokenMap map;
     uint32_t active;

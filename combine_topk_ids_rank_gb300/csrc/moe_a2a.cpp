@@ -83,7 +83,7 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
         L->tile_counts = take(R * NT * E * 4);
         L->tile_prefix = take(0);
         L->tile_ticket = take(0);
-        L->hist_accum = take(0);
+        L->hist_accum = take(E * 4);  // zero between calls
         L->local_slot = take(0);
         L->flags = take(kAlign);
         L->total = off;
@@ -182,7 +182,7 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
             cudaEventCreateWithFlags(&h->ev_scan, cudaEventDisableTiming) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    h->accum_dirty = h->L.layout == MOE_LAYOUT_RANK;
+    h->accum_dirty = true;  // routing accumulators: zero them before the first pass
     h->ready = true;
     return MOE_OK;
 }
@@ -291,9 +291,12 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
                 cudaSuccess)
             return MOE_ERR_CUDA;
     } else if (expert) {
-        if (cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (h->accum_dirty) {  // the histogram accumulator
+            if (cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * E, st) !=
+                cudaSuccess)
+                return MOE_ERR_CUDA;
+            h->accum_dirty = false;
+        }
         moe::RouteExpertParams rp;
         rp.topk_ids = d_topk_ids;
         rp.topk_w = d_topk_w;
@@ -303,6 +306,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rp.src_token = at<int32_t>(h, h->L.src_token);
         rp.recv_w = at<float>(h, h->L.recv_w);
         rp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+        rp.hist_accum = at<int32_t>(h, h->L.hist_accum);
         rp.local_counts = at<int32_t>(h, h->L.local_counts);
         rp.flags = flags;
         rp.map = map;
@@ -312,7 +316,9 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         // Top-k slots per CTA of the second pass: all, or one each while the
         // (tile, source) grid would cover fewer than half the SMs.
         rp.kg = R * rp.ntiles * 2 >= h->num_sms ? rp.KP : 1;
+        h->accum_dirty = true;  // until the pass that clears the accumulator is queued
         if (moe::launch_route_expert(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+        h->accum_dirty = false;
         rc = launch_rows(h, d_x, map, m, dest, ntok, st);
         if (rc != MOE_OK) return rc;
     } else {

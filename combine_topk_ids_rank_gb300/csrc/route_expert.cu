@@ -20,8 +20,9 @@
 //   pass 1 (route_e_count): each warp marks, per expert, the lanes whose
 //          token carries it (shared-memory lane masks, atomicOr), then the
 //          tile's rows per expert are the popcounts, written to
-//          tile_counts[s][tile][e]; local_expert_counts (duplicates
-//          included) and the bad-id flag as in the rank layout.
+//          tile_counts[s][tile][e]; the expert histogram (duplicates
+//          included) into an accumulator that pass 2 moves to
+//          local_expert_counts and clears; the bad-id flag.
 //   pass 2 (route_e_scan): rebuilds the masks while pass 1 still runs
 //          (programmatic dependent launch), sums the counts of every
 //          earlier (source, tile) per expert -- O(tiles * E) reads per CTA,
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kTile) route_e_count_kernel(const RouteExpertP
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) c += __popc(masks[w][e]);
         counts[e] = c;
-        if (hist[e] != 0) atomicAdd(&p.local_counts[e], hist[e]);
+        if (hist[e] != 0) atomicAdd(&p.hist_accum[e], hist[e]);
     }
 }
 
@@ -140,7 +141,17 @@ __global__ void __launch_bounds__(kTile) route_e_scan_kernel(const RouteExpertPa
             if (ids[k] >= 0) atomicOr(&masks[warp][ids[k]], 1u << lane);
         }
     }
-    ptx::grid_dependency_wait();  // tile counts of the count pass
+    ptx::grid_dependency_wait();  // tile counts and histogram of the count pass
+
+    // This CTA's share of the experts: move the histogram out, leave zero.
+    {
+        const int ncta = p.R * p.ntiles * (int)gridDim.z;
+        const int cta = (s * p.ntiles + tile) * (int)gridDim.z + (int)blockIdx.z;
+        for (int e = cta + (int)threadIdx.x * ncta; e < p.E; e += kTile * ncta) {
+            p.local_counts[e] = __ldcg(p.hist_accum + e);
+            p.hist_accum[e] = 0;
+        }
+    }
 
     // Rows of this expert that come before this tile: all tiles of earlier
     // sources and the earlier tiles of this source.  With few experts the
