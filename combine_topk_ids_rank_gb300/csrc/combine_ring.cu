@@ -33,6 +33,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "fp8.cuh"
+#include "f32x2.cuh"
 
 #include "moe_a2a.h"
 
@@ -115,18 +116,32 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
                       pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
 }
 
-template <bool WEIGHTED>
+// a[j] += w * v[j] (or v[j]), each product and sum rounded to binary32 (no
+// FMA).  PACKED: the sums two lanes per instruction (identical results);
+// used by the FP8-output combine at 4 or more vectors per thread.
+// The products stay scalar: a paired multiply feeding a paired add was
+// measured to come out fused (one rounding), which the sum must not be.
+template <bool WEIGHTED, bool PACKED>
 __device__ __forceinline__ void accumulate8(float (&a)[8], const uint4 v, const float w) {
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (PACKED) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = lo_f(u[i]), hi = hi_f(u[i]);
-        if (WEIGHTED) {
-            a[2 * i] = __fadd_rn(a[2 * i], __fmul_rn(w, lo));
-            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __fmul_rn(w, hi));
-        } else {
-            a[2 * i] = __fadd_rn(a[2 * i], lo);
-            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], hi);
+        for (int i = 0; i < 4; ++i) {
+            const x2::f2 x = WEIGHTED ? x2::pack(__fmul_rn(w, lo_f(u[i])), __fmul_rn(w, hi_f(u[i])))
+                                      : x2::bf16x2(u[i]);
+            x2::unpack(x2::add(x2::pack(a[2 * i], a[2 * i + 1]), x), a[2 * i], a[2 * i + 1]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = lo_f(u[i]), hi = hi_f(u[i]);
+            if (WEIGHTED) {
+                a[2 * i] = __fadd_rn(a[2 * i], __fmul_rn(w, lo));
+                a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __fmul_rn(w, hi));
+            } else {
+                a[2 * i] = __fadd_rn(a[2 * i], lo);
+                a[2 * i + 1] = __fadd_rn(a[2 * i + 1], hi);
+            }
         }
     }
 }
@@ -245,6 +260,10 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
     // gamma stays in registers for the whole kernel where the row is short
     // enough (it is read once per token, on the epilogue's critical path)
     constexpr bool kGammaRegs = FUSED && VPT == 4;
+    // Paired fp32 arithmetic where the FP8 output's extra per-element work
+    // makes the kernel issue-bound (measured: FP8-output combine 432.7 ->
+    // 413.4 us at prefill; no gain for the bf16 output, which stays scalar).
+    constexpr bool kPacked = OUT8 && VPT >= 4;
     uint4 gv[kGammaRegs ? VPT : 1];
     if constexpr (kGammaRegs) {
 #pragma unroll
@@ -332,7 +351,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 const int c = tid + v * nct;
-                if (c < p.H8) accumulate8<WEIGHTED>(acc[v], row[c], wi);
+                if (c < p.H8) accumulate8<WEIGHTED, kPacked>(acc[v], row[c], wi);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&r.empty[b]);
@@ -362,12 +381,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
             float ss = 0.0f, gmax = 0.0f;
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
-                const uint32_t u[4] = {rv[v].x, rv[v].y, rv[v].z, rv[v].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[v][2 * i] = __fadd_rn(acc[v][2 * i], lo_f(u[i]));
-                    acc[v][2 * i + 1] = __fadd_rn(acc[v][2 * i + 1], hi_f(u[i]));
-                }
+                accumulate8<false, kPacked>(acc[v], rv[v], 1.0f);  // + residual
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ss += acc[v][e] * acc[v][e];
                 const int c = tid + v * nct;
@@ -377,8 +391,14 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
                     const uint32_t gu[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        acc[v][2 * i] = __fmul_rn(acc[v][2 * i], lo_f(gu[i]));
-                        acc[v][2 * i + 1] = __fmul_rn(acc[v][2 * i + 1], hi_f(gu[i]));
+                        if constexpr (kPacked) {
+                            x2::unpack(x2::mul(x2::pack(acc[v][2 * i], acc[v][2 * i + 1]),
+                                               x2::bf16x2(gu[i])),
+                                       acc[v][2 * i], acc[v][2 * i + 1]);
+                        } else {
+                            acc[v][2 * i] = __fmul_rn(acc[v][2 * i], lo_f(gu[i]));
+                            acc[v][2 * i + 1] = __fmul_rn(acc[v][2 * i + 1], hi_f(gu[i]));
+                        }
                     }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) gmax = fmaxf(gmax, fabsf(acc[v][e]));
@@ -391,10 +411,13 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
             }
             const float inv = rsqrtf(total / (float)p.H + p.eps);
             if (OUT8) {
+                const x2::f2 inv2 = x2::pack(inv, inv);
 #pragma unroll
                 for (int v = 0; v < VPT; ++v)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[v][e] = __fmul_rn(inv, acc[v][e]);
+                    for (int e = 0; e < 8; e += 2)
+                        x2::unpack(x2::mul(inv2, x2::pack(acc[v][e], acc[v][e + 1])), acc[v][e],
+                                   acc[v][e + 1]);
                 amax = __fmul_rn(inv, gtot);
             } else {
 #pragma unroll

@@ -29,6 +29,8 @@
 
 #include <cstdint>
 
+#include "f32x2.cuh"
+
 namespace moe {
 namespace fp8 {
 
@@ -50,17 +52,25 @@ __device__ __forceinline__ RowScale row_scale(float amax) {
     return r;
 }
 
-// RN32(x / s).  SCALED: the pair is prescaled by r.m (rows whose scale is
-// outside [2^-100, 2^100]); otherwise r.m = 1 and r.sd = r.s.
+// RN32(a / s) and RN32(b / s), two elements per instruction (paired fp32,
+// each lane rounded as the scalar operation would be; x' - q*s' is formed as
+// fma(q, -s', x'), the same exact product).  SCALED: the pair is prescaled
+// by r.m (rows whose scale is outside [2^-100, 2^100]); otherwise r.m = 1
+// and r.sd = r.s.
 template <bool SCALED>
-__device__ __forceinline__ float quotient(float x, const RowScale &r) {
-    const float xs = SCALED ? __fmul_rn(x, r.m) : x;
-    float q = __fmul_rn(xs, r.y);
-    float e = __fmaf_rn(-q, r.sd, xs);
-    q = __fmaf_rn(e, r.y, q);
-    e = __fmaf_rn(-q, r.sd, xs);
-    q = __fmaf_rn(e, r.y, q);
-    return copysignf(q, x);
+__device__ __forceinline__ void quotient2(float a, float b, const RowScale &r, float &qa,
+                                          float &qb) {
+    x2::f2 xs = x2::pack(a, b);
+    if (SCALED) xs = x2::mul(xs, x2::pack(r.m, r.m));
+    const x2::f2 y = x2::pack(r.y, r.y), nsd = x2::pack(-r.sd, -r.sd);
+    x2::f2 q = x2::mul(xs, y);
+    x2::f2 e = x2::fma(q, nsd, xs);
+    q = x2::fma(e, y, q);
+    e = x2::fma(q, nsd, xs);
+    q = x2::fma(e, y, q);
+    x2::unpack(q, qa, qb);
+    qa = copysignf(qa, a);
+    qb = copysignf(qb, b);
 }
 
 // Two binary32 values -> two E4M3 codes (low byte first), RN, saturating.
@@ -73,8 +83,11 @@ template <bool SCALED>
 __device__ __forceinline__ uint2 quantize8(const float (&v)[8], const RowScale &r) {
     uint32_t c[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        c[i] = cvt2(quotient<SCALED>(v[2 * i], r), quotient<SCALED>(v[2 * i + 1], r));
+    for (int i = 0; i < 4; ++i) {
+        float qa, qb;
+        quotient2<SCALED>(v[2 * i], v[2 * i + 1], r, qa, qb);
+        c[i] = cvt2(qa, qb);
+    }
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
