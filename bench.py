@@ -545,43 +545,57 @@ def run_gpu(args, w, rank, world, local_rank):
         for i in range(4):
             e2e_step(i)
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(compute)
-        up.wait_event(e0)
-        for i in range(args.e2e_steps):
-            e2e_step(i)
-        compute.wait_stream(down)
-        e1.record(compute)
-        torch.cuda.synchronize()
-        e2e_ms, _, e2e_tps = aggregate_over_ranks(e0.elapsed_time(e1), N, args.e2e_steps,
-                                                  world, dev)
+        # The host link's throughput varies between and within runs on the
+        # same machine (seen: 5.6 and 8.0 ms for the same step, copies alone
+        # 5.5 and 11 ms), so both figures are taken in three trials: the
+        # median trial for the end-to-end value, the fastest copy-only trial
+        # as the link's bound.
+        trials = []
+        for _ in range(3):
+            if world > 1:
+                dist.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(compute)
+            up.wait_event(e0)
+            for i in range(args.e2e_steps):
+                e2e_step(i)
+            compute.wait_stream(down)
+            e1.record(compute)
+            torch.cuda.synchronize()
+            trials.append(aggregate_over_ranks(e0.elapsed_time(e1), N, args.e2e_steps, world,
+                                               dev))
+        trials.sort(key=lambda r: r[0])
+        e2e_ms, _, e2e_tps = trials[1]
         # The same copies with no kernels, up and down at once: the host
         # link's bound on this machine for the end-to-end step.
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        copy_trials = []
         reps = max(4, args.e2e_steps // 4)
-        torch.cuda.synchronize()
-        c0.record(compute)
-        up.wait_event(c0)
-        down.wait_event(c0)
-        for i in range(reps):
-            b = i & 1
-            with torch.cuda.stream(up):
-                for dst, src in zip(din[b], hin):
-                    dst.copy_(src, non_blocking=True)
-            with torch.cuda.stream(down):
-                for dst, src in zip(hout[b], dout[b]):
-                    dst.copy_(src, non_blocking=True)
-        compute.wait_stream(up)
-        compute.wait_stream(down)
-        c1.record(compute)
-        torch.cuda.synchronize()
-        copy_ms = c0.elapsed_time(c1) / reps
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            c0.record(compute)
+            up.wait_event(c0)
+            down.wait_event(c0)
+            for i in range(reps):
+                b = i & 1
+                with torch.cuda.stream(up):
+                    for dst, src in zip(din[b], hin):
+                        dst.copy_(src, non_blocking=True)
+                with torch.cuda.stream(down):
+                    for dst, src in zip(hout[b], dout[b]):
+                        dst.copy_(src, non_blocking=True)
+            compute.wait_stream(up)
+            compute.wait_stream(down)
+            c1.record(compute)
+            torch.cuda.synchronize()
+            copy_trials.append(c0.elapsed_time(c1) / reps)
+        copy_ms = min(copy_trials)
         e2e = {"value": e2e_tps, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
+               "trials_ms_per_step": [t[0] / args.e2e_steps for t in trials],
                "copy_only_ms_per_step": copy_ms,
+               "copy_only_trials_ms": copy_trials,
                "link_gbs": (h2d + d2h) / copy_ms / 1e6,
                "frac_of_copy_bound": copy_ms / (e2e_ms / args.e2e_steps),
                "path": "pinned host -> device copies on a copy stream, moe_dispatch + "
