@@ -10,14 +10,16 @@
 //   recv_x8[d][s][slot(s,t,d)][:] = q(x[s][t]),  recv_scale[d][s][slot] = scale
 // for every destination of the token; padding never written.
 //
-// GB300 design: persistent CTAs of 256 threads, one token row at a time.
+// GB300 design: persistent CTAs of up to 256 threads fitted to the row (128
+// threads x 7 vectors at H = 7168), one token row at a time.
 // One thread keeps the next few bf16 rows of the CTA in flight with 1-D bulk
 // copies into a shared-memory ring (mbarrier completion, bounded waits);
 // each thread takes VPT 16-byte vectors of the row into registers, the
 // row's amax is a warp shuffle + one cross-warp step (the only CTA barrier
 // per token, which also frees the stage for the next copy), and every
 // thread quantises its own vectors (fp8.cuh: one reciprocal per row,
-// FMA-refined quotients) and writes 8 code bytes per vector straight to each
+// FMA-refined quotients, two elements per paired-fp32 instruction) and
+// writes 8 code bytes per vector straight to each
 // destination row -- consecutive threads write consecutive 8-byte pieces,
 // so each warp store covers 256 contiguous bytes.  The row is read once and
 // written once per destination at half the bf16 bytes.
