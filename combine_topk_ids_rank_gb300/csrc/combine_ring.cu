@@ -588,8 +588,11 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, in
     // About 48 KB of ring per CTA (3 rows at H=7168): the residency of
     // several CTAs per SM (several tokens in the reduce/epilogue stage at
     // once) matters more than a deep ring; measured best on the prefill
-    // shape (2-6 slots swept).
-    int s = (int)(kRingBytesTarget / ring_stride(2 * H));
+    // shape (2-6 slots swept).  The FP8 output's longer epilogue wants one
+    // row more in flight: 64 KB (4 rows; prefill 412.4 -> 397.1 us, where
+    // 4 rows made the bf16 output slower).
+    const size_t target = out8 ? 64 * 1024 : kRingBytesTarget;
+    int s = (int)(target / ring_stride(2 * H));
     s = s < 2 ? 2 : (s > kMaxRingSlots ? kMaxRingSlots : s);
     if (const char *e = std::getenv("MOE_COMBINE_RING_SLOTS")) {
         const int x = std::atoi(e);
