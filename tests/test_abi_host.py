@@ -232,3 +232,38 @@ def test_expert_gemm_host_checks(abi):
     assert abi.moe_expert_gemm_fp8(h, A, A, 256, 0) == abi.MOE_ERR_PHASE
     assert abi.moe_a2a_phase(h) == 0
     abi.moe_a2a_destroy(h)
+
+
+def _regions_total(sizes):
+    off = 0
+    for b in sizes:
+        off = (off + b + 255) // 256 * 256
+    return off
+
+
+@pytest.mark.parametrize("R,M,H,E,K", [(8, 4096, 7168, 256, 8), (6, 300, 136, 48, 5),
+                                       (32, 48, 64, 256, 32)])
+def test_workspace_is_the_documented_regions(abi, R, M, H, E, K):
+    # The rank layout's regions, each 256-byte aligned, in the order the
+    # design notes list them: receive rows, combine payload, metadata rows,
+    # scales, source map, counts, send table and weights, top-k slot ranks,
+    # per-tile counts and prefixes (tiles of 32 tokens, the smallest routing
+    # tile), per-source tickets and expert accumulators, tile-local slots,
+    # the flag word.
+    RP = (R + 3) // 4 * 4
+    NT = (M + 31) // 32
+    rank = [R * R * M * H * 2, R * R * M * H * 2, R * R * M * K * 4, R * R * M * K * 4,
+            R * R * M * 4, R * R * M * 4, R * R * 4, E * 4, R * M * RP * 4, R * M * RP * 4,
+            R * M * K, R * NT * RP * 4, R * NT * RP * 4, R * 4, R * E * 4, R * M * RP * 4, 256]
+    c = abi.config(R, M, H, E, K)
+    assert abi.moe_a2a_workspace_bytes(c) == _regions_total(rank)
+    # Expert layout: per-expert planes of cap = R * M rows, send table of KP
+    # entries per token, per-tile expert counts (256-token tiles), the
+    # expert histogram accumulator, the flag word.
+    if E <= 1024 and E * R * M < 2 ** 31:
+        KP = (K + 3) // 4 * 4
+        cap, NTe = R * M, (M + 255) // 256
+        ex = [E * cap * H * 2, E * cap * H * 2, E * cap * 4, E * cap * 4, E * cap * 4, E * 4,
+              E * 4, R * M * KP * 4, R * M * KP * 4, R * NTe * E * 4, E * 4, 256]
+        assert abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_EXPERT) == \
+            _regions_total(ex)
