@@ -175,6 +175,10 @@ def test_expert_layout_limits():
     run(2, 10, 16384, 4, 2, 43, True, True)
 
 
+def test_expert_layout_single_rank():
+    run(1, 300, 128, 8, 2, 44, True, True)
+
+
 def test_expert_layout_varlen_and_dead_rank():
     run(8, 96, 256, 64, 8, 7, True, True, counts=[96, 0, 5, 95, 1, 64, 33, 96], dead=0b100100)
 

@@ -83,6 +83,14 @@ def test_limit_hidden_16384(weighted, fused):
     parity.Case(w).run(seed=6)
 
 
+@pytest.mark.parametrize("weighted,fused", [(False, False), (True, True)])
+def test_single_rank(weighted, fused):
+    # ep_size 1: every expert is local, one plane, three routing tiles
+    w = small("decode", ep_size=1, tokens_per_rank=600, max_tokens=600, runtime_max=600,
+              hidden=256, num_experts=16, top_k=4, weighted=weighted, fused=fused)
+    parity.Case(w).run(seed=9)
+
+
 def test_limit_8192_experts():
     w = small("decode", ep_size=8, tokens_per_rank=300, max_tokens=300, runtime_max=300,
               hidden=64, num_experts=8192, top_k=8)
