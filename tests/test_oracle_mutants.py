@@ -97,6 +97,15 @@ MUTANTS = {
     "gemm_fp8_ignores_channel_scale": (
         "(double)sx[(size_t)e * cap + j] * (double)sw[(size_t)e * N + n] * acc;",
         "(double)sx[(size_t)e * cap + j] * acc;"),
+    "fp8_f32_amax_without_fabs": (
+        "if (fabsf(row[h]) > amax)\n                amax = fabsf(row[h]);",
+        "if (row[h] > amax)\n                amax = row[h];"),
+    "fp8_f32_quotient_multiplies": (
+        "oracle_fp8e4m3_from_f32(row[h] / sc);",
+        "oracle_fp8e4m3_from_f32(row[h] * sc);"),
+    "fp8_f32_zero_row_scale_zero": (
+        "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;\n        scale[i] = sc;\n        for (int h = 0; h < H; ++h)\n            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(row[h] / sc);",
+        "float sc = amax / 448.0f;\n        scale[i] = sc;\n        for (int h = 0; h < H; ++h)\n            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(row[h] / sc);"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -142,6 +151,9 @@ class MutantOracle:
     def expert_gemm_fp8(self, *a, **k):
         return real.expert_gemm_fp8(*a, handle=self.h, **k)
 
+    def quantize_f32_rows_fp8(self, x):
+        return real.quantize_f32_rows_fp8(x, handle=self.h)
+
     def fp8_bits(self, v):
         return real.fp8_bits(v, handle=self.h)
 
@@ -176,6 +188,9 @@ PIN_TESTS = [
     (pins.test_fp8_saturates_and_keeps_nan, {}),
     (pins.test_fp8_row_scaling_closed_forms, {}),
     (pins.test_fp8_round_trip_within_format_bound, {}),
+    (pins.test_fp8_f32_rows_closed_forms, {}),
+    (pins.test_fp8_f32_rows_match_library_cast, {}),
+    (pins.test_fp8_f32_rows_round_trip_over_the_binary32_range, {}),
     (pins.test_route_experts_brute_force, {"seed": 1}),
     (pins.test_expert_dispatch_payload_identity, {}),
     (pins.test_expert_identity_unweighted_counts_distinct_experts, {}),

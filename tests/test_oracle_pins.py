@@ -620,6 +620,64 @@ def test_fp8_round_trip_within_format_bound(oracle):
     assert (np.abs(back - xv) <= 2.0 ** -4 * np.abs(xv) + 2.0 ** -10 * sc[:, None] * 1.0001).all()
 
 
+# The binary32-row quantiser (the FP8 combine output: the value the bf16
+# combine would narrow, quantised per token).  Same format reading as above:
+# scale = amax |v| / 448 in binary32, codes = e4m3(RN32(v / scale)).
+
+def test_fp8_f32_rows_closed_forms(oracle):
+    # amax exactly 448 -> scale 1 and the plain narrowing of each value (the
+    # values are not bf16-representable, so nothing passes through bf16)
+    r = np.array([448.0, -3.3, 0.51, 1.1 * 2 ** -9, 0.0, 100.7, -447.9, 7.01], np.float32)
+    z = np.zeros(8, np.float32)
+    q, sc = oracle.quantize_f32_rows_fp8(np.stack([r, z]))
+    assert sc[0] == 1.0 and np.array_equal(q[0], oracle.fp8_bits(r))
+    assert sc[1] == 1.0 and not q[1].any()
+    # negative-dominated rows: the scale comes from the magnitude of the most
+    # negative value; amax 896 gives scale 2 exactly, codes of v / 2
+    n = np.array([[-896.0, 3.0, 448.0, -1.0], [5.0, -7.0, 1.0, -0.25]], np.float32)
+    q, sc = oracle.quantize_f32_rows_fp8(n)
+    assert sc[0] == 2.0
+    assert np.array_equal(oracle.fp8_to_f32(q[0]), np.array([-448.0, 1.5, 224.0, -0.5], np.float32))
+    assert sc[1] == np.float32(7.0) / np.float32(448.0)
+    assert oracle.fp8_to_f32(q[1])[1] == -448.0
+
+
+def test_fp8_f32_rows_match_library_cast(oracle):
+    # random binary32 rows (not bf16-representable, either sign dominant):
+    # scale = amax / 448 in binary32 (numpy), codes = torch's e4m3 cast of the
+    # binary32 quotient row / scale
+    import torch
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((48, 200)) * np.logspace(-6, 6, 48)[:, None]).astype(np.float32)
+    x[::3] -= np.float32(3) * np.abs(x[::3]).max(axis=1, keepdims=True)  # negative-dominated
+    x[5] = 0.0
+    assert (f32(bits(x[:4])) != x[:4]).any()
+    q, sc = oracle.quantize_f32_rows_fp8(x)
+    amax = np.abs(x).max(axis=1)
+    want_sc = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    assert np.array_equal(sc.view(np.uint32), want_sc.view(np.uint32))
+    quot = (x / want_sc[:, None]).astype(np.float32)
+    assert np.abs(quot).max() <= 448.0 * (1 + 2.0 ** -22)
+    ref = torch.from_numpy(quot).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+
+
+def test_fp8_f32_rows_round_trip_over_the_binary32_range(oracle):
+    # row maxima from 2^-120 to 3e38: dequantised values stay within the
+    # format's half step, 2^-4 |x| for normals plus 2^-10 * scale for
+    # subnormals (the product taken in float64 so that it adds no rounding)
+    rng = np.random.default_rng(9)
+    amax = np.exp2(np.linspace(-120.0, np.log2(3e38), 40))
+    x = (rng.standard_normal((40, 128)) * (amax / 4.0)[:, None]).astype(np.float32)
+    x[:, 0] = amax.astype(np.float32) * np.where(np.arange(40) % 2 == 0, 1, -1)
+    q, sc = oracle.quantize_f32_rows_fp8(x)
+    back = oracle.fp8_to_f32(q).astype(np.float64) * sc.astype(np.float64)[:, None]
+    xv = x.astype(np.float64)
+    tol = 2.0 ** -4 * np.abs(xv) * (1 + 2.0 ** -20) + 2.0 ** -10 * sc.astype(np.float64)[:, None]
+    assert (np.abs(back - xv) <= tol).all()
+    assert np.array_equal(np.abs(oracle.fp8_to_f32(q[:, 0])), np.full(40, 448.0, np.float32))
+
+
 # --------------------------------------------------------------------------
 # Expert-major layout (one expert per received row, "weighted-kernel-sum")
 # --------------------------------------------------------------------------
