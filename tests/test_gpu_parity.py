@@ -110,13 +110,16 @@ def test_decode():
 
 
 def test_prefill_zipf():
-    rep = parity.Case(synth.WORKLOADS["prefill"]).run(sample=2048)
+    # every token of the full-size batch, element by element
+    rep = parity.Case(synth.WORKLOADS["prefill"]).run(sample=None)
+    assert rep["tokens_checked"] == 8 * 4096 and rep["padding_checked"]
     # Zipf(1.2) with contiguous placement: ~2.9 destination ranks per token
     assert 2.7 < rep["recv_rows"] / (8 * 4096) < 3.1
 
 
 def test_wide_ep():
-    rep = parity.Case(synth.WORKLOADS["wide"]).run(sample=4096)
+    rep = parity.Case(synth.WORKLOADS["wide"]).run(sample=None)
+    assert rep["tokens_checked"] == 16 * 1024 and rep["padding_checked"]
     assert 6.3 < rep["recv_rows"] / (16 * 1024) < 6.7
 
 
@@ -129,8 +132,9 @@ def test_ladder_all_rungs_one_workspace():
     big_eo = synth.expert_out_planes(0, w.ep_size, w.max_tokens, w.hidden,
                                      r_big["recv_counts"])
     for T in synth.LADDER_RUNGS:
-        rep = case.run(T=T, inputs=inputs, big_eo=big_eo, sample=1024)
-        assert rep["T"] == T
+        # every token of every rung, element by element
+        rep = case.run(T=T, inputs=inputs, big_eo=big_eo, sample=None)
+        assert rep["T"] == T and rep["tokens_checked"] == 8 * T
 
 
 def test_repeat_calls_bit_identical():
