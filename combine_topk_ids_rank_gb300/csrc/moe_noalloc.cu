@@ -18,6 +18,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -34,25 +35,74 @@ constexpr int kMaxDevices = 64;
 // Shared by every call on a device.
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
+// The array's device address belongs to the context that loaded the module:
+// a device reset (cudaDeviceReset, or a framework that tears down and
+// recreates the primary context) reloads the module, possibly elsewhere.  So
+// the address is kept together with the driver's unique id of the context it
+// was looked up in, and looked up again whenever the current context differs.
+struct ScratchSlot {
+    unsigned long long ctx_id;  // 0: never looked up
+    void *addr;
+};
+
 std::mutex g_mutex;
-void *g_scratch_addr[kMaxDevices];
+ScratchSlot g_slot[kMaxDevices];
+
+// Driver entry points reached through the runtime (no link against the
+// driver library): the current context and its process-unique id.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+bool resolve_driver_calls() {  // under g_mutex
+    if (g_ctx_get_current != nullptr && g_ctx_get_id != nullptr) return true;
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) !=
+            cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+            cudaSuccess ||
+        qb != cudaDriverEntryPointSuccess || a == nullptr || b == nullptr)
+        return false;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+    return true;
+}
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Device address of g_route_scratch on the current device, looked up once
-// per device (host code cannot use the symbol itself as a device pointer).
-int scratch_address(void **out) {
+// Device address of g_route_scratch in the current context (host code cannot
+// use the symbol itself as a device pointer).  Looked up with
+// cudaGetSymbolAddress the first time a context is seen; that lookup is not
+// made while `st` is capturing (it can load the module), which returns
+// MOE_ERR_SETUP_IN_CAPTURE instead.
+int scratch_address(cudaStream_t st, void **out) {
+    // A runtime call that needs the context first, so that the device's
+    // primary context exists and is current before it is queried.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    if (!resolve_driver_calls()) return MOE_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        g_ctx_get_id(ctx, &id) != CUDA_SUCCESS || id == 0)
+        return MOE_ERR_CUDA;
+    ScratchSlot &slot = g_slot[dev];
+    if (slot.ctx_id != id) {
+        if (cap != cudaStreamCaptureStatusNone) return MOE_ERR_SETUP_IN_CAPTURE;
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
             return MOE_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        slot.addr = p;
+        slot.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return MOE_OK;
 }
 
@@ -108,7 +158,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     }
 
     void *base = nullptr;
-    const int rc = scratch_address(&base);
+    const int rc = scratch_address(st, &base);
     if (rc != MOE_OK) return rc;
 
     // Carve the scratch: per-tile counts and prefixes (written before they

@@ -21,6 +21,7 @@ MOE_ERR_CUDA = 4
 MOE_ERR_ROUTING = 5
 MOE_ERR_DEVICE_TIMEOUT = 6
 MOE_ERR_INTERNAL = 7
+MOE_ERR_SETUP_IN_CAPTURE = 8
 MOE_DEVICE_FLAG_BAD_EXPERT_ID = 0x1
 MOE_DEVICE_FLAG_WAIT_TIMEOUT = 0x2
 MOE_DEVICE_FLAG_BAD_SLOT = 0x4

@@ -78,9 +78,12 @@ enum moe_status {
     MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     MOE_ERR_ROUTING = 5,       /* device flag: an expert id outside [-1, E) */
     MOE_ERR_DEVICE_TIMEOUT = 6,/* device flag: a bounded on-chip wait ran out */
-    MOE_ERR_INTERNAL = 7       /* device flag: a consistency guard fired (a
+    MOE_ERR_INTERNAL = 7,      /* device flag: a consistency guard fired (a
                                   routing slot outside its plane was skipped);
                                   never expected, reported rather than faulting */
+    MOE_ERR_SETUP_IN_CAPTURE = 8 /* moe_route_static_scratch: the first call in
+                                  a CUDA context came while `stream` was
+                                  capturing; nothing was queued */
 };
 
 /* Bits of the sticky device flag word (see moe_a2a_get_error). */
@@ -399,9 +402,15 @@ int moe_quantize_rows_fp8(const float *d_x, int64_t rows, int32_t hidden, void *
  * by the CUDA runtime on every device that loads the library and is held
  * until the process exits.
  *
- * Set-up: the first call on a device (with that device current) looks up
- * the array's device address once; make that first call before any stream
- * capture.  All calls on a device share the one array and it keeps the last
+ * Set-up: the first call in a CUDA context (with its device current) looks
+ * up the array's device address with cudaGetSymbolAddress and keeps it with
+ * the context's unique id; a later call in another context of that device
+ * (after cudaDeviceReset, or after a framework recreated the primary
+ * context, which reloads the library's device code) looks it up again, so a
+ * stale address is never used.  Make the first call in each context before
+ * any stream capture: a first call made while `stream` is capturing queues
+ * nothing and returns MOE_ERR_SETUP_IN_CAPTURE.  All calls on a device share
+ * the one array and it keeps the last
  * call's contents: calls whose work overlaps on the GPU (other streams, or
  * other threads without ordering) race on it and must be serialised by the
  * caller.  The parts that must start at zero (a ticket and an expert
