@@ -21,6 +21,7 @@ share no data); rank 0 prints.
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -234,6 +235,33 @@ def oracle_seconds_per_token(w, seed):
     return min(s.step() for _ in range(2)) / s.tokens
 
 
+def host_cpu():
+    """The host the oracle runs on: logical CPUs and the CPU model (from
+    /proc/cpuinfo; Arm hosts give no model name, so the implementer / part
+    numbers stand in), recorded beside the single core the oracle uses."""
+    model = None
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" not in line:
+                    continue
+                k, v = (x.strip() for x in line.split(":", 1))
+                if k in ("model name", "Model") and model is None and v:
+                    model = v
+                fields.setdefault(k, v)
+    except OSError:
+        pass
+    if model is None and "CPU part" in fields:
+        parts = {"0xd4f": "Neoverse-V2", "0xd40": "Neoverse-V1", "0xd0c": "Neoverse-N1",
+                 "0xd49": "Neoverse-N2"}
+        part = fields["CPU part"]
+        model = "Arm %s (implementer %s, part %s)" % (
+            parts.get(part.lower(), "core"), fields.get("CPU implementer", "?"), part)
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or "unknown",
+            "machine": platform.machine(), "threads_used": 1}
+
+
 def cpu_baseline(w, seed, target_seconds):
     per_tok = oracle_seconds_per_token(w, seed)
     T_s = int(max(1, min(w.tokens_per_rank, target_seconds / per_tok / w.ep_size)))
@@ -242,7 +270,8 @@ def cpu_baseline(w, seed, target_seconds):
     return {"value": sample.tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": "route+dispatch+combine of the first %d tokens per rank (%d tokens, "
                       "%s), single-threaded C oracle, %.1f s" % (
-                          T_s, sample.tokens, w.name, sec)}
+                          T_s, sample.tokens, w.name, sec),
+            "host": host_cpu()}
 
 
 def run_reference(args, w, rank):
@@ -266,7 +295,7 @@ def run_reference(args, w, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_dict(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "host": host_cpu()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -574,7 +574,7 @@ cudaError_t by_vpt(Act a, int vpt, bool w, bool f, bool o, const CombineParams *
 }  // namespace
 
 cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, int num_sms,
-                                 LaunchShape *shape, int *vpt, int *slots) {
+                                 const Tuning &tn, LaunchShape *shape, int *vpt, int *slots) {
     const int H8 = H / 8;
     int v = 1;
     while (v < 8 && (H8 + v - 1) / v > consumer_warps_max(v) * 32) v *= 2;
@@ -594,10 +594,8 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, in
     const size_t target = out8 ? 64 * 1024 : kRingBytesTarget;
     int s = (int)(target / ring_stride(2 * H));
     s = s < 2 ? 2 : (s > kMaxRingSlots ? kMaxRingSlots : s);
-    if (const char *e = std::getenv("MOE_COMBINE_RING_SLOTS")) {
-        const int x = std::atoi(e);
-        if (x >= 2 && x <= kMaxRingSlots) s = x;
-    }
+    if (tn.combine_ring_slots >= 2 && tn.combine_ring_slots <= kMaxRingSlots)
+        s = tn.combine_ring_slots;
     while (s > 2 && ring_smem_bytes(2 * H, s) > (size_t)optin) --s;
     if (ring_smem_bytes(2 * H, s) > (size_t)optin) return cudaErrorInvalidValue;
     *vpt = v;

@@ -27,8 +27,6 @@
 
 #include "moe_a2a.h"
 
-#include <cstdlib>
-
 namespace moe {
 namespace {
 
@@ -146,24 +144,17 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
     ptx::bulk_wait_all();
 }
 
-int env_int(const char *name, int fallback) {
-    const char *v = std::getenv(name);
-    if (!v || !*v) return fallback;
-    const int x = std::atoi(v);
-    return x > 0 ? x : fallback;
-}
-
 }  // namespace
 
-cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, DispatchParams *p,
-                             LaunchShape *shape) {
+cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, const Tuning &tn,
+                             DispatchParams *p, LaunchShape *shape) {
     const int chunks = (row_bytes + kMaxChunk - 1) / kMaxChunk;
     int chunk = (row_bytes + chunks - 1) / chunks;
     chunk = (chunk + 15) / 16 * 16;
     const int stage_bytes = (chunk + 2 * P * 4 + 127) / 128 * 128;  // row, slots, prefixes
     int stages = 65536 / stage_bytes;
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-    stages = env_int("MOE_DISPATCH_STAGES", stages);
+    if (tn.dispatch_stages > 0) stages = tn.dispatch_stages;
     const size_t smem = (size_t)stages * stage_bytes + (size_t)stages * sizeof(uint64_t);
 
     cudaError_t err = cudaFuncSetAttribute(dispatch_rows_kernel,
@@ -173,7 +164,7 @@ cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, DispatchParams *
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_rows_kernel, 32, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    per_sm = env_int("MOE_DISPATCH_CTAS_PER_SM", per_sm);
+    if (tn.dispatch_ctas_per_sm > 0) per_sm = tn.dispatch_ctas_per_sm;
 
     p->row_bytes = row_bytes;
     p->chunk_bytes = chunk;

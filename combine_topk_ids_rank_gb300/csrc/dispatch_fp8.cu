@@ -29,8 +29,6 @@
 
 #include "moe_a2a.h"
 
-#include <cstdlib>
-
 namespace moe {
 namespace {
 
@@ -218,16 +216,16 @@ int fit_threads(int H8) {
     return ((H8 + 7) / 8 + 31) / 32 * 32;
 }
 
+// Ring depth and residency of the FP8 dispatch, once per handle.  Stages:
+// about 42 KB of bf16 rows per CTA (3 rows at H = 7168), at least 2
+// (Tuning::fp8_dispatch_stages overrides, 2..8).
 template <int VPT>
-cudaError_t launch_t(DispatchFp8Params p, int num_sms, cudaStream_t st) {
-    const int threads = fit_threads(p.H8);
-    // Stages: about 42 KB of bf16 rows per CTA (3 rows at H = 7168), at
-    // least 2.  MOE_FP8_DISPATCH_STAGES overrides (2..8).
-    const size_t stride = ((size_t)p.H * 2 + 127) / 128 * 128;
+cudaError_t prepare_t(int H, int num_sms, int stages_override, int *stages, LaunchShape *shape) {
+    const int threads = fit_threads(H / 8);
+    const size_t stride = ((size_t)H * 2 + 127) / 128 * 128;
     int S = (int)((42u << 10) / stride);
-    if (const char *e = std::getenv("MOE_FP8_DISPATCH_STAGES")) S = std::atoi(e);
+    if (stages_override > 0) S = stages_override;
     S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
-    p.stages = S;
     const size_t smem = stride * S;
     cudaError_t err = cudaFuncSetAttribute(dispatch_fp8_kernel<VPT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -236,13 +234,22 @@ cudaError_t launch_t(DispatchFp8Params p, int num_sms, cudaStream_t st) {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel<VPT>,
                                                         threads, smem);
     if (err != cudaSuccess) return err;
-    long long grid = (long long)num_sms * (per_sm < 1 ? 1 : per_sm);
+    *stages = S;
+    shape->grid = num_sms * (per_sm < 1 ? 1 : per_sm);
+    shape->block = threads;
+    shape->smem = smem;
+    return cudaSuccess;
+}
+
+template <int VPT>
+cudaError_t launch_t(const DispatchFp8Params &p, const LaunchShape &shape, cudaStream_t st) {
+    long long grid = shape.grid;
     if (grid > p.tokens) grid = p.tokens;
     if (grid < 1) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(shape.block, 1, 1);
+    cfg.dynamicSmemBytes = shape.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -289,9 +296,18 @@ cudaError_t by_vpt(int vpt, A... a) {
 }
 
 template <int VPT>
+struct DispatchPrepare {
+    static cudaError_t run(int H, int num_sms, int stages_override, int *stages,
+                           LaunchShape *shape) {
+        return prepare_t<VPT>(H, num_sms, stages_override, stages, shape);
+    }
+};
+
+template <int VPT>
 struct DispatchLaunch {
-    static cudaError_t run(const DispatchFp8Params *p, int num_sms, cudaStream_t st) {
-        return launch_t<VPT>(*p, num_sms, st);
+    static cudaError_t run(const DispatchFp8Params *p, const LaunchShape *shape,
+                           cudaStream_t st) {
+        return launch_t<VPT>(*p, *shape, st);
     }
 };
 
@@ -305,9 +321,17 @@ struct QuantLaunch {
 
 }  // namespace
 
-cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, int num_sms, cudaStream_t st) {
-    if (p.H % 16 != 0 || p.H8 > 2048) return cudaErrorInvalidValue;
-    return by_vpt<DispatchLaunch>(vectors_per_thread(p.H8), &p, num_sms, st);
+cudaError_t dispatch_fp8_prepare(int H, int num_sms, const Tuning &tn, DispatchFp8Params *p,
+                                 LaunchShape *shape) {
+    if (H % 16 != 0 || H / 8 > 2048) return cudaErrorInvalidValue;
+    return by_vpt<DispatchPrepare>(vectors_per_thread(H / 8), H, num_sms,
+                                   tn.fp8_dispatch_stages, &p->stages, shape);
+}
+
+cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, const LaunchShape &shape,
+                                cudaStream_t st) {
+    if (p.H % 16 != 0 || p.H8 > 2048 || p.stages < 2) return cudaErrorInvalidValue;
+    return by_vpt<DispatchLaunch>(vectors_per_thread(p.H8), &p, &shape, st);
 }
 
 cudaError_t launch_quantize_rows_fp8(const float *x, long long rows, int H, uint8_t *q,

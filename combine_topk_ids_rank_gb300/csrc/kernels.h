@@ -4,7 +4,6 @@
 
 #include <cstddef>
 #include <cstdint>
-#include <cstdlib>
 
 #include <cuda_runtime.h>
 
@@ -41,18 +40,27 @@ __host__ __device__ inline void token_of(const TokenMap &m, int R, long long i, 
 constexpr int kRouteTile = 256;
 constexpr int kRouteMinTile = 32;
 
+// Tuning switches, for sweeps only: read from the environment once, when a
+// handle is created (read_tuning in moe_a2a.cpp), never on the call path.
+// 0 selects the measured default of each.
+struct Tuning {
+    int route_overlap;         // MOE_ROUTE_OVERLAP: 0 = passes in stream order (default 1)
+    int route_tile;            // MOE_ROUTE_TILE: 32, 64, 128 or 256 tokens
+    int dispatch_stages;       // MOE_DISPATCH_STAGES: ring depth of the bf16 row copy
+    int dispatch_ctas_per_sm;  // MOE_DISPATCH_CTAS_PER_SM
+    int fp8_dispatch_stages;   // MOE_FP8_DISPATCH_STAGES: 2..8
+    int combine_kernel;        // MOE_COMBINE_KERNEL: 1 = ring, 2 = registers
+    int combine_ring_slots;    // MOE_COMBINE_RING_SLOTS: 2..32
+};
+
 // Tile of one call: 256 tokens.  Smaller tiles (more CTAs per SM) measured
 // slower on every shape tried -- wide EP 206.6 us at 32 vs 199-200 us at
 // 128-256, prefill 321.5 vs 318.8, decode 32.0 vs 31.4 (dispatch phase) --
 // since the work per token is a few dependent memory accesses and more CTAs
-// only add scan steps.  MOE_ROUTE_TILE=32|64|128|256 overrides (tuning).
-inline int route_tile(long long R, long long T, int num_sms) {
-    (void)R, (void)T, (void)num_sms;
-    if (const char *e = std::getenv("MOE_ROUTE_TILE")) {
-        const int t = std::atoi(e);
-        if (t == 32 || t == 64 || t == 128 || t == 256) return t;
-    }
-    return kRouteTile;
+// only add scan steps.  Tuning::route_tile overrides.
+inline int route_tile(const Tuning &tn) {
+    const int t = tn.route_tile;
+    return (t == 32 || t == 64 || t == 128 || t == 256) ? t : kRouteTile;
 }
 
 // Routing, pass 1: per-tile destination counts, their exclusive per-tile
@@ -220,8 +228,8 @@ cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pd
 
 // Dispatch: ring depth and per-SM residency for a row size and P send-row
 // entries per token.
-cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, DispatchParams *p,
-                             LaunchShape *shape);
+cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, const Tuning &tn,
+                             DispatchParams *p, LaunchShape *shape);
 cudaError_t launch_dispatch_rows(const DispatchParams &p, const LaunchShape &shape,
                                  cudaStream_t st, bool pdl);
 
@@ -234,7 +242,7 @@ cudaError_t launch_combine(const CombineParams &p, bool weighted, bool fused, in
 // Combine with bulk-copy row streaming (one CTA per SM, producer warp +
 // consumer warps): vectors per consumer thread, ring depth and shape.
 cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, int num_sms,
-                                 LaunchShape *shape, int *vpt, int *slots);
+                                 const Tuning &tn, LaunchShape *shape, int *vpt, int *slots);
 cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, bool out8,
                                 int vpt, const LaunchShape &shape, cudaStream_t st);
 
@@ -251,10 +259,15 @@ struct DispatchFp8Params {
     TokenMap map;
     DestRows dest;
     int R, RP, m, H, H8;
-    int stages;               // set by the launcher
+    int stages;               // set by dispatch_fp8_prepare
     long long tokens;
 };
-cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, int num_sms, cudaStream_t st);
+// Ring depth, residency and function attributes of the FP8 dispatch for a
+// hidden size (once per handle): fills p->stages and the launch shape.
+cudaError_t dispatch_fp8_prepare(int H, int num_sms, const Tuning &tn, DispatchFp8Params *p,
+                                 LaunchShape *shape);
+cudaError_t launch_dispatch_fp8(const DispatchFp8Params &p, const LaunchShape &shape,
+                                cudaStream_t st);
 // fp32 rows [rows][H] -> e4m3 codes [rows][H] + scale [rows] (H % 8 == 0).
 cudaError_t launch_quantize_rows_fp8(const float *x, long long rows, int H, uint8_t *q,
                                      float *scale, int num_sms, cudaStream_t st);

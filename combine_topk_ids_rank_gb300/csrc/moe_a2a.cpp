@@ -115,6 +115,27 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+int env_int(const char *name) {
+    const char *v = std::getenv(name);
+    return (v != nullptr && *v) ? std::atoi(v) : 0;
+}
+
+// The tuning switches (kernels.h), read once when a handle is created.
+moe::Tuning read_tuning() {
+    moe::Tuning tn;
+    const char *ov = std::getenv("MOE_ROUTE_OVERLAP");
+    tn.route_overlap = (ov != nullptr && ov[0] == '0') ? 0 : 1;
+    tn.route_tile = env_int("MOE_ROUTE_TILE");
+    tn.dispatch_stages = env_int("MOE_DISPATCH_STAGES");
+    tn.dispatch_ctas_per_sm = env_int("MOE_DISPATCH_CTAS_PER_SM");
+    tn.fp8_dispatch_stages = env_int("MOE_FP8_DISPATCH_STAGES");
+    const char *ck = std::getenv("MOE_COMBINE_KERNEL");
+    tn.combine_kernel = ck == nullptr ? 0 : std::strcmp(ck, "ring") == 0 ? 1
+                                          : std::strcmp(ck, "regs") == 0 ? 2 : 0;
+    tn.combine_ring_slots = env_int("MOE_COMBINE_RING_SLOTS");
+    return tn;
+}
+
 }  // namespace
 
 struct moe_a2a {
@@ -130,12 +151,15 @@ struct moe_a2a {
     bool accum_dirty;  // routing pass interrupted: re-zero its accumulators
     int reduction;     // MOE_REDUCE_*
     int recv_format;   // MOE_FORMAT_*
+    moe::Tuning tuning;  // read at creation
     // lazily initialised on the first call that queues work
     bool ready;
     int device;
     int num_sms;
     moe::DispatchParams dispatch_tmpl;
     moe::LaunchShape dispatch_shape;
+    int fp8_stages;  // FP8 dispatch ring depth and shape (H % 16 == 0 only)
+    moe::LaunchShape fp8_shape;
     // The rank layout's second routing pass runs on `side`, beside the row
     // copy: forked after the first pass (ev_count), joined before the call
     // returns (ev_scan).
@@ -164,13 +188,19 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
         cudaSuccess)
         return MOE_ERR_CUDA;
     std::memset(&h->dispatch_tmpl, 0, sizeof h->dispatch_tmpl);
-    if (moe::dispatch_prepare(2 * h->cfg.hidden, h->L.P, h->num_sms, &h->dispatch_tmpl,
-                              &h->dispatch_shape) != cudaSuccess)
+    if (moe::dispatch_prepare(2 * h->cfg.hidden, h->L.P, h->num_sms, h->tuning,
+                              &h->dispatch_tmpl, &h->dispatch_shape) != cudaSuccess)
         return MOE_ERR_CUDA;
+    if (h->cfg.hidden % 16 == 0) {
+        moe::DispatchFp8Params fp;
+        if (moe::dispatch_fp8_prepare(h->cfg.hidden, h->num_sms, h->tuning, &fp,
+                                      &h->fp8_shape) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        h->fp8_stages = fp.stages;
+    }
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    const char *ov = std::getenv("MOE_ROUTE_OVERLAP");
-    h->overlap = h->L.layout == MOE_LAYOUT_RANK && !(ov != nullptr && ov[0] == '0');
+    h->overlap = h->L.layout == MOE_LAYOUT_RANK && h->tuning.route_overlap != 0;
     if (h->overlap) {  // each object once, also after a partial failure
         if (h->side == nullptr &&
             cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
@@ -230,6 +260,7 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
         fp.R = R, fp.RP = h->L.RP, fp.m = m;
         fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
         fp.tokens = ntok;
+        fp.stages = h->fp8_stages;
         fp.tile_prefix = nullptr;
         fp.tile = fp.ntiles = 0;
         if (tile > 0) {
@@ -237,8 +268,8 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
             fp.tile_prefix = at<int32_t>(h, h->L.tile_prefix);
             fp.tile = tile, fp.ntiles = ntiles;
         }
-        return moe::launch_dispatch_fp8(fp, h->num_sms, st) == cudaSuccess ? MOE_OK
-                                                                            : MOE_ERR_CUDA;
+        return moe::launch_dispatch_fp8(fp, h->fp8_shape, st) == cudaSuccess ? MOE_OK
+                                                                              : MOE_ERR_CUDA;
     }
     moe::DispatchParams dp = h->dispatch_tmpl;
     dp.x = static_cast<const uint8_t *>(d_x);
@@ -330,7 +361,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
                 return MOE_ERR_CUDA;
             h->accum_dirty = false;
         }
-        const int tile = moe::route_tile(R, tmax, h->num_sms);
+        const int tile = moe::route_tile(h->tuning);
         const int ntiles = (tmax + tile - 1) / tile;
 
         moe::RouteCountParams rc_p;
@@ -468,15 +499,15 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
             // The fused combine streams its rows through a shared-memory
             // ring (its epilogue then overlaps other tokens' loads); the
             // plain gather-sum keeps rows in registers, which measured
-            // faster there.  MOE_COMBINE_KERNEL=ring|regs overrides.  The
-            // FP8 output exists on the ring kernel only.
-            const char *sel = std::getenv("MOE_COMBINE_KERNEL");
+            // faster there.  Tuning::combine_kernel overrides.  The FP8
+            // output exists on the ring kernel only.
             bool ring = fused || out8;
-            if (sel != nullptr && std::strcmp(sel, "regs") == 0) ring = out8;
-            if (sel != nullptr && std::strcmp(sel, "ring") == 0) ring = true;
+            if (h->tuning.combine_kernel == 2) ring = out8;
+            if (h->tuning.combine_kernel == 1) ring = true;
             cudaError_t e =
                 ring ? moe::combine_ring_prepare(h->cfg.hidden, weighted != 0, fused, out8,
-                                                 h->num_sms, &h->combine_shape[variant],
+                                                 h->num_sms, h->tuning,
+                                                 &h->combine_shape[variant],
                                                  &h->combine_vpt[variant],
                                                  &h->combine_slots[variant])
                      : moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
@@ -551,6 +582,7 @@ int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_w
     h->L = L;
     h->phase = 0;
     h->active = cfg->ep_size >= 32 ? 0xffffffffu : ((1u << cfg->ep_size) - 1u);
+    h->tuning = read_tuning();
     *out = h;
     return MOE_OK;
 }
@@ -751,6 +783,8 @@ const char *moe_a2a_status_string(int status) {
         case MOE_ERR_ROUTING: return "expert id outside [-1, num_experts) seen on device";
         case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
         case MOE_ERR_INTERNAL: return "internal consistency guard fired on device";
+        case MOE_ERR_SETUP_IN_CAPTURE:
+            return "first allocation-free routing call in a context made during stream capture";
         default: return "unknown status";
     }
 }
