@@ -611,6 +611,74 @@ void oracle_expert_gemm(int E, long cap, int H, int N, const int32_t *recv_count
     }
 }
 
+/*
+ * The same expert-side product on the rank planes (the receive layout the
+ * rank dispatch produces).  A received row (d, s, j) carries one token and
+ * the token's experts that live on rank d (recv_ids, -1 elsewhere).  [IX]
+ * "Why": each expert applies its weights to the rows it received; vLLM
+ * applies the gates in the MoE layer, so rank d's message for the token is
+ * its experts' outputs summed with their gates.  Readings (the pages give no
+ * arithmetic): the output of expert e_k on the row is a bf16 value,
+ *   y_k[n] = bf16_rn(f32_rn(sum_h x[h] * w[e_k][n][h]))   (the sum exact here,
+ *            in double, then rounded to binary32 and to bf16),
+ * and the row's message is
+ *   msg[n] = bf16_rn(sum over k ascending with recv_ids[k] >= 0 of
+ *                    g_k * y_k[n]),  g_k = recv_w[k] (apply_gates) or 1,
+ * in binary32 from +0.0, one multiply and one add per term (no FMA).
+ * Only rows j < recv_counts[d][s] are computed, or only the flat rows
+ * (d * R + s) * m + j listed in `rows` (n_rows of them) when rows != NULL;
+ * msg is [R][R][m][N] (other rows untouched).  ymag / smag (optional, same
+ * shape, double) receive the magnitudes sum_k |g_k| |y_k exact| and
+ * sum_k |g_k| sum_h |x[h] w[e_k][n][h]| that bound rounding differences.
+ */
+void oracle_expert_gemm_rank(int R, int m, int K, int H, int N, const int32_t *recv_counts,
+                             const uint16_t *recv_x, const int32_t *recv_ids,
+                             const float *recv_w, const uint16_t *w, int apply_gates,
+                             const int64_t *rows, long n_rows, uint16_t *msg, double *ymag,
+                             double *smag)
+{
+    long total = rows != NULL ? n_rows : (long)R * R * m;
+    for (long i = 0; i < total; ++i) {
+        long flat = rows != NULL ? (long)rows[i] : i;
+        long plane = flat / m;
+        long j = flat - plane * m;
+        int d = (int)(plane / R), s = (int)(plane % R);
+        if (d >= R || j >= recv_counts[d * R + s])
+            continue;
+        const uint16_t *xr = recv_x + (size_t)flat * H;
+        const int32_t *ids = recv_ids + (size_t)flat * K;
+        const float *g = recv_w + (size_t)flat * K;
+        for (int n = 0; n < N; ++n) {
+            float a = 0.0f;
+            double ym = 0.0, sm = 0.0;
+            for (int k = 0; k < K; ++k) {
+                int e = ids[k];
+                if (e < 0)
+                    continue;
+                const uint16_t *wr = w + ((size_t)e * N + n) * H;
+                double y = 0.0, mag = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    double prod = (double)oracle_f32_from_bf16(xr[h]) *
+                                  (double)oracle_f32_from_bf16(wr[h]);
+                    y += prod;
+                    mag += fabs(prod);
+                }
+                float yk = oracle_f32_from_bf16(oracle_bf16_from_f32((float)y));
+                float gk = apply_gates ? g[k] : 1.0f;
+                float p = gk * yk;
+                a = a + p;
+                ym += fabs((double)gk) * fabs(y);
+                sm += fabs((double)gk) * mag;
+            }
+            msg[(size_t)flat * N + n] = oracle_bf16_from_f32(a);
+            if (ymag != NULL)
+                ymag[(size_t)flat * N + n] = ym;
+            if (smag != NULL)
+                smag[(size_t)flat * N + n] = sm;
+        }
+    }
+}
+
 /* forward declaration: the e4m3 decoding defined with the FP8 helpers below */
 float oracle_f32_from_fp8e4m3(uint8_t q);
 

@@ -53,6 +53,9 @@ def _bind(handle):
     handle.oracle_expert_gemm.restype = None
     handle.oracle_expert_gemm_fp8.argtypes = [c_int, c_long, c_int, c_int] + [p] * 6
     handle.oracle_expert_gemm_fp8.restype = None
+    handle.oracle_expert_gemm_rank.argtypes = ([c_int] * 5 + [p] * 5 + [c_int, p, c_long]
+                                               + [p] * 3)
+    handle.oracle_expert_gemm_rank.restype = None
     handle.oracle_f32_from_fp8e4m3.argtypes = [ctypes.c_uint8]
     handle.oracle_f32_from_fp8e4m3.restype = c_float
     handle.oracle_fp8e4m3_from_f32.argtypes = [c_float]
@@ -302,6 +305,37 @@ def expert_gemm(x, w, recv_counts, handle=None):
     h.oracle_expert_gemm(E, cap, H, N, _ptr(_need(recv_counts, np.int32, (E,))), _ptr(xb),
                          _ptr(wb), _ptr(y))
     return y
+
+
+def expert_gemm_rank(recv_x, recv_ids, recv_w, recv_counts, w, apply_gates=True, rows=None,
+                     magnitudes=False, handle=None):
+    """The expert product on the rank planes: for every received row (or the
+    flat rows (d*R+s)*m+j listed in `rows`), msg = bf16 of the gate-weighted
+    (or plain) binary32 sum, ascending k, of the bf16 outputs of the row's
+    local experts.  recv_x [R, R, m, H] uint16, recv_ids [R, R, m, K] int32,
+    recv_w [R, R, m, K] float32, recv_counts [R, R], w [E, N, H] uint16.
+    Returns msg uint16 [R, R, m, N] (0xFFFF in rows not computed) and, with
+    magnitudes=True, also ymag and smag float64 of the same shape."""
+    h = handle or lib()
+    xb = _need(recv_x, np.uint16)
+    R, R2, m, H = xb.shape
+    ids = _need(recv_ids, np.int32)
+    K = ids.shape[-1]
+    if R2 != R or ids.shape != (R, R, m, K):
+        raise ValueError("recv_ids must be [R, R, m, K]")
+    wb = _need(w, np.uint16)
+    N = wb.shape[1]
+    if wb.shape[2] != H:
+        raise ValueError("w must be [E, N, H]")
+    rl = None if rows is None else _need(rows, np.int64)
+    msg = np.full((R, R, m, N), 0xFFFF, np.uint16)
+    ym = np.full((R, R, m, N), np.nan, np.float64) if magnitudes else None
+    sm = np.full((R, R, m, N), np.nan, np.float64) if magnitudes else None
+    h.oracle_expert_gemm_rank(R, m, K, H, N, _ptr(_need(recv_counts, np.int32, (R, R))), _ptr(xb),
+                              _ptr(ids), _ptr(_need(recv_w, np.float32, ids.shape)), _ptr(wb),
+                              int(bool(apply_gates)), _ptr(rl), 0 if rl is None else rl.shape[0],
+                              _ptr(msg), _ptr(ym), _ptr(sm))
+    return (msg, ym, sm) if magnitudes else msg
 
 
 def expert_gemm_fp8(qx, sx, qw, sw, recv_counts, handle=None):

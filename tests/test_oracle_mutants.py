@@ -106,6 +106,21 @@ MUTANTS = {
     "fp8_f32_zero_row_scale_zero": (
         "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;\n        scale[i] = sc;\n        for (int h = 0; h < H; ++h)\n            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(row[h] / sc);",
         "float sc = amax / 448.0f;\n        scale[i] = sc;\n        for (int h = 0; h < H; ++h)\n            q[(size_t)i * H + h] = oracle_fp8e4m3_from_f32(row[h] / sc);"),
+    "gemm_rank_descending_k": (
+        "for (int k = 0; k < K; ++k) {\n                int e = ids[k];\n                if (e < 0)\n                    continue;\n                const uint16_t *wr",
+        "for (int k = K - 1; k >= 0; --k) {\n                int e = ids[k];\n                if (e < 0)\n                    continue;\n                const uint16_t *wr"),
+    "gemm_rank_gates_ignored": (
+        "float gk = apply_gates ? g[k] : 1.0f;",
+        "float gk = 1.0f;"),
+    "gemm_rank_uses_fma": (
+        "float p = gk * yk;\n                a = a + p;",
+        "a = fmaf(gk, yk, a);"),
+    "gemm_rank_expert_output_not_narrowed": (
+        "float yk = oracle_f32_from_bf16(oracle_bf16_from_f32((float)y));",
+        "float yk = (float)y;"),
+    "gemm_rank_wrong_expert_weights": (
+        "const uint16_t *wr = w + ((size_t)e * N + n) * H;\n                double y = 0.0, mag = 0.0;",
+        "const uint16_t *wr = w + ((size_t)(e ^ 1) * N + n) * H;\n                double y = 0.0, mag = 0.0;"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -147,6 +162,9 @@ class MutantOracle:
 
     def expert_gemm(self, *a, **k):
         return real.expert_gemm(*a, handle=self.h, **k)
+
+    def expert_gemm_rank(self, *a, **k):
+        return real.expert_gemm_rank(*a, handle=self.h, **k)
 
     def expert_gemm_fp8(self, *a, **k):
         return real.expert_gemm_fp8(*a, handle=self.h, **k)
@@ -199,6 +217,11 @@ PIN_TESTS = [
     (pins.test_expert_gemm_identity_and_power_of_two_weights, {}),
     (pins.test_expert_gemm_matches_library_matmul, {}),
     (pins.test_expert_gemm_fp8_identity_and_library_matmul, {}),
+    (pins.test_expert_gemm_rank_identity_weights_count_local_experts, {}),
+    (pins.test_expert_gemm_rank_power_of_two_weights_and_dyadic_gates, {}),
+    (pins.test_expert_gemm_rank_matches_library_matmul_and_gate_order, {}),
+    (pins.test_expert_gemm_rank_equals_expert_layout_with_one_expert_per_rank, {}),
+    (pins.test_expert_gemm_rank_sums_in_top_k_order, {}),
 ]
 
 

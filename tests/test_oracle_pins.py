@@ -884,3 +884,140 @@ def test_expert_gemm_fp8_identity_and_library_matmul(oracle):
         c = counts[e]
         ref = (fx[e, :c] @ fw[e].T) * sx[e, :c, None] * sw[e][None, :]
         assert np.allclose(y[e, :c], ref, rtol=1e-14, atol=0)
+
+
+# --------------------------------------------------------------------------
+# Expert-side product on the rank planes: each received row's local experts,
+# their bf16 outputs summed with the gates in ascending k, one narrowing
+# --------------------------------------------------------------------------
+
+def _rank_planes(oracle, R=4, T=30, K=4, E=16, H=32, seed=13):
+    from combine_topk_ids_rank_gb300 import synth
+    ids = synth.topk_ids(seed, R, T, E, K)
+    w = synth.topk_weights(seed, R, T, K)
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    r = oracle.route(ids, w, E, T)
+    d = oracle.dispatch(ids, w, x, E, T, r)
+    return ids, w, x, r, d
+
+
+def test_expert_gemm_rank_identity_weights_count_local_experts(oracle):
+    # W_e = I for every expert, no gates: each row's message is n * x, with n
+    # the row's local (valid) ids; n * x is exact in binary32, so the message
+    # is torch's round-to-nearest-even of n * x (a library routine)
+    import torch
+    R, T, K, E, H = 4, 30, 4, 8, 32           # 2 experts per rank: rows carry 1 or 2
+    ids, w, x, r, d = _rank_planes(oracle, R, T, K, E, H)
+    eye = bits(np.stack([np.eye(H, dtype=np.float32)] * E))
+    msg = oracle.expert_gemm_rank(d["recv_x"], d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                  eye, apply_gates=False)
+    seen = set()
+    for dd in range(R):
+        for s in range(R):
+            c = r["recv_counts"][dd, s]
+            n = (d["recv_ids"][dd, s, :c] >= 0).sum(axis=1).astype(np.float32)
+            seen.update(n.tolist())
+            want = torch.from_numpy(f32(d["recv_x"][dd, s, :c]) * n[:, None]).to(
+                torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(msg[dd, s, :c], want)
+            assert (msg[dd, s, c:] == 0xFFFF).all()       # rows past a count untouched
+    assert {1.0, 2.0} <= seen
+
+
+def test_expert_gemm_rank_power_of_two_weights_and_dyadic_gates(oracle):
+    # W_e = 2^(e mod 3) I and gates 1/8 (exact): message = x * sum over the
+    # row's local k of 2^(e_k mod 3) / 8, exact in binary32 and in bf16 range
+    R, T, K, E, H = 2, 20, 8, 8, 16
+    ids, _, x, r, _ = _rank_planes(oracle, R, T, K, E, H, seed=14)
+    w8 = np.full((R, T, K), 0.125, np.float32)
+    d = oracle.dispatch(ids, w8, x, E, T, r)
+    scale = 2.0 ** (np.arange(E) % 3)
+    W = bits(np.stack([np.eye(H, dtype=np.float32) * scale[e] for e in range(E)]))
+    msg = oracle.expert_gemm_rank(d["recv_x"], d["recv_ids"], d["recv_w"], r["recv_counts"], W,
+                                  apply_gates=True)
+    for dd in range(R):
+        for s in range(R):
+            c = r["recv_counts"][dd, s]
+            rid = d["recv_ids"][dd, s, :c]
+            f = np.where(rid >= 0, scale[np.maximum(rid, 0)], 0.0).sum(axis=1) / 8.0
+            want = f32(d["recv_x"][dd, s, :c]).astype(np.float64) * f[:, None]
+            got = f32(msg[dd, s, :c]).astype(np.float64)
+            exact = f32(bits(want.astype(np.float32))).astype(np.float64)
+            assert np.array_equal(got, exact)
+
+
+def test_expert_gemm_rank_matches_library_matmul_and_gate_order(oracle):
+    # random weights: each local expert's output is numpy's float64 matmul
+    # rounded to binary32 then bf16 (torch), the gates applied in binary32 in
+    # ascending k, one product and one sum per term, then bf16
+    import torch
+    R, T, K, E, H, N = 3, 14, 4, 12, 24, 40
+    ids, w, x, r, d = _rank_planes(oracle, R, T, K, E, H, seed=15)
+    rng = np.random.default_rng(16)
+    W = bits((rng.standard_normal((E, N, H)) / 4).astype(np.float32))
+    msg, ym, sm = oracle.expert_gemm_rank(d["recv_x"], d["recv_ids"], d["recv_w"],
+                                          r["recv_counts"], W, apply_gates=True,
+                                          magnitudes=True)
+
+    def to_bf16(v):
+        return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).float().numpy()
+
+    Wf = f32(W).astype(np.float64)
+    for dd in range(R):
+        for s in range(R):
+            for j in range(r["recv_counts"][dd, s]):
+                xr = f32(d["recv_x"][dd, s, j]).astype(np.float64)
+                acc = np.zeros(N, np.float32)
+                ymag = np.zeros(N)
+                for k in range(K):
+                    e = d["recv_ids"][dd, s, j, k]
+                    if e < 0:
+                        continue
+                    y = Wf[e] @ xr
+                    g = d["recv_w"][dd, s, j, k]
+                    acc = (acc + (np.float32(g) * to_bf16(y.astype(np.float32))).astype(
+                        np.float32)).astype(np.float32)
+                    ymag += abs(float(g)) * np.abs(y)
+                want = torch.from_numpy(acc).to(torch.bfloat16).view(torch.int16).numpy().view(
+                    np.uint16)
+                assert np.array_equal(msg[dd, s, j], want)
+                assert np.allclose(ym[dd, s, j], ymag, rtol=1e-12, atol=0)
+                assert (sm[dd, s, j] >= ym[dd, s, j] * (1 - 1e-12)).all()
+
+
+def test_expert_gemm_rank_equals_expert_layout_with_one_expert_per_rank(oracle):
+    # one expert per rank and distinct ids: every received row carries exactly
+    # one local expert, so without gates the rank message is that expert's
+    # bf16 output -- the expert-layout product of the same rows
+    R, T, K, H, N = 4, 16, 2, 32, 64
+    E = R
+    ids, w, x, r, d = _rank_planes(oracle, R, T, K, E, H, seed=17)
+    rng = np.random.default_rng(18)
+    W = bits((rng.standard_normal((E, N, H)) / 4).astype(np.float32))
+    msg = oracle.expert_gemm_rank(d["recv_x"], d["recv_ids"], d["recv_w"], r["recv_counts"], W,
+                                  apply_gates=False)
+    re = oracle.route_experts(ids, w, E, T)
+    xe = oracle.dispatch_experts(x, E, T, re)
+    y = oracle.expert_gemm(xe, W, re["recv_counts"])
+    for e in range(E):
+        rows = np.concatenate([msg[e, s, :r["recv_counts"][e, s]] for s in range(R)])
+        c = re["recv_counts"][e]
+        assert rows.shape[0] == c
+        assert np.array_equal(rows, bits(y[e, :c].astype(np.float32)))
+
+
+def test_expert_gemm_rank_sums_in_top_k_order(oracle):
+    # one row with three local experts in top-k order [2, 0, 1] whose outputs
+    # are 2^24, 1 and -2^24 (x = ones, W_e = c_e I): in binary32, ascending k
+    # gives (2^24 + 1) - 2^24 = 0; expert-id order or descending k give 1
+    R, T, K, E, H = 1, 1, 3, 4, 8
+    ids = np.array([[[2, 0, 1]]], np.int32)
+    w = np.ones((R, T, K), np.float32)
+    x = bits(np.ones((R, T, H), np.float32))
+    r = oracle.route(ids, w, E, T)
+    d = oracle.dispatch(ids, w, x, E, T, r)
+    c = {2: 2.0 ** 24, 0: 1.0, 1: -2.0 ** 24, 3: 0.0}
+    W = bits(np.stack([np.eye(H, dtype=np.float32) * c[e] for e in range(E)]))
+    msg = oracle.expert_gemm_rank(d["recv_x"], d["recv_ids"], d["recv_w"], r["recv_counts"], W,
+                                  apply_gates=False)
+    assert (f32(msg[0, 0, 0]) == 0.0).all()
