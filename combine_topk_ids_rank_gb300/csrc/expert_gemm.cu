@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 namespace moe {
@@ -47,6 +48,11 @@ constexpr int kEpiWarps = 4;      // warps 0-3: epilogue (tensor-memory lane qua
 constexpr int kProducerWarp = 4;  // TMA
 constexpr int kMmaWarp = 5;       // MMA issue + tensor-memory allocation
 constexpr int kThreads = 6 * 32;
+// Gathered rows (rank planes): warps 6-9 fetch the A tile, one thread per
+// tile row, with 16-byte cp.async copies into the 128-byte-swizzled layout.
+constexpr int kLoaderWarp0 = 6;
+constexpr int kLoaderThreads = kBM;
+constexpr int kThreadsGather = kThreads + kLoaderThreads;
 constexpr int kGroupM = 8;        // row tiles per raster group
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000;  // 0.5 s of wall time per wait
 
@@ -95,8 +101,14 @@ struct TileMap {
     }
 };
 
-template <int BN, int STAGES, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+// GATHER = false: the A rows of expert e are rows e * cap + j of the expert
+//   planes (2-D TMA tiles), the output rows likewise.
+// GATHER = true (rank planes): expert e's A rows are the receive rows
+//   pair_row[pbase[e] + j], j < count[e] (pbase: exclusive prefix of the
+//   counts), fetched by the loader warps; output row pbase[e] + j of the
+//   pair-major output.
+template <int BN, int STAGES, bool FP8, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                        const __grid_constant__ CUtensorMap tmap_w, const ExpertGemmParams p) {
     using L = GemmSmem<BN, STAGES>;
@@ -104,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_first[kMaxExpertsExpertLayout + 1];
     __shared__ int s_mtiles[kMaxExpertsExpertLayout];
     __shared__ int s_count[kMaxExpertsExpertLayout];
+    __shared__ int s_pbase[GATHER ? kMaxExpertsExpertLayout + 1 : 1];
     __shared__ volatile int s_failed;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nthreads = GATHER ? kThreadsGather : kThreads;
 
     const uint32_t base = ptx::smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
@@ -119,14 +133,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     // tile list from the device-side counts
-    for (int e = tid; e < p.E; e += kThreads) {
+    for (int e = tid; e < p.E; e += nthreads) {
         const int c = p.recv_counts[e];
         s_count[e] = c;
         s_mtiles[e] = (c + kBM - 1) / kBM;
     }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], 1);
+            // gathered rows: the B copy's arrival plus one per loader thread
+            ptx::mbar_init(&full[s], GATHER ? 1 + kLoaderThreads : 1);
             ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -145,6 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int NT = p.N / BN;
         s_first[0] = 0;
         for (int e = 0; e < p.E; ++e) s_first[e + 1] = s_first[e] + s_mtiles[e] * NT;
+        if constexpr (GATHER) {
+            s_pbase[0] = 0;
+            for (int e = 0; e < p.E; ++e) s_pbase[e + 1] = s_pbase[e] + s_count[e];
+        }
     }
     __syncthreads();
     const uint32_t taddr = *tmem_slot;
@@ -166,8 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s_failed = 1;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)(L::kA + L::kB));
-                    tc::tma_load_2d(a_tiles + s * L::kA, &tmap_x, kb * kBK, row0, &full[s]);
+                    if constexpr (GATHER) {  // A comes from the loader warps
+                        ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)L::kB);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)(L::kA + L::kB));
+                        tc::tma_load_2d(a_tiles + s * L::kA, &tmap_x, kb * kBK, row0, &full[s]);
+                    }
                     tc::tma_load_2d(b_tiles + s * L::kB, &tmap_w, kb * kBK, wrow0, &full[s]);
                 }
             }
@@ -196,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
+                    // rows written by the loaders' cp.async (generic proxy),
+                    // read next by the tensor cores (async proxy)
+                    if constexpr (GATHER) ptx::fence_proxy_async_smem();
                     const uint64_t ad = tc::smem_desc_sw128(ptx::smem_u32(a_tiles + s * L::kA));
                     const uint64_t bd = tc::smem_desc_sw128(ptx::smem_u32(b_tiles + s * L::kB));
                     // four K steps of 32 bytes (16 bf16 or 32 e4m3) = 2 descriptor units
@@ -215,7 +241,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::commit(drain);
             ptx::mbar_wait_timed(drain, 0, kWaitNs);
         }
-    } else {
+    } else if (GATHER && warp >= kLoaderWarp0) {
+        // Loader thread li fetches tile row li: for every k block the eight
+        // 16-byte chunks of its 128-byte row segment, chunk c stored at
+        // position c ^ (li mod 8) -- the 128-byte swizzle a TMA load would
+        // apply (the stage starts on a 1024-byte boundary) -- and one arrival
+        // on the stage's barrier once its copies have landed.
+        const int li = tid - kLoaderWarp0 * 32;
+        const uint8_t *xb = static_cast<const uint8_t *>(p.x);
+        const size_t row_bytes = (size_t)p.H * 2;
+        uint32_t kc = 0;
+        for (int t = blockIdx.x; t < ntiles && !s_failed; t += gridDim.x) {
+            int e, mt, nt;
+            tm.of(t, e, mt, nt);
+            int r = mt * kBM + li;
+            if (r >= s_count[e]) r = s_count[e] - 1;  // rows past the count: not stored
+            long long arow = __ldg(p.pair_row + s_pbase[e] + r);
+            if (arow < 0 || arow >= p.a_rows) {  // guard: never produced by the pair lists
+                atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                arow = 0;
+            }
+            const uint8_t *src = xb + (size_t)arow * row_bytes;
+            for (int kb = 0; kb < KB; ++kb, ++kc) {
+                const int s = (int)(kc % STAGES);
+                if (!ptx::mbar_wait_timed(&empty[s], ((kc / STAGES) & 1u) ^ 1u, kWaitNs)) {
+                    s_failed = 1;
+                    break;
+                }
+                uint8_t *dst = a_tiles + s * L::kA + li * kRowBytes;
+                const uint8_t *g = src + (size_t)kb * kRowBytes;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (li & 7)) << 4), g + (c << 4));
+                ptx::cp_async_mbar_arrive_noinc(&full[s]);
+            }
+        }
+        ptx::cp_async_wait_all();  // copies land before shared memory goes away
+    } else if (warp < kEpiWarps) {
         // epilogue: warp w owns tensor-memory lanes 32w..32w+31 = tile rows
         __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out);
         uint32_t it = 0;
@@ -235,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // FP8 operands: y = acc * sx[row] * sw[column], two fp32 products
             const float sx = (FP8 && live) ? p.x_scale[(long long)e * p.cap + r] : 1.0f;
             const float *swr = FP8 ? p.w_scale + (long long)e * p.N + (long long)nt * BN : nullptr;
-            __nv_bfloat16 *dst_row = out + ((long long)e * p.cap + r) * p.N + (long long)nt * BN;
+            const long long orow = GATHER ? (long long)s_pbase[e] + r : (long long)e * p.cap + r;
+            __nv_bfloat16 *dst_row = out + orow * p.N + (long long)nt * BN;
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tc::ld_32x32(taddr + b * BN + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
@@ -314,14 +376,16 @@ bool make_map(CUtensorMap *m, const void *base, long long rows, int cols, int bo
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool FP8>
+template <int BN, int STAGES, bool FP8, bool GATHER>
 cudaError_t launch_t(const ExpertGemmParams &p, cudaStream_t st) {
     using L = GemmSmem<BN, STAGES>;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, p.x, (long long)p.E * p.cap, p.H, kBM, FP8) ||
+    // (gathered rows are fetched without a tensor map; mx is then unused)
+    if ((!GATHER && !make_map(&mx, p.x, (long long)p.E * p.cap, p.H, kBM, FP8)) ||
         !make_map(&mw, p.w, (long long)p.E * p.N, p.H, BN, FP8))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<BN, STAGES, FP8>,
+    if (GATHER) std::memset(&mx, 0, sizeof mx);
+    cudaError_t err = cudaFuncSetAttribute(expert_gemm_kernel<BN, STAGES, FP8, GATHER>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            L::kBytes);
     if (err != cudaSuccess) return err;
@@ -334,7 +398,8 @@ cudaError_t launch_t(const ExpertGemmParams &p, cudaStream_t st) {
     const long long most = (long long)p.E * p.mtiles * (p.N / BN);
     const int grid = (int)(most < sms ? most : sms);
     if (grid < 1) return cudaSuccess;
-    expert_gemm_kernel<BN, STAGES, FP8><<<grid, kThreads, L::kBytes, st>>>(mx, mw, p);
+    expert_gemm_kernel<BN, STAGES, FP8, GATHER>
+        <<<grid, GATHER ? kThreadsGather : kThreads, L::kBytes, st>>>(mx, mw, p);
     return cudaGetLastError();
 }
 
@@ -345,11 +410,18 @@ cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st) {
     if (p.H % bk != 0 || p.H < bk || p.N % 128 != 0 || p.N < 128 || p.cap < 1 ||
         p.E > kMaxExpertsExpertLayout)
         return cudaErrorInvalidValue;
+    if (p.gather) {  // rank planes: bf16 rows gathered through pair_row
+        if (p.fp8 || p.pair_row == nullptr) return cudaErrorInvalidValue;
+        return p.N % 256 == 0 ? launch_t<256, 4, false, true>(p, st)
+                              : launch_t<128, 6, false, true>(p, st);
+    }
     if (p.fp8) {
         if (p.x_scale == nullptr || p.w_scale == nullptr) return cudaErrorInvalidValue;
-        return p.N % 256 == 0 ? launch_t<256, 4, true>(p, st) : launch_t<128, 6, true>(p, st);
+        return p.N % 256 == 0 ? launch_t<256, 4, true, false>(p, st)
+                              : launch_t<128, 6, true, false>(p, st);
     }
-    return p.N % 256 == 0 ? launch_t<256, 4, false>(p, st) : launch_t<128, 6, false>(p, st);
+    return p.N % 256 == 0 ? launch_t<256, 4, false, false>(p, st)
+                          : launch_t<128, 6, false, false>(p, st);
 }
 
 }  // namespace moe

@@ -1,0 +1,178 @@
+// expert_rank.cu -- the expert-side product on the rank planes: the pair
+// lists that feed the gathered tcgen05 product (expert_gemm.cu) and the
+// gated sum of each received row's expert outputs.
+//
+// Operation (InferenceX PR #2450, "CollectiveX: add FlashInfer one-sided
+// NVLink EP for the GB SKUs", "Why": each expert applies its weights to the
+// rows it received; vLLM applies the gates in the MoE layer).  A received
+// row (d, s, j) carries one token and, in recv_topk_ids, the token's experts
+// that live on rank d (-1 elsewhere).  Readings: expert e_k's output on the
+// row is bf16 (the product of expert_gemm.cu), and rank d's message is
+//   out[d][s][j][n] = bf16_rn( sum over k ascending with a local id of
+//                              g_k * y_k[n] ),  g_k = recv_topk_w or 1,
+// in binary32 from +0.0, one multiply and one add per term (no FMA).
+//
+// GB300 design:
+//   * rank_pairs: one (row, k) pair per local id.  Every CTA forms the
+//     exclusive prefix of the experts' pair counts (local_expert_counts of
+//     the dispatch) in shared memory; each thread walks received rows and
+//     places its pairs with one atomic per expert and warp (lanes naming
+//     the same expert are grouped with a match), writing the pair's
+//     receive row (expert-major, what the product gathers) and the pair
+//     index of (row, k) (what the sum reads).  The order of pairs inside an
+//     expert is not fixed; every pair's product is the same whatever its
+//     place in a tile, and the sum runs over k in a fixed order.
+//   * rank_aggregate: one thread per 16-byte vector of an output row; the
+//     row's pairs are taken in ascending k, their bf16 outputs widened and
+//     summed in fp32 registers, the message stored as bf16.  An HBM stream:
+//     pairs x N x 2 bytes read, rows x N x 2 bytes written.
+#include "kernels.h"
+
+#include "moe_a2a.h"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kPairThreads = 256;
+constexpr int kAggThreads = 256;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__global__ void __launch_bounds__(kPairThreads) rank_pairs_kernel(const RankPairsParams p) {
+    __shared__ int32_t pbase[kMaxExpertsExpertLayout + 1];
+    __shared__ int32_t wsum[kPairThreads / 32];
+    // exclusive prefix of the pair counts, 256 experts per step
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += kPairThreads) {
+        const int e = e0 + (int)threadIdx.x;
+        const int c = e < p.E ? __ldg(p.pair_counts + e) : 0;
+        int v = c;  // inclusive scan inside the warp
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += u;
+        }
+        if (lane == 31) wsum[warp] = v;
+        __syncthreads();
+        int before = carry;
+        for (int w = 0; w < warp; ++w) before += wsum[w];
+        if (e < p.E) pbase[e] = before + v - c;
+        int total = 0;
+        for (int w = 0; w < kPairThreads / 32; ++w) total += wsum[w];
+        carry += total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) pbase[p.E] = carry;
+    __syncthreads();
+
+    const long long rows = (long long)p.R * p.R * p.m;
+    const long long first = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long step = (long long)gridDim.x * blockDim.x;
+    const uint32_t lt = lanemask_lt();
+    // whole warps iterate together (the match and the shuffles need them)
+    for (long long base = first - (threadIdx.x & 31); base < rows; base += step) {
+        const long long row = base + (threadIdx.x & 31);
+        bool live = row < rows;
+        if (live) {
+            const long long plane = row / p.m;
+            const int j = (int)(row - plane * p.m);
+            live = j < __ldg(p.recv_counts + plane);
+        }
+        for (int k = 0; k < p.K; ++k) {
+            const int e = live ? __ldg(p.recv_ids + row * p.K + k) : -1;
+            const uint32_t want = __ballot_sync(kFull, e >= 0);
+            int pos = -1;
+            if (want != 0) {
+                const uint32_t same = __match_any_sync(kFull, e);
+                if (e >= 0) {
+                    const int leader = __ffs(same) - 1;
+                    int got = 0;
+                    if ((int)(threadIdx.x & 31) == leader)
+                        got = atomicAdd(p.cursor + e, __popc(same));
+                    got = __shfl_sync(same, got, leader);
+                    pos = pbase[e] + got + __popc(same & lt);
+                    if (pos < pbase[e + 1]) {
+                        p.pair_row[pos] = (int32_t)row;
+                    } else {  // guard: more pairs than the dispatch counted
+                        atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
+                        pos = -1;
+                    }
+                }
+            }
+            if (live) p.pair_of[row * p.K + k] = pos;
+        }
+    }
+}
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__global__ void __launch_bounds__(kAggThreads) rank_aggregate_kernel(const RankPairsParams p) {
+    const int N8 = p.N / 8;
+    const long long units = (long long)p.R * p.R * p.m * N8;
+    const uint4 *y = reinterpret_cast<const uint4 *>(p.y);
+    uint4 *out = reinterpret_cast<uint4 *>(p.out);
+    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (long long)gridDim.x * blockDim.x) {
+        const long long row = u / N8;
+        const int c = (int)(u - row * N8);
+        const long long plane = row / p.m;
+        const int j = (int)(row - plane * p.m);
+        if (j >= __ldg(p.recv_counts + plane)) continue;  // padding: never written
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = 0.0f;
+        for (int k = 0; k < p.K; ++k) {
+            const int pr = __ldg(p.pair_of + row * p.K + k);
+            if (pr < 0) continue;
+            const float g = p.apply_gates ? __ldg(p.recv_w + row * p.K + k) : 1.0f;
+            const uint4 v = __ldcs(y + (long long)pr * N8 + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[2 * i] = __fadd_rn(a[2 * i], __fmul_rn(g, lo_f(w[i])));
+                a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __fmul_rn(g, hi_f(w[i])));
+            }
+        }
+        __stcs(out + row * N8 + c,
+               make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                          pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7])));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rank_pairs(const RankPairsParams &p, int num_sms, cudaStream_t st) {
+    if (p.E > kMaxExpertsExpertLayout || p.K < 1 || p.K > kMaxTopK) return cudaErrorInvalidValue;
+    const long long rows = (long long)p.R * p.R * p.m;
+    long long grid = (rows + kPairThreads - 1) / kPairThreads;
+    if (grid > 4LL * num_sms) grid = 4LL * num_sms;
+    if (grid < 1) return cudaSuccess;
+    rank_pairs_kernel<<<(unsigned)grid, kPairThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rank_aggregate(const RankPairsParams &p, int num_sms, cudaStream_t st) {
+    if (p.N % 8 != 0) return cudaErrorInvalidValue;
+    const long long units = (long long)p.R * p.R * p.m * (p.N / 8);
+    long long grid = (units + kAggThreads - 1) / kAggThreads;
+    if (grid > 8LL * num_sms) grid = 8LL * num_sms;
+    if (grid < 1) return cudaSuccess;
+    rank_aggregate_kernel<<<(unsigned)grid, kAggThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

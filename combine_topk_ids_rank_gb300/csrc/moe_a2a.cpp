@@ -743,12 +743,103 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
     gp.N = N;
     gp.mtiles = (gp.cap + 127) / 128;
     gp.fp8 = fp8 ? 1 : 0;
+    gp.gather = 0;
+    gp.pair_row = nullptr;
+    gp.a_rows = 0;
     return moe::launch_expert_gemm(gp, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
 }
 
+// Scratch of the rank-plane product, sized for max_tokens_per_rank: the
+// per-expert pair cursors, the receive row of each pair, the pair of each
+// (row, k) and the experts' bf16 outputs, pair-major.
+struct RankScratch {
+    size_t cursor, pair_row, pair_of, y, total;
+};
+
+bool rank_scratch_layout(const moe_a2a_config_t *c, int N, RankScratch *S) {
+    if (!config_ok(c) || N < 128 || N % 128 != 0) return false;
+    const size_t R = c->ep_size, M = c->max_tokens_per_rank, K = c->top_k, E = c->num_experts;
+    const size_t pairs = R * M * K;  // every token's K ids valid and local somewhere
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, kAlign);
+        return o;
+    };
+    S->cursor = take(E * 4);
+    S->pair_row = take(pairs * 4);
+    S->pair_of = take(R * R * M * K * 4);
+    S->y = take(pairs * (size_t)N * 2);
+    S->total = off;
+    return true;
+}
+
 }  // namespace
+
+size_t moe_expert_gemm_rank_scratch_bytes(const moe_a2a_config_t *cfg, int32_t N) {
+    RankScratch S;
+    return rank_scratch_layout(cfg, N, &S) ? S.total : 0;
+}
+
+int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply_gates,
+                         void *d_out, void *d_scratch, size_t scratch_bytes, void *stream) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->phase != 1) return MOE_ERR_PHASE;
+    const int H = h->cfg.hidden, E = h->cfg.num_experts, R = h->cfg.ep_size, K = h->cfg.top_k;
+    if (h->L.layout != MOE_LAYOUT_RANK || h->recv_format != MOE_FORMAT_BF16 ||
+        E > moe::kMaxExpertsExpertLayout)
+        return MOE_ERR_INVALID_ARG;
+    if (H % 64 != 0 || N < 128 || N % 128 != 0 || d_w == nullptr || !aligned(d_w, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (d_out == nullptr && N != H) return MOE_ERR_INVALID_ARG;
+    if (d_out != nullptr && !aligned(d_out, 16)) return MOE_ERR_INVALID_ARG;
+    if (d_scratch == nullptr || !aligned(d_scratch, kAlign)) return MOE_ERR_INVALID_ARG;
+    RankScratch S;
+    if (!rank_scratch_layout(&h->cfg, N, &S)) return MOE_ERR_INVALID_ARG;
+    if (scratch_bytes < S.total) return MOE_ERR_CAPACITY;
+    if (h->ntok == 0) return MOE_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *sc = static_cast<uint8_t *>(d_scratch);
+    const int m = h->m;
+
+    moe::RankPairsParams rp;
+    rp.recv_ids = at<int32_t>(h, h->L.recv_ids);
+    rp.recv_w = at<float>(h, h->L.recv_w);
+    rp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+    rp.pair_counts = at<int32_t>(h, h->L.local_counts);
+    rp.cursor = reinterpret_cast<int32_t *>(sc + S.cursor);
+    rp.pair_row = reinterpret_cast<int32_t *>(sc + S.pair_row);
+    rp.pair_of = reinterpret_cast<int32_t *>(sc + S.pair_of);
+    rp.y = reinterpret_cast<const uint16_t *>(sc + S.y);
+    rp.out = static_cast<uint16_t *>(d_out != nullptr ? d_out : h->ws + h->L.expert_out);
+    rp.flags = at<uint32_t>(h, h->L.flags);
+    rp.R = R, rp.m = m, rp.K = K, rp.E = E, rp.N = N;
+    rp.apply_gates = apply_gates ? 1 : 0;
+    if (cudaMemsetAsync(rp.cursor, 0, sizeof(int32_t) * E, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_rank_pairs(rp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+    moe::ExpertGemmParams gp;
+    gp.x = h->ws + h->L.recv_x;
+    gp.w = d_w;
+    gp.out = sc + S.y;
+    gp.recv_counts = rp.pair_counts;
+    gp.x_scale = nullptr;
+    gp.w_scale = nullptr;
+    gp.flags = at<uint32_t>(h, h->L.flags);
+    gp.E = E;
+    gp.cap = R * m * K;  // pairs of one expert at most
+    gp.H = H;
+    gp.N = N;
+    gp.mtiles = (gp.cap + 127) / 128;
+    gp.fp8 = 0;
+    gp.gather = 1;
+    gp.pair_row = rp.pair_row;
+    gp.a_rows = (long long)R * R * m;
+    if (moe::launch_expert_gemm(gp, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return moe::launch_rank_aggregate(rp, h->num_sms, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream) {
     return expert_gemm_impl(h, d_w, nullptr, N, d_out, false, stream);

@@ -116,6 +116,27 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- 16-byte asynchronous copies (cp.async, no tensor map) ------------------
+
+// global -> shared, 16 bytes, cached in L2 only; tracked per issuing thread.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
+// One arrival on `bar` (counted in its expected arrivals: .noinc) once every
+// cp.async this thread issued so far has completed.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Wait until every cp.async this thread issued has completed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---- programmatic dependent launch -----------------------------------------
 
 // Block until the preceding kernel in the stream completed and its memory

@@ -33,7 +33,8 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_a2a_set_reduction", "moe_dispatch_varlen", "moe_a2a_set_active_ranks",
            "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8",
            "moe_a2a_workspace_bytes_layout", "moe_a2a_create_layout",
-           "moe_expert_gemm", "moe_expert_gemm_fp8")
+           "moe_expert_gemm", "moe_expert_gemm_fp8", "moe_expert_gemm_rank_scratch_bytes",
+           "moe_expert_gemm_rank")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
@@ -110,6 +111,10 @@ def _load(path: str = LIBRARY):
     lib.moe_expert_gemm.restype = ctypes.c_int
     lib.moe_expert_gemm_fp8.argtypes = [p, p, p, i32, p, p]
     lib.moe_expert_gemm_fp8.restype = ctypes.c_int
+    lib.moe_expert_gemm_rank_scratch_bytes.argtypes = [ctypes.POINTER(MoeA2AConfig), i32]
+    lib.moe_expert_gemm_rank_scratch_bytes.restype = ctypes.c_size_t
+    lib.moe_expert_gemm_rank.argtypes = [p, p, i32, i32, p, p, ctypes.c_size_t, p]
+    lib.moe_expert_gemm_rank.restype = ctypes.c_int
     lib.moe_a2a_set_recv_format.argtypes = [p, i32]
     lib.moe_a2a_set_recv_format.restype = ctypes.c_int
     lib.moe_a2a_set_reduction.argtypes = [p, i32]
@@ -229,6 +234,17 @@ def quantize_rows_fp8(x, out=None, scale=None, stream=None):
 def moe_expert_gemm(h, d_w: int, N: int, d_out: int, stream: int = 0) -> int:
     v = ctypes.c_void_p
     return _lib.moe_expert_gemm(h, v(d_w), N, v(d_out), v(stream))
+
+
+def moe_expert_gemm_rank_scratch_bytes(cfg: MoeA2AConfig, N: int) -> int:
+    return _lib.moe_expert_gemm_rank_scratch_bytes(ctypes.byref(cfg), N)
+
+
+def moe_expert_gemm_rank(h, d_w: int, N: int, apply_gates: int, d_out: int, d_scratch: int,
+                         scratch_bytes: int, stream: int = 0) -> int:
+    v = ctypes.c_void_p
+    return _lib.moe_expert_gemm_rank(h, v(d_w), N, apply_gates, v(d_out), v(d_scratch),
+                                     scratch_bytes, v(stream))
 
 
 def moe_expert_gemm_fp8(h, d_w8: int, d_w_scale: int, N: int, d_out: int,
@@ -512,6 +528,34 @@ class MoeA2A:
         st = moe_expert_gemm(self.handle, _ptr(w), N, _ptr(out), self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_expert_gemm")
+        return out if out is not None else self.combine_payload()
+
+    def expert_gemm_rank(self, w, apply_gates=True, out=None, scratch=None, stream=None):
+        """Rank layout: each received row's local experts applied to it, their
+        bf16 outputs summed with the gates (or plainly) in ascending top-k
+        order.  w: bf16 [E, N, H]; out: bf16 [R, R, m, N], or None to write the
+        combine payload (N == H); scratch: uint8 device tensor of at least
+        moe_expert_gemm_rank_scratch_bytes bytes (allocated and kept here if
+        None).  Returns the output tensor."""
+        import torch
+        E, H, R = self.num_experts, self.hidden, self.ep_size
+        N = w.shape[1]
+        self._check(w, torch.bfloat16, (E, N, H), "w")
+        if out is not None:
+            self._check(out, torch.bfloat16, (R, R, self.last_view.plane_stride, N), "out")
+        need = moe_expert_gemm_rank_scratch_bytes(self.cfg, N)
+        if need == 0:
+            raise MoeA2AError(MOE_ERR_INVALID_ARG, "moe_expert_gemm_rank_scratch_bytes")
+        if scratch is None:
+            if getattr(self, "_rank_scratch", None) is None or self._rank_scratch.numel() < need:
+                self._rank_scratch = torch.empty(need, dtype=torch.uint8, device=self.device)
+            scratch = self._rank_scratch
+        if scratch.dtype != torch.uint8 or scratch.device != self.workspace.device:
+            raise ValueError("scratch: expected a uint8 tensor on %s" % self.workspace.device)
+        st = moe_expert_gemm_rank(self.handle, _ptr(w), N, int(bool(apply_gates)), _ptr(out),
+                                  scratch.data_ptr(), scratch.numel(), self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_expert_gemm_rank")
         return out if out is not None else self.combine_payload()
 
     def expert_gemm_fp8(self, w8, w_scale, out=None, stream=None):

@@ -214,6 +214,36 @@ int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void 
 int moe_expert_gemm_fp8(moe_a2a_t *h, const void *d_w8, const float *d_w_scale, int32_t N,
                         void *d_out, void *stream);
 
+/* The expert-side product on the rank planes that moe_dispatch produces in
+ * the rank layout ([IX] "Why": each expert applies its weights to the rows
+ * it received; vLLM applies the gates in the MoE layer).  A received row
+ * (d, s, j), j < recv_counts[d][s], carries one token and, in recv_topk_ids,
+ * the token's experts that live on rank d.  For every such row and column n:
+ *   y_k[n]  = bf16_rn( sum_h x[d][s][j][h] * w[e_k][n][h] )   (e_k local;
+ *             bf16 products accumulated in fp32 on the tensor cores),
+ *   out[d][s][j][n] = bf16_rn( sum over k ascending with a local e_k of
+ *             g_k * y_k[n] ),  g_k = recv_topk_w[d][s][j][k] if apply_gates
+ *             else 1, in fp32 from +0.0, one multiply and one add per term.
+ * With apply_gates and out = the combine payload, an unweighted
+ * moe_combine(h, NULL, 0, ...) then returns sum_k w_k * y_k per token.
+ *   d_w      bf16 [E][N][H] (row n = the weights of output n), 16-byte aligned;
+ *   N        a multiple of 128; H must be a multiple of 64; E <= 1024;
+ *   d_out    bf16 [R][R][m][N], or NULL for the combine payload (N == H);
+ *            rows past a plane's count are not written;
+ *   d_scratch caller-owned device memory of at least
+ *            moe_expert_gemm_rank_scratch_bytes(cfg, N) bytes, 256-byte
+ *            aligned (pair lists and the experts' bf16 outputs; contents
+ *            need not be initialised, and are garbage afterwards).
+ * Requires the rank layout and the bf16 receive format (MOE_ERR_INVALID_ARG
+ * otherwise), a pending dispatch (MOE_ERR_PHASE); the phase does not change.
+ * MOE_ERR_CAPACITY if scratch_bytes is too small.  Queues a memset and three
+ * kernels on `stream` (pair lists, the gathered tcgen05 product, the gated
+ * sum per row). */
+size_t moe_expert_gemm_rank_scratch_bytes(const moe_a2a_config_t *cfg, int32_t N);
+
+int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply_gates,
+                         void *d_out, void *d_scratch, size_t scratch_bytes, void *stream);
+
 /* moe_a2a_workspace_bytes for a layout (0 if the pair is invalid). */
 size_t moe_a2a_workspace_bytes_layout(const moe_a2a_config_t *cfg, int32_t layout);
 

@@ -267,3 +267,28 @@ def test_workspace_is_the_documented_regions(abi, R, M, H, E, K):
               E * 4, R * M * KP * 4, R * M * KP * 4, R * NTe * E * 4, E * 4, 256]
         assert abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_EXPERT) == \
             _regions_total(ex)
+
+
+def test_expert_gemm_rank_host_checks(abi):
+    # scratch: pair cursors [E], the receive row of each pair [R*M*K], the pair
+    # of each (row, k) [R*R*M*K] and the pair-major bf16 outputs [R*M*K][N]
+    R, M, H, E, K, N = 8, 64, 256, 32, 4, 384
+    c = abi.config(R, M, H, E, K)
+    assert abi.moe_expert_gemm_rank_scratch_bytes(c, N) == _regions_total(
+        [E * 4, R * M * K * 4, R * R * M * K * 4, R * M * K * N * 2])
+    assert abi.moe_expert_gemm_rank_scratch_bytes(c, 100) == 0        # N % 128
+    A = 1 << 20
+    assert abi.moe_expert_gemm_rank(None, A, 256, 1, 0, A, 1 << 30) == abi.MOE_ERR_INVALID_ARG
+    need = abi.moe_a2a_workspace_bytes(c)
+    st, h = abi.moe_a2a_create(c, 1 << 30, need)
+    assert st == abi.MOE_OK
+    # no dispatch pending: the phase error comes first, nothing is queued
+    assert abi.moe_expert_gemm_rank(h, A, 256, 1, 0, A, 1 << 30) == abi.MOE_ERR_PHASE
+    assert abi.moe_a2a_phase(h) == 0
+    abi.moe_a2a_destroy(h)
+    # the expert layout has its own product
+    ex = abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_EXPERT)
+    st, h = abi.moe_a2a_create_layout(c, abi.MOE_LAYOUT_EXPERT, 1 << 30, ex)
+    assert st == abi.MOE_OK
+    assert abi.moe_expert_gemm_rank(h, A, 256, 1, 0, A, 1 << 30) == abi.MOE_ERR_PHASE
+    abi.moe_a2a_destroy(h)
