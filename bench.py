@@ -54,16 +54,19 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--layout", choices=["rank", "expert"], default="rank",
-                    help="receive layout: planes per (destination, source) rank, or one "
-                         "row per (token, expert) in per-expert planes")
+    ap.add_argument("--layout", choices=["rank", "expert"], default=None,
+                    help="receive layout: planes per (destination, source) rank (default), "
+                         "or one row per (token, expert) in per-expert planes (the default "
+                         "with --expert-gemm)")
     ap.add_argument("--l2-hot", action="store_true",
                     help="no L2 flush between steps even for small inputs (reports the "
                          "L2-hot figure beside the default flushed one; not a bench line)")
     ap.add_argument("--expert-gemm", action="store_true",
-                    help="expert layout with the expert-side product between dispatch and "
-                         "combine (random bf16 weights W_e of H x H, output into the combine "
-                         "payload): one step is a whole single-matrix MoE layer")
+                    help="the expert-side product between dispatch and combine (random bf16 "
+                         "weights W_e of H x H, output into the combine payload): one step is "
+                         "a whole single-matrix MoE layer.  Expert layout by default; with "
+                         "--layout rank the product runs on the rank planes and applies the "
+                         "gates, and the combine is the unweighted rank sum")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 payloads: e4m3 dispatch rows with a per-token scale and an "
                          "e4m3 combine output with a per-token scale (needs hidden %% 16 == 0)")
@@ -74,7 +77,12 @@ def parse_args():
     if args.expert_gemm:
         if args.graph:
             ap.error("--expert-gemm takes direct calls")
-        args.layout = "expert"
+        if args.layout is None:
+            args.layout = "expert"
+        if args.layout == "rank" and args.fp8:
+            ap.error("the rank-plane product takes bf16 rows")
+    if args.layout is None:
+        args.layout = "rank"
     return args
 
 
@@ -364,6 +372,10 @@ def run_gpu(args, w, rank, world, local_rank):
                   .to(torch.bfloat16))
     eo = view.recv_x if identity else None
     gemm = args.expert_gemm
+    gemm_rank = gemm and args.layout == "rank"
+    # the rank-plane product applies the gates; the combine is then the
+    # pages' unweighted rank sum
+    comb_weighted = False if gemm_rank else w.weighted
     if gemm:
         gw = torch.Generator(device=dev).manual_seed(args.seed + 2)
         w_exp = torch.randn((E, H, H), generator=gw, device=dev, dtype=torch.bfloat16)
@@ -375,6 +387,12 @@ def run_gpu(args, w, rank, world, local_rank):
 
             def run_gemm():
                 a2a.expert_gemm_fp8(w8, w8_scale)   # into the combine payload
+        elif gemm_rank:
+            w_exp.mul_(1.0 / H ** 0.5)
+            a2a.expert_gemm_rank(w_exp, True)   # allocates its scratch once, untimed
+
+            def run_gemm():
+                a2a.expert_gemm_rank(w_exp, True)   # gated, into the combine payload
         else:
             w_exp.mul_(1.0 / H ** 0.5)      # in place: E x H x H can be tens of GB
 
@@ -383,14 +401,17 @@ def run_gpu(args, w, rank, world, local_rank):
 
     def combine_into(res_, outs):
         if fp8:
-            a2a.combine_fp8(eo, w.weighted, res_, gam, w.eps, outs[0], outs[1], outs[2])
+            a2a.combine_fp8(eo, comb_weighted, res_, gam, w.eps, outs[0], outs[1], outs[2])
         else:
-            a2a.combine(eo, w.weighted, res_, gam, w.eps, outs[0], outs[1])
+            a2a.combine(eo, comb_weighted, res_, gam, w.eps, outs[0], outs[1])
 
     outs_main = [out8, osc, rout] if fp8 else [out, rout]
     combine_into(res, outs_main)
     torch.cuda.synchronize()
     recv_rows = int(view.recv_counts.sum().item())
+    # rows the product multiplies: one per received row in the expert layout,
+    # one per (row, local expert) pair on the rank planes
+    gemm_rows = int(view.local_expert_counts.sum().item()) if gemm_rank else recv_rows
     st, flags = a2a.get_error()
     if st != 0:
         raise RuntimeError("device flag set: status %d flags %#x" % (st, flags))
@@ -507,9 +528,11 @@ def run_gpu(args, w, rank, world, local_rank):
         **({"expert_gemm": {
             "ms_avg": statistics.fmean(gemm_ms), "ms_p50": pct(gemm_ms, 0.5),
             "ms_p10": pct(gemm_ms, 0.1), "ms_p90": pct(gemm_ms, 0.9),
-            "flops": 2.0 * recv_rows * H * H, "weight_bytes": E * H * H * (1 if fp8 else 2),
-            "tflops": 2.0 * recv_rows * H * H / statistics.fmean(gemm_ms) / 1e9,
-            "kernels": ["expert_gemm"]}} if gemm else {}),
+            "flops": 2.0 * gemm_rows * H * H, "weight_bytes": E * H * H * (1 if fp8 else 2),
+            "tflops": 2.0 * gemm_rows * H * H / statistics.fmean(gemm_ms) / 1e9,
+            "rows": gemm_rows,
+            "kernels": (["rank_pairs", "expert_gemm (gathered rows)", "rank_aggregate"]
+                        if gemm_rank else ["expert_gemm"])}} if gemm else {}),
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
                     "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
                     "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
@@ -657,7 +680,8 @@ def run_gpu(args, w, rank, world, local_rank):
                      "peak": peak, "unit": "GB/s", "frac": c_bytes / c_avg / 1e6 / peak,
                      "traffic": traffic, "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)"
                      % peak_kind if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "gpu_launches": (5 if gemm else 4) * args.steps if T > 0 else 0,
+        "gpu_launches": (4 + (3 if gemm_rank else 1 if gemm else 0)) * args.steps
+                        if T > 0 else 0,
         "launch": "CUDA-graph replay of each phase's C-ABI call" if args.graph
                   else "direct C-ABI calls",
         "clocks": clk,
@@ -688,6 +712,12 @@ def run_gpu(args, w, rank, world, local_rank):
                                     "frac": c_bytes / c_avg / 1e6 / peak}
         cfg["expert_gemm"] = ("W_e %s [%d][%d][%d], output into the combine payload" % (
             "e4m3 (per-channel scale 1/sqrt(H))" if fp8 else "bf16 N(0,1/H)", E, H, H))
+        if gemm_rank:
+            cfg["expert_gemm"] += ("; rank planes: each received row times each of its local "
+                                   "experts (%d pairs), gated sum per row in ascending top-k "
+                                   "order; combine unweighted (the rank sum)" % gemm_rows)
+            line["roofline"]["achieved_over"] = ("the whole product call: pair lists, the "
+                                                 "gathered tcgen05 product and the gated sum")
     return line
 
 

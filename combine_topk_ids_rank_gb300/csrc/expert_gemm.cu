@@ -242,36 +242,50 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
             ptx::mbar_wait_timed(drain, 0, kWaitNs);
         }
     } else if (GATHER && warp >= kLoaderWarp0) {
-        // Loader thread li fetches tile row li: for every k block the eight
-        // 16-byte chunks of its 128-byte row segment, chunk c stored at
-        // position c ^ (li mod 8) -- the 128-byte swizzle a TMA load would
-        // apply (the stage starts on a 1024-byte boundary) -- and one arrival
-        // on the stage's barrier once its copies have landed.
-        const int li = tid - kLoaderWarp0 * 32;
+        // Loader warp w fetches tile rows 32w' .. 32w'+31 (w' = w - 6); lane l
+        // knows the receive row of tile row 32w' + l.  For every k block one
+        // warp instruction covers four rows: lane l copies 16-byte chunk l % 8
+        // of row 4i + l / 8 (eight instructions per warp per stage, each
+        // reading four whole 128-byte lines), stored at chunk position
+        // c ^ (row mod 8) -- the 128-byte swizzle a TMA load would apply (the
+        // stage starts on a 1024-byte boundary).  Each thread then adds one
+        // arrival on the stage's barrier for when its copies have landed.
+        const int lw = warp - kLoaderWarp0;
+        const int c = lane & 7, sub = lane >> 3;
         const uint8_t *xb = static_cast<const uint8_t *>(p.x);
         const size_t row_bytes = (size_t)p.H * 2;
         uint32_t kc = 0;
         for (int t = blockIdx.x; t < ntiles && !s_failed; t += gridDim.x) {
             int e, mt, nt;
             tm.of(t, e, mt, nt);
-            int r = mt * kBM + li;
+            int r = mt * kBM + 32 * lw + lane;
             if (r >= s_count[e]) r = s_count[e] - 1;  // rows past the count: not stored
             long long arow = __ldg(p.pair_row + s_pbase[e] + r);
             if (arow < 0 || arow >= p.a_rows) {  // guard: never produced by the pair lists
                 atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
                 arow = 0;
             }
-            const uint8_t *src = xb + (size_t)arow * row_bytes;
+            // this lane's source rows for the eight instructions of a stage
+            const uint8_t *src[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                src[i] = xb + (size_t)__shfl_sync(0xffffffffu, arow, 4 * i + sub) * row_bytes +
+                         (c << 4);
             for (int kb = 0; kb < KB; ++kb, ++kc) {
                 const int s = (int)(kc % STAGES);
-                if (!ptx::mbar_wait_timed(&empty[s], ((kc / STAGES) & 1u) ^ 1u, kWaitNs)) {
+                // the warp stops together (the shuffles above need whole warps)
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait_timed(
+                                                 &empty[s], ((kc / STAGES) & 1u) ^ 1u, kWaitNs))) {
                     s_failed = 1;
                     break;
                 }
-                uint8_t *dst = a_tiles + s * L::kA + li * kRowBytes;
-                const uint8_t *g = src + (size_t)kb * kRowBytes;
+                uint8_t *stage = a_tiles + s * L::kA;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (li & 7)) << 4), g + (c << 4));
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 32 * lw + 4 * i + sub;  // tile row (row mod 8 = (4i + sub) mod 8)
+                    ptx::cp_async16(stage + row * kRowBytes + ((c ^ (row & 7)) << 4),
+                                    src[i] + (size_t)kb * kRowBytes);
+                }
                 ptx::cp_async_mbar_arrive_noinc(&full[s]);
             }
         }
