@@ -1,0 +1,313 @@
+// dispatch_small.cu -- the whole dispatch phase in one launch, for batches
+// of at most one routing tile (256 tokens) per source rank.
+//
+// Operation: the same as route.cu + dispatch.cu (InferenceX PR #2450,
+// "CollectiveX: add FlashInfer one-sided NVLink EP for the GB SKUs": "Why",
+// "The adapter", the bring-up run table, "Synthesis"):
+//   slot(s,t,d) = #{t' < t : d in dmask(s,t')},
+//   recv_x[d][s][slot][:] = x[s][t][:] for every d in dmask(s,t),
+// with the send table, per-destination weights, source map, masked metadata
+// rows, recv counts and local-expert counts of the routing pass.
+//
+// GB300 design, for small batches where launches and dependent round trips
+// cost more than the bytes: one-warp CTAs, several per SM, each taking
+// units (a token row, or a chunk of it when there are few tokens) of the
+// grid-strided unit list.  A warp derives its token's slots itself from the
+// expert ids of the tokens before it in the same source (one warp ballot per
+// destination and 32 tokens; at most 8 x 32 tokens), so no CTA waits for
+// another and there is no second pass, second stream or event.  Meanwhile
+// lane 0 has already requested the unit's x chunk into a shared-memory stage
+// with a bulk copy; once the slots are known it stores the chunk to every
+// destination row with bulk shared -> global copies.  The warp holding a
+// token's first chunk writes its send row, weights, source-map entries and
+// metadata rows (the token's ids and weights held one per lane) and adds its
+// ids to the local-expert counts with atomics; the warp of a source's last
+// token writes its recv counts.  The counts live in one of two buffers that
+// alternate between calls: each call adds into the buffer the previous call
+// cleared and clears the other one, so nothing waits for a last CTA.
+// Waits are bounded: on time-out the kernel raises the flag, drains its
+// copies and returns.
+#include "kernels.h"
+#include "ptx.cuh"
+
+#include "moe_a2a.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kMaxTileWords = kRouteTile / 32;  // 32-token groups of a source
+
+__device__ __forceinline__ int live_rank(int e, int E, int Epr, uint32_t active) {
+    if (e < 0 || e >= E) return -1;
+    const int d = e / Epr;
+    return ((active >> d) & 1u) ? d : -1;
+}
+
+// Destination mask of a token: ranks of its valid ids on active ranks.
+template <int KT>
+__device__ __forceinline__ uint32_t token_mask(const int32_t *ids, int K, int E, int Epr,
+                                               uint32_t active) {
+    uint32_t mask = 0;
+    if constexpr (KT > 0) {
+        int e[KT];
+#pragma unroll
+        for (int k = 0; k < KT; ++k) e[k] = __ldg(ids + k);
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+            const int d = live_rank(e[k], E, Epr, active);
+            if (d >= 0) mask |= 1u << d;
+        }
+    } else {
+        for (int k = 0; k < K; ++k) {
+            const int d = live_rank(__ldg(ids + k), E, Epr, active);
+            if (d >= 0) mask |= 1u << d;
+        }
+    }
+    return mask;
+}
+
+template <int KT>
+__global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x;
+    const int K = KT > 0 ? KT : p.K;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)p.stages * p.stage_bytes);
+    if (lane == 0) {
+        for (int i = 0; i < p.stages; ++i) ptx::mbar_init(&bars[i], 1);
+        ptx::fence_mbar_init();
+    }
+    __syncwarp();
+
+    const long long first = blockIdx.x, step = gridDim.x;
+    const long long n = first < p.units ? (p.units - 1 - first) / step + 1 : 0;
+    auto unit_bytes = [&](int chunk) -> uint32_t {
+        const int left = p.row_bytes - chunk * p.chunk_bytes;
+        return (uint32_t)(left < p.chunk_bytes ? left : p.chunk_bytes);
+    };
+    auto issue_x = [&](long long i) {  // lane 0: the unit's x chunk into its stage
+        const long long u = first + i * step;
+        const long long tok = u / p.chunks;
+        const int chunk = (int)(u - tok * p.chunks);
+        const int stage = (int)(i % p.stages);
+        const uint32_t bytes = unit_bytes(chunk);
+        ptx::mbar_arrive_expect_tx(&bars[stage], bytes);
+        ptx::bulk_g2s(smem + (size_t)stage * p.stage_bytes,
+                      p.x + tok * p.row_bytes + (long long)chunk * p.chunk_bytes, bytes,
+                      &bars[stage]);
+    };
+
+    // x is an input of the call: request the first chunks right away.
+    const long long prologue = n < p.stages ? n : p.stages;
+    if (lane == 0)
+        for (long long i = 0; i < prologue; ++i) issue_x(i);
+    long long issued = prologue, failed = -1;
+    bool ok = true, waited = false;
+
+    for (long long i = 0; i < n && ok; ++i) {
+        const long long u = first + i * step;
+        const long long tok = u / p.chunks;          // s * T + t
+        const int chunk = (int)(u - tok * p.chunks);
+        const int s = (int)(tok / p.T), t = (int)(tok - (long long)s * p.T);
+        const int32_t *src_ids = p.topk_ids + (size_t)s * p.T * K;
+
+        // the token's own ids and weights, one per lane (K <= 32)
+        const int my_e = lane < K ? __ldg(src_ids + (size_t)t * K + lane) : -1;
+        const float my_w = lane < K ? __ldg(p.topk_w + tok * K + lane) : 0.0f;
+
+        // ---- slots: lane d counts the earlier tokens of source s sent to d ----
+        uint32_t masks[kMaxTileWords];
+        const int words = t / 32 + 1;
+#pragma unroll
+        for (int j = 0; j < kMaxTileWords; ++j) {
+            const int tt = j * 32 + lane;
+            masks[j] = (j < words && tt <= t)
+                           ? token_mask<KT>(src_ids + (size_t)tt * K, K, p.E, p.Epr, p.active)
+                           : 0u;
+        }
+        int cnt = 0;
+        uint32_t own = 0;
+#pragma unroll
+        for (int j = 0; j < kMaxTileWords; ++j) {
+            if (j >= words) break;
+            const int tt = j * 32 + lane;
+            const uint32_t before = tt < t ? masks[j] : 0u;
+            for (int d = 0; d < p.R; ++d) {
+                const uint32_t b = __ballot_sync(kFull, (before >> d) & 1u);
+                if (lane == d) cnt += __popc(b);
+            }
+            if (j == t / 32) own = __shfl_sync(kFull, masks[j], t & 31);
+        }
+
+        // The ids are inputs too; before the first write, wait for the kernels
+        // before this one in the stream (a combine still reading the
+        // previous dispatch's tables).
+        if (!waited) {
+            ptx::grid_dependency_wait();
+            waited = true;
+        }
+
+        // ---- routing outputs, by the warp holding the token's first chunk ----
+        if (chunk == 0) {
+            const int my_d = live_rank(my_e, p.E, p.Epr, p.active);
+            // lane d: the weight sum of the token's experts on d, ascending k
+            // from +0.0; lane k: whether slot k is its rank's first
+            float wsum = 0.0f;
+            bool first_of_rank = my_d >= 0;
+            for (int k = 0; k < K; ++k) {
+                const int e = __shfl_sync(kFull, my_e, k);
+                const float wk = __shfl_sync(kFull, my_w, k);
+                const int d = live_rank(e, p.E, p.Epr, p.active);
+                if (d == lane) wsum = __fadd_rn(wsum, wk);
+                if (k < lane && d == my_d) first_of_rank = false;
+            }
+            if (lane < p.RP) {
+                const bool has = lane < p.R && ((own >> lane) & 1u);
+                p.send_slot[tok * p.RP + lane] = has ? cnt : -1;
+                p.dest_weight[tok * p.RP + lane] = has ? wsum : 0.0f;
+            }
+            if (lane < K) {
+                if (my_e < -1 || my_e >= p.E) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_EXPERT_ID);
+                else if (my_d >= 0) atomicAdd(p.counts + my_e, 1);
+                if (p.topk_dest != nullptr)  // first slot of each rank carries its message
+                    p.topk_dest[tok * K + lane] = (int8_t)(first_of_rank ? my_d : -1);
+            }
+            for (uint32_t b = own; b != 0; b &= b - 1) {  // uniform over the warp
+                const int d = __ffs(b) - 1;
+                const int slot = __shfl_sync(kFull, cnt, d);
+                const size_t row = ((size_t)d * p.R + s) * p.m + slot;
+                if (lane == 0) p.src_token[row] = t;
+                if (lane < K) {
+                    const bool local = my_e >= 0 && my_e < p.E && my_e / p.Epr == d;
+                    p.recv_ids[row * K + lane] = local ? my_e : -1;
+                    p.recv_w[row * K + lane] = local ? my_w : 0.0f;
+                }
+            }
+            if (t == p.T - 1 && lane < p.R)
+                p.recv_counts[lane * p.R + s] = cnt + (int)((own >> lane) & 1u);
+        }
+
+        // ---- the row copy: the chunk to every destination row ----
+        const int stage = (int)(i % p.stages);
+        const uint32_t parity = (uint32_t)((i / p.stages) & 1);
+        bool ready = true;
+        if (lane == 0) ready = ptx::mbar_wait_bounded(&bars[stage], parity, kWaitLimit);
+        if (!__shfl_sync(kFull, ready, 0)) {
+            ok = false;
+            failed = i;
+            break;
+        }
+        const uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
+        const uint32_t bytes = unit_bytes(chunk);
+        const long long col = (long long)chunk * p.chunk_bytes;
+        for (uint32_t b = own; b != 0; b &= b - 1) {
+            const int d = __ffs(b) - 1;
+            const int slot = __shfl_sync(kFull, cnt, d);
+            if (lane == 0)
+                ptx::bulk_s2g(p.recv_x + (((long long)d * p.R + s) * p.m + slot) * p.row_bytes +
+                                  col,
+                              buf, bytes);
+        }
+        if (lane == 0) {
+            ptx::bulk_commit();
+            // refill the stage of unit i - 1 once its stores left shared memory
+            if (i >= 1 && issued < n) {
+                ptx::bulk_wait_read<1>();
+                issue_x(issued);
+            }
+        }
+        if (i >= 1 && issued < n) ++issued;
+    }
+    if (!waited) ptx::grid_dependency_wait();  // (a CTA whose units all failed)
+    if (blockIdx.x == 0)  // the next call's counts buffer starts at zero
+        for (int e = lane; e < p.E; e += 32) p.counts_clear[e] = 0;
+
+    if (lane == 0) {
+        ptx::bulk_wait_all();
+        if (!ok) {
+            atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+            // chunks requested after the one that timed out, still landing in
+            // shared memory, before the CTA exits
+            for (long long j = failed + 1; j < issued; ++j)
+                ptx::mbar_wait_bounded(&bars[j % p.stages], (uint32_t)((j / p.stages) & 1),
+                                       kWaitLimit);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t dispatch_small_prepare(int row_bytes, int num_sms, DispatchSmallShapes *out) {
+    // For 1..8 chunks per row: chunk bytes (a multiple of 16, bulk copies),
+    // two stages of shared memory, CTAs per SM from the occupancy (at most 16).
+    const int max_stage = (row_bytes + 15) / 16 * 16;
+    const size_t max_smem = 2 * (size_t)((max_stage + 127) / 128 * 128) + 2 * sizeof(uint64_t);
+    const void *kern[5] = {(const void *)dispatch_small_kernel<0>,
+                           (const void *)dispatch_small_kernel<1>,
+                           (const void *)dispatch_small_kernel<2>,
+                           (const void *)dispatch_small_kernel<4>,
+                           (const void *)dispatch_small_kernel<8>};
+    for (const void *k : kern) {
+        cudaError_t err =
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+        if (err != cudaSuccess) return err;
+    }
+    out->stages = 2;
+    for (int c = 1; c <= kSmallMaxChunks; ++c) {
+        int chunk = (row_bytes + c - 1) / c;
+        chunk = (chunk + 15) / 16 * 16;
+        const int stage_bytes = (chunk + 127) / 128 * 128;
+        const size_t smem = (size_t)out->stages * stage_bytes + out->stages * sizeof(uint64_t);
+        int per_sm = 0;
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, dispatch_small_kernel<8>, 32, smem);
+        if (err != cudaSuccess) return err;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        if (per_sm > 16) per_sm = 16;
+        out->chunk_bytes[c] = chunk;
+        out->chunks[c] = (row_bytes + chunk - 1) / chunk;
+        out->stage_bytes[c] = stage_bytes;
+        out->shape[c].grid = num_sms * per_sm;
+        out->shape[c].block = 32;
+        out->shape[c].smem = smem;
+    }
+    return cudaSuccess;
+}
+
+int dispatch_small_chunks(int row_bytes, int num_sms, long long tokens) {
+    // about four units per SM, 1..8 chunks per row, chunks of at least 1 KB
+    const long long t = tokens > 0 ? tokens : 1;
+    long long c = (4LL * num_sms + t - 1) / t;
+    c = c < 1 ? 1 : (c > kSmallMaxChunks ? kSmallMaxChunks : c);
+    while (c > 1 && row_bytes / c < 1024) --c;
+    return (int)c;
+}
+
+cudaError_t launch_dispatch_small(const DispatchSmallParams &p, const LaunchShape &shape,
+                                  cudaStream_t st) {
+    if (p.T < 1 || p.T > kRouteTile || p.R > kMaxRanks || p.K > kMaxTopK)
+        return cudaErrorInvalidValue;
+    long long grid = shape.grid;
+    if (grid > p.units) grid = p.units;
+    if (grid < 1) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.dynamicSmemBytes = shape.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (p.K) {
+        case 1: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<1>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<2>, p);
+        case 4: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<4>, p);
+        case 8: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<8>, p);
+        default: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<0>, p);
+    }
+}
+
+}  // namespace moe

@@ -51,6 +51,8 @@ struct Tuning {
     int fp8_dispatch_stages;   // MOE_FP8_DISPATCH_STAGES: 2..8
     int combine_kernel;        // MOE_COMBINE_KERNEL: 1 = ring, 2 = registers
     int combine_ring_slots;    // MOE_COMBINE_RING_SLOTS: 2..32
+    int dispatch_small_max;    // MOE_DISPATCH_SMALL_MAX: largest T for the one-launch
+                               // dispatch (0: the default, -1: never)
 };
 
 // Tile of one call: 256 tokens.  Smaller tiles (more CTAs per SM) measured
@@ -245,6 +247,40 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, in
                                  const Tuning &tn, LaunchShape *shape, int *vpt, int *slots);
 cudaError_t launch_combine_ring(const CombineParams &p, bool weighted, bool fused, bool out8,
                                 int vpt, const LaunchShape &shape, cudaStream_t st);
+
+// The whole dispatch phase in one launch for batches of at most one routing
+// tile per source (dispatch_small.cu; rank layout, bf16 rows, uniform T).
+constexpr int kSmallMaxChunks = 8;
+struct DispatchSmallParams {
+    const int32_t *topk_ids;   // [R][T][K]
+    const float *topk_w;       // [R][T][K]
+    const uint8_t *x;          // bf16 [R][T][H] as bytes
+    uint8_t *recv_x;           // bf16 [R][R][m][H] as bytes
+    int32_t *send_slot;        // [R][T][RP]
+    float *dest_weight;        // [R][T][RP]
+    int32_t *src_token;        // [R][R][m]
+    int32_t *recv_ids;         // [R][R][m][K]
+    float *recv_w;             // [R][R][m][K]
+    int8_t *topk_dest;         // [R][T][K] or null
+    int32_t *recv_counts;      // [R][R]
+    int32_t *counts;           // [E] local-expert counts of this call: zero on entry
+    int32_t *counts_clear;     // [E] the other counts buffer, zeroed for the next call
+    uint32_t *flags;
+    uint32_t active;
+    int R, K, E, Epr, RP, m, T;
+    int row_bytes, chunk_bytes, chunks, stages, stage_bytes;
+    long long units;           // R * T * chunks
+};
+struct DispatchSmallShapes {   // per chunk count 1..kSmallMaxChunks
+    int chunk_bytes[kSmallMaxChunks + 1], chunks[kSmallMaxChunks + 1];
+    int stage_bytes[kSmallMaxChunks + 1];
+    LaunchShape shape[kSmallMaxChunks + 1];
+    int stages;
+};
+cudaError_t dispatch_small_prepare(int row_bytes, int num_sms, DispatchSmallShapes *out);
+int dispatch_small_chunks(int row_bytes, int num_sms, long long tokens);
+cudaError_t launch_dispatch_small(const DispatchSmallParams &p, const LaunchShape &shape,
+                                  cudaStream_t st);
 
 // Dispatch with FP8 rows: per-token e4m3 quantisation into the receive
 // planes plus a per-row scale (see dispatch_fp8.cu).

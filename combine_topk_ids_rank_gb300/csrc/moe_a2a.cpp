@@ -22,12 +22,18 @@
 namespace {
 
 constexpr size_t kAlign = 256;
+// Largest tokens per rank for the one-launch dispatch by default: measured
+// faster than the two routing passes + row copy up to 64 tokens per rank
+// (T = 1: 14.0 vs 16.8 us; T = 64: 18.4 vs 19.2 us, L2 flushed) and slower
+// from 128 on (26.6 vs 24.4 us), where every copy warp rescans up to 255
+// earlier tokens of its source.
+constexpr int kSmallDispatchMaxT = 64;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
     size_t recv_x, expert_out, recv_ids, recv_w, recv_scale, src_token, recv_counts,
-        local_counts;
+        local_counts, local_counts2;
     size_t send_slot, dest_weight, topk_dest, tile_counts, tile_prefix, tile_ticket, hist_accum,
         local_slot, flags;
     size_t total;
@@ -77,6 +83,7 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
         L->src_token = take(E * cap * 4);
         L->recv_counts = take(E * 4);
         L->local_counts = take(E * 4);
+        L->local_counts2 = L->local_counts;
         L->send_slot = take(R * M * KP * 4);
         L->dest_weight = take(R * M * KP * 4);
         L->topk_dest = take(0);
@@ -100,6 +107,7 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
     L->src_token = take(R * R * M * 4);
     L->recv_counts = take(R * R * 4);
     L->local_counts = take(E * 4);
+    L->local_counts2 = take(E * 4);  // the one-launch dispatch alternates the two
     L->send_slot = take(R * M * RP * 4);
     L->dest_weight = take(R * M * RP * 4);
     L->topk_dest = take(R * M * K);
@@ -133,6 +141,7 @@ moe::Tuning read_tuning() {
     tn.combine_kernel = ck == nullptr ? 0 : std::strcmp(ck, "ring") == 0 ? 1
                                           : std::strcmp(ck, "regs") == 0 ? 2 : 0;
     tn.combine_ring_slots = env_int("MOE_COMBINE_RING_SLOTS");
+    tn.dispatch_small_max = env_int("MOE_DISPATCH_SMALL_MAX");
     return tn;
 }
 
@@ -160,6 +169,13 @@ struct moe_a2a {
     moe::LaunchShape dispatch_shape;
     int fp8_stages;  // FP8 dispatch ring depth and shape (H % 16 == 0 only)
     moe::LaunchShape fp8_shape;
+    moe::DispatchSmallShapes small;  // one-launch dispatch (rank layout)
+    // Local-expert counts: the region holding the current dispatch's counts,
+    // and for the one-launch dispatch the buffer (0: local_counts, 1:
+    // local_counts2) its next call adds into, and whether that one is zero.
+    size_t cur_counts;
+    int small_sel;
+    bool small_zero_ok;
     // The rank layout's second routing pass runs on `side`, beside the row
     // copy: forked after the first pass (ev_count), joined before the call
     // returns (ev_scan).
@@ -198,6 +214,9 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
             return MOE_ERR_CUDA;
         h->fp8_stages = fp.stages;
     }
+    if (h->L.layout == MOE_LAYOUT_RANK &&
+        moe::dispatch_small_prepare(2 * h->cfg.hidden, h->num_sms, &h->small) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     h->overlap = h->L.layout == MOE_LAYOUT_RANK && h->tuning.route_overlap != 0;
@@ -290,6 +309,17 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
                : MOE_ERR_CUDA;
 }
 
+// The one-launch dispatch (dispatch_small.cu) serves the rank layout's bf16
+// rows when every source holds the same T tokens, T at most one routing tile
+// and at most Tuning::dispatch_small_max (measured break-even, below).
+bool small_dispatch(const moe_a2a_t *h, const moe::TokenMap &map) {
+    if (h->L.layout != MOE_LAYOUT_RANK || h->recv_format != MOE_FORMAT_BF16 || !map.uniform)
+        return false;
+    const int lim = h->tuning.dispatch_small_max;
+    const int T_max = lim < 0 ? 0 : (lim == 0 ? kSmallDispatchMaxT : lim);
+    return map.stride >= 1 && map.stride <= T_max && map.stride <= moe::kRouteTile;
+}
+
 // The dispatch phase for the tokens described by `map` (rows of stride
 // map.stride in the [R][stride] input arrays).
 int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
@@ -352,6 +382,45 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         h->accum_dirty = false;
         rc = launch_rows(h, d_x, map, m, dest, ntok, st);
         if (rc != MOE_OK) return rc;
+    } else if (small_dispatch(h, map)) {
+        // one launch: every copy warp derives its token's slots itself
+        const size_t bufs[2] = {h->L.local_counts, h->L.local_counts2};
+        const int sel = h->small_sel;
+        if (!h->small_zero_ok &&
+            cudaMemsetAsync(h->ws + bufs[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        const int T = map.stride;
+        const int row_bytes = 2 * h->cfg.hidden;
+        const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
+        moe::DispatchSmallParams sp;
+        sp.topk_ids = d_topk_ids;
+        sp.topk_w = d_topk_w;
+        sp.x = static_cast<const uint8_t *>(d_x);
+        sp.recv_x = at<uint8_t>(h, h->L.recv_x);
+        sp.send_slot = at<int32_t>(h, h->L.send_slot);
+        sp.dest_weight = at<float>(h, h->L.dest_weight);
+        sp.src_token = at<int32_t>(h, h->L.src_token);
+        sp.recv_ids = at<int32_t>(h, h->L.recv_ids);
+        sp.recv_w = at<float>(h, h->L.recv_w);
+        sp.topk_dest = at<int8_t>(h, h->L.topk_dest);
+        sp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+        sp.counts = at<int32_t>(h, bufs[sel]);
+        sp.counts_clear = at<int32_t>(h, bufs[sel ^ 1]);
+        sp.flags = flags;
+        sp.active = h->active;
+        sp.R = R, sp.K = K, sp.E = E, sp.Epr = E / R, sp.RP = RP, sp.m = m, sp.T = T;
+        sp.row_bytes = row_bytes;
+        sp.chunk_bytes = h->small.chunk_bytes[c];
+        sp.chunks = h->small.chunks[c];
+        sp.stages = h->small.stages;
+        sp.stage_bytes = h->small.stage_bytes[c];
+        sp.units = ntok * sp.chunks;
+        h->small_zero_ok = false;  // until the launch that clears the other buffer is queued
+        if (moe::launch_dispatch_small(sp, h->small.shape[c], st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        h->cur_counts = bufs[sel];
+        h->small_sel = sel ^ 1;
+        h->small_zero_ok = true;
     } else {
         if (h->accum_dirty) {
             if (cudaMemsetAsync(h->ws + h->L.tile_ticket, 0, sizeof(int32_t) * R, st) !=
@@ -425,6 +494,11 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         }
     }
 
+    if (ntok == 0 || !small_dispatch(h, map)) {
+        // the routing pass (or the empty call) wrote local_counts
+        h->cur_counts = h->L.local_counts;
+        if (h->small_sel == 0) h->small_zero_ok = false;
+    }
     h->map = map;
     h->ntok = ntok;
     h->m = m;
@@ -435,7 +509,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         out_view->recv_topk_w = at<float>(h, h->L.recv_w);
         out_view->src_token = at<int32_t>(h, h->L.src_token);
         out_view->recv_counts = at<int32_t>(h, h->L.recv_counts);
-        out_view->local_expert_counts = at<int32_t>(h, h->L.local_counts);
+        out_view->local_expert_counts = at<int32_t>(h, h->cur_counts);
         out_view->send_slot = at<int32_t>(h, h->L.send_slot);
         out_view->dest_weight = at<float>(h, h->L.dest_weight);
         out_view->plane_stride = expert ? dest.cap : m;
@@ -808,7 +882,7 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     rp.recv_ids = at<int32_t>(h, h->L.recv_ids);
     rp.recv_w = at<float>(h, h->L.recv_w);
     rp.recv_counts = at<int32_t>(h, h->L.recv_counts);
-    rp.pair_counts = at<int32_t>(h, h->L.local_counts);
+    rp.pair_counts = at<int32_t>(h, h->cur_counts);
     rp.cursor = reinterpret_cast<int32_t *>(sc + S.cursor);
     rp.pair_row = reinterpret_cast<int32_t *>(sc + S.pair_row);
     rp.pair_of = reinterpret_cast<int32_t *>(sc + S.pair_of);

@@ -376,7 +376,7 @@ class MoeA2A:
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_a2a_create")
         self.last_view = None
-        self._view_key = None
+        self._views = {}
         self._payload = None
 
     def _stream(self, stream) -> int:
@@ -413,12 +413,18 @@ class MoeA2A:
                                self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_dispatch")
-        # The views depend only on (m, token stride, format): reuse them across calls.
-        key = (raw.plane_stride, raw.token_stride, raw.recv_format)
-        if self.last_view is None or self._view_key != key:
-            self.last_view = DispatchView(self, raw)
-            self._view_key = key
-        return self.last_view
+        return self._view(raw)
+
+    def _view(self, raw) -> DispatchView:
+        # The views depend only on (m, token stride, format) and on which of
+        # the two count regions holds this call's local-expert counts: reuse
+        # them across calls.
+        key = (raw.plane_stride, raw.token_stride, raw.recv_format, raw.local_expert_counts)
+        view = self._views.get(key)
+        if view is None:
+            view = self._views[key] = DispatchView(self, raw)
+        self.last_view = view
+        return view
 
     def dispatch_varlen(self, topk_ids, topk_w, x, tokens_per_rank, stream=None) -> DispatchView:
         """Per-rank token counts: inputs [R, m, ...], rows t < tokens_per_rank[s]."""
@@ -432,11 +438,7 @@ class MoeA2A:
                                       list(tokens_per_rank), m, self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_dispatch_varlen")
-        key = (raw.plane_stride, raw.token_stride, raw.recv_format)
-        if self.last_view is None or self._view_key != key:
-            self.last_view = DispatchView(self, raw)
-            self._view_key = key
-        return self.last_view
+        return self._view(raw)
 
     def set_active_ranks(self, active: int):
         """Bit d set = logical rank d alive (default: all)."""

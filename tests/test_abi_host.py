@@ -246,15 +246,17 @@ def _regions_total(sizes):
 def test_workspace_is_the_documented_regions(abi, R, M, H, E, K):
     # The rank layout's regions, each 256-byte aligned, in the order the
     # design notes list them: receive rows, combine payload, metadata rows,
-    # scales, source map, counts, send table and weights, top-k slot ranks,
+    # scales, source map, counts (two local-expert count buffers: the
+    # one-launch dispatch alternates them), send table and weights, top-k slot ranks,
     # per-tile counts and prefixes (tiles of 32 tokens, the smallest routing
     # tile), per-source tickets and expert accumulators, tile-local slots,
     # the flag word.
     RP = (R + 3) // 4 * 4
     NT = (M + 31) // 32
     rank = [R * R * M * H * 2, R * R * M * H * 2, R * R * M * K * 4, R * R * M * K * 4,
-            R * R * M * 4, R * R * M * 4, R * R * 4, E * 4, R * M * RP * 4, R * M * RP * 4,
-            R * M * K, R * NT * RP * 4, R * NT * RP * 4, R * 4, R * E * 4, R * M * RP * 4, 256]
+            R * R * M * 4, R * R * M * 4, R * R * 4, E * 4, E * 4, R * M * RP * 4,
+            R * M * RP * 4, R * M * K, R * NT * RP * 4, R * NT * RP * 4, R * 4, R * E * 4,
+            R * M * RP * 4, 256]
     c = abi.config(R, M, H, E, K)
     assert abi.moe_a2a_workspace_bytes(c) == _regions_total(rank)
     # Expert layout: per-expert planes of cap = R * M rows, send table of KP

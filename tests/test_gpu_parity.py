@@ -59,6 +59,31 @@ def test_route_overlap_modes(monkeypatch, overlap):
     parity.Case(w).run(seed=11)
 
 
+@pytest.mark.parametrize("small_max", ["-1", "0"])
+@pytest.mark.parametrize("T", [1, 33, 64, 256])
+def test_one_launch_dispatch_modes(monkeypatch, small_max, T):
+    # Batches of at most one 256-token routing tile per source: "0" (the
+    # default) dispatches in one launch, each copy warp deriving its token's
+    # slots from the ids before it; "-1" forces the two routing passes and the
+    # row copy.  Both must equal the oracle (rows chunked when tokens are few).
+    monkeypatch.setenv("MOE_DISPATCH_SMALL_MAX", small_max)
+    w = small("decode", ep_size=6, tokens_per_rank=T, max_tokens=260, runtime_max=T + 3,
+              hidden=1032, num_experts=48, top_k=5, weighted=True, fused=True)
+    parity.Case(w).run(seed=T)
+
+
+def test_one_launch_and_two_pass_dispatches_interleaved():
+    # One handle, batches alternating between the one-launch dispatch (which
+    # alternates two local-expert count buffers between calls) and the
+    # two-pass routing (T > 256): every call's counts and tables must be the
+    # oracle's.
+    w = small("decode", ep_size=4, tokens_per_rank=600, max_tokens=600, runtime_max=600,
+              hidden=256, num_experts=32, top_k=4, weighted=True, fused=True)
+    case = parity.Case(w)
+    for T in (64, 40, 600, 7, 64, 300, 33, 33):
+        case.run(T=T, seed=T)
+
+
 @pytest.mark.parametrize("K", [1, 2, 4, 8, 3])
 def test_top_k_variants(K):
     w = small("decode", ep_size=4, tokens_per_rank=77, max_tokens=80, runtime_max=80,
