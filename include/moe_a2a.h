@@ -122,7 +122,9 @@ typedef struct moe_dispatch_view {
     int32_t *src_token;           /* int32 [R][R][m]: source token of slot j */
     int32_t *recv_counts;         /* int32 [R dst][R src] */
     int32_t *local_expert_counts; /* int32 [R][Epr]: valid (token, k) entries
-                                     per local expert, over all sources */
+                                     per local expert, over all sources (one of
+                                     two workspace regions: take the pointer
+                                     from each call's view) */
     int32_t *send_slot;           /* int32 [R src][T][send_stride]: slot of
                                      token (s,t) in plane (d,s), -1 if not sent */
     float *dest_weight;           /* fp32 [R src][T][send_stride]: sum, in
@@ -270,7 +272,9 @@ int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_w
  * message per (token, rank)), assigns slots in ascending source-token order
  * within each (destination, source) plane, copies x rows and the masked
  * top-k metadata into the planes, and counts rows per plane and per local
- * expert.  Queues three kernels on `stream`.  IDLE -> DISPATCHED; returns
+ * expert.  Queues one kernel on `stream` when every source holds at most 64
+ * tokens (rank layout, bf16 rows), else three (the second on the handle's
+ * own stream, as described above).  IDLE -> DISPATCHED; returns
  * MOE_ERR_PHASE if already DISPATCHED.  If out_view is not NULL it receives
  * the views of this call. */
 int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,
