@@ -53,7 +53,6 @@ constexpr int kThreads = 6 * 32;
 constexpr int kLoaderWarp0 = 6;
 constexpr int kLoaderThreads = kBM;
 constexpr int kThreadsGather = kThreads + kLoaderThreads;
-constexpr int kGroupM = 8;        // row tiles per raster group
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000;  // 0.5 s of wall time per wait
 
 template <int BN, int STAGES>
@@ -78,14 +77,17 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
 }
 
 // Useful tiles of the call, in raster order: experts in turn; inside an
-// expert, groups of kGroupM row tiles, column tile outer and row tile inner
+// expert, groups of GM row tiles, column tile outer and row tile inner
 // within a group, so that the CTAs at work at one time share a few weight
-// tiles and a group of row tiles in L2.
+// tiles and a group of row tiles in L2 (each weight tile is read from DRAM
+// about once per group).
 struct TileMap {
     const int *first;  // [E + 1] exclusive prefix of tiles per expert (shared memory)
     int E, NT;
     const int *mtiles;  // [E] row tiles per expert (shared memory)
+    int GM;             // row tiles per raster group
     __device__ void of(int t, int &e, int &mt, int &nt) const {
+        const int kGroupM = GM;
         int lo = 0, hi = E - 1;  // last expert whose first tile is <= t
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
     }
     __syncthreads();
     const uint32_t taddr = *tmem_slot;
-    const TileMap tm{s_first, p.E, p.N / BN, s_mtiles};
+    const TileMap tm{s_first, p.E, p.N / BN, s_mtiles, p.group_m};
     const int ntiles = s_first[p.E];
     constexpr int kBK = FP8 ? kRowBytes : kRowBytes / 2;  // values of a stage row
     const int KB = p.H / kBK;
@@ -422,7 +424,7 @@ cudaError_t launch_t(const ExpertGemmParams &p, cudaStream_t st) {
 cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st) {
     const int bk = p.fp8 ? kRowBytes : kRowBytes / 2;
     if (p.H % bk != 0 || p.H < bk || p.N % 128 != 0 || p.N < 128 || p.cap < 1 ||
-        p.E > kMaxExpertsExpertLayout)
+        p.E > kMaxExpertsExpertLayout || p.group_m < 1)
         return cudaErrorInvalidValue;
     if (p.gather) {  // rank planes: bf16 rows gathered through pair_row
         if (p.fp8 || p.pair_row == nullptr) return cudaErrorInvalidValue;

@@ -53,6 +53,8 @@ struct Tuning {
     int combine_ring_slots;    // MOE_COMBINE_RING_SLOTS: 2..32
     int dispatch_small_max;    // MOE_DISPATCH_SMALL_MAX: largest T for the one-launch
                                // dispatch (0: the default, -1: never)
+    int gemm_group_m;          // MOE_GEMM_GROUP_M: row tiles per raster group of the
+                               // expert product
 };
 
 // Tile of one call: 256 tokens.  Smaller tiles (more CTAs per SM) measured
@@ -328,6 +330,7 @@ struct ExpertGemmParams {
     int gather;
     const int32_t *pair_row;
     long long a_rows;            // rows of x (gather guard)
+    int group_m;                 // row tiles per raster group
 };
 cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st);
 

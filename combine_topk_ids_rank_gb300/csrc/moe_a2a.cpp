@@ -22,6 +22,18 @@
 namespace {
 
 constexpr size_t kAlign = 256;
+// Row tiles per raster group of the expert product by default (each
+// weight tile is read from DRAM about once per group).  Measured on the
+// moe_layer product (8 experts x 8192 rows, H = N = 7168), full-size DRAM
+// bytes per launch and live TFLOP/s: 8 -> 9.83 GB, 1657; 16 -> 6.17 GB, 1761;
+// 32 -> 8.08 GB, 1724; 64 -> 13.96 GB, 1581 (the group's rows no longer stay
+// in L2 while its weight tiles pass).
+constexpr int kGemmGroupM = 16;
+
+int gemm_group_m(const moe::Tuning &tn) {
+    return tn.gemm_group_m > 0 ? tn.gemm_group_m : kGemmGroupM;
+}
+
 // Largest tokens per rank for the one-launch dispatch by default: measured
 // faster than the two routing passes + row copy up to 64 tokens per rank
 // (T = 1: 14.0 vs 16.8 us; T = 64: 18.4 vs 19.2 us, L2 flushed) and slower
@@ -142,6 +154,7 @@ moe::Tuning read_tuning() {
                                           : std::strcmp(ck, "regs") == 0 ? 2 : 0;
     tn.combine_ring_slots = env_int("MOE_COMBINE_RING_SLOTS");
     tn.dispatch_small_max = env_int("MOE_DISPATCH_SMALL_MAX");
+    tn.gemm_group_m = env_int("MOE_GEMM_GROUP_M");
     return tn;
 }
 
@@ -820,6 +833,7 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
     gp.gather = 0;
     gp.pair_row = nullptr;
     gp.a_rows = 0;
+    gp.group_m = gemm_group_m(h->tuning);
     return moe::launch_expert_gemm(gp, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
@@ -911,6 +925,7 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     gp.gather = 1;
     gp.pair_row = rp.pair_row;
     gp.a_rows = (long long)R * R * m;
+    gp.group_m = gemm_group_m(h->tuning);
     if (moe::launch_expert_gemm(gp, st) != cudaSuccess) return MOE_ERR_CUDA;
     return moe::launch_rank_aggregate(rp, h->num_sms, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
