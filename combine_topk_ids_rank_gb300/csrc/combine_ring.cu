@@ -588,10 +588,10 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, in
     // About 48 KB of ring per CTA (3 rows at H=7168): the residency of
     // several CTAs per SM (several tokens in the reduce/epilogue stage at
     // once) matters more than a deep ring; measured best on the prefill
-    // shape (2-6 slots swept).  The FP8 output's longer epilogue wants one
-    // row more in flight: 64 KB (4 rows; prefill 412.4 -> 397.1 us, where
-    // 4 rows made the bf16 output slower).
-    const size_t target = out8 ? 64 * 1024 : kRingBytesTarget;
+    // shape (2-6 slots swept).  The FP8 output's longer epilogue wants rows
+    // more in flight: 80 KB (5 rows; prefill 412.4 us at 3 rows, 397.1 at 4,
+    // 393.7 at 5, where 4 rows made the bf16 output slower).
+    const size_t target = out8 ? 80 * 1024 : kRingBytesTarget;
     int s = (int)(target / ring_stride(2 * H));
     s = s < 2 ? 2 : (s > kMaxRingSlots ? kMaxRingSlots : s);
     if (tn.combine_ring_slots >= 2 && tn.combine_ring_slots <= kMaxRingSlots)
