@@ -55,6 +55,8 @@ struct Tuning {
                                // dispatch (0: the default, -1: never)
     int gemm_group_m;          // MOE_GEMM_GROUP_M: row tiles per raster group of the
                                // expert product
+    int combine_small_max;     // MOE_COMBINE_SMALL_MAX: most tokens (all sources) for the
+                               // cluster combine (0: the default, -1: never)
 };
 
 // Tile of one call: 256 tokens.  Smaller tiles (more CTAs per SM) measured
@@ -203,6 +205,20 @@ struct CombineParams {
     int ring_slots;               // shared-memory row buffers (ring kernel)
     long long tokens;             // map.first[R]
 };
+
+// Combine for small batches (combine_small.cu): each token's row split over
+// a cluster of kClusterCtas CTAs; bf16 output.
+constexpr int kClusterCtas = 4;
+constexpr int kSmallCombineMaxThreads = 256;
+struct SmallCombineShape {
+    int cluster;  // CTAs per token
+    int cols8;    // 16-byte vectors of the row per CTA
+    int vpt;      // vectors per thread (1 or 2)
+    int threads;  // per CTA
+};
+bool combine_small_shape(int H, SmallCombineShape *sh);
+cudaError_t launch_combine_small(const CombineParams &p, bool weighted, bool fused,
+                                 const SmallCombineShape &sh, cudaStream_t st);
 
 // Compatibility combine: bf16 pairwise tree over the top-k slots.
 struct CombineTreeParams {

@@ -22,6 +22,14 @@
 namespace {
 
 constexpr size_t kAlign = 256;
+// Most tokens of a call (all sources) for the cluster combine by default.
+// L2-flushed CUDA-event times against the persistent combines (fused,
+// H = 7168): 8 tokens 8.2 vs 10.2 us, 64 tokens 10.2 vs 10.2, 256 tokens
+// 18.4 vs 12.3, 512 tokens 28.6 vs 18.4: beyond a few dozen tokens its
+// CTAs run in waves, each paying the whole chain of round trips, where the
+// persistent combines overlap one token's loads with another's epilogue.
+constexpr long long kSmallCombineMaxTokens = 64;
+
 // Row tiles per raster group of the expert product by default (each
 // weight tile is read from DRAM about once per group).  Measured on the
 // moe_layer product (8 experts x 8192 rows, H = N = 7168), full-size DRAM
@@ -155,6 +163,7 @@ moe::Tuning read_tuning() {
     tn.combine_ring_slots = env_int("MOE_COMBINE_RING_SLOTS");
     tn.dispatch_small_max = env_int("MOE_DISPATCH_SMALL_MAX");
     tn.gemm_group_m = env_int("MOE_GEMM_GROUP_M");
+    tn.combine_small_max = env_int("MOE_COMBINE_SMALL_MAX");
     return tn;
 }
 
@@ -183,6 +192,8 @@ struct moe_a2a {
     int fp8_stages;  // FP8 dispatch ring depth and shape (H % 16 == 0 only)
     moe::LaunchShape fp8_shape;
     moe::DispatchSmallShapes small;  // one-launch dispatch (rank layout)
+    moe::SmallCombineShape small_combine;  // cluster combine for small batches
+    bool small_combine_ok;
     // Local-expert counts: the region holding the current dispatch's counts,
     // and for the one-launch dispatch the buffer (0: local_counts, 1:
     // local_counts2) its next call adds into, and whether that one is zero.
@@ -233,6 +244,7 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     h->overlap = h->L.layout == MOE_LAYOUT_RANK && h->tuning.route_overlap != 0;
+    h->small_combine_ok = moe::combine_small_shape(h->cfg.hidden, &h->small_combine);
     if (h->overlap) {  // each object once, also after a partial failure
         if (h->side == nullptr &&
             cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
@@ -331,6 +343,14 @@ bool small_dispatch(const moe_a2a_t *h, const moe::TokenMap &map) {
     const int lim = h->tuning.dispatch_small_max;
     const int T_max = lim < 0 ? 0 : (lim == 0 ? kSmallDispatchMaxT : lim);
     return map.stride >= 1 && map.stride <= T_max && map.stride <= moe::kRouteTile;
+}
+
+// The cluster combine (combine_small.cu) serves bf16 outputs of calls with
+// at most Tuning::combine_small_max tokens (all sources).
+bool small_combine(const moe_a2a_t *h, long long ntok) {
+    const int lim = h->tuning.combine_small_max;
+    const long long most = lim < 0 ? 0 : (lim == 0 ? kSmallCombineMaxTokens : lim);
+    return h->small_combine_ok && ntok <= most;
 }
 
 // The dispatch phase for the tokens described by `map` (rows of stride
@@ -580,6 +600,30 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
         while (tp.P < tp.K) tp.P *= 2;
         tp.tokens = h->ntok;
         if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    } else if (h->ntok > 0 && !out8 && small_combine(h, h->ntok)) {
+        // few tokens: each row split over a cluster, all its messages in flight
+        moe::CombineParams cp;
+        cp.expert_out = static_cast<const uint16_t *>(eo);
+        cp.send_slot = at<int32_t>(h, h->L.send_slot);
+        cp.dest_weight = at<float>(h, h->L.dest_weight);
+        cp.residual = static_cast<const uint16_t *>(d_residual);
+        cp.gamma = static_cast<const uint16_t *>(d_gamma);
+        cp.out = static_cast<uint16_t *>(d_out);
+        cp.residual_out = static_cast<uint16_t *>(d_residual_out);
+        cp.out8 = nullptr;
+        cp.out_scale = nullptr;
+        cp.eps = eps;
+        cp.flags = at<uint32_t>(h, h->L.flags);
+        cp.map = h->map;
+        cp.active = h->active;
+        cp.dest = dest_rows(h, h->m);
+        cp.R = h->cfg.ep_size, cp.RP = h->L.RP, cp.m = h->m;
+        cp.H = h->cfg.hidden, cp.H8 = h->cfg.hidden / 8;
+        cp.tokens = h->ntok;
+        cp.ring_slots = 0;
+        if (moe::launch_combine_small(cp, weighted != 0, fused, h->small_combine, st) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
     } else if (h->ntok > 0) {
         const int variant = (out8 ? 4 : 0) + (weighted ? 2 : 0) + (fused ? 1 : 0);
         if (!h->combine_ready[variant]) {

@@ -72,6 +72,23 @@ def test_one_launch_dispatch_modes(monkeypatch, small_max, T):
     parity.Case(w).run(seed=T)
 
 
+@pytest.mark.parametrize("small_max", ["-1", "4096"])
+@pytest.mark.parametrize("R,T,H,E,K,weighted,fused", [
+    (6, 33, 136, 48, 5, True, True), (6, 33, 136, 48, 5, False, False),
+    (8, 64, 7168, 256, 8, True, True), (4, 20, 16384, 16, 4, True, True),
+    (32, 8, 64, 256, 32, False, True), (8, 128, 1032, 64, 8, True, False)])
+def test_cluster_combine_modes(monkeypatch, small_max, R, T, H, E, K, weighted, fused):
+    # "4096" combines each token of these calls on a cluster of CTAs, each
+    # owning a column slice, the fused sum of squares exchanged through
+    # distributed shared memory (the default does so up to 64 tokens); "-1"
+    # forces the persistent combines.  Both must equal the oracle (ragged
+    # slices at H = 136, two vectors per thread at H = 16384, 32 ranks).
+    monkeypatch.setenv("MOE_COMBINE_SMALL_MAX", small_max)
+    w = small("decode", ep_size=R, tokens_per_rank=T, max_tokens=T, runtime_max=T, hidden=H,
+              num_experts=E, top_k=K, weighted=weighted, fused=fused)
+    parity.Case(w).run(seed=T + H)
+
+
 def test_one_launch_and_two_pass_dispatches_interleaved():
     # One handle, batches alternating between the one-launch dispatch (which
     # alternates two local-expert count buffers between calls) and the
