@@ -252,10 +252,10 @@ cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStrea
     if (grid > p.tokens) grid = p.tokens;
     if (grid < 1) return cudaSuccess;
     if (p.dest.expert)
-        combine_kernel<VPT, G, W, F, true><<<(unsigned)grid, shape.block, 0, st>>>(p);
-    else
-        combine_kernel<VPT, G, W, F, false><<<(unsigned)grid, shape.block, 0, st>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<VPT, G, W, F, true>, dim3((unsigned)grid),
+                          dim3(shape.block), 0, st, p);
+    return launch_pdl(combine_kernel<VPT, G, W, F, false>, dim3((unsigned)grid),
+                      dim3(shape.block), 0, st, p);
 }
 
 // Rows in flight per group: 8 while a thread holds at most 2 vectors of a

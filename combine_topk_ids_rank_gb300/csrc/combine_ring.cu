@@ -520,8 +520,8 @@ cudaError_t launch_t(const CombineParams &p, const LaunchShape &shape, cudaStrea
     long long grid = shape.grid;
     if (grid > p.tokens) grid = p.tokens;
     if (grid < 1) return cudaSuccess;
-    ring_kernel<VPT, W, F, O>()<<<(unsigned)grid, shape.block, shape.smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(ring_kernel<VPT, W, F, O>(), dim3((unsigned)grid), dim3(shape.block),
+                      shape.smem, st, p);
 }
 
 // One of three actions on the instantiation selected by (vpt, w, f, o):

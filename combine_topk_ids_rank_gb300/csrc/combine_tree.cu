@@ -157,11 +157,9 @@ cudaError_t launch_combine_tree(const CombineTreeParams &p, int num_sms, cudaStr
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
         if (err != cudaSuccess) return err;
-        combine_tree_kernel<true><<<(unsigned)grid, nt, smem, st>>>(p);
-    } else {
-        combine_tree_kernel<false><<<(unsigned)grid, nt, 0, st>>>(p);
+        return launch_pdl(combine_tree_kernel<true>, dim3((unsigned)grid), dim3(nt), smem, st, p);
     }
-    return cudaGetLastError();
+    return launch_pdl(combine_tree_kernel<false>, dim3((unsigned)grid), dim3(nt), 0, st, p);
 }
 
 }  // namespace moe

@@ -243,6 +243,26 @@ struct LaunchShape {
     size_t smem;
 };
 
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel of the stream finishes.  Only for
+// kernels that run griddepcontrol.wait before touching anything an earlier
+// kernel writes or reads.
+template <typename Kern, typename... Args>
+inline cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              const Args &...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st);
 cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pdl);
 

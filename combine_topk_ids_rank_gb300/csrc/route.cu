@@ -382,10 +382,10 @@ cudaError_t launch2d(Kern kern, const P &p, size_t smem, cudaStream_t st, bool p
 cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st) {
     const size_t smem = (size_t)(p.E > kScanChunk ? p.E : kScanChunk) * sizeof(int32_t);
     switch (p.K) {
-        case 2: return launch2d(route_count_kernel<2>, p, smem, st, false);
-        case 4: return launch2d(route_count_kernel<4>, p, smem, st, false);
-        case 8: return launch2d(route_count_kernel<8>, p, smem, st, false);
-        default: return launch2d(route_count_kernel<0>, p, smem, st, false);
+        case 2: return launch2d(route_count_kernel<2>, p, smem, st, true);
+        case 4: return launch2d(route_count_kernel<4>, p, smem, st, true);
+        case 8: return launch2d(route_count_kernel<8>, p, smem, st, true);
+        default: return launch2d(route_count_kernel<0>, p, smem, st, true);
     }
 }
 
