@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
             tm.of(t, e, mt, nt);
             int r = mt * kBM + 32 * lw + lane;
             if (r >= s_count[e]) r = s_count[e] - 1;  // rows past the count: not stored
-            long long arow = __ldg(p.pair_row + s_pbase[e] + r);
-            if (arow < 0 || arow >= p.a_rows) {  // guard: never produced by the pair lists
+            long long arow = __ldg(p.pair_row + s_pbase[e] + r) & 0x7fffffff;  // (bit 31: a flag)
+            if (arow >= p.a_rows) {  // guard: never produced by the pair lists
                 atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
                 arow = 0;
             }
@@ -312,8 +312,25 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
             // FP8 operands: y = acc * sx[row] * sw[column], two fp32 products
             const float sx = (FP8 && live) ? p.x_scale[(long long)e * p.cap + r] : 1.0f;
             const float *swr = FP8 ? p.w_scale + (long long)e * p.N + (long long)nt * BN : nullptr;
-            const long long orow = GATHER ? (long long)s_pbase[e] + r : (long long)e * p.cap + r;
-            __nv_bfloat16 *dst_row = out + orow * p.N + (long long)nt * BN;
+            long long orow = GATHER ? (long long)s_pbase[e] + r : (long long)e * p.cap + r;
+            // Rank planes: a row whose only local expert this is gets its
+            // final message here, bf16(+0 + g * bf16(y)), in the caller's
+            // output; the others' bf16 outputs go to the pair-major buffer.
+            float gate = 0.0f;
+            bool direct = false;
+            if constexpr (GATHER) {
+                if (live) {
+                    const int32_t pr = __ldg(p.pair_row + orow);
+                    direct = pr < 0;  // bit 31: the row's only local expert
+                    if (direct) {
+                        gate = __ldg(p.pair_gate + orow);
+                        orow = pr & 0x7fffffff;
+                    }
+                }
+            }
+            __nv_bfloat16 *dst_row =
+                (direct ? reinterpret_cast<__nv_bfloat16 *>(p.final_out) : out) + orow * p.N +
+                (long long)nt * BN;
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
                 tc::ld_32x32(taddr + b * BN + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
@@ -323,6 +340,13 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         v[i] = __float_as_uint(
                             __fmul_rn(__fmul_rn(__uint_as_float(v[i]), sx), __ldg(swr + c0 + i)));
+                }
+                if (GATHER && direct) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float y = __bfloat162float(__float2bfloat16_rn(__uint_as_float(v[i])));
+                        v[i] = __float_as_uint(__fadd_rn(0.0f, __fmul_rn(gate, y)));
+                    }
                 }
                 if (live) {
                     uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c0);

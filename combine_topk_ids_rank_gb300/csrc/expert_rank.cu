@@ -22,10 +22,14 @@
 //     index of (row, k) (what the sum reads).  The order of pairs inside an
 //     expert is not fixed; every pair's product is the same whatever its
 //     place in a tile, and the sum runs over k in a fixed order.
-//   * rank_aggregate: one thread per 16-byte vector of an output row; the
-//     row's pairs are taken in ascending k, their bf16 outputs widened and
-//     summed in fp32 registers, the message stored as bf16.  An HBM stream:
-//     pairs x N x 2 bytes read, rows x N x 2 bytes written.
+//   * rows with one local expert (one pair) get their message straight from
+//     the product's epilogue, bf16(+0 + g * bf16(y)) -- the same arithmetic
+//     (rank_pairs marks such a pair with bit 31 of its row and keeps its gate).
+//   * rank_aggregate: for the rows with several local experts, one thread
+//     per 16-byte vector of an output row; the row's pairs are taken in
+//     ascending k, their bf16 outputs widened and summed in fp32 registers,
+//     the message stored as bf16.  An HBM stream: those pairs x N x 2 bytes
+//     read, those rows x N x 2 bytes written.
 #include "kernels.h"
 
 #include "moe_a2a.h"
@@ -86,6 +90,9 @@ __global__ void __launch_bounds__(kPairThreads) rank_pairs_kernel(const RankPair
             const int j = (int)(row - plane * p.m);
             live = j < __ldg(p.recv_counts + plane);
         }
+        int n_local = 0;  // a row with one local expert gets its message from the product
+        if (live)
+            for (int k = 0; k < p.K; ++k) n_local += __ldg(p.recv_ids + row * p.K + k) >= 0;
         for (int k = 0; k < p.K; ++k) {
             const int e = live ? __ldg(p.recv_ids + row * p.K + k) : -1;
             const uint32_t want = __ballot_sync(kFull, e >= 0);
@@ -100,7 +107,10 @@ __global__ void __launch_bounds__(kPairThreads) rank_pairs_kernel(const RankPair
                     got = __shfl_sync(same, got, leader);
                     pos = pbase[e] + got + __popc(same & lt);
                     if (pos < pbase[e + 1]) {
-                        p.pair_row[pos] = (int32_t)row;
+                        p.pair_row[pos] = (int32_t)((uint32_t)row | (n_local == 1 ? 0x80000000u : 0u));
+                        if (n_local == 1)
+                            p.pair_gate[pos] = p.apply_gates ? __ldg(p.recv_w + row * p.K + k)
+                                                             : 1.0f;
                     } else {  // guard: more pairs than the dispatch counted
                         atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);
                         pos = -1;
@@ -132,6 +142,9 @@ __global__ void __launch_bounds__(kAggThreads) rank_aggregate_kernel(const RankP
         const long long plane = row / p.m;
         const int j = (int)(row - plane * p.m);
         if (j >= __ldg(p.recv_counts + plane)) continue;  // padding: never written
+        int n_local = 0;  // rows with one local expert: written by the product
+        for (int k = 0; k < p.K; ++k) n_local += __ldg(p.pair_of + row * p.K + k) >= 0;
+        if (n_local == 1) continue;
         float a[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) a[i] = 0.0f;

@@ -364,7 +364,10 @@ struct ExpertGemmParams {
     // row of each pair (expert-major, pbase[e] = prefix of the counts) and
     // out is pair-major [pairs][N].
     int gather;
-    const int32_t *pair_row;
+    const int32_t *pair_row;     // [pairs]: receive row; bit 31 set when it is the row's
+                                 // only local expert (its message is written here)
+    const float *pair_gate;      // [pairs]: the gate of such a row's expert
+    void *final_out;             // bf16 [rows][N]: messages of single-expert rows
     long long a_rows;            // rows of x (gather guard)
     int group_m;                 // row tiles per raster group
 };
@@ -378,7 +381,9 @@ struct RankPairsParams {
     const int32_t *recv_counts;  // [R][R]
     const int32_t *pair_counts;  // [E]: local_expert_counts of the dispatch
     int32_t *cursor;             // [E], zero on entry
-    int32_t *pair_row;           // [pairs]: receive row of each pair, expert-major
+    int32_t *pair_row;           // [pairs]: receive row of each pair, expert-major; bit
+                                 // 31 set when it is the row's only local expert
+    float *pair_gate;            // [pairs]: the gate of such a row's expert
     int32_t *pair_of;            // [R][R][m][K]: pair of (row, k), -1 if none
     const uint16_t *y;           // [pairs][N] bf16 expert outputs
     uint16_t *out;               // [R][R][m][N] bf16 messages

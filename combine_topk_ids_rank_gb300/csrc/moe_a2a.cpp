@@ -876,6 +876,8 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
     gp.fp8 = fp8 ? 1 : 0;
     gp.gather = 0;
     gp.pair_row = nullptr;
+    gp.pair_gate = nullptr;
+    gp.final_out = nullptr;
     gp.a_rows = 0;
     gp.group_m = gemm_group_m(h->tuning);
     return moe::launch_expert_gemm(gp, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -884,10 +886,10 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
 }
 
 // Scratch of the rank-plane product, sized for max_tokens_per_rank: the
-// per-expert pair cursors, the receive row of each pair, the pair of each
-// (row, k) and the experts' bf16 outputs, pair-major.
+// per-expert pair cursors, the receive row and gate mark of each pair, the
+// pair of each (row, k) and the experts' bf16 outputs, pair-major.
 struct RankScratch {
-    size_t cursor, pair_row, pair_of, y, total;
+    size_t cursor, pair_row, pair_gate, pair_of, y, total;
 };
 
 bool rank_scratch_layout(const moe_a2a_config_t *c, int N, RankScratch *S) {
@@ -902,6 +904,7 @@ bool rank_scratch_layout(const moe_a2a_config_t *c, int N, RankScratch *S) {
     };
     S->cursor = take(E * 4);
     S->pair_row = take(pairs * 4);
+    S->pair_gate = take(pairs * 4);
     S->pair_of = take(R * R * M * K * 4);
     S->y = take(pairs * (size_t)N * 2);
     S->total = off;
@@ -928,6 +931,7 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     if (d_out == nullptr && N != H) return MOE_ERR_INVALID_ARG;
     if (d_out != nullptr && !aligned(d_out, 16)) return MOE_ERR_INVALID_ARG;
     if (d_scratch == nullptr || !aligned(d_scratch, kAlign)) return MOE_ERR_INVALID_ARG;
+    if ((long long)R * R * h->m >= (1LL << 31)) return MOE_ERR_INVALID_ARG;  // 31-bit rows
     RankScratch S;
     if (!rank_scratch_layout(&h->cfg, N, &S)) return MOE_ERR_INVALID_ARG;
     if (scratch_bytes < S.total) return MOE_ERR_CAPACITY;
@@ -943,6 +947,7 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     rp.pair_counts = at<int32_t>(h, h->cur_counts);
     rp.cursor = reinterpret_cast<int32_t *>(sc + S.cursor);
     rp.pair_row = reinterpret_cast<int32_t *>(sc + S.pair_row);
+    rp.pair_gate = reinterpret_cast<float *>(sc + S.pair_gate);
     rp.pair_of = reinterpret_cast<int32_t *>(sc + S.pair_of);
     rp.y = reinterpret_cast<const uint16_t *>(sc + S.y);
     rp.out = static_cast<uint16_t *>(d_out != nullptr ? d_out : h->ws + h->L.expert_out);
@@ -968,6 +973,8 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     gp.fp8 = 0;
     gp.gather = 1;
     gp.pair_row = rp.pair_row;
+    gp.pair_gate = rp.pair_gate;
+    gp.final_out = rp.out;
     gp.a_rows = (long long)R * R * m;
     gp.group_m = gemm_group_m(h->tuning);
     if (moe::launch_expert_gemm(gp, st) != cudaSuccess) return MOE_ERR_CUDA;

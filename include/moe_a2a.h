@@ -237,7 +237,8 @@ int moe_expert_gemm_fp8(moe_a2a_t *h, const void *d_w8, const float *d_w_scale, 
  *            aligned (pair lists and the experts' bf16 outputs; contents
  *            need not be initialised, and are garbage afterwards).
  * Requires the rank layout and the bf16 receive format (MOE_ERR_INVALID_ARG
- * otherwise), a pending dispatch (MOE_ERR_PHASE); the phase does not change.
+ * otherwise), R * R * m < 2^31, a pending dispatch (MOE_ERR_PHASE); the
+ * phase does not change.
  * MOE_ERR_CAPACITY if scratch_bytes is too small.  Queues a memset and three
  * kernels on `stream` (pair lists, the gathered tcgen05 product, the gated
  * sum per row). */

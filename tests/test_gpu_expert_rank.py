@@ -104,10 +104,14 @@ def check(got, d, w_dev, apply_gates, rows):
 @pytest.mark.parametrize("R,T,H,E,K,N,gates", [(2, 64, 128, 4, 2, 128, True),
                                                (3, 50, 192, 6, 3, 384, False),
                                                (4, 100, 256, 16, 4, 512, True),
-                                               (4, 300, 256, 8, 8, 256, True)])
+                                               (4, 300, 256, 8, 8, 256, True),
+                                               (4, 300, 256, 4, 2, 256, True),
+                                               (4, 300, 256, 4, 2, 256, False)])
 def test_expert_gemm_rank_small(R, T, H, E, K, N, gates):
     # one and several row tiles per expert, 128- and 256-wide column tiles,
-    # rows carrying one to K local experts, every row compared
+    # rows carrying one to K local experts (with one expert per rank every
+    # row carries one: its message comes straight from the product's
+    # epilogue), every row compared
     a, view, d = dispatched(R, T, H, E, K, seed=R * 10 + K)
     m = view.plane_stride
     wb = weights(7, E, N, H, 1.0 / np.sqrt(H))
