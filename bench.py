@@ -523,8 +523,11 @@ def run_gpu(args, w, rank, world, local_rank):
         "dispatch": {"ms_avg": d_avg, "ms_p50": pct(disp_ms, 0.5), "ms_p10": pct(disp_ms, 0.1),
                      "ms_p90": pct(disp_ms, 0.9), "bytes": d_bytes,
                      "gbs": d_bytes / d_avg / 1e6, "frac": d_bytes / d_avg / 1e6 / peak,
-                     "kernels": ["route_count", "route_scan",
-                                 "dispatch_fp8" if fp8 else "dispatch_rows"]},
+                     "kernels": (["dispatch_small"] if view.kernels == 1 else
+                                 ["route_e_count", "route_e_scan"] if args.layout == "expert"
+                                 else ["route_count", "route_scan"]) +
+                                ([] if view.kernels == 1 else
+                                 ["dispatch_fp8" if fp8 else "dispatch_rows"])},
         **({"expert_gemm": {
             "ms_avg": statistics.fmean(gemm_ms), "ms_p50": pct(gemm_ms, 0.5),
             "ms_p10": pct(gemm_ms, 0.1), "ms_p90": pct(gemm_ms, 0.9),
@@ -536,7 +539,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
                     "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
                     "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
-                    "kernels": ["combine"]},
+                    "kernels": ["combine_small" if N <= 64 and not fp8 else "combine"]},
     }
     eff_gbs = (d_bytes + c_bytes) / ms_per_step / 1e6
 
@@ -680,7 +683,10 @@ def run_gpu(args, w, rank, world, local_rank):
                      "peak": peak, "unit": "GB/s", "frac": c_bytes / c_avg / 1e6 / peak,
                      "traffic": traffic, "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)"
                      % peak_kind if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "gpu_launches": (4 + (3 if gemm_rank else 1 if gemm else 0)) * args.steps
+        # the library's own kernels per step: what the dispatch reports it
+        # queued (one launch for small batches, else three), the combine,
+        # and the product's (three on the rank planes, one otherwise)
+        "gpu_launches": (view.kernels + 1 + (3 if gemm_rank else 1 if gemm else 0)) * args.steps
                         if T > 0 else 0,
         "launch": "CUDA-graph replay of each phase's C-ABI call" if args.graph
                   else "direct C-ABI calls",

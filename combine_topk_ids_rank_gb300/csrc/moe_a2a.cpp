@@ -527,7 +527,8 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         }
     }
 
-    if (ntok == 0 || !small_dispatch(h, map)) {
+    const bool one_launch = ntok > 0 && small_dispatch(h, map);
+    if (!one_launch) {
         // the routing pass (or the empty call) wrote local_counts
         h->cur_counts = h->L.local_counts;
         if (h->small_sel == 0) h->small_zero_ok = false;
@@ -553,6 +554,9 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         out_view->recv_scale = fp8 ? at<float>(h, h->L.recv_scale) : nullptr;
         out_view->recv_format = h->recv_format;
         out_view->layout = h->L.layout;
+        // route_count + route_scan (or the expert layout's two passes) + the
+        // row copy, or the one-launch dispatch
+        out_view->kernels = ntok == 0 ? 0 : (one_launch ? 1 : 3);
     }
     return MOE_OK;
 }

@@ -58,7 +58,7 @@ class MoeDispatchView(ctypes.Structure):
                 ("plane_stride", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int32),
                 ("send_stride", ctypes.c_int32), ("token_stride", ctypes.c_int32),
                 ("recv_scale", ctypes.c_void_p), ("recv_format", ctypes.c_int32),
-                ("layout", ctypes.c_int32)]
+                ("layout", ctypes.c_int32), ("kernels", ctypes.c_int32)]
 
 
 class MoeA2AError(RuntimeError):
@@ -332,6 +332,7 @@ class DispatchView:
         self.plane_stride, self.send_stride = m, RP
         self.tokens_per_rank, self.token_stride = raw.tokens_per_rank, T
         self.recv_format, self.layout = raw.recv_format, raw.layout
+        self.kernels = raw.kernels
         # planes: (dst rank, src rank) of m rows, or (expert) of cap = m rows
         planes = (E,) if raw.layout == MOE_LAYOUT_EXPERT else (R, R)
         if raw.recv_format == MOE_FORMAT_FP8_E4M3:

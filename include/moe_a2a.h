@@ -141,6 +141,8 @@ typedef struct moe_dispatch_view {
                                      in the expert layout), else NULL */
     int32_t recv_format;          /* MOE_FORMAT_* of recv_x */
     int32_t layout;               /* MOE_LAYOUT_* of the handle */
+    int32_t kernels;              /* kernels this dispatch queued (0 for an
+                                     empty call: memsets only) */
 } moe_dispatch_view_t;
 
 /* Bytes of device workspace a handle with this config needs (0 if the
