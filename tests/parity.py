@@ -99,6 +99,7 @@ class Case:
         torch.cuda.synchronize()
         st, flags = a.get_error()
         assert st == 0 and flags == 0, (st, flags)
+        rep["kernels"] = view.kernels
 
         counts = view.recv_counts.cpu().numpy()
         assert np.array_equal(counts, r["recv_counts"]), "recv_counts"

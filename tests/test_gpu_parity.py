@@ -69,7 +69,8 @@ def test_one_launch_dispatch_modes(monkeypatch, small_max, T):
     monkeypatch.setenv("MOE_DISPATCH_SMALL_MAX", small_max)
     w = small("decode", ep_size=6, tokens_per_rank=T, max_tokens=260, runtime_max=T + 3,
               hidden=1032, num_experts=48, top_k=5, weighted=True, fused=True)
-    parity.Case(w).run(seed=T)
+    rep = parity.Case(w).run(seed=T)
+    assert rep["kernels"] == (1 if small_max == "0" and T <= 64 else 3)
 
 
 @pytest.mark.parametrize("small_max", ["-1", "4096"])
