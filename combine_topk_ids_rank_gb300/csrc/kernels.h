@@ -1,5 +1,6 @@
-// kernels.h -- parameter blocks and host launchers of the four kernels of
-// the dispatch / combine path.  Internal to libmoe_a2a.so.
+// kernels.h -- parameter blocks and host launchers of the kernels of the
+// dispatch / combine path and the expert-side products.  Internal to
+// libmoe_a2a.so.
 #pragma once
 
 #include <cstddef>
