@@ -33,6 +33,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of GB300 peak), 1 GPU"
+# Sets of device input / output buffers the end-to-end leg rotates through.
+E2E_BUFFERS = 3
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -50,6 +52,8 @@ def parse_args():
                          "cases); default: the workload's max_tokens_per_rank")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--e2e-buffers", type=int, default=E2E_BUFFERS,
+                    help="input / output buffer sets the end-to-end leg rotates through")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -545,9 +549,11 @@ def run_gpu(args, w, rank, world, local_rank):
 
     # ---- end to end through the public API, host buffers ----
     # Every step copies its inputs (ids, weights, x, residual) from pinned
-    # host memory and its outputs (y, residual_out) back.  Double-buffered on
-    # three streams: step i+1's inputs go up and step i-1's outputs come down
-    # while step i runs dispatch + combine on the compute stream.
+    # host memory and its outputs (y, residual_out) back, on three streams:
+    # later steps' inputs go up and earlier steps' outputs come down while
+    # step i runs dispatch + combine on the compute stream.  The steps rotate
+    # through NB buffer sets, so a step's copies wait only for the step NB
+    # before it.
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.pin_memory()
@@ -558,22 +564,23 @@ def run_gpu(args, w, rank, world, local_rank):
             [((R, T, H), torch.bfloat16)]
         if w.fused:
             specs.append(((R, T, H), torch.bfloat16))
-        hout = [[torch.empty(sh, dtype=dt).pin_memory() for sh, dt in specs] for _ in range(2)]
-        din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(2)]
-        dout = [[torch.empty(sh, dtype=dt, device=dev) for sh, dt in specs] for _ in range(2)]
+        NB = max(2, args.e2e_buffers)
+        hout = [[torch.empty(sh, dtype=dt).pin_memory() for sh, dt in specs] for _ in range(NB)]
+        din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(NB)]
+        dout = [[torch.empty(sh, dtype=dt, device=dev) for sh, dt in specs] for _ in range(NB)]
         h2d = sum(t.numel() * t.element_size() for t in hin)
         d2h = sum(t.numel() * t.element_size() for t in hout[0])
         compute = torch.cuda.current_stream(dev)
         up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()
-        in_ready, in_free = [ev(), ev()], [ev(), ev()]
-        out_ready, out_free = [ev(), ev()], [ev(), ev()]
-        for b in range(2):
+        in_ready, in_free = [ev() for _ in range(NB)], [ev() for _ in range(NB)]
+        out_ready, out_free = [ev() for _ in range(NB)], [ev() for _ in range(NB)]
+        for b in range(NB):
             in_free[b].record(compute)
             out_free[b].record(compute)
 
         def e2e_step(i):
-            b = i & 1
+            b = i % NB
             with torch.cuda.stream(up):
                 up.wait_event(in_free[b])
                 for dst, src in zip(din[b], hin):
@@ -632,7 +639,7 @@ def run_gpu(args, w, rank, world, local_rank):
             up.wait_event(c0)
             down.wait_event(c0)
             for i in range(reps):
-                b = i & 1
+                b = i % NB
                 with torch.cuda.stream(up):
                     for dst, src in zip(din[b], hin):
                         dst.copy_(src, non_blocking=True)
@@ -655,8 +662,8 @@ def run_gpu(args, w, rank, world, local_rank):
                "frac_of_copy_bound": copy_ms / (e2e_ms / args.e2e_steps),
                "path": "pinned host -> device copies on a copy stream, moe_dispatch + "
                        "moe_combine on the compute stream, device -> pinned host copies on a "
-                       "third stream; double-buffered so one step's inputs and another's "
-                       "outputs move while a step computes"}
+                       "third stream; %d buffer sets in rotation so one step's inputs and another's "
+                       "outputs move while a step computes" % NB}
 
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
