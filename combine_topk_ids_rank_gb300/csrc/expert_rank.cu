@@ -25,11 +25,13 @@
 //   * rows with one local expert (one pair) get their message straight from
 //     the product's epilogue, bf16(+0 + g * bf16(y)) -- the same arithmetic
 //     (rank_pairs marks such a pair with bit 31 of its row and keeps its gate).
-//   * rank_aggregate: for the rows with several local experts, one thread
-//     per 16-byte vector of an output row; the row's pairs are taken in
+//   * rank_pairs also lists the rows with several local experts (one
+//     atomic per warp), so that the sum touches those rows only.
+//   * rank_aggregate: one CTA per listed row at a time, each thread a few
+//     16-byte vectors of the output row; the row's pairs are taken in
 //     ascending k, their bf16 outputs widened and summed in fp32 registers,
 //     the message stored as bf16.  An HBM stream: those pairs x N x 2 bytes
-//     read, those rows x N x 2 bytes written.
+//     read, those rows x N x 2 bytes written; nothing else is read.
 #include "kernels.h"
 
 #include "moe_a2a.h"
@@ -41,7 +43,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kPairThreads = 256;
-constexpr int kAggThreads = 256;
+constexpr int kAggThreads = 128;  // threads on one output row
+constexpr int kAggVec = 4;        // 16-byte vectors a thread has in flight per pair
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -93,6 +96,19 @@ __global__ void __launch_bounds__(kPairThreads) rank_pairs_kernel(const RankPair
         int n_local = 0;  // a row with one local expert gets its message from the product
         if (live)
             for (int k = 0; k < p.K; ++k) n_local += __ldg(p.recv_ids + row * p.K + k) >= 0;
+        {  // rows with several local experts: on the list the gated sum walks
+            const uint32_t many = __ballot_sync(kFull, n_local >= 2);
+            if (many != 0) {
+                const int leader = __ffs(many) - 1;
+                int at = 0;
+                if ((int)(threadIdx.x & 31) == leader) at = atomicAdd(p.cursor + p.E, __popc(many));
+                at = __shfl_sync(kFull, at, leader) + __popc(many & lt);
+                if (n_local >= 2) {
+                    if (at < p.multi_cap) p.multi[at] = (int32_t)row;
+                    else atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_SLOT);  // guard: never expected
+                }
+            }
+        }
         for (int k = 0; k < p.K; ++k) {
             const int e = live ? __ldg(p.recv_ids + row * p.K + k) : -1;
             const uint32_t want = __ballot_sync(kFull, e >= 0);
@@ -132,37 +148,63 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kAggThreads) rank_aggregate_kernel(const RankPairsParams p) {
     const int N8 = p.N / 8;
-    const long long units = (long long)p.R * p.R * p.m * N8;
     const uint4 *y = reinterpret_cast<const uint4 *>(p.y);
     uint4 *out = reinterpret_cast<uint4 *>(p.out);
-    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
-         u += (long long)gridDim.x * blockDim.x) {
-        const long long row = u / N8;
-        const int c = (int)(u - row * N8);
-        const long long plane = row / p.m;
-        const int j = (int)(row - plane * p.m);
-        if (j >= __ldg(p.recv_counts + plane)) continue;  // padding: never written
-        int n_local = 0;  // rows with one local expert: written by the product
-        for (int k = 0; k < p.K; ++k) n_local += __ldg(p.pair_of + row * p.K + k) >= 0;
-        if (n_local == 1) continue;
-        float a[8];
+    __shared__ int s_pr[kMaxTopK];  // the row's pairs in ascending k
+    __shared__ float s_g[kMaxTopK];  // and their gates
+    __shared__ int s_n;
+    long long rows = __ldg(p.cursor + p.E);
+    if (rows > p.multi_cap) rows = p.multi_cap;  // (flagged by rank_pairs)
+    for (long long i = blockIdx.x; i < rows; i += gridDim.x) {
+        const long long row = __ldg(p.multi + i);
+        if (threadIdx.x < 32) {  // K <= 32: one warp compacts the local slots
+            const int k = threadIdx.x;
+            const int q = k < p.K ? __ldg(p.pair_of + row * p.K + k) : -1;
+            const uint32_t has = __ballot_sync(kFull, q >= 0);
+            if (q >= 0) {
+                const int at = __popc(has & lanemask_lt());
+                s_pr[at] = q;
+                s_g[at] = p.apply_gates ? __ldg(p.recv_w + row * p.K + k) : 1.0f;
+            }
+            if (k == 0) s_n = __popc(has);
+        }
+        __syncthreads();
+        const int n = s_n;
+        for (int c0 = threadIdx.x; c0 < N8; c0 += kAggThreads * kAggVec) {
+            float a[kAggVec][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = 0.0f;
-        for (int k = 0; k < p.K; ++k) {
-            const int pr = __ldg(p.pair_of + row * p.K + k);
-            if (pr < 0) continue;
-            const float g = p.apply_gates ? __ldg(p.recv_w + row * p.K + k) : 1.0f;
-            const uint4 v = __ldcs(y + (long long)pr * N8 + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            for (int u = 0; u < kAggVec; ++u)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[2 * i] = __fadd_rn(a[2 * i], __fmul_rn(g, lo_f(w[i])));
-                a[2 * i + 1] = __fadd_rn(a[2 * i + 1], __fmul_rn(g, hi_f(w[i])));
+                for (int e = 0; e < 8; ++e) a[u][e] = 0.0f;
+            for (int t = 0; t < n; ++t) {
+                const long long pr = s_pr[t];
+                const float g = s_g[t];
+                uint4 v[kAggVec];
+#pragma unroll
+                for (int u = 0; u < kAggVec; ++u) {
+                    const int c = c0 + u * kAggThreads;
+                    v[u] = c < N8 ? __ldcs(y + pr * N8 + c) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kAggVec; ++u) {
+                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        a[u][2 * e] = __fadd_rn(a[u][2 * e], __fmul_rn(g, lo_f(w[e])));
+                        a[u][2 * e + 1] = __fadd_rn(a[u][2 * e + 1], __fmul_rn(g, hi_f(w[e])));
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kAggVec; ++u) {
+                const int c = c0 + u * kAggThreads;
+                if (c < N8)
+                    __stcs(out + row * N8 + c,
+                           make_uint4(pack_bf16x2(a[u][0], a[u][1]), pack_bf16x2(a[u][2], a[u][3]),
+                                      pack_bf16x2(a[u][4], a[u][5]), pack_bf16x2(a[u][6], a[u][7])));
             }
         }
-        __stcs(out + row * N8 + c,
-               make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                          pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7])));
+        __syncthreads();  // the next row's pairs replace these
     }
 }
 
@@ -179,10 +221,11 @@ cudaError_t launch_rank_pairs(const RankPairsParams &p, int num_sms, cudaStream_
 }
 
 cudaError_t launch_rank_aggregate(const RankPairsParams &p, int num_sms, cudaStream_t st) {
-    if (p.N % 8 != 0) return cudaErrorInvalidValue;
-    const long long units = (long long)p.R * p.R * p.m * (p.N / 8);
-    long long grid = (units + kAggThreads - 1) / kAggThreads;
-    if (grid > 8LL * num_sms) grid = 8LL * num_sms;
+    if (p.N % 8 != 0 || p.K > kMaxTopK) return cudaErrorInvalidValue;
+    // the number of listed rows is on the device: a persistent grid, one
+    // row per CTA at a time (at most as many CTAs as the list can hold)
+    long long grid = 8LL * num_sms;
+    if (grid > p.multi_cap) grid = p.multi_cap;
     if (grid < 1) return cudaSuccess;
     rank_aggregate_kernel<<<(unsigned)grid, kAggThreads, 0, st>>>(p);
     return cudaGetLastError();

@@ -381,11 +381,15 @@ struct RankPairsParams {
     const float *recv_w;         // [R][R][m][K]
     const int32_t *recv_counts;  // [R][R]
     const int32_t *pair_counts;  // [E]: local_expert_counts of the dispatch
-    int32_t *cursor;             // [E], zero on entry
+    int32_t *cursor;             // [E + 1], zero on entry: pairs placed per expert, then
+                                 // the number of rows with several local experts
     int32_t *pair_row;           // [pairs]: receive row of each pair, expert-major; bit
                                  // 31 set when it is the row's only local expert
     float *pair_gate;            // [pairs]: the gate of such a row's expert
     int32_t *pair_of;            // [R][R][m][K]: pair of (row, k), -1 if none
+    int32_t *multi;              // [multi_cap]: the rows with several local experts
+                                 // (in no particular order; count in cursor[E])
+    long long multi_cap;
     const uint16_t *y;           // [pairs][N] bf16 expert outputs
     uint16_t *out;               // [R][R][m][N] bf16 messages
     uint32_t *flags;             // device flag word (consistency guard)

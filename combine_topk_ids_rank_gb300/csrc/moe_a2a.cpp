@@ -893,7 +893,8 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
 // per-expert pair cursors, the receive row and gate mark of each pair, the
 // pair of each (row, k) and the experts' bf16 outputs, pair-major.
 struct RankScratch {
-    size_t cursor, pair_row, pair_gate, pair_of, y, total;
+    size_t cursor, pair_row, pair_gate, pair_of, multi, y, total;
+    long long multi_cap;
 };
 
 bool rank_scratch_layout(const moe_a2a_config_t *c, int N, RankScratch *S) {
@@ -906,10 +907,13 @@ bool rank_scratch_layout(const moe_a2a_config_t *c, int N, RankScratch *S) {
         off = align_up(off + bytes, kAlign);
         return o;
     };
-    S->cursor = take(E * 4);
+    S->cursor = take((E + 1) * 4);  // + the count of rows with several local experts
     S->pair_row = take(pairs * 4);
     S->pair_gate = take(pairs * 4);
     S->pair_of = take(R * R * M * K * 4);
+    // such a row holds at least two of the pairs
+    S->multi_cap = (long long)(R * M * (K / 2));
+    S->multi = take((size_t)S->multi_cap * 4);
     S->y = take(pairs * (size_t)N * 2);
     S->total = off;
     return true;
@@ -953,12 +957,15 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     rp.pair_row = reinterpret_cast<int32_t *>(sc + S.pair_row);
     rp.pair_gate = reinterpret_cast<float *>(sc + S.pair_gate);
     rp.pair_of = reinterpret_cast<int32_t *>(sc + S.pair_of);
+    rp.multi = reinterpret_cast<int32_t *>(sc + S.multi);
+    rp.multi_cap = S.multi_cap;
     rp.y = reinterpret_cast<const uint16_t *>(sc + S.y);
     rp.out = static_cast<uint16_t *>(d_out != nullptr ? d_out : h->ws + h->L.expert_out);
     rp.flags = at<uint32_t>(h, h->L.flags);
     rp.R = R, rp.m = m, rp.K = K, rp.E = E, rp.N = N;
     rp.apply_gates = apply_gates ? 1 : 0;
-    if (cudaMemsetAsync(rp.cursor, 0, sizeof(int32_t) * E, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(rp.cursor, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (moe::launch_rank_pairs(rp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
 
     moe::ExpertGemmParams gp;

@@ -272,13 +272,20 @@ def test_workspace_is_the_documented_regions(abi, R, M, H, E, K):
 
 
 def test_expert_gemm_rank_host_checks(abi):
-    # scratch: pair cursors [E], the receive row and gate mark of each pair
-    # [R*M*K] each, the pair of each (row, k) [R*R*M*K] and the pair-major
+    # scratch: pair cursors [E] and the count of rows with several local
+    # experts, the receive row and gate mark of each pair [R*M*K] each, the
+    # pair of each (row, k) [R*R*M*K], the list of rows with several local
+    # experts [R*M*(K/2)] (each holds two pairs or more) and the pair-major
     # bf16 outputs [R*M*K][N]
     R, M, H, E, K, N = 8, 64, 256, 32, 4, 384
     c = abi.config(R, M, H, E, K)
     assert abi.moe_expert_gemm_rank_scratch_bytes(c, N) == _regions_total(
-        [E * 4, R * M * K * 4, R * M * K * 4, R * R * M * K * 4, R * M * K * N * 2])
+        [(E + 1) * 4, R * M * K * 4, R * M * K * 4, R * R * M * K * 4, R * M * (K // 2) * 4,
+         R * M * K * N * 2])
+    c3 = abi.config(R, M, H, E, 3)  # odd top-k: floor(K / 2) list entries per token
+    assert abi.moe_expert_gemm_rank_scratch_bytes(c3, N) == _regions_total(
+        [(E + 1) * 4, R * M * 3 * 4, R * M * 3 * 4, R * R * M * 3 * 4, R * M * 1 * 4,
+         R * M * 3 * N * 2])
     assert abi.moe_expert_gemm_rank_scratch_bytes(c, 100) == 0        # N % 128
     A = 1 << 20
     assert abi.moe_expert_gemm_rank(None, A, 256, 1, 0, A, 1 << 30) == abi.MOE_ERR_INVALID_ARG
