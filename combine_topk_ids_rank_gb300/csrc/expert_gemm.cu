@@ -26,6 +26,7 @@
 //     of the tile) 32 columns at a time, narrows to bf16, stores the rows
 //     below the expert's count and frees the accumulator, while the MMA
 //     thread already fills the other one.
+#include "expert.h"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"

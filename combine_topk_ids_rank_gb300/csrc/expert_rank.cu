@@ -32,6 +32,7 @@
 //     ascending k, their bf16 outputs widened and summed in fp32 registers,
 //     the message stored as bf16.  An HBM stream: those pairs x N x 2 bytes
 //     read, those rows x N x 2 bytes written; nothing else is read.
+#include "expert.h"
 #include "kernels.h"
 
 #include "moe_a2a.h"

@@ -17,6 +17,7 @@
 
 #include <cuda_runtime.h>
 
+#include "expert.h"
 #include "kernels.h"
 
 namespace {
