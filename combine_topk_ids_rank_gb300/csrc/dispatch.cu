@@ -60,18 +60,19 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
     // s * stride + t of the token arrays.
     auto unit_of = [&](long long i, int &s, long long &row, int &chunk, int &t) {
         const long long u = first + i * step;
-        const long long k = u / p.chunks;
+        // rows up to 16 KB (H <= 8192) are one chunk: no division on the
+        // issuing lane's path
+        const long long k = p.chunks == 1 ? u : u / p.chunks;
         chunk = (int)(u - k * p.chunks);
         token_of(p.map, p.R, k, s, t);
         row = (long long)s * p.map.stride + t;
     };
     // A unit's stage receives its row chunk (an input of the call) and its
     // send row (written by the routing pass); both complete on one barrier.
-    auto issue_row = [&](long long i) {
+    auto issue_row = [&](long long i, int stage) {  // stage = i mod stages
         int s, chunk, t;
         long long token;
         unit_of(i, s, token, chunk, t);
-        const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         const uint32_t bytes = unit_bytes(chunk);
         ptx::fence_proxy_async_smem();  // earlier ordinary reads of this stage
@@ -79,11 +80,10 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
         ptx::bulk_g2s(buf, p.x + token * p.row_bytes + (long long)chunk * p.chunk_bytes, bytes,
                       &bars[stage]);
     };
-    auto issue_meta = [&](long long i) {
+    auto issue_meta = [&](long long i, int stage) {
         int s, chunk, t;
         long long token;
         unit_of(i, s, token, chunk, t);
-        const int stage = (int)(i % p.stages);
         uint8_t *buf = smem + (size_t)stage * p.stage_bytes;
         ptx::bulk_g2s(buf + p.chunk_bytes, p.send_slot + token * p.dest.P, meta_bytes,
                       &bars[stage]);
@@ -92,21 +92,22 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
                           p.tile_prefix + ((long long)s * p.ntiles + t / p.tile) * p.dest.P,
                           meta_bytes, &bars[stage]);
     };
-    auto issue = [&](long long i) {
-        issue_row(i);
-        issue_meta(i);
+    auto issue = [&](long long i, int stage) {
+        issue_row(i, stage);
+        issue_meta(i, stage);
     };
 
     // The first stages' rows are in flight while the routing pass finishes.
     const long long prologue = n < p.stages ? n : p.stages;
-    for (long long i = 0; i < prologue; ++i) issue_row(i);
+    for (long long i = 0; i < prologue; ++i) issue_row(i, (int)i);
     ptx::grid_dependency_wait();  // send-slot table of the routing pass
-    for (long long i = 0; i < prologue; ++i) issue_meta(i);
+    for (long long i = 0; i < prologue; ++i) issue_meta(i, (int)i);
     long long issued = prologue;
 
+    // stage = i mod stages and the barrier parity, stepped along with i
+    int stage = 0, prev_stage = p.stages - 1;
+    uint32_t parity = 0;
     for (long long i = 0; i < n; ++i) {
-        const int stage = (int)(i % p.stages);
-        const uint32_t parity = (uint32_t)((i / p.stages) & 1);
         if (!ptx::mbar_wait_bounded(&bars[stage], parity, kWaitLimit)) {
             atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
             ptx::bulk_wait_all();
@@ -134,11 +135,17 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(const DispatchParams 
             ptx::bulk_s2g(p.recv_x + row * p.row_bytes + col, buf, bytes);
         }
         ptx::bulk_commit();
-        // Refill the stage of iteration i-1 once its stores left shared memory.
+        // Refill the stage of iteration i-1 once its stores left shared memory
+        // (issued = i - 1 + stages: that stage).
         if (i >= 1 && issued < n) {
             ptx::bulk_wait_read<1>();
-            issue(issued);
+            issue(issued, prev_stage);
             ++issued;
+        }
+        prev_stage = stage;
+        if (++stage == p.stages) {
+            stage = 0;
+            parity ^= 1u;
         }
     }
     ptx::bulk_wait_all();

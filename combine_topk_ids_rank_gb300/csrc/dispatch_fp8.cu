@@ -64,12 +64,11 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
 
     // Token k of this CTA is i = blockIdx.x + k * gridDim.x; its row goes
     // to stage k % S.  Thread 0 keeps S rows in flight.
-    auto issue = [&](long long k) {
+    auto issue = [&](long long k, int b) {  // b = k mod S
         const long long i = blockIdx.x + k * (long long)gridDim.x;
         if (i >= p.tokens) return;
         int s, t;
         token_of(p.map, p.R, i, s, t);
-        const int b = (int)(k % S);
         ptx::mbar_arrive_expect_tx(&full[b], row_bytes);
         ptx::bulk_g2s(smem + b * stride, p.x + ((long long)s * p.map.stride + t) * p.H,
                       row_bytes, &full[b]);
@@ -77,13 +76,15 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
     if (tid == 0) {
         for (int b = 0; b < S; ++b) ptx::mbar_init(&full[b], 1);
         ptx::fence_mbar_init();
-        for (int k = 0; k < S; ++k) issue(k);  // inputs: before the routing pass ends
+        for (int k = 0; k < S; ++k) issue(k, k);  // inputs: before the routing pass ends
     }
     __syncthreads();
     ptx::grid_dependency_wait();
 
     bool ok = true;
     long long k = 0;
+    int b = 0;             // k mod S, stepped with k
+    uint32_t phase = 0;    // (k / S) & 1
     for (long long i = blockIdx.x; i < p.tokens; i += gridDim.x, ++k) {
         const int par = (int)(k & 1);
         int s, t;
@@ -101,8 +102,7 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
             }
             rows[par][tid] = row;
         }
-        const int b = (int)(k % S);
-        ok = ptx::mbar_wait_bounded(&full[b], (uint32_t)((k / S) & 1), kWaitLimit);
+        ok = ptx::mbar_wait_bounded(&full[b], phase, kWaitLimit);
         uint4 cur[VPT];
         const uint4 *row = reinterpret_cast<const uint4 *>(smem + b * stride);
         float amax = 0.0f;
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
         }
         if (tid == 0) {
             ptx::fence_proxy_async_smem();
-            issue(k + S);
+            issue(k + S, b);  // the stage just released
         }
         amax = red[par][0];
         for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[par][w]);
@@ -150,6 +150,10 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_fp8_kernel(const Dispatc
                 if (c < p.H8) __stcs(dst + c, q[j]);
             }
             if (tid == 0) p.recv_scale[dst_row] = rs.s;
+        }
+        if (++b == S) {
+            b = 0;
+            phase ^= 1u;
         }
     }
     if (!ok && tid == 0) {

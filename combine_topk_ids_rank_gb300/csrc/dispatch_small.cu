@@ -37,18 +37,21 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kStages = 2;  // x chunks in flight per CTA (shared-memory stages)
 constexpr int kMaxTileWords = kRouteTile / 32;  // 32-token groups of a source
 
-__device__ __forceinline__ int live_rank(int e, int E, int Epr, uint32_t active) {
+// (magic: owner_magic(Epr), kernels.h)
+__device__ __forceinline__ int live_rank(int e, int E, unsigned long long magic,
+                                         uint32_t active) {
     if (e < 0 || e >= E) return -1;
-    const int d = e / Epr;
+    const int d = owner_of(e, magic);
     return ((active >> d) & 1u) ? d : -1;
 }
 
 // Destination mask of a token: ranks of its valid ids on active ranks.
 template <int KT>
-__device__ __forceinline__ uint32_t token_mask(const int32_t *ids, int K, int E, int Epr,
-                                               uint32_t active) {
+__device__ __forceinline__ uint32_t token_mask(const int32_t *ids, int K, int E,
+                                               unsigned long long magic, uint32_t active) {
     uint32_t mask = 0;
     if constexpr (KT > 0) {
         int e[KT];
@@ -56,12 +59,12 @@ __device__ __forceinline__ uint32_t token_mask(const int32_t *ids, int K, int E,
         for (int k = 0; k < KT; ++k) e[k] = __ldg(ids + k);
 #pragma unroll
         for (int k = 0; k < KT; ++k) {
-            const int d = live_rank(e[k], E, Epr, active);
+            const int d = live_rank(e[k], E, magic, active);
             if (d >= 0) mask |= 1u << d;
         }
     } else {
         for (int k = 0; k < K; ++k) {
-            const int d = live_rank(__ldg(ids + k), E, Epr, active);
+            const int d = live_rank(__ldg(ids + k), E, magic, active);
             if (d >= 0) mask |= 1u << d;
         }
     }
@@ -73,43 +76,46 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x;
     const int K = KT > 0 ? KT : p.K;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)p.stages * p.stage_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * p.stage_bytes);
     if (lane == 0) {
-        for (int i = 0; i < p.stages; ++i) ptx::mbar_init(&bars[i], 1);
+        for (int i = 0; i < kStages; ++i) ptx::mbar_init(&bars[i], 1);
         ptx::fence_mbar_init();
     }
     __syncwarp();
 
-    const long long first = blockIdx.x, step = gridDim.x;
-    const long long n = first < p.units ? (p.units - 1 - first) / step + 1 : 0;
+    // Units (< 2^16: at most 32 x 256 tokens x 8 chunks) in 32-bit
+    // arithmetic; divisions by chunks and T as multiply-highs.
+    const int units = (int)p.units;
+    const int first = blockIdx.x, step = gridDim.x;
+    const int n = first < units ? (units - 1 - first) / step + 1 : 0;
     auto unit_bytes = [&](int chunk) -> uint32_t {
         const int left = p.row_bytes - chunk * p.chunk_bytes;
         return (uint32_t)(left < p.chunk_bytes ? left : p.chunk_bytes);
     };
-    auto issue_x = [&](long long i) {  // lane 0: the unit's x chunk into its stage
-        const long long u = first + i * step;
-        const long long tok = u / p.chunks;
-        const int chunk = (int)(u - tok * p.chunks);
-        const int stage = (int)(i % p.stages);
+    auto issue_x = [&](int i) {  // lane 0: the unit's x chunk into its stage
+        const int u = first + i * step;
+        const int tok = div_by(u, p.chunks_magic);
+        const int chunk = u - tok * p.chunks;
+        const int stage = i & (kStages - 1);
         const uint32_t bytes = unit_bytes(chunk);
         ptx::mbar_arrive_expect_tx(&bars[stage], bytes);
         ptx::bulk_g2s(smem + (size_t)stage * p.stage_bytes,
-                      p.x + tok * p.row_bytes + (long long)chunk * p.chunk_bytes, bytes,
-                      &bars[stage]);
+                      p.x + (long long)tok * p.row_bytes + (long long)chunk * p.chunk_bytes,
+                      bytes, &bars[stage]);
     };
 
     // x is an input of the call: request the first chunks right away.
-    const long long prologue = n < p.stages ? n : p.stages;
+    const int prologue = n < kStages ? n : kStages;
     if (lane == 0)
-        for (long long i = 0; i < prologue; ++i) issue_x(i);
-    long long issued = prologue, failed = -1;
+        for (int i = 0; i < prologue; ++i) issue_x(i);
+    int issued = prologue, failed = -1;
     bool ok = true, waited = false;
 
-    for (long long i = 0; i < n && ok; ++i) {
-        const long long u = first + i * step;
-        const long long tok = u / p.chunks;          // s * T + t
-        const int chunk = (int)(u - tok * p.chunks);
-        const int s = (int)(tok / p.T), t = (int)(tok - (long long)s * p.T);
+    for (int i = 0; i < n && ok; ++i) {
+        const int u = first + i * step;
+        const int tok = div_by(u, p.chunks_magic);   // s * T + t
+        const int chunk = u - tok * p.chunks;
+        const int s = div_by(tok, p.T_magic), t = tok - s * p.T;
         const int32_t *src_ids = p.topk_ids + (size_t)s * p.T * K;
 
         // the token's own ids and weights, one per lane (K <= 32)
@@ -120,11 +126,13 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
         uint32_t masks[kMaxTileWords];
         const int words = t / 32 + 1;
 #pragma unroll
-        for (int j = 0; j < kMaxTileWords; ++j) {
+        for (int j = 0; j < kMaxTileWords; ++j) masks[j] = 0u;
+#pragma unroll
+        for (int j = 0; j < kMaxTileWords; ++j) {  // only the words up to token t
+            if (j >= words) break;
             const int tt = j * 32 + lane;
-            masks[j] = (j < words && tt <= t)
-                           ? token_mask<KT>(src_ids + (size_t)tt * K, K, p.E, p.Epr, p.active)
-                           : 0u;
+            if (tt <= t)
+                masks[j] = token_mask<KT>(src_ids + (size_t)tt * K, K, p.E, p.epr_magic, p.active);
         }
         int cnt = 0;
         uint32_t own = 0;
@@ -150,7 +158,7 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
 
         // ---- routing outputs, by the warp holding the token's first chunk ----
         if (chunk == 0) {
-            const int my_d = live_rank(my_e, p.E, p.Epr, p.active);
+            const int my_d = live_rank(my_e, p.E, p.epr_magic, p.active);
             // lane d: the weight sum of the token's experts on d, ascending k
             // from +0.0; lane k: whether slot k is its rank's first
             float wsum = 0.0f;
@@ -158,7 +166,7 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
             for (int k = 0; k < K; ++k) {
                 const int e = __shfl_sync(kFull, my_e, k);
                 const float wk = __shfl_sync(kFull, my_w, k);
-                const int d = live_rank(e, p.E, p.Epr, p.active);
+                const int d = live_rank(e, p.E, p.epr_magic, p.active);
                 if (d == lane) wsum = __fadd_rn(wsum, wk);
                 if (k < lane && d == my_d) first_of_rank = false;
             }
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
                 const size_t row = ((size_t)d * p.R + s) * p.m + slot;
                 if (lane == 0) p.src_token[row] = t;
                 if (lane < K) {
-                    const bool local = my_e >= 0 && my_e < p.E && my_e / p.Epr == d;
+                    const bool local = my_d == d;  // (d is active)
                     p.recv_ids[row * K + lane] = local ? my_e : -1;
                     p.recv_w[row * K + lane] = local ? my_w : 0.0f;
                 }
@@ -189,8 +197,8 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
         }
 
         // ---- the row copy: the chunk to every destination row ----
-        const int stage = (int)(i % p.stages);
-        const uint32_t parity = (uint32_t)((i / p.stages) & 1);
+        const int stage = i & (kStages - 1);
+        const uint32_t parity = (uint32_t)(i / kStages) & 1u;
         bool ready = true;
         if (lane == 0) ready = ptx::mbar_wait_bounded(&bars[stage], parity, kWaitLimit);
         if (!__shfl_sync(kFull, ready, 0)) {
@@ -229,8 +237,8 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
             atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
             // chunks requested after the one that timed out, still landing in
             // shared memory, before the CTA exits
-            for (long long j = failed + 1; j < issued; ++j)
-                ptx::mbar_wait_bounded(&bars[j % p.stages], (uint32_t)((j / p.stages) & 1),
+            for (int j = failed + 1; j < issued; ++j)
+                ptx::mbar_wait_bounded(&bars[j & (kStages - 1)], (uint32_t)(j / kStages) & 1u,
                                        kWaitLimit);
         }
     }
@@ -253,7 +261,7 @@ cudaError_t dispatch_small_prepare(int row_bytes, int num_sms, DispatchSmallShap
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
         if (err != cudaSuccess) return err;
     }
-    out->stages = 2;
+    out->stages = kStages;
     for (int c = 1; c <= kSmallMaxChunks; ++c) {
         int chunk = (row_bytes + c - 1) / c;
         chunk = (chunk + 15) / 16 * 16;
@@ -284,10 +292,16 @@ int dispatch_small_chunks(int row_bytes, int num_sms, long long tokens) {
     return (int)c;
 }
 
-cudaError_t launch_dispatch_small(const DispatchSmallParams &p, const LaunchShape &shape,
+cudaError_t launch_dispatch_small(const DispatchSmallParams &pc, const LaunchShape &shape,
                                   cudaStream_t st) {
-    if (p.T < 1 || p.T > kRouteTile || p.R > kMaxRanks || p.K > kMaxTopK)
+    DispatchSmallParams p = pc;
+    p.epr_magic = owner_magic(p.Epr);
+    if (p.T < 1 || p.T > kRouteTile || p.R > kMaxRanks || p.K > kMaxTopK ||
+        p.stages != kStages || p.chunks < 1 || p.chunks > kSmallMaxChunks ||
+        p.units != (long long)p.R * p.T * p.chunks)
         return cudaErrorInvalidValue;
+    p.chunks_magic = div_magic(p.chunks);  // exact: units < 2^16, chunks <= 8
+    p.T_magic = div_magic(p.T);            // exact: tokens < 2^13, T <= 256
     long long grid = shape.grid;
     if (grid > p.units) grid = p.units;
     if (grid < 1) return cudaSuccess;

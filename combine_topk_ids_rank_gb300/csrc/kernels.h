@@ -36,6 +36,25 @@ __host__ __device__ inline void token_of(const TokenMap &m, int R, long long i, 
     t = (int)(i - m.first[s]);
 }
 
+// Division by a divisor D fixed for a launch, as a multiply-high: with
+// magic = ceil(2^32 / D), floor(n * magic / 2^32) = floor(n / D) for every
+// n >= 0 with n * D < 2^32.  Used where both stay below 2^16: the owner rank
+// of an expert, e / Epr (ids and Epr below 2^13, MOE_MAX_EXPERTS), and the
+// small dispatch's unit / chunks and token / T.  The launchers fill the
+// magics themselves.
+inline unsigned long long div_magic(int D) {
+    return ((1ull << 32) + (unsigned long long)D - 1) / (unsigned long long)D;
+}
+inline unsigned long long owner_magic(int Epr) { return div_magic(Epr); }
+#ifdef __CUDACC__
+__device__ __forceinline__ int div_by(int n, unsigned long long magic) {
+    return (int)(((unsigned long long)(unsigned)n * magic) >> 32);
+}
+__device__ __forceinline__ int owner_of(int e, unsigned long long magic) {
+    return div_by(e, magic);
+}
+#endif
+
 // Largest number of tokens per CTA of the two routing kernels (one token
 // per thread); the tile of a call is 32, 64, 128 or 256.
 constexpr int kRouteTile = 256;
@@ -85,6 +104,7 @@ struct RouteCountParams {
     TokenMap map;
     uint32_t active;          // ranks that receive messages
     int R, K, E, Epr, RP, ntiles, tile;
+    unsigned long long epr_magic;  // owner_magic(Epr), set by the launcher
 };
 
 // Routing, pass 2: slots (ascending token order per plane), send table,
@@ -105,6 +125,7 @@ struct RouteScanParams {
     uint32_t active;
     int R, K, E, Epr, RP, m, ntiles, tile;
     int dg;                    // destinations per CTA (1 or 4): grid z = RP / dg
+    unsigned long long epr_magic;  // owner_magic(Epr), set by the launcher
 };
 
 // Expert-major layout routing (route_expert.cu).
@@ -309,6 +330,8 @@ struct DispatchSmallParams {
     int R, K, E, Epr, RP, m, T;
     int row_bytes, chunk_bytes, chunks, stages, stage_bytes;
     long long units;           // R * T * chunks
+    unsigned long long epr_magic;  // owner_magic(Epr), set by the launcher
+    unsigned long long chunks_magic, T_magic;  // div_magic(chunks), div_magic(T): launcher
 };
 struct DispatchSmallShapes {   // per chunk count 1..kSmallMaxChunks
     int chunk_bytes[kSmallMaxChunks + 1], chunks[kSmallMaxChunks + 1];

@@ -52,14 +52,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-__device__ __forceinline__ bool is_local(int e, int E, int Epr, int d) {
-    return e >= 0 && e < E && e / Epr == d;
+// (magic: owner_magic(Epr), kernels.h)
+__device__ __forceinline__ bool is_local(int e, int E, unsigned long long magic, int d) {
+    return e >= 0 && e < E && owner_of(e, magic) == d;
 }
 
 // Destination rank of a valid expert on an active rank, else -1.
-__device__ __forceinline__ int live_rank(int e, int E, int Epr, uint32_t active) {
+__device__ __forceinline__ int live_rank(int e, int E, unsigned long long magic,
+                                         uint32_t active) {
     if (e < 0 || e >= E) return -1;
-    const int d = e / Epr;
+    const int d = owner_of(e, magic);
     return ((active >> d) & 1u) ? d : -1;
 }
 
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kRouteTile) route_count_kernel(const RouteCoun
                 bad = true;
                 continue;
             }
-            const int d = e / p.Epr;
+            const int d = owner_of(e, p.epr_magic);
             if (!((p.active >> d) & 1u)) continue;  // expert on an inactive rank
             mask |= 1u << d;
             atomicAdd(&hist[e], 1);
@@ -219,12 +221,12 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
             for (int k = 0; k < KR; ++k) {
                 id_r[k] = ids[k];
                 w_r[k] = wts[k];
-                const int d = live_rank(id_r[k], p.E, p.Epr, p.active);
+                const int d = live_rank(id_r[k], p.E, p.epr_magic, p.active);
                 if (d >= 0) mask |= 1u << d;
             }
         } else {
             for (int k = 0; k < K; ++k) {
-                const int d = live_rank(ids[k], p.E, p.Epr, p.active);
+                const int d = live_rank(ids[k], p.E, p.epr_magic, p.active);
                 if (d >= 0) mask |= 1u << d;
             }
         }
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
         uint32_t seen = 0;
         for (int k = 0; k < K; ++k) {
             const int e = KT > 0 ? id_r[k < KR ? k : 0] : ids[k];
-            const int d = live_rank(e, p.E, p.Epr, p.active);
+            const int d = live_rank(e, p.E, p.epr_magic, p.active);
             int8_t v = -1;
             if (d >= 0 && !((seen >> d) & 1u)) {
                 v = (int8_t)d;
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
                         float *fe = &fv.x;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const bool local = is_local(id_r[k0 + u], p.E, p.Epr, d);
+                            const bool local = is_local(id_r[k0 + u], p.E, p.epr_magic, d);
                             ie[u] = local ? id_r[k0 + u] : -1;
                             fe[u] = local ? w_r[k0 + u] : 0.0f;
                             if (local) wsum = __fadd_rn(wsum, w_r[k0 + u]);
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
                 } else if constexpr (KT > 0) {
 #pragma unroll
                     for (int k = 0; k < KT; ++k) {
-                        const bool local = is_local(id_r[k], p.E, p.Epr, d);
+                        const bool local = is_local(id_r[k], p.E, p.epr_magic, d);
                         rid[k] = local ? id_r[k] : -1;
                         rw[k] = local ? w_r[k] : 0.0f;
                         if (local) wsum = __fadd_rn(wsum, w_r[k]);
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(kRouteTile) route_scan_kernel(const RouteScanP
                     for (int k = 0; k < K; ++k) {
                         const int e = ids[k];
                         const float wk = wts[k];
-                        const bool local = is_local(e, p.E, p.Epr, d);
+                        const bool local = is_local(e, p.E, p.epr_magic, d);
                         rid[k] = local ? e : -1;
                         rw[k] = local ? wk : 0.0f;
                         if (local) wsum = __fadd_rn(wsum, wk);
@@ -379,7 +381,9 @@ cudaError_t launch2d(Kern kern, const P &p, size_t smem, cudaStream_t st, bool p
 
 }  // namespace
 
-cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st) {
+cudaError_t launch_route_count(const RouteCountParams &pc, cudaStream_t st) {
+    RouteCountParams p = pc;
+    p.epr_magic = owner_magic(p.Epr);
     const size_t smem = (size_t)(p.E > kScanChunk ? p.E : kScanChunk) * sizeof(int32_t);
     switch (p.K) {
         case 2: return launch2d(route_count_kernel<2>, p, smem, st, true);
@@ -389,7 +393,9 @@ cudaError_t launch_route_count(const RouteCountParams &p, cudaStream_t st) {
     }
 }
 
-cudaError_t launch_route_scan(const RouteScanParams &p, cudaStream_t st, bool pdl) {
+cudaError_t launch_route_scan(const RouteScanParams &pc, cudaStream_t st, bool pdl) {
+    RouteScanParams p = pc;
+    p.epr_magic = owner_magic(p.Epr);
     if ((p.dg != 1 && p.dg != 4) || p.RP % p.dg != 0) return cudaErrorInvalidValue;
     const unsigned gz = (unsigned)(p.RP / p.dg);
     switch (p.K) {

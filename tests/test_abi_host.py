@@ -8,6 +8,7 @@ one-sided NVLink EP for the GB SKUs", "The adapter" table).
 import os
 import re
 
+import numpy as np
 import pytest
 
 from conftest import ROOT
@@ -302,3 +303,13 @@ def test_expert_gemm_rank_host_checks(abi):
     assert st == abi.MOE_OK
     assert abi.moe_expert_gemm_rank(h, A, 256, 1, 0, A, 1 << 30) == abi.MOE_ERR_PHASE
     abi.moe_a2a_destroy(h)
+
+
+def test_owner_multiply_high_is_exact():
+    # The kernels find an expert's owner rank e // Epr as (e * ceil(2^32 / Epr)) >> 32
+    # (owner_magic in kernels.h).  Exact for e * Epr < 2^32: every expert id and every
+    # Epr allowed by MOE_MAX_EXPERTS = 8192, checked exhaustively.
+    e = np.arange(8192, dtype=np.uint64)
+    for D in range(1, 8193):
+        magic = np.uint64(((1 << 32) + D - 1) // D)
+        assert np.array_equal((e * magic) >> np.uint64(32), e // np.uint64(D)), D
