@@ -184,16 +184,21 @@ __device__ void produce(const CombineParams &p, const Ring &r, int slots) {
     };
 
     uint32_t q = 0;  // rows issued
+    int qb = 0;            // q mod slots, stepped with q
+    uint32_t qph = 0;      // (q / slots) & 1
     bool ok = true;
     auto issue_row = [&](const uint8_t *src) -> bool {
-        const uint32_t b = q % slots;
-        if (!ptx::mbar_wait_bounded(&r.empty[b], ((q / slots) & 1u) ^ 1u, kWaitLimit))
-            return false;
+        const int b = qb;
+        if (!ptx::mbar_wait_bounded(&r.empty[b], qph ^ 1u, kWaitLimit)) return false;
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(&r.full[b], row_bytes);
             ptx::bulk_g2s(r.rows + b * stride, src, row_bytes, &r.full[b]);
         }
         ++q;
+        if (++qb == slots) {
+            qb = 0;
+            qph ^= 1u;
+        }
         return true;
     };
 
@@ -273,7 +278,16 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
         }
     }
 
-    uint32_t q = 0, nred = 0;
+    uint32_t q = 0, nred = 0;  // rows consumed, reductions done
+    int qb = 0;                // q mod slots, stepped with q
+    uint32_t qph = 0;          // (q / slots) & 1
+    auto next_row = [&]() {
+        ++q;
+        if (++qb == slots) {
+            qb = 0;
+            qph ^= 1u;
+        }
+    };
     bool ok = true;
     // Over the CTA's consumer threads: the sum of `a` and, if TWO, the max of
     // `b` -- warp shuffles, then one slot per warp and value in shared
@@ -318,8 +332,8 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
 
         uint4 rv[FUSED ? VPT : 1];
         if (FUSED) {
-            const uint32_t b = q % slots;
-            if (!ptx::mbar_wait_bounded(&r.full[b], (q / slots) & 1u, kWaitLimit)) {
+            const int b = qb;
+            if (!ptx::mbar_wait_bounded(&r.full[b], qph, kWaitLimit)) {
                 ok = false;
                 break;
             }
@@ -331,7 +345,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&r.empty[b]);
-            ++q;
+            next_row();
         }
 
         float acc[VPT][8];
@@ -342,8 +356,8 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
 
         for (int i = 0; i < n; ++i) {
             const float wi = WEIGHTED ? r.desc[ds].w[i] : 1.0f;
-            const uint32_t b = q % slots;
-            if (!ptx::mbar_wait_bounded(&r.full[b], (q / slots) & 1u, kWaitLimit)) {
+            const int b = qb;
+            if (!ptx::mbar_wait_bounded(&r.full[b], qph, kWaitLimit)) {
                 ok = false;
                 break;
             }
@@ -355,7 +369,7 @@ __device__ void consume(const CombineParams &p, const Ring &r, int slots, int nc
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&r.empty[b]);
-            ++q;
+            next_row();
         }
         if (!ok) break;
         __syncwarp();
