@@ -543,7 +543,8 @@ def run_gpu(args, w, rank, world, local_rank):
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
                     "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
                     "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
-                    "kernels": ["combine_small" if N <= 64 and not fp8 else "combine"]},
+                    "kernels": ["combine_small" if N <= combine_small_max() and not fp8
+                                else "combine"]},
     }
     eff_gbs = (d_bytes + c_bytes) / ms_per_step / 1e6
 
@@ -748,6 +749,13 @@ def aggregate_over_ranks(local_ms: float, tokens_per_rank_batch: int, steps: int
         max_ms = float(t.item())
     ms_per_step = max_ms / steps
     return max_ms, ms_per_step, tokens_per_rank_batch * world / (ms_per_step / 1e3)
+
+
+def combine_small_max():
+    """Most tokens of a call the library combines on CTA clusters: its default (64)
+    or the MOE_COMBINE_SMALL_MAX override (-1: never), for the phase's kernel label."""
+    v = int(os.environ.get("MOE_COMBINE_SMALL_MAX", "0") or 0)
+    return 64 if v == 0 else (0 if v < 0 else v)
 
 
 def sources_sha1(names):

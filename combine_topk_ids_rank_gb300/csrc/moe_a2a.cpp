@@ -43,12 +43,12 @@ int gemm_group_m(const moe::Tuning &tn) {
     return tn.gemm_group_m > 0 ? tn.gemm_group_m : kGemmGroupM;
 }
 
-// Largest tokens per rank for the one-launch dispatch by default: measured
-// faster than the two routing passes + row copy up to 64 tokens per rank
-// (T = 1: 14.0 vs 16.8 us; T = 64: 18.4 vs 19.2 us, L2 flushed) and slower
-// from 128 on (26.6 vs 24.4 us), where every copy warp rescans up to 255
-// earlier tokens of its source.
-constexpr int kSmallDispatchMaxT = 64;
+// Largest tokens per rank for the one-launch dispatch by default: one
+// routing tile, the most it serves.  Measured faster than the two routing
+// passes + row copy at every size up to there (L2 flushed): T = 1 8.9 us,
+// T = 64 14.3 vs 18.2-19.1 us, T = 128 20.9 vs 24.5-25.3 us, T = 256
+// 33.3-35.2 vs 38.4-38.7 us.
+constexpr int kSmallDispatchMaxT = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

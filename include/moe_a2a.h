@@ -275,8 +275,8 @@ int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_w
  * message per (token, rank)), assigns slots in ascending source-token order
  * within each (destination, source) plane, copies x rows and the masked
  * top-k metadata into the planes, and counts rows per plane and per local
- * expert.  Queues one kernel on `stream` when every source holds at most 64
- * tokens (rank layout, bf16 rows), else three (the second on the handle's
+ * expert.  Queues one kernel on `stream` when every source holds the same
+ * number of tokens, at most 256 (rank layout, bf16 rows), else three (the second on the handle's
  * own stream, as described above).  IDLE -> DISPATCHED; returns
  * MOE_ERR_PHASE if already DISPATCHED.  If out_view is not NULL it receives
  * the views of this call. */

@@ -63,14 +63,14 @@ def test_route_overlap_modes(monkeypatch, overlap):
 @pytest.mark.parametrize("T", [1, 33, 64, 256])
 def test_one_launch_dispatch_modes(monkeypatch, small_max, T):
     # Batches of at most one 256-token routing tile per source: "0" (the
-    # default) dispatches in one launch, each copy warp deriving its token's
+    # default, up to 256 tokens) dispatches in one launch, each copy warp deriving its token's
     # slots from the ids before it; "-1" forces the two routing passes and the
     # row copy.  Both must equal the oracle (rows chunked when tokens are few).
     monkeypatch.setenv("MOE_DISPATCH_SMALL_MAX", small_max)
     w = small("decode", ep_size=6, tokens_per_rank=T, max_tokens=260, runtime_max=T + 3,
               hidden=1032, num_experts=48, top_k=5, weighted=True, fused=True)
     rep = parity.Case(w).run(seed=T)
-    assert rep["kernels"] == (1 if small_max == "0" and T <= 64 else 3)
+    assert rep["kernels"] == (1 if small_max == "0" and T <= 256 else 3)
 
 
 @pytest.mark.parametrize("small_max", ["-1", "4096"])
