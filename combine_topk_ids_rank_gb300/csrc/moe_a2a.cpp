@@ -378,6 +378,18 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
 
     const bool expert = h->L.layout == MOE_LAYOUT_EXPERT;
     const moe::DestRows dest = dest_rows(h, m);
+    // The one-launch dispatch alternates its two local-expert count buffers
+    // on the host (each call adds into the one the previous call cleared),
+    // which a CUDA graph cannot replay: a captured call would add into the
+    // same buffer at every replay.  While `stream` is capturing, the call
+    // takes the routing passes, whose accumulators are cleared inside the
+    // call.  (An unknown capture state counts as capturing.)
+    bool one_launch = ntok > 0 && small_dispatch(h, map);
+    if (one_launch) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            one_launch = false;
+    }
     if (ntok == 0) {
         const size_t nrc = expert ? (size_t)E : (size_t)R * R;
         if (cudaMemsetAsync(h->ws + h->L.recv_counts, 0, sizeof(int32_t) * nrc, st) !=
@@ -416,7 +428,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         h->accum_dirty = false;
         rc = launch_rows(h, d_x, map, m, dest, ntok, st);
         if (rc != MOE_OK) return rc;
-    } else if (small_dispatch(h, map)) {
+    } else if (one_launch) {
         // one launch: every copy warp derives its token's slots itself
         const size_t bufs[2] = {h->L.local_counts, h->L.local_counts2};
         const int sel = h->small_sel;
@@ -528,7 +540,6 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         }
     }
 
-    const bool one_launch = ntok > 0 && small_dispatch(h, map);
     if (!one_launch) {
         // the routing pass (or the empty call) wrote local_counts
         h->cur_counts = h->L.local_counts;

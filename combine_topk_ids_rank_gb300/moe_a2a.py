@@ -424,6 +424,8 @@ class MoeA2A:
         view = self._views.get(key)
         if view is None:
             view = self._views[key] = DispatchView(self, raw)
+        else:  # the per-call scalars of this call
+            view.kernels, view.tokens_per_rank = raw.kernels, raw.tokens_per_rank
         self.last_view = view
         return view
 

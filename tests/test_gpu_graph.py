@@ -1,0 +1,102 @@
+"""CUDA-graph capture of a dispatch + combine pair, replayed on new inputs.
+
+The inputs live in fixed device buffers; each replay follows a copy of a new
+seeded input set into them, and every replay's routing, counts (the
+local-expert counts included), dispatched rows and combine outputs must be
+the oracle's for that input set.  The experts are the identity (the combine
+reads the dispatched rows), so the whole pair runs on the device.  A batch
+that a direct call dispatches in one launch is captured through the routing
+passes, whose accumulators are cleared inside each call.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+from combine_topk_ids_rank_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import parity  # noqa: E402
+from oracle import oracle  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from combine_topk_ids_rank_gb300 import build_lib
+    build_lib.build()
+
+
+@pytest.mark.parametrize("T", [40, 300])
+def test_graph_replays_match_the_oracle(T):
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+    R, M, H, E, K = 4, 300, 256, 32, 4
+    w = replace(synth.WORKLOADS["decode"], ep_size=R, tokens_per_rank=T, max_tokens=M,
+                runtime_max=T, hidden=H, num_experts=E, top_k=K, weighted=True, fused=True)
+    a = MoeA2A(R, M, H, E, K, "cuda")
+    a.workspace.fill_(parity.POISON)
+
+    def inputs(seed):
+        inp = synth.inputs(w, seed)
+        return {k: np.ascontiguousarray(inp[k]) for k in ("topk_ids", "topk_w", "x", "residual",
+                                                          "gamma")}
+
+    first = inputs(100)
+    ids = parity.to_dev(first["topk_ids"], torch.int32)
+    wts = parity.to_dev(first["topk_w"], torch.float32)
+    x = parity.to_dev(first["x"], torch.bfloat16)
+    res = parity.to_dev(first["residual"], torch.bfloat16)
+    gam = parity.to_dev(first["gamma"], torch.bfloat16)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(res)
+
+    # a direct call first (it also creates the handle's stream and events)
+    view = a.dispatch(ids, wts, x, T)
+    assert view.kernels == (1 if T <= 256 else 3)
+    a.combine(view.recv_x, True, res, gam, w.eps, out, rout)
+    torch.cuda.synchronize()
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        view = a.dispatch(ids, wts, x, T)
+        a.combine(view.recv_x, True, res, gam, w.eps, out, rout)
+    assert view.kernels == 3  # captured through the routing passes
+    assert a.phase == 0
+
+    for seed in (1, 2, 3):
+        inp = inputs(seed)
+        ids.copy_(parity.to_dev(inp["topk_ids"], torch.int32))
+        wts.copy_(parity.to_dev(inp["topk_w"], torch.float32))
+        x.copy_(parity.to_dev(inp["x"], torch.bfloat16))
+        res.copy_(parity.to_dev(inp["residual"], torch.bfloat16))
+        gam.copy_(parity.to_dev(inp["gamma"], torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        st, flags = a.get_error()
+        assert st == 0 and flags == 0, (st, flags)
+
+        r = oracle.route(inp["topk_ids"], inp["topk_w"], E, T)
+        counts = view.recv_counts.cpu().numpy()
+        assert np.array_equal(counts, r["recv_counts"]), ("recv_counts", seed)
+        assert np.array_equal(view.local_expert_counts.cpu().numpy(),
+                              r["local_expert_counts"]), ("local_expert_counts", seed)
+        assert np.array_equal(view.send_slot.cpu().numpy()[:, :, :R], r["send_slot"]), seed
+        od = oracle.dispatch(inp["topk_ids"], inp["topk_w"], inp["x"], E, T, r)
+        gx = parity.to_host_u16(view.recv_x)
+        for d in range(R):
+            for s in range(R):
+                c = counts[d, s]
+                assert np.array_equal(gx[d, s, :c], od["recv_x"][d, s, :c]), (d, s, seed)
+
+        oc = oracle.combine(r, od["recv_x"], True, inp["residual"], inp["gamma"], w.eps,
+                            tokens=np.arange(R * T))
+        g_rout = parity.to_host_u16(rout).reshape(R * T, H)
+        assert np.array_equal(g_rout, oc["residual_out"]), ("residual_out", seed)
+        y = parity.f32(parity.to_host_u16(out).reshape(R * T, H)).astype(np.float64)
+        err = np.abs(y - oc["y"])
+        bad = (err > parity.ABS_TOL) | (err > parity.REL_TOL * np.abs(oc["y"]))
+        assert not bad.any(), ("RMSNorm tolerance", seed, float(err.max()))
