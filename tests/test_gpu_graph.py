@@ -100,3 +100,111 @@ def test_graph_replays_match_the_oracle(T):
         err = np.abs(y - oc["y"])
         bad = (err > parity.ABS_TOL) | (err > parity.REL_TOL * np.abs(oc["y"]))
         assert not bad.any(), ("RMSNorm tolerance", seed, float(err.max()))
+
+
+def test_graph_replays_expert_layout():
+    # The expert-major layout (one row per (token, expert), the gates applied
+    # in the combine): its two routing passes move the expert histogram out of
+    # an accumulator and clear it inside each call, so replays stay exact.
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_LAYOUT_EXPERT
+    R, T, H, E, K = 4, 50, 128, 16, 4
+    a = MoeA2A(R, T, H, E, K, "cuda", layout=MOE_LAYOUT_EXPERT)
+
+    def inputs(seed):
+        return dict(ids=synth.topk_ids(seed, R, T, E, K, "uniform"),
+                    w=synth.topk_weights(seed, R, T, K),
+                    x=synth.per_rank_rows(seed, synth.X, R, T, H),
+                    res=synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H),
+                    g=synth.gamma(seed, H))
+
+    first = inputs(200)
+    ids = parity.to_dev(first["ids"], torch.int32)
+    wts = parity.to_dev(first["w"], torch.float32)
+    x = parity.to_dev(first["x"], torch.bfloat16)
+    res = parity.to_dev(first["res"], torch.bfloat16)
+    gam = parity.to_dev(first["g"], torch.bfloat16)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(res)
+    view = a.dispatch(ids, wts, x, T)
+    a.combine(view.recv_x, True, res, gam, 1e-6, out, rout)
+    torch.cuda.synchronize()
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        view = a.dispatch(ids, wts, x, T)
+        a.combine(view.recv_x, True, res, gam, 1e-6, out, rout)
+
+    for seed in (4, 5, 6):
+        inp = inputs(seed)
+        for dst, src, dt in ((ids, inp["ids"], torch.int32), (wts, inp["w"], torch.float32),
+                             (x, inp["x"], torch.bfloat16), (res, inp["res"], torch.bfloat16),
+                             (gam, inp["g"], torch.bfloat16)):
+            dst.copy_(parity.to_dev(src, dt))
+        g.replay()
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0)
+        r = oracle.route_experts(inp["ids"], inp["w"], E, T)
+        assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"]), seed
+        assert np.array_equal(view.local_expert_counts.cpu().numpy(),
+                              r["local_expert_counts"]), seed
+        rx = oracle.dispatch_experts(inp["x"], E, T, r)
+        oc = oracle.combine_experts(r, rx, True, inp["res"], inp["g"], 1e-6,
+                                    tokens=np.arange(R * T))
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H),
+                              oc["residual_out"]), ("residual_out", seed)
+        y = parity.f32(parity.to_host_u16(out).reshape(R * T, H)).astype(np.float64)
+        err = np.abs(y - oc["y"])
+        assert (err <= parity.ABS_TOL).all() and (err <= parity.REL_TOL * np.abs(oc["y"])).all()
+
+
+def test_graph_replays_fp8_dispatch():
+    # FP8 receive rows: every replay's e4m3 codes and per-row scales are the
+    # oracle's quantisation of that replay's rows; the combine (bf16 output)
+    # reads a payload written once, at the slots of each replay's routing.
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    R, T, H, E, K = 4, 30, 256, 32, 4
+    w = replace(synth.WORKLOADS["decode"], ep_size=R, tokens_per_rank=T, max_tokens=T,
+                runtime_max=T, hidden=H, num_experts=E, top_k=K, weighted=True, fused=False)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    first = synth.inputs(w, 300)
+    ids = parity.to_dev(first["topk_ids"], torch.int32)
+    wts = parity.to_dev(first["topk_w"], torch.float32)
+    x = parity.to_dev(first["x"], torch.bfloat16)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    view = a.dispatch(ids, wts, x, T)
+    eo = synth.expert_out_planes(7, R, T, H, np.full((R, R), T))  # every slot drawn
+    a.combine_payload().copy_(parity.to_dev(eo, torch.bfloat16))
+    a.combine(None, True, out=out)
+    torch.cuda.synchronize()
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        view = a.dispatch(ids, wts, x, T)
+        a.combine(None, True, out=out)
+
+    for seed in (7, 8, 9):
+        inp = synth.inputs(w, seed)
+        ids.copy_(parity.to_dev(inp["topk_ids"], torch.int32))
+        wts.copy_(parity.to_dev(inp["topk_w"], torch.float32))
+        x.copy_(parity.to_dev(inp["x"], torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0)
+        r = oracle.route(inp["topk_ids"], inp["topk_w"], E, T)
+        counts = view.recv_counts.cpu().numpy()
+        assert np.array_equal(counts, r["recv_counts"]), seed
+        assert np.array_equal(view.local_expert_counts.cpu().numpy(),
+                              r["local_expert_counts"]), seed
+        q_ref, s_ref = oracle.quantize_rows_fp8(inp["x"])
+        codes = view.recv_x.view(torch.uint8).cpu().numpy()
+        scales = view.recv_scale.cpu().numpy()
+        src = view.src_token.cpu().numpy()
+        for d in range(R):
+            for s in range(R):
+                for j in range(counts[d, s]):
+                    t = src[d, s, j]
+                    assert np.array_equal(codes[d, s, j], q_ref[s, t]), (d, s, j, seed)
+                    assert scales[d, s, j] == s_ref[s, t]
+        oc = oracle.combine(r, eo, True, tokens=np.arange(R * T))
+        assert np.array_equal(parity.to_host_u16(out).reshape(R * T, H), oc["out"]), seed
