@@ -73,8 +73,12 @@ template <int VPT, bool WEIGHTED, bool FUSED>
 __global__ void __launch_bounds__(kSmallCombineMaxThreads)
     combine_small_kernel(const CombineParams p, const int cols8) {
     __shared__ float red[kSmallCombineMaxThreads / 32];
-    __shared__ float part;  // this CTA's sum of squares (read by the whole cluster)
+    __shared__ float parts[kClusterCtas];  // every CTA's sum of squares, pushed by each
     cg::cluster_group cluster = cg::this_cluster();
+    // This CTA has started: the arrival half of a split cluster barrier,
+    // waited on just before the partial sums are pushed into the other
+    // CTAs' shared memory (which needs every CTA of the cluster running).
+    if constexpr (FUSED) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthreads = blockDim.x, nwarps = nthreads >> 5;
     const int crank = (int)cluster.block_rank(), csize = (int)cluster.num_blocks();
@@ -181,15 +185,13 @@ __global__ void __launch_bounds__(kSmallCombineMaxThreads)
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
         if (lane == 0) red[warp] = ss;
         __syncthreads();
-        if (tid == 0) {
-            float v = 0.0f;
-            for (int k = 0; k < nwarps; ++k) v += red[k];
-            part = v;
-        }
-        cluster.sync();  // every CTA's partial is written
+        float v = 0.0f;
+        for (int k = 0; k < nwarps; ++k) v += red[k];
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // all CTAs started
+        if (tid < csize) *cluster.map_shared_rank(&parts[crank], tid) = v;  // into CTA tid
+        cluster.sync();  // every CTA's partial has arrived; nothing remote after this
         float total = 0.0f;
-        for (int r = 0; r < csize; ++r) total += *cluster.map_shared_rank(&part, r);
-        cluster.sync();  // no CTA leaves while another still reads its partial
+        for (int r = 0; r < csize; ++r) total += parts[r];  // ascending rank, as before
         const float inv = rsqrtf(total / (float)p.H + p.eps);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
