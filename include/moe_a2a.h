@@ -56,6 +56,18 @@
  * captures both branches.  Calls return without synchronising, except
  * moe_a2a_get_error.  A handle is bound to the CUDA device that is current
  * at its first dispatch; moe_a2a_destroy releases its stream and events.
+ *
+ * CUDA graphs: calls made while `stream` is capturing queue the same
+ * kernels and memsets into the graph; a replay runs them with the pointers,
+ * sizes and options of the capture, on whatever the buffers hold then (the
+ * host-side phase is not replayed).  Every call's device state is cleared
+ * inside the call, so captured dispatch / combine pairs can be replayed any
+ * number of times (moe_dispatch takes its routing passes while capturing,
+ * see below).
+ *
+ * Host threads: a handle keeps host-side state (phase, views, which count
+ * buffer is current), so calls on one handle must not run concurrently;
+ * distinct handles are independent.
  */
 #ifndef MOE_A2A_H
 #define MOE_A2A_H
