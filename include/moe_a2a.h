@@ -391,7 +391,7 @@ int moe_a2a_set_reduction(moe_a2a_t *h, int32_t reduction);
 /* ---- FP8 payloads ----------------------------------------------------------
  * [IX] "The adapter" (the paragraph on why the adapter is BF16-only): an FP8
  * dispatch carries a scale payload beside the rows and is validated against
- * the cast round trip; the combine side accepts FP8 output dtypes ([IX] the
+ * the cast round trip; the upstream combine can emit FP8 outputs ([IX] the
  * comment on the shipped combine signature: upstream output_dtype /
  * use_low_precision).  Readings: OCP FP8 E4M3 (bias 7, largest finite 448,
  * no infinities), one scale per token row:

@@ -2,8 +2,8 @@
 
 InferenceX PR #2450, "CollectiveX: add FlashInfer one-sided NVLink EP for the
 GB SKUs", "The adapter": an FP8 dispatch carries a per-token scale payload
-next to the rows and is checked against the cast round trip; the combine
-side accepts FP8 output dtypes.  Readings: OCP e4m3, scale = amax / 448 in
+next to the rows and is checked against the cast round trip; the upstream
+combine can emit FP8 outputs.  Readings: OCP e4m3, scale = amax / 448 in
 binary32 (1 for a zero row), codes = e4m3_rn_satfinite(v / scale).
 
 Dispatch in the FP8 receive format and the unfused FP8 combine are compared
