@@ -902,8 +902,10 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
 }
 
 // Scratch of the rank-plane product, sized for max_tokens_per_rank: the
-// per-expert pair cursors, the receive row and gate mark of each pair, the
-// pair of each (row, k) and the experts' bf16 outputs, pair-major.
+// per-expert pair cursors (and the count of rows with several local
+// experts), the receive row and gate mark of each pair, the pair of each
+// (row, k), the list of rows with several local experts and the experts'
+// bf16 outputs, pair-major.
 struct RankScratch {
     size_t cursor, pair_row, pair_gate, pair_of, multi, y, total;
     long long multi_cap;
