@@ -604,8 +604,11 @@ cudaError_t combine_ring_prepare(int H, bool weighted, bool fused, bool out8, in
     // once) matters more than a deep ring; measured best on the prefill
     // shape (2-6 slots swept).  The FP8 output's longer epilogue wants rows
     // more in flight: 80 KB (5 rows; prefill 412.4 us at 3 rows, 397.1 at 4,
-    // 393.7 at 5, where 4 rows made the bf16 output slower).
-    const size_t target = out8 ? 80 * 1024 : kRingBytesTarget;
+    // 393.7 at 5, where 4 rows made the bf16 output slower).  So does the
+    // plain sum, whose tokens carry more messages than the ring holds (wide
+    // EP, 6.5 rows of 8 KB per token: 163.6 us at 10 rows against 171.7 at 6
+    // and 166.6-167.7 for the register combine; 14 rows lose a CTA per SM).
+    const size_t target = (out8 || !fused) ? 80 * 1024 : kRingBytesTarget;
     int s = (int)(target / ring_stride(2 * H));
     s = s < 2 ? 2 : (s > kMaxRingSlots ? kMaxRingSlots : s);
     if (tn.combine_ring_slots >= 2 && tn.combine_ring_slots <= kMaxRingSlots)

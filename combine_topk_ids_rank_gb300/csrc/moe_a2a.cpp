@@ -643,12 +643,14 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
     } else if (h->ntok > 0) {
         const int variant = (out8 ? 4 : 0) + (weighted ? 2 : 0) + (fused ? 1 : 0);
         if (!h->combine_ready[variant]) {
-            // The fused combine streams its rows through a shared-memory
-            // ring (its epilogue then overlaps other tokens' loads); the
-            // plain gather-sum keeps rows in registers, which measured
-            // faster there.  Tuning::combine_kernel overrides.  The FP8
-            // output exists on the ring kernel only.
-            bool ring = fused || out8;
+            // Every combine streams its rows through a shared-memory ring
+            // (the fused epilogue then overlaps other tokens' loads; the
+            // plain sum keeps more rows in flight than registers allow:
+            // wide EP 163.6 us against 166.6-167.7 us for the register
+            // combine).  Tuning::combine_kernel overrides ("regs": the
+            // register combine where it exists; the FP8 output exists on
+            // the ring kernel only).
+            bool ring = true;
             if (h->tuning.combine_kernel == 2) ring = out8;
             if (h->tuning.combine_kernel == 1) ring = true;
             cudaError_t e =
