@@ -27,6 +27,8 @@
 // cleared and clears the other one, so nothing waits for a last CTA.
 // Waits are bounded: on time-out the kernel raises the flag, drains its
 // copies and returns.
+#include "dispatch_small.h"
+#include "fp8.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -38,6 +40,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStages = 2;  // x chunks in flight per CTA (shared-memory stages)
+constexpr int kSmallFp8MaxThreads = 256;  // threads of the FP8 kernel: at most
 constexpr int kMaxTileWords = kRouteTile / 32;  // 32-token groups of a source
 
 // (magic: owner_magic(Epr), kernels.h)
@@ -69,6 +72,85 @@ __device__ __forceinline__ uint32_t token_mask(const int32_t *ids, int K, int E,
         }
     }
     return mask;
+}
+
+// Slots of token t of a source whose ids start at src_ids (one warp): lane d
+// gets the number of the source's earlier tokens sent to rank d (cnt), every
+// lane the token's destination mask (own).  One ballot per destination and
+// 32 earlier tokens.
+template <int KT>
+__device__ __forceinline__ void token_slots(const int32_t *src_ids, int t, int K, int E, int R,
+                                            unsigned long long magic, uint32_t active,
+                                            int lane, int &cnt, uint32_t &own) {
+    uint32_t masks[kMaxTileWords];
+    const int words = t / 32 + 1;
+#pragma unroll
+    for (int j = 0; j < kMaxTileWords; ++j) masks[j] = 0u;
+#pragma unroll
+    for (int j = 0; j < kMaxTileWords; ++j) {  // only the words up to token t
+        if (j >= words) break;
+        const int tt = j * 32 + lane;
+        if (tt <= t) masks[j] = token_mask<KT>(src_ids + (size_t)tt * K, K, E, magic, active);
+    }
+    cnt = 0;
+    own = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTileWords; ++j) {
+        if (j >= words) break;
+        const int tt = j * 32 + lane;
+        const uint32_t before = tt < t ? masks[j] : 0u;
+        for (int d = 0; d < R; ++d) {
+            const uint32_t b = __ballot_sync(kFull, (before >> d) & 1u);
+            if (lane == d) cnt += __popc(b);
+        }
+        if (j == t / 32) own = __shfl_sync(kFull, masks[j], t & 31);
+    }
+}
+
+// The routing outputs of token tok = (s, t) (one warp; its ids and weights
+// one per lane): send row and per-destination weights, the top-k slots'
+// destinations, the local-expert counts, the source map and metadata rows
+// of every destination, and, for the source's last token, its recv counts.
+template <class P>
+__device__ __forceinline__ void write_routing(const P &p, int K, int tok, int s, int t,
+                                              int my_e, float my_w, int cnt, uint32_t own,
+                                              int lane) {
+    const int my_d = live_rank(my_e, p.E, p.epr_magic, p.active);
+    // lane d: the weight sum of the token's experts on d, ascending k from
+    // +0.0; lane k: whether slot k is its rank's first
+    float wsum = 0.0f;
+    bool first_of_rank = my_d >= 0;
+    for (int k = 0; k < K; ++k) {
+        const int e = __shfl_sync(kFull, my_e, k);
+        const float wk = __shfl_sync(kFull, my_w, k);
+        const int d = live_rank(e, p.E, p.epr_magic, p.active);
+        if (d == lane) wsum = __fadd_rn(wsum, wk);
+        if (k < lane && d == my_d) first_of_rank = false;
+    }
+    if (lane < p.RP) {
+        const bool has = lane < p.R && ((own >> lane) & 1u);
+        p.send_slot[tok * p.RP + lane] = has ? cnt : -1;
+        p.dest_weight[tok * p.RP + lane] = has ? wsum : 0.0f;
+    }
+    if (lane < K) {
+        if (my_e < -1 || my_e >= p.E) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_EXPERT_ID);
+        else if (my_d >= 0) atomicAdd(p.counts + my_e, 1);
+        if (p.topk_dest != nullptr)  // first slot of each rank carries its message
+            p.topk_dest[tok * K + lane] = (int8_t)(first_of_rank ? my_d : -1);
+    }
+    for (uint32_t b = own; b != 0; b &= b - 1) {  // uniform over the warp
+        const int d = __ffs(b) - 1;
+        const int slot = __shfl_sync(kFull, cnt, d);
+        const size_t row = ((size_t)d * p.R + s) * p.m + slot;
+        if (lane == 0) p.src_token[row] = t;
+        if (lane < K) {
+            const bool local = my_d == d;  // (d is active)
+            p.recv_ids[row * K + lane] = local ? my_e : -1;
+            p.recv_w[row * K + lane] = local ? my_w : 0.0f;
+        }
+    }
+    if (t == p.T - 1 && lane < p.R)
+        p.recv_counts[lane * p.R + s] = cnt + (int)((own >> lane) & 1u);
 }
 
 template <int KT>
@@ -123,30 +205,9 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
         const float my_w = lane < K ? __ldg(p.topk_w + tok * K + lane) : 0.0f;
 
         // ---- slots: lane d counts the earlier tokens of source s sent to d ----
-        uint32_t masks[kMaxTileWords];
-        const int words = t / 32 + 1;
-#pragma unroll
-        for (int j = 0; j < kMaxTileWords; ++j) masks[j] = 0u;
-#pragma unroll
-        for (int j = 0; j < kMaxTileWords; ++j) {  // only the words up to token t
-            if (j >= words) break;
-            const int tt = j * 32 + lane;
-            if (tt <= t)
-                masks[j] = token_mask<KT>(src_ids + (size_t)tt * K, K, p.E, p.epr_magic, p.active);
-        }
-        int cnt = 0;
-        uint32_t own = 0;
-#pragma unroll
-        for (int j = 0; j < kMaxTileWords; ++j) {
-            if (j >= words) break;
-            const int tt = j * 32 + lane;
-            const uint32_t before = tt < t ? masks[j] : 0u;
-            for (int d = 0; d < p.R; ++d) {
-                const uint32_t b = __ballot_sync(kFull, (before >> d) & 1u);
-                if (lane == d) cnt += __popc(b);
-            }
-            if (j == t / 32) own = __shfl_sync(kFull, masks[j], t & 31);
-        }
+        int cnt;
+        uint32_t own;
+        token_slots<KT>(src_ids, t, K, p.E, p.R, p.epr_magic, p.active, lane, cnt, own);
 
         // The ids are inputs too; before the first write, wait for the kernels
         // before this one in the stream (a combine still reading the
@@ -157,44 +218,7 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
         }
 
         // ---- routing outputs, by the warp holding the token's first chunk ----
-        if (chunk == 0) {
-            const int my_d = live_rank(my_e, p.E, p.epr_magic, p.active);
-            // lane d: the weight sum of the token's experts on d, ascending k
-            // from +0.0; lane k: whether slot k is its rank's first
-            float wsum = 0.0f;
-            bool first_of_rank = my_d >= 0;
-            for (int k = 0; k < K; ++k) {
-                const int e = __shfl_sync(kFull, my_e, k);
-                const float wk = __shfl_sync(kFull, my_w, k);
-                const int d = live_rank(e, p.E, p.epr_magic, p.active);
-                if (d == lane) wsum = __fadd_rn(wsum, wk);
-                if (k < lane && d == my_d) first_of_rank = false;
-            }
-            if (lane < p.RP) {
-                const bool has = lane < p.R && ((own >> lane) & 1u);
-                p.send_slot[tok * p.RP + lane] = has ? cnt : -1;
-                p.dest_weight[tok * p.RP + lane] = has ? wsum : 0.0f;
-            }
-            if (lane < K) {
-                if (my_e < -1 || my_e >= p.E) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_EXPERT_ID);
-                else if (my_d >= 0) atomicAdd(p.counts + my_e, 1);
-                if (p.topk_dest != nullptr)  // first slot of each rank carries its message
-                    p.topk_dest[tok * K + lane] = (int8_t)(first_of_rank ? my_d : -1);
-            }
-            for (uint32_t b = own; b != 0; b &= b - 1) {  // uniform over the warp
-                const int d = __ffs(b) - 1;
-                const int slot = __shfl_sync(kFull, cnt, d);
-                const size_t row = ((size_t)d * p.R + s) * p.m + slot;
-                if (lane == 0) p.src_token[row] = t;
-                if (lane < K) {
-                    const bool local = my_d == d;  // (d is active)
-                    p.recv_ids[row * K + lane] = local ? my_e : -1;
-                    p.recv_w[row * K + lane] = local ? my_w : 0.0f;
-                }
-            }
-            if (t == p.T - 1 && lane < p.R)
-                p.recv_counts[lane * p.R + s] = cnt + (int)((own >> lane) & 1u);
-        }
+        if (chunk == 0) write_routing(p, K, tok, s, t, my_e, my_w, cnt, own, lane);
 
         // ---- the row copy: the chunk to every destination row ----
         const int stage = i & (kStages - 1);
@@ -241,6 +265,108 @@ __global__ void __launch_bounds__(32) dispatch_small_kernel(const DispatchSmallP
                 ptx::mbar_wait_bounded(&bars[j & (kStages - 1)], (uint32_t)(j / kStages) & 1u,
                                        kWaitLimit);
         }
+    }
+}
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// FP8 receive rows, one CTA per token: thread 0 requests the bf16 row into
+// shared memory, warp 0 derives the token's slots and writes its routing
+// outputs (as the bf16 kernel's first-chunk warp), every thread takes VPT
+// vectors of the row; the row's amax is one CTA reduction (the same
+// barrier publishes the destination rows), and each thread stores the e4m3
+// codes of its vectors to every destination row (fp8.cuh's quotient).
+template <int KT, int VPT>
+__global__ void __launch_bounds__(kSmallFp8MaxThreads)
+    dispatch_small_fp8_kernel(const DispatchSmallFp8Params p) {
+    extern __shared__ __align__(128) uint8_t row_smem[];  // the token's bf16 row
+    __shared__ uint64_t bar;
+    __shared__ long long rows[kMaxRanks];                  // destination rows (-1: none)
+    __shared__ float red[kSmallFp8MaxThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nt = blockDim.x, nw = nt >> 5;
+    const int K = KT > 0 ? KT : p.K;
+    const int tok = blockIdx.x;  // s * T + t, below 2^13
+    const int s = div_by(tok, p.T_magic), t = tok - s * p.T;
+    const uint32_t row_bytes = (uint32_t)p.H * 2;
+
+    if (tid == 0) {  // x is an input of the call: requested right away
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+        ptx::mbar_arrive_expect_tx(&bar, row_bytes);
+        ptx::bulk_g2s(row_smem, p.x + (size_t)tok * p.H, row_bytes, &bar);
+    }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+
+    if (warp == 0) {
+        const int32_t *src_ids = p.topk_ids + (size_t)s * p.T * K;
+        const int my_e = lane < K ? __ldg(src_ids + (size_t)t * K + lane) : -1;
+        const float my_w = lane < K ? __ldg(p.topk_w + (size_t)tok * K + lane) : 0.0f;
+        int cnt;
+        uint32_t own;
+        token_slots<KT>(src_ids, t, K, p.E, p.R, p.epr_magic, p.active, lane, cnt, own);
+        ptx::grid_dependency_wait();  // before the first write
+        write_routing(p, K, tok, s, t, my_e, my_w, cnt, own, lane);
+        if (lane < p.RP)
+            rows[lane] = (lane < p.R && ((own >> lane) & 1u))
+                             ? ((long long)lane * p.R + s) * p.m + cnt
+                             : -1;
+    } else {
+        ptx::grid_dependency_wait();
+    }
+    if (blockIdx.x == 0)  // the next call's counts buffer starts at zero
+        for (int e = tid; e < p.E; e += nt) p.counts_clear[e] = 0;
+
+    const bool landed = ptx::mbar_wait_bounded(&bar, 0, kWaitLimit);
+    const uint4 *row = reinterpret_cast<const uint4 *>(row_smem);
+    uint4 cur[VPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int c = tid + j * nt;
+        cur[j] = (landed && c < p.H8) ? row[c] : make_uint4(0, 0, 0, 0);
+        const uint32_t u[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(lo_f(u[e])), fabsf(hi_f(u[e]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    if (lane == 0) red[warp] = amax;
+    if (!__syncthreads_and(landed)) {  // (also publishes rows[] and red[])
+        if (tid == 0) {
+            atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+            // the row copy lands before the shared memory goes away
+            ptx::mbar_wait_bounded(&bar, 0, kWaitLimit);
+        }
+        return;
+    }
+    amax = red[0];
+    for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[w]);
+    const fp8::RowScale rs = fp8::row_scale(amax);
+    float f[VPT][8];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const uint32_t u[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[j][2 * e] = lo_f(u[e]);
+            f[j][2 * e + 1] = hi_f(u[e]);
+        }
+    }
+    uint2 q[VPT];
+    fp8::quantize_row<VPT>(f, rs, q);
+    for (int d = 0; d < p.RP; ++d) {
+        const long long dst_row = rows[d];
+        if (dst_row < 0) continue;
+        uint2 *dst = reinterpret_cast<uint2 *>(p.recv_x8 + dst_row * p.H);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = tid + j * nt;
+            if (c < p.H8) __stcs(dst + c, q[j]);
+        }
+        if (tid == 0) p.recv_scale[dst_row] = rs.s;
     }
 }
 
@@ -322,6 +448,83 @@ cudaError_t launch_dispatch_small(const DispatchSmallParams &pc, const LaunchSha
         case 8: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<8>, p);
         default: return cudaLaunchKernelEx(&cfg, dispatch_small_kernel<0>, p);
     }
+}
+
+
+namespace {
+
+// Threads for a row of H8 16-byte vectors: 128 while the row fits in 8
+// vectors per thread, else the fewest whole warps that cover it with 8.
+int fp8_threads(int H8) {
+    if (H8 <= 8 * 128) return 128;
+    return ((H8 + 7) / 8 + 31) / 32 * 32;
+}
+
+template <int VPT>
+struct SmallFp8 {
+    static cudaError_t attr(size_t smem) {
+        cudaError_t e = cudaFuncSetAttribute(dispatch_small_fp8_kernel<8, VPT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(dispatch_small_fp8_kernel<0, VPT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    }
+    static cudaError_t launch(const DispatchSmallFp8Params &p, const DispatchSmallFp8Shape &sh,
+                              cudaStream_t st) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(p.R * p.T), 1, 1);
+        cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
+        cfg.dynamicSmemBytes = sh.smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (p.K == 8) return cudaLaunchKernelEx(&cfg, dispatch_small_fp8_kernel<8, VPT>, p);
+        return cudaLaunchKernelEx(&cfg, dispatch_small_fp8_kernel<0, VPT>, p);
+    }
+};
+
+template <template <int> class F, typename Fn>
+cudaError_t by_vpt(int vpt, Fn fn) {
+    switch (vpt) {
+        case 1: return fn(F<1>());
+        case 2: return fn(F<2>());
+        case 3: return fn(F<3>());
+        case 4: return fn(F<4>());
+        case 5: return fn(F<5>());
+        case 6: return fn(F<6>());
+        case 7: return fn(F<7>());
+        case 8: return fn(F<8>());
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t dispatch_small_fp8_prepare(int H, DispatchSmallFp8Shape *out) {
+    if (H % 16 != 0 || H / 8 > 2048) return cudaErrorInvalidValue;
+    const int H8 = H / 8;
+    out->threads = fp8_threads(H8);
+    out->vpt = (H8 + out->threads - 1) / out->threads;
+    out->smem = (size_t)H * 2;
+    if (out->threads > kSmallFp8MaxThreads) return cudaErrorInvalidValue;
+    const size_t smem = out->smem;
+    return by_vpt<SmallFp8>(out->vpt, [&](auto f) { return decltype(f)::attr(smem); });
+}
+
+cudaError_t launch_dispatch_small_fp8(const DispatchSmallFp8Params &pc,
+                                      const DispatchSmallFp8Shape &shape, cudaStream_t st) {
+    DispatchSmallFp8Params p = pc;
+    if (p.T < 1 || p.T > kRouteTile || p.R > kMaxRanks || p.K > kMaxTopK || p.H % 16 != 0 ||
+        p.H8 != p.H / 8 || shape.smem != (size_t)p.H * 2 ||
+        (long long)shape.threads * shape.vpt < p.H8)
+        return cudaErrorInvalidValue;
+    p.epr_magic = owner_magic(p.Epr);
+    p.T_magic = div_magic(p.T);  // exact: tokens < 2^13, T <= 256
+    return by_vpt<SmallFp8>(shape.vpt, [&](auto f) { return decltype(f)::launch(p, shape, st); });
 }
 
 }  // namespace moe

@@ -17,6 +17,7 @@
 
 #include <cuda_runtime.h>
 
+#include "dispatch_small.h"
 #include "expert.h"
 #include "kernels.h"
 
@@ -49,6 +50,12 @@ int gemm_group_m(const moe::Tuning &tn) {
 // T = 64 14.3 vs 18.2-19.1 us, T = 128 20.9 vs 24.5-25.3 us, T = 256
 // 33.3-35.2 vs 38.4-38.7 us.
 constexpr int kSmallDispatchMaxT = 256;
+
+// The same for FP8 receive rows (one CTA per token, dispatch_small.cu):
+// measured faster than the routing passes + FP8 row copy up to 128 tokens
+// per rank (T = 1 10.2 vs 14.9 us, T = 64 13.4 vs 16.8, T = 128 16.4 vs
+// 21.0) and slower at 256 (30.7 vs 26.5: 2048 CTAs in waves).
+constexpr int kSmallFp8MaxT = 128;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -193,6 +200,9 @@ struct moe_a2a {
     int fp8_stages;  // FP8 dispatch ring depth and shape (H % 16 == 0 only)
     moe::LaunchShape fp8_shape;
     moe::DispatchSmallShapes small;  // one-launch dispatch (rank layout)
+    moe::DispatchSmallFp8Shape small_fp8;  // its FP8 receive-row variant
+    bool small_fp8_ok;
+    int small_fp8_max;  // MOE_DISPATCH_SMALL_FP8_MAX (0: the default, -1: never)
     moe::SmallCombineShape small_combine;  // cluster combine for small batches
     bool small_combine_ok;
     // Local-expert counts: the region holding the current dispatch's counts,
@@ -242,6 +252,9 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
     if (h->L.layout == MOE_LAYOUT_RANK &&
         moe::dispatch_small_prepare(2 * h->cfg.hidden, h->num_sms, &h->small) != cudaSuccess)
         return MOE_ERR_CUDA;
+    h->small_fp8_ok = h->L.layout == MOE_LAYOUT_RANK && h->cfg.hidden % 16 == 0 &&
+                      moe::dispatch_small_fp8_prepare(h->cfg.hidden, &h->small_fp8) ==
+                          cudaSuccess;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     h->overlap = h->L.layout == MOE_LAYOUT_RANK && h->tuning.route_overlap != 0;
@@ -339,10 +352,15 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
 // rows when every source holds the same T tokens, T at most one routing tile
 // and at most Tuning::dispatch_small_max (measured break-even, below).
 bool small_dispatch(const moe_a2a_t *h, const moe::TokenMap &map) {
-    if (h->L.layout != MOE_LAYOUT_RANK || h->recv_format != MOE_FORMAT_BF16 || !map.uniform)
-        return false;
-    const int lim = h->tuning.dispatch_small_max;
-    const int T_max = lim < 0 ? 0 : (lim == 0 ? kSmallDispatchMaxT : lim);
+    if (h->L.layout != MOE_LAYOUT_RANK || !map.uniform) return false;
+    int T_max = 0;
+    if (h->recv_format == MOE_FORMAT_BF16) {
+        const int lim = h->tuning.dispatch_small_max;
+        T_max = lim < 0 ? 0 : (lim == 0 ? kSmallDispatchMaxT : lim);
+    } else if (h->recv_format == MOE_FORMAT_FP8_E4M3 && h->small_fp8_ok) {
+        const int lim = h->small_fp8_max;
+        T_max = lim < 0 ? 0 : (lim == 0 ? kSmallFp8MaxT : lim);
+    }
     return map.stride >= 1 && map.stride <= T_max && map.stride <= moe::kRouteTile;
 }
 
@@ -436,34 +454,59 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
             cudaMemsetAsync(h->ws + bufs[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess)
             return MOE_ERR_CUDA;
         const int T = map.stride;
-        const int row_bytes = 2 * h->cfg.hidden;
-        const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
-        moe::DispatchSmallParams sp;
-        sp.topk_ids = d_topk_ids;
-        sp.topk_w = d_topk_w;
-        sp.x = static_cast<const uint8_t *>(d_x);
-        sp.recv_x = at<uint8_t>(h, h->L.recv_x);
-        sp.send_slot = at<int32_t>(h, h->L.send_slot);
-        sp.dest_weight = at<float>(h, h->L.dest_weight);
-        sp.src_token = at<int32_t>(h, h->L.src_token);
-        sp.recv_ids = at<int32_t>(h, h->L.recv_ids);
-        sp.recv_w = at<float>(h, h->L.recv_w);
-        sp.topk_dest = at<int8_t>(h, h->L.topk_dest);
-        sp.recv_counts = at<int32_t>(h, h->L.recv_counts);
-        sp.counts = at<int32_t>(h, bufs[sel]);
-        sp.counts_clear = at<int32_t>(h, bufs[sel ^ 1]);
-        sp.flags = flags;
-        sp.active = h->active;
-        sp.R = R, sp.K = K, sp.E = E, sp.Epr = E / R, sp.RP = RP, sp.m = m, sp.T = T;
-        sp.row_bytes = row_bytes;
-        sp.chunk_bytes = h->small.chunk_bytes[c];
-        sp.chunks = h->small.chunks[c];
-        sp.stages = h->small.stages;
-        sp.stage_bytes = h->small.stage_bytes[c];
-        sp.units = ntok * sp.chunks;
-        h->small_zero_ok = false;  // until the launch that clears the other buffer is queued
-        if (moe::launch_dispatch_small(sp, h->small.shape[c], st) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (h->recv_format == MOE_FORMAT_FP8_E4M3) {  // e4m3 rows, one CTA per token
+            moe::DispatchSmallFp8Params fp;
+            fp.topk_ids = d_topk_ids;
+            fp.topk_w = d_topk_w;
+            fp.x = static_cast<const uint16_t *>(d_x);
+            fp.recv_x8 = at<uint8_t>(h, h->L.recv_x);
+            fp.recv_scale = at<float>(h, h->L.recv_scale);
+            fp.send_slot = at<int32_t>(h, h->L.send_slot);
+            fp.dest_weight = at<float>(h, h->L.dest_weight);
+            fp.src_token = at<int32_t>(h, h->L.src_token);
+            fp.recv_ids = at<int32_t>(h, h->L.recv_ids);
+            fp.recv_w = at<float>(h, h->L.recv_w);
+            fp.topk_dest = at<int8_t>(h, h->L.topk_dest);
+            fp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+            fp.counts = at<int32_t>(h, bufs[sel]);
+            fp.counts_clear = at<int32_t>(h, bufs[sel ^ 1]);
+            fp.flags = flags;
+            fp.active = h->active;
+            fp.R = R, fp.K = K, fp.E = E, fp.Epr = E / R, fp.RP = RP, fp.m = m, fp.T = T;
+            fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
+            h->small_zero_ok = false;  // until the launch that clears the other buffer is queued
+            if (moe::launch_dispatch_small_fp8(fp, h->small_fp8, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        } else {
+            const int row_bytes = 2 * h->cfg.hidden;
+            const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
+            moe::DispatchSmallParams sp;
+            sp.topk_ids = d_topk_ids;
+            sp.topk_w = d_topk_w;
+            sp.x = static_cast<const uint8_t *>(d_x);
+            sp.recv_x = at<uint8_t>(h, h->L.recv_x);
+            sp.send_slot = at<int32_t>(h, h->L.send_slot);
+            sp.dest_weight = at<float>(h, h->L.dest_weight);
+            sp.src_token = at<int32_t>(h, h->L.src_token);
+            sp.recv_ids = at<int32_t>(h, h->L.recv_ids);
+            sp.recv_w = at<float>(h, h->L.recv_w);
+            sp.topk_dest = at<int8_t>(h, h->L.topk_dest);
+            sp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+            sp.counts = at<int32_t>(h, bufs[sel]);
+            sp.counts_clear = at<int32_t>(h, bufs[sel ^ 1]);
+            sp.flags = flags;
+            sp.active = h->active;
+            sp.R = R, sp.K = K, sp.E = E, sp.Epr = E / R, sp.RP = RP, sp.m = m, sp.T = T;
+            sp.row_bytes = row_bytes;
+            sp.chunk_bytes = h->small.chunk_bytes[c];
+            sp.chunks = h->small.chunks[c];
+            sp.stages = h->small.stages;
+            sp.stage_bytes = h->small.stage_bytes[c];
+            sp.units = ntok * sp.chunks;
+            h->small_zero_ok = false;  // until the launch that clears the other buffer is queued
+            if (moe::launch_dispatch_small(sp, h->small.shape[c], st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
         h->cur_counts = bufs[sel];
         h->small_sel = sel ^ 1;
         h->small_zero_ok = true;
@@ -732,6 +775,8 @@ int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_w
     h->phase = 0;
     h->active = cfg->ep_size >= 32 ? 0xffffffffu : ((1u << cfg->ep_size) - 1u);
     h->tuning = read_tuning();
+    h->small_fp8_max = env_int("MOE_DISPATCH_SMALL_FP8_MAX");
+    h->small_fp8_ok = false;
     *out = h;
     return MOE_OK;
 }

@@ -96,7 +96,20 @@ def run_dispatch_fp8(R, T, H, E, K, seed, m=None, counts=None, routing="uniform"
     r = oracle.route(ids_o, w, E, m)
     cnt = view.recv_counts.cpu().numpy()
     assert np.array_equal(cnt, r["recv_counts"])
-    assert np.array_equal(view.send_slot.cpu().numpy()[:, :, :R], r["send_slot"])
+    T_ = view.token_stride
+    assert np.array_equal(view.send_slot.cpu().numpy()[:, :T, :R], r["send_slot"][:, :T])
+    assert np.array_equal(view.local_expert_counts.cpu().numpy(), r["local_expert_counts"])
+    dw = view.dest_weight.cpu().numpy()[:, :T_, :R]
+    live = np.ones((R, T_), bool) if counts is None else \
+        np.array([[t < c for t in range(T_)] for c in counts])
+    assert np.array_equal(dw[live].view(np.uint32), r["wd"][:, :T_][live].view(np.uint32))
+    od = oracle.dispatch(ids_o, w, x, E, m, r)
+    rid, rw = view.recv_topk_ids.cpu().numpy(), view.recv_topk_w.cpu().numpy()
+    for d in range(R):
+        for s in range(R):
+            c = int(cnt[d, s])
+            assert np.array_equal(rid[d, s, :c], od["recv_ids"][d, s, :c])
+            assert np.array_equal(rw[d, s, :c].view(np.uint32), od["recv_w"][d, s, :c].view(np.uint32))
     q_ref, sc_ref = oracle.quantize_rows_fp8(x)            # [R, T, H], [R, T]
     gq, gs = u8(view.recv_x), view.recv_scale.cpu().numpy()
     src = view.src_token.cpu().numpy()
@@ -117,6 +130,19 @@ def run_dispatch_fp8(R, T, H, E, K, seed, m=None, counts=None, routing="uniform"
                                        (8, 64, 7168, 256, 8)])
 def test_fp8_dispatch_codes_and_scales_bit_exact(R, T, H, E, K):
     run_dispatch_fp8(R, T, H, E, K, seed=R + K)
+
+
+@pytest.mark.parametrize("small_max", ["-1", "256"])
+@pytest.mark.parametrize("T", [1, 33, 64, 200])
+def test_fp8_one_launch_dispatch_modes(monkeypatch, small_max, T):
+    # Up to 128 tokens per rank by default ("256" here for every size) the FP8
+    # dispatch is one launch: one CTA per token derives the token's slots from
+    # the ids before it, reduces the row's amax and stores its codes; "-1"
+    # forces the routing passes and the FP8 row copy.  Both must equal the
+    # oracle, routing tables and local-expert counts included.
+    monkeypatch.setenv("MOE_DISPATCH_SMALL_FP8_MAX", small_max)
+    a, view, d = run_dispatch_fp8(6, T, 1040, 48, 5, seed=T, m=T + 3)
+    assert view.kernels == (1 if small_max == "256" else 3)
 
 
 @pytest.mark.parametrize("overlap", ["0", "1"])
