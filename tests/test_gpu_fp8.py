@@ -67,21 +67,23 @@ def code_step(c):
     return np.where(c & 0x80, -mag, mag)
 
 
-def run_dispatch_fp8(R, T, H, E, K, seed, m=None, counts=None, routing="uniform"):
+def run_dispatch_fp8(R, T, H, E, K, seed, m=None, counts=None, routing="uniform", dead=()):
     from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
     m = T if m is None else m
     ids = synth.topk_ids(seed, R, T, E, K, routing)
     w = synth.topk_weights(seed, R, T, K)
     x = edge_rows(synth.per_rank_rows(seed, synth.X, R, T, H), H)
+    ids_o = ids.copy()
     if counts is not None:
-        ids_o = ids.copy()
         for s, c in enumerate(counts):
             ids_o[s, c:] = -1
-    else:
-        ids_o = ids
+    for d in dead:  # an expert on a dead rank is an absent expert
+        ids_o[(ids_o >= 0) & (ids_o // (E // R) == d)] = -1
     a = MoeA2A(R, m, H, E, K, "cuda")
     a.workspace.fill_(parity.POISON)
     a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    if dead:
+        a.set_active_ranks(((1 << R) - 1) & ~sum(1 << d for d in dead))
     dev = parity.to_dev
     if counts is not None:
         view = a.dispatch_varlen(dev(ids, torch.int32), dev(w, torch.float32),
@@ -143,6 +145,17 @@ def test_fp8_one_launch_dispatch_modes(monkeypatch, small_max, T):
     monkeypatch.setenv("MOE_DISPATCH_SMALL_FP8_MAX", small_max)
     a, view, d = run_dispatch_fp8(6, T, 1040, 48, 5, seed=T, m=T + 3)
     assert view.kernels == (1 if small_max == "256" else 3)
+
+
+@pytest.mark.parametrize("small_max", ["-1", "0"])
+def test_fp8_dispatch_dead_ranks(monkeypatch, small_max):
+    # ranks 1 and 6 dead: they receive nothing, and the tokens' other
+    # destinations keep the oracle's slots (one launch and routing passes)
+    monkeypatch.setenv("MOE_DISPATCH_SMALL_FP8_MAX", small_max)
+    a, view, d = run_dispatch_fp8(8, 60, 512, 64, 8, seed=9, dead=(1, 6))
+    cnt = view.recv_counts.cpu().numpy()
+    assert cnt[1].sum() == 0 and cnt[6].sum() == 0
+    assert view.kernels == (1 if small_max == "0" else 3)
 
 
 @pytest.mark.parametrize("overlap", ["0", "1"])
