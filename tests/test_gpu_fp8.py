@@ -221,9 +221,13 @@ def _dispatch_bf16(R, T, H, E, K, seed):
     return a, view, r
 
 
-@pytest.mark.parametrize("weighted", [False, True])
-@pytest.mark.parametrize("R,T,H,E,K", [(6, 300, 136, 48, 5), (8, 512, 7168, 256, 8)])
+@pytest.mark.parametrize("weighted,R,T,H,E,K", [(False, 6, 300, 136, 48, 5),
+                                                 (True, 6, 300, 136, 48, 5),
+                                                 (False, 8, 512, 7168, 256, 8),
+                                                 (True, 8, 512, 7168, 256, 8),
+                                                 (True, 8, 4096, 7168, 256, 8)])
 def test_fp8_combine_unfused_bit_exact(weighted, R, T, H, E, K):
+    # the last case: a prefill-sized call (32 768 tokens), every token compared
     a, view, r = _dispatch_bf16(R, T, H, E, K, seed=11)
     cnt = view.recv_counts.cpu().numpy()
     eo = _payload(a, cnt, T, H, 11)
@@ -237,9 +241,13 @@ def test_fp8_combine_unfused_bit_exact(weighted, R, T, H, E, K):
     assert (s_ref[:3] == 1.0).all() and (q_ref[:3] == 0).all()      # empty tokens
 
 
-@pytest.mark.parametrize("weighted", [False, True])
-@pytest.mark.parametrize("R,T,H,E,K", [(6, 300, 136, 48, 5), (8, 512, 7168, 256, 8)])
+@pytest.mark.parametrize("weighted,R,T,H,E,K", [(False, 6, 300, 136, 48, 5),
+                                                 (True, 6, 300, 136, 48, 5),
+                                                 (False, 8, 512, 7168, 256, 8),
+                                                 (True, 8, 512, 7168, 256, 8),
+                                                 (True, 8, 4096, 7168, 256, 8)])
 def test_fp8_combine_fused(weighted, R, T, H, E, K):
+    # the last case: a prefill-sized call (32 768 tokens), every token compared
     a, view, r = _dispatch_bf16(R, T, H, E, K, seed=12)
     cnt = view.recv_counts.cpu().numpy()
     eo = _payload(a, cnt, T, H, 12)
