@@ -710,6 +710,72 @@ void oracle_expert_gemm_fp8(int E, long cap, int H, int N, const int32_t *recv_c
     }
 }
 
+/*
+ * The product on the rank planes with FP8 operands: the received rows as the
+ * FP8 receive format holds them (e4m3 codes qx, one scale sx per received
+ * row), the weights as e4m3 codes qw with one scale sw per output channel.
+ * Readings: as oracle_expert_gemm_rank, with each expert output formed from
+ * the dequantised operands as in oracle_expert_gemm_fp8,
+ *   y_k[n] = bf16_rn(f32_rn(sx * sw[e_k][n] * sum_h f(qx[h]) * f(qw[e_k][n][h])))
+ * (the product and the scaling exact here, in double), then
+ *   msg[n] = bf16_rn(sum over k ascending with recv_ids[k] >= 0 of g_k * y_k[n])
+ * in binary32 from +0.0, one multiply and one add per term.  recv_x8
+ * [R][R][m][H] codes, recv_scale [R][R][m], qw [E][N][H], sw [E][N]; rows,
+ * msg, ymag and smag as in oracle_expert_gemm_rank (the magnitudes include
+ * |sx sw|).
+ */
+void oracle_expert_gemm_rank_fp8(int R, int m, int K, int H, int N,
+                                 const int32_t *recv_counts, const uint8_t *recv_x8,
+                                 const float *recv_scale, const int32_t *recv_ids,
+                                 const float *recv_w, const uint8_t *qw, const float *sw,
+                                 int apply_gates, const int64_t *rows, long n_rows,
+                                 uint16_t *msg, double *ymag, double *smag)
+{
+    long total = rows != NULL ? n_rows : (long)R * R * m;
+    for (long i = 0; i < total; ++i) {
+        long flat = rows != NULL ? (long)rows[i] : i;
+        long plane = flat / m;
+        long j = flat - plane * m;
+        int d = (int)(plane / R), s = (int)(plane % R);
+        if (d >= R || j >= recv_counts[d * R + s])
+            continue;
+        const uint8_t *xr = recv_x8 + (size_t)flat * H;
+        const double sx = (double)recv_scale[flat];
+        const int32_t *ids = recv_ids + (size_t)flat * K;
+        const float *g = recv_w + (size_t)flat * K;
+        for (int n = 0; n < N; ++n) {
+            float a = 0.0f;
+            double ym = 0.0, sm = 0.0;
+            for (int k = 0; k < K; ++k) {
+                int e = ids[k];
+                if (e < 0)
+                    continue;
+                const uint8_t *wr = qw + ((size_t)e * N + n) * H;
+                const double scale = sx * (double)sw[(size_t)e * N + n];
+                double acc = 0.0, mag = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    double prod = (double)oracle_f32_from_fp8e4m3(xr[h]) *
+                                  (double)oracle_f32_from_fp8e4m3(wr[h]);
+                    acc += prod;
+                    mag += fabs(prod);
+                }
+                double y = scale * acc;
+                float yk = oracle_f32_from_bf16(oracle_bf16_from_f32((float)y));
+                float gk = apply_gates ? g[k] : 1.0f;
+                float p = gk * yk;
+                a = a + p;
+                ym += fabs((double)gk) * fabs(y);
+                sm += fabs((double)gk) * fabs(scale) * mag;
+            }
+            msg[(size_t)flat * N + n] = oracle_bf16_from_f32(a);
+            if (ymag != NULL)
+                ymag[(size_t)flat * N + n] = ym;
+            if (smag != NULL)
+                smag[(size_t)flat * N + n] = sm;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* FP8 (OCP e4m3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no  */
 /* infinity, NaN = S.1111.111, largest finite 448) and per-token scaling     */

@@ -56,6 +56,9 @@ def _bind(handle):
     handle.oracle_expert_gemm_rank.argtypes = ([c_int] * 5 + [p] * 5 + [c_int, p, c_long]
                                                + [p] * 3)
     handle.oracle_expert_gemm_rank.restype = None
+    handle.oracle_expert_gemm_rank_fp8.argtypes = ([c_int] * 5 + [p] * 7 + [c_int, p, c_long]
+                                                   + [p] * 3)
+    handle.oracle_expert_gemm_rank_fp8.restype = None
     handle.oracle_f32_from_fp8e4m3.argtypes = [ctypes.c_uint8]
     handle.oracle_f32_from_fp8e4m3.restype = c_float
     handle.oracle_fp8e4m3_from_f32.argtypes = [c_float]
@@ -354,6 +357,38 @@ def expert_gemm_fp8(qx, sx, qw, sw, recv_counts, handle=None):
                              _ptr(_need(sx, np.float32, (E, cap))), _ptr(qwb),
                              _ptr(_need(sw, np.float32, (E, N))), _ptr(y))
     return y
+
+
+def expert_gemm_rank_fp8(recv_x8, recv_scale, recv_ids, recv_w, recv_counts, qw, sw,
+                         apply_gates=True, rows=None, magnitudes=False, handle=None):
+    """The rank-plane product on FP8 operands (oracle_expert_gemm_rank_fp8):
+    recv_x8 [R, R, m, H] uint8 e4m3 codes with recv_scale [R, R, m] float32,
+    recv_ids [R, R, m, K] int32, recv_w [R, R, m, K] float32, recv_counts
+    [R, R], qw [E, N, H] uint8 codes with sw [E, N] float32.  Returns msg
+    uint16 [R, R, m, N] (0xFFFF in rows not computed) and, with
+    magnitudes=True, also ymag and smag float64 of the same shape."""
+    h = handle or lib()
+    xb = _need(recv_x8, np.uint8)
+    R, R2, m, H = xb.shape
+    ids = _need(recv_ids, np.int32)
+    K = ids.shape[-1]
+    if R2 != R or ids.shape != (R, R, m, K):
+        raise ValueError("recv_ids must be [R, R, m, K]")
+    wb = _need(qw, np.uint8)
+    E, N = wb.shape[0], wb.shape[1]
+    if wb.shape[2] != H:
+        raise ValueError("qw must be [E, N, H]")
+    rl = None if rows is None else _need(rows, np.int64)
+    msg = np.full((R, R, m, N), 0xFFFF, np.uint16)
+    ym = np.full((R, R, m, N), np.nan, np.float64) if magnitudes else None
+    sm = np.full((R, R, m, N), np.nan, np.float64) if magnitudes else None
+    h.oracle_expert_gemm_rank_fp8(R, m, K, H, N, _ptr(_need(recv_counts, np.int32, (R, R))),
+                                  _ptr(xb), _ptr(_need(recv_scale, np.float32, (R, R, m))),
+                                  _ptr(ids), _ptr(_need(recv_w, np.float32, ids.shape)),
+                                  _ptr(wb), _ptr(_need(sw, np.float32, (E, N))),
+                                  int(bool(apply_gates)), _ptr(rl),
+                                  0 if rl is None else rl.shape[0], _ptr(msg), _ptr(ym), _ptr(sm))
+    return (msg, ym, sm) if magnitudes else msg
 
 
 def fp8_bits(values, handle=None):

@@ -121,6 +121,36 @@ MUTANTS = {
     "gemm_rank_wrong_expert_weights": (
         "const uint16_t *wr = w + ((size_t)e * N + n) * H;\n                double y = 0.0, mag = 0.0;",
         "const uint16_t *wr = w + ((size_t)(e ^ 1) * N + n) * H;\n                double y = 0.0, mag = 0.0;"),
+    "gemm_rank_fp8_ignores_row_scale": (
+        "const double scale = sx * (double)sw[(size_t)e * N + n];",
+        "const double scale = (double)sw[(size_t)e * N + n];"),
+    "gemm_rank_fp8_ignores_channel_scale": (
+        "const double scale = sx * (double)sw[(size_t)e * N + n];",
+        "const double scale = sx;"),
+    "gemm_rank_fp8_next_row_scale": (
+        "const double sx = (double)recv_scale[flat];",
+        "const double sx = (double)recv_scale[(flat + 1) % ((long)R * R * m)];"),
+    "gemm_rank_fp8_descending_k": (
+        "for (int k = 0; k < K; ++k) {\n                int e = ids[k];\n                if (e < 0)\n                    continue;\n                const uint8_t *wr",
+        "for (int k = K - 1; k >= 0; --k) {\n                int e = ids[k];\n                if (e < 0)\n                    continue;\n                const uint8_t *wr"),
+    "gemm_rank_fp8_expert_output_not_narrowed": (
+        "double y = scale * acc;\n                float yk = oracle_f32_from_bf16(oracle_bf16_from_f32((float)y));",
+        "double y = scale * acc;\n                float yk = (float)y;"),
+    "gemm_rank_fp8_gates_ignored": (
+        "double y = scale * acc;\n                float yk = oracle_f32_from_bf16(oracle_bf16_from_f32((float)y));\n                float gk = apply_gates ? g[k] : 1.0f;",
+        "double y = scale * acc;\n                float yk = oracle_f32_from_bf16(oracle_bf16_from_f32((float)y));\n                float gk = 1.0f;"),
+    "gemm_rank_fp8_uses_fma": (
+        "float gk = apply_gates ? g[k] : 1.0f;\n                float p = gk * yk;\n                a = a + p;\n                ym += fabs((double)gk) * fabs(y);\n                sm += fabs((double)gk) * fabs(scale) * mag;",
+        "float gk = apply_gates ? g[k] : 1.0f;\n                a = fmaf(gk, yk, a);\n                ym += fabs((double)gk) * fabs(y);\n                sm += fabs((double)gk) * fabs(scale) * mag;"),
+    "gemm_rank_fp8_wrong_expert_weights": (
+        "const uint8_t *wr = qw + ((size_t)e * N + n) * H;\n                const double scale",
+        "const uint8_t *wr = qw + ((size_t)(e ^ 1) * N + n) * H;\n                const double scale"),
+    "gemm_rank_fp8_weights_transposed": (
+        "double prod = (double)oracle_f32_from_fp8e4m3(xr[h]) *\n                                  (double)oracle_f32_from_fp8e4m3(wr[h]);",
+        "double prod = (double)oracle_f32_from_fp8e4m3(xr[h]) *\n                                  (double)oracle_f32_from_fp8e4m3(qw[(size_t)e * N * H + (size_t)(h % N) * H + n % H]);"),
+    "gemm_rank_fp8_reads_first_row_of_plane": (
+        "const uint8_t *xr = recv_x8 + (size_t)flat * H;",
+        "const uint8_t *xr = recv_x8 + (size_t)(flat - j) * H;"),
     "dispatch_copies_wrong_source_token": (
         "const uint16_t *row = x + ((size_t)s * T + t) * H;",
         "const uint16_t *row = x + ((size_t)s * T + (t + 1) % T) * H;"),
@@ -165,6 +195,9 @@ class MutantOracle:
 
     def expert_gemm_rank(self, *a, **k):
         return real.expert_gemm_rank(*a, handle=self.h, **k)
+
+    def expert_gemm_rank_fp8(self, *a, **k):
+        return real.expert_gemm_rank_fp8(*a, handle=self.h, **k)
 
     def expert_gemm_fp8(self, *a, **k):
         return real.expert_gemm_fp8(*a, handle=self.h, **k)
@@ -222,6 +255,12 @@ PIN_TESTS = [
     (pins.test_expert_gemm_rank_matches_library_matmul_and_gate_order, {}),
     (pins.test_expert_gemm_rank_equals_expert_layout_with_one_expert_per_rank, {}),
     (pins.test_expert_gemm_rank_sums_in_top_k_order, {}),
+    (pins.test_expert_gemm_rank_fp8_identity_codes_count_local_experts, {}),
+    (pins.test_expert_gemm_rank_fp8_matches_library_matmul_and_gate_order, {}),
+    (pins.test_expert_gemm_rank_fp8_equals_expert_layout_with_one_expert_per_rank, {}),
+    (pins.test_expert_gemm_rank_fp8_sums_in_top_k_order, {}),
+    (pins.test_expert_gemm_rank_fp8_row_list_matches_full, {}),
+    (pins.test_expert_gemm_rank_fp8_gate_product_is_not_fused, {}),
 ]
 
 

@@ -1021,3 +1021,179 @@ def test_expert_gemm_rank_sums_in_top_k_order(oracle):
     msg = oracle.expert_gemm_rank(d["recv_x"], d["recv_ids"], d["recv_w"], r["recv_counts"], W,
                                   apply_gates=False)
     assert (f32(msg[0, 0, 0]) == 0.0).all()
+
+
+# --------------------------------------------------------------------------
+# The product on the rank planes with FP8 operands: the FP8 receive rows
+# (codes and one scale per row) times FP8 weights (one scale per channel)
+# --------------------------------------------------------------------------
+
+def _fp8_rank_planes(oracle, R, T, K, E, H, seed):
+    """Rank planes whose rows are the oracle's FP8 quantisation of each
+    token, placed at the slots the routing gives (src_token)."""
+    ids, w, x, r, d = _rank_planes(oracle, R, T, K, E, H, seed)
+    q, sc = oracle.quantize_rows_fp8(x)
+    m = T
+    qx = np.zeros((R, R, m, H), np.uint8)
+    sx = np.zeros((R, R, m), np.float32)
+    for dd in range(R):
+        for s in range(R):
+            for j in range(r["recv_counts"][dd, s]):
+                t = r["src_token"][dd, s, j]
+                qx[dd, s, j] = q[s, t]
+                sx[dd, s, j] = sc[s, t]
+    return ids, w, x, r, d, qx, sx
+
+
+def _bf16_of(v):
+    import torch
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def test_expert_gemm_rank_fp8_identity_codes_count_local_experts(oracle):
+    # qw = identity codes (0x38 = 1.0), unit channel scales, no gates: each
+    # expert output is bf16(f32(sx * f(qx))) and the message is n times it,
+    # n the row's local ids (n * y exact in binary32 for bf16 y, n <= 2)
+    R, T, K, E, H = 4, 30, 4, 8, 32
+    ids, w, x, r, d, qx, sx = _fp8_rank_planes(oracle, R, T, K, E, H, seed=31)
+    eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+    msg = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                      np.stack([eye] * E), np.ones((E, H), np.float32),
+                                      apply_gates=False)
+    fx = oracle.fp8_to_f32(qx).astype(np.float64)
+    seen = set()
+    for dd in range(R):
+        for s in range(R):
+            c = r["recv_counts"][dd, s]
+            n = (d["recv_ids"][dd, s, :c] >= 0).sum(axis=1).astype(np.float32)
+            seen.update(n.tolist())
+            y = f32(_bf16_of((fx[dd, s, :c] * sx[dd, s, :c, None]).astype(np.float32)))
+            assert np.array_equal(msg[dd, s, :c], _bf16_of(y * n[:, None]))
+            assert (msg[dd, s, c:] == 0xFFFF).all()       # rows past a count untouched
+    assert {1.0, 2.0} <= seen
+
+
+def test_expert_gemm_rank_fp8_matches_library_matmul_and_gate_order(oracle):
+    # random weight codes and channel scales: each local expert's output is
+    # numpy's float64 matmul of the decoded codes (exact: few-bit products,
+    # short sums) times sx * sw, rounded to binary32 and bf16; the gates in
+    # binary32 in ascending k, one product and one sum per term, then bf16
+    R, T, K, E, H, N = 3, 14, 4, 12, 32, 40
+    ids, w, x, r, d, qx, sx = _fp8_rank_planes(oracle, R, T, K, E, H, seed=32)
+    rng = np.random.default_rng(33)
+    qw = rng.integers(0, 256, (E, N, H)).astype(np.uint8)
+    qw[(qw & 0x7F) == 0x7F] = 0x21                      # no NaN codes
+    sw = rng.uniform(0.01, 2.0, (E, N)).astype(np.float32)
+    msg, ym, sm = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"],
+                                              r["recv_counts"], qw, sw, apply_gates=True,
+                                              magnitudes=True)
+    fx = oracle.fp8_to_f32(qx).astype(np.float64)
+    fw = oracle.fp8_to_f32(qw).astype(np.float64)
+    for dd in range(R):
+        for s in range(R):
+            for j in range(r["recv_counts"][dd, s]):
+                acc = np.zeros(N, np.float32)
+                ymag = np.zeros(N)
+                for k in range(K):
+                    e = d["recv_ids"][dd, s, j, k]
+                    if e < 0:
+                        continue
+                    y = (fw[e] @ fx[dd, s, j]) * (float(sx[dd, s, j]) * sw[e].astype(np.float64))
+                    g = d["recv_w"][dd, s, j, k]
+                    acc = (acc + (np.float32(g) * f32(_bf16_of(y.astype(np.float32))))
+                           .astype(np.float32)).astype(np.float32)
+                    ymag += abs(float(g)) * np.abs(y)
+                assert np.array_equal(msg[dd, s, j], _bf16_of(acc))
+                assert np.allclose(ym[dd, s, j], ymag, rtol=1e-12, atol=0)
+                assert (sm[dd, s, j] >= ym[dd, s, j] * (1 - 1e-12)).all()
+
+
+def test_expert_gemm_rank_fp8_equals_expert_layout_with_one_expert_per_rank(oracle):
+    # one expert per rank: each received row carries exactly one local
+    # expert, so without gates the message is bf16 of the expert-layout FP8
+    # product of the same codes and scales
+    R, T, K, H, N = 4, 16, 2, 32, 48
+    E = R
+    ids, w, x, r, d, qx, sx = _fp8_rank_planes(oracle, R, T, K, E, H, seed=34)
+    rng = np.random.default_rng(35)
+    qw = rng.integers(0, 256, (E, N, H)).astype(np.uint8)
+    qw[(qw & 0x7F) == 0x7F] = 0x13
+    sw = rng.uniform(0.1, 1.0, (E, N)).astype(np.float32)
+    msg = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                      qw, sw, apply_gates=False)
+    cap = R * T
+    qe = np.zeros((E, cap, H), np.uint8)
+    se = np.zeros((E, cap), np.float32)
+    counts = np.zeros(E, np.int32)
+    rows = []
+    for e in range(E):
+        for s in range(R):
+            for j in range(r["recv_counts"][e, s]):
+                qe[e, counts[e]] = qx[e, s, j]
+                se[e, counts[e]] = sx[e, s, j]
+                rows.append(msg[e, s, j])
+                counts[e] += 1
+    y = oracle.expert_gemm_fp8(qe, se, qw, sw, counts)
+    want = np.concatenate([_bf16_of(y[e, :counts[e]].astype(np.float32)) for e in range(E)])
+    assert np.array_equal(np.stack(rows), want)
+
+
+def test_expert_gemm_rank_fp8_sums_in_top_k_order(oracle):
+    # one row, three local experts in top-k order [2, 0, 1], codes 1.0
+    # everywhere on the diagonal and channel scales 2^24, 1, -2^24: ascending k
+    # gives (2^24 + 1) - 2^24 = 0 in binary32; other orders give 1
+    R, T, K, E, H = 1, 1, 3, 4, 16
+    ids = np.array([[[2, 0, 1]]], np.int32)
+    w = np.ones((R, T, K), np.float32)
+    x = bits(np.ones((R, T, H), np.float32))
+    r = oracle.route(ids, w, E, T)
+    d = oracle.dispatch(ids, w, x, E, T, r)
+    qx = np.full((R, R, T, H), 0x38, np.uint8)
+    sx = np.ones((R, R, T), np.float32)
+    eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+    c = {2: 2.0 ** 24, 0: 1.0, 1: -2.0 ** 24, 3: 0.0}
+    sw = np.stack([np.full(H, c[e], np.float32) for e in range(E)])
+    msg = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                      np.stack([eye] * E), sw, apply_gates=False)
+    assert (f32(msg[0, 0, 0]) == 0.0).all()
+
+
+def test_expert_gemm_rank_fp8_row_list_matches_full(oracle):
+    # the listed-row form computes exactly the listed rows of the full call
+    R, T, K, E, H, N = 2, 12, 4, 8, 32, 16
+    ids, w, x, r, d, qx, sx = _fp8_rank_planes(oracle, R, T, K, E, H, seed=36)
+    rng = np.random.default_rng(37)
+    qw = rng.integers(0, 0x70, (E, N, H)).astype(np.uint8)
+    sw = rng.uniform(0.1, 1.0, (E, N)).astype(np.float32)
+    full = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                       qw, sw)
+    flat = [(dd * R + s) * T + j for dd in range(R) for s in range(R)
+            for j in range(r["recv_counts"][dd, s])][::3]
+    part = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                       qw, sw, rows=np.array(flat, np.int64))
+    fm, pm = full.reshape(-1, N), part.reshape(-1, N)
+    assert np.array_equal(pm[flat], fm[flat])
+    others = np.setdiff1d(np.arange(fm.shape[0]), flat)
+    assert (pm[others] == 0xFFFF).all()
+
+
+def test_expert_gemm_rank_fp8_gate_product_is_not_fused(oracle):
+    # two local experts with outputs 1 and 1 + 2^-7 (unit codes, channel
+    # scales 1 and 1 + 2^-7), gates 1 and 1 + 2^-23.  Unfused: the product
+    # rounds to 1 + 2^-7 + 2^-23, the sum 2 + 2^-7 + 2^-23 is a binary32 tie
+    # that goes to 2 + 2^-7, a bf16 tie that goes to 2.  Fused, the sum sits
+    # above both ties and the message is 2 + 2^-6.
+    R, T, K, E, H = 1, 1, 2, 2, 16
+    ids = np.array([[[0, 1]]], np.int32)
+    w = np.array([[[1.0, 1.0 + 2.0 ** -23]]], np.float32)
+    x = bits(np.ones((R, T, H), np.float32))
+    r = oracle.route(ids, w, E, T)
+    d = oracle.dispatch(ids, w, x, E, T, r)
+    qx = np.full((R, R, T, H), 0x38, np.uint8)
+    sx = np.ones((R, R, T), np.float32)
+    eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+    sw = np.stack([np.ones(H, np.float32), np.full(H, 1.0 + 2.0 ** -7, np.float32)])
+    msg = oracle.expert_gemm_rank_fp8(qx, sx, d["recv_ids"], d["recv_w"], r["recv_counts"],
+                                      np.stack([eye] * E), sw, apply_gates=True)
+    assert (f32(msg[0, 0, 0]) == 2.0).all()
