@@ -70,7 +70,8 @@ def parse_args():
                          "weights W_e of H x H, output into the combine payload): one step is "
                          "a whole single-matrix MoE layer.  Expert layout by default; with "
                          "--layout rank the product runs on the rank planes and applies the "
-                         "gates, and the combine is the unweighted rank sum")
+                         "gates, and the combine is the unweighted rank sum; with --fp8 the "
+                         "product takes the e4m3 receive rows and e4m3 weights")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 payloads: e4m3 dispatch rows with a per-token scale and an "
                          "e4m3 combine output with a per-token scale (needs hidden %% 16 == 0)")
@@ -83,8 +84,6 @@ def parse_args():
             ap.error("--expert-gemm takes direct calls")
         if args.layout is None:
             args.layout = "expert"
-        if args.layout == "rank" and args.fp8:
-            ap.error("the rank-plane product takes bf16 rows")
     if args.layout is None:
         args.layout = "rank"
     return args
@@ -388,9 +387,14 @@ def run_gpu(args, w, rank, world, local_rank):
             w8 = w_exp.to(torch.float8_e4m3fn)
             del w_exp
             w8_scale = torch.full((E, H), 1.0 / H ** 0.5, dtype=torch.float32, device=dev)
+            if gemm_rank:
+                a2a.expert_gemm_rank_fp8(w8, w8_scale, True)   # allocates its scratch, untimed
 
-            def run_gemm():
-                a2a.expert_gemm_fp8(w8, w8_scale)   # into the combine payload
+                def run_gemm():
+                    a2a.expert_gemm_rank_fp8(w8, w8_scale, True)   # gated, into the payload
+            else:
+                def run_gemm():
+                    a2a.expert_gemm_fp8(w8, w8_scale)   # into the combine payload
         elif gemm_rank:
             w_exp.mul_(1.0 / H ** 0.5)
             a2a.expert_gemm_rank(w_exp, True)   # allocates its scratch once, untimed

@@ -12,9 +12,9 @@
 //
 // GB300 design: a persistent kernel, one CTA per SM, over the useful
 // 128 x BN output tiles only (tile list built in shared memory from the
-// device-side row counts; raster: expert by expert, groups of 8 row tiles,
-// column tile outer inside a group, so that concurrent CTAs share weight and
-// row tiles in L2).  Six warps:
+// device-side row counts; raster: expert by expert, groups of row tiles
+// (16 by default), column tile outer inside a group, so that concurrent CTAs
+// share weight and row tiles in L2).  Six warps:
 //   warp 4, one thread: TMA producer -- 2-D tiled loads (128-byte swizzle)
 //     of the A tile (128 rows x 64 of x) and the B tile (BN rows x 64 of W)
 //     into a ring of shared-memory stages that runs on across tiles;
@@ -26,6 +26,9 @@
 //     of the tile) 32 columns at a time, narrows to bf16, stores the rows
 //     below the expert's count and frees the accumulator, while the MMA
 //     thread already fills the other one.
+// FP8 operands (either row source): e4m3 codes, 128 per stage row, products
+// of .kind::f8f6f4 into the same fp32 accumulators; the epilogue multiplies
+// by the A row's scale and the column's scale before the bf16 narrowing.
 #include "expert.h"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
         const int lw = warp - kLoaderWarp0;
         const int c = lane & 7, sub = lane >> 3;
         const uint8_t *xb = static_cast<const uint8_t *>(p.x);
-        const size_t row_bytes = (size_t)p.H * 2;
+        const size_t row_bytes = (size_t)p.H * (FP8 ? 1 : 2);  // e4m3 codes or bf16
         uint32_t kc = 0;
         for (int t = blockIdx.x; t < ntiles && !s_failed; t += gridDim.x) {
             int e, mt, nt;
@@ -310,25 +313,29 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
             tm.of(t, e, mt, nt);
             const int r = mt * kBM + 32 * warp + lane;  // row within the expert
             const bool live = r < s_count[e];
-            // FP8 operands: y = acc * sx[row] * sw[column], two fp32 products
-            const float sx = (FP8 && live) ? p.x_scale[(long long)e * p.cap + r] : 1.0f;
-            const float *swr = FP8 ? p.w_scale + (long long)e * p.N + (long long)nt * BN : nullptr;
             long long orow = GATHER ? (long long)s_pbase[e] + r : (long long)e * p.cap + r;
+            long long xrow = orow;  // the A row (its FP8 scale)
             // Rank planes: a row whose only local expert this is gets its
             // final message here, bf16(+0 + g * bf16(y)), in the caller's
             // output; the others' bf16 outputs go to the pair-major buffer.
             float gate = 0.0f;
             bool direct = false;
             if constexpr (GATHER) {
+                xrow = 0;
                 if (live) {
                     const int32_t pr = __ldg(p.pair_row + orow);
+                    xrow = pr & 0x7fffffff;
+                    if (xrow >= p.a_rows) xrow = 0;  // (the loaders flag such a row)
                     direct = pr < 0;  // bit 31: the row's only local expert
                     if (direct) {
                         gate = __ldg(p.pair_gate + orow);
-                        orow = pr & 0x7fffffff;
+                        orow = xrow;
                     }
                 }
             }
+            // FP8 operands: y = acc * sx[row] * sw[column], two fp32 products
+            const float sx = (FP8 && live) ? __ldg(p.x_scale + xrow) : 1.0f;
+            const float *swr = FP8 ? p.w_scale + (long long)e * p.N + (long long)nt * BN : nullptr;
             __nv_bfloat16 *dst_row =
                 (direct ? reinterpret_cast<__nv_bfloat16 *>(p.final_out) : out) + orow * p.N +
                 (long long)nt * BN;
@@ -451,16 +458,18 @@ cudaError_t launch_expert_gemm(const ExpertGemmParams &p, cudaStream_t st) {
     if (p.H % bk != 0 || p.H < bk || p.N % 128 != 0 || p.N < 128 || p.cap < 1 ||
         p.E > kMaxExpertsExpertLayout || p.group_m < 1)
         return cudaErrorInvalidValue;
-    if (p.gather) {  // rank planes: bf16 rows gathered through pair_row
-        if (p.fp8 || p.pair_row == nullptr) return cudaErrorInvalidValue;
+    if (p.fp8 && (p.x_scale == nullptr || p.w_scale == nullptr)) return cudaErrorInvalidValue;
+    if (p.gather) {  // rank planes: rows gathered through pair_row
+        if (p.pair_row == nullptr) return cudaErrorInvalidValue;
+        if (p.fp8)
+            return p.N % 256 == 0 ? launch_t<256, 4, true, true>(p, st)
+                                  : launch_t<128, 6, true, true>(p, st);
         return p.N % 256 == 0 ? launch_t<256, 4, false, true>(p, st)
                               : launch_t<128, 6, false, true>(p, st);
     }
-    if (p.fp8) {
-        if (p.x_scale == nullptr || p.w_scale == nullptr) return cudaErrorInvalidValue;
+    if (p.fp8)
         return p.N % 256 == 0 ? launch_t<256, 4, true, false>(p, st)
                               : launch_t<128, 6, true, false>(p, st);
-    }
     return p.N % 256 == 0 ? launch_t<256, 4, false, false>(p, st)
                           : launch_t<128, 6, false, false>(p, st);
 }

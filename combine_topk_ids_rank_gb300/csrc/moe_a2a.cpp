@@ -987,16 +987,22 @@ size_t moe_expert_gemm_rank_scratch_bytes(const moe_a2a_config_t *cfg, int32_t N
     return rank_scratch_layout(cfg, N, &S) ? S.total : 0;
 }
 
-int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply_gates,
-                         void *d_out, void *d_scratch, size_t scratch_bytes, void *stream) {
+namespace {
+
+int expert_gemm_rank_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int32_t N,
+                          int32_t apply_gates, void *d_out, void *d_scratch,
+                          size_t scratch_bytes, bool fp8, void *stream) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;
     if (h->phase != 1) return MOE_ERR_PHASE;
     const int H = h->cfg.hidden, E = h->cfg.num_experts, R = h->cfg.ep_size, K = h->cfg.top_k;
-    if (h->L.layout != MOE_LAYOUT_RANK || h->recv_format != MOE_FORMAT_BF16 ||
+    const int want = fp8 ? MOE_FORMAT_FP8_E4M3 : MOE_FORMAT_BF16;
+    if (h->L.layout != MOE_LAYOUT_RANK || h->recv_format != want ||
         E > moe::kMaxExpertsExpertLayout)
         return MOE_ERR_INVALID_ARG;
-    if (H % 64 != 0 || N < 128 || N % 128 != 0 || d_w == nullptr || !aligned(d_w, 16))
+    if (H % (fp8 ? 128 : 64) != 0 || N < 128 || N % 128 != 0 || d_w == nullptr ||
+        !aligned(d_w, 16))
         return MOE_ERR_INVALID_ARG;
+    if (fp8 && (d_w_scale == nullptr || !aligned(d_w_scale, 4))) return MOE_ERR_INVALID_ARG;
     if (d_out == nullptr && N != H) return MOE_ERR_INVALID_ARG;
     if (d_out != nullptr && !aligned(d_out, 16)) return MOE_ERR_INVALID_ARG;
     if (d_scratch == nullptr || !aligned(d_scratch, kAlign)) return MOE_ERR_INVALID_ARG;
@@ -1034,15 +1040,15 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     gp.w = d_w;
     gp.out = sc + S.y;
     gp.recv_counts = rp.pair_counts;
-    gp.x_scale = nullptr;
-    gp.w_scale = nullptr;
+    gp.x_scale = fp8 ? at<float>(h, h->L.recv_scale) : nullptr;  // [R][R][m]: per receive row
+    gp.w_scale = fp8 ? d_w_scale : nullptr;
     gp.flags = at<uint32_t>(h, h->L.flags);
     gp.E = E;
     gp.cap = R * m * K;  // pairs of one expert at most
     gp.H = H;
     gp.N = N;
     gp.mtiles = (gp.cap + 127) / 128;
-    gp.fp8 = 0;
+    gp.fp8 = fp8 ? 1 : 0;
     gp.gather = 1;
     gp.pair_row = rp.pair_row;
     gp.pair_gate = rp.pair_gate;
@@ -1051,6 +1057,21 @@ int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply
     gp.group_m = gemm_group_m(h->tuning);
     if (moe::launch_expert_gemm(gp, st) != cudaSuccess) return MOE_ERR_CUDA;
     return moe::launch_rank_aggregate(rp, h->num_sms, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply_gates,
+                         void *d_out, void *d_scratch, size_t scratch_bytes, void *stream) {
+    return expert_gemm_rank_impl(h, d_w, nullptr, N, apply_gates, d_out, d_scratch,
+                                 scratch_bytes, false, stream);
+}
+
+int moe_expert_gemm_rank_fp8(moe_a2a_t *h, const void *d_w8, const float *d_w_scale, int32_t N,
+                             int32_t apply_gates, void *d_out, void *d_scratch,
+                             size_t scratch_bytes, void *stream) {
+    return expert_gemm_rank_impl(h, d_w8, d_w_scale, N, apply_gates, d_out, d_scratch,
+                                 scratch_bytes, true, stream);
 }
 
 int moe_expert_gemm(moe_a2a_t *h, const void *d_w, int32_t N, void *d_out, void *stream) {

@@ -34,7 +34,7 @@ EXPORTS = ("moe_a2a_workspace_bytes", "moe_a2a_create", "moe_dispatch",
            "moe_a2a_set_recv_format", "moe_combine_fp8", "moe_quantize_rows_fp8",
            "moe_a2a_workspace_bytes_layout", "moe_a2a_create_layout",
            "moe_expert_gemm", "moe_expert_gemm_fp8", "moe_expert_gemm_rank_scratch_bytes",
-           "moe_expert_gemm_rank")
+           "moe_expert_gemm_rank", "moe_expert_gemm_rank_fp8")
 MOE_REDUCE_FP32_RANK_ORDER = 0
 MOE_REDUCE_BF16_TOPK_TREE = 1
 MOE_STATIC_SCRATCH_BYTES = 4 << 20
@@ -115,6 +115,8 @@ def _load(path: str = LIBRARY):
     lib.moe_expert_gemm_rank_scratch_bytes.restype = ctypes.c_size_t
     lib.moe_expert_gemm_rank.argtypes = [p, p, i32, i32, p, p, ctypes.c_size_t, p]
     lib.moe_expert_gemm_rank.restype = ctypes.c_int
+    lib.moe_expert_gemm_rank_fp8.argtypes = [p, p, p, i32, i32, p, p, ctypes.c_size_t, p]
+    lib.moe_expert_gemm_rank_fp8.restype = ctypes.c_int
     lib.moe_a2a_set_recv_format.argtypes = [p, i32]
     lib.moe_a2a_set_recv_format.restype = ctypes.c_int
     lib.moe_a2a_set_reduction.argtypes = [p, i32]
@@ -245,6 +247,14 @@ def moe_expert_gemm_rank(h, d_w: int, N: int, apply_gates: int, d_out: int, d_sc
     v = ctypes.c_void_p
     return _lib.moe_expert_gemm_rank(h, v(d_w), N, apply_gates, v(d_out), v(d_scratch),
                                      scratch_bytes, v(stream))
+
+
+def moe_expert_gemm_rank_fp8(h, d_w8: int, d_w_scale: int, N: int, apply_gates: int,
+                             d_out: int, d_scratch: int, scratch_bytes: int,
+                             stream: int = 0) -> int:
+    v = ctypes.c_void_p
+    return _lib.moe_expert_gemm_rank_fp8(h, v(d_w8), v(d_w_scale), N, apply_gates, v(d_out),
+                                         v(d_scratch), scratch_bytes, v(stream))
 
 
 def moe_expert_gemm_fp8(h, d_w8: int, d_w_scale: int, N: int, d_out: int,
@@ -535,17 +545,9 @@ class MoeA2A:
             raise MoeA2AError(st, "moe_expert_gemm")
         return out if out is not None else self.combine_payload()
 
-    def expert_gemm_rank(self, w, apply_gates=True, out=None, scratch=None, stream=None):
-        """Rank layout: each received row's local experts applied to it, their
-        bf16 outputs summed with the gates (or plainly) in ascending top-k
-        order.  w: bf16 [E, N, H]; out: bf16 [R, R, m, N], or None to write the
-        combine payload (N == H); scratch: uint8 device tensor of at least
-        moe_expert_gemm_rank_scratch_bytes bytes (allocated and kept here if
-        None).  Returns the output tensor."""
+    def _rank_out_scratch(self, N, out, scratch):
         import torch
-        E, H, R = self.num_experts, self.hidden, self.ep_size
-        N = w.shape[1]
-        self._check(w, torch.bfloat16, (E, N, H), "w")
+        R = self.ep_size
         if out is not None:
             self._check(out, torch.bfloat16, (R, R, self.last_view.plane_stride, N), "out")
         need = moe_expert_gemm_rank_scratch_bytes(self.cfg, N)
@@ -557,10 +559,46 @@ class MoeA2A:
             scratch = self._rank_scratch
         if scratch.dtype != torch.uint8 or scratch.device != self.workspace.device:
             raise ValueError("scratch: expected a uint8 tensor on %s" % self.workspace.device)
+        return scratch
+
+    def expert_gemm_rank(self, w, apply_gates=True, out=None, scratch=None, stream=None):
+        """Rank layout: each received row's local experts applied to it, their
+        bf16 outputs summed with the gates (or plainly) in ascending top-k
+        order.  w: bf16 [E, N, H]; out: bf16 [R, R, m, N], or None to write the
+        combine payload (N == H); scratch: uint8 device tensor of at least
+        moe_expert_gemm_rank_scratch_bytes bytes (allocated and kept here if
+        None).  Returns the output tensor."""
+        import torch
+        E, H = self.num_experts, self.hidden
+        N = w.shape[1]
+        self._check(w, torch.bfloat16, (E, N, H), "w")
+        scratch = self._rank_out_scratch(N, out, scratch)
         st = moe_expert_gemm_rank(self.handle, _ptr(w), N, int(bool(apply_gates)), _ptr(out),
                                   scratch.data_ptr(), scratch.numel(), self._stream(stream))
         if st != MOE_OK:
             raise MoeA2AError(st, "moe_expert_gemm_rank")
+        return out if out is not None else self.combine_payload()
+
+    def expert_gemm_rank_fp8(self, w8, w_scale, apply_gates=True, out=None, scratch=None,
+                             stream=None):
+        """expert_gemm_rank on FP8 operands, for a rank-layout dispatch in the
+        FP8 receive format: each expert output is (qx . qw[e]^T) sx sw[e],
+        narrowed to bf16, then gated and summed as expert_gemm_rank does.
+        w8: e4m3 [E, N, H] (float8_e4m3fn or uint8); w_scale: float32 [E, N];
+        out and scratch as for expert_gemm_rank."""
+        import torch
+        E, H = self.num_experts, self.hidden
+        N = w8.shape[1]
+        if w8.dtype not in (torch.float8_e4m3fn, torch.uint8) or tuple(w8.shape) != (E, N, H) \
+                or not w8.is_contiguous():
+            raise ValueError("w8: expected contiguous e4m3 [%d, N, %d]" % (E, H))
+        self._check(w_scale, torch.float32, (E, N), "w_scale")
+        scratch = self._rank_out_scratch(N, out, scratch)
+        st = moe_expert_gemm_rank_fp8(self.handle, _ptr(w8), _ptr(w_scale), N,
+                                      int(bool(apply_gates)), _ptr(out), scratch.data_ptr(),
+                                      scratch.numel(), self._stream(stream))
+        if st != MOE_OK:
+            raise MoeA2AError(st, "moe_expert_gemm_rank_fp8")
         return out if out is not None else self.combine_payload()
 
     def expert_gemm_fp8(self, w8, w_scale, out=None, stream=None):

@@ -261,6 +261,25 @@ size_t moe_expert_gemm_rank_scratch_bytes(const moe_a2a_config_t *cfg, int32_t N
 int moe_expert_gemm_rank(moe_a2a_t *h, const void *d_w, int32_t N, int32_t apply_gates,
                          void *d_out, void *d_scratch, size_t scratch_bytes, void *stream);
 
+/* moe_expert_gemm_rank on FP8 operands (tcgen05 .kind::f8f6f4, e4m3 x e4m3
+ * into fp32), for a rank-layout dispatch made in the FP8 receive format: the
+ * rows are the e4m3 codes qx with one scale sx per received row (the
+ * dispatch's recv_scale [R][R][m]), the weights e4m3 codes qw [E][N][H] with
+ * one fp32 scale per output channel sw [E][N] (reading: dequantised
+ * operands, the FP8 payload of [IX] "The adapter", as moe_expert_gemm_fp8):
+ *   y_k[n]  = bf16_rn( (sum_h f(qx[h]) * f(qw[e_k][n][h])) * sx * sw[e_k][n] ),
+ * the products of e4m3 values exact, the sum in fp32 on the tensor cores,
+ * then two fp32 multiplies; the message is the gated sum of
+ * moe_expert_gemm_rank, in fp32 from +0.0 in ascending k, narrowed once.
+ * H must be a multiple of 128, N of 128, E <= 1024; d_w8 16-byte and
+ * d_w_scale 4-byte aligned; d_out, d_scratch (the same size:
+ * moe_expert_gemm_rank_scratch_bytes) and the errors as for
+ * moe_expert_gemm_rank, with the FP8 receive format required.  Queues a
+ * memset and three kernels on `stream`. */
+int moe_expert_gemm_rank_fp8(moe_a2a_t *h, const void *d_w8, const float *d_w_scale, int32_t N,
+                             int32_t apply_gates, void *d_out, void *d_scratch,
+                             size_t scratch_bytes, void *stream);
+
 /* moe_a2a_workspace_bytes for a layout (0 if the pair is invalid). */
 size_t moe_a2a_workspace_bytes_layout(const moe_a2a_config_t *cfg, int32_t layout);
 

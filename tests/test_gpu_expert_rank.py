@@ -250,3 +250,242 @@ def test_expert_gemm_rank_contract():
     assert e.value.status == mod.MOE_ERR_CAPACITY
     assert a2.phase == 1
     a2.combine(None, False)
+
+
+# --------------------------------------------------------------------------
+# FP8 operands (moe_expert_gemm_rank_fp8): the FP8 receive rows (e4m3 codes,
+# one scale per received row) against e4m3 weights with one scale per
+# output channel.  Beyond the bf16 bound, the epilogue's two fp32 scale
+# multiplies add at most 2^-22 |y_k| per expert output.
+# --------------------------------------------------------------------------
+
+def dispatched_fp8(R, T, H, E, K, seed, routing="uniform", gates=None):
+    """A rank-layout dispatch in the FP8 receive format, and the oracle's
+    rank planes: its routing, its quantisation of every token placed at the
+    slots of that routing (codes qx [R, R, m, H], scales sx [R, R, m])."""
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    ids = synth.topk_ids(seed, R, T, E, K, routing)
+    w = synth.topk_weights(seed, R, T, K) if gates is None else gates
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    a.workspace.fill_(parity.POISON)
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    view = a.dispatch(parity.to_dev(ids, torch.int32), parity.to_dev(w, torch.float32),
+                      parity.to_dev(x, torch.bfloat16))
+    m = view.plane_stride
+    r = oracle.route(ids, w, E, T)
+    od = oracle.dispatch(ids, w, x, E, T, r)
+    q, sc = oracle.quantize_rows_fp8(x)
+    qx = np.zeros((R, R, m, H), np.uint8)
+    sx = np.zeros((R, R, m), np.float32)
+    for dd in range(R):
+        for s in range(R):
+            c = r["recv_counts"][dd, s]
+            src = r["src_token"][dd, s, :c]
+            qx[dd, s, :c] = q[s, src]
+            sx[dd, s, :c] = sc[s, src]
+    return a, view, dict(ids=ids, w=w, x=x, r=r, od=od, qx=qx, sx=sx)
+
+
+def fp8_weights(seed, E, N, H):
+    """e4m3 codes [E, N, H] (no NaN codes, |w| <= 1.875 before the scale)
+    from torch's seeded generator on the device, and channel scales [E, N]
+    near 1 / sqrt(H)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    qw = torch.randint(0, 256, (E, N, H), dtype=torch.uint8, device="cuda", generator=g)
+    big = (qw & 0x7F) >= 0x40
+    qw = torch.where(big, qw & 0xBF, qw)                # exponent field below 8: |f| < 2
+    sw = (torch.rand((E, N), generator=g, device="cuda") * 1.5 + 0.5) / np.sqrt(H)
+    return qw.contiguous(), sw.float().contiguous()
+
+
+def check_fp8(got, d, qw_dev, sw_dev, apply_gates, rows):
+    """As check(), through oracle.expert_gemm_rank_fp8 on the oracle's codes."""
+    od, r = d["od"], d["r"]
+    K = od["recv_ids"].shape[-1]
+    H = d["qx"].shape[-1]
+    ids = od["recv_ids"]
+    used = np.unique(ids.reshape(-1, K)[rows])
+    used = used[used >= 0]
+    lut = np.full(qw_dev.shape[0], -1, np.int32)
+    lut[used] = np.arange(used.size, dtype=np.int32)
+    ok = (ids >= 0) & (ids < qw_dev.shape[0])
+    ids_sub = np.where(ok, lut[np.where(ok, ids, 0)], -1).astype(np.int32)
+    sel = torch.from_numpy(used).cuda()
+    qw = qw_dev[sel].cpu().numpy()
+    sw = sw_dev[sel].cpu().numpy()
+    msg, ym, sm = oracle.expert_gemm_rank_fp8(d["qx"], d["sx"], ids_sub, od["recv_w"],
+                                              r["recv_counts"], qw, sw, apply_gates,
+                                              rows=rows, magnitudes=True)
+    N = msg.shape[-1]
+    g = parity.f32(got.reshape(-1, N)[rows]).astype(np.float64)
+    o = parity.f32(msg.reshape(-1, N)[rows]).astype(np.float64)
+    ym = ym.reshape(-1, N)[rows]
+    sm = sm.reshape(-1, N)[rows]
+    bound = (2.0 ** -7 * np.abs(o) + 1.01 * (2.0 ** -7 + 2.0 ** -22 + K * 2.0 ** -23) * ym +
+             1.01 * H * 2.0 ** -23 * sm + 1e-30)
+    err = np.abs(g - o)
+    assert np.isfinite(g).all()
+    assert (err <= bound).all(), (float(err.max()), float((err / bound).max()))
+    assert err.mean() <= 2.0 ** -8 * np.abs(o).mean()
+    return float(err.max()), float((err == 0).mean())
+
+
+@pytest.mark.parametrize("R,T,H,E,K,N,gates", [(2, 64, 128, 4, 2, 128, True),
+                                               (3, 50, 384, 6, 3, 384, False),
+                                               (4, 100, 256, 16, 4, 512, True),
+                                               (4, 300, 256, 8, 8, 256, True),
+                                               (4, 300, 256, 4, 2, 256, True),
+                                               (4, 300, 128, 4, 2, 128, False)])
+def test_expert_gemm_rank_fp8_small(R, T, H, E, K, N, gates):
+    # one and several row tiles per expert, 128- and 256-wide column tiles,
+    # rows carrying one (written by the product's epilogue) to K local
+    # experts (summed after it), every row compared
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=R * 10 + K + 1)
+    m = view.plane_stride
+    qw, sw = fp8_weights(7, E, N, H)
+    out = torch.full((R, R, m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    a.expert_gemm_rank_fp8(qw, sw, gates, out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0) and a.phase == 1
+    got = parity.to_host_u16(out)
+    counts = d["r"]["recv_counts"]
+    check_fp8(got, d, qw, sw, gates, valid_rows(counts, m))
+    for dd in range(R):                       # rows past a count are not written
+        for s in range(R):
+            assert np.isnan(parity.f32(got[dd, s, counts[dd, s]:])).all()
+    a.combine(None, False)
+
+
+def test_expert_gemm_rank_fp8_exact_weights_bit_exact_and_whole_step():
+    # identity codes (1.0) with channel scales 2^(e mod 3) and gates 1/8: an
+    # expert output is bf16(f32(sx f(qx)) 2^j) on both sides (one product on
+    # the tensor cores, exact), so messages and the unweighted fused combine
+    # after them equal the oracle bit for bit
+    R, T, H, E, K = 8, 64, 256, 64, 8
+    gates = np.full((R, T, K), 0.125, np.float32)
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=4, gates=gates)
+    eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+    qw = np.ascontiguousarray(np.broadcast_to(eye, (E, H, H)))
+    sw = np.repeat((2.0 ** (np.arange(E) % 3)).astype(np.float32)[:, None], H, axis=1)
+    a.expert_gemm_rank_fp8(parity.to_dev(qw, torch.uint8), parity.to_dev(sw, torch.float32),
+                           True)                                   # into the payload
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(a.combine_payload())
+    od, r = d["od"], d["r"]
+    msg = oracle.expert_gemm_rank_fp8(d["qx"], d["sx"], od["recv_ids"], od["recv_w"],
+                                      r["recv_counts"], qw, sw, True)
+    for dd in range(R):
+        for s in range(R):
+            c = r["recv_counts"][dd, s]
+            assert np.array_equal(got[dd, s, :c], msg[dd, s, :c]), (dd, s)
+    res = synth.per_rank_rows(4, synth.RESIDUAL, R, T, H)
+    gam = synth.gamma(4, H)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(out)
+    a.combine(None, False, parity.to_dev(res, torch.bfloat16), parity.to_dev(gam, torch.bfloat16),
+              1e-6, out, rout)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    oc = oracle.combine(r, msg, False, res, gam, 1e-6)
+    assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H), oc["residual_out"])
+    y = parity.f32(parity.to_host_u16(out).reshape(R * T, H)).astype(np.float64)
+    err = np.abs(y - oc["y"])
+    assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all()
+
+
+def test_expert_gemm_rank_fp8_decode_shape():
+    # decode: 8 ranks x 64 tokens, H = N = 7168, 256 experts, top-8, output
+    # into the combine payload; a seeded sample of rows against the oracle
+    R, T, H, E, K = 8, 64, 7168, 256, 8
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=0)
+    m = view.plane_stride
+    qw, sw = fp8_weights(11, E, H, H)
+    a.expert_gemm_rank_fp8(qw, sw, True)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(a.combine_payload())
+    counts = d["r"]["recv_counts"]
+    rows = valid_rows(counts, m)
+    assert np.isfinite(parity.f32(got.reshape(-1, H)[rows])).all()
+    rng = np.random.default_rng(3)
+    pick = set(rng.choice(rows, 10, replace=False).tolist())
+    c = counts[7, 7]
+    if c:
+        pick.update([(7 * R + 7) * m, (7 * R + 7) * m + c - 1])
+    check_fp8(got, d, qw, sw, True, np.array(sorted(pick), np.int64))
+    a.combine(None, False)
+
+
+def test_expert_gemm_rank_fp8_prefill_shape():
+    # prefill-sized rank planes: 8 ranks x 4096 tokens, H = 7168, 256
+    # experts, top-8 with Zipf(1.2) popularity, N = 256 into a caller buffer
+    R, T, H, E, K, N = 8, 4096, 7168, 256, 8, 256
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=0, routing="zipf")
+    m = view.plane_stride
+    qw, sw = fp8_weights(12, E, N, H)
+    out = torch.full((R, R, m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    a.expert_gemm_rank_fp8(qw, sw, True, out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(out)
+    counts = d["r"]["recv_counts"]
+    rows = valid_rows(counts, m)
+    assert np.isfinite(parity.f32(got.reshape(-1, N)[rows])).all()
+    rng = np.random.default_rng(4)
+    pick = set(rng.choice(rows, 384, replace=False).tolist())
+    for dd in range(R):
+        for s in range(R):
+            c = counts[dd, s]
+            if c:
+                pick.update([(dd * R + s) * m, (dd * R + s) * m + c - 1])
+    check_fp8(got, d, qw, sw, True, np.array(sorted(pick), np.int64))
+    for dd in range(R):
+        for s in range(R):
+            assert np.isnan(parity.f32(got[dd, s, counts[dd, s]:])).all()
+    a.combine(None, False)
+
+
+def test_expert_gemm_rank_fp8_repeat_calls_bit_identical():
+    R, T, H, E, K, N = 4, 200, 256, 8, 4, 256
+    a, view, d = dispatched_fp8(R, T, H, E, K, seed=9)
+    m = view.plane_stride
+    qw, sw = fp8_weights(13, E, N, H)
+    outs = []
+    for _ in range(3):
+        out = torch.zeros((R, R, m, N), dtype=torch.bfloat16, device="cuda")
+        a.expert_gemm_rank_fp8(qw, sw, True, out)
+        outs.append(parity.to_host_u16(out))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    a.combine(None, False)
+
+
+def test_expert_gemm_rank_fp8_contract():
+    from combine_topk_ids_rank_gb300 import moe_a2a as mod
+    R, T, H, E, K = 2, 16, 128, 4, 2
+    qw = torch.zeros((E, H, H), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((E, H), dtype=torch.float32, device="cuda")
+    wb = torch.zeros((E, H, H), dtype=torch.bfloat16, device="cuda")
+    a, view, d = dispatched(R, T, H, E, K, seed=1)             # bf16 receive format
+    with pytest.raises(mod.MoeA2AError) as e:
+        a.expert_gemm_rank_fp8(qw, sw, True)
+    assert e.value.status == mod.MOE_ERR_INVALID_ARG
+    a.combine(None, False)
+    b, view, d = dispatched_fp8(R, T, H, E, K, seed=1)         # FP8 receive format
+    with pytest.raises(mod.MoeA2AError) as e:                 # bf16 product on e4m3 rows
+        b.expert_gemm_rank(wb, True)
+    assert e.value.status == mod.MOE_ERR_INVALID_ARG
+    scratch = torch.empty(mod.moe_expert_gemm_rank_scratch_bytes(b.cfg, H), dtype=torch.uint8,
+                          device="cuda")
+    st = mod.moe_expert_gemm_rank_fp8(b.handle, qw.data_ptr(), 0, H, 1, 0,   # no channel scales
+                                      scratch.data_ptr(), scratch.numel())
+    assert st == mod.MOE_ERR_INVALID_ARG
+    with pytest.raises(mod.MoeA2AError) as e:                 # scratch too small
+        b.expert_gemm_rank_fp8(qw, sw, True, scratch=scratch[:-256])
+    assert e.value.status == mod.MOE_ERR_CAPACITY
+    b.expert_gemm_rank_fp8(qw, sw, True)
+    torch.cuda.synchronize()
+    assert b.get_error() == (0, 0) and b.phase == 1
+    b.combine(None, False)
