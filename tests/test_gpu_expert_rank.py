@@ -489,3 +489,62 @@ def test_expert_gemm_rank_fp8_contract():
     torch.cuda.synchronize()
     assert b.get_error() == (0, 0) and b.phase == 1
     b.combine(None, False)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_expert_gemm_rank_varlen_and_dead_ranks(fp8):
+    # per-rank token counts and two dead ranks: the product sees exactly the
+    # rows and local experts of the oracle's routing on the masked ids (a
+    # token past its rank's count, or an expert on a dead rank, is absent)
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    R, M, H, E, K, N = 8, 96, 256, 64, 8, 256
+    counts = [96, 0, 50, 1, 96, 33, 70, 5]
+    dead = (2, 5)
+    ids = synth.topk_ids(21, R, M, E, K)
+    w = synth.topk_weights(21, R, M, K)
+    x = synth.per_rank_rows(21, synth.X, R, M, H)
+    mids = ids.copy()
+    for s, c in enumerate(counts):
+        mids[s, c:] = -1
+    for dd in dead:
+        mids[(mids >= 0) & (mids // (E // R) == dd)] = -1
+    a = MoeA2A(R, M, H, E, K, "cuda")
+    a.workspace.fill_(parity.POISON)
+    if fp8:
+        a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    a.set_active_ranks(0xFF & ~sum(1 << dd for dd in dead))
+    view = a.dispatch_varlen(parity.to_dev(ids, torch.int32), parity.to_dev(w, torch.float32),
+                             parity.to_dev(x, torch.bfloat16), counts)
+    assert view.plane_stride == M
+    r = oracle.route(mids, w, E, M)
+    assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"])
+    od = oracle.dispatch(mids, w, x, E, M, r)
+    d = dict(r=r, od=od)
+    out = torch.full((R, R, M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if fp8:
+        q, sc = oracle.quantize_rows_fp8(x)
+        d["qx"] = np.zeros((R, R, M, H), np.uint8)
+        d["sx"] = np.zeros((R, R, M), np.float32)
+        for dd in range(R):
+            for s in range(R):
+                c = r["recv_counts"][dd, s]
+                d["qx"][dd, s, :c] = q[s, r["src_token"][dd, s, :c]]
+                d["sx"][dd, s, :c] = sc[s, r["src_token"][dd, s, :c]]
+        qw, sw = fp8_weights(22, E, N, H)
+        a.expert_gemm_rank_fp8(qw, sw, True, out)
+    else:
+        wb = weights(22, E, N, H, 1.0 / np.sqrt(H))
+        a.expert_gemm_rank(wb, True, out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(out)
+    rows = valid_rows(r["recv_counts"], M)
+    if fp8:
+        check_fp8(got, d, qw, sw, True, rows)
+    else:
+        check(got, d, wb, True, rows)
+    for dd in range(R):
+        for s in range(R):
+            assert np.isnan(parity.f32(got[dd, s, r["recv_counts"][dd, s]:])).all()
+    assert r["recv_counts"][list(dead)].sum() == 0
+    a.combine(None, False)

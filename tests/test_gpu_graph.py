@@ -208,3 +208,95 @@ def test_graph_replays_fp8_dispatch():
                     assert scales[d, s, j] == s_ref[s, t]
         oc = oracle.combine(r, eo, True, tokens=np.arange(R * T))
         assert np.array_equal(parity.to_host_u16(out).reshape(R * T, H), oc["out"]), seed
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_graph_replays_rank_plane_moe_step(fp8):
+    # A whole MoE step on the rank planes captured once: dispatch, the
+    # expert product with the gates (pair lists cleared inside each call),
+    # the unweighted fused combine.  W_e = 2^(e mod 3) I (bf16, or unit
+    # codes with that channel scale) makes each expert output exact, so the
+    # gated sums are the same IEEE operations on both sides: the messages
+    # equal the oracle's bit for bit on every replay.
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    R, T, H, E, K = 4, 40, 256, 16, 4
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    if fp8:
+        a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    scale = (2.0 ** (np.arange(E) % 3)).astype(np.float32)
+    if fp8:
+        eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+        qw = np.ascontiguousarray(np.broadcast_to(eye, (E, H, H)))
+        sw = np.repeat(scale[:, None], H, axis=1)
+        qw_d, sw_d = parity.to_dev(qw, torch.uint8), parity.to_dev(sw, torch.float32)
+        product = lambda: a.expert_gemm_rank_fp8(qw_d, sw_d, True)
+    else:
+        wb = parity.f32_to_bits(np.stack([np.eye(H, dtype=np.float32) * scale[e]
+                                          for e in range(E)]))
+        wb_d = parity.to_dev(wb, torch.bfloat16)
+        product = lambda: a.expert_gemm_rank(wb_d, True)
+
+    def inputs(seed):
+        return dict(ids=synth.topk_ids(seed, R, T, E, K, "uniform"),
+                    w=synth.topk_weights(seed, R, T, K),
+                    x=synth.per_rank_rows(seed, synth.X, R, T, H),
+                    res=synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H),
+                    g=synth.gamma(seed, H))
+
+    first = inputs(400)
+    ids = parity.to_dev(first["ids"], torch.int32)
+    wts = parity.to_dev(first["w"], torch.float32)
+    x = parity.to_dev(first["x"], torch.bfloat16)
+    res = parity.to_dev(first["res"], torch.bfloat16)
+    gam = parity.to_dev(first["g"], torch.bfloat16)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(res)
+    view = a.dispatch(ids, wts, x, T)          # direct calls first: stream, events, scratch
+    product()
+    a.combine(None, False, res, gam, 1e-6, out, rout)
+    torch.cuda.synchronize()
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        view = a.dispatch(ids, wts, x, T)
+        product()
+        a.combine(None, False, res, gam, 1e-6, out, rout)
+
+    for seed in (41, 42, 43):
+        inp = inputs(seed)
+        for dst, src, dt in ((ids, inp["ids"], torch.int32), (wts, inp["w"], torch.float32),
+                             (x, inp["x"], torch.bfloat16), (res, inp["res"], torch.bfloat16),
+                             (gam, inp["g"], torch.bfloat16)):
+            dst.copy_(parity.to_dev(src, dt))
+        g.replay()
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0)
+        r = oracle.route(inp["ids"], inp["w"], E, T)
+        counts = view.recv_counts.cpu().numpy()
+        assert np.array_equal(counts, r["recv_counts"]), seed
+        od = oracle.dispatch(inp["ids"], inp["w"], inp["x"], E, T, r)
+        if fp8:
+            q, sc = oracle.quantize_rows_fp8(inp["x"])
+            qx = np.zeros((R, R, T, H), np.uint8)
+            sx = np.zeros((R, R, T), np.float32)
+            for d in range(R):
+                for s in range(R):
+                    c = counts[d, s]
+                    qx[d, s, :c] = q[s, r["src_token"][d, s, :c]]
+                    sx[d, s, :c] = sc[s, r["src_token"][d, s, :c]]
+            msg = oracle.expert_gemm_rank_fp8(qx, sx, od["recv_ids"], od["recv_w"],
+                                              r["recv_counts"], qw, sw, True)
+        else:
+            msg = oracle.expert_gemm_rank(od["recv_x"], od["recv_ids"], od["recv_w"],
+                                          r["recv_counts"], wb, True)
+        pay = parity.to_host_u16(a.combine_payload())
+        for d in range(R):
+            for s in range(R):
+                c = counts[d, s]
+                assert np.array_equal(pay[d, s, :c], msg[d, s, :c]), (d, s, seed)
+        oc = oracle.combine(r, msg, False, inp["res"], inp["g"], 1e-6, tokens=np.arange(R * T))
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H),
+                              oc["residual_out"]), ("residual_out", seed)
+        y = parity.f32(parity.to_host_u16(out).reshape(R * T, H)).astype(np.float64)
+        err = np.abs(y - oc["y"])
+        assert (err <= parity.ABS_TOL).all() and (err <= parity.REL_TOL * np.abs(oc["y"])).all()
