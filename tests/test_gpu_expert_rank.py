@@ -1,5 +1,6 @@
-"""Expert-side product on the rank planes (moe_expert_gemm_rank) against the
-oracle, through the C ABI.
+"""Expert-side product on the rank planes (moe_expert_gemm_rank, and
+moe_expert_gemm_rank_fp8 on the FP8 receive rows) against the oracle,
+through the C ABI.
 
 InferenceX PR #2450, "CollectiveX: add FlashInfer one-sided NVLink EP for the
 GB SKUs", "Why": each expert applies its weights to the rows it received;
@@ -17,6 +18,9 @@ with the two magnitude sums taken from the oracle.  The mean error must also
 stay below 2^-8 of the mean message.  Power-of-two diagonal weights and
 dyadic gates make every step exact: those cases are compared bit for bit,
 and through the whole step (dispatch, product, unweighted fused combine).
+On FP8 operands each expert output also carries two fp32 scale multiplies
+(2^-22 relative); identity codes with power-of-two channel scales make that
+case exact too.
 """
 import numpy as np
 import pytest
