@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of GB300 peak), 1 GPU"
 # Sets of device input / output buffers the end-to-end leg rotates through.
 E2E_BUFFERS = 3
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal: each phase also reports its fraction of it
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -531,6 +532,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "dispatch": {"ms_avg": d_avg, "ms_p50": pct(disp_ms, 0.5), "ms_p10": pct(disp_ms, 0.1),
                      "ms_p90": pct(disp_ms, 0.9), "bytes": d_bytes,
                      "gbs": d_bytes / d_avg / 1e6, "frac": d_bytes / d_avg / 1e6 / peak,
+                     "frac_of_nominal": d_bytes / d_avg / 1e6 / NOMINAL_HBM_GBS,
                      "kernels": (["dispatch_small"] if view.kernels == 1 else
                                  ["route_e_count", "route_e_scan"] if args.layout == "expert"
                                  else ["route_count", "route_scan"]) +
@@ -547,6 +549,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "combine": {"ms_avg": c_avg, "ms_p50": pct(comb_ms, 0.5), "ms_p10": pct(comb_ms, 0.1),
                     "ms_p90": pct(comb_ms, 0.9), "bytes": c_bytes,
                     "gbs": c_bytes / c_avg / 1e6, "frac": c_bytes / c_avg / 1e6 / peak,
+                    "frac_of_nominal": c_bytes / c_avg / 1e6 / NOMINAL_HBM_GBS,
                     "kernels": ["combine_small" if N <= combine_small_max() and not fp8
                                 else "combine"]},
     }
