@@ -552,3 +552,63 @@ def test_expert_gemm_rank_varlen_and_dead_ranks(fp8):
             assert np.isnan(parity.f32(got[dd, s, r["recv_counts"][dd, s]:])).all()
     assert r["recv_counts"][list(dead)].sum() == 0
     a.combine(None, False)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_expert_gemm_rank_empty_and_no_pairs(fp8):
+    # an empty dispatch, and one whose tokens name no expert (all ids -1):
+    # the product queues nothing or finds no pairs, writes nothing and
+    # reports no error
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    R, H, E, K, N = 4, 128, 8, 2, 128
+    for T in (0, 20):
+        a = MoeA2A(R, 32, H, E, K, "cuda")
+        if fp8:
+            a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+        ids = torch.full((R, T, K), -1, dtype=torch.int32, device="cuda")
+        w = torch.ones((R, T, K), dtype=torch.float32, device="cuda")
+        x = torch.ones((R, T, H), dtype=torch.bfloat16, device="cuda")
+        view = a.dispatch(ids, w, x, 8 if T == 0 else None)
+        assert int(view.recv_counts.sum().item()) == 0
+        m = view.plane_stride
+        out = torch.full((R, R, m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if fp8:
+            a.expert_gemm_rank_fp8(torch.zeros((E, N, H), dtype=torch.uint8, device="cuda"),
+                                   torch.ones((E, N), dtype=torch.float32, device="cuda"),
+                                   True, out)
+        else:
+            a.expert_gemm_rank(torch.zeros((E, N, H), dtype=torch.bfloat16, device="cuda"),
+                               True, out)
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0) and a.phase == 1
+        assert torch.isnan(out.float()).all()
+        a.combine(None, False)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_expert_gemm_rank_single_rank_top1(fp8):
+    # one rank, top-1: every received row carries exactly one local expert,
+    # so every message comes from the product's epilogue (bf16(+0 + g y))
+    R, T, H, E, K, N = 1, 200, 256, 4, 1, 256
+    if fp8:
+        a, view, d = dispatched_fp8(R, T, H, E, K, seed=51)
+        qw, sw = fp8_weights(52, E, N, H)
+    else:
+        a, view, d = dispatched(R, T, H, E, K, seed=51)
+        wb = weights(52, E, N, H, 1.0 / np.sqrt(H))
+    m = view.plane_stride
+    out = torch.full((R, R, m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if fp8:
+        a.expert_gemm_rank_fp8(qw, sw, True, out)
+    else:
+        a.expert_gemm_rank(wb, True, out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0)
+    got = parity.to_host_u16(out)
+    rows = valid_rows(d["r"]["recv_counts"], m)
+    assert rows.size == T
+    if fp8:
+        check_fp8(got, d, qw, sw, True, rows)
+    else:
+        check(got, d, wb, True, rows)
+    a.combine(None, False)
