@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["route.cu", "dispatch.cu", "combine.cu", "combine_ring.cu", "combine_small.cu", "combine_tree.cu",
            "dispatch_fp8.cu", "dispatch_small.cu", "route_expert.cu", "expert_gemm.cu", "expert_rank.cu",
            "moe_a2a.cpp", "moe_noalloc.cu"]
-HEADERS = ["kernels.h", "expert.h", "dispatch_small.h", "ptx.cuh", "fp8.cuh", "tcgen05.cuh", "f32x2.cuh"]
+HEADERS = ["kernels.h", "expert.h", "dispatch_small.h", "smem_limit.h", "ptx.cuh", "fp8.cuh",
+           "tcgen05.cuh", "f32x2.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -32,6 +32,7 @@
 // the producer waits (bounded) for its copies still landing before exit.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "smem_limit.h"
 #include "fp8.cuh"
 #include "f32x2.cuh"
 
@@ -547,9 +548,7 @@ cudaError_t act_t(Act a, const CombineParams *p, const LaunchShape &shape, cudaS
                   int *per_sm) {
     switch (a) {
         case Act::Prepare:
-            return cudaFuncSetAttribute(ring_kernel<VPT, W, F, O>(),
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)shape.smem);
+            return raise_smem_limit(ring_kernel<VPT, W, F, O>(), shape.smem);
         case Act::Occupancy:
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 per_sm, ring_kernel<VPT, W, F, O>(), shape.block, shape.smem);

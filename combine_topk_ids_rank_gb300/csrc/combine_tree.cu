@@ -18,6 +18,7 @@
 // kept in shared memory for the normalisation.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "smem_limit.h"
 
 #include "moe_a2a.h"
 
@@ -153,9 +154,7 @@ cudaError_t launch_combine_tree(const CombineTreeParams &p, int num_sms, cudaStr
     if (grid < 1) return cudaSuccess;
     const size_t smem = fused ? (size_t)p.H * sizeof(float) : 0;
     if (fused) {
-        cudaError_t err = cudaFuncSetAttribute(combine_tree_kernel<true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+        cudaError_t err = raise_smem_limit(combine_tree_kernel<true>, smem);
         if (err != cudaSuccess) return err;
         return launch_pdl(combine_tree_kernel<true>, dim3((unsigned)grid), dim3(nt), smem, st, p);
     }

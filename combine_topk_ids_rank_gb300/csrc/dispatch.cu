@@ -24,6 +24,7 @@
 // drains its copies and returns.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "smem_limit.h"
 
 #include "moe_a2a.h"
 
@@ -164,8 +165,7 @@ cudaError_t dispatch_prepare(int row_bytes, int P, int num_sms, const Tuning &tn
     if (tn.dispatch_stages > 0) stages = tn.dispatch_stages;
     const size_t smem = (size_t)stages * stage_bytes + (size_t)stages * sizeof(uint64_t);
 
-    cudaError_t err = cudaFuncSetAttribute(dispatch_rows_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = raise_smem_limit(dispatch_rows_kernel, smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_rows_kernel, 32, smem);

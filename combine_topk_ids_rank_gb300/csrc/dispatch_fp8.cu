@@ -25,6 +25,7 @@
 // written once per destination at half the bf16 bytes.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "smem_limit.h"
 #include "fp8.cuh"
 
 #include "moe_a2a.h"
@@ -231,8 +232,7 @@ cudaError_t prepare_t(int H, int num_sms, int stages_override, int *stages, Laun
     if (stages_override > 0) S = stages_override;
     S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
     const size_t smem = stride * S;
-    cudaError_t err = cudaFuncSetAttribute(dispatch_fp8_kernel<VPT>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = raise_smem_limit(dispatch_fp8_kernel<VPT>, smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel<VPT>,

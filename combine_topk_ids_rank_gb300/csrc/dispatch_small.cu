@@ -31,6 +31,7 @@
 #include "fp8.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "smem_limit.h"
 
 #include "moe_a2a.h"
 
@@ -383,8 +384,7 @@ cudaError_t dispatch_small_prepare(int row_bytes, int num_sms, DispatchSmallShap
                            (const void *)dispatch_small_kernel<4>,
                            (const void *)dispatch_small_kernel<8>};
     for (const void *k : kern) {
-        cudaError_t err =
-            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+        cudaError_t err = raise_smem_limit(k, max_smem);
         if (err != cudaSuccess) return err;
     }
     out->stages = kStages;
@@ -463,12 +463,9 @@ int fp8_threads(int H8) {
 template <int VPT>
 struct SmallFp8 {
     static cudaError_t attr(size_t smem) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_small_fp8_kernel<8, VPT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = raise_smem_limit(dispatch_small_fp8_kernel<8, VPT>, smem);
         if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(dispatch_small_fp8_kernel<0, VPT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return raise_smem_limit(dispatch_small_fp8_kernel<0, VPT>, smem);
     }
     static cudaError_t launch(const DispatchSmallFp8Params &p, const DispatchSmallFp8Shape &sh,
                               cudaStream_t st) {

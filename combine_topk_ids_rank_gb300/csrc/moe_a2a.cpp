@@ -23,6 +23,14 @@
 
 namespace {
 
+// A CUDA call of this library failed.  The status says so; the runtime's
+// last error, which a refused launch also leaves behind, is cleared so that
+// the caller's next, unrelated CUDA call does not report it again.
+int cuda_failed() {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+}
+
 constexpr size_t kAlign = 256;
 // Most tokens of a call (all sources) for the cluster combine by default.
 // L2-flushed CUDA-event times against the persistent combines (fused,
@@ -234,41 +242,41 @@ T *at(moe_a2a_t *h, size_t off) {
 
 int init_device(moe_a2a_t *h, cudaStream_t st) {
     if (h->ready) return MOE_OK;
-    if (cudaGetDevice(&h->device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaGetDevice(&h->device) != cudaSuccess) return cuda_failed();
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
         cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     std::memset(&h->dispatch_tmpl, 0, sizeof h->dispatch_tmpl);
     if (moe::dispatch_prepare(2 * h->cfg.hidden, h->L.P, h->num_sms, h->tuning,
                               &h->dispatch_tmpl, &h->dispatch_shape) != cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     if (h->cfg.hidden % 16 == 0) {
         moe::DispatchFp8Params fp;
         if (moe::dispatch_fp8_prepare(h->cfg.hidden, h->num_sms, h->tuning, &fp,
                                       &h->fp8_shape) != cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
         h->fp8_stages = fp.stages;
     }
     if (h->L.layout == MOE_LAYOUT_RANK &&
         moe::dispatch_small_prepare(2 * h->cfg.hidden, h->num_sms, &h->small) != cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     h->small_fp8_ok = h->L.layout == MOE_LAYOUT_RANK && h->cfg.hidden % 16 == 0 &&
                       moe::dispatch_small_fp8_prepare(h->cfg.hidden, &h->small_fp8) ==
                           cudaSuccess;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     h->overlap = h->L.layout == MOE_LAYOUT_RANK && h->tuning.route_overlap != 0;
     h->small_combine_ok = moe::combine_small_shape(h->cfg.hidden, &h->small_combine);
     if (h->overlap) {  // each object once, also after a partial failure
         if (h->side == nullptr &&
             cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
         if (h->ev_count == nullptr &&
             cudaEventCreateWithFlags(&h->ev_count, cudaEventDisableTiming) != cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
         if (h->ev_scan == nullptr &&
             cudaEventCreateWithFlags(&h->ev_scan, cudaEventDisableTiming) != cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
     }
     h->accum_dirty = true;  // routing accumulators: zero them before the first pass
     h->ready = true;
@@ -327,7 +335,7 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
             fp.tile = tile, fp.ntiles = ntiles;
         }
         return moe::launch_dispatch_fp8(fp, h->fp8_shape, st) == cudaSuccess ? MOE_OK
-                                                                              : MOE_ERR_CUDA;
+                                                                              : cuda_failed();
     }
     moe::DispatchParams dp = h->dispatch_tmpl;
     dp.x = static_cast<const uint8_t *>(d_x);
@@ -345,7 +353,7 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
     }
     return moe::launch_dispatch_rows(dp, h->dispatch_shape, st, true) == cudaSuccess
                ? MOE_OK
-               : MOE_ERR_CUDA;
+               : cuda_failed();
 }
 
 // The one-launch dispatch (dispatch_small.cu) serves the rank layout's bf16
@@ -414,12 +422,12 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
                 cudaSuccess ||
             cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
                 cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
     } else if (expert) {
         if (h->accum_dirty) {  // the histogram accumulator
             if (cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * E, st) !=
                 cudaSuccess)
-                return MOE_ERR_CUDA;
+                return cuda_failed();
             h->accum_dirty = false;
         }
         moe::RouteExpertParams rp;
@@ -442,7 +450,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         // (tile, source) grid would cover fewer than half the SMs.
         rp.kg = R * rp.ntiles * 2 >= h->num_sms ? rp.KP : 1;
         h->accum_dirty = true;  // until the pass that clears the accumulator is queued
-        if (moe::launch_route_expert(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::launch_route_expert(rp, st) != cudaSuccess) return cuda_failed();
         h->accum_dirty = false;
         rc = launch_rows(h, d_x, map, m, dest, ntok, st);
         if (rc != MOE_OK) return rc;
@@ -452,7 +460,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         const int sel = h->small_sel;
         if (!h->small_zero_ok &&
             cudaMemsetAsync(h->ws + bufs[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
         const int T = map.stride;
         if (h->recv_format == MOE_FORMAT_FP8_E4M3) {  // e4m3 rows, one CTA per token
             moe::DispatchSmallFp8Params fp;
@@ -476,7 +484,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
             fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
             h->small_zero_ok = false;  // until the launch that clears the other buffer is queued
             if (moe::launch_dispatch_small_fp8(fp, h->small_fp8, st) != cudaSuccess)
-                return MOE_ERR_CUDA;
+                return cuda_failed();
         } else {
             const int row_bytes = 2 * h->cfg.hidden;
             const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
@@ -505,7 +513,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
             sp.units = ntok * sp.chunks;
             h->small_zero_ok = false;  // until the launch that clears the other buffer is queued
             if (moe::launch_dispatch_small(sp, h->small.shape[c], st) != cudaSuccess)
-                return MOE_ERR_CUDA;
+                return cuda_failed();
         }
         h->cur_counts = bufs[sel];
         h->small_sel = sel ^ 1;
@@ -516,7 +524,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
                     cudaSuccess ||
                 cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * R * E, st) !=
                     cudaSuccess)
-                return MOE_ERR_CUDA;
+                return cuda_failed();
             h->accum_dirty = false;
         }
         const int tile = moe::route_tile(h->tuning);
@@ -537,7 +545,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         rc_p.tile = tile;
         const bool overlap = h->overlap;
         rc_p.local_slot = overlap ? at<int32_t>(h, h->L.local_slot) : nullptr;
-        if (moe::launch_route_count(rc_p, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::launch_route_count(rc_p, st) != cudaSuccess) return cuda_failed();
         h->accum_dirty = true;  // until the scan pass that clears it is queued
 
         moe::RouteScanParams rs;
@@ -566,17 +574,17 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
             // table, weights, metadata rows) runs beside it on `side`.
             if (cudaEventRecord(h->ev_count, st) != cudaSuccess ||
                 cudaStreamWaitEvent(h->side, h->ev_count, 0) != cudaSuccess)
-                return MOE_ERR_CUDA;
-            if (moe::launch_route_scan(rs, h->side, false) != cudaSuccess) return MOE_ERR_CUDA;
+                return cuda_failed();
+            if (moe::launch_route_scan(rs, h->side, false) != cudaSuccess) return cuda_failed();
             const int rows_rc = launch_rows(h, d_x, map, m, dest, ntok, st, tile, ntiles);
             // Join whatever happened to the copy, so `side` never outlives the call.
             if (cudaEventRecord(h->ev_scan, h->side) != cudaSuccess ||
                 cudaStreamWaitEvent(st, h->ev_scan, 0) != cudaSuccess)
-                return MOE_ERR_CUDA;
+                return cuda_failed();
             h->accum_dirty = false;
             if (rows_rc != MOE_OK) return rows_rc;
         } else {
-            if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+            if (moe::launch_route_scan(rs, st, true) != cudaSuccess) return cuda_failed();
             h->accum_dirty = false;
             rc = launch_rows(h, d_x, map, m, dest, ntok, st);
             if (rc != MOE_OK) return rc;
@@ -658,7 +666,7 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
         tp.P = 1;
         while (tp.P < tp.K) tp.P *= 2;
         tp.tokens = h->ntok;
-        if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::launch_combine_tree(tp, h->num_sms, st) != cudaSuccess) return cuda_failed();
     } else if (h->ntok > 0 && !out8 && small_combine(h, h->ntok)) {
         // few tokens: each row split over a cluster, all its messages in flight
         moe::CombineParams cp;
@@ -682,7 +690,7 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
         cp.ring_slots = 0;
         if (moe::launch_combine_small(cp, weighted != 0, fused, h->small_combine, st) !=
             cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
     } else if (h->ntok > 0) {
         const int variant = (out8 ? 4 : 0) + (weighted ? 2 : 0) + (fused ? 1 : 0);
         if (!h->combine_ready[variant]) {
@@ -704,7 +712,7 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
                                                  &h->combine_slots[variant])
                      : moe::combine_prepare(h->cfg.hidden, weighted != 0, fused, h->num_sms,
                                             &h->combine_shape[variant], &h->combine_vpt[variant]);
-            if (e != cudaSuccess) return MOE_ERR_CUDA;
+            if (e != cudaSuccess) return cuda_failed();
             h->combine_ring[variant] = ring;
             h->combine_ready[variant] = true;
         }
@@ -733,7 +741,7 @@ int combine_impl(moe_a2a_t *h, const void *d_expert_out, int32_t weighted, const
                                            h->combine_vpt[variant], h->combine_shape[variant], st)
                 : moe::launch_combine(cp, weighted != 0, fused, h->combine_vpt[variant],
                                       h->combine_shape[variant], st);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        if (e != cudaSuccess) return cuda_failed();
     }
     h->phase = 0;
     return MOE_OK;
@@ -855,11 +863,11 @@ int moe_a2a_get_error(moe_a2a_t *h, void *stream, uint32_t *flags) {
     if (cudaMemcpyAsync(&bits, h->ws + h->L.flags, sizeof bits, cudaMemcpyDeviceToHost, st) !=
             cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     if (bits != 0 &&
         (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof bits, st) != cudaSuccess ||
          cudaStreamSynchronize(st) != cudaSuccess))
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     if (flags != nullptr) *flags = bits;
     if (bits & MOE_DEVICE_FLAG_WAIT_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
     if (bits & MOE_DEVICE_FLAG_BAD_SLOT) return MOE_ERR_INTERNAL;
@@ -900,11 +908,11 @@ int moe_quantize_rows_fp8(const float *d_x, int64_t rows, int32_t hidden, void *
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     return moe::launch_quantize_rows_fp8(d_x, rows, hidden, static_cast<uint8_t *>(d_q), d_scale,
                                          sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MOE_OK
-               : MOE_ERR_CUDA;
+               : cuda_failed();
 }
 
 namespace {
@@ -945,7 +953,7 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
     gp.group_m = gemm_group_m(h->tuning);
     return moe::launch_expert_gemm(gp, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MOE_OK
-               : MOE_ERR_CUDA;
+               : cuda_failed();
 }
 
 // Scratch of the rank-plane product, sized for max_tokens_per_rank: the
@@ -1032,8 +1040,8 @@ int expert_gemm_rank_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale,
     rp.R = R, rp.m = m, rp.K = K, rp.E = E, rp.N = N;
     rp.apply_gates = apply_gates ? 1 : 0;
     if (cudaMemsetAsync(rp.cursor, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (moe::launch_rank_pairs(rp, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        return cuda_failed();
+    if (moe::launch_rank_pairs(rp, h->num_sms, st) != cudaSuccess) return cuda_failed();
 
     moe::ExpertGemmParams gp;
     gp.x = h->ws + h->L.recv_x;
@@ -1055,8 +1063,8 @@ int expert_gemm_rank_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale,
     gp.final_out = rp.out;
     gp.a_rows = (long long)R * R * m;
     gp.group_m = gemm_group_m(h->tuning);
-    if (moe::launch_expert_gemm(gp, st) != cudaSuccess) return MOE_ERR_CUDA;
-    return moe::launch_rank_aggregate(rp, h->num_sms, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (moe::launch_expert_gemm(gp, st) != cudaSuccess) return cuda_failed();
+    return moe::launch_rank_aggregate(rp, h->num_sms, st) == cudaSuccess ? MOE_OK : cuda_failed();
 }
 
 }  // namespace

@@ -25,6 +25,14 @@
 
 namespace {
 
+// A CUDA call of this library failed.  The status says so; the runtime's
+// last error, which a refused launch also leaves behind, is cleared so that
+// the caller's next, unrelated CUDA call does not report it again.
+int cuda_failed() {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+}
+
 constexpr size_t kScratchBytes = MOE_STATIC_SCRATCH_BYTES;
 constexpr size_t kAlign = 256;
 constexpr int kMaxDevices = 64;
@@ -82,23 +90,23 @@ int scratch_address(cudaStream_t st, void **out) {
     // A runtime call that needs the context first, so that the device's
     // primary context exists and is current before it is queried.
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return cuda_failed();
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!resolve_driver_calls()) return MOE_ERR_CUDA;
+    if (!resolve_driver_calls()) return cuda_failed();
     CUcontext ctx = nullptr;
     unsigned long long id = 0;
     if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
         g_ctx_get_id(ctx, &id) != CUDA_SUCCESS || id == 0)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     ScratchSlot &slot = g_slot[dev];
     if (slot.ctx_id != id) {
         if (cap != cudaStreamCaptureStatusNone) return MOE_ERR_SETUP_IN_CAPTURE;
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
         slot.addr = p;
         slot.ctx_id = id;
     }
@@ -153,7 +161,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     if (T == 0) {
         if (cudaMemsetAsync(d_recv_counts, 0, sizeof(int32_t) * R * R, st) != cudaSuccess ||
             cudaMemsetAsync(d_local_expert_counts, 0, sizeof(int32_t) * E, st) != cudaSuccess)
-            return MOE_ERR_CUDA;
+            return cuda_failed();
         return MOE_OK;
     }
 
@@ -175,7 +183,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     int32_t *hist_accum = tile_ticket + R;
     if (cudaMemsetAsync(tile_ticket, 0, sizeof(int32_t) * ((size_t)R + (size_t)R * E), st) !=
         cudaSuccess)
-        return MOE_ERR_CUDA;
+        return cuda_failed();
     p += align_up((size_t)R * 4 + (size_t)R * E * 4, kAlign);
     uint32_t *sink_flags = reinterpret_cast<uint32_t *>(p);
 
@@ -202,7 +210,7 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     c.active = all;
     c.R = R, c.K = K, c.E = E, c.Epr = E / R, c.RP = RP, c.ntiles = ntiles;
     c.tile = moe::kRouteTile;
-    if (moe::launch_route_count(c, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_route_count(c, st) != cudaSuccess) return cuda_failed();
 
     moe::RouteScanParams s;
     s.topk_ids = d_topk_ids;
@@ -221,6 +229,6 @@ extern "C" int moe_route_static_scratch(int32_t ep_size, int32_t num_experts, in
     s.R = R, s.K = K, s.E = E, s.Epr = E / R, s.RP = RP, s.m = m, s.ntiles = ntiles;
     s.tile = moe::kRouteTile;
     s.dg = 4;
-    if (moe::launch_route_scan(s, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_route_scan(s, st, true) != cudaSuccess) return cuda_failed();
     return MOE_OK;
 }

@@ -178,3 +178,65 @@ def test_no_leakage_between_calls(mod):
     shared.w = small
     rep = shared.run(seed=2)
     assert rep["T"] == 10
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_handles_of_different_sizes_interleaved(mod, fp8):
+    # Two handles with different hidden sizes in one process, the larger
+    # prepared first: each kernel's shared-memory limit is one per process,
+    # so preparing the smaller handle must not take it below what the larger
+    # one launches with.  Both stay usable, and both match the oracle, on the
+    # one-launch dispatch, the routing passes + row copy and the combines.
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_FORMAT_FP8_E4M3
+    R, E, K = 4, 16, 4
+    handles = {}
+    for H in (2048, 512):          # the larger first
+        handles[H] = MoeA2A(R, 300, H, E, K, "cuda")
+        if fp8:
+            handles[H].set_recv_format(MOE_FORMAT_FP8_E4M3)
+    for rnd in range(2):
+        for H in (2048, 512):
+            for T in (40, 300):    # one launch, then the routing passes
+                a = handles[H]
+                seed = 100 * rnd + T + H
+                ids = synth.topk_ids(seed, R, T, E, K)
+                w = synth.topk_weights(seed, R, T, K)
+                x = synth.per_rank_rows(seed, synth.X, R, T, H)
+                res = synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H)
+                gam = synth.gamma(seed, H)
+                view = a.dispatch(dev(ids, torch.int32), dev(w, torch.float32),
+                                  dev(x, torch.bfloat16))
+                r = oracle.route(ids, w, E, T)
+                assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"])
+                eo = synth.expert_out_planes(seed, R, T, H, r["recv_counts"])
+                if fp8:
+                    q_ref, s_ref = oracle.quantize_rows_fp8(x)
+                    codes = view.recv_x.view(torch.uint8).cpu().numpy()
+                    src = view.src_token.cpu().numpy()
+                    for d in range(R):
+                        for s in range(R):
+                            for j in range(r["recv_counts"][d, s]):
+                                assert np.array_equal(codes[d, s, j], q_ref[s, src[d, s, j]])
+                    a.combine_payload().copy_(dev(eo, torch.bfloat16))
+                    rout = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+                    out = a.combine(None, True, dev(res, torch.bfloat16),
+                                    dev(gam, torch.bfloat16), 1e-6, residual_out=rout)
+                else:
+                    od = oracle.dispatch(ids, w, x, E, T, r)
+                    rx = parity.to_host_u16(view.recv_x)
+                    for d in range(R):
+                        for s in range(R):
+                            c = r["recv_counts"][d, s]
+                            assert np.array_equal(rx[d, s, :c], od["recv_x"][d, s, :c])
+                    eo = od["recv_x"]
+                    rout = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+                    out = a.combine(view.recv_x, True, dev(res, torch.bfloat16),
+                                    dev(gam, torch.bfloat16), 1e-6, residual_out=rout)
+                torch.cuda.synchronize()
+                assert a.get_error() == (mod.MOE_OK, 0)
+                oc = oracle.combine(r, eo, True, res, gam, 1e-6)
+                assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H),
+                                      oc["residual_out"]), (H, T, rnd)
+                y = parity.f32(parity.to_host_u16(out)).reshape(-1, H).astype(np.float64)
+                err = np.abs(y - oc["y"])
+                assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all()
