@@ -67,7 +67,14 @@
  *
  * Host threads: a handle keeps host-side state (phase, views, which count
  * buffer is current), so calls on one handle must not run concurrently;
- * distinct handles are independent.
+ * distinct handles are independent.  Handles of different sizes may share
+ * one process and device: a kernel's dynamic shared-memory limit, which is
+ * one per process, is raised to the largest size a handle needs and never
+ * lowered.
+ *
+ * Errors: MOE_ERR_CUDA means a CUDA call of the library failed; the
+ * runtime's last error (cudaGetLastError) is cleared before returning, so
+ * that it is not reported again by the caller's next CUDA call.
  */
 #ifndef MOE_A2A_H
 #define MOE_A2A_H
