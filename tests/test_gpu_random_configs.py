@@ -1,0 +1,126 @@
+"""Seeded random configurations through dispatch and combine, against the oracle.
+
+Each case draws a shape the fixed tests do not pin down: ranks 1-32 (not
+only powers of two), 1-8 experts per rank, top-1 to top-8, hidden sizes from
+one 16-byte vector to 7168 (ragged against a warp's vector span), batches on
+either side of the one-launch dispatch's limit, a runtime maximum above the
+batch, uniform or Zipf routing, weighted or not, fused or not; on the rank
+layout with bf16 or FP8 rows, and on the expert layout.  The checks are the
+fixed tests' own (routing tables, counts, rows or codes and scales, padding
+left untouched, combine outputs), so a failure names its case by index and
+the drawn shape.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+from combine_topk_ids_rank_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import parity  # noqa: E402
+from oracle import oracle  # noqa: E402
+
+N_CASES = 96
+FAMILIES = ("rank-bf16", "rank-fp8", "expert-bf16", "expert-fp8")
+WORKSPACE_BUDGET = 1 << 30   # bytes of the two row regions of one case
+
+
+def draw(i):
+    """The i-th case: family and shape, from a generator seeded by i."""
+    rng = np.random.default_rng(1000 + i)
+    family = FAMILIES[i % len(FAMILIES)]
+    fp8 = family.endswith("fp8")
+    R = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 12, 16, 32]))
+    Epr = int(rng.integers(1, 9))
+    E = R * Epr
+    K = int(rng.integers(1, min(8, E) + 1))
+    H = int(rng.choice([16, 48, 64, 144, 512, 1040, 2048, 4112, 7168] if fp8 else
+                       [8, 24, 64, 136, 512, 1032, 2048, 4104, 7168]))
+    M = int(rng.choice([1, 7, 33, 64, 100, 256, 257, 300, 700]))
+    planes = E * R if family.startswith("expert") else R * R
+    while planes * M * H * 4 > WORKSPACE_BUDGET and M > 1:
+        M = max(1, M // 2)
+    T = int(rng.integers(0, M + 1))
+    m = int(rng.integers(max(T, 1), M + 1))
+    return dict(family=family, R=R, E=E, K=K, H=H, M=M, T=T, m=m,
+                routing=str(rng.choice(["uniform", "zipf"])),
+                weighted=bool(rng.integers(2)), fused=bool(rng.integers(2)), seed=i)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from combine_topk_ids_rank_gb300 import build_lib
+    build_lib.build()
+
+
+def run_rank_bf16(c):
+    w = replace(synth.WORKLOADS["tiny"], name="random", ep_size=c["R"], tokens_per_rank=c["T"],
+                max_tokens=c["M"], runtime_max=c["m"], hidden=c["H"], num_experts=c["E"],
+                top_k=c["K"], routing=c["routing"], weighted=c["weighted"], fused=c["fused"],
+                identity_experts=False)
+    case = parity.Case(w)
+    rep = case.run(seed=c["seed"], sample=None)
+    assert rep["T"] == c["T"]
+    case.a2a.close()
+
+
+def run_rank_fp8(c):
+    import test_gpu_fp8 as f
+    R, T, H, E, K, m = c["R"], c["T"], c["H"], c["E"], c["K"], c["m"]
+    a, view, d = f.run_dispatch_fp8(R, T, H, E, K, c["seed"], m=m, routing=c["routing"])
+    # combine of bf16 messages written into the payload, plain or fused
+    cnt, r = d["cnt"], d["r"]
+    eo = synth.expert_out_planes(c["seed"], R, m, H, cnt)
+    pay = a.combine_payload()
+    for dd in range(R):
+        for s in range(R):
+            if cnt[dd, s]:
+                pay[dd, s, :cnt[dd, s]].copy_(parity.to_dev(eo[dd, s, :cnt[dd, s]], torch.bfloat16))
+    res = synth.per_rank_rows(c["seed"], synth.RESIDUAL, R, T, H)
+    gam = synth.gamma(c["seed"], H)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    if c["fused"]:
+        rout = torch.empty_like(out)
+        a.combine(None, c["weighted"], parity.to_dev(res, torch.bfloat16),
+                  parity.to_dev(gam, torch.bfloat16), 1e-6, out, rout)
+    else:
+        a.combine(None, c["weighted"], out=out)
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0) and a.phase == 0
+    oc = oracle.combine(r, eo, c["weighted"], res if c["fused"] else None,
+                        gam if c["fused"] else None, 1e-6)
+    got = parity.to_host_u16(out).reshape(R * T, H)
+    if c["fused"]:
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H), oc["residual_out"])
+        y = parity.f32(got).astype(np.float64)
+        err = np.abs(y - oc["y"])
+        assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all()
+    else:
+        assert np.array_equal(got, oc["out"])
+    a.close()
+
+
+def run_expert(c, fp8):
+    import test_gpu_expert_layout as x
+    x.run(c["R"], c["T"], c["H"], c["E"], c["K"], c["seed"], c["weighted"], c["fused"],
+          m=c["m"], routing=c["routing"], fp8=fp8)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_configuration(i):
+    c = draw(i)
+    try:
+        if c["family"] == "rank-bf16":
+            run_rank_bf16(c)
+        elif c["family"] == "rank-fp8":
+            run_rank_fp8(c)
+        else:
+            run_expert(c, c["family"] == "expert-fp8")
+    except AssertionError as e:
+        raise AssertionError("case %d %s: %s" % (i, c, e)) from e
