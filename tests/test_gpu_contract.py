@@ -240,3 +240,71 @@ def test_handles_of_different_sizes_interleaved(mod, fp8):
                 y = parity.f32(parity.to_host_u16(out)).reshape(-1, H).astype(np.float64)
                 err = np.abs(y - oc["y"])
                 assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all()
+
+
+def test_dispatch_and_combine_on_two_user_streams(mod):
+    # The inputs are written on stream 1 after a long sleep there; dispatch
+    # runs on stream 1 (its second routing pass on the handle's own stream,
+    # forked from and joined back into the caller's), and the combine on
+    # stream 2 after stream 2 waits for stream 1 only.  Any step that ran on
+    # another stream without those dependencies would read stale inputs or
+    # tables; every result must be the oracle's.
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+    R, T, H, E, K = 4, 300, 256, 32, 4           # the routing passes (T > 256)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    i = inputs(seed=77, R=R, T=T, H=H, E=E, K=K)
+    ids = torch.zeros((R, T, K), dtype=torch.int32, device="cuda")
+    w = torch.zeros((R, T, K), dtype=torch.float32, device="cuda")
+    x = torch.zeros((R, T, H), dtype=torch.bfloat16, device="cuda")
+    ids_h, w_h, x_h = dev(i["topk_ids"], torch.int32), dev(i["topk_w"], torch.float32), \
+        dev(i["x"], torch.bfloat16)
+    res, gam = dev(i["residual"], torch.bfloat16), dev(i["gamma"], torch.bfloat16)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for rnd in range(3):
+        with torch.cuda.stream(s1):
+            torch.cuda._sleep(20_000_000)          # ~10 ms of spinning on stream 1
+            ids.copy_(ids_h)
+            w.copy_(w_h)
+            x.copy_(x_h)
+            view = a.dispatch(ids, w, x)
+        s2.wait_stream(s1)
+        with torch.cuda.stream(s2):
+            rout = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+            out = a.combine(view.recv_x, True, res, gam, 1e-6, residual_out=rout)
+        torch.cuda.synchronize()
+        assert a.get_error(s2) == (mod.MOE_OK, 0)
+        r = oracle.route(i["topk_ids"], i["topk_w"], E, T)
+        assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"]), rnd
+        od = oracle.dispatch(i["topk_ids"], i["topk_w"], i["x"], E, T, r)
+        oc = oracle.combine(r, od["recv_x"], True, i["residual"], i["gamma"], 1e-6)
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H), oc["residual_out"]), rnd
+        y = parity.f32(parity.to_host_u16(out)).reshape(-1, H).astype(np.float64)
+        err = np.abs(y - oc["y"])
+        assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all(), rnd
+        ids.zero_(), w.zero_(), x.zero_()           # (on the current stream, after the sync)
+        torch.cuda.synchronize()
+
+
+def test_many_handles_created_and_destroyed(mod):
+    # create, use and destroy handles repeatedly: every call succeeds, the
+    # results stay the oracle's, and no device memory is left behind
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+    R, T, H, E, K = 4, 40, 128, 16, 4
+    i = inputs(seed=78, R=R, T=T, H=H, E=E, K=K)
+    r = oracle.route(i["topk_ids"], i["topk_w"], E, T)
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    for n in range(50):
+        a = MoeA2A(R, T, H, E, K, "cuda")
+        view = a.dispatch(dev(i["topk_ids"], torch.int32), dev(i["topk_w"], torch.float32),
+                          dev(i["x"], torch.bfloat16))
+        out = a.combine(view.recv_x, False)
+        if n % 10 == 0:
+            torch.cuda.synchronize()
+            assert a.get_error() == (mod.MOE_OK, 0)
+            assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"])
+        a.close()
+        del a, view, out
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == base

@@ -124,3 +124,90 @@ def test_random_configuration(i):
             run_expert(c, c["family"] == "expert-fp8")
     except AssertionError as e:
         raise AssertionError("case %d %s: %s" % (i, c, e)) from e
+
+
+# --------------------------------------------------------------------------
+# The expert-side products on random shapes: both layouts, bf16 or e4m3
+# operands, experts that receive no row or a few (partial row tiles), one or
+# several column tiles of 128 or 256.
+# --------------------------------------------------------------------------
+
+N_PRODUCT_CASES = 24
+
+
+def draw_product(i):
+    rng = np.random.default_rng(5000 + i)
+    layout = ("rank", "expert")[i % 2]
+    fp8 = bool((i // 2) % 2)
+    R = int(rng.choice([1, 2, 3, 4, 8]))
+    Epr = int(rng.integers(1, 5))
+    E = R * Epr
+    K = int(rng.integers(1, min(4, E) + 1))
+    H = int(rng.choice([128, 256, 384, 640]))          # multiples of 128 (e4m3 stage rows)
+    N = int(rng.choice([128, 256, 384, 512]))
+    T = int(rng.integers(1, 161))
+    return dict(layout=layout, fp8=fp8, R=R, E=E, K=K, H=H, N=N, T=T,
+                routing=str(rng.choice(["uniform", "zipf"])), seed=i)
+
+
+@pytest.mark.parametrize("i", range(N_PRODUCT_CASES))
+def test_random_product(i):
+    c = draw_product(i)
+    try:
+        if c["layout"] == "rank":
+            import test_gpu_expert_rank as t
+            R, T, H, E, K, N = c["R"], c["T"], c["H"], c["E"], c["K"], c["N"]
+            if c["fp8"]:
+                a, view, d = t.dispatched_fp8(R, T, H, E, K, c["seed"], c["routing"])
+                qw, sw = t.fp8_weights(c["seed"] + 1, E, N, H)
+            else:
+                a, view, d = t.dispatched(R, T, H, E, K, c["seed"], c["routing"])
+                wb = t.weights(c["seed"] + 1, E, N, H, 1.0 / np.sqrt(H))
+            m = view.plane_stride
+            out = torch.full((R, R, m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            if c["fp8"]:
+                a.expert_gemm_rank_fp8(qw, sw, True, out)
+            else:
+                a.expert_gemm_rank(wb, True, out)
+            torch.cuda.synchronize()
+            assert a.get_error() == (0, 0)
+            got = parity.to_host_u16(out)
+            rows = t.valid_rows(d["r"]["recv_counts"], m)
+            if c["fp8"]:
+                t.check_fp8(got, d, qw, sw, True, rows)
+            else:
+                t.check(got, d, wb, True, rows)
+            counts = d["r"]["recv_counts"]
+            for dd in range(R):
+                for s in range(R):
+                    assert np.isnan(parity.f32(got[dd, s, counts[dd, s]:])).all()
+            a.combine(None, False)
+        else:
+            import test_gpu_expert_gemm as g
+            R, T, H, E, K, N = c["R"], c["T"], c["H"], c["E"], c["K"], c["N"]
+            if c["fp8"]:
+                a, view, d = g.dispatched_fp8(R, T, H, E, K, c["seed"])
+                qw, sw = g.fp8_weights(c["seed"] + 1, E, N, H)
+            else:
+                a, view, d = g.dispatched(R, T, H, E, K, c["seed"], c["routing"])
+                wb = g.weights(c["seed"] + 1, E, N, H, 1.0 / np.sqrt(H))
+            cap = view.plane_stride
+            out = torch.full((E, cap, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            if c["fp8"]:
+                a.expert_gemm_fp8(parity.to_dev(qw, torch.uint8), parity.to_dev(sw, torch.float32),
+                                  out)
+            else:
+                a.expert_gemm(parity.to_dev(wb, torch.bfloat16), out)
+            torch.cuda.synchronize()
+            assert a.get_error() == (0, 0)
+            got = parity.to_host_u16(out)
+            counts = d["r"]["recv_counts"]
+            if c["fp8"]:
+                g.check_rows_fp8(got, d, qw, sw, range(cap))
+            else:
+                g.check_rows(got, d["rx"], wb, counts, range(cap))
+            for e in range(E):
+                assert (got[e, counts[e]:] == 0x7FC0).all()
+            a.combine(None, False)
+    except AssertionError as e:
+        raise AssertionError("product case %d %s: %s" % (i, c, e)) from e
