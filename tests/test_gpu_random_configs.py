@@ -5,10 +5,12 @@ only powers of two), 1-8 experts per rank, top-1 to top-8, hidden sizes from
 one 16-byte vector to 7168 (ragged against a warp's vector span), batches on
 either side of the one-launch dispatch's limit, a runtime maximum above the
 batch, uniform or Zipf routing, weighted or not, fused or not; on the rank
-layout with bf16 or FP8 rows, and on the expert layout.  The checks are the
-fixed tests' own (routing tables, counts, rows or codes and scales, padding
-left untouched, combine outputs), so a failure names its case by index and
-the drawn shape.
+layout with bf16 or FP8 rows, and on the expert layout.  Two more sweeps
+draw shapes of the expert products (both layouts, bf16 and e4m3) and of the
+combine modes (per-rank token counts with dead ranks, the bf16 top-k-slot
+tree, the FP8 output).  The checks are the fixed tests' own (routing
+tables, counts, rows or codes and scales, padding left untouched, combine
+outputs), so a failure names its case by index and the drawn shape.
 """
 from dataclasses import replace
 
@@ -211,3 +213,123 @@ def test_random_product(i):
             a.combine(None, False)
     except AssertionError as e:
         raise AssertionError("product case %d %s: %s" % (i, c, e)) from e
+
+
+# --------------------------------------------------------------------------
+# Combine modes on random shapes (rank layout): per-rank token counts with
+# dead ranks, the bf16 top-k-slot tree, and the FP8 output (plain and fused).
+# --------------------------------------------------------------------------
+
+N_MODE_CASES = 48
+MODES = ("varlen-dead", "tree", "out8", "out8-fused")
+
+
+def draw_mode(i):
+    rng = np.random.default_rng(9000 + i)
+    mode = MODES[i % len(MODES)]
+    R = int(rng.choice([2, 3, 4, 5, 8, 12, 16]))
+    Epr = int(rng.integers(1, 9))
+    E = R * Epr
+    K = int(rng.integers(1, min(8, E) + 1))
+    H = int(rng.choice([16, 48, 144, 512, 1040, 2048, 7168]))
+    T = int(rng.integers(1, 301))
+    while R * R * T * H * 4 > WORKSPACE_BUDGET and T > 1:
+        T = max(1, T // 2)
+    counts = [int(v) for v in rng.integers(0, T + 1, R)]
+    dead = [d for d in range(R) if rng.random() < 0.25][:R - 1]
+    return dict(mode=mode, R=R, E=E, K=K, H=H, T=T, counts=counts, dead=dead,
+                routing=str(rng.choice(["uniform", "zipf"])),
+                weighted=bool(rng.integers(2)) and mode != "tree",
+                fused=bool(rng.integers(2)) or mode == "out8-fused", seed=i)
+
+
+def run_mode(c):
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_REDUCE_BF16_TOPK_TREE
+    R, E, K, H, T, seed = c["R"], c["E"], c["K"], c["H"], c["T"], c["seed"]
+    ids = synth.topk_ids(seed, R, T, E, K, c["routing"])
+    w = synth.topk_weights(seed, R, T, K)
+    x = synth.per_rank_rows(seed, synth.X, R, T, H)
+    res = synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H)
+    gam = synth.gamma(seed, H)
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    dev = parity.to_dev
+    live = np.ones((R, T), bool)
+    ids_o = ids.copy()
+    if c["mode"] == "varlen-dead":
+        for s, n in enumerate(c["counts"]):
+            ids_o[s, n:] = -1
+            live[s, n:] = False
+        for d in c["dead"]:
+            ids_o[(ids_o >= 0) & (ids_o // (E // R) == d)] = -1
+        a.set_active_ranks(((1 << R) - 1) & ~sum(1 << d for d in c["dead"]))
+        view = a.dispatch_varlen(dev(ids, torch.int32), dev(w, torch.float32),
+                                 dev(x, torch.bfloat16), c["counts"])
+    else:
+        if c["mode"] == "tree":
+            a.set_reduction(MOE_REDUCE_BF16_TOPK_TREE)
+        view = a.dispatch(dev(ids, torch.int32), dev(w, torch.float32), dev(x, torch.bfloat16))
+    r = oracle.route(ids_o, w, E, T)
+    cnt = view.recv_counts.cpu().numpy()
+    assert np.array_equal(cnt, r["recv_counts"]), "recv_counts"
+    eo = synth.expert_out_planes(seed, R, T, H, cnt)
+    pay = a.combine_payload()
+    for d in range(R):
+        for s in range(R):
+            if cnt[d, s]:
+                pay[d, s, :cnt[d, s]].copy_(dev(eo[d, s, :cnt[d, s]], torch.bfloat16))
+    fused = c["fused"]
+    rout = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    res_d, gam_d = dev(res, torch.bfloat16), dev(gam, torch.bfloat16)
+    tok = np.flatnonzero(live.ravel())
+    if c["mode"].startswith("out8"):
+        if fused:
+            out, sc = a.combine_fp8(None, c["weighted"], res_d, gam_d, 1e-6, residual_out=rout)
+        else:
+            out, sc = a.combine_fp8(None, c["weighted"])
+    elif fused:
+        out = a.combine(None, c["weighted"], res_d, gam_d, 1e-6, residual_out=rout)
+    else:
+        out = a.combine(None, c["weighted"])
+    torch.cuda.synchronize()
+    assert a.get_error() == (0, 0) and a.phase == 0
+    if c["mode"] == "tree":
+        oc = oracle.combine_topk_tree(r, ids_o, E, eo, res if fused else None,
+                                      gam if fused else None, 1e-6, tokens=tok)
+    else:
+        oc = oracle.combine(r, eo, c["weighted"], res if fused else None,
+                            gam if fused else None, 1e-6, tokens=tok)
+    if fused:
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H)[tok],
+                              oc["residual_out"]), "residual_out"
+    if c["mode"].startswith("out8"):
+        g_q = out.view(torch.uint8).cpu().numpy().reshape(R * T, H)[tok]
+        g_s = sc.cpu().numpy().ravel()[tok]
+        if fused:
+            y = oc["y"]
+            q_ref, s_ref = oracle.quantize_f32_rows_fp8(y.astype(np.float32))
+            assert (np.abs(g_s.astype(np.float64) - s_ref) <= 1e-5 * s_ref).all(), "scales"
+            deq = oracle.fp8_to_f32(g_q).astype(np.float64) * g_s[:, None].astype(np.float64)
+            bound = (2.0 ** -4 + 1e-4) * np.abs(y) + 2.0 ** -10 * g_s[:, None] + 1e-6
+            assert (np.abs(deq - y) <= bound).all(), "FP8 fused output"
+        else:
+            q_ref, s_ref = oracle.quantize_f32_rows_fp8(oc["acc"])
+            assert np.array_equal(g_q, q_ref), "FP8 codes"
+            assert np.array_equal(g_s.view(np.uint32), s_ref.view(np.uint32)), "FP8 scales"
+    else:
+        got = parity.to_host_u16(out).reshape(R * T, H)[tok]
+        if fused:
+            y = parity.f32(got).astype(np.float64)
+            err = np.abs(y - oc["y"])
+            assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all()
+        else:
+            assert np.array_equal(got, oc["out"]), "combine sum"
+    a.close()
+
+
+@pytest.mark.parametrize("i", range(N_MODE_CASES))
+def test_random_combine_mode(i):
+    c = draw_mode(i)
+    try:
+        run_mode(c)
+    except AssertionError as e:
+        raise AssertionError("mode case %d %s: %s" % (i, c, e)) from e
