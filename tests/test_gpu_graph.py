@@ -300,3 +300,93 @@ def test_graph_replays_rank_plane_moe_step(fp8):
         y = parity.f32(parity.to_host_u16(out).reshape(R * T, H)).astype(np.float64)
         err = np.abs(y - oc["y"])
         assert (err <= parity.ABS_TOL).all() and (err <= parity.REL_TOL * np.abs(oc["y"])).all()
+
+
+@pytest.mark.parametrize("mode", ["out8-fused", "tree", "varlen-dead"])
+def test_graph_replays_combine_modes(mode):
+    # Dispatch + combine captured once in the FP8-output, bf16-tree or
+    # per-rank-count (with a dead rank) mode, replayed on three new input
+    # sets (counts and the dead rank are host-side and fixed by the capture):
+    # every replay equals the oracle on that replay's inputs.
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_REDUCE_BF16_TOPK_TREE
+    R, T, H, E, K = 4, 60, 256, 32, 4
+    counts = [60, 0, 33, 7]
+    dead = 2
+    a = MoeA2A(R, T, H, E, K, "cuda")
+    if mode == "tree":
+        a.set_reduction(MOE_REDUCE_BF16_TOPK_TREE)
+    if mode == "varlen-dead":
+        a.set_active_ranks(0xF & ~(1 << dead))
+
+    def inputs(seed):
+        return dict(ids=synth.topk_ids(seed, R, T, E, K), w=synth.topk_weights(seed, R, T, K),
+                    x=synth.per_rank_rows(seed, synth.X, R, T, H),
+                    res=synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H),
+                    g=synth.gamma(seed, H))
+
+    first = inputs(500)
+    ids = parity.to_dev(first["ids"], torch.int32)
+    wts = parity.to_dev(first["w"], torch.float32)
+    x = parity.to_dev(first["x"], torch.bfloat16)
+    res = parity.to_dev(first["res"], torch.bfloat16)
+    gam = parity.to_dev(first["g"], torch.bfloat16)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    out8 = torch.empty((R, T, H), dtype=torch.float8_e4m3fn, device="cuda")
+    osc = torch.empty((R, T), dtype=torch.float32, device="cuda")
+    rout = torch.empty_like(res)
+
+    def step():
+        v = a.dispatch_varlen(ids, wts, x, counts) if mode == "varlen-dead" else \
+            a.dispatch(ids, wts, x, T)
+        if mode == "out8-fused":
+            a.combine_fp8(v.recv_x, True, res, gam, 1e-6, out8, osc, rout)
+        elif mode == "tree":
+            a.combine(v.recv_x, False, out=out)
+        else:
+            a.combine(v.recv_x, True, res, gam, 1e-6, out, rout)
+        return v
+
+    view = step()                                  # direct first (stream, events)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        view = step()
+
+    for seed in (51, 52, 53):
+        inp = inputs(seed)
+        for dst, src, dt in ((ids, inp["ids"], torch.int32), (wts, inp["w"], torch.float32),
+                             (x, inp["x"], torch.bfloat16), (res, inp["res"], torch.bfloat16),
+                             (gam, inp["g"], torch.bfloat16)):
+            dst.copy_(parity.to_dev(src, dt))
+        g.replay()
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0)
+        ids_o = inp["ids"].copy()
+        live = np.ones((R, T), bool)
+        if mode == "varlen-dead":
+            for s, n in enumerate(counts):
+                ids_o[s, n:] = -1
+                live[s, n:] = False
+            ids_o[(ids_o >= 0) & (ids_o // (E // R) == dead)] = -1
+        tok = np.flatnonzero(live.ravel())
+        r = oracle.route(ids_o, inp["w"], E, T)
+        assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"]), (mode, seed)
+        od = oracle.dispatch(ids_o, inp["w"], inp["x"], E, T, r)
+        if mode == "tree":
+            oc = oracle.combine_topk_tree(r, ids_o, E, od["recv_x"], tokens=tok)
+            assert np.array_equal(parity.to_host_u16(out).reshape(R * T, H)[tok], oc["out"]), seed
+            continue
+        oc = oracle.combine(r, od["recv_x"], True, inp["res"], inp["g"], 1e-6, tokens=tok)
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H)[tok],
+                              oc["residual_out"]), (mode, seed)
+        y = oc["y"]
+        if mode == "out8-fused":
+            g_q = out8.view(torch.uint8).cpu().numpy().reshape(R * T, H)[tok]
+            g_s = osc.cpu().numpy().ravel()[tok].astype(np.float64)
+            deq = oracle.fp8_to_f32(g_q).astype(np.float64) * g_s[:, None]
+            bound = (2.0 ** -4 + 1e-4) * np.abs(y) + 2.0 ** -10 * g_s[:, None] + 1e-6
+            assert (np.abs(deq - y) <= bound).all(), seed
+        else:
+            got = parity.f32(parity.to_host_u16(out).reshape(R * T, H)[tok]).astype(np.float64)
+            err = np.abs(got - y)
+            assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(y))).all(), seed
