@@ -308,3 +308,58 @@ def test_many_handles_created_and_destroyed(mod):
         del a, view, out
     torch.cuda.synchronize()
     assert torch.cuda.memory_allocated() == base
+
+
+def test_two_host_threads_with_their_own_handles(mod):
+    # Distinct handles are independent: two host threads, each with its own
+    # handle (different sizes, so each prepares its own kernel shapes while
+    # the other runs) and its own stream, dispatch and combine at the same
+    # time; every call's result is the oracle's.
+    import threading
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A
+    cfgs = [dict(R=4, T=300, H=512, E=16, K=4, seed=81), dict(R=8, T=40, H=2048, E=64, K=8, seed=82)]
+    expect, inputs_dev = [], []
+    for c in cfgs:
+        i = inputs(seed=c["seed"], R=c["R"], T=c["T"], H=c["H"], E=c["E"], K=c["K"])
+        r = oracle.route(i["topk_ids"], i["topk_w"], c["E"], c["T"])
+        od = oracle.dispatch(i["topk_ids"], i["topk_w"], i["x"], c["E"], c["T"], r)
+        oc = oracle.combine(r, od["recv_x"], True, i["residual"], i["gamma"], 1e-6)
+        expect.append((r, oc))
+        inputs_dev.append([dev(i["topk_ids"], torch.int32), dev(i["topk_w"], torch.float32),
+                           dev(i["x"], torch.bfloat16), dev(i["residual"], torch.bfloat16),
+                           dev(i["gamma"], torch.bfloat16)])
+    torch.cuda.synchronize()
+    errors = []
+    barrier = threading.Barrier(len(cfgs))
+
+    def work(k):
+        try:
+            c, (r, oc) = cfgs[k], expect[k]
+            ids, w, x, res, gam = inputs_dev[k]
+            stream = torch.cuda.Stream()
+            barrier.wait()
+            a = MoeA2A(c["R"], c["T"], c["H"], c["E"], c["K"], "cuda")
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    view = a.dispatch(ids, w, x)
+                    rout = torch.empty_like(res)
+                    out = a.combine(view.recv_x, True, res, gam, 1e-6, residual_out=rout)
+                stream.synchronize()
+            assert a.get_error(stream) == (mod.MOE_OK, 0)
+            assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"])
+            H = c["H"]
+            assert np.array_equal(parity.to_host_u16(rout).reshape(-1, H), oc["residual_out"])
+            y = parity.f32(parity.to_host_u16(out)).reshape(-1, H).astype(np.float64)
+            err = np.abs(y - oc["y"])
+            assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all()
+            a.close()
+        except Exception as e:          # reported by the main thread
+            errors.append((k, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(len(cfgs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not any(t.is_alive() for t in threads)
+    assert not errors, errors
