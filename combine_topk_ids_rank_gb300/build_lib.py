@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(HERE, "libmoe_a2a.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["route.cu", "dispatch.cu", "combine.cu", "combine_ring.cu", "combine_small.cu", "combine_tree.cu",
-           "dispatch_fp8.cu", "dispatch_small.cu", "route_expert.cu", "expert_gemm.cu", "expert_rank.cu",
+           "dispatch_fp8.cu", "dispatch_small.cu", "dispatch_small_expert.cu", "route_expert.cu",
+           "expert_gemm.cu", "expert_rank.cu",
            "moe_a2a.cpp", "moe_noalloc.cu"]
 HEADERS = ["kernels.h", "expert.h", "dispatch_small.h", "smem_limit.h", "ptx.cuh", "fp8.cuh",
            "tcgen05.cuh", "f32x2.cuh"]

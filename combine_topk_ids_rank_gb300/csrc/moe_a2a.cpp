@@ -59,6 +59,14 @@ int gemm_group_m(const moe::Tuning &tn) {
 // 33.3-35.2 vs 38.4-38.7 us.
 constexpr int kSmallDispatchMaxT = 256;
 
+// Largest tokens per rank for the expert layout's one-launch dispatch by
+// default (dispatch_small_expert.cu; each warp reads the ids of every token
+// before it, so its work grows with the batch).  Measured faster than the
+// two routing passes + row copy at every size up to one routing tile (L2
+// flushed, p50): T = 1 8.2 vs 15.8 us, T = 32 12.7 vs 17.8, T = 64 16.8 vs
+// 22.0, T = 128 25.0-26.4 vs 30.1, T = 192 35.3 vs 38.3, T = 256 47.6 vs 50.9.
+constexpr int kSmallExpertDispatchMaxT = 256;
+
 // The same for FP8 receive rows (one CTA per token, dispatch_small.cu):
 // measured faster than the routing passes + FP8 row copy up to 128 tokens
 // per rank (T = 1 10.2 vs 14.9 us, T = 64 13.4 vs 16.8, T = 128 16.4 vs
@@ -69,7 +77,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
     size_t recv_x, expert_out, recv_ids, recv_w, recv_scale, src_token, recv_counts,
-        local_counts, local_counts2;
+        local_counts, local_counts2, recv_counts2;
     size_t send_slot, dest_weight, topk_dest, tile_counts, tile_prefix, tile_ticket, hist_accum,
         local_slot, flags;
     size_t total;
@@ -119,7 +127,9 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
         L->src_token = take(E * cap * 4);
         L->recv_counts = take(E * 4);
         L->local_counts = take(E * 4);
-        L->local_counts2 = L->local_counts;
+        // the one-launch dispatch alternates two (histogram, rows) pairs
+        L->local_counts2 = take(E * 4);
+        L->recv_counts2 = take(E * 4);
         L->send_slot = take(R * M * KP * 4);
         L->dest_weight = take(R * M * KP * 4);
         L->topk_dest = take(0);
@@ -144,6 +154,7 @@ bool compute_layout(const moe_a2a_config_t *c, int layout, Layout *L) {
     L->recv_counts = take(R * R * 4);
     L->local_counts = take(E * 4);
     L->local_counts2 = take(E * 4);  // the one-launch dispatch alternates the two
+    L->recv_counts2 = L->recv_counts;  // (its recv counts are written, not added)
     L->send_slot = take(R * M * RP * 4);
     L->dest_weight = take(R * M * RP * 4);
     L->topk_dest = take(R * M * K);
@@ -207,7 +218,8 @@ struct moe_a2a {
     moe::LaunchShape dispatch_shape;
     int fp8_stages;  // FP8 dispatch ring depth and shape (H % 16 == 0 only)
     moe::LaunchShape fp8_shape;
-    moe::DispatchSmallShapes small;  // one-launch dispatch (rank layout)
+    moe::DispatchSmallShapes small;  // one-launch dispatch (rank layout, or the expert
+                                     // layout's own kernel)
     moe::DispatchSmallFp8Shape small_fp8;  // its FP8 receive-row variant
     bool small_fp8_ok;
     int small_fp8_max;  // MOE_DISPATCH_SMALL_FP8_MAX (0: the default, -1: never)
@@ -216,7 +228,9 @@ struct moe_a2a {
     // Local-expert counts: the region holding the current dispatch's counts,
     // and for the one-launch dispatch the buffer (0: local_counts, 1:
     // local_counts2) its next call adds into, and whether that one is zero.
-    size_t cur_counts;
+    // The expert layout's one-launch dispatch alternates its rows per expert
+    // the same way (recv_counts / recv_counts2, in step with the histogram).
+    size_t cur_counts, cur_recv_counts;
     int small_sel;
     bool small_zero_ok;
     // The rank layout's second routing pass runs on `side`, beside the row
@@ -257,8 +271,10 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
             return cuda_failed();
         h->fp8_stages = fp.stages;
     }
-    if (h->L.layout == MOE_LAYOUT_RANK &&
-        moe::dispatch_small_prepare(2 * h->cfg.hidden, h->num_sms, &h->small) != cudaSuccess)
+    if ((h->L.layout == MOE_LAYOUT_RANK
+             ? moe::dispatch_small_prepare(2 * h->cfg.hidden, h->num_sms, &h->small)
+             : moe::dispatch_small_expert_prepare(2 * h->cfg.hidden, h->num_sms, &h->small)) !=
+        cudaSuccess)
         return cuda_failed();
     h->small_fp8_ok = h->L.layout == MOE_LAYOUT_RANK && h->cfg.hidden % 16 == 0 &&
                       moe::dispatch_small_fp8_prepare(h->cfg.hidden, &h->small_fp8) ==
@@ -360,7 +376,13 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
 // rows when every source holds the same T tokens, T at most one routing tile
 // and at most Tuning::dispatch_small_max (measured break-even, below).
 bool small_dispatch(const moe_a2a_t *h, const moe::TokenMap &map) {
-    if (h->L.layout != MOE_LAYOUT_RANK || !map.uniform) return false;
+    if (!map.uniform) return false;
+    if (h->L.layout == MOE_LAYOUT_EXPERT) {  // bf16 rows only
+        if (h->recv_format != MOE_FORMAT_BF16) return false;
+        const int lim = h->tuning.dispatch_small_max;
+        const int T_max = lim < 0 ? 0 : (lim == 0 ? kSmallExpertDispatchMaxT : lim);
+        return map.stride >= 1 && map.stride <= T_max && map.stride <= moe::kRouteTile;
+    }
     int T_max = 0;
     if (h->recv_format == MOE_FORMAT_BF16) {
         const int lim = h->tuning.dispatch_small_max;
@@ -423,6 +445,47 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
             cudaMemsetAsync(h->ws + h->L.local_counts, 0, sizeof(int32_t) * E, st) !=
                 cudaSuccess)
             return cuda_failed();
+    } else if (expert && one_launch) {
+        // one launch: every copy warp derives its token's rows itself
+        const size_t hist[2] = {h->L.local_counts, h->L.local_counts2};
+        const size_t rows[2] = {h->L.recv_counts, h->L.recv_counts2};
+        const int sel = h->small_sel;
+        if (!h->small_zero_ok &&
+            (cudaMemsetAsync(h->ws + hist[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess ||
+             cudaMemsetAsync(h->ws + rows[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess))
+            return cuda_failed();
+        const int row_bytes = 2 * h->cfg.hidden;
+        const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
+        moe::DispatchSmallExpertParams sp;
+        sp.topk_ids = d_topk_ids;
+        sp.topk_w = d_topk_w;
+        sp.x = static_cast<const uint8_t *>(d_x);
+        sp.recv_x = at<uint8_t>(h, h->L.recv_x);
+        sp.send_row = at<int32_t>(h, h->L.send_slot);
+        sp.wsum = at<float>(h, h->L.dest_weight);
+        sp.src_token = at<int32_t>(h, h->L.src_token);
+        sp.recv_w = at<float>(h, h->L.recv_w);
+        sp.counts = at<int32_t>(h, hist[sel]);
+        sp.counts_clear = at<int32_t>(h, hist[sel ^ 1]);
+        sp.recv_counts = at<int32_t>(h, rows[sel]);
+        sp.recv_counts_clear = at<int32_t>(h, rows[sel ^ 1]);
+        sp.flags = flags;
+        sp.active = h->active;
+        sp.R = R, sp.K = K, sp.E = E, sp.Epr = E / R, sp.KP = h->L.P, sp.T = map.stride;
+        sp.cap = dest.cap;
+        sp.row_bytes = row_bytes;
+        sp.chunk_bytes = h->small.chunk_bytes[c];
+        sp.chunks = h->small.chunks[c];
+        sp.stages = h->small.stages;
+        sp.stage_bytes = h->small.stage_bytes[c];
+        sp.units = ntok * sp.chunks;
+        h->small_zero_ok = false;  // until the launch that clears the other pair is queued
+        if (moe::launch_dispatch_small_expert(sp, h->small.shape[c], st) != cudaSuccess)
+            return cuda_failed();
+        h->cur_counts = hist[sel];
+        h->cur_recv_counts = rows[sel];
+        h->small_sel = sel ^ 1;
+        h->small_zero_ok = true;
     } else if (expert) {
         if (h->accum_dirty) {  // the histogram accumulator
             if (cudaMemsetAsync(h->ws + h->L.hist_accum, 0, sizeof(int32_t) * E, st) !=
@@ -516,6 +579,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
                 return cuda_failed();
         }
         h->cur_counts = bufs[sel];
+        h->cur_recv_counts = h->L.recv_counts;
         h->small_sel = sel ^ 1;
         h->small_zero_ok = true;
     } else {
@@ -592,8 +656,10 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
     }
 
     if (!one_launch) {
-        // the routing pass (or the empty call) wrote local_counts
+        // the routing pass (or the empty call) wrote local_counts and
+        // recv_counts (the first buffer of each pair)
         h->cur_counts = h->L.local_counts;
+        h->cur_recv_counts = h->L.recv_counts;
         if (h->small_sel == 0) h->small_zero_ok = false;
     }
     h->map = map;
@@ -605,7 +671,7 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
         out_view->recv_topk_ids = expert ? nullptr : at<int32_t>(h, h->L.recv_ids);
         out_view->recv_topk_w = at<float>(h, h->L.recv_w);
         out_view->src_token = at<int32_t>(h, h->L.src_token);
-        out_view->recv_counts = at<int32_t>(h, h->L.recv_counts);
+        out_view->recv_counts = at<int32_t>(h, h->cur_recv_counts);
         out_view->local_expert_counts = at<int32_t>(h, h->cur_counts);
         out_view->send_slot = at<int32_t>(h, h->L.send_slot);
         out_view->dest_weight = at<float>(h, h->L.dest_weight);
@@ -935,7 +1001,7 @@ int expert_gemm_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale, int3
     gp.x = h->ws + h->L.recv_x;
     gp.w = d_w;
     gp.out = d_out != nullptr ? d_out : h->ws + h->L.expert_out;
-    gp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+    gp.recv_counts = at<int32_t>(h, h->cur_recv_counts);
     gp.x_scale = fp8 ? at<float>(h, h->L.recv_scale) : nullptr;
     gp.w_scale = fp8 ? d_w_scale : nullptr;
     gp.flags = at<uint32_t>(h, h->L.flags);
@@ -1026,7 +1092,7 @@ int expert_gemm_rank_impl(moe_a2a_t *h, const void *d_w, const float *d_w_scale,
     moe::RankPairsParams rp;
     rp.recv_ids = at<int32_t>(h, h->L.recv_ids);
     rp.recv_w = at<float>(h, h->L.recv_w);
-    rp.recv_counts = at<int32_t>(h, h->L.recv_counts);
+    rp.recv_counts = at<int32_t>(h, h->cur_recv_counts);
     rp.pair_counts = at<int32_t>(h, h->cur_counts);
     rp.cursor = reinterpret_cast<int32_t *>(sc + S.cursor);
     rp.pair_row = reinterpret_cast<int32_t *>(sc + S.pair_row);

@@ -314,11 +314,13 @@ int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_w
  * within each (destination, source) plane, copies x rows and the masked
  * top-k metadata into the planes, and counts rows per plane and per local
  * expert.  Queues one kernel on `stream` when every source holds the same
- * number of tokens, at most 256 (rank layout, bf16 rows; 128 for FP8 rows),
- * and `stream` is
- * not capturing into a CUDA graph (that kernel alternates two count buffers
- * between calls, which a replay cannot follow); else three (the second on the handle's
- * own stream, as described above).  IDLE -> DISPATCHED; returns
+ * number of tokens, at most 256 (rank layout with bf16 rows, or the expert
+ * layout with bf16 rows; 128 for the rank layout's FP8 rows), and `stream`
+ * is not capturing into a CUDA graph (that kernel alternates two count
+ * buffers between calls, which a replay cannot follow; in the expert layout
+ * the rows per expert alternate with them, so read them through the view);
+ * else three (the rank layout's second on the handle's own stream, as
+ * described above).  IDLE -> DISPATCHED; returns
  * MOE_ERR_PHASE if already DISPATCHED.  If out_view is not NULL it receives
  * the views of this call. */
 int moe_dispatch(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w,

@@ -260,14 +260,15 @@ def test_workspace_is_the_documented_regions(abi, R, M, H, E, K):
             R * M * RP * 4, 256]
     c = abi.config(R, M, H, E, K)
     assert abi.moe_a2a_workspace_bytes(c) == _regions_total(rank)
-    # Expert layout: per-expert planes of cap = R * M rows, send table of KP
-    # entries per token, per-tile expert counts (256-token tiles), the
-    # expert histogram accumulator, the flag word.
+    # Expert layout: per-expert planes of cap = R * M rows, rows per expert
+    # and the expert histogram (two pairs: the one-launch dispatch alternates
+    # them), send table of KP entries per token, per-tile expert counts
+    # (256-token tiles), the expert histogram accumulator, the flag word.
     if E <= 1024 and E * R * M < 2 ** 31:
         KP = (K + 3) // 4 * 4
         cap, NTe = R * M, (M + 255) // 256
         ex = [E * cap * H * 2, E * cap * H * 2, E * cap * 4, E * cap * 4, E * cap * 4, E * 4,
-              E * 4, R * M * KP * 4, R * M * KP * 4, R * NTe * E * 4, E * 4, 256]
+              E * 4, E * 4, E * 4, R * M * KP * 4, R * M * KP * 4, R * NTe * E * 4, E * 4, 256]
         assert abi.moe_a2a_workspace_bytes_layout(c, abi.MOE_LAYOUT_EXPERT) == \
             _regions_total(ex)
 

@@ -235,3 +235,53 @@ def test_expert_layout_fp8_combine_output(fused):
         assert (np.abs(g_s.astype(np.float64) - s_ref) <= 1e-5 * s_ref).all()
         step = lambda c: np.where(c & 0x80, -(c.astype(np.int32) & 0x7F), c.astype(np.int32) & 0x7F)
         assert (np.abs(step(g_q) - step(q_ref)) <= 1).all()
+
+
+@pytest.mark.parametrize("small_max", ["-1", "256"])
+@pytest.mark.parametrize("T", [1, 33, 64, 200, 256])
+def test_expert_one_launch_dispatch_modes(monkeypatch, small_max, T):
+    # the same batches through the routing passes + row copy (-1) and the
+    # one-launch dispatch (up to 256 tokens per rank): both equal the oracle
+    # (routing tables, counts, rows, untouched padding, combines)
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_LAYOUT_EXPERT
+    monkeypatch.setenv("MOE_DISPATCH_SMALL_MAX", small_max)
+    run(8, T, 256, 64, 8, seed=T + 7, weighted=True, fused=True)
+    run(4, T, 128, 16, 4, seed=T + 8, weighted=False, fused=False, routing="zipf")
+    a = MoeA2A(4, T, 128, 16, 4, "cuda", layout=MOE_LAYOUT_EXPERT)
+    view = a.dispatch(parity.to_dev(synth.topk_ids(1, 4, T, 16, 4), torch.int32),
+                      parity.to_dev(synth.topk_weights(1, 4, T, 4), torch.float32),
+                      torch.zeros((4, T, 128), dtype=torch.bfloat16, device="cuda"))
+    assert view.kernels == (3 if small_max == "-1" else 1)
+    a.combine(None, False)
+
+
+def test_expert_one_launch_alternates_with_the_routing_passes():
+    # One handle, calls alternating between the one-launch dispatch (T <= 256)
+    # and the routing passes (T = 300), with ranks marked dead and alive again
+    # in between: every call's rows per expert and histogram are the
+    # oracle's (the one-launch path adds into a buffer pair that the previous
+    # call cleared; the routing passes write the first pair).
+    from combine_topk_ids_rank_gb300.moe_a2a import MoeA2A, MOE_LAYOUT_EXPERT
+    R, M, H, E, K = 4, 300, 128, 16, 4
+    a = MoeA2A(R, M, H, E, K, "cuda", layout=MOE_LAYOUT_EXPERT)
+    plan = [(40, 0), (40, 0), (300, 0), (17, 0b0100), (300, 0b0010), (64, 0), (1, 0), (40, 0)]
+    for n, (T, dead) in enumerate(plan):
+        a.set_active_ranks(((1 << R) - 1) & ~dead)
+        inp = make(R, T, H, E, K, seed=100 + n)
+        view = a.dispatch(parity.to_dev(inp["ids"], torch.int32),
+                          parity.to_dev(inp["w"], torch.float32),
+                          parity.to_dev(inp["x"], torch.bfloat16))
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0)
+        assert view.kernels == (1 if T <= 256 else 3), (n, T)
+        ids_o = inp["ids"].copy()
+        for d in range(R):
+            if dead >> d & 1:
+                ids_o[(ids_o >= 0) & (ids_o // (E // R) == d)] = -1
+        r = oracle.route_experts(ids_o, inp["w"], E, T)
+        assert np.array_equal(view.recv_counts.cpu().numpy(), r["recv_counts"]), (n, T)
+        assert np.array_equal(view.local_expert_counts.cpu().numpy(),
+                              r["local_expert_counts"]), (n, T)
+        ss = view.send_slot.cpu().numpy()[:, :T, :K]
+        assert np.array_equal(ss, r["send_row"]), (n, T)
+        a.combine(None, False)
