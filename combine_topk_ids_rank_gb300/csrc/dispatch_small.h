@@ -70,4 +70,27 @@ cudaError_t dispatch_small_expert_prepare(int row_bytes, int num_sms, DispatchSm
 cudaError_t launch_dispatch_small_expert(const DispatchSmallExpertParams &p,
                                          const LaunchShape &shape, cudaStream_t st);
 
+// The same with FP8 receive rows: one CTA per token (the whole row, so that
+// its amax is one CTA reduction), its e4m3 codes and scale stored to each of
+// its rows.  Shapes as for the rank layout's FP8 one-launch dispatch.
+struct DispatchSmallExpertFp8Params {
+    const int32_t *topk_ids;   // [R][T][K]
+    const float *topk_w;       // [R][T][K]
+    const uint16_t *x;         // bf16 [R][T][H]
+    uint8_t *recv_x8;          // e4m3 [E][cap][H]
+    float *recv_scale;         // [E][cap]
+    int32_t *send_row;         // [R][T][KP]
+    float *wsum;               // [R][T][KP]
+    int32_t *src_token;        // [E][cap]
+    float *recv_w;             // [E][cap]
+    int32_t *counts, *counts_clear, *recv_counts, *recv_counts_clear;  // as above
+    uint32_t *flags;
+    uint32_t active;
+    int R, K, E, Epr, KP, T, cap, H, H8;
+    unsigned long long epr_magic;  // set by the launcher
+};
+cudaError_t dispatch_small_expert_fp8_prepare(int H, DispatchSmallFp8Shape *out);
+cudaError_t launch_dispatch_small_expert_fp8(const DispatchSmallExpertFp8Params &p,
+                                             const DispatchSmallFp8Shape &shape, cudaStream_t st);
+
 }  // namespace moe

@@ -29,6 +29,7 @@
 // previous call cleared and clears the other one.  Waits are bounded: on
 // time-out the kernel raises the flag, drains its copies and returns.
 #include "dispatch_small.h"
+#include "fp8.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "smem_limit.h"
@@ -90,6 +91,58 @@ __device__ __forceinline__ int rows_before(const int32_t *ids_all, int tok, int 
     return cnt;
 }
 
+// The routing outputs of token `tok` (one warp; its raw ids, live experts
+// and weights one per lane, first_of_e and my_row per lane as the kernels
+// derive them): send row and weights of every top-k slot (padding slots up
+// to KP included), source map and row weight of each of its rows, the two
+// count arrays, the bad-id flag.
+template <class P>
+__device__ __forceinline__ void write_expert_routing(const P &p, int K, int tok, int raw,
+                                                     int my_e, float my_w, bool first_of_e,
+                                                     long long my_row, int lane) {
+    // slot k's weight: its expert's weights over k' >= k in ascending k',
+    // from +0.0 (only the first slot of an expert keeps it)
+    float wsum = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        const int e = __shfl_sync(kFull, my_e, k);
+        const float wk = __shfl_sync(kFull, my_w, k);
+        if (k >= lane && e == my_e && my_e >= 0) wsum = __fadd_rn(wsum, wk);
+    }
+    const long long trow = (long long)tok * p.KP;
+    if (lane < K) {
+        p.send_row[trow + lane] = (int32_t)my_row;
+        p.wsum[trow + lane] = first_of_e ? wsum : 0.0f;
+        if (raw < -1 || raw >= p.E) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_EXPERT_ID);
+        if (my_e >= 0) atomicAdd(p.counts + my_e, 1);
+        if (first_of_e) {
+            p.src_token[my_row] = tok;  // s * T + t (uniform T)
+            p.recv_w[my_row] = wsum;
+            atomicAdd(p.recv_counts + my_e, 1);
+        }
+    } else if (lane < p.KP) {
+        p.send_row[trow + lane] = -1;
+        p.wsum[trow + lane] = 0.0f;
+    }
+}
+
+// Lane k's live expert of token `tok`, whether slot k is its first, and its
+// row (-1 if none); raw id and weight of slot k.
+template <int KT, class P>
+__device__ __forceinline__ void token_rows(const P &p, int K, int tok, int lane, int &raw,
+                                           int &my_e, float &my_w, bool &first_of_e,
+                                           long long &my_row) {
+    raw = lane < K ? __ldg(p.topk_ids + (size_t)tok * K + lane) : -1;
+    my_w = lane < K ? __ldg(p.topk_w + (size_t)tok * K + lane) : 0.0f;
+    my_e = live_expert(raw, p.E, p.epr_magic, p.active);
+    first_of_e = my_e >= 0;
+    for (int k = 0; k < K; ++k) {
+        const int e = __shfl_sync(kFull, my_e, k);
+        if (k < lane && e == my_e) first_of_e = false;
+    }
+    const int before = rows_before<KT>(p.topk_ids, tok, K, my_e, lane);
+    my_row = first_of_e ? (long long)my_e * p.cap + before : -1;  // before < R*T <= cap
+}
+
 template <int KT>
 __global__ void __launch_bounds__(32)
     dispatch_small_expert_kernel(const DispatchSmallExpertParams p) {
@@ -136,19 +189,12 @@ __global__ void __launch_bounds__(32)
         const int tok = div_by(u, p.chunks_magic);  // s * T + t
         const int chunk = u - tok * p.chunks;
 
-        // the token's ids and weights, one per lane (K <= 32); lane k's
-        // expert if live, and whether slot k is that expert's first
-        const int raw = lane < K ? __ldg(p.topk_ids + (size_t)tok * K + lane) : -1;
-        const float my_w = lane < K ? __ldg(p.topk_w + (size_t)tok * K + lane) : 0.0f;
-        const int my_e = live_expert(raw, p.E, p.epr_magic, p.active);
-        bool first_of_e = my_e >= 0;
-        for (int k = 0; k < K; ++k) {
-            const int e = __shfl_sync(kFull, my_e, k);
-            if (k < lane && e == my_e) first_of_e = false;
-        }
-        const int before = rows_before<KT>(p.topk_ids, tok, K, my_e, lane);
-        const long long my_row =
-            first_of_e ? (long long)my_e * p.cap + before : -1;  // before < R*T <= cap
+        // the token's ids and weights, one per lane (K <= 32), and its rows
+        int raw, my_e;
+        float my_w;
+        bool first_of_e;
+        long long my_row;
+        token_rows<KT>(p, K, tok, lane, raw, my_e, my_w, first_of_e, my_row);
 
         // The ids are inputs too; before the first write, wait for the kernels
         // before this one in the stream (a combine still reading the
@@ -159,31 +205,7 @@ __global__ void __launch_bounds__(32)
         }
 
         // ---- routing outputs, by the warp holding the token's first chunk ----
-        if (chunk == 0) {
-            // slot k's weight: its expert's weights over k' >= k in ascending
-            // k', from +0.0 (only the first slot of an expert keeps it)
-            float wsum = 0.0f;
-            for (int k = 0; k < K; ++k) {
-                const int e = __shfl_sync(kFull, my_e, k);
-                const float wk = __shfl_sync(kFull, my_w, k);
-                if (k >= lane && e == my_e && my_e >= 0) wsum = __fadd_rn(wsum, wk);
-            }
-            const long long trow = (long long)tok * p.KP;
-            if (lane < K) {
-                p.send_row[trow + lane] = (int32_t)my_row;
-                p.wsum[trow + lane] = first_of_e ? wsum : 0.0f;
-                if (raw < -1 || raw >= p.E) atomicOr(p.flags, MOE_DEVICE_FLAG_BAD_EXPERT_ID);
-                if (my_e >= 0) atomicAdd(p.counts + my_e, 1);
-                if (first_of_e) {
-                    p.src_token[my_row] = tok;  // s * T + t (uniform T)
-                    p.recv_w[my_row] = wsum;
-                    atomicAdd(p.recv_counts + my_e, 1);
-                }
-            } else if (lane < p.KP) {
-                p.send_row[trow + lane] = -1;
-                p.wsum[trow + lane] = 0.0f;
-            }
-        }
+        if (chunk == 0) write_expert_routing(p, K, tok, raw, my_e, my_w, first_of_e, my_row, lane);
 
         // ---- the row copy: the chunk to every row of the token ----
         const int stage = i & (kStages - 1);
@@ -233,7 +255,180 @@ __global__ void __launch_bounds__(32)
     }
 }
 
+constexpr int kFp8MaxThreads = 256;  // threads of the FP8 kernel: at most
+
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// FP8 receive rows, one CTA per token: thread 0 requests the bf16 row into
+// shared memory, warp 0 finds the token's rows and writes its routing
+// outputs (as the bf16 kernel's first-chunk warp), every thread takes VPT
+// vectors of the row; the row's amax is one CTA reduction (the same
+// barrier publishes the rows), and each thread stores the e4m3 codes of its
+// vectors to every row of the token (fp8.cuh's quotient).
+template <int KT, int VPT>
+__global__ void __launch_bounds__(kFp8MaxThreads)
+    dispatch_small_expert_fp8_kernel(const DispatchSmallExpertFp8Params p) {
+    extern __shared__ __align__(128) uint8_t row_smem[];  // the token's bf16 row
+    __shared__ uint64_t bar;
+    __shared__ long long rows[kMaxTopK];                   // by top-k slot (-1: none)
+    __shared__ float red[kFp8MaxThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nt = blockDim.x, nw = nt >> 5;
+    const int K = KT > 0 ? KT : p.K;
+    const int tok = blockIdx.x;  // s * T + t, below 2^13
+    const uint32_t row_bytes = (uint32_t)p.H * 2;
+
+    if (tid == 0) {  // x is an input of the call: requested right away
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+        ptx::mbar_arrive_expect_tx(&bar, row_bytes);
+        ptx::bulk_g2s(row_smem, p.x + (size_t)tok * p.H, row_bytes, &bar);
+    }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+
+    if (warp == 0) {
+        int raw, my_e;
+        float my_w;
+        bool first_of_e;
+        long long my_row;
+        token_rows<KT>(p, K, tok, lane, raw, my_e, my_w, first_of_e, my_row);
+        ptx::grid_dependency_wait();  // before the first write
+        write_expert_routing(p, K, tok, raw, my_e, my_w, first_of_e, my_row, lane);
+        if (lane < K) rows[lane] = my_row;
+    } else {
+        ptx::grid_dependency_wait();
+    }
+    if (blockIdx.x == 0)  // the next call's count buffers start at zero
+        for (int e = tid; e < p.E; e += nt) {
+            p.counts_clear[e] = 0;
+            p.recv_counts_clear[e] = 0;
+        }
+
+    const bool landed = ptx::mbar_wait_bounded(&bar, 0, kWaitLimit);
+    const uint4 *row = reinterpret_cast<const uint4 *>(row_smem);
+    uint4 cur[VPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int c = tid + j * nt;
+        cur[j] = (landed && c < p.H8) ? row[c] : make_uint4(0, 0, 0, 0);
+        const uint32_t u[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(lo_f(u[e])), fabsf(hi_f(u[e]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    if (lane == 0) red[warp] = amax;
+    if (!__syncthreads_and(landed)) {  // (also publishes rows[] and red[])
+        if (tid == 0) {
+            atomicOr(p.flags, MOE_DEVICE_FLAG_WAIT_TIMEOUT);
+            // the row copy lands before the shared memory goes away
+            ptx::mbar_wait_bounded(&bar, 0, kWaitLimit);
+        }
+        return;
+    }
+    amax = red[0];
+    for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[w]);
+    const fp8::RowScale rs = fp8::row_scale(amax);
+    float f[VPT][8];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const uint32_t u[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[j][2 * e] = lo_f(u[e]);
+            f[j][2 * e + 1] = hi_f(u[e]);
+        }
+    }
+    uint2 q[VPT];
+    fp8::quantize_row<VPT>(f, rs, q);
+    for (int k = 0; k < K; ++k) {
+        const long long dst_row = rows[k];
+        if (dst_row < 0) continue;
+        uint2 *dst = reinterpret_cast<uint2 *>(p.recv_x8 + dst_row * p.H);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = tid + j * nt;
+            if (c < p.H8) __stcs(dst + c, q[j]);
+        }
+        if (tid == 0) p.recv_scale[dst_row] = rs.s;
+    }
+}
+
+// Threads for a row of H8 16-byte vectors: 128 while the row fits in 8
+// vectors per thread, else the fewest whole warps that cover it with 8.
+int fp8_threads(int H8) {
+    if (H8 <= 8 * 128) return 128;
+    return ((H8 + 7) / 8 + 31) / 32 * 32;
+}
+
+template <int VPT>
+struct ExpertFp8 {
+    static cudaError_t attr(size_t smem) {
+        cudaError_t e = raise_smem_limit(dispatch_small_expert_fp8_kernel<8, VPT>, smem);
+        if (e != cudaSuccess) return e;
+        return raise_smem_limit(dispatch_small_expert_fp8_kernel<0, VPT>, smem);
+    }
+    static cudaError_t launch(const DispatchSmallExpertFp8Params &p,
+                              const DispatchSmallFp8Shape &sh, cudaStream_t st) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(p.R * p.T), 1, 1);
+        cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
+        cfg.dynamicSmemBytes = sh.smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (p.K == 8) return cudaLaunchKernelEx(&cfg, dispatch_small_expert_fp8_kernel<8, VPT>, p);
+        return cudaLaunchKernelEx(&cfg, dispatch_small_expert_fp8_kernel<0, VPT>, p);
+    }
+};
+
+template <typename Fn>
+cudaError_t by_vpt(int vpt, Fn fn) {
+    switch (vpt) {
+        case 1: return fn(ExpertFp8<1>());
+        case 2: return fn(ExpertFp8<2>());
+        case 3: return fn(ExpertFp8<3>());
+        case 4: return fn(ExpertFp8<4>());
+        case 5: return fn(ExpertFp8<5>());
+        case 6: return fn(ExpertFp8<6>());
+        case 7: return fn(ExpertFp8<7>());
+        case 8: return fn(ExpertFp8<8>());
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
+
+cudaError_t dispatch_small_expert_fp8_prepare(int H, DispatchSmallFp8Shape *out) {
+    if (H % 16 != 0 || H / 8 > 2048) return cudaErrorInvalidValue;
+    const int H8 = H / 8;
+    out->threads = fp8_threads(H8);
+    out->vpt = (H8 + out->threads - 1) / out->threads;
+    out->smem = (size_t)H * 2;
+    if (out->threads > kFp8MaxThreads) return cudaErrorInvalidValue;
+    const size_t smem = out->smem;
+    return by_vpt(out->vpt, [&](auto f) { return decltype(f)::attr(smem); });
+}
+
+cudaError_t launch_dispatch_small_expert_fp8(const DispatchSmallExpertFp8Params &pc,
+                                             const DispatchSmallFp8Shape &shape,
+                                             cudaStream_t st) {
+    DispatchSmallExpertFp8Params p = pc;
+    if (p.T < 1 || p.T > kRouteTile || p.R < 1 || p.R > kMaxRanks || p.K < 1 ||
+        p.K > kMaxTopK || p.KP < p.K || p.KP > 32 || p.E < p.R || p.E % p.R != 0 ||
+        p.Epr != p.E / p.R || p.cap < p.R * p.T || p.H % 16 != 0 || p.H8 != p.H / 8 ||
+        shape.smem != (size_t)p.H * 2 || shape.threads > kFp8MaxThreads ||
+        (long long)shape.threads * shape.vpt < p.H8)
+        return cudaErrorInvalidValue;
+    p.epr_magic = owner_magic(p.Epr);  // exact: e < E <= 1024 experts
+    return by_vpt(shape.vpt, [&](auto f) { return decltype(f)::launch(p, shape, st); });
+}
 
 cudaError_t dispatch_small_expert_prepare(int row_bytes, int num_sms, DispatchSmallShapes *out) {
     // For 1..8 chunks per row: chunk bytes (a multiple of 16, bulk copies),

@@ -67,6 +67,13 @@ constexpr int kSmallDispatchMaxT = 256;
 // 22.0, T = 128 25.0-26.4 vs 30.1, T = 192 35.3 vs 38.3, T = 256 47.6 vs 50.9.
 constexpr int kSmallExpertDispatchMaxT = 256;
 
+// The same for the expert layout's FP8 receive rows (one CTA per token):
+// faster than the routing passes + FP8 row copy up to 64 tokens per rank
+// (p50: T = 1 8.2 vs 13.7 us, T = 32 10.3-12.3 vs 15.8, T = 64 16.3 vs 17.9)
+// and slower beyond (T = 128 26.6 vs 24.0, T = 256 53.3 vs 32.2: one CTA per
+// token runs in waves).
+constexpr int kSmallExpertFp8MaxT = 64;
+
 // The same for FP8 receive rows (one CTA per token, dispatch_small.cu):
 // measured faster than the routing passes + FP8 row copy up to 128 tokens
 // per rank (T = 1 10.2 vs 14.9 us, T = 64 13.4 vs 16.8, T = 128 16.4 vs
@@ -276,9 +283,12 @@ int init_device(moe_a2a_t *h, cudaStream_t st) {
              : moe::dispatch_small_expert_prepare(2 * h->cfg.hidden, h->num_sms, &h->small)) !=
         cudaSuccess)
         return cuda_failed();
-    h->small_fp8_ok = h->L.layout == MOE_LAYOUT_RANK && h->cfg.hidden % 16 == 0 &&
-                      moe::dispatch_small_fp8_prepare(h->cfg.hidden, &h->small_fp8) ==
-                          cudaSuccess;
+    h->small_fp8_ok =
+        h->cfg.hidden % 16 == 0 &&
+        (h->L.layout == MOE_LAYOUT_RANK
+             ? moe::dispatch_small_fp8_prepare(h->cfg.hidden, &h->small_fp8)
+             : moe::dispatch_small_expert_fp8_prepare(h->cfg.hidden, &h->small_fp8)) ==
+            cudaSuccess;
     if (cudaMemsetAsync(h->ws + h->L.flags, 0, sizeof(uint32_t), st) != cudaSuccess)
         return cuda_failed();
     h->overlap = h->L.layout == MOE_LAYOUT_RANK && h->tuning.route_overlap != 0;
@@ -377,10 +387,15 @@ int launch_rows(moe_a2a_t *h, const void *d_x, const moe::TokenMap &map, int m,
 // and at most Tuning::dispatch_small_max (measured break-even, below).
 bool small_dispatch(const moe_a2a_t *h, const moe::TokenMap &map) {
     if (!map.uniform) return false;
-    if (h->L.layout == MOE_LAYOUT_EXPERT) {  // bf16 rows only
-        if (h->recv_format != MOE_FORMAT_BF16) return false;
-        const int lim = h->tuning.dispatch_small_max;
-        const int T_max = lim < 0 ? 0 : (lim == 0 ? kSmallExpertDispatchMaxT : lim);
+    if (h->L.layout == MOE_LAYOUT_EXPERT) {
+        int T_max = 0;
+        if (h->recv_format == MOE_FORMAT_BF16) {
+            const int lim = h->tuning.dispatch_small_max;
+            T_max = lim < 0 ? 0 : (lim == 0 ? kSmallExpertDispatchMaxT : lim);
+        } else if (h->recv_format == MOE_FORMAT_FP8_E4M3 && h->small_fp8_ok) {
+            const int lim = h->small_fp8_max;
+            T_max = lim < 0 ? 0 : (lim == 0 ? kSmallExpertFp8MaxT : lim);
+        }
         return map.stride >= 1 && map.stride <= T_max && map.stride <= moe::kRouteTile;
     }
     int T_max = 0;
@@ -454,34 +469,58 @@ int dispatch_impl(moe_a2a_t *h, const int32_t *d_topk_ids, const float *d_topk_w
             (cudaMemsetAsync(h->ws + hist[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess ||
              cudaMemsetAsync(h->ws + rows[sel], 0, sizeof(int32_t) * E, st) != cudaSuccess))
             return cuda_failed();
-        const int row_bytes = 2 * h->cfg.hidden;
-        const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
-        moe::DispatchSmallExpertParams sp;
-        sp.topk_ids = d_topk_ids;
-        sp.topk_w = d_topk_w;
-        sp.x = static_cast<const uint8_t *>(d_x);
-        sp.recv_x = at<uint8_t>(h, h->L.recv_x);
-        sp.send_row = at<int32_t>(h, h->L.send_slot);
-        sp.wsum = at<float>(h, h->L.dest_weight);
-        sp.src_token = at<int32_t>(h, h->L.src_token);
-        sp.recv_w = at<float>(h, h->L.recv_w);
-        sp.counts = at<int32_t>(h, hist[sel]);
-        sp.counts_clear = at<int32_t>(h, hist[sel ^ 1]);
-        sp.recv_counts = at<int32_t>(h, rows[sel]);
-        sp.recv_counts_clear = at<int32_t>(h, rows[sel ^ 1]);
-        sp.flags = flags;
-        sp.active = h->active;
-        sp.R = R, sp.K = K, sp.E = E, sp.Epr = E / R, sp.KP = h->L.P, sp.T = map.stride;
-        sp.cap = dest.cap;
-        sp.row_bytes = row_bytes;
-        sp.chunk_bytes = h->small.chunk_bytes[c];
-        sp.chunks = h->small.chunks[c];
-        sp.stages = h->small.stages;
-        sp.stage_bytes = h->small.stage_bytes[c];
-        sp.units = ntok * sp.chunks;
-        h->small_zero_ok = false;  // until the launch that clears the other pair is queued
-        if (moe::launch_dispatch_small_expert(sp, h->small.shape[c], st) != cudaSuccess)
-            return cuda_failed();
+        if (h->recv_format == MOE_FORMAT_FP8_E4M3) {  // e4m3 rows, one CTA per token
+            moe::DispatchSmallExpertFp8Params fp;
+            fp.topk_ids = d_topk_ids;
+            fp.topk_w = d_topk_w;
+            fp.x = static_cast<const uint16_t *>(d_x);
+            fp.recv_x8 = at<uint8_t>(h, h->L.recv_x);
+            fp.recv_scale = at<float>(h, h->L.recv_scale);
+            fp.send_row = at<int32_t>(h, h->L.send_slot);
+            fp.wsum = at<float>(h, h->L.dest_weight);
+            fp.src_token = at<int32_t>(h, h->L.src_token);
+            fp.recv_w = at<float>(h, h->L.recv_w);
+            fp.counts = at<int32_t>(h, hist[sel]);
+            fp.counts_clear = at<int32_t>(h, hist[sel ^ 1]);
+            fp.recv_counts = at<int32_t>(h, rows[sel]);
+            fp.recv_counts_clear = at<int32_t>(h, rows[sel ^ 1]);
+            fp.flags = flags;
+            fp.active = h->active;
+            fp.R = R, fp.K = K, fp.E = E, fp.Epr = E / R, fp.KP = h->L.P, fp.T = map.stride;
+            fp.cap = dest.cap, fp.H = h->cfg.hidden, fp.H8 = h->cfg.hidden / 8;
+            h->small_zero_ok = false;  // until the launch that clears the other pair is queued
+            if (moe::launch_dispatch_small_expert_fp8(fp, h->small_fp8, st) != cudaSuccess)
+                return cuda_failed();
+        } else {
+            const int row_bytes = 2 * h->cfg.hidden;
+            const int c = moe::dispatch_small_chunks(row_bytes, h->num_sms, ntok);
+            moe::DispatchSmallExpertParams sp;
+            sp.topk_ids = d_topk_ids;
+            sp.topk_w = d_topk_w;
+            sp.x = static_cast<const uint8_t *>(d_x);
+            sp.recv_x = at<uint8_t>(h, h->L.recv_x);
+            sp.send_row = at<int32_t>(h, h->L.send_slot);
+            sp.wsum = at<float>(h, h->L.dest_weight);
+            sp.src_token = at<int32_t>(h, h->L.src_token);
+            sp.recv_w = at<float>(h, h->L.recv_w);
+            sp.counts = at<int32_t>(h, hist[sel]);
+            sp.counts_clear = at<int32_t>(h, hist[sel ^ 1]);
+            sp.recv_counts = at<int32_t>(h, rows[sel]);
+            sp.recv_counts_clear = at<int32_t>(h, rows[sel ^ 1]);
+            sp.flags = flags;
+            sp.active = h->active;
+            sp.R = R, sp.K = K, sp.E = E, sp.Epr = E / R, sp.KP = h->L.P, sp.T = map.stride;
+            sp.cap = dest.cap;
+            sp.row_bytes = row_bytes;
+            sp.chunk_bytes = h->small.chunk_bytes[c];
+            sp.chunks = h->small.chunks[c];
+            sp.stages = h->small.stages;
+            sp.stage_bytes = h->small.stage_bytes[c];
+            sp.units = ntok * sp.chunks;
+            h->small_zero_ok = false;  // until the launch that clears the other pair is queued
+            if (moe::launch_dispatch_small_expert(sp, h->small.shape[c], st) != cudaSuccess)
+                return cuda_failed();
+        }
         h->cur_counts = hist[sel];
         h->cur_recv_counts = rows[sel];
         h->small_sel = sel ^ 1;

@@ -314,8 +314,8 @@ int moe_a2a_create_layout(const moe_a2a_config_t *cfg, int32_t layout, void *d_w
  * within each (destination, source) plane, copies x rows and the masked
  * top-k metadata into the planes, and counts rows per plane and per local
  * expert.  Queues one kernel on `stream` when every source holds the same
- * number of tokens, at most 256 (rank layout with bf16 rows, or the expert
- * layout with bf16 rows; 128 for the rank layout's FP8 rows), and `stream`
+ * number of tokens, at most 256 (bf16 rows, either layout; FP8 rows: 128 in
+ * the rank layout, 64 in the expert layout), and `stream`
  * is not capturing into a CUDA graph (that kernel alternates two count
  * buffers between calls, which a replay cannot follow; in the expert layout
  * the rows per expert alternate with them, so read them through the view);

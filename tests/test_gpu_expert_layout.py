@@ -285,3 +285,23 @@ def test_expert_one_launch_alternates_with_the_routing_passes():
         ss = view.send_slot.cpu().numpy()[:, :T, :K]
         assert np.array_equal(ss, r["send_row"]), (n, T)
         a.combine(None, False)
+
+
+@pytest.mark.parametrize("small_max", ["-1", "256"])
+@pytest.mark.parametrize("T", [1, 40, 128, 200])
+def test_expert_fp8_one_launch_dispatch_modes(monkeypatch, small_max, T):
+    # FP8 receive rows on the expert layout, through the routing passes + FP8
+    # row copy (-1) and the one-launch dispatch (one CTA per token): codes,
+    # scales, routing tables and combines equal the oracle on both
+    from combine_topk_ids_rank_gb300.moe_a2a import (MoeA2A, MOE_LAYOUT_EXPERT,
+                                                     MOE_FORMAT_FP8_E4M3)
+    monkeypatch.setenv("MOE_DISPATCH_SMALL_FP8_MAX", small_max)
+    run(8, T, 256, 64, 8, seed=T + 9, weighted=True, fused=True, fp8=True)
+    run(4, T, 7168, 16, 3, seed=T + 10, weighted=False, fused=False, fp8=True, routing="zipf")
+    a = MoeA2A(4, T, 128, 16, 4, "cuda", layout=MOE_LAYOUT_EXPERT)
+    a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    view = a.dispatch(parity.to_dev(synth.topk_ids(2, 4, T, 16, 4), torch.int32),
+                      parity.to_dev(synth.topk_weights(2, 4, T, 4), torch.float32),
+                      torch.zeros((4, T, 128), dtype=torch.bfloat16, device="cuda"))
+    assert view.kernels == (3 if small_max == "-1" else 1)
+    a.combine(None, False)
