@@ -64,7 +64,7 @@ struct DispatchSmallExpertParams {
     int R, K, E, Epr, KP, T, cap;
     int row_bytes, chunk_bytes, chunks, stages, stage_bytes;
     long long units;           // R * T * chunks
-    unsigned long long epr_magic, chunks_magic, T_magic;  // set by the launcher
+    unsigned long long epr_magic, chunks_magic;  // set by the launcher
 };
 cudaError_t dispatch_small_expert_prepare(int row_bytes, int num_sms, DispatchSmallShapes *out);
 cudaError_t launch_dispatch_small_expert(const DispatchSmallExpertParams &p,

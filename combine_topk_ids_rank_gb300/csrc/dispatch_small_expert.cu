@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(32)
     }
     __syncwarp();
 
-    // Units (at most 32 x 256 tokens x 8 chunks) in 32-bit arithmetic;
-    // divisions by chunks and T as multiply-highs.
+    // Units (at most 32 x 256 tokens x 8 chunks) in 32-bit arithmetic; the
+    // division by chunks as a multiply-high (tokens are flat: s * T + t).
     const int units = (int)p.units;
     const int first = blockIdx.x, step = gridDim.x;
     const int n = first < units ? (units - 1 - first) / step + 1 : 0;
@@ -477,7 +477,6 @@ cudaError_t launch_dispatch_small_expert(const DispatchSmallExpertParams &pc,
         return cudaErrorInvalidValue;
     p.epr_magic = owner_magic(p.Epr);      // exact: e < E <= 1024 experts
     p.chunks_magic = div_magic(p.chunks);  // exact: units < 2^17, chunks <= 8
-    p.T_magic = div_magic(p.T);            // exact: tokens < 2^13, T <= 256
     long long grid = shape.grid;
     if (grid > p.units) grid = p.units;
     if (grid < 1) return cudaSuccess;
