@@ -278,11 +278,17 @@ def cpu_baseline(w, seed, target_seconds):
     per_tok = oracle_seconds_per_token(w, seed)
     T_s = int(max(1, min(w.tokens_per_rank, target_seconds / per_tok / w.ep_size)))
     sample = OracleSample(w, T_s, seed)
-    sec = sample.step()
-    return {"value": sample.tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    # the whole batch when it takes less than the target: repeated passes
+    # (at most 4) until the target is reached
+    secs = [sample.step()]
+    while sum(secs) < target_seconds and T_s == w.tokens_per_rank and len(secs) < 4:
+        secs.append(sample.step())
+    sec = sum(secs)
+    return {"value": sample.tokens * len(secs) / sec, "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
             "sample": "route+dispatch+combine of the first %d tokens per rank (%d tokens, "
-                      "%s), single-threaded C oracle, %.1f s" % (
-                          T_s, sample.tokens, w.name, sec),
+                      "%s), %d pass(es), single-threaded C oracle, %.1f s" % (
+                          T_s, sample.tokens, w.name, len(secs), sec),
             "host": host_cpu()}
 
 
