@@ -539,7 +539,9 @@ def run_gpu(args, w, rank, world, local_rank):
                      "ms_p90": pct(disp_ms, 0.9), "bytes": d_bytes,
                      "gbs": d_bytes / d_avg / 1e6, "frac": d_bytes / d_avg / 1e6 / peak,
                      "frac_of_nominal": d_bytes / d_avg / 1e6 / NOMINAL_HBM_GBS,
-                     "kernels": (["dispatch_small"] if view.kernels == 1 else
+                     "kernels": ([("dispatch_small_expert" if args.layout == "expert"
+                                   else "dispatch_small") + ("_fp8" if fp8 else "")]
+                                 if view.kernels == 1 else
                                  ["route_e_count", "route_e_scan"] if args.layout == "expert"
                                  else ["route_count", "route_scan"]) +
                                 ([] if view.kernels == 1 else
