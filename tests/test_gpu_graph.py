@@ -390,3 +390,100 @@ def test_graph_replays_combine_modes(mode):
             got = parity.f32(parity.to_host_u16(out).reshape(R * T, H)[tok]).astype(np.float64)
             err = np.abs(got - y)
             assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(y))).all(), seed
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_graph_replays_expert_layout_moe_step(fp8):
+    # A whole MoE step on the expert-major layout captured once: dispatch,
+    # the expert product into the combine payload (it reads the rows per
+    # expert of the current dispatch), the weighted fused combine.  Direct
+    # calls first take the one-launch dispatch, which alternates its count
+    # buffers; the captured call takes the routing passes.  W_e = 2^(e mod 3) I
+    # (bf16, or unit codes with that channel scale) makes every expert output
+    # exact, so each replay's outputs are the oracle's.
+    from combine_topk_ids_rank_gb300.moe_a2a import (MoeA2A, MOE_LAYOUT_EXPERT,
+                                                     MOE_FORMAT_FP8_E4M3)
+    R, T, H, E, K = 4, 40, 256, 16, 4
+    a = MoeA2A(R, T, H, E, K, "cuda", layout=MOE_LAYOUT_EXPERT)
+    if fp8:
+        a.set_recv_format(MOE_FORMAT_FP8_E4M3)
+    scale = (2.0 ** (np.arange(E) % 3)).astype(np.float32)
+    if fp8:
+        eye = np.where(np.eye(H, dtype=bool), 0x38, 0).astype(np.uint8)
+        qw_d = parity.to_dev(np.ascontiguousarray(np.broadcast_to(eye, (E, H, H))), torch.uint8)
+        sw_d = parity.to_dev(np.repeat(scale[:, None], H, axis=1), torch.float32)
+        product = lambda: a.expert_gemm_fp8(qw_d, sw_d)
+    else:
+        wb = parity.f32_to_bits(np.stack([np.eye(H, dtype=np.float32) * scale[e]
+                                          for e in range(E)]))
+        wb_d = parity.to_dev(wb, torch.bfloat16)
+        product = lambda: a.expert_gemm(wb_d)
+
+    def inputs(seed):
+        return dict(ids=synth.topk_ids(seed, R, T, E, K), w=synth.topk_weights(seed, R, T, K),
+                    x=synth.per_rank_rows(seed, synth.X, R, T, H),
+                    res=synth.per_rank_rows(seed, synth.RESIDUAL, R, T, H),
+                    g=synth.gamma(seed, H))
+
+    first = inputs(600)
+    ids = parity.to_dev(first["ids"], torch.int32)
+    wts = parity.to_dev(first["w"], torch.float32)
+    x = parity.to_dev(first["x"], torch.bfloat16)
+    res = parity.to_dev(first["res"], torch.bfloat16)
+    gam = parity.to_dev(first["g"], torch.bfloat16)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(res)
+
+    def step():
+        v = a.dispatch(ids, wts, x, T)
+        product()
+        a.combine(None, True, res, gam, 1e-6, out, rout)
+        return v
+
+    for _ in range(3):                             # direct calls: the one-launch dispatch
+        view = step()
+        assert view.kernels == 1
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        view = step()
+    assert view.kernels == 3
+
+    for seed in (61, 62, 63):
+        inp = inputs(seed)
+        for dst, src, dt in ((ids, inp["ids"], torch.int32), (wts, inp["w"], torch.float32),
+                             (x, inp["x"], torch.bfloat16), (res, inp["res"], torch.bfloat16),
+                             (gam, inp["g"], torch.bfloat16)):
+            dst.copy_(parity.to_dev(src, dt))
+        g.replay()
+        torch.cuda.synchronize()
+        assert a.get_error() == (0, 0)
+        r = oracle.route_experts(inp["ids"], inp["w"], E, T)
+        cnt = view.recv_counts.cpu().numpy()
+        assert np.array_equal(cnt, r["recv_counts"]), seed
+        rx = oracle.dispatch_experts(inp["x"], E, T, r)
+        cap = R * T
+        eo = np.zeros((E, cap, H), np.uint16)
+        if fp8:
+            # the product's epilogue: bf16 of (f(qx) * sx) * sw, each product
+            # rounded to binary32 (the sum is a single exact term)
+            q, sc = oracle.quantize_rows_fp8(inp["x"])
+            fq = oracle.fp8_to_f32(q).astype(np.float32)
+            where, vals = [], []
+            for e in range(E):
+                for j in range(cnt[e]):
+                    s, t = divmod(int(r["src_row"][e, j]), T)
+                    where.append((e, j))
+                    vals.append((fq[s, t] * np.float32(sc[s, t])) * np.float32(scale[e]))
+            bits = oracle.bf16_bits(np.stack(vals)).reshape(len(vals), H)
+            for (e, j), b in zip(where, bits):
+                eo[e, j] = b
+        else:
+            for e in range(E):
+                c = cnt[e]
+                eo[e, :c] = parity.f32_to_bits(parity.f32(rx[e, :c]) * scale[e])
+        oc = oracle.combine_experts(r, eo, True, inp["res"], inp["g"], 1e-6)
+        assert np.array_equal(parity.to_host_u16(rout).reshape(R * T, H), oc["residual_out"]), seed
+        y = parity.f32(parity.to_host_u16(out).reshape(R * T, H)).astype(np.float64)
+        err = np.abs(y - oc["y"])
+        assert ((err <= parity.ABS_TOL) & (err <= parity.REL_TOL * np.abs(oc["y"]))).all(), seed
